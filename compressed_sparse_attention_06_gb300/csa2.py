@@ -1,0 +1,259 @@
+"""Python binding of the CSA2 C ABI (libcsa2.so): argument marshalling only.
+
+Each function has the name of its C entry point, takes torch CUDA tensors,
+passes their data pointers and the current CUDA stream to the library, and
+raises Csa2Error on a non-OK status.  Every step of the path runs in the
+library's CUDA kernels; if the library is missing this module refuses to load.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcsa2.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
+F32, BF16, FP4_E4M3x16, MXFP4_E8M0x32 = range(4)
+QNORM, KVNORM, ROPE = 1, 2, 4
+ATTN_DEFAULT = QNORM | KVNORM | ROPE
+W_NORM, W_ROPE = 1, 2
+
+# symbols declared in include/csa2.h
+EXPORTS = (
+    "csa2_status_string", "csa2_version", "csa2_ctx_create", "csa2_ctx_destroy", "csa2_ctx_check",
+    "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
+    "csa2_block_pool", "csa2_sparse_attn",
+)
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {_lib().csa2_status_string(status).decode()} (status {status})")
+
+
+_LIB = None
+_CTX = {}
+
+_vp, _i, _i64, _u, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint, ctypes.c_float
+
+
+def _declare(lib):
+    sig = {
+        "csa2_status_string": (ctypes.c_char_p, [_i]),
+        "csa2_version": (_i, []),
+        "csa2_ctx_create": (_i, [_i, ctypes.POINTER(_vp)]),
+        "csa2_ctx_destroy": (_i, [_vp]),
+        "csa2_ctx_check": (_i, [_vp, _vp]),
+        "csa2_compress": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _f, _u,
+                               _vp, _i, _vp]),
+        "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _vp]),
+        "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
+        "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
+                                  _vp, _vp]),
+        "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
+        "csa2_block_pool": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp]),
+        "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
+                                  _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() (the CSA2 path has no "
+                              f"other implementation)")
+        lib = ctypes.CDLL(LIB_PATH)
+        _declare(lib)
+        _LIB = lib
+    return _LIB
+
+
+def load():
+    """Load the library (raises if it is missing) and return the ctypes handle."""
+    return _lib()
+
+
+def ctx(device: Optional[int] = None):
+    """The library context of a CUDA device (created on first use)."""
+    if device is None:
+        device = torch.cuda.current_device()
+    if device not in _CTX:
+        h = _vp()
+        st = _lib().csa2_ctx_create(device, ctypes.byref(h))
+        if st != OK:
+            raise Csa2Error("csa2_ctx_create", st)
+        _CTX[device] = h
+    return _CTX[device]
+
+
+def _stream(t: Optional[torch.Tensor] = None):
+    dev = t.device if t is not None else torch.device("cuda", torch.cuda.current_device())
+    return _vp(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("CSA2 tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("CSA2 tensors must be contiguous")
+    return _vp(t.data_ptr())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _check(fn: str, st: int):
+    if st != OK:
+        raise Csa2Error(fn, st)
+
+
+def fp4_row_bytes(c: int) -> int:
+    return c // 2 + c // 16
+
+
+def mxfp4_row_bytes(d: int) -> int:
+    return d // 2 + d // 32
+
+
+def csa2_ctx_check(device: Optional[int] = None):
+    """Synchronise the current stream and raise if a kernel recorded an error."""
+    dev = torch.cuda.current_device() if device is None else device
+    _check("csa2_ctx_check", _lib().csa2_ctx_check(ctx(dev), _vp(torch.cuda.current_stream(dev).cuda_stream)))
+
+
+def csa2_fp4_pack(x: torch.Tensor, fmt: int = FP4_E4M3x16, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Pack rows [..., c] into FP4 (E2M1 + E4M3/16) or MXFP4 (E2M1 + E8M0/32) rows."""
+    c = x.shape[-1]
+    rows = x.numel() // c if c else 0
+    rb = fp4_row_bytes(c) if fmt == FP4_E4M3x16 else mxfp4_row_bytes(c)
+    if out is None:
+        out = torch.empty((*x.shape[:-1], rb), dtype=torch.uint8, device=x.device)
+    _check("csa2_fp4_pack", _lib().csa2_fp4_pack(ctx(x.device.index), _p(x), _dt(x), rows, c, fmt, _p(out),
+                                                 _stream(x)))
+    return out
+
+
+def csa2_fp4_unpack(b: torch.Tensor, fmt: int, c: int, out_dtype=torch.float32,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    rows = b.numel() // b.shape[-1] if b.shape[-1] else 0
+    if out is None:
+        out = torch.empty((*b.shape[:-1], c), dtype=out_dtype, device=b.device)
+    _check("csa2_fp4_unpack", _lib().csa2_fp4_unpack(ctx(b.device.index), _p(b), fmt, rows, c, _p(out), _dt(out),
+                                                     _stream(b)))
+    return out
+
+
+def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=None, prev_zb=None,
+                  pos0: int = 0, rope_base: float = 10000.0, flags: int = 0, out_fmt: str = "f32",
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Compressed entries [n/m, c]; out_fmt 'f32', 'bf16' or 'fp4' (packed rows)."""
+    n, c = ca.shape
+    if out is None:
+        if out_fmt == "fp4":
+            out = torch.empty((n // m, fp4_row_bytes(c)), dtype=torch.uint8, device=ca.device)
+        else:
+            out = torch.empty((n // m, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16,
+                              device=ca.device)
+    out_dt = FP4_E4M3x16 if out.dtype == torch.uint8 else _dt(out)
+    st = _lib().csa2_compress(ctx(ca.device.index), _p(ca), _p(za), _p(cb), _p(zb), _dt(ca), _p(ba), _p(bb),
+                              _p(prev_cb), _p(prev_zb), n, c, m, pos0, rope_base, flags, _p(out), out_dt,
+                              _stream(ca))
+    _check("csa2_compress", st)
+    return out
+
+
+def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=None, block: int = 8,
+                     scores: Optional[torch.Tensor] = None, block_max: Optional[torch.Tensor] = None,
+                     want_scores: bool = True, want_block_max: bool = False):
+    """qI [B,Q,H_I,d], w [B,Q,H_I], kI [B,N,d] (f32/bf16) or [B,N,row_bytes] uint8 (MXFP4),
+    n_visible [B,Q] int64.  Returns (scores, block_max); either may be None."""
+    B, Q, H_I, d = qI.shape
+    N = kI.shape[1]
+    if kI.dtype == torch.uint8:
+        k_dt = MXFP4_E8M0x32 if k_fmt is None else k_fmt
+    else:
+        k_dt = _dt(kI)
+    n_pool = 0
+    if pool is not None:
+        n_pool = pool.shape[-1]
+        if scores is None:
+            scores = torch.empty((B, Q, n_pool * block), dtype=torch.float32, device=qI.device)
+    else:
+        if want_scores and scores is None:
+            scores = torch.empty((B, Q, N), dtype=torch.float32, device=qI.device)
+        if want_block_max and block_max is None:
+            block_max = torch.empty((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
+    st = _lib().csa2_index_score(ctx(qI.device.index), _p(qI), _dt(qI), _p(w), _p(kI), k_dt, B, Q, N, H_I, d,
+                                 _p(n_visible), _p(pool), n_pool, block, _p(scores), _p(block_max), _stream(qI))
+    _check("csa2_index_score", st)
+    return scores, block_max
+
+
+def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores: bool = False,
+              out_idx: Optional[torch.Tensor] = None, out_score: Optional[torch.Tensor] = None):
+    """scores [..., n] -> (idx [..., k] int32 ascending, -1 padded; matching scores or None)."""
+    n = scores.shape[-1]
+    rows = scores.numel() // n if n else 0
+    lead = scores.shape[:-1]
+    if out_idx is None:
+        out_idx = torch.empty((*lead, k), dtype=torch.int32, device=scores.device)
+    if want_scores and out_score is None:
+        out_score = torch.empty((*lead, k), dtype=torch.float32, device=scores.device)
+    n_pool = pool.shape[-1] if pool is not None else 0
+    st = _lib().csa2_topk(ctx(scores.device.index), _p(scores), rows, n, n, _p(n_visible), _p(pool), n_pool, block,
+                          k, _p(out_idx), _p(out_score), _stream(scores))
+    _check("csa2_topk", st)
+    return out_idx, out_score
+
+
+def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    ld = block_max.shape[-1]
+    rows = block_max.numel() // ld if ld else 0
+    if out is None:
+        out = torch.empty((*block_max.shape[:-1], n_keep), dtype=torch.int32, device=block_max.device)
+    st = _lib().csa2_block_pool(ctx(block_max.device.index), _p(block_max), rows, ld, _p(n_visible), block, n_keep,
+                                _p(out), _stream(block_max))
+    _check("csa2_block_pool", st)
+    return out
+
+
+def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_pos0: int = 0,
+                     kv_fmt: Optional[int] = None, rope_base: float = 10000.0, flags: int = ATTN_DEFAULT,
+                     out_dtype=None, want_lse: bool = False, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None):
+    """q [B,Q,H,c]; kv [B,N,c] (f32/bf16) or [B,N,row_bytes] uint8 (FP4); idx [B,Q,k] int32;
+    swa [B,cap,c]; q_pos [B,Q] int64.  Returns (out [B,Q,H,c], lse [B,Q,H] or None)."""
+    B, Q, H, c = q.shape
+    k = idx.shape[-1] if idx is not None else 0
+    N = kv.shape[1] if kv is not None else 0
+    kv_dt = (FP4_E4M3x16 if kv_fmt is None else kv_fmt) if kv is not None and kv.dtype == torch.uint8 else \
+        (_dt(kv) if kv is not None else F32)
+    swa_cap = swa.shape[1] if swa is not None else 0
+    swa_dt = _dt(swa) if swa is not None else F32
+    if out is None:
+        out = torch.empty((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
+    st = _lib().csa2_sparse_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(idx), k, _p(swa), swa_dt,
+                                 swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
+                                 _p(out), _dt(out), _p(lse), _stream(q))
+    _check("csa2_sparse_attn", st)
+    return out, lse

@@ -1,0 +1,221 @@
+// Gated token compressor with its write epilogue.
+//
+// Non-overlapping form: Attention-evolution page §4.1 and DSA-to-CSA/HCA page
+// eqs. (22)-(23).  Overlapping form: DSA-to-CSA/HCA page eqs. (11)-(12), block 0
+// without history (Z^b = -inf, C^b = 0) unless the previous block's state is
+// carried (Attention-evolution page §3.3).  Epilogue: RMSNorm (kv_norm) -> RoPE on
+// the last 64 channels at position pos0 + m*i -> f32 / bf16 / FP4 store.
+//
+// One CTA per compressed entry, c/4 threads, each owning 4 adjacent channels, so
+// loads are coalesced float4 / 8-byte vectors and a 16-channel FP4 group is 4
+// adjacent lanes.
+#include "csa2_internal.cuh"
+
+namespace {
+
+template <typename T> __device__ __forceinline__ float4 load4(const T* p);
+template <> __device__ __forceinline__ float4 load4<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xFFFF0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xFFFF0000u);
+    return r;
+}
+
+__device__ __forceinline__ float4 load4_bias(const float* b, int64_t off) {
+    return b ? *reinterpret_cast<const float4*>(b + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ float f4get(const float4& v, int k) {
+    return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_FP4 = 2 };
+
+template <typename T, int OUT>
+__global__ void __launch_bounds__(256) compress_kernel(
+    const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
+    const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
+    const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int c, int m, int64_t pos0,
+    float rope_base, unsigned flags, void* __restrict__ out) {
+    const int64_t i = blockIdx.x;
+    const int t = threadIdx.x;
+    const int ch = 4 * t;
+    const bool overlap = cb != nullptr;
+    // history rows: block i-1 of (cb, zb), or the carried state for block 0
+    const T* hc = nullptr;
+    const T* hz = nullptr;
+    if (overlap) {
+        if (i > 0) {
+            hc = cb + (m * (i - 1)) * (int64_t)c;
+            hz = zb + (m * (i - 1)) * (int64_t)c;
+        } else if (prev_cb) {
+            hc = prev_cb;
+            hz = prev_zb;
+        }
+    }
+    const T* cur_c = ca + (m * i) * (int64_t)c;
+    const T* cur_z = za + (m * i) * (int64_t)c;
+
+    // pass 1: per-channel max of the logits
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int j = 0; j < m; ++j) {
+        float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
+        float4 b = load4_bias(ba, (int64_t)j * c + ch);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], f4get(z, k) + f4get(b, k));
+    }
+    if (hz) {
+        for (int j = 0; j < m; ++j) {
+            float4 z = load4<T>(hz + (int64_t)j * c + ch);
+            float4 b = load4_bias(bb, (int64_t)j * c + ch);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], f4get(z, k) + f4get(b, k));
+        }
+    }
+    // pass 2: softmax-weighted sum
+    float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < m; ++j) {
+        float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
+        float4 b = load4_bias(ba, (int64_t)j * c + ch);
+        float4 v = load4<T>(cur_c + (int64_t)j * c + ch);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float e = expf(f4get(z, k) + f4get(b, k) - mx[k]);
+            den[k] += e;
+            num[k] = fmaf(e, f4get(v, k), num[k]);
+        }
+    }
+    if (hz) {
+        for (int j = 0; j < m; ++j) {
+            float4 z = load4<T>(hz + (int64_t)j * c + ch);
+            float4 b = load4_bias(bb, (int64_t)j * c + ch);
+            float4 v = load4<T>(hc + (int64_t)j * c + ch);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float e = expf(f4get(z, k) + f4get(b, k) - mx[k]);
+                den[k] += e;
+                num[k] = fmaf(e, f4get(v, k), num[k]);
+            }
+        }
+    }
+    float y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = num[k] / den[k];
+
+    // RMSNorm over the c channels of the entry
+    if (flags & CSA2_W_NORM) {
+        __shared__ float red[32];
+        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+        ss = warp_sum(ss);
+        if ((t & 31) == 0) red[t >> 5] = ss;
+        __syncthreads();
+        if (t < 32) {
+            float v = (t < (int)(blockDim.x >> 5)) ? red[t] : 0.f;
+            v = warp_sum(v);
+            if (t == 0) red[0] = v;
+        }
+        __syncthreads();
+        float r = 1.0f / sqrtf(red[0] / (float)c + 1e-6f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[k] *= r;
+    }
+    // RoPE on the last 64 channels (interleaved pairs) at the entry's position
+    if ((flags & CSA2_W_ROPE) && ch >= c - 64) {
+        const int64_t pos = pos0 + (int64_t)m * i;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            int j = (ch + 2 * p - (c - 64)) >> 1;
+            float cs, sn;
+            rope_cos_sin(pos, j, rope_base, cs, sn);
+            float x0 = y[2 * p], x1 = y[2 * p + 1];
+            y[2 * p] = x0 * cs - x1 * sn;
+            y[2 * p + 1] = x0 * sn + x1 * cs;
+        }
+    }
+    // store
+    if (OUT == OUT_F32) {
+        float* o = reinterpret_cast<float*>(out) + i * (int64_t)c + ch;
+        *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
+    } else if (OUT == OUT_BF16) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + i * (int64_t)c + ch;
+        uint2 u;
+        u.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[0])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[1])) << 16);
+        u.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[2])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[3])) << 16);
+        *reinterpret_cast<uint2*>(o) = u;
+    } else {
+        // FP4: the 16-channel group is lanes 4g..4g+3 of this warp
+        float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        uint32_t sb = e4m3_byte(__fdiv_rn(amax, 6.0f));
+        float s = e4m3_to_f32(sb);
+        uint32_t codes = 0;
+        if (s != 0.0f)
+            codes = e2m1x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s)) |
+                    (e2m1x2(__fdiv_rn(y[2], s), __fdiv_rn(y[3], s)) << 8);
+        uint8_t* row = reinterpret_cast<uint8_t*>(out) + i * fp4_row_bytes(c);
+        *reinterpret_cast<uint16_t*>(row + ch / 2) = (uint16_t)codes;
+        if ((t & 3) == 0) row[c / 2 + ch / 16] = (uint8_t)sb;
+    }
+}
+
+template <typename T>
+csa2_status launch_compress(const void* ca, const void* za, const void* cb, const void* zb,
+                            const float* ba, const float* bb, const void* pcb, const void* pzb,
+                            int64_t n_entries, int c, int m, int64_t pos0, float base,
+                            unsigned flags, void* out, csa2_dtype out_dt, cudaStream_t s) {
+    dim3 grid((unsigned)n_entries), block(c / 4);
+    const T* a = (const T*)ca;
+    const T* z = (const T*)za;
+    const T* b = (const T*)cb;
+    const T* zz = (const T*)zb;
+    const T* p1 = (const T*)pcb;
+    const T* p2 = (const T*)pzb;
+    if (out_dt == CSA2_F32)
+        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+    else if (out_dt == CSA2_BF16)
+        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+    else
+        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+    return csa2_launch_status();
+}
+
+}  // namespace
+
+extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* za, const void* cb,
+                                     const void* zb, csa2_dtype in_dt, const float* ba, const float* bb,
+                                     const void* prev_cb, const void* prev_zb, int64_t n_tokens, int c,
+                                     int m, int64_t pos0, float rope_base, unsigned flags, void* out,
+                                     csa2_dtype out_dt, void* stream) {
+    if (!ctx || n_tokens < 0 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
+    if (n_tokens % m) return CSA2_ERR_INVALID_ARG;
+    if (c % 128 || c > 1024) return CSA2_ERR_INVALID_ARG;
+    if ((cb == nullptr) != (zb == nullptr)) return CSA2_ERR_INVALID_ARG;
+    if ((prev_cb == nullptr) != (prev_zb == nullptr)) return CSA2_ERR_INVALID_ARG;
+    if (prev_cb && !cb) return CSA2_ERR_INVALID_ARG;
+    if (flags & ~(CSA2_W_NORM | CSA2_W_ROPE)) return CSA2_ERR_INVALID_ARG;
+    if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16) return CSA2_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return CSA2_OK;
+    if (!ca || !za || !out) return CSA2_ERR_INVALID_ARG;
+    const size_t va = in_dt == CSA2_F32 ? 16 : 8;
+    if (!aligned(ca, va) || !aligned(za, va) || (cb && (!aligned(cb, va) || !aligned(zb, va))) ||
+        (prev_cb && (!aligned(prev_cb, va) || !aligned(prev_zb, va))) || (ba && !aligned(ba, 16)) ||
+        (bb && !aligned(bb, 16)) || !aligned(out, 16))
+        return CSA2_ERR_INVALID_ARG;
+    if (n_tokens / m > 0x7FFFFFFF) return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (in_dt == CSA2_F32)
+        return launch_compress<float>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, n_tokens / m, c, m, pos0,
+                                      rope_base, flags, out, out_dt, s);
+    return launch_compress<__nv_bfloat16>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, n_tokens / m, c, m, pos0,
+                                          rope_base, flags, out, out_dt, s);
+}

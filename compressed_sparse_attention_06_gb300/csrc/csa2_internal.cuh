@@ -1,0 +1,131 @@
+// Internal helpers shared by the CSA2 kernel files (device and host side).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+struct csa2_ctx {
+    int device;
+    int num_sms;
+    unsigned int* status;   // device word: bit 0 = out-of-range index, bit 1 = timeout
+};
+
+#define CSA2_DEVBIT_RANGE 1u
+#define CSA2_DEVBIT_TIMEOUT 2u
+
+#define CSA2_CHECK_CUDA(call)                                   \
+    do {                                                        \
+        cudaError_t e_ = (call);                                \
+        if (e_ != cudaSuccess) return CSA2_ERR_CUDA;            \
+    } while (0)
+
+static inline csa2_status csa2_launch_status() {
+    return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
+
+static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+static inline bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void csa2_flag(unsigned int* st, unsigned bit) {
+    if (st) atomicOr(st, bit);
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key); -0.0 is
+// folded onto +0.0 so the two compare equal.
+__device__ __forceinline__ uint32_t order_key(float x) {
+    uint32_t b = __float_as_uint(x);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+    uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(b);
+}
+
+// cos/sin of pos * theta_j with theta_j = base^(-2j/64): angle in double, reduced
+// modulo 2 pi, then rounded to float.
+__device__ __forceinline__ void rope_cos_sin(int64_t pos, int j, float base, float& c, float& s) {
+    double theta = pow((double)base, -2.0 * (double)j / 64.0);
+    double ang = fmod((double)pos * theta, 6.283185307179586);
+    double sd, cd;
+    sincos(ang, &sd, &cd);
+    c = (float)cd;
+    s = (float)sd;
+}
+
+// E2M1 pair from two floats: RNE, saturating to +-6, sign kept; `lo` goes to the
+// low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// E4M3 (satfinite, RNE) of one float, as a byte.
+__device__ __forceinline__ uint32_t e4m3_byte(float x) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+    return (uint32_t)(r & 0xFF);
+}
+
+// E4M3 byte -> float (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    uint32_t h2;
+    unsigned short in = (unsigned short)(b & 0xFF);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// E8M0 byte -> float 2^(b-127) (exact, 2^-127 is a float subnormal).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float((b & 0xFF) << 23);
+}
+
+// Magnitudes of the 8 E2M1 codes (format definition: 2 exponent bits with bias
+// 1, one mantissa bit).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
+    uint32_t e = (nib >> 1) & 3u, mbit = nib & 1u;
+    float mag = (e == 0) ? 0.5f * (float)mbit : ldexpf(1.0f + 0.5f * (float)mbit, (int)e - 1);
+    return (nib & 8u) ? -mag : mag;
+}
+
+// Row bytes of the packed formats.
+__host__ __device__ constexpr inline int64_t fp4_row_bytes(int c) { return c / 2 + c / 16; }
+__host__ __device__ constexpr inline int64_t mxfp4_row_bytes(int d) { return d / 2 + d / 32; }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}

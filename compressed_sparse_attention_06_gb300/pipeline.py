@@ -1,0 +1,90 @@
+"""Per-layer steps of the CSA2 hot path, strung from the C-ABI entry points.
+
+Every arithmetic step runs in libcsa2.so; this module only allocates outputs
+(torch device memory) and orders the calls on the current stream.
+
+Layer modes (CSA2 page, «三种模式：谁算、谁复用»):
+  Full    -- own indexer over all visible entries (+ block pool in the decoder),
+  Reindex -- own indexer over the pooled candidates only,
+  Reuse   -- upstream indices, attention only.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import csa2 as C
+
+TOPK = 512
+POOL_BLOCK = 8
+POOL_KEEP = 2048
+
+
+def visible_entries(q_pos: torch.Tensor, m: int) -> torch.Tensor:
+    """Entries visible to each query: entry j needs t >= m(j+1), so floor(t/m)
+    (DSA-to-CSA/HCA page, «因果边界与短滑窗»)."""
+    return torch.div(q_pos, m, rounding_mode="floor")
+
+
+@dataclass
+class DecodeBuffers:
+    """Preallocated outputs of a Full-mode decode step (reused across steps)."""
+    block_max: torch.Tensor
+    pool: torch.Tensor
+    cand_scores: torch.Tensor
+    idx: torch.Tensor
+    out: torch.Tensor
+
+
+def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch.bfloat16,
+                 k: int = TOPK, block: int = POOL_BLOCK, n_keep: int = POOL_KEEP) -> DecodeBuffers:
+    nb = (N + block - 1) // block
+    return DecodeBuffers(
+        block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
+        pool=torch.empty((B, Q, n_keep), dtype=torch.int32, device=device),
+        cand_scores=torch.empty((B, Q, n_keep * block), dtype=torch.float32, device=device),
+        idx=torch.empty((B, Q, k), dtype=torch.int32, device=device),
+        out=torch.empty((B, Q, H, c), dtype=out_dtype, device=device),
+    )
+
+
+def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeBuffers, *,
+                     window: int = 128, swa_pos0: int = 0, k: int = TOPK, block: int = POOL_BLOCK,
+                     n_keep: int = POOL_KEEP, flags: int = C.ATTN_DEFAULT):
+    """Full layer with the hierarchical pool (CSA2 page, «解码器里的分层索引»):
+    scan all visible entries keeping only block maxima, pick the pool, rescore its
+    candidates, take the top-k (the top-k of all entries lies inside the pool), and
+    attend over the selected entries plus the window."""
+    C.csa2_index_score(qI, w, kI, n_visible, block=block, want_scores=False, want_block_max=True,
+                       block_max=buf.block_max)
+    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool)
+    C.csa2_index_score(qI, w, kI, n_visible, pool=buf.pool, block=block, scores=buf.cand_scores)
+    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.pool, block=block, out_idx=buf.idx)
+    C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
+                       out=buf.out)
+    return buf
+
+
+def reindex_step(qI, w, kI, pool, n_visible, cand_scores=None, idx=None, k: int = TOPK, block: int = POOL_BLOCK):
+    """Reindex layer: own indexer query over the pooled candidates, then top-k."""
+    sc, _ = C.csa2_index_score(qI, w, kI, n_visible, pool=pool, block=block, scores=cand_scores)
+    ids, _ = C.csa2_topk(sc, n_visible, k, pool=pool, block=block, out_idx=idx)
+    return ids
+
+
+def reuse_attention(q, kv, idx, swa, q_pos, sink, out=None, window: int = 128, swa_pos0: int = 0,
+                    flags: int = C.ATTN_DEFAULT):
+    """Reuse layer (and the attention of Full/Reindex layers): upstream indices, own
+    query and own window."""
+    o, _ = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
+                              out=out)
+    return o
+
+
+def full_topk_step(qI, w, kI, n_visible, k: int = TOPK, scores=None, idx=None):
+    """Full layer without a pool (encoder / prefill): full scores, then top-k."""
+    sc, _ = C.csa2_index_score(qI, w, kI, n_visible, scores=scores)
+    ids, _ = C.csa2_topk(sc, n_visible, k, out_idx=idx)
+    return sc, ids

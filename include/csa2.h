@@ -1,0 +1,221 @@
+/*
+ * csa2.h -- C ABI of the CSA2 compressed-sparse-attention hot path (sm_103a).
+ *
+ * The path (all on one GPU, all in this library's CUDA kernels):
+ *   compressor -> [FP4 pack] -> Lightning-indexer scores (+ block max)
+ *   -> block pool / top-512 (Full, Reindex) or upstream indices (Reuse)
+ *   -> shared-KV MQA over the selected entries plus the sliding window.
+ *
+ * Sources, cited by short title:
+ *   "CSA2 page"                 «CSA2：跨层共享的压缩稀疏注意力» (daiw.org)
+ *   "Attention-evolution page"  «DeepSeek 的 Attention 演进 -【DSA、CSA、CSA2】»
+ *   "DSA-to-CSA/HCA page"       «从 DSA 到 CSA/HCA：先压缩时间轴，再决定怎样寻址»
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates tensors.  All tensors are dense row-major with the shapes given.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Arguments are validated on the host before any launch;
+ *     on a validation failure nothing is launched.
+ *   - Kernels never trap.  A kernel that meets an out-of-range index skips the
+ *     access and records CSA2_ERR_DEVICE in the context's status word; a bounded
+ *     wait that expires records CSA2_ERR_TIMEOUT.  csa2_ctx_check() reads (and
+ *     clears) that word.
+ *   - No call throws, exits or prints.
+ *   - A context is used by one host thread at a time.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CSA2_OK = 0,
+    CSA2_ERR_INVALID_ARG = 1,   /* bad pointer / size / alignment; nothing launched   */
+    CSA2_ERR_UNSUPPORTED = 2,   /* valid, but a dtype/shape combination not provided  */
+    CSA2_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
+    CSA2_ERR_TIMEOUT = 4,       /* a device-side bounded wait expired (from the ctx)  */
+    CSA2_ERR_DEVICE = 5         /* a kernel saw an out-of-range index (from the ctx)  */
+} csa2_status;
+
+typedef enum {
+    CSA2_F32 = 0,
+    CSA2_BF16 = 1,
+    /* FP4 main-KV row, 512 channels -> 288 B: 256 B of E2M1 codes (channel 2i in the
+       low nibble of byte i) then 32 E4M3 scales, one per 16 channels (CSA2 page,
+       «890 字节是怎么来的»).  Rows of other widths c (c % 16 == 0): c/2 + c/16 B. */
+    CSA2_FP4_E4M3x16 = 2,
+    /* MXFP4 indexer-K row, 128 dims -> 68 B: 64 B of E2M1 codes then 4 E8M0 scales,
+       one per 32 values (same section).  Width d (d % 32 == 0): d/2 + d/32 B.        */
+    CSA2_MXFP4_E8M0x32 = 3
+} csa2_dtype;
+
+/* attention flags */
+#define CSA2_QNORM  1u   /* RMSNorm each query head before attention              */
+#define CSA2_KVNORM 2u   /* RMSNorm each key/value row (compressed and window)    */
+#define CSA2_ROPE   4u   /* RoPE_t on the query's last 64 dims, RoPE_-t on output */
+#define CSA2_ATTN_DEFAULT (CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE)
+
+/* compressor write-epilogue flags */
+#define CSA2_W_NORM 1u   /* RMSNorm of each compressed entry (kv_norm)            */
+#define CSA2_W_ROPE 2u   /* RoPE of the entry's last 64 dims at position pos0+m*i */
+
+typedef struct csa2_ctx csa2_ctx;
+
+const char* csa2_status_string(csa2_status s);
+int csa2_version(void);
+
+/* Create a context on `device`: it holds a 4-byte device status word (the only
+   allocation this library makes) and the device's SM count. */
+csa2_status csa2_ctx_create(int device, csa2_ctx** out);
+csa2_status csa2_ctx_destroy(csa2_ctx* ctx);
+/* Synchronise `stream`, then return (and clear) the status kernels recorded:
+   CSA2_OK, CSA2_ERR_DEVICE or CSA2_ERR_TIMEOUT; CSA2_ERR_CUDA if the stream
+   itself reports an error. */
+csa2_status csa2_ctx_check(csa2_ctx* ctx, void* stream);
+
+/*
+ * csa2_compress -- gated token compressor with its write epilogue.
+ *
+ * Non-overlapping form (cb == NULL): Attention-evolution page §4.1 and
+ * DSA-to-CSA/HCA page eqs. (22)-(23):
+ *     E[i, ch] = sum_{j<m} softmax_j(za[m i + j, ch] + ba[j, ch]) * ca[m i + j, ch]
+ * Overlapping form (cb != NULL): DSA-to-CSA/HCA page eqs. (11)-(12): a per-channel
+ * softmax over the 2m rows [za[block i] + ba ; zb[block i-1] + bb] weighting
+ * [ca[block i] ; cb[block i-1]].  Block 0 has no history (zb = -inf, cb = 0)
+ * unless prev_cb/prev_zb carry the previous block's rows (the compressor state
+ * of the Attention-evolution page §3.3).
+ * Epilogue (Attention-evolution page §4.1): [RMSNorm] -> [RoPE at pos0 + m i]
+ * -> store as out_dt (CSA2_FP4_E4M3x16 packs the row).
+ *
+ *   ca, za, cb, zb : [n_tokens, c] in in_dt (F32 or BF16)
+ *   ba, bb         : [m, c] f32, NULL = 0
+ *   prev_cb/prev_zb: [m, c] in in_dt, or both NULL
+ *   out            : [n_tokens/m, c] in out_dt (F32, BF16) or [n_tokens/m, c/2+c/16] B
+ * n_tokens % m == 0, c % 16 == 0, 64 <= c <= 1024 when CSA2_W_ROPE (RoPE on the
+ * last 64 channels), m >= 1.
+ */
+csa2_status csa2_compress(csa2_ctx* ctx,
+                          const void* ca, const void* za, const void* cb, const void* zb,
+                          csa2_dtype in_dt, const float* ba, const float* bb,
+                          const void* prev_cb, const void* prev_zb,
+                          int64_t n_tokens, int c, int m, int64_t pos0, float rope_base,
+                          unsigned flags, void* out, csa2_dtype out_dt, void* stream);
+
+/*
+ * csa2_fp4_pack / csa2_fp4_unpack -- the two 4-bit cache formats.
+ *   CSA2_FP4_E4M3x16  (c % 64 == 0): per 16 channels s = E4M3_RNE(amax/6) (satfinite, f32 IEEE
+ *                       division); s == 0 -> codes 0; code = E2M1_RNE(x/s), sat. +-6.
+ *   CSA2_MXFP4_E8M0x32 (c % 128 == 0): per 32 values X = 2^(floor(log2 amax) - 2) as E8M0,
+ *                       amax == 0 -> scale byte 0, codes 0; code = E2M1_RNE(x/X).
+ * x: [rows, c] in x_dt (F32 or BF16); out: [rows, row_bytes]; unpack writes F32 or
+ * BF16 (exact: every FP4 value times its scale fits in bf16).
+ */
+csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_dt, int64_t rows, int c,
+                          csa2_dtype fmt, uint8_t* out, void* stream);
+csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, int64_t rows,
+                            int c, void* out, csa2_dtype out_dt, void* stream);
+
+/*
+ * csa2_index_score -- Lightning-indexer scores (DSA-to-CSA/HCA page eq. (16)):
+ *     I[b,q,s] = sum_h w[b,q,h] * ReLU(q_idx[b,q,h,:] . k_idx[b,s,:])
+ * with no scale and no softmax, for the entries visible to the query
+ * (s < n_visible[b,q]; the causal rule t >= m(j+1) gives n_visible = floor(t/m)).
+ *
+ *   q_idx  : [B, Q, H_I, d_I] in q_dt (F32 or BF16)
+ *   w      : [B, Q, H_I] f32
+ *   k_idx  : [B, N, d_I] in k_dt (F32, BF16) or [B, N, d_I/2 + d_I/32] B (MXFP4)
+ *   n_visible : [B, Q] int64, device
+ * Full scan (pool_blocks == NULL):
+ *   scores    : [B, Q, N] f32 or NULL; entries s >= n_visible get -inf
+ *   block_max : [B, Q, ceil(N/block)] f32 or NULL: max over the visible members of
+ *               each block of `block` entries (CSA2 page, «解码器里的分层索引»);
+ *               blocks with no visible member get -inf
+ * Candidate mode (Reindex, CSA2 page «三种模式» and «解码器里的分层索引»):
+ *   pool_blocks : [B, Q, n_pool] int32 block ids (-1 = empty slot)
+ *   scores      : [B, Q, n_pool*block] f32 (required); candidate c is entry
+ *                 pool[c/block]*block + c%block; invalid candidates get -inf
+ *   block_max must be NULL.
+ * d_I == 128, 1 <= H_I <= 128, block a power of two <= 32, B*Q <= 65535.
+ */
+csa2_status csa2_index_score(csa2_ctx* ctx,
+                             const void* q_idx, csa2_dtype q_dt, const float* w,
+                             const void* k_idx, csa2_dtype k_dt,
+                             int B, int Q, int64_t N, int H_I, int d_I,
+                             const int64_t* n_visible,
+                             const int32_t* pool_blocks, int n_pool, int block,
+                             float* scores, float* block_max, void* stream);
+
+/*
+ * csa2_topk -- top-k selection (DSA-to-CSA/HCA page eq. (17)) in one total order:
+ * score descending, entry index ascending (the lower index wins a tie).
+ * Row r of `scores` (stride ld floats) covers:
+ *   full mode (pool_blocks == NULL): entries 0 .. n_visible[r]-1;
+ *   candidate mode: candidate c -> entry pool_blocks[r, c/block]*block + c%block,
+ *                   valid if that block id >= 0 and the entry < n_visible[r].
+ * If a row has <= k valid elements, all are returned.  -0.0 equals +0.0.
+ *   out_idx   : [rows, k] int32 entry ids, ascending, padded with -1
+ *   out_score : [rows, k] f32 matching scores (-inf in padding), or NULL
+ * Scores must be finite (NaN order is unspecified).  1 <= k <= 4096.
+ */
+csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t rows, int64_t n, int64_t ld,
+                      const int64_t* n_visible, const int32_t* pool_blocks, int n_pool,
+                      int block, int k, int32_t* out_idx, float* out_score, void* stream);
+
+/*
+ * csa2_block_pool -- candidate pool of the hierarchical sparse indexer (CSA2 page,
+ * «解码器里的分层索引»; Attention-evolution page §4.4): blocks of `block` entries,
+ * block score = the block max (from csa2_index_score); the newest visible block
+ * floor((V-1)/block) is always kept and the remaining n_keep-1 slots go to the best
+ * other blocks by (block max desc, block id asc).  If ceil(V/block) <= n_keep,
+ * every visible block is kept; V == 0 gives an all -1 row.
+ *   block_max  : [rows, ld] f32 (first ceil(V/block) used)
+ *   n_visible  : [rows] int64 (V per row)
+ *   out_blocks : [rows, n_keep] int32 ascending, -1 padded.   1 <= n_keep <= 4096.
+ */
+csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
+                            const int64_t* n_visible, int block, int n_keep,
+                            int32_t* out_blocks, void* stream);
+
+/*
+ * csa2_sparse_attn -- shared-KV MQA over the selected compressed entries plus the
+ * sliding window (DSA-to-CSA/HCA page eqs. (18)-(19), (27), «因果边界与短滑窗»;
+ * CSA2 page «保留了 CSA 的骨架»).  For query (b,q) at position t = q_pos[b,q] and
+ * head i, the key/value rows are
+ *     { kv[b, s] : s in idx[b,q,:], s != -1 }  U  { window rows at positions
+ *       max(0, t-window+1) .. t, slot (p - swa_pos0) mod swa_cap of swa[b] }.
+ * With the default flags: q^ = RoPE_t(RMSNorm(q)), k^_j = RMSNorm(row_j) (stored
+ * rows are already rotated at their own positions), z_j = q^.k^_j / sqrt(c),
+ * p_j = e^{z_j} / (sum_l e^{z_l} + e^{sink_i}),  out = RoPE_{-t}(sum_j p_j k^_j).
+ * Reuse layers call this with an upstream layer's idx (no indexer).
+ *
+ *   q     : [B, Q, H, c] in q_dt (F32 or BF16)
+ *   kv    : [B, N, c] (F32, BF16) or [B, N, c/2 + c/16] B (CSA2_FP4_E4M3x16)
+ *   idx   : [B, Q, k] int32, -1 = none; ids outside [0, N) are skipped and flagged
+ *   swa   : [B, swa_cap, c] in swa_dt (F32 or BF16); window <= swa_cap
+ *   q_pos : [B, Q] int64
+ *   sink  : [H] f32 or NULL (no sink term)
+ *   out   : [B, Q, H, c] in out_dt (F32 or BF16);  lse: [B, Q, H] f32 or NULL,
+ *           lse = log(sum_j e^{z_j} + e^{sink_i})
+ * c == 512 (RoPE needs c >= 64 when CSA2_ROPE), 1 <= H <= 128, 0 <= k <= 2048,
+ * 0 <= window <= 1024.
+ */
+csa2_status csa2_sparse_attn(csa2_ctx* ctx,
+                             const void* q, csa2_dtype q_dt,
+                             const void* kv, csa2_dtype kv_dt, int64_t N,
+                             const int32_t* idx, int k,
+                             const void* swa, csa2_dtype swa_dt, int64_t swa_cap,
+                             int64_t swa_pos0, int window,
+                             const int64_t* q_pos, const float* sink,
+                             int B, int Q, int H, int c, float rope_base, unsigned flags,
+                             void* out, csa2_dtype out_dt, float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

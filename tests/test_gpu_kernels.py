@@ -1,0 +1,355 @@
+"""GPU parity of each C-ABI entry point against the oracle (seeded inputs, sizes
+that span several tiles and a ragged tail, plus the edge cases)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_06_gb300 import csa2 as C
+from compressed_sparse_attention_06_gb300 import workloads as W
+from oracle import csa2_oracle as O
+from tests.helpers import assert_close, to_np, topk_swaps
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    C.load()
+    yield
+    C.csa2_ctx_check()
+
+
+def _rows(n, width, seed, dtype):
+    x = W.normal_tensor((n, width), seed, 0, torch.float64, DEV)
+    r = torch.exp(0.5 * W.normal_tensor((n, 1), seed, 1, torch.float64, DEV))
+    return (x * r).to(dtype)
+
+
+def _edge_rows(width, dtype):
+    """Rows that hit the format's corner cases."""
+    rows = []
+    z = torch.zeros(width, dtype=torch.float64)
+    rows.append(z.clone())                                      # all zero
+    r = z.clone(); r[: width // 2] = -0.0; rows.append(r)       # negative zeros
+    r = torch.full((width,), 1e-5, dtype=torch.float64); r[1::2] *= -1; rows.append(r)   # tiny
+    r = torch.full((width,), 1e4, dtype=torch.float64); r[::3] *= -0.37; rows.append(r)  # huge
+    ties = torch.tensor([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5,
+                         -5.0, -6.0], dtype=torch.float64)
+    rows.append(ties.repeat(width // 16))                       # RNE ties at scale 1
+    r = torch.linspace(-7, 7, width, dtype=torch.float64); rows.append(r)
+    r = torch.full((width,), 2.0 ** -130, dtype=torch.float64); r[0] = 2.0 ** -128; rows.append(r)  # subnormal
+    r = torch.full((width,), 448.0 * 6, dtype=torch.float64); rows.append(r)             # scale at E4M3 max
+    return torch.stack(rows).to(dtype).to(DEV)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt", [C.FP4_E4M3x16, C.MXFP4_E8M0x32])
+def test_fp4_pack_unpack_bit_exact(dtype, fmt):
+    width = 512 if fmt == C.FP4_E4M3x16 else 128
+    x = torch.cat([_rows(3001, width, 77, dtype), _edge_rows(width, dtype)])
+    got = to_np(C.csa2_fp4_pack(x, fmt))
+    xo = x.float().cpu().numpy()
+    ref = O.nvfp4_pack(xo) if fmt == C.FP4_E4M3x16 else O.mxfp4_pack(xo)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:5].tolist()}"
+    b = torch.from_numpy(ref).to(DEV)
+    for odt in (torch.float32, torch.bfloat16):
+        un = to_np(C.csa2_fp4_unpack(b, fmt, width, odt))
+        exp = O.nvfp4_unpack(ref, width) if fmt == C.FP4_E4M3x16 else O.mxfp4_unpack(ref, width)
+        np.testing.assert_array_equal(un, exp)
+
+
+@pytest.mark.parametrize("case", ["nonoverlap_f32_m2", "overlap_bf16_m4_state", "overlap_f32_m4_nostate",
+                                  "m1_identity_rope"])
+def test_compress(case):
+    c = 512
+    if case == "nonoverlap_f32_m2":
+        m, n, dt, overlap, state, flags = 2, 2 * 301, torch.float32, False, False, C.W_NORM | C.W_ROPE
+    elif case == "overlap_bf16_m4_state":
+        m, n, dt, overlap, state, flags = 4, 4 * 203, torch.bfloat16, True, True, C.W_NORM | C.W_ROPE
+    elif case == "overlap_f32_m4_nostate":
+        m, n, dt, overlap, state, flags = 4, 4 * 77, torch.float32, True, False, 0
+    else:
+        m, n, dt, overlap, state, flags = 1, 37, torch.bfloat16, False, False, C.W_ROPE
+    g = lambda s, shape, std=1.0: W.normal_tensor(shape, 900 + s, 0, dt if s < 6 else torch.float32, DEV, std=std)
+    Ca, Za, Cb, Zb = g(1, (n, c)), g(2, (n, c)), g(3, (n, c)), g(4, (n, c))
+    Ba, Bb = g(6, (m, c), 0.1), g(7, (m, c), 0.1)
+    pCb, pZb = g(8, (m, c)).to(dt), g(9, (m, c)).to(dt)
+    pos0 = 131072
+    kw = dict(ba=Ba, pos0=pos0, flags=flags)
+    if overlap:
+        kw.update(cb=Cb, zb=Zb, bb=Bb)
+        if state:
+            kw.update(prev_cb=pCb, prev_zb=pZb)
+    out = C.csa2_compress(Ca, Za, m, out_fmt="f32" if dt == torch.float32 else "bf16", **kw)
+    npy = lambda t: None if t is None else t.double().cpu().numpy()
+    E = O.compress(npy(Ca), npy(Za), m, npy(Ba), npy(Cb) if overlap else None, npy(Zb) if overlap else None,
+                   npy(Bb) if overlap else None, npy(pCb) if state else None, npy(pZb) if state else None)
+    ref = O.compress_write(E, flags, m, pos0)
+    assert_close(to_np(out), ref, 1e-4 if dt == torch.float32 else 2e-2, case)
+    if m == 1 and flags == C.W_ROPE:
+        # m = 1: the entry is its token, only rotated
+        np.testing.assert_allclose(to_np(out)[:, :448], npy(Ca)[:, :448], rtol=0, atol=0)
+    # the fused FP4 store equals packing the f32 result with csa2_fp4_pack
+    out32 = C.csa2_compress(Ca, Za, m, out_fmt="f32", **kw)
+    packed = C.csa2_compress(Ca, Za, m, out_fmt="fp4", **kw)
+    np.testing.assert_array_equal(to_np(packed), to_np(C.csa2_fp4_pack(out32)))
+
+
+def test_compress_worked_example_padded():
+    # The pages' csa_compress example (m=2, c=3) embedded in 128 channels.
+    g = O  # noqa: F841
+    Ca = torch.zeros((4, 128), device=DEV)
+    Cb = torch.zeros((4, 128), device=DEV)
+    Ca[:2, :3], Ca[2:, :3] = 1.0, 3.0
+    Cb[:2, :3], Cb[2:, :3] = 2.0, 4.0
+    Z = torch.zeros_like(Ca)
+    y = to_np(C.csa2_compress(Ca, Z, 2, cb=Cb, zb=Z))
+    np.testing.assert_array_equal(y[0, :3], [1, 1, 1])
+    np.testing.assert_array_equal(y[1, :3], [2.5, 2.5, 2.5])
+
+
+def _index_inputs(B, Q, N, H_I, seed, q_dt, k_kind, grid=False):
+    qI = W.normal_tensor((B, Q, H_I, 128), seed, 1, torch.float64, DEV)
+    w = W.normal_tensor((B, Q, H_I), seed, 2, torch.float64, DEV)
+    KI = W.normal_tensor((B, N, 128), seed, 3, torch.float64, DEV) * torch.exp(
+        0.5 * W.normal_tensor((B, N, 1), seed, 4, torch.float64, DEV))
+    if grid:
+        # exact-grid inputs: every partial sum is exact in f32 in any order
+        qI = torch.clamp(torch.round(qI * 8) / 8, -4, 4)
+        KI = torch.clamp(torch.round(KI * 2) / 2, -4, 4)
+        w = torch.round(w * 2) / 2
+    qI = qI.to(q_dt)
+    w = w.float()
+    if k_kind == "mx":
+        kI = C.csa2_fp4_pack(KI.float().reshape(B * N, 128), C.MXFP4_E8M0x32).reshape(B, N, 68)
+        K_np = O.mxfp4_unpack(O.mxfp4_pack(KI.float().reshape(B * N, 128).cpu().numpy())).reshape(B, N, 128)
+    else:
+        kI = KI.to(torch.float32 if k_kind == "f32" else torch.bfloat16)
+        K_np = kI.double().cpu().numpy()
+    return qI, w, kI, K_np
+
+
+@pytest.mark.parametrize("q_dt,k_kind", [(torch.float32, "f32"), (torch.bfloat16, "bf16"),
+                                         (torch.bfloat16, "mx"), (torch.float32, "mx")])
+@pytest.mark.parametrize("grid", [False, True])
+def test_index_score_full_scan(q_dt, k_kind, grid):
+    B, Q, N, H_I = 2, 3, 1000 + 357, 64 if q_dt == torch.bfloat16 else 8
+    qI, w, kI, K_np = _index_inputs(B, Q, N, H_I, 31, q_dt, k_kind, grid)
+    nv = torch.tensor([[N, N - 1, 0], [777, 1, N - 8]], dtype=torch.int64, device=DEV)
+    sc, bm = C.csa2_index_score(qI, w, kI, nv, want_block_max=True)
+    sc, bm = to_np(sc), to_np(bm)
+    qn, wn = qI.double().cpu().numpy(), w.double().cpu().numpy()
+    for b in range(B):
+        for q in range(Q):
+            V = int(nv[b, q])
+            ref = O.index_score(qn[b, q], wn[b, q], K_np[b], V)
+            if grid:
+                np.testing.assert_array_equal(sc[b, q], ref)        # exact in f32 in any order
+            else:
+                assert_close(sc[b, q], ref, 1e-4, f"scores b{b} q{q}")
+            refb = O.block_max(ref, V, 8)
+            nb = (N + 7) // 8
+            full = np.full(nb, -np.inf)
+            full[: len(refb)] = refb
+            if grid:
+                np.testing.assert_array_equal(bm[b, q], full)
+            else:
+                assert_close(bm[b, q], full, 1e-4, "block max")
+
+
+@pytest.mark.parametrize("k_kind", ["bf16", "mx"])
+def test_index_score_candidates(k_kind):
+    B, Q, N, H_I = 2, 1, 5000, 64
+    qI, w, kI, K_np = _index_inputs(B, Q, N, H_I, 41, torch.bfloat16, k_kind)
+    nv = torch.tensor([[N - 3], [4000]], dtype=torch.int64, device=DEV)
+    n_pool = 300
+    pool = torch.full((B, Q, n_pool), -1, dtype=torch.int32)
+    for b in range(B):
+        V = int(nv[b, 0])
+        nb = (V + 7) // 8
+        sel = W.distinct_sample(nb - 1, 250, 55, b)
+        pool[b, 0, :251] = torch.sort(torch.cat([sel, torch.tensor([nb - 1])])).values.to(torch.int32)
+    pool = pool.to(DEV)
+    sc, _ = C.csa2_index_score(qI, w, kI, nv, pool=pool)
+    idx, val = C.csa2_topk(sc, nv, 512, pool=pool, want_scores=True)
+    sc, idx = to_np(sc), to_np(idx)
+    qn, wn = qI.double().cpu().numpy(), w.double().cpu().numpy()
+    for b in range(B):
+        V = int(nv[b, 0])
+        full = O.index_score(qn[b, 0], wn[b, 0], K_np[b], V)
+        pl = to_np(pool[b, 0])
+        for c_ in range(n_pool * 8):
+            blk = pl[c_ // 8]
+            s = blk * 8 + c_ % 8
+            if blk < 0 or s >= V:
+                assert sc[b, 0, c_] == -np.inf
+            else:
+                assert abs(sc[b, 0, c_] - full[s]) <= 1e-4 * (abs(full[s]) + 64)
+        ref = O.reindex_topk(full, pl, V, 512)
+        cand = O.pool_candidates(pl, V)
+        masked = np.full(N, -np.inf)
+        masked[cand] = full[cand]
+        # compare as a top-k restricted to the candidates
+        gpu = [i for i in idx[b, 0] if i >= 0]
+        assert len(gpu) == len([i for i in ref if i >= 0])
+        assert set(gpu) <= set(cand.tolist())
+        if gpu != [i for i in ref if i >= 0]:
+            kth = np.sort(full[cand])[::-1][511]
+            for i in set(gpu) ^ set(int(x) for x in ref if x >= 0):
+                assert abs(full[i] - kth) <= 1e-5 * np.sqrt(np.mean(full[:V] ** 2))
+
+
+def _score_rows(rows, n, seed, ties):
+    x = W.normal_tensor((rows, n), seed, 0, torch.float64, DEV)
+    if ties:
+        x = torch.round(x * 2)           # heavy ties
+    x = x.float()
+    x[0, ::3] = -0.0                      # negative zeros mixed with zeros
+    x[0, 1::3] = 0.0
+    return x
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (100, 512), (5000, 512), (70001, 512), (16384, 512), (3000, 2048)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_bit_exact(n, k, ties):
+    rows = 5
+    s = _score_rows(rows, n, 61 + n, ties)
+    nv = torch.tensor([n, max(n - 1, 0), min(n, k), 0, n // 2], dtype=torch.int64, device=DEV)
+    idx, val = C.csa2_topk(s, nv, k, want_scores=True)
+    idx, val, sn = to_np(idx), to_np(val), s.double().cpu().numpy()
+    for r in range(rows):
+        ref = O.topk(sn[r], int(nv[r]), k)
+        np.testing.assert_array_equal(idx[r], ref)
+        exp_val = np.where(ref >= 0, sn[r][np.maximum(ref, 0)], -np.inf)
+        np.testing.assert_array_equal(val[r], exp_val)
+
+
+def test_topk_all_equal_scores():
+    s = torch.full((2, 10000), 3.25, device=DEV)
+    nv = torch.tensor([10000, 600], dtype=torch.int64, device=DEV)
+    idx, _ = C.csa2_topk(s, nv, 512)
+    np.testing.assert_array_equal(to_np(idx), np.stack([np.arange(512), np.arange(512)]))
+
+
+@pytest.mark.parametrize("V", [0, 1, 8, 9, 100, 8 * 2048, 8 * 2048 + 1, 131071, 1048575])
+@pytest.mark.parametrize("ties", [False, True])
+def test_block_pool_bit_exact(V, ties):
+    nb_max = (1048575 + 7) // 8
+    n_keep = 2048
+    bm = _score_rows(2, nb_max, 71, ties)
+    nv = torch.tensor([V, max(V - 5, 0)], dtype=torch.int64, device=DEV)
+    pool = to_np(C.csa2_block_pool(bm, nv, 8, n_keep))
+    bmn = bm.double().cpu().numpy()
+    for r in range(2):
+        Vr = int(nv[r])
+        ref = O.block_pool(bmn[r][: (Vr + 7) // 8], Vr, 8, n_keep)
+        np.testing.assert_array_equal(pool[r], ref)
+
+
+def test_sink_and_worked_example_through_abi(golden):
+    """The pages' sparse_shared_kv example through csa2_index_score, csa2_topk and
+    csa2_sparse_attn (flags off, no window).  Vectors are zero-padded to the
+    library's widths and the query is scaled by sqrt(512/2) so the 1/sqrt(c)
+    logit scale equals the example's 1/sqrt(2)."""
+    g = golden("sparse_shared_kv_example.json")
+    hd = g["hand_derived"]
+    iq = torch.zeros((1, 1, 2, 128), device=DEV)
+    iq[0, 0, :, :2] = torch.tensor(g["iq"])
+    ik = torch.zeros((1, 3, 128), device=DEV)
+    ik[0, :, :2] = torch.tensor(g["ik"])
+    w = torch.tensor([[g["head_weight"]]], device=DEV)
+    nv = torch.tensor([[3]], dtype=torch.int64, device=DEV)
+    sc, _ = C.csa2_index_score(iq, w, ik, nv)
+    np.testing.assert_array_equal(to_np(sc)[0, 0], hd["scores"])
+    idx, _ = C.csa2_topk(sc, nv, g["k"])
+    np.testing.assert_array_equal(to_np(idx)[0, 0], hd["ids_ascending"])
+    q = torch.zeros((1, 1, 1, 512), device=DEV)
+    q[0, 0, 0, :2] = torch.tensor(g["q"]) * math.sqrt(512 / 2)
+    kv = torch.zeros((1, 3, 512), device=DEV)
+    kv[0, :, :2] = torch.tensor(g["kv"])
+    pos = torch.tensor([[0]], dtype=torch.int64, device=DEV)
+    sink = torch.tensor([g["sink_logit"]], device=DEV)
+    out, lse = C.csa2_sparse_attn(q, kv, idx, None, pos, sink, window=0, flags=0, want_lse=True)
+    o = to_np(out)[0, 0, 0]
+    np.testing.assert_allclose(o[:2], hd["out"], rtol=1e-6)
+    assert np.all(o[2:] == 0)
+    a, b = math.exp(math.sqrt(2)), math.exp(1 / math.sqrt(2))
+    np.testing.assert_allclose(to_np(lse)[0, 0, 0], math.log(a + b + 1), rtol=1e-6)
+
+
+@pytest.mark.parametrize("kv_kind", ["f32", "bf16", "fp4"])
+@pytest.mark.parametrize("flags", [C.ATTN_DEFAULT, 0, C.QNORM | C.KVNORM])
+def test_sparse_attn(kv_kind, flags):
+    B, Q, H, N = 2, 3, 16, 3000
+    q_dt = torch.float32 if kv_kind == "f32" else torch.bfloat16
+    q = W.normal_tensor((B, Q, H, 512), 81, 1, q_dt, DEV)
+    kv_f = W.normal_tensor((B, N, 512), 81, 2, torch.float32, DEV) * 1.5
+    if kv_kind == "fp4":
+        kv = C.csa2_fp4_pack(kv_f)
+        kv_np = O.nvfp4_unpack(O.nvfp4_pack(kv_f.reshape(-1, 512).cpu().numpy())).reshape(B, N, 512)
+    else:
+        kv = kv_f.to(q_dt)
+        kv_np = kv.double().cpu().numpy()
+    cap = 128
+    swa = W.normal_tensor((B, cap, 512), 81, 3, q_dt, DEV)
+    q_pos = torch.tensor([[N, 5, 1000], [70, N + 200, 0]], dtype=torch.int64, device=DEV)
+    k = 512
+    idx = torch.full((B, Q, k), -1, dtype=torch.int32)
+    for b in range(B):
+        for qq in range(Q):
+            V = min(int(q_pos[b, qq]), N)
+            n = min(V, [512, 300, 17][qq % 3])
+            if n:
+                idx[b, qq, :n] = W.distinct_sample(V, n, 83 + b, qq).to(torch.int32)
+    idx = idx.to(DEV)
+    sink = W.normal_tensor((H,), 81, 4, torch.float32, DEV)
+    out, lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=128, flags=flags, out_dtype=torch.float32,
+                                  want_lse=True)
+    out, lse = to_np(out), to_np(lse)
+    tol = 1e-4 if kv_kind == "f32" else 2e-2
+    for b in range(B):
+        for qq in range(Q):
+            t = int(q_pos[b, qq])
+            o, l, mass = O.sparse_attn(q[b, qq].double().cpu().numpy(), kv_np[b], to_np(idx[b, qq]),
+                                       swa[b].double().cpu().numpy(), 0, t, sink.double().cpu().numpy(), 128, flags)
+            assert_close(out[b, qq], o, tol, f"out b{b} q{qq}")
+            assert_close(lse[b, qq], l, 1e-5, "lse")
+            assert np.all((mass > 0) & (mass < 1))
+
+
+def test_sparse_attn_linear_window_and_no_sink():
+    B, Q, H, N = 1, 2, 8, 500
+    q = W.normal_tensor((B, Q, H, 512), 91, 1, torch.bfloat16, DEV)
+    kv = W.normal_tensor((B, N, 512), 91, 2, torch.bfloat16, DEV)
+    pos0 = 10000
+    swa = W.normal_tensor((B, 400, 512), 91, 3, torch.bfloat16, DEV)   # positions 10000..10399
+    q_pos = torch.tensor([[10127, 10399]], dtype=torch.int64, device=DEV)
+    idx = torch.arange(0, 512, dtype=torch.int32, device=DEV).clamp(max=N - 1).reshape(1, 1, 512).repeat(1, 2, 1)
+    idx[:, :, N:] = -1
+    out, _ = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, None, window=128, swa_pos0=pos0, out_dtype=torch.float32)
+    for qq in range(Q):
+        o, _, mass = O.sparse_attn(q[0, qq].double().cpu().numpy(), kv[0].double().cpu().numpy(),
+                                   to_np(idx[0, qq]), swa[0].double().cpu().numpy(), pos0, int(q_pos[0, qq]),
+                                   None, 128)
+        assert_close(to_np(out)[0, qq], o, 2e-2, "linear window")
+        np.testing.assert_allclose(mass, 1.0, rtol=1e-12)
+
+
+def test_out_of_range_index_is_flagged_not_faulted():
+    B, Q, H, N = 1, 1, 8, 100
+    q = torch.randn((B, Q, H, 512), device=DEV)
+    kv = torch.randn((B, N, 512), device=DEV)
+    idx = torch.tensor([[[3, 7, N + 5, -1]]], dtype=torch.int32, device=DEV)
+    pos = torch.tensor([[50]], dtype=torch.int64, device=DEV)
+    C.csa2_sparse_attn(q, kv, idx, None, pos, None, window=0)
+    with pytest.raises(C.Csa2Error) as e:
+        C.csa2_ctx_check()
+    assert e.value.status == C.ERR_DEVICE
+    C.csa2_ctx_check()   # cleared
