@@ -25,6 +25,7 @@ W_NORM, W_ROPE = 1, 2
 # symbols declared in include/csa2.h
 EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_ctx_create", "csa2_ctx_destroy", "csa2_ctx_check",
+    "csa2_ctx_test_stall_next",
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
     "csa2_block_pool", "csa2_sparse_attn",
 )
@@ -49,9 +50,10 @@ def _declare(lib):
         "csa2_ctx_create": (_i, [_i, ctypes.POINTER(_vp)]),
         "csa2_ctx_destroy": (_i, [_vp]),
         "csa2_ctx_check": (_i, [_vp, _vp]),
-        "csa2_compress": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _f, _u,
-                               _vp, _i, _vp]),
-        "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _vp]),
+        "csa2_ctx_test_stall_next": (_i, [_vp, ctypes.c_longlong]),
+        "csa2_compress": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _vp, _f, _u,
+                               _vp, _i, _i64, _vp]),
+        "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
                                   _vp, _vp]),
@@ -138,14 +140,25 @@ def csa2_ctx_check(device: Optional[int] = None):
     _check("csa2_ctx_check", _lib().csa2_ctx_check(ctx(dev), _vp(torch.cuda.current_stream(dev).cuda_stream)))
 
 
-def csa2_fp4_pack(x: torch.Tensor, fmt: int = FP4_E4M3x16, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Pack rows [..., c] into FP4 (E2M1 + E4M3/16) or MXFP4 (E2M1 + E8M0/32) rows."""
+def csa2_ctx_test_stall_next(budget_cycles: int = 0, device: Optional[int] = None):
+    """Test hook: the next tensor-core indexer launch runs with a silent producer, so its
+    bounded waits expire and csa2_ctx_check() raises a timeout."""
+    _check("csa2_ctx_test_stall_next", _lib().csa2_ctx_test_stall_next(ctx(device), budget_cycles))
+
+
+def csa2_fp4_pack(x: torch.Tensor, fmt: int = FP4_E4M3x16, out: Optional[torch.Tensor] = None,
+                  out_ld: int = 0) -> torch.Tensor:
+    """Pack rows [..., c] into FP4 (E2M1 + E4M3/16) or MXFP4 (E2M1 + E8M0/32) rows.
+    With out_ld > 0, packed row r goes to byte offset r*out_ld of `out` (e.g. one new
+    row per sequence written straight into a [B, N, row_bytes] cache)."""
     c = x.shape[-1]
     rows = x.numel() // c if c else 0
     rb = fp4_row_bytes(c) if fmt == FP4_E4M3x16 else mxfp4_row_bytes(c)
     if out is None:
         out = torch.empty((*x.shape[:-1], rb), dtype=torch.uint8, device=x.device)
-    _check("csa2_fp4_pack", _lib().csa2_fp4_pack(ctx(x.device.index), _p(x), _dt(x), rows, c, fmt, _p(out),
+        out_ld = 0
+    ptr = _vp(out.data_ptr()) if out_ld else _p(out)
+    _check("csa2_fp4_pack", _lib().csa2_fp4_pack(ctx(x.device.index), _p(x), _dt(x), rows, c, fmt, ptr, out_ld,
                                                  _stream(x)))
     return out
 
@@ -161,20 +174,31 @@ def csa2_fp4_unpack(b: torch.Tensor, fmt: int, c: int, out_dtype=torch.float32,
 
 
 def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=None, prev_zb=None,
-                  pos0: int = 0, rope_base: float = 10000.0, flags: int = 0, out_fmt: str = "f32",
-                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Compressed entries [n/m, c]; out_fmt 'f32', 'bf16' or 'fp4' (packed rows)."""
-    n, c = ca.shape
+                  pos0=0, rope_base: float = 10000.0, flags: int = 0, out_fmt: str = "f32",
+                  out: Optional[torch.Tensor] = None, out_seq_stride: Optional[int] = None) -> torch.Tensor:
+    """Compressed entries of one token stream [n, c] or a batch [B, n, c] -> [.., n/m, c]
+    (out_fmt 'f32', 'bf16') or packed FP4 rows ('fp4').  pos0: int or [B] int64 tensor
+    (position of each stream's first token).  With `out` and `out_seq_stride`, entry i
+    of stream b goes to row b*out_seq_stride + i of `out` (e.g. into a cache)."""
+    batched = ca.dim() == 3
+    B, n, c = (ca.shape if batched else (1, *ca.shape))
+    n_ent = n // m
     if out is None:
+        shape = (B, n_ent) if batched else (n_ent,)
         if out_fmt == "fp4":
-            out = torch.empty((n // m, fp4_row_bytes(c)), dtype=torch.uint8, device=ca.device)
+            out = torch.empty((*shape, fp4_row_bytes(c)), dtype=torch.uint8, device=ca.device)
         else:
-            out = torch.empty((n // m, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16,
+            out = torch.empty((*shape, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16,
                               device=ca.device)
+    oss = n_ent if out_seq_stride is None else out_seq_stride
     out_dt = FP4_E4M3x16 if out.dtype == torch.uint8 else _dt(out)
+    if isinstance(pos0, torch.Tensor):
+        pos_t = pos0.to(device=ca.device, dtype=torch.int64).contiguous()
+    else:
+        pos_t = torch.full((B,), int(pos0), dtype=torch.int64, device=ca.device)
     st = _lib().csa2_compress(ctx(ca.device.index), _p(ca), _p(za), _p(cb), _p(zb), _dt(ca), _p(ba), _p(bb),
-                              _p(prev_cb), _p(prev_zb), n, c, m, pos0, rope_base, flags, _p(out), out_dt,
-                              _stream(ca))
+                              _p(prev_cb), _p(prev_zb), B, n, c, m, _p(pos_t), rope_base, flags,
+                              _vp(out.data_ptr()), out_dt, oss, _stream(ca))
     _check("csa2_compress", st)
     return out
 

@@ -41,12 +41,26 @@ template <typename T, int OUT>
 __global__ void __launch_bounds__(256) compress_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
     const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
-    const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int c, int m, int64_t pos0,
-    float rope_base, unsigned flags, void* __restrict__ out) {
-    const int64_t i = blockIdx.x;
+    const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
+    const int64_t* __restrict__ pos0_arr, float rope_base, unsigned flags, void* __restrict__ out,
+    int64_t out_seq_stride) {
+    const int64_t i = blockIdx.x;            // entry within the stream
+    const int64_t bseq = blockIdx.y;         // stream (sequence)
     const int t = threadIdx.x;
     const int ch = 4 * t;
     const bool overlap = cb != nullptr;
+    const int64_t in_off = bseq * n_tokens * (int64_t)c;
+    ca += in_off;
+    za += in_off;
+    if (overlap) {
+        cb += in_off;
+        zb += in_off;
+    }
+    if (prev_cb) {
+        prev_cb += bseq * (int64_t)m * c;
+        prev_zb += bseq * (int64_t)m * c;
+    }
+    const int64_t orow = bseq * out_seq_stride + i;
     // history rows: block i-1 of (cb, zb), or the carried state for block 0
     const T* hc = nullptr;
     const T* hz = nullptr;
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
     }
     // RoPE on the last 64 channels (interleaved pairs) at the entry's position
     if ((flags & CSA2_W_ROPE) && ch >= c - 64) {
-        const int64_t pos = pos0 + (int64_t)m * i;
+        const int64_t pos = (pos0_arr ? pos0_arr[bseq] : 0) + (int64_t)m * i;
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             int j = (ch + 2 * p - (c - 64)) >> 1;
@@ -140,10 +154,10 @@ __global__ void __launch_bounds__(256) compress_kernel(
     }
     // store
     if (OUT == OUT_F32) {
-        float* o = reinterpret_cast<float*>(out) + i * (int64_t)c + ch;
+        float* o = reinterpret_cast<float*>(out) + orow * (int64_t)c + ch;
         *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
     } else if (OUT == OUT_BF16) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + i * (int64_t)c + ch;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + orow * (int64_t)c + ch;
         uint2 u;
         u.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[0])) |
               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[1])) << 16);
@@ -161,7 +175,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
         if (s != 0.0f)
             codes = e2m1x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s)) |
                     (e2m1x2(__fdiv_rn(y[2], s), __fdiv_rn(y[3], s)) << 8);
-        uint8_t* row = reinterpret_cast<uint8_t*>(out) + i * fp4_row_bytes(c);
+        uint8_t* row = reinterpret_cast<uint8_t*>(out) + orow * fp4_row_bytes(c);
         *reinterpret_cast<uint16_t*>(row + ch / 2) = (uint16_t)codes;
         if ((t & 3) == 0) row[c / 2 + ch / 16] = (uint8_t)sb;
     }
@@ -169,10 +183,10 @@ __global__ void __launch_bounds__(256) compress_kernel(
 
 template <typename T>
 csa2_status launch_compress(const void* ca, const void* za, const void* cb, const void* zb,
-                            const float* ba, const float* bb, const void* pcb, const void* pzb,
-                            int64_t n_entries, int c, int m, int64_t pos0, float base,
-                            unsigned flags, void* out, csa2_dtype out_dt, cudaStream_t s) {
-    dim3 grid((unsigned)n_entries), block(c / 4);
+                            const float* ba, const float* bb, const void* pcb, const void* pzb, int B,
+                            int64_t n_tokens, int c, int m, const int64_t* pos0, float base, unsigned flags,
+                            void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
+    dim3 grid((unsigned)(n_tokens / m), (unsigned)B), block(c / 4);
     const T* a = (const T*)ca;
     const T* z = (const T*)za;
     const T* b = (const T*)cb;
@@ -180,11 +194,14 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
     const T* p1 = (const T*)pcb;
     const T* p2 = (const T*)pzb;
     if (out_dt == CSA2_F32)
-        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+                                                            flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+                                                             flags, out, oss);
     else
-        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, c, m, pos0, base, flags, out);
+        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+                                                            flags, out, oss);
     return csa2_launch_status();
 }
 
@@ -192,10 +209,10 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
 
 extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* za, const void* cb,
                                      const void* zb, csa2_dtype in_dt, const float* ba, const float* bb,
-                                     const void* prev_cb, const void* prev_zb, int64_t n_tokens, int c,
-                                     int m, int64_t pos0, float rope_base, unsigned flags, void* out,
-                                     csa2_dtype out_dt, void* stream) {
-    if (!ctx || n_tokens < 0 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
+                                     const void* prev_cb, const void* prev_zb, int B, int64_t n_tokens, int c,
+                                     int m, const int64_t* pos0, float rope_base, unsigned flags, void* out,
+                                     csa2_dtype out_dt, int64_t out_seq_stride, void* stream) {
+    if (!ctx || B < 0 || B > 65535 || n_tokens < 0 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
     if (n_tokens % m) return CSA2_ERR_INVALID_ARG;
     if (c % 128 || c > 1024) return CSA2_ERR_INVALID_ARG;
     if ((cb == nullptr) != (zb == nullptr)) return CSA2_ERR_INVALID_ARG;
@@ -204,7 +221,8 @@ extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* 
     if (flags & ~(CSA2_W_NORM | CSA2_W_ROPE)) return CSA2_ERR_INVALID_ARG;
     if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
     if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16) return CSA2_ERR_UNSUPPORTED;
-    if (n_tokens == 0) return CSA2_OK;
+    if (n_tokens == 0 || B == 0) return CSA2_OK;
+    if (out_seq_stride < n_tokens / m && B > 1) return CSA2_ERR_INVALID_ARG;
     if (!ca || !za || !out) return CSA2_ERR_INVALID_ARG;
     const size_t va = in_dt == CSA2_F32 ? 16 : 8;
     if (!aligned(ca, va) || !aligned(za, va) || (cb && (!aligned(cb, va) || !aligned(zb, va))) ||
@@ -214,8 +232,8 @@ extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* 
     if (n_tokens / m > 0x7FFFFFFF) return CSA2_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
     if (in_dt == CSA2_F32)
-        return launch_compress<float>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, n_tokens / m, c, m, pos0,
-                                      rope_base, flags, out, out_dt, s);
-    return launch_compress<__nv_bfloat16>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, n_tokens / m, c, m, pos0,
-                                          rope_base, flags, out, out_dt, s);
+        return launch_compress<float>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, B, n_tokens, c, m, pos0, rope_base,
+                                      flags, out, out_dt, out_seq_stride, s);
+    return launch_compress<__nv_bfloat16>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, B, n_tokens, c, m, pos0,
+                                          rope_base, flags, out, out_dt, out_seq_stride, s);
 }

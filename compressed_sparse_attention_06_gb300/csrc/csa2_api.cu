@@ -31,6 +31,8 @@ extern "C" csa2_status csa2_ctx_create(int device, csa2_ctx** out) {
     c->device = device;
     c->status = nullptr;
     c->num_sms = 0;
+    c->stall_next = 0;
+    c->stall_budget = 0;
     cudaError_t e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = cudaMalloc(&c->status, sizeof(unsigned int));
     if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(unsigned int));
@@ -62,5 +64,12 @@ extern "C" csa2_status csa2_ctx_check(csa2_ctx* ctx, void* stream) {
     }
     if (word & CSA2_DEVBIT_TIMEOUT) return CSA2_ERR_TIMEOUT;
     if (word & CSA2_DEVBIT_RANGE) return CSA2_ERR_DEVICE;
+    return CSA2_OK;
+}
+
+extern "C" csa2_status csa2_ctx_test_stall_next(csa2_ctx* ctx, long long budget_cycles) {
+    if (!ctx || budget_cycles < 0) return CSA2_ERR_INVALID_ARG;
+    ctx->stall_next = 1;
+    ctx->stall_budget = budget_cycles;
     return CSA2_OK;
 }

@@ -11,6 +11,8 @@ struct csa2_ctx {
     int device;
     int num_sms;
     unsigned int* status;   // device word: bit 0 = out-of-range index, bit 1 = timeout
+    int stall_next;         // test hook: next tensor-core scan runs with a silent producer
+    long long stall_budget; // wait budget (cycles) for that launch
 };
 
 #define CSA2_DEVBIT_RANGE 1u

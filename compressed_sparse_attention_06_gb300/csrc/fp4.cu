@@ -13,7 +13,8 @@ namespace {
 
 // One thread per 16-channel group.
 template <typename T>
-__global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, uint8_t* __restrict__ out) {
+__global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, uint8_t* __restrict__ out,
+                                int64_t out_ld) {
     const int gpr = c / 16;
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= rows * gpr) return;
@@ -36,7 +37,7 @@ __global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, ui
             w1 |= e2m1x2(__fdiv_rn(v[8 + i], s), __fdiv_rn(v[8 + i + 1], s)) << (4 * i);
         }
     }
-    uint8_t* row = out + r * fp4_row_bytes(c);
+    uint8_t* row = out + r * out_ld;
     uint32_t* codes = reinterpret_cast<uint32_t*>(row + gi * 8);   // rows are 4-byte aligned
     codes[0] = w0;
     codes[1] = w1;
@@ -45,7 +46,8 @@ __global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, ui
 
 // One thread per 32-value group.
 template <typename T>
-__global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, uint8_t* __restrict__ out) {
+__global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, uint8_t* __restrict__ out,
+                                  int64_t out_ld) {
     const int gpr = d / 32;
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= rows * gpr) return;
@@ -73,7 +75,7 @@ __global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, 
         for (int i = 0; i < 32; i += 2)
             w[i / 8] |= e2m1x2(__fdiv_rn(v[i], X), __fdiv_rn(v[i + 1], X)) << (4 * (i % 8));
     }
-    uint8_t* row = out + r * mxfp4_row_bytes(d);
+    uint8_t* row = out + r * out_ld;
     uint32_t* codes = reinterpret_cast<uint32_t*>(row + gi * 16);
 #pragma unroll
     for (int i = 0; i < 4; ++i) codes[i] = w[i];
@@ -104,8 +106,8 @@ __global__ void fp4_unpack_kernel(const uint8_t* __restrict__ in, int64_t rows, 
 }  // namespace
 
 extern "C" csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_dt, int64_t rows, int c,
-                                     csa2_dtype fmt, uint8_t* out, void* stream) {
-    if (!ctx || rows < 0 || c <= 0) return CSA2_ERR_INVALID_ARG;
+                                     csa2_dtype fmt, uint8_t* out, int64_t out_ld, void* stream) {
+    if (!ctx || rows < 0 || c <= 0 || out_ld < 0 || (out_ld % 4)) return CSA2_ERR_INVALID_ARG;
     if (rows == 0) return CSA2_OK;
     if (!x || !out) return CSA2_ERR_INVALID_ARG;
     if (x_dt != CSA2_F32 && x_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
@@ -113,20 +115,24 @@ extern "C" csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_
     const int threads = 256;
     if (fmt == CSA2_FP4_E4M3x16) {
         if (c % 64) return CSA2_ERR_INVALID_ARG;   // keeps every row 4-byte aligned
+        if (out_ld == 0) out_ld = fp4_row_bytes(c);
+        if (out_ld < fp4_row_bytes(c)) return CSA2_ERR_INVALID_ARG;
         int64_t n = rows * (c / 16);
         dim3 grid((unsigned)((n + threads - 1) / threads));
         if (x_dt == CSA2_F32)
-            fp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out);
+            fp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out, out_ld);
         else
-            fp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out);
+            fp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out, out_ld);
     } else if (fmt == CSA2_MXFP4_E8M0x32) {
         if (c % 128) return CSA2_ERR_INVALID_ARG;  // keeps every row 4-byte aligned
+        if (out_ld == 0) out_ld = mxfp4_row_bytes(c);
+        if (out_ld < mxfp4_row_bytes(c)) return CSA2_ERR_INVALID_ARG;
         int64_t n = rows * (c / 32);
         dim3 grid((unsigned)((n + threads - 1) / threads));
         if (x_dt == CSA2_F32)
-            mxfp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out);
+            mxfp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out, out_ld);
         else
-            mxfp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out);
+            mxfp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out, out_ld);
     } else {
         return CSA2_ERR_UNSUPPORTED;
     }

@@ -79,6 +79,13 @@ csa2_status csa2_ctx_destroy(csa2_ctx* ctx);
    itself reports an error. */
 csa2_status csa2_ctx_check(csa2_ctx* ctx, void* stream);
 
+/* Failure-detection test hook.  The next tensor-core indexer launch on this
+   context runs with a producer that never signals its consumers, whose bounded
+   waits then expire after `budget_cycles` (0 = the default of 2^31 cycles) and
+   record CSA2_ERR_TIMEOUT; the kernel frees its tensor memory and exits, and the
+   context stays usable.  The flag clears after that one launch. */
+csa2_status csa2_ctx_test_stall_next(csa2_ctx* ctx, long long budget_cycles);
+
 /*
  * csa2_compress -- gated token compressor with its write epilogue.
  *
@@ -93,19 +100,25 @@ csa2_status csa2_ctx_check(csa2_ctx* ctx, void* stream);
  * Epilogue (Attention-evolution page §4.1): [RMSNorm] -> [RoPE at pos0 + m i]
  * -> store as out_dt (CSA2_FP4_E4M3x16 packs the row).
  *
- *   ca, za, cb, zb : [n_tokens, c] in in_dt (F32 or BF16)
+ * B independent token streams (sequences) are compressed in one call.
+ *   ca, za, cb, zb : [B, n_tokens, c] in in_dt (F32 or BF16)
  *   ba, bb         : [m, c] f32, NULL = 0
- *   prev_cb/prev_zb: [m, c] in in_dt, or both NULL
- *   out            : [n_tokens/m, c] in out_dt (F32, BF16) or [n_tokens/m, c/2+c/16] B
- * n_tokens % m == 0, c % 16 == 0, 64 <= c <= 1024 when CSA2_W_ROPE (RoPE on the
- * last 64 channels), m >= 1.
+ *   prev_cb/prev_zb: [B, m, c] in in_dt, or both NULL
+ *   pos0           : [B] int64 device array, position of each stream's first token
+ *                    (NULL = 0); entry i of stream b sits at pos0[b] + m*i
+ *   out            : entry i of stream b goes to row b*out_seq_stride + i of out,
+ *                    rows of c values in out_dt (F32, BF16) or c/2 + c/16 bytes
+ *                    (CSA2_FP4_E4M3x16); out_seq_stride >= n_tokens/m
+ * n_tokens % m == 0, c % 128 == 0, c <= 1024, m >= 1; RoPE acts on the last 64
+ * channels.
  */
 csa2_status csa2_compress(csa2_ctx* ctx,
                           const void* ca, const void* za, const void* cb, const void* zb,
                           csa2_dtype in_dt, const float* ba, const float* bb,
                           const void* prev_cb, const void* prev_zb,
-                          int64_t n_tokens, int c, int m, int64_t pos0, float rope_base,
-                          unsigned flags, void* out, csa2_dtype out_dt, void* stream);
+                          int B, int64_t n_tokens, int c, int m, const int64_t* pos0,
+                          float rope_base, unsigned flags, void* out, csa2_dtype out_dt,
+                          int64_t out_seq_stride, void* stream);
 
 /*
  * csa2_fp4_pack / csa2_fp4_unpack -- the two 4-bit cache formats.
@@ -113,11 +126,14 @@ csa2_status csa2_compress(csa2_ctx* ctx,
  *                       division); s == 0 -> codes 0; code = E2M1_RNE(x/s), sat. +-6.
  *   CSA2_MXFP4_E8M0x32 (c % 128 == 0): per 32 values X = 2^(floor(log2 amax) - 2) as E8M0,
  *                       amax == 0 -> scale byte 0, codes 0; code = E2M1_RNE(x/X).
- * x: [rows, c] in x_dt (F32 or BF16); out: [rows, row_bytes]; unpack writes F32 or
- * BF16 (exact: every FP4 value times its scale fits in bf16).
+ * x: [rows, c] in x_dt (F32 or BF16); packed row r is written at out + r*out_ld
+ * (out_ld in bytes, a multiple of 4, >= the row size; 0 = rows back to back), so a
+ * batch of new rows can go straight into per-sequence cache slots.  Unpack reads
+ * back-to-back rows and writes F32 or BF16 (exact: every FP4 value times its scale
+ * fits in bf16).
  */
 csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_dt, int64_t rows, int c,
-                          csa2_dtype fmt, uint8_t* out, void* stream);
+                          csa2_dtype fmt, uint8_t* out, int64_t out_ld, void* stream);
 csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, int64_t rows,
                             int c, void* out, csa2_dtype out_dt, void* stream);
 
