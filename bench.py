@@ -192,9 +192,9 @@ class FP4Decode:
         C.csa2_index_score(self.qI, self.w, self.ki, self.nv, pool=b.pool, block=self.block, scores=b.cand_scores)
         C.csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx)
         C.csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, window=self.window,
-                           out=b.out)
+                           out=b.out, ws=b.attn_ws)
 
-    launches_per_step = 7
+    launches_per_step = 8      # write x2, scan, pool, candidate scan, top-k, attention split + combine
 
     def scan_bytes(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row

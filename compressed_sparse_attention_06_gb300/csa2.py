@@ -27,7 +27,7 @@ EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_ctx_create", "csa2_ctx_destroy", "csa2_ctx_check",
     "csa2_ctx_test_stall_next",
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
-    "csa2_block_pool", "csa2_sparse_attn",
+    "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes",
 )
 
 
@@ -60,7 +60,8 @@ def _declare(lib):
         "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
         "csa2_block_pool": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
-                                  _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp]),
+                                  _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+        "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -259,12 +260,18 @@ def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
     return out
 
 
+def csa2_sparse_attn_workspace_bytes(B: int, Q: int, H: int, k: int, window: int,
+                                     device: Optional[int] = None) -> int:
+    return int(_lib().csa2_sparse_attn_workspace_bytes(ctx(device), B, Q, H, k, window))
+
+
 def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_pos0: int = 0,
                      kv_fmt: Optional[int] = None, rope_base: float = 10000.0, flags: int = ATTN_DEFAULT,
                      out_dtype=None, want_lse: bool = False, out: Optional[torch.Tensor] = None,
-                     lse: Optional[torch.Tensor] = None):
+                     lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None):
     """q [B,Q,H,c]; kv [B,N,c] (f32/bf16) or [B,N,row_bytes] uint8 (FP4); idx [B,Q,k] int32;
-    swa [B,cap,c]; q_pos [B,Q] int64.  Returns (out [B,Q,H,c], lse [B,Q,H] or None)."""
+    swa [B,cap,c]; q_pos [B,Q] int64.  Returns (out [B,Q,H,c], lse [B,Q,H] or None).
+    `ws` is the split-key workspace (allocated here when not given)."""
     B, Q, H, c = q.shape
     k = idx.shape[-1] if idx is not None else 0
     N = kv.shape[1] if kv is not None else 0
@@ -276,8 +283,11 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
         out = torch.empty((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
     if want_lse and lse is None:
         lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k, window, q.device.index)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
     st = _lib().csa2_sparse_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(idx), k, _p(swa), swa_dt,
                                  swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
-                                 _p(out), _dt(out), _p(lse), _stream(q))
+                                 _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
     _check("csa2_sparse_attn", st)
     return out, lse

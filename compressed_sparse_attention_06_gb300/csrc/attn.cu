@@ -4,24 +4,50 @@
 // head; the query is RMSNorm'd and rotated by RoPE_t on its last 64 dims; the
 // output is rotated back by RoPE_-t; the sink adds e^{z'_h} to the denominator only.
 //
-// CUDA-core kernel: a CTA per (query, group of 8 heads), one warp per head.  Key
-// slots (the k selected ids, then the window positions) are processed in chunks of
-// 32 rows staged in shared memory as f32 (FP4 rows are dequantised on the way in);
+// Split-key (flash-decoding) layout: a CTA per (key split, group of 8 heads,
+// query), one warp per head.  The CTA stages its key slots in chunks of 32 rows in
+// shared memory as f32 (FP4 rows dequantised on the way in, with each row's RMS),
 // each lane owns channels lane + 32 i of its head's query and accumulator, logits
-// are warp reductions, and the softmax is online (running max, running sum).
+// are warp reductions, and the softmax is online.  With one split the CTA finishes
+// the head (sink, normalisation, inverse RoPE); with several, each split writes its
+// partial (max, sum, unnormalised output) to the caller's workspace and
+// attn_combine_kernel merges them by log-sum-exp.
+#include <algorithm>
+
 #include "csa2_internal.cuh"
 
 namespace {
 
 constexpr int ATT_HG = 8;            // heads per CTA (one warp each)
 constexpr int ATT_THREADS = 32 * ATT_HG;
-constexpr int ATT_KC = 32;           // key rows per chunk
+constexpr int ATT_KC = 32;           // key rows per staged chunk
 constexpr int ATT_C = 512;           // head dim this kernel is built for
 constexpr int ATT_PER_LANE = ATT_C / 32;
+constexpr int PART = ATT_C + 2;      // floats per partial: max, sum, output
 
 enum KvKind { KV_F32 = 0, KV_BF16 = 1, KV_FP4 = 2 };
 
-// Load 16 channels [16*lane, 16*lane+16) of a row into f32.
+// Eight E2M1 codes (one 32-bit word, code 2i in the low nibble of byte i) -> f32,
+// through the exact E2M1 -> f16 conversion.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&o)[8]) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(*reinterpret_cast<__half2*>(&h[i]));
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+
+// Load 16 channels [16*lane, 16*lane+16) of a row into f32 (exact for every format).
 template <int KIND>
 __device__ __forceinline__ void load_row16(const void* base, int64_t row, int lane, float (&v)[16]) {
     if (KIND == KV_F32) {
@@ -46,98 +72,126 @@ __device__ __forceinline__ void load_row16(const void* base, int64_t row, int la
     } else {
         const uint8_t* r = reinterpret_cast<const uint8_t*>(base) + row * fp4_row_bytes(ATT_C);
         uint2 codes = *reinterpret_cast<const uint2*>(r + 8 * lane);
-        float s = e4m3_to_f32(r[ATT_C / 2 + lane]);
+        const float s = e4m3_to_f32(r[ATT_C / 2 + lane]);
+        float lo[8], hi[8];
+        e2m1x8_to_f32(codes.x, lo);
+        e2m1x8_to_f32(codes.y, hi);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            v[j] = e2m1_to_f32((codes.x >> (4 * j)) & 0xF) * s;
-            v[8 + j] = e2m1_to_f32((codes.y >> (4 * j)) & 0xF) * s;
+            v[j] = lo[j] * s;
+            v[8 + j] = hi[j] * s;
         }
     }
 }
 
-template <typename TQ, int KVK, typename TS, typename TO>
-__global__ void __launch_bounds__(ATT_THREADS) sparse_attn_simt_kernel(
-    const TQ* __restrict__ q, const void* __restrict__ kv, int64_t N, const int32_t* __restrict__ idx, int k,
-    const TS* __restrict__ swa, int64_t swa_cap, int64_t swa_pos0, int window, const int64_t* __restrict__ q_pos,
-    const float* __restrict__ sink, int Q, int H, float rope_base, unsigned flags, TO* __restrict__ out,
-    float* __restrict__ lse, unsigned int* st) {
-    extern __shared__ float smem[];
-    float* xs = smem;                                  // [ATT_KC][ATT_C]
-    float* rinv = xs + ATT_KC * ATT_C;                 // [ATT_KC]
-    int* slot_ref = reinterpret_cast<int*>(rinv + ATT_KC);   // [ATT_KC] >=0 entry id, <-1 window, -1 none
+struct AttnArgs {
+    const void* q;
+    const void* kv;
+    int64_t N;
+    const int32_t* idx;
+    int k;
+    const void* swa;
+    int64_t swa_cap, swa_pos0;
+    int window;
+    const int64_t* q_pos;
+    const float* sink;
+    int Q, H;
+    float rope_base;
+    unsigned flags;
+    void* out;
+    float* lse;
+    float* ws;            // [B*Q, H, n_split, PART] partials (n_split > 1)
+    int n_split;
+    int spl;              // key slots per split (multiple of ATT_KC)
+    unsigned int* st;
+};
 
-    const int64_t bq = blockIdx.x;
-    const int64_t b = bq / Q;
+// Rotate this warp's channels 448..511 (lanes hold lane+448 and lane+480) by +t
+// (sign = 1) or -t (sign = -1); pairs are (even lane, odd lane).
+__device__ __forceinline__ void rope_lanes(float (&x)[ATT_PER_LANE], int lane, const float* cs, const float* sn,
+                                           float sign) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int j = (lane + 32 * i) >> 1;
+        const float c = cs[j], s = sign * sn[j];
+        float v = x[14 + i];
+        float p = __shfl_xor_sync(0xffffffffu, v, 1);
+        x[14 + i] = (lane & 1) ? fmaf(p, s, v * c) : fmaf(-p, s, v * c);
+    }
+}
+
+template <typename TQ, int KVK, typename TS, typename TO>
+__global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnArgs a) {
+    extern __shared__ float smem[];
+    float* xs = smem;                                   // [ATT_KC][ATT_C]
+    float* rinv = xs + ATT_KC * ATT_C;                  // [ATT_KC]
+    int* slot_ok = reinterpret_cast<int*>(rinv + ATT_KC);   // [ATT_KC]
+    float* cs = reinterpret_cast<float*>(slot_ok + ATT_KC);  // [32] RoPE cos at t
+    float* sn = cs + 32;                                      // [32] RoPE sin at t
+
+    const int split = blockIdx.x;
+    const int64_t bq = blockIdx.z;
+    const int64_t b = bq / a.Q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * ATT_HG + warp;
-    const bool head_ok = h < H;
-    const int64_t t = q_pos[bq];
+    const bool head_ok = h < a.H;
+    const int64_t t = a.q_pos[bq];
     const float inv_sqrt_c = 1.0f / sqrtf((float)ATT_C);
+    const TQ* q = reinterpret_cast<const TQ*>(a.q);
+    if (threadIdx.x < 32) rope_cos_sin(t, threadIdx.x, a.rope_base, cs[threadIdx.x], sn[threadIdx.x]);
+    __syncthreads();
 
-    // ---- query: RMSNorm, RoPE_t; lane owns channels lane + 32 i ----
-    float qv[ATT_PER_LANE];
-    float acc[ATT_PER_LANE];
+    float qv[ATT_PER_LANE], acc[ATT_PER_LANE];
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) {
-        qv[i] = head_ok ? to_f32<TQ>(q[(bq * H + h) * (int64_t)ATT_C + lane + 32 * i]) : 0.0f;
+        qv[i] = head_ok ? to_f32<TQ>(q[(bq * a.H + h) * (int64_t)ATT_C + lane + 32 * i]) : 0.0f;
         acc[i] = 0.0f;
     }
-    if (flags & CSA2_QNORM) {
+    if (a.flags & CSA2_QNORM) {
         float ss = 0.0f;
 #pragma unroll
         for (int i = 0; i < ATT_PER_LANE; ++i) ss = fmaf(qv[i], qv[i], ss);
         ss = warp_sum(ss);
-        float r = 1.0f / sqrtf(ss / (float)ATT_C + 1e-6f);
+        const float r = 1.0f / sqrtf(ss / (float)ATT_C + 1e-6f);
 #pragma unroll
         for (int i = 0; i < ATT_PER_LANE; ++i) qv[i] *= r;
     }
-    // RoPE pair (448+2j, 449+2j) = (even lane, odd lane) of chunks i = 14, 15
-    float rc[2], rs[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        int ch = lane + 32 * (14 + i);
-        int j = (ch - (ATT_C - 64)) >> 1;
-        rope_cos_sin(t, j, rope_base, rc[i], rs[i]);
-    }
-    if (flags & CSA2_ROPE) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float x = qv[14 + i];
-            float p = __shfl_xor_sync(0xffffffffu, x, 1);
-            qv[14 + i] = (lane & 1) ? fmaf(p, rs[i], x * rc[i]) : fmaf(-p, rs[i], x * rc[i]);
-        }
-    }
+    if (a.flags & CSA2_ROPE) rope_lanes(qv, lane, cs, sn, 1.0f);
 
+    const int nw = (int)max((int64_t)0, min((int64_t)a.window, t + 1));   // window rows (positions >= 0)
+    const int n_slots = a.k + nw;
+    const int s_begin = split * a.spl;
+    const int s_end = min(n_slots, s_begin + a.spl);
     float m_run = -INFINITY, l_run = 0.0f;
-    const int nw = (int)max((int64_t)0, min((int64_t)window, t + 1));   // window rows present (positions >= 0)
-    const int n_slots = k + nw;
-    for (int c0 = 0; c0 < n_slots; c0 += ATT_KC) {
-        // ---- stage the chunk: warp w loads rows w, w+8, w+16, w+24 ----
+    for (int c0 = s_begin; c0 < s_end; c0 += ATT_KC) {
+        // stage the chunk: warp w loads rows w, w+8, w+16, w+24
         for (int r = warp; r < ATT_KC; r += ATT_HG) {
             const int sl = c0 + r;
-            int ref = -1;
+            int ok = 0;
             bool from_window = false;
             int64_t row = 0;
-            if (sl < k) {
-                int32_t id = idx[bq * k + sl];
-                if (id >= 0) {
-                    if (id < N) { ref = id; row = b * N + id; }
-                    else if (lane == 0) csa2_flag(st, CSA2_DEVBIT_RANGE);
+            if (sl < s_end) {
+                if (sl < a.k) {
+                    const int32_t id = a.idx[bq * a.k + sl];
+                    if (id >= 0) {
+                        if (id < a.N) { ok = 1; row = b * a.N + id; }
+                        else if (lane == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
+                    }
+                } else {
+                    const int64_t p = t - nw + 1 + (sl - a.k);
+                    const int64_t slot = ((p - a.swa_pos0) % a.swa_cap + a.swa_cap) % a.swa_cap;
+                    ok = 1;
+                    from_window = true;
+                    row = b * a.swa_cap + slot;
                 }
-            } else if (sl < n_slots) {
-                int64_t p = t - nw + 1 + (sl - k);
-                int64_t slot = ((p - swa_pos0) % swa_cap + swa_cap) % swa_cap;
-                ref = -2;
-                from_window = true;
-                row = b * swa_cap + slot;
             }
             float v[16];
-            if (ref != -1) {
+            if (ok) {
                 if (from_window) {
-                    if (sizeof(TS) == 4) load_row16<KV_F32>(swa, row, lane, v);
-                    else load_row16<KV_BF16>(swa, row, lane, v);
+                    if (sizeof(TS) == 4) load_row16<KV_F32>(a.swa, row, lane, v);
+                    else load_row16<KV_BF16>(a.swa, row, lane, v);
                 } else {
-                    load_row16<KVK>(kv, row, lane, v);
+                    load_row16<KVK>(a.kv, row, lane, v);
                 }
             } else {
 #pragma unroll
@@ -151,34 +205,34 @@ __global__ void __launch_bounds__(ATT_THREADS) sparse_attn_simt_kernel(
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             if (lane == 0) {
-                rinv[r] = (flags & CSA2_KVNORM) ? 1.0f / sqrtf(ss / (float)ATT_C + 1e-6f) : 1.0f;
-                slot_ref[r] = ref;
+                rinv[r] = (a.flags & CSA2_KVNORM) ? 1.0f / sqrtf(ss / (float)ATT_C + 1e-6f) : 1.0f;
+                slot_ok[r] = ok;
             }
         }
         __syncthreads();
-        // ---- logits: lane j ends up holding key j's logit ----
+        // logits: lane j ends up holding key j's logit
         float z_mine = -INFINITY;
-        const int n_here = min(ATT_KC, n_slots - c0);
+        const int n_here = min(ATT_KC, s_end - c0);
         for (int j = 0; j < n_here; ++j) {
             const float* xr = xs + j * ATT_C;
             float d = 0.0f;
 #pragma unroll
             for (int i = 0; i < ATT_PER_LANE; ++i) d = fmaf(qv[i], xr[lane + 32 * i], d);
             d = warp_sum(d);
-            if (lane == j && slot_ref[j] != -1) z_mine = d * rinv[j] * inv_sqrt_c;
+            if (lane == j && slot_ok[j]) z_mine = d * rinv[j] * inv_sqrt_c;
         }
-        // ---- online softmax update ----
-        float cmax = warp_max(z_mine);
-        float m_new = fmaxf(m_run, cmax);
-        float scale = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
-        float p_mine = (z_mine == -INFINITY) ? 0.0f : expf(z_mine - m_new);
+        // online softmax update
+        const float cmax = warp_max(z_mine);
+        const float m_new = fmaxf(m_run, cmax);
+        const float scale = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
+        const float p_mine = (z_mine == -INFINITY) ? 0.0f : expf(z_mine - m_new);
         l_run = l_run * scale + warp_sum(p_mine);
         m_run = m_new;
-        float pr = p_mine * rinv[lane];
+        const float pr = p_mine * rinv[lane];
 #pragma unroll
         for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] *= scale;
         for (int j = 0; j < n_here; ++j) {
-            float pj = __shfl_sync(0xffffffffu, pr, j);
+            const float pj = __shfl_sync(0xffffffffu, pr, j);
             if (pj == 0.0f) continue;
             const float* xr = xs + j * ATT_C;
 #pragma unroll
@@ -187,86 +241,141 @@ __global__ void __launch_bounds__(ATT_THREADS) sparse_attn_simt_kernel(
         __syncthreads();
     }
     if (!head_ok) return;
-    // ---- sink, normalisation, inverse RoPE, store ----
-    float zs = sink ? sink[h] : -INFINITY;
-    float m_fin = fmaxf(m_run, zs);
-    float denom, a_scale;
-    if (m_fin == -INFINITY) {
-        denom = 0.0f;
-        a_scale = 0.0f;
-    } else {
-        float e_run = (m_run == -INFINITY) ? 0.0f : expf(m_run - m_fin);
+    if (a.n_split > 1) {
+        float* part = a.ws + ((bq * a.H + h) * (int64_t)a.n_split + split) * PART;
+        if (lane == 0) {
+            part[0] = m_run;
+            part[1] = l_run;
+        }
+#pragma unroll
+        for (int i = 0; i < ATT_PER_LANE; ++i) part[2 + lane + 32 * i] = acc[i];
+        return;
+    }
+    // single split: sink, normalisation, inverse RoPE, store
+    const float zs = a.sink ? a.sink[h] : -INFINITY;
+    const float m_fin = fmaxf(m_run, zs);
+    float denom = 0.0f, a_scale = 0.0f;
+    if (m_fin != -INFINITY) {
+        const float e_run = (m_run == -INFINITY) ? 0.0f : expf(m_run - m_fin);
         denom = l_run * e_run + ((zs == -INFINITY) ? 0.0f : expf(zs - m_fin));
         a_scale = denom > 0.0f ? e_run / denom : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] *= a_scale;
-    if (flags & CSA2_ROPE) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float x = acc[14 + i];
-            float p = __shfl_xor_sync(0xffffffffu, x, 1);
-            // rotation by -t: (x0 c + x1 s, -x0 s + x1 c)
-            acc[14 + i] = (lane & 1) ? fmaf(-p, rs[i], x * rc[i]) : fmaf(p, rs[i], x * rc[i]);
-        }
-    }
-    TO* o = out + (bq * H + h) * (int64_t)ATT_C;
+    if (a.flags & CSA2_ROPE) rope_lanes(acc, lane, cs, sn, -1.0f);
+    TO* o = reinterpret_cast<TO*>(a.out) + (bq * a.H + h) * (int64_t)ATT_C;
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
-    if (lse && lane == 0) lse[bq * H + h] = (denom > 0.0f) ? m_fin + logf(denom) : -INFINITY;
+    if (a.lse && lane == 0) a.lse[bq * a.H + h] = (denom > 0.0f) ? m_fin + logf(denom) : -INFINITY;
 }
 
+// Merge the splits of one (query, head) per warp.
+template <typename TO>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int64_t rows) {
+    __shared__ float cs_all[8][32], sn_all[8][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * 8 + warp;      // (bq, h)
+    if (r >= rows) return;
+    const int64_t bq = r / a.H;
+    const int h = (int)(r % a.H);
+    const int64_t t = a.q_pos[bq];
+    float* cs = cs_all[warp];
+    float* sn = sn_all[warp];
+    if (a.flags & CSA2_ROPE) rope_cos_sin(t, lane, a.rope_base, cs[lane], sn[lane]);
+    __syncwarp();
+    const float* part = a.ws + r * (int64_t)a.n_split * PART;
+    const float zs = a.sink ? a.sink[h] : -INFINITY;
+    float M = zs;
+    for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, part[s * PART]);
+    float acc[ATT_PER_LANE];
+#pragma unroll
+    for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = 0.0f;
+    float denom = 0.0f;
+    if (M != -INFINITY) {
+        denom = (zs == -INFINITY) ? 0.0f : expf(zs - M);
+        for (int s = 0; s < a.n_split; ++s) {
+            const float ms = part[s * PART];
+            if (ms == -INFINITY) continue;
+            const float e = expf(ms - M);
+            denom = fmaf(part[s * PART + 1], e, denom);
+#pragma unroll
+            for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e, part[s * PART + 2 + lane + 32 * i], acc[i]);
+        }
+    }
+    const float inv = denom > 0.0f ? 1.0f / denom : 0.0f;
+#pragma unroll
+    for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] *= inv;
+    if (a.flags & CSA2_ROPE) rope_lanes(acc, lane, cs, sn, -1.0f);
+    TO* o = reinterpret_cast<TO*>(a.out) + r * (int64_t)ATT_C;
+#pragma unroll
+    for (int i = 0; i < ATT_PER_LANE; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
+    if (a.lse && lane == 0) a.lse[r] = (denom > 0.0f) ? M + logf(denom) : -INFINITY;
+}
+
+constexpr size_t ATT_SMEM = (size_t)ATT_KC * ATT_C * sizeof(float) + ATT_KC * sizeof(float) + ATT_KC * sizeof(int) +
+                            64 * sizeof(float);
+
 template <typename TQ, int KVK, typename TS, typename TO>
-csa2_status launch_attn(const void* q, const void* kv, int64_t N, const int32_t* idx, int k, const void* swa,
-                        int64_t swa_cap, int64_t swa_pos0, int window, const int64_t* q_pos, const float* sink,
-                        int B, int Q, int H, float base, unsigned flags, void* out, float* lse, unsigned int* st,
-                        cudaStream_t s) {
-    auto kern = sparse_attn_simt_kernel<TQ, KVK, TS, TO>;
-    size_t sm = (size_t)ATT_KC * ATT_C * sizeof(float) + ATT_KC * sizeof(float) + ATT_KC * sizeof(int);
+csa2_status launch_attn(AttnArgs& a, int B, int Q, cudaStream_t s) {
+    auto kern = attn_split_kernel<TQ, KVK, TS, TO>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM) != cudaSuccess)
             return CSA2_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid((unsigned)(B * Q), (unsigned)((H + ATT_HG - 1) / ATT_HG));
-    kern<<<grid, ATT_THREADS, sm, s>>>((const TQ*)q, kv, N, idx, k, (const TS*)swa, swa_cap, swa_pos0, window,
-                                       q_pos, sink, Q, H, base, flags, (TO*)out, lse, st);
+    dim3 grid((unsigned)a.n_split, (unsigned)((a.H + ATT_HG - 1) / ATT_HG), (unsigned)(B * Q));
+    kern<<<grid, ATT_THREADS, ATT_SMEM, s>>>(a);
+    if (a.n_split > 1) {
+        const int64_t rows = (int64_t)B * Q * a.H;
+        attn_combine_kernel<TO><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, rows);
+    }
     return csa2_launch_status();
 }
 
 template <typename TQ, int KVK, typename TS>
-csa2_status dispatch_out(csa2_dtype out_dt, const void* q, const void* kv, int64_t N, const int32_t* idx, int k,
-                         const void* swa, int64_t cap, int64_t p0, int window, const int64_t* q_pos,
-                         const float* sink, int B, int Q, int H, float base, unsigned flags, void* out, float* lse,
-                         unsigned int* st, cudaStream_t s) {
-    if (out_dt == CSA2_F32)
-        return launch_attn<TQ, KVK, TS, float>(q, kv, N, idx, k, swa, cap, p0, window, q_pos, sink, B, Q, H, base,
-                                               flags, out, lse, st, s);
-    return launch_attn<TQ, KVK, TS, __nv_bfloat16>(q, kv, N, idx, k, swa, cap, p0, window, q_pos, sink, B, Q, H,
-                                                   base, flags, out, lse, st, s);
+csa2_status dispatch_out(csa2_dtype out_dt, AttnArgs& a, int B, int Q, cudaStream_t s) {
+    if (out_dt == CSA2_F32) return launch_attn<TQ, KVK, TS, float>(a, B, Q, s);
+    return launch_attn<TQ, KVK, TS, __nv_bfloat16>(a, B, Q, s);
 }
 
 template <typename TQ, int KVK>
-csa2_status dispatch_swa(csa2_dtype swa_dt, csa2_dtype out_dt, const void* q, const void* kv, int64_t N,
-                         const int32_t* idx, int k, const void* swa, int64_t cap, int64_t p0, int window,
-                         const int64_t* q_pos, const float* sink, int B, int Q, int H, float base, unsigned flags,
-                         void* out, float* lse, unsigned int* st, cudaStream_t s) {
-    if (swa_dt == CSA2_F32)
-        return dispatch_out<TQ, KVK, float>(out_dt, q, kv, N, idx, k, swa, cap, p0, window, q_pos, sink, B, Q, H,
-                                            base, flags, out, lse, st, s);
-    return dispatch_out<TQ, KVK, __nv_bfloat16>(out_dt, q, kv, N, idx, k, swa, cap, p0, window, q_pos, sink, B, Q,
-                                                H, base, flags, out, lse, st, s);
+csa2_status dispatch_swa(csa2_dtype swa_dt, csa2_dtype out_dt, AttnArgs& a, int B, int Q, cudaStream_t s) {
+    if (swa_dt == CSA2_F32) return dispatch_out<TQ, KVK, float>(out_dt, a, B, Q, s);
+    return dispatch_out<TQ, KVK, __nv_bfloat16>(out_dt, a, B, Q, s);
+}
+
+// Number of key splits: about two waves of CTAs, at least 32 slots per split, and
+// no more than the workspace holds.
+int choose_splits(const csa2_ctx* ctx, int64_t groups, int n_slots_max, int64_t rows_bqh, size_t ws_bytes,
+                  bool have_ws) {
+    const int64_t target = 4LL * ctx->num_sms;
+    int want = 1;
+    if (groups < target) want = (int)((target + groups - 1) / groups);
+    const int max_by_slots = (n_slots_max + ATT_KC - 1) / ATT_KC;
+    want = std::min(want, std::max(1, max_by_slots));
+    if (!have_ws || want <= 1) return 1;
+    const int64_t fit = (int64_t)(ws_bytes / ((size_t)rows_bqh * PART * sizeof(float)));
+    if (fit < 2) return 1;
+    return (int)std::min<int64_t>(want, fit);
 }
 
 }  // namespace
+
+extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
+    if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0) return 0;
+    const int64_t groups = (int64_t)B * Q * ((H + ATT_HG - 1) / ATT_HG);
+    const int splits = choose_splits(ctx, groups, k + window, (int64_t)B * Q * H, SIZE_MAX / 2, true);
+    if (splits <= 1) return 0;
+    return (size_t)B * Q * H * splits * PART * sizeof(float);
+}
 
 extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
                                         csa2_dtype kv_dt, int64_t N, const int32_t* idx, int k, const void* swa,
                                         csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0, int window,
                                         const int64_t* q_pos, const float* sink, int B, int Q, int H, int c,
                                         float rope_base, unsigned flags, void* out, csa2_dtype out_dt, float* lse,
-                                        void* stream) {
+                                        void* ws, size_t ws_bytes, void* stream) {
     if (!ctx || B < 0 || Q < 0 || N < 0 || k < 0 || k > 2048 || window < 0 || window > 1024) return CSA2_ERR_INVALID_ARG;
     if (H < 1 || H > 128) return CSA2_ERR_INVALID_ARG;
     if (c != ATT_C) return CSA2_ERR_UNSUPPORTED;
@@ -275,18 +384,41 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     if (kv_dt != CSA2_F32 && kv_dt != CSA2_BF16 && kv_dt != CSA2_FP4_E4M3x16) return CSA2_ERR_UNSUPPORTED;
     if (swa_dt != CSA2_F32 && swa_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
     if (out_dt != CSA2_F32 && out_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
-    if ((int64_t)B * Q > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
+    if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;     // one grid.z slice per query
     if (B == 0 || Q == 0) return CSA2_OK;
     if (!q || !q_pos || !out) return CSA2_ERR_INVALID_ARG;
     if (k > 0 && (!idx || !kv)) return CSA2_ERR_INVALID_ARG;
     if (window > 0 && (!swa || swa_cap < window)) return CSA2_ERR_INVALID_ARG;
     if (window == 0) swa_cap = 1;
-    if (!aligned(kv, 16) || !aligned(swa, 16) || !aligned(q, 16)) return CSA2_ERR_INVALID_ARG;
+    if (!aligned(kv, 16) || !aligned(swa, 16) || !aligned(q, 16) || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    AttnArgs a;
+    a.q = q;
+    a.kv = kv;
+    a.N = N;
+    a.idx = idx;
+    a.k = k;
+    a.swa = swa;
+    a.swa_cap = swa_cap;
+    a.swa_pos0 = swa_pos0;
+    a.window = window;
+    a.q_pos = q_pos;
+    a.sink = sink;
+    a.Q = Q;
+    a.H = H;
+    a.rope_base = rope_base;
+    a.flags = flags;
+    a.out = out;
+    a.lse = lse;
+    a.ws = reinterpret_cast<float*>(ws);
+    a.st = ctx->status;
+    const int64_t groups = (int64_t)B * Q * ((H + ATT_HG - 1) / ATT_HG);
+    const int n_slots_max = k + window;
+    a.n_split = choose_splits(ctx, groups, n_slots_max, (int64_t)B * Q * H, ws_bytes, ws != nullptr);
+    a.spl = ((n_slots_max + a.n_split - 1) / a.n_split + ATT_KC - 1) / ATT_KC * ATT_KC;
+    if (a.spl == 0) a.spl = ATT_KC;
+    a.n_split = std::max(1, (n_slots_max + a.spl - 1) / a.spl);
     cudaStream_t s = as_stream(stream);
-    unsigned int* st = ctx->status;
-#define CSA2_ATT(TQ, KVK)                                                                                   \
-    return dispatch_swa<TQ, KVK>(swa_dt, out_dt, q, kv, N, idx, k, swa, swa_cap, swa_pos0, window, q_pos, sink, \
-                                 B, Q, H, rope_base, flags, out, lse, st, s)
+#define CSA2_ATT(TQ, KVK) return dispatch_swa<TQ, KVK>(swa_dt, out_dt, a, B, Q, s)
     if (q_dt == CSA2_F32) {
         if (kv_dt == CSA2_F32) CSA2_ATT(float, KV_F32);
         if (kv_dt == CSA2_BF16) CSA2_ATT(float, KV_BF16);

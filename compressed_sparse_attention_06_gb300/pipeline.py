@@ -36,10 +36,12 @@ class DecodeBuffers:
     cand_scores: torch.Tensor
     idx: torch.Tensor
     out: torch.Tensor
+    attn_ws: torch.Tensor
 
 
 def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch.bfloat16,
-                 k: int = TOPK, block: int = POOL_BLOCK, n_keep: int = POOL_KEEP) -> DecodeBuffers:
+                 k: int = TOPK, block: int = POOL_BLOCK, n_keep: int = POOL_KEEP,
+                 window: int = 128) -> DecodeBuffers:
     nb = (N + block - 1) // block
     return DecodeBuffers(
         block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
@@ -47,6 +49,9 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
         cand_scores=torch.empty((B, Q, n_keep * block), dtype=torch.float32, device=device),
         idx=torch.empty((B, Q, k), dtype=torch.int32, device=device),
         out=torch.empty((B, Q, H, c), dtype=out_dtype, device=device),
+        attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
+                                                                       torch.device(device).index)),
+                            dtype=torch.uint8, device=device),
     )
 
 
@@ -63,7 +68,7 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     C.csa2_index_score(qI, w, kI, n_visible, pool=buf.pool, block=block, scores=buf.cand_scores)
     C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.pool, block=block, out_idx=buf.idx)
     C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
-                       out=buf.out)
+                       out=buf.out, ws=buf.attn_ws)
     return buf
 
 

@@ -218,9 +218,16 @@ csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows,
  *   sink  : [H] f32 or NULL (no sink term)
  *   out   : [B, Q, H, c] in out_dt (F32 or BF16);  lse: [B, Q, H] f32 or NULL,
  *           lse = log(sum_j e^{z_j} + e^{sink_i})
- * c == 512 (RoPE needs c >= 64 when CSA2_ROPE), 1 <= H <= 128, 0 <= k <= 2048,
- * 0 <= window <= 1024.
+ * c == 512, 1 <= H <= 128, 0 <= k <= 2048, 0 <= window <= 1024, B*Q <= 65535.
+ *
+ * Workspace: with few queries the keys of each query are split over several CTAs
+ * whose partial results go to `ws` (caller-owned device memory, 16-byte aligned)
+ * and are merged by log-sum-exp.  csa2_sparse_attn_workspace_bytes() gives the
+ * size that enables the full split; a smaller (or NULL) workspace gives fewer
+ * splits (same result, less parallelism).  Calls that share a workspace must not
+ * overlap on the GPU.
  */
+size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window);
 csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              const void* q, csa2_dtype q_dt,
                              const void* kv, csa2_dtype kv_dt, int64_t N,
@@ -229,7 +236,8 @@ csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              int64_t swa_pos0, int window,
                              const int64_t* q_pos, const float* sink,
                              int B, int Q, int H, int c, float rope_base, unsigned flags,
-                             void* out, csa2_dtype out_dt, float* lse, void* stream);
+                             void* out, csa2_dtype out_dt, float* lse,
+                             void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }
