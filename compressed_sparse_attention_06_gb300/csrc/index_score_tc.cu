@@ -74,7 +74,8 @@ struct TcArgs {
 template <int KF, int QT>
 struct Cfg {
     static constexpr int N = HEADS * QT;
-    static constexpr int STAGES = KF == KF_MX ? 6 : (QT == 1 ? 3 : 2);
+    static constexpr int STAGES = KF == KF_MX ? 6 : 2;
+    static constexpr int MIN_BLOCKS = QT == 1 ? 2 : 1;               // resident CTAs per SM we ask for
     static constexpr int STAGE_BYTES = KF == KF_MX ? MX_STAGE : BF_STAGE;
     static constexpr int B_BYTES = N * DIM * 2;                   // two K-chunks of N x 128 B
     static constexpr int A_COLS = KF == KF_MX ? 2 * 64 : 0;       // two f16 A buffers (64 cols each)
@@ -131,7 +132,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 template <int KF, int QT, bool CAND>
-__global__ void __launch_bounds__(NTHREADS, 1) index_scan_tc_kernel(const TcArgs a,
+__global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_tc_kernel(const TcArgs a,
                                                                   const __grid_constant__ CUtensorMap tmap_full,
                                                                   const __grid_constant__ CUtensorMap tmap_blk) {
     using C = Cfg<KF, QT>;
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) index_scan_tc_kernel(const TcArgs
 #pragma unroll
             for (int qi = 0; qi < QT; ++qi) {
                 uint32_t d[32];
-                float acc = 0.0f;
+                float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // four independent chains
                 const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + C::D_COL0 + j * C::N + qi * HEADS;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -399,8 +400,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) index_scan_tc_kernel(const TcArgs
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        acc = fmaf(sW[qi * HEADS + hh * 32 + i], fmaxf(__uint_as_float(d[i]), 0.0f), acc);
+                        a4[i & 3] = fmaf(sW[qi * HEADS + hh * 32 + i], fmaxf(__uint_as_float(d[i]), 0.0f), a4[i & 3]);
                 }
+                float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
                 if (KF == KF_MX) acc = ldexpf(acc, rho);
                 const bool vis = sid < V[qi] && e < n_elems;
                 sc[qi] = vis ? acc : -INFINITY;

@@ -93,3 +93,41 @@ def full_topk_step(qI, w, kI, n_visible, k: int = TOPK, scores=None, idx=None):
     sc, _ = C.csa2_index_score(qI, w, kI, n_visible, scores=scores)
     ids, _ = C.csa2_topk(sc, n_visible, k, out_idx=idx)
     return sc, ids
+
+
+@dataclass
+class PrefillBuffers:
+    scores: torch.Tensor
+    idx: torch.Tensor
+    out: torch.Tensor
+    n_visible: torch.Tensor
+    attn_ws: torch.Tensor
+
+
+def alloc_prefill(Q: int, N: int, H: int, c: int, device, q_pos: torch.Tensor, m: int,
+                  out_dtype=torch.bfloat16, k: int = TOPK, window: int = 128) -> PrefillBuffers:
+    return PrefillBuffers(
+        scores=torch.empty((1, Q, N), dtype=torch.float32, device=device),
+        idx=torch.empty((1, Q, k), dtype=torch.int32, device=device),
+        out=torch.empty((1, Q, H, c), dtype=out_dtype, device=device),
+        n_visible=visible_entries(q_pos, m),
+        attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(1, Q, H, k, window,
+                                                                       torch.device(device).index)),
+                            dtype=torch.uint8, device=device),
+    )
+
+
+def prefill_chunk_step(Ca, Cb, Za, Zb, Ba, Bb, prev_Cb, prev_Zb, kv_cache, n_ctx_entries: int, pos0: torch.Tensor,
+                       m: int, qI, w, kI, q, swa, swa_pos0: int, q_pos, sink, buf: PrefillBuffers, *,
+                       k: int = TOPK, window: int = 128, write_flags: int = C.W_NORM | C.W_ROPE):
+    """Encoder prefill chunk (Full layer): the overlapped compressor turns the chunk's
+    tokens into new cache entries (carrying the previous block's state), then every
+    query of the chunk scores all entries it can see, takes its top-k and attends
+    over them plus its window."""
+    C.csa2_compress(Ca, Za, m, cb=Cb, zb=Zb, ba=Ba, bb=Bb, prev_cb=prev_Cb, prev_zb=prev_Zb, pos0=pos0,
+                    flags=write_flags, out=kv_cache[0, n_ctx_entries:], out_seq_stride=0)
+    C.csa2_index_score(qI, w, kI, buf.n_visible, scores=buf.scores)
+    C.csa2_topk(buf.scores, buf.n_visible, k, out_idx=buf.idx)
+    C.csa2_sparse_attn(q, kv_cache, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, out=buf.out,
+                       ws=buf.attn_ws)
+    return buf
