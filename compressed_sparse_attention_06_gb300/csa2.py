@@ -27,7 +27,7 @@ EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_ctx_create", "csa2_ctx_destroy", "csa2_ctx_check",
     "csa2_ctx_test_stall_next",
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
-    "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes",
+    "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
 )
 
 
@@ -62,6 +62,8 @@ def _declare(lib):
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i]),
+        "csa2_sparse_attn_noalloc": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
+                                          _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -290,4 +292,24 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
                                  swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
                                  _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
     _check("csa2_sparse_attn", st)
+    return out, lse
+
+
+def csa2_sparse_attn_noalloc(q, kv, idx, swa, q_pos, out: torch.Tensor, sink=None, window: int = 128,
+                             swa_pos0: int = 0, kv_fmt: Optional[int] = None, rope_base: float = 10000.0,
+                             flags: int = ATTN_DEFAULT, lse: Optional[torch.Tensor] = None):
+    """csa2_sparse_attn without a workspace, for callers that may not allocate device
+    memory: the library keeps the partial results in its own fixed device array.
+    The caller passes every tensor, outputs included; nothing is allocated here."""
+    B, Q, H, c = q.shape
+    k = idx.shape[-1] if idx is not None else 0
+    N = kv.shape[1] if kv is not None else 0
+    kv_dt = (FP4_E4M3x16 if kv_fmt is None else kv_fmt) if kv is not None and kv.dtype == torch.uint8 else \
+        (_dt(kv) if kv is not None else F32)
+    swa_cap = swa.shape[1] if swa is not None else 0
+    swa_dt = _dt(swa) if swa is not None else F32
+    st = _lib().csa2_sparse_attn_noalloc(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(idx), k, _p(swa),
+                                         swa_dt, swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c,
+                                         rope_base, flags, _p(out), _dt(out), _p(lse), _stream(q))
+    _check("csa2_sparse_attn_noalloc", st)
     return out, lse

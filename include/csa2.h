@@ -239,6 +239,37 @@ csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              void* out, csa2_dtype out_dt, float* lse,
                              void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * csa2_sparse_attn_noalloc -- csa2_sparse_attn for callers that may not allocate
+ * device memory.  The paper has no counterpart: this is a deployment convenience.
+ *
+ * Hosts that manage all device memory themselves (a serving engine that reserves
+ * one arena at start-up and does not let plugins call cudaMalloc, or a loop that
+ * cannot afford an allocation's latency and implicit synchronisation) cannot pass
+ * the split-key workspace.  This entry point takes the same arguments minus the
+ * workspace and keeps the partial results in a device array compiled into the
+ * library, CSA2_NOALLOC_SCRATCH_BYTES large; every GPU that loads the library holds
+ * that array until the process exits.  It calls no allocator.
+ *   - The first call on a device looks up the array's device address (a one-time
+ *     set-up that allocates nothing); make that first call before any stream
+ *     capture.
+ *   - All calls share the array: calls whose kernels overlap on the GPU race.
+ *     Nothing in it needs to start at zero (each call rewrites what it reads).
+ *   - A call whose split would need more than CSA2_NOALLOC_SCRATCH_BYTES is rejected
+ *     with CSA2_ERR_INVALID_ARG before anything is launched.
+ * Results equal csa2_sparse_attn's with a full workspace.
+ */
+#define CSA2_NOALLOC_SCRATCH_BYTES (24u << 20)
+csa2_status csa2_sparse_attn_noalloc(csa2_ctx* ctx,
+                                     const void* q, csa2_dtype q_dt,
+                                     const void* kv, csa2_dtype kv_dt, int64_t N,
+                                     const int32_t* idx, int k,
+                                     const void* swa, csa2_dtype swa_dt, int64_t swa_cap,
+                                     int64_t swa_pos0, int window,
+                                     const int64_t* q_pos, const float* sink,
+                                     int B, int Q, int H, int c, float rope_base, unsigned flags,
+                                     void* out, csa2_dtype out_dt, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
