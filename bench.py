@@ -188,13 +188,13 @@ class FP4Decode:
     def select_and_attend(self):
         from compressed_sparse_attention_06_gb300 import csa2 as C
         b = self.buf
-        C.csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool)
+        C.csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
         C.csa2_index_score(self.qI, self.w, self.ki, self.nv, pool=b.pool, block=self.block, scores=b.cand_scores)
-        C.csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx)
+        C.csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx, ws=b.topk_ws)
         C.csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, window=self.window,
                            out=b.out, ws=b.attn_ws)
 
-    launches_per_step = 8      # write x2, scan, pool, candidate scan, top-k, attention split + combine
+    launches_per_step = 10     # write x2, scan, pool x2, candidate scan, top-k x2, attention split + combine
 
     def scan_bytes(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row

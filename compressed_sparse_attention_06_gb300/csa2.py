@@ -28,6 +28,7 @@ EXPORTS = (
     "csa2_ctx_test_stall_next",
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
+    "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
 )
 
 
@@ -57,8 +58,10 @@ def _declare(lib):
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
                                   _vp, _vp]),
-        "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
-        "csa2_block_pool": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp]),
+        "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+        "csa2_topk_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
+        "csa2_block_pool": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+        "csa2_block_pool_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i]),
@@ -233,9 +236,23 @@ def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=Non
     return scores, block_max
 
 
+def csa2_topk_workspace_bytes(rows: int, n: int, k: int, device: Optional[int] = None) -> int:
+    return int(_lib().csa2_topk_workspace_bytes(ctx(device), rows, n, k))
+
+
+def csa2_block_pool_workspace_bytes(rows: int, ld: int, n_keep: int, device: Optional[int] = None) -> int:
+    return int(_lib().csa2_block_pool_workspace_bytes(ctx(device), rows, ld, n_keep))
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
 def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores: bool = False,
-              out_idx: Optional[torch.Tensor] = None, out_score: Optional[torch.Tensor] = None):
-    """scores [..., n] -> (idx [..., k] int32 ascending, -1 padded; matching scores or None)."""
+              out_idx: Optional[torch.Tensor] = None, out_score: Optional[torch.Tensor] = None,
+              ws: Optional[torch.Tensor] = None):
+    """scores [..., n] -> (idx [..., k] int32 ascending, -1 padded; matching scores or None).
+    `ws` is the split-row workspace (allocated here when not given)."""
     n = scores.shape[-1]
     rows = scores.numel() // n if n else 0
     lead = scores.shape[:-1]
@@ -244,20 +261,25 @@ def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores:
     if want_scores and out_score is None:
         out_score = torch.empty((*lead, k), dtype=torch.float32, device=scores.device)
     n_pool = pool.shape[-1] if pool is not None else 0
+    if ws is None:
+        ws = _ws(csa2_topk_workspace_bytes(rows, n, k, scores.device.index) if rows else 0, scores.device)
     st = _lib().csa2_topk(ctx(scores.device.index), _p(scores), rows, n, n, _p(n_visible), _p(pool), n_pool, block,
-                          k, _p(out_idx), _p(out_score), _stream(scores))
+                          k, _p(out_idx), _p(out_score), _p(ws), ws.numel(), _stream(scores))
     _check("csa2_topk", st)
     return out_idx, out_score
 
 
 def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
-                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                    out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
     ld = block_max.shape[-1]
     rows = block_max.numel() // ld if ld else 0
     if out is None:
         out = torch.empty((*block_max.shape[:-1], n_keep), dtype=torch.int32, device=block_max.device)
+    if ws is None:
+        ws = _ws(csa2_block_pool_workspace_bytes(rows, ld, n_keep, block_max.device.index) if rows else 0,
+                 block_max.device)
     st = _lib().csa2_block_pool(ctx(block_max.device.index), _p(block_max), rows, ld, _p(n_visible), block, n_keep,
-                                _p(out), _stream(block_max))
+                                _p(out), _p(ws), ws.numel(), _stream(block_max))
     _check("csa2_block_pool", st)
     return out
 

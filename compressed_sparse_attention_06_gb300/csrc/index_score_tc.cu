@@ -481,11 +481,20 @@ csa2_status launch_tc(csa2_ctx* ctx, TcArgs& a, const void* kbf, cudaStream_t s)
     auto kern = index_scan_tc_kernel<KF, QT, CAND>;
     static int occ = 0;     // resident CTAs per SM for this variant
     if (occ == 0) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
             return CSA2_ERR_CUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NTHREADS, C::SMEM) != cudaSuccess || occ < 1)
+        // residency from registers, shared memory and the 512 tensor-memory columns
+        cudaFuncAttributes fa;
+        int smem_sm = 0, regs_sm = 0, dev = 0;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
             return CSA2_ERR_CUDA;
-        occ = std::min(occ, 512 / C::TMEM_COLS);
+        const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;      // allocation unit of 256 per warp
+        const int by_regs = regs_sm / (warp_regs * (NTHREADS / 32));
+        const int by_smem = smem_sm / (C::SMEM + 1024);                     // + per-CTA reserved shared memory
+        occ = std::max(1, std::min(std::min(by_regs, by_smem), 512 / C::TMEM_COLS));
     }
     CUtensorMap mfull, mblk;
     memset(&mfull, 0, sizeof(mfull));

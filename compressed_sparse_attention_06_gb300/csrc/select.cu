@@ -1,18 +1,32 @@
 // Deterministic top-k selection and the hierarchical block pool.
 //
 // Top-k (DSA-to-CSA/HCA page eq. (17)) and the pool (CSA2 page,
-// «解码器里的分层索引»; Attention-evolution page §4.4) share one kernel: a CTA per
-// row finds the exact k-th largest key by 4 passes of 8-bit radix histograms over
-// the order-preserving uint32 of each score, then writes the winners in index order
-// (one coalesced pass with block-wide scans).  Keys equal to the threshold are taken
-// lowest index first, so the order is (score desc, index asc) with no dependence on
-// thread timing.
+// «解码器里的分层索引»; Attention-evolution page §4.4) share one exact radix select:
+// every score becomes an order-preserving uint32 key, four 8-bit histogram passes
+// find the k-th largest key T, and one ordered pass emits the keys above T plus the
+// first (lowest-index) keys equal to T.  The result is the top-k in the order
+// (score desc, index asc), independent of thread timing.
+//
+// Layouts:
+//   * a row that fits (<= SEL_SMEM_CAP elements) is staged in shared memory once and
+//     every pass runs there, one CTA per row;
+//   * a long row with few rows (the 1M-context pool: 131,072 blocks per query) is
+//     split over several CTAs; each keeps its chunk's top-k (key, id) pairs in the
+//     caller's workspace, and a merge CTA per row selects the final top-k from
+//     those (the union of per-chunk top-k lists contains the row's top-k under the
+//     same total order);
+//   * without a workspace a long row falls back to one CTA reading global memory
+//     on every pass.
+// Histogram increments are aggregated per warp (__match_any_sync), since scores of
+// one row often share their top key bits.
+#include <algorithm>
+
 #include "csa2_internal.cuh"
 
 namespace {
 
 constexpr int SEL_THREADS = 1024;
-constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_SMEM_CAP = 40960;        // keys staged in shared memory (160 KB)
 
 enum SelMode { SEL_TOPK = 0, SEL_CAND = 1, SEL_POOL = 2 };
 
@@ -29,6 +43,10 @@ struct SelArgs {
     int32_t* out_idx;
     float* out_val;
     unsigned int* st;         // context status word (out-of-range rows are flagged)
+    int chunks;               // > 1: two-stage path through the workspace
+    int64_t chunk_len;
+    uint32_t* ws_key;         // [rows, chunks, k]
+    int32_t* ws_id;           // [rows, chunks, k]
 };
 
 struct ElemInfo {
@@ -46,109 +64,132 @@ __device__ __forceinline__ ElemInfo elem_info(const SelArgs& a, int64_t row, int
     if (MODE == SEL_TOPK) {
         r.valid = e < V;
     } else if (MODE == SEL_CAND) {
-        int32_t pb = a.pool[row * a.n_pool + e / a.block];
+        const int32_t pb = a.pool[row * a.n_pool + e / a.block];
         r.id = (int64_t)pb * a.block + e % a.block;
         r.valid = pb >= 0 && r.id < V;
     } else {
-        // blocks 0 .. nb-1 are visible; the newest (nb-1) is added separately
-        const int64_t nb = (V + a.block - 1) / a.block;
-        r.valid = e < nb - 1;
+        r.valid = e < n_elems - 1;          // the newest visible block is added separately
     }
     return r;
+}
+
+// Elements of a row: candidate / score count, or the visible blocks for the pool.
+template <int MODE>
+__device__ __forceinline__ int64_t row_elems(const SelArgs& a, int64_t V) {
+    if (MODE != SEL_POOL) return a.n;
+    int64_t nb = V > 0 ? (V + a.block - 1) / a.block : 0;
+    if (nb > a.ld) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
+        nb = a.ld;
+    }
+    return nb;
+}
+
+// Key of a valid score: order-preserving, never 0 (0 marks "not a candidate"; only an
+// all-ones NaN would map to 0 and NaN scores are outside the contract).
+template <int MODE>
+__device__ __forceinline__ uint32_t key_of(const SelArgs& a, int64_t row, int64_t e, int64_t V, int64_t n_elems) {
+    ElemInfo inf = elem_info<MODE>(a, row, e, V, n_elems);
+    return inf.valid ? order_key(a.vals[row * a.ld + e]) : 0u;
+}
+
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active) {
+    const uint32_t d = active ? digit : 256u;
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (active && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
 }
 
 // Block-wide exclusive scan of a 0/1 flag; returns the prefix, writes the total.
 __device__ __forceinline__ int block_excl_scan(bool flag, int* warp_tot, int& total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    unsigned bal = __ballot_sync(0xffffffffu, flag);
-    int in_warp = __popc(bal & ((1u << lane) - 1u));
+    const unsigned bal = __ballot_sync(0xffffffffu, flag);
+    const int in_warp = __popc(bal & ((1u << lane) - 1u));
     if (lane == 0) warp_tot[wid] = __popc(bal);
     __syncthreads();
     if (wid == 0) {
-        int v = warp_tot[lane];
+        const int v = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
         int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int u = __shfl_up_sync(0xffffffffu, incl, o);
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += u;
         }
-        warp_tot[lane] = incl - v;              // exclusive
-        if (lane == 31) warp_tot[32] = incl;    // total
+        warp_tot[lane] = incl - v;
+        if (lane == 31) warp_tot[32] = incl;
     }
     __syncthreads();
-    int r = warp_tot[wid] + in_warp;
+    const int r = warp_tot[wid] + in_warp;
     total = warp_tot[32];
     __syncthreads();
     return r;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(SelArgs a) {
-    __shared__ unsigned int hist[256];
-    __shared__ int warp_tot[33];
-    __shared__ unsigned int s_digit;
-    __shared__ int s_remaining;
-    __shared__ unsigned int s_nvalid;
+struct SelState {
+    uint32_t T;
+    int remaining;
+    bool take_all;
+};
 
-    const int64_t row = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int64_t V = a.nv[row];
-    const float* vals = a.vals + row * a.ld;
-    int64_t n_elems = (MODE == SEL_POOL) ? (V > 0 ? ((V + a.block - 1) / a.block) : 0) : a.n;
-    if (MODE == SEL_POOL && n_elems > a.ld) {
-        // more visible blocks than the row holds: flag it and use what is there
-        if (tid == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
-        n_elems = a.ld;
-    }
-    const int k = a.k;
+struct SelShared {
+    uint32_t hist[256];
+    int warp_tot[33];
+    int digit, remaining, nvalid;
+};
 
+// Exact k-th largest key over n elements given by key_at(e) (0 = not a candidate).
+template <class KeyAt>
+__device__ SelState block_radix_select(KeyAt key_at, int64_t n, int k, SelShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    SelState r;
+    r.take_all = false;
+    r.T = 0xFFFFFFFFu;
+    r.remaining = 0;
+    if (k <= 0) return r;
     uint32_t prefix = 0, pmask = 0;
     int remaining = k;
-    bool take_all = false;
-    for (int pass = 0; pass < 4 && k > 0; ++pass) {
+    for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
-        if (tid == 0) s_nvalid = 0;
+        for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
+        if (tid == 0) sh.nvalid = 0;
         __syncthreads();
-        unsigned int local_valid = 0;
-        for (int64_t e = tid; e < n_elems; e += SEL_THREADS) {
-            ElemInfo inf = elem_info<MODE>(a, row, e, V, n_elems);
-            if (!inf.valid) continue;
-            ++local_valid;
-            uint32_t key = order_key(vals[e]);
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        int local_valid = 0;
+        for (int64_t base = 0; base < n; base += blockDim.x) {
+            const int64_t e = base + tid;
+            const uint32_t key = e < n ? key_at(e) : 0u;
+            local_valid += key != 0u;
+            hist_add(sh.hist, (key >> shift) & 255u, key != 0u && (key & pmask) == prefix);
         }
         if (pass == 0) {
-            local_valid = __reduce_add_sync(0xffffffffu, local_valid);
-            if ((tid & 31) == 0 && local_valid) atomicAdd(&s_nvalid, local_valid);
+            const int w = __reduce_add_sync(0xffffffffu, local_valid);
+            if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
         }
         __syncthreads();
-        if (pass == 0 && s_nvalid <= (unsigned)k) {
-            take_all = true;
-            break;
+        if (pass == 0 && sh.nvalid <= k) {
+            r.take_all = true;
+            r.T = 0;
+            return r;
         }
         if (tid < 32) {
-            const int lane = tid;
-            unsigned int loc[8];
-            unsigned int lsum = 0;
+            uint32_t loc[8];
+            uint32_t lsum = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                loc[j] = hist[255 - 8 * lane - j];
+                loc[j] = sh.hist[255 - 8 * lane - j];
                 lsum += loc[j];
             }
-            unsigned int incl = lsum;
+            uint32_t incl = lsum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                unsigned int u = __shfl_up_sync(0xffffffffu, incl, o);
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += u;
             }
-            unsigned int excl = incl - lsum;
-            if (excl < (unsigned)remaining && (unsigned)remaining <= incl) {
-                unsigned int cum = excl;
+            const uint32_t excl = incl - lsum;
+            if (excl < (uint32_t)remaining && (uint32_t)remaining <= incl) {
+                uint32_t cum = excl;
                 for (int j = 0; j < 8; ++j) {
-                    if (cum + loc[j] >= (unsigned)remaining) {
-                        s_digit = 255u - 8u * lane - j;
-                        s_remaining = remaining - (int)cum;
+                    if (cum + loc[j] >= (uint32_t)remaining) {
+                        sh.digit = 255 - 8 * lane - j;
+                        sh.remaining = remaining - (int)cum;
                         break;
                     }
                     cum += loc[j];
@@ -156,62 +197,191 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(SelArgs a) {
             }
         }
         __syncthreads();
-        prefix |= s_digit << shift;
+        prefix |= (uint32_t)sh.digit << shift;
         pmask |= 255u << shift;
-        remaining = s_remaining;
+        remaining = sh.remaining;
         __syncthreads();
     }
-    const uint32_t T = prefix;
+    r.T = prefix;
+    r.remaining = remaining;
+    return r;
+}
 
-    // ordered compaction: winners are keys > T, plus the first `remaining` keys == T
+// Emit the winners in element order: keys > T, then the first `remaining` keys == T.
+template <class KeyAt, class Emit>
+__device__ int block_ordered_emit(KeyAt key_at, int64_t n, const SelState& r, int k, SelShared& sh, Emit emit) {
     int eq_run = 0, out_run = 0;
-    for (int64_t base = 0; base < n_elems && out_run < k; base += SEL_THREADS) {
-        const int64_t e = base + tid;
-        ElemInfo inf = elem_info<MODE>(a, row, e, V, n_elems);
-        float v = inf.valid ? vals[e] : 0.0f;
-        uint32_t key = inf.valid ? order_key(v) : 0u;
-        bool gt, eq;
-        if (take_all) {
-            gt = inf.valid;
-            eq = false;
-        } else {
-            gt = inf.valid && key > T;
-            eq = inf.valid && key == T;
-        }
+    for (int64_t base = 0; base < n && out_run < k; base += blockDim.x) {
+        const int64_t e = base + threadIdx.x;
+        const uint32_t key = e < n ? key_at(e) : 0u;
+        const bool valid = key != 0u;
+        const bool gt = r.take_all ? valid : (valid && key > r.T);
+        const bool eq = !r.take_all && valid && key == r.T;
         int eq_tot;
-        int eq_rank = block_excl_scan(eq, warp_tot, eq_tot) + eq_run;
-        bool sel = gt || (eq && eq_rank < remaining);
+        const int eq_rank = block_excl_scan(eq, sh.warp_tot, eq_tot) + eq_run;
+        const bool sel = gt || (eq && eq_rank < r.remaining);
         int sel_tot;
-        int pos = block_excl_scan(sel, warp_tot, sel_tot) + out_run;
-        if (sel && pos < k) {
-            a.out_idx[row * a.out_len + pos] = (int32_t)inf.id;
-            if (a.out_val) a.out_val[row * a.out_len + pos] = v;
-        }
+        const int pos = block_excl_scan(sel, sh.warp_tot, sel_tot) + out_run;
+        if (sel && pos < k) emit(e, pos, key);
         eq_run += eq_tot;
         out_run += sel_tot;
     }
-    if (out_run > k) out_run = k;
-    int filled = out_run;
+    return min(out_run, k);
+}
+
+template <int MODE>
+__device__ void finish_row(const SelArgs& a, int64_t row, int filled, int64_t n_elems) {
     if (MODE == SEL_POOL && n_elems > 0) {
-        // the newest visible block is always kept; it is the largest id
-        if (tid == 0) a.out_idx[row * a.out_len + filled] = (int32_t)(n_elems - 1);
+        if (threadIdx.x == 0) a.out_idx[row * a.out_len + filled] = (int32_t)(n_elems - 1);
         ++filled;
     }
-    for (int i = filled + tid; i < a.out_len; i += SEL_THREADS) {
+    for (int i = filled + threadIdx.x; i < a.out_len; i += blockDim.x) {
         a.out_idx[row * a.out_len + i] = -1;
         if (a.out_val) a.out_val[row * a.out_len + i] = -INFINITY;
     }
 }
 
+// Stage 1 (or the whole selection when chunks == 1): a CTA per (chunk, row).
+template <int MODE, bool SMEM>
+__global__ void __launch_bounds__(SEL_THREADS) sel_chunk_kernel(SelArgs a) {
+    extern __shared__ uint32_t skey[];
+    __shared__ SelShared sh;
+    const int64_t row = blockIdx.y;
+    const int chunk = blockIdx.x;
+    const int64_t V = a.nv[row];
+    const int64_t n_elems = row_elems<MODE>(a, V);
+    const int64_t c0 = (int64_t)chunk * a.chunk_len;
+    const int64_t c1 = min(n_elems, c0 + a.chunk_len);
+    const int64_t n = max((int64_t)0, c1 - c0);
+    if (SMEM) {
+        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) skey[i] = key_of<MODE>(a, row, c0 + i, V, n_elems);
+        __syncthreads();
+    }
+    auto key_at = [&](int64_t i) -> uint32_t { return SMEM ? skey[i] : key_of<MODE>(a, row, c0 + i, V, n_elems); };
+    const SelState r = block_radix_select(key_at, n, a.k, sh);
+    if (a.chunks > 1) {
+        const int64_t base = (row * a.chunks + chunk) * (int64_t)a.k;
+        const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
+            a.ws_key[base + pos] = key;
+            a.ws_id[base + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+        });
+        for (int i = filled + threadIdx.x; i < a.k; i += blockDim.x) a.ws_key[base + i] = 0u;
+        return;
+    }
+    const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
+        a.out_idx[row * a.out_len + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+        if (a.out_val) a.out_val[row * a.out_len + pos] = a.vals[row * a.ld + c0 + i];
+    });
+    finish_row<MODE>(a, row, filled, n_elems);
+}
+
+// Stage 2: a CTA per row selects the top-k of its chunks' winners (in chunk order,
+// which is index order).
+template <int MODE>
+__global__ void __launch_bounds__(SEL_THREADS) sel_merge_kernel(SelArgs a) {
+    extern __shared__ uint32_t skey[];
+    __shared__ SelShared sh;
+    const int64_t row = blockIdx.x;
+    const int64_t V = a.nv[row];
+    const int64_t n_elems = row_elems<MODE>(a, V);
+    const int64_t n = (int64_t)a.chunks * a.k;
+    const int64_t base = row * n;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) skey[i] = a.ws_key[base + i];
+    __syncthreads();
+    auto key_at = [&](int64_t i) -> uint32_t { return skey[i]; };
+    const SelState r = block_radix_select(key_at, n, a.k, sh);
+    const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
+        a.out_idx[row * a.out_len + pos] = a.ws_id[base + i];
+        if (a.out_val) a.out_val[row * a.out_len + pos] = key_to_float(key);
+    });
+    finish_row<MODE>(a, row, filled, n_elems);
+}
+
+// Chunking: enough CTAs for the GPU when rows are few, each chunk holding at least 4k
+// elements, chunks that fit shared memory, and a merge that fits shared memory.
+void choose_chunks(const csa2_ctx* ctx, int64_t rows, int64_t n_max, int k, size_t ws_bytes, bool have_ws,
+                   int& chunks, int64_t& chunk_len, bool& smem) {
+    int64_t need = (n_max + SEL_SMEM_CAP - 1) / SEL_SMEM_CAP;
+    int64_t want = std::max<int64_t>(need, std::min<int64_t>((2LL * ctx->num_sms + rows - 1) / rows,
+                                                             n_max / std::max(1, 4 * k)));
+    want = std::max<int64_t>(want, 1);
+    const int64_t merge_cap = k > 0 ? SEL_SMEM_CAP / k : 1;
+    want = std::min<int64_t>(want, merge_cap);
+    const size_t per_chunk = (size_t)rows * k * (sizeof(uint32_t) + sizeof(int32_t));
+    if (want > 1 && have_ws && ws_bytes / std::max<size_t>(per_chunk, 1) >= (size_t)want &&
+        (n_max + want - 1) / want <= SEL_SMEM_CAP) {
+        chunks = (int)want;
+        chunk_len = (n_max + want - 1) / want;
+        smem = true;
+        return;
+    }
+    chunks = 1;
+    chunk_len = std::max<int64_t>(n_max, 1);
+    smem = n_max <= SEL_SMEM_CAP;
+}
+
+template <int MODE>
+csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, void* ws, size_t ws_bytes,
+                       cudaStream_t s) {
+    bool smem = false;
+    choose_chunks(ctx, rows, n_max, a.k, ws_bytes, ws != nullptr, a.chunks, a.chunk_len, smem);
+    if (a.chunks > 1) {
+        a.ws_key = reinterpret_cast<uint32_t*>(ws);
+        a.ws_id = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) +
+                                             (size_t)rows * a.chunks * a.k * sizeof(uint32_t));
+    } else {
+        a.ws_key = nullptr;
+        a.ws_id = nullptr;
+    }
+    static bool attr = false;
+    if (!attr) {
+        const int bytes = SEL_SMEM_CAP * (int)sizeof(uint32_t);
+        if (cudaFuncSetAttribute(sel_chunk_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(sel_merge_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+                cudaSuccess)
+            return CSA2_ERR_CUDA;
+        attr = true;
+    }
+    dim3 grid((unsigned)a.chunks, (unsigned)rows);
+    if (smem)
+        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, a.chunk_len * sizeof(uint32_t), s>>>(a);
+    else
+        sel_chunk_kernel<MODE, false><<<grid, SEL_THREADS, 0, s>>>(a);
+    if (a.chunks > 1)
+        sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS, (size_t)a.chunks * a.k * sizeof(uint32_t), s>>>(a);
+    return csa2_launch_status();
+}
+
+size_t select_ws_bytes(csa2_ctx* ctx, int64_t rows, int64_t n_max, int k) {
+    int chunks = 1;
+    int64_t len = 0;
+    bool smem = false;
+    choose_chunks(ctx, rows, n_max, k, SIZE_MAX / 4, true, chunks, len, smem);
+    if (chunks <= 1) return 0;
+    return (size_t)rows * chunks * k * (sizeof(uint32_t) + sizeof(int32_t));
+}
+
 }  // namespace
+
+extern "C" size_t csa2_topk_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t n, int k) {
+    if (!ctx || rows <= 0 || n <= 0 || k < 1 || rows > 65535) return 0;
+    return select_ws_bytes(ctx, rows, n, k);
+}
+
+extern "C" size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, int n_keep) {
+    if (!ctx || rows <= 0 || ld <= 0 || n_keep < 2 || rows > 65535) return 0;
+    return select_ws_bytes(ctx, rows, ld, n_keep - 1);
+}
 
 extern "C" csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t rows, int64_t n, int64_t ld,
                                  const int64_t* n_visible, const int32_t* pool_blocks, int n_pool, int block,
-                                 int k, int32_t* out_idx, float* out_score, void* stream) {
+                                 int k, int32_t* out_idx, float* out_score, void* ws, size_t ws_bytes,
+                                 void* stream) {
     if (!ctx || rows < 0 || n < 0 || k < 1 || k > 4096) return CSA2_ERR_INVALID_ARG;
     if (rows == 0) return CSA2_OK;
-    if (rows > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
-    if (!scores || !n_visible || !out_idx) return CSA2_ERR_INVALID_ARG;
+    if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (!scores || !n_visible || !out_idx || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
     SelArgs a;
     a.vals = scores;
     a.ld = ld;
@@ -229,22 +399,20 @@ extern "C" csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t row
         if (block < 1 || n_pool < 0) return CSA2_ERR_INVALID_ARG;
         a.n = (int64_t)n_pool * block;
         if (ld < a.n) return CSA2_ERR_INVALID_ARG;
-        select_kernel<SEL_CAND><<<(unsigned)rows, SEL_THREADS, 0, s>>>(a);
-    } else {
-        if (ld < n) return CSA2_ERR_INVALID_ARG;
-        a.n = n;
-        select_kernel<SEL_TOPK><<<(unsigned)rows, SEL_THREADS, 0, s>>>(a);
+        return run_select<SEL_CAND>(ctx, a, rows, a.n, ws, ws_bytes, s);
     }
-    return csa2_launch_status();
+    if (ld < n) return CSA2_ERR_INVALID_ARG;
+    a.n = n;
+    return run_select<SEL_TOPK>(ctx, a, rows, n, ws, ws_bytes, s);
 }
 
 extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
                                        const int64_t* n_visible, int block, int n_keep, int32_t* out_blocks,
-                                       void* stream) {
+                                       void* ws, size_t ws_bytes, void* stream) {
     if (!ctx || rows < 0 || ld < 0 || block < 1 || n_keep < 1 || n_keep > 4096) return CSA2_ERR_INVALID_ARG;
     if (rows == 0) return CSA2_OK;
-    if (rows > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
-    if (!block_max || !n_visible || !out_blocks) return CSA2_ERR_INVALID_ARG;
+    if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (!block_max || !n_visible || !out_blocks || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
     SelArgs a;
     a.vals = block_max;
     a.n = ld;
@@ -258,6 +426,5 @@ extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, in
     a.out_idx = out_blocks;
     a.out_val = nullptr;
     a.st = ctx->status;
-    select_kernel<SEL_POOL><<<(unsigned)rows, SEL_THREADS, 0, as_stream(stream)>>>(a);
-    return csa2_launch_status();
+    return run_select<SEL_POOL>(ctx, a, rows, ld, ws, ws_bytes, as_stream(stream));
 }

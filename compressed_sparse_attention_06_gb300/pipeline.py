@@ -37,6 +37,8 @@ class DecodeBuffers:
     idx: torch.Tensor
     out: torch.Tensor
     attn_ws: torch.Tensor
+    pool_ws: torch.Tensor
+    topk_ws: torch.Tensor
 
 
 def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch.bfloat16,
@@ -52,6 +54,8 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
         attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
                                                                        torch.device(device).index)),
                             dtype=torch.uint8, device=device),
+        pool_ws=C._ws(C.csa2_block_pool_workspace_bytes(B * Q, nb, n_keep, torch.device(device).index), device),
+        topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_keep * block, k, torch.device(device).index), device),
     )
 
 
@@ -64,9 +68,9 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     attend over the selected entries plus the window."""
     C.csa2_index_score(qI, w, kI, n_visible, block=block, want_scores=False, want_block_max=True,
                        block_max=buf.block_max)
-    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool)
+    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws)
     C.csa2_index_score(qI, w, kI, n_visible, pool=buf.pool, block=block, scores=buf.cand_scores)
-    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.pool, block=block, out_idx=buf.idx)
+    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.pool, block=block, out_idx=buf.idx, ws=buf.topk_ws)
     C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
                        out=buf.out, ws=buf.attn_ws)
     return buf
@@ -102,6 +106,7 @@ class PrefillBuffers:
     out: torch.Tensor
     n_visible: torch.Tensor
     attn_ws: torch.Tensor
+    topk_ws: torch.Tensor
 
 
 def alloc_prefill(Q: int, N: int, H: int, c: int, device, q_pos: torch.Tensor, m: int,
@@ -114,6 +119,7 @@ def alloc_prefill(Q: int, N: int, H: int, c: int, device, q_pos: torch.Tensor, m
         attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(1, Q, H, k, window,
                                                                        torch.device(device).index)),
                             dtype=torch.uint8, device=device),
+        topk_ws=C._ws(C.csa2_topk_workspace_bytes(Q, N, k, torch.device(device).index), device),
     )
 
 
@@ -127,7 +133,7 @@ def prefill_chunk_step(Ca, Cb, Za, Zb, Ba, Bb, prev_Cb, prev_Zb, kv_cache, n_ctx
     C.csa2_compress(Ca, Za, m, cb=Cb, zb=Zb, ba=Ba, bb=Bb, prev_cb=prev_Cb, prev_zb=prev_Zb, pos0=pos0,
                     flags=write_flags, out=kv_cache[0, n_ctx_entries:], out_seq_stride=0)
     C.csa2_index_score(qI, w, kI, buf.n_visible, scores=buf.scores)
-    C.csa2_topk(buf.scores, buf.n_visible, k, out_idx=buf.idx)
+    C.csa2_topk(buf.scores, buf.n_visible, k, out_idx=buf.idx, ws=buf.topk_ws)
     C.csa2_sparse_attn(q, kv_cache, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, out=buf.out,
                        ws=buf.attn_ws)
     return buf

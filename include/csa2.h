@@ -181,7 +181,14 @@ csa2_status csa2_index_score(csa2_ctx* ctx,
  */
 csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t rows, int64_t n, int64_t ld,
                       const int64_t* n_visible, const int32_t* pool_blocks, int n_pool,
-                      int block, int k, int32_t* out_idx, float* out_score, void* stream);
+                      int block, int k, int32_t* out_idx, float* out_score,
+                      void* ws, size_t ws_bytes, void* stream);
+/* Workspace of the selections (csa2_topk, csa2_block_pool): when rows are few and
+   long, each row is split over several CTAs that keep their chunk's top-k in `ws`
+   (caller-owned device memory, 16-byte aligned) for an exact merge.  The
+   *_workspace_bytes functions give the size that enables it; with a smaller or NULL
+   workspace a row is handled by one CTA (same result, slower).  rows <= 65535. */
+size_t csa2_topk_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t n, int k);
 
 /*
  * csa2_block_pool -- candidate pool of the hierarchical sparse indexer (CSA2 page,
@@ -196,7 +203,8 @@ csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t rows, int64_t 
  */
 csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
                             const int64_t* n_visible, int block, int n_keep,
-                            int32_t* out_blocks, void* stream);
+                            int32_t* out_blocks, void* ws, size_t ws_bytes, void* stream);
+size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, int n_keep);
 
 /*
  * csa2_sparse_attn -- shared-KV MQA over the selected compressed entries plus the

@@ -353,3 +353,23 @@ def test_out_of_range_index_is_flagged_not_faulted():
         C.csa2_ctx_check()
     assert e.value.status == C.ERR_DEVICE
     C.csa2_ctx_check()   # cleared
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_selection_without_workspace_matches(ties):
+    """Long rows with no workspace take the one-CTA-per-row path through global
+    memory; the result is the same exact selection."""
+    tiny = torch.empty(16, dtype=torch.uint8, device=DEV)
+    bm = _score_rows(2, 131072, 171, ties)
+    nv = torch.tensor([1048575, 700001], dtype=torch.int64, device=DEV)
+    pool = to_np(C.csa2_block_pool(bm, nv, 8, 2048, ws=tiny))
+    bmn = bm.double().cpu().numpy()
+    for r in range(2):
+        Vr = int(nv[r])
+        np.testing.assert_array_equal(pool[r], O.block_pool(bmn[r][: (Vr + 7) // 8], Vr, 8, 2048))
+    s = _score_rows(3, 70001, 172, ties)
+    nv = torch.tensor([70001, 45000, 100], dtype=torch.int64, device=DEV)
+    idx, _ = C.csa2_topk(s, nv, 512, ws=tiny)
+    sn = s.double().cpu().numpy()
+    for r in range(3):
+        np.testing.assert_array_equal(to_np(idx)[r], O.topk(sn[r], int(nv[r]), 512))
