@@ -96,7 +96,7 @@ struct AttnArgs {
     const int64_t* q_pos;
     const float* sink;
     int Q, H;
-    float rope_base;
+    RopeTable rope;
     unsigned flags;
     void* out;
     float* lse;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
     const int64_t t = a.q_pos[bq];
     const float inv_sqrt_c = 1.0f / sqrtf((float)ATT_C);
     const TQ* q = reinterpret_cast<const TQ*>(a.q);
-    if (threadIdx.x < 32) rope_cos_sin(t, threadIdx.x, a.rope_base, cs[threadIdx.x], sn[threadIdx.x]);
+    if (threadIdx.x < 32) rope_cos_sin(a.rope, t, threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
     __syncthreads();
 
     float qv[ATT_PER_LANE], acc[ATT_PER_LANE];
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int
     const int64_t t = a.q_pos[bq];
     float* cs = cs_all[warp];
     float* sn = sn_all[warp];
-    if (a.flags & CSA2_ROPE) rope_cos_sin(t, lane, a.rope_base, cs[lane], sn[lane]);
+    if (a.flags & CSA2_ROPE) rope_cos_sin(a.rope, t, lane, cs[lane], sn[lane]);
     __syncwarp();
     const float* part = a.ws + r * (int64_t)a.n_split * PART;
     const float zs = a.sink ? a.sink[h] : -INFINITY;
@@ -405,7 +405,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     a.sink = sink;
     a.Q = Q;
     a.H = H;
-    a.rope_base = rope_base;
+    a.rope = make_rope_table(rope_base);
     a.flags = flags;
     a.out = out;
     a.lse = lse;

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
     const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
     const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
-    const int64_t* __restrict__ pos0_arr, float rope_base, unsigned flags, void* __restrict__ out,
+    const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
     int64_t out_seq_stride) {
     const int64_t i = blockIdx.x;            // entry within the stream
     const int64_t bseq = blockIdx.y;         // stream (sequence)
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
         for (int p = 0; p < 2; ++p) {
             int j = (ch + 2 * p - (c - 64)) >> 1;
             float cs, sn;
-            rope_cos_sin(pos, j, rope_base, cs, sn);
+            rope_cos_sin(rope, pos, j, cs, sn);
             float x0 = y[2 * p], x1 = y[2 * p + 1];
             y[2 * p] = x0 * cs - x1 * sn;
             y[2 * p + 1] = x0 * sn + x1 * cs;
@@ -187,6 +187,7 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
                             int64_t n_tokens, int c, int m, const int64_t* pos0, float base, unsigned flags,
                             void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
     dim3 grid((unsigned)(n_tokens / m), (unsigned)B), block(c / 4);
+    const RopeTable rope = make_rope_table(base);
     const T* a = (const T*)ca;
     const T* z = (const T*)za;
     const T* b = (const T*)cb;
@@ -194,13 +195,13 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
     const T* p1 = (const T*)pcb;
     const T* p2 = (const T*)pzb;
     if (out_dt == CSA2_F32)
-        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
                                                             flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
                                                              flags, out, oss);
     else
-        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, base,
+        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
                                                             flags, out, oss);
     return csa2_launch_status();
 }

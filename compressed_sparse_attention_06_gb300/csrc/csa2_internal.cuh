@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "csa2.h"
@@ -67,15 +68,26 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
     return __uint_as_float(b);
 }
 
-// cos/sin of pos * theta_j with theta_j = base^(-2j/64): angle in double, reduced
-// modulo 2 pi, then rounded to float.
-__device__ __forceinline__ void rope_cos_sin(int64_t pos, int j, float base, float& c, float& s) {
-    double theta = pow((double)base, -2.0 * (double)j / 64.0);
-    double ang = fmod((double)pos * theta, 6.283185307179586);
-    double sd, cd;
-    sincos(ang, &sd, &cd);
-    c = (float)cd;
-    s = (float)sd;
+// RoPE angles.  theta_j = base^(-2j/64) for the 32 pairs of the last 64 dims; the
+// table holds theta_j / (2 pi) in double, computed once on the host.  On the device
+// the angle pos * theta_j is reduced exactly to a fractional turn in double (one
+// multiply and a floor: (double)pos is exact and the subtraction is exact), and cos
+// and sin of that turn are evaluated in float.  Double-precision transcendental
+// calls are avoided: their throughput on this part is very low.
+struct RopeTable {
+    double turns[32];
+};
+
+static inline RopeTable make_rope_table(float base) {
+    RopeTable t;
+    for (int j = 0; j < 32; ++j) t.turns[j] = pow((double)base, -2.0 * (double)j / 64.0) / 6.283185307179586;
+    return t;
+}
+
+__device__ __forceinline__ void rope_cos_sin(const RopeTable& rt, int64_t pos, int j, float& c, float& s) {
+    double u = (double)pos * rt.turns[j];
+    u -= floor(u);
+    sincospif(2.0f * (float)u, &s, &c);
 }
 
 // E2M1 pair from two floats: RNE, saturating to +-6, sign kept; `lo` goes to the

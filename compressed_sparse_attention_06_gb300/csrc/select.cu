@@ -208,25 +208,71 @@ __device__ SelState block_radix_select(KeyAt key_at, int64_t n, int k, SelShared
 }
 
 // Emit the winners in element order: keys > T, then the first `remaining` keys == T.
+// Each warp owns one contiguous segment: it counts its winners, one prefix over the
+// warp totals gives every warp its output offset and its rank among the ties, and
+// each warp then writes its winners in order (ballot prefix sums, two barriers).
 template <class KeyAt, class Emit>
 __device__ int block_ordered_emit(KeyAt key_at, int64_t n, const SelState& r, int k, SelShared& sh, Emit emit) {
-    int eq_run = 0, out_run = 0;
-    for (int64_t base = 0; base < n && out_run < k; base += blockDim.x) {
-        const int64_t e = base + threadIdx.x;
-        const uint32_t key = e < n ? key_at(e) : 0u;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    const int64_t seg = ((n + nw - 1) / nw + 31) / 32 * 32;
+    const int64_t s0 = (int64_t)wid * seg, s1 = min(n, s0 + seg);
+    int cnt_gt = 0, cnt_eq = 0;
+    for (int64_t base = s0; base < s1; base += 32) {
+        const int64_t e = base + lane;
+        const uint32_t key = e < s1 ? key_at(e) : 0u;
         const bool valid = key != 0u;
         const bool gt = r.take_all ? valid : (valid && key > r.T);
         const bool eq = !r.take_all && valid && key == r.T;
-        int eq_tot;
-        const int eq_rank = block_excl_scan(eq, sh.warp_tot, eq_tot) + eq_run;
-        const bool sel = gt || (eq && eq_rank < r.remaining);
-        int sel_tot;
-        const int pos = block_excl_scan(sel, sh.warp_tot, sel_tot) + out_run;
-        if (sel && pos < k) emit(e, pos, key);
-        eq_run += eq_tot;
-        out_run += sel_tot;
+        cnt_gt += __popc(__ballot_sync(0xffffffffu, gt));
+        cnt_eq += __popc(__ballot_sync(0xffffffffu, eq));
     }
-    return min(out_run, k);
+    int* wgt = sh.warp_tot;            // [32] gt counts, then exclusive prefixes
+    __shared__ int weq[32];
+    if (lane == 0) {
+        wgt[wid] = cnt_gt;
+        weq[wid] = cnt_eq;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        const int g = lane < nw ? wgt[lane] : 0, q = lane < nw ? weq[lane] : 0;
+        int ig = g, iq = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ug = __shfl_up_sync(0xffffffffu, ig, o), uq = __shfl_up_sync(0xffffffffu, iq, o);
+            if (lane >= o) {
+                ig += ug;
+                iq += uq;
+            }
+        }
+        if (lane < nw) {
+            wgt[lane] = ig - g;        // gt before this warp
+            weq[lane] = iq - q;        // ties before this warp
+        }
+        if (lane == 31) sh.warp_tot[32] = ig + min(iq, r.remaining);
+    }
+    __syncthreads();
+    const int gt_before = wgt[wid], eq_before = weq[wid];
+    int run_gt = 0, run_eq = 0;
+    for (int64_t base = s0; base < s1; base += 32) {
+        const int64_t e = base + lane;
+        const uint32_t key = e < s1 ? key_at(e) : 0u;
+        const bool valid = key != 0u;
+        const bool gt = r.take_all ? valid : (valid && key > r.T);
+        const bool eq = !r.take_all && valid && key == r.T;
+        const unsigned bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+        const int eq_rank = eq_before + run_eq + __popc(be & lt);
+        const bool tie_in = eq && eq_rank < r.remaining;
+        const int sel_eq_before = min(eq_before + run_eq, r.remaining);
+        const unsigned bs = __ballot_sync(0xffffffffu, tie_in);
+        const int pos = gt_before + run_gt + sel_eq_before + __popc(bg & lt) + __popc(bs & lt);
+        if ((gt || tie_in) && pos < k) emit(e, pos, key);
+        run_gt += __popc(bg);
+        run_eq += __popc(be);
+    }
+    const int total = sh.warp_tot[32];
+    __syncthreads();
+    return min(total, k);
 }
 
 template <int MODE>

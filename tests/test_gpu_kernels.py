@@ -373,3 +373,17 @@ def test_selection_without_workspace_matches(ties):
     sn = s.double().cpu().numpy()
     for r in range(3):
         np.testing.assert_array_equal(to_np(idx)[r], O.topk(sn[r], int(nv[r]), 512))
+
+
+@pytest.mark.parametrize("pos", [0, 1, 4095, 131072, (1 << 20) - 1, (1 << 31) - 7])
+def test_rope_angles_at_large_positions(pos):
+    """The write epilogue's RoPE (m = 1: the entry is its token, rotated at its
+    position) against the oracle's f64 angles, to 2e-6 of the row scale."""
+    B = 4
+    C_ = W.normal_tensor((B, 1, 512), 181, 1, torch.float32, DEV)
+    Z_ = W.normal_tensor((B, 1, 512), 181, 2, torch.float32, DEV)
+    pos0 = torch.tensor([pos, pos + 1, pos // 3, 7], dtype=torch.int64, device=DEV)
+    out = C.csa2_compress(C_, Z_, 1, pos0=pos0, flags=C.W_ROPE, out_fmt="f32")
+    for b in range(B):
+        ref = O.rope(C_[b, 0].double().cpu().numpy(), int(pos0[b]))
+        np.testing.assert_allclose(to_np(out)[b, 0], ref, rtol=0, atol=2e-6 * np.abs(ref).max())
