@@ -8,19 +8,21 @@ FP4 / MXFP4 pack), full indexer scan with fused block max, block pool, candidate
 rescoring, top-512, sparse shared-KV attention.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload fp4_decode_1M|decode_full_bf16|reindex_reuse_bf16]
+                  [--workload fp4_decode_1M|decode_full_bf16|reindex_reuse_bf16|
+                              prefill_chunk_bf16|tiny_full_layer_fp32]
 
-With torchrun (N > 1) every rank runs the same per-GPU workload on its own
-sequences (weak scaling, no data-path collective); time = max over ranks.
-`--impl reference` times the CPU oracle (the only other implementation of the
-path) on a bounded sample of the same workload.
+Besides the step rate, the line carries each stage's time (timed separately with
+CUDA events after the main loop) against its own roofline.  With torchrun (N > 1)
+every rank runs the same per-GPU workload on its own sequences (weak scaling, no
+data-path collective); time = max over ranks.  `--impl reference` times the CPU
+oracle (the only other implementation of the path) on a bounded sample of the
+same workload.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -78,8 +80,16 @@ def _profile_traffic(name, src_hash):
         return None
 
 
+def _cores():
+    try:
+        import threadpoolctl
+        return max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
     Q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -87,15 +97,14 @@ class ClockSampler:
     def __init__(self, device):
         self.proc = None
         try:
-            props = torch.cuda.get_device_properties(device)
-            self.bus = getattr(props, "pci_bus_id", None)
+            self.bus = getattr(torch.cuda.get_device_properties(device), "pci_bus_id", None)
         except Exception:
             self.bus = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except Exception:
             self.proc = None
@@ -123,14 +132,59 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "window": "warm-up and timed steps"}
+
+
+def _C():
+    from compressed_sparse_attention_06_gb300 import csa2
+    return csa2
 
 
 # ----------------------------------------------------------------------------- workloads
-class FP4Decode:
-    """FP4-cache long-context decode, B sequences x N entries."""
-    name = "fp4_decode_1M"
+class Workload:
+    """A step = pre() ; main() ; post().  main() is the kernel the roofline entry
+    describes (timed with CUDA events inside every timed step); pre/post are
+    captured in CUDA graphs.  stages() lists (name, fn, bytes, flops) for the
+    separate per-stage timing."""
+    name = ""
+    main_name = ""
+    main_bound = "hbm"
     kernel_files = ("index_score_tc.cu", "index_score.cu", "sm100_ptx.cuh", "csa2_internal.cuh")
+    profile = None
+    dtype = "f16/bf16 MMA, fp32 accumulate"
+
+    def pre(self):
+        pass
+
+    def post(self):
+        pass
+
+    def stages(self):
+        return []
+
+    def launches_per_step(self):
+        return 0
+
+    # generic end-to-end: refresh e2e_in from pinned host copies, read e2e_out back
+    def e2e_inputs(self):
+        self.h_in = [(t, t.detach().cpu().pin_memory()) for t in self.e2e_in]
+        self.h_out = [(t, torch.empty(t.shape, dtype=t.dtype).pin_memory()) for t in self.e2e_out]
+        return (sum(h.numel() * h.element_size() for _, h in self.h_in),
+                sum(h.numel() * h.element_size() for _, h in self.h_out))
+
+    def e2e_copy_in(self):
+        for d, h in self.h_in:
+            d.copy_(h, non_blocking=True)
+
+    def e2e_copy_out(self):
+        for d, h in self.h_out:
+            h.copy_(d, non_blocking=True)
+
+
+class FP4Decode(Workload):
+    """FP4-cache long-context decode, B sequences x N entries (the headline)."""
+    name = "fp4_decode_1M"
+    main_name = "csa2_index_score (MXFP4 full scan, fused block max)"
     profile = "index_score_fp4_decode_1M.txt"
 
     def __init__(self, B=8, N=1 << 20, seq0=0):
@@ -144,10 +198,10 @@ class FP4Decode:
                 "indexer_dim": 128, "heads": self.H, "head_dim": 512, "topk": self.k, "window": self.window,
                 "pool": f"{self.n_keep} blocks of {self.block}",
                 "cache": "main KV FP4 E2M1+E4M3/16 (288 B/entry), indexer K MXFP4 (68 B/entry)",
-                "l2": "inputs larger than L2 (3.0 GB of caches per step)"}
+                "l2": f"inputs larger than L2 ({self.B * self.N * 356 / 1e9:.1f} GB of caches per step)"}
 
     def setup(self, dev):
-        from compressed_sparse_attention_06_gb300 import csa2 as C
+        C = _C()
         from compressed_sparse_attention_06_gb300 import pipeline as P
         from compressed_sparse_attention_06_gb300 import workloads as W
         B, N = self.B, self.N
@@ -161,8 +215,7 @@ class FP4Decode:
                                 out=self.kv[b, r0:r0 + n])
                 C.csa2_fp4_pack(W.fp4_rows("KI", self.seq0 + b, r0, n, N, dev), C.MXFP4_E8M0x32,
                                 out=self.ki[b, r0:r0 + n])
-        wl = W.fp4_decode(dev, B=B, N=N) if self.seq0 == 0 else _offset_workload(W.fp4_decode, dev, B, N,
-                                                                                self.seq0)
+        wl = W.fp4_decode(dev, B=B, N=N) if self.seq0 == 0 else _offset_workload(W.fp4_decode, dev, B, N, self.seq0)
         self.wl = wl
         self.qI, self.w, self.q, self.swa, self.sink = wl["qI"], wl["w"], wl["q"], wl["swa"], wl["sink"]
         self.C_new, self.Z_new, self.KI_new = wl["C_new"], wl["Z_new"], wl["KI_new"].reshape(B, 128)
@@ -170,67 +223,79 @@ class FP4Decode:
         self.nv = P.visible_entries(self.q_pos, 1)
         self.pos_new = self.q_pos[:, 0].clone()
         self.buf = P.alloc_decode(B, 1, N, self.H, 512, dev, out_dtype=torch.bfloat16)
+        self.swa_row = self.swa[:, self.t % 128]
+        self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new, self.KI_new]
+        self.e2e_out = [self.buf.out, self.buf.idx]
         torch.cuda.synchronize()
 
-    # the pieces of a step (all on the current stream)
-    def write_new_rows(self):
-        from compressed_sparse_attention_06_gb300 import csa2 as C
+    def e2e_inputs(self):
+        h2d, d2h = super().e2e_inputs()
+        self.h_swa = self.swa_row.detach().cpu().pin_memory()
+        return h2d + self.h_swa.numel() * self.h_swa.element_size(), d2h
+
+    def e2e_copy_in(self):
+        super().e2e_copy_in()
+        self.swa_row.copy_(self.h_swa, non_blocking=True)      # the new token's window row
+
+    # stages
+    def write(self):
+        C = _C()
         t = self.t
-        C.csa2_compress(self.C_new, self.Z_new, 1, pos0=self.pos_new, flags=C.W_ROPE,
-                        out=self.kv[:, t], out_seq_stride=self.N)
+        C.csa2_compress(self.C_new, self.Z_new, 1, pos0=self.pos_new, flags=C.W_ROPE, out=self.kv[:, t],
+                        out_seq_stride=self.N)
         C.csa2_fp4_pack(self.KI_new, C.MXFP4_E8M0x32, out=self.ki[:, t], out_ld=self.N * 68)
 
-    def scan(self):
-        from compressed_sparse_attention_06_gb300 import csa2 as C
-        C.csa2_index_score(self.qI, self.w, self.ki, self.nv, block=self.block, want_scores=False,
-                           want_block_max=True, block_max=self.buf.block_max)
+    def main(self):
+        _C().csa2_index_score(self.qI, self.w, self.ki, self.nv, block=self.block, want_scores=False,
+                              want_block_max=True, block_max=self.buf.block_max)
 
-    def select_and_attend(self):
-        from compressed_sparse_attention_06_gb300 import csa2 as C
+    def pool(self):
         b = self.buf
-        C.csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
-        C.csa2_index_score(self.qI, self.w, self.ki, self.nv, pool=b.pool, block=self.block, scores=b.cand_scores)
-        C.csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx, ws=b.topk_ws)
-        C.csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, window=self.window,
-                           out=b.out, ws=b.attn_ws)
+        _C().csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
 
-    launches_per_step = 10     # write x2, scan, pool x2, candidate scan, top-k x2, attention split + combine
+    def cand(self):
+        b = self.buf
+        _C().csa2_index_score(self.qI, self.w, self.ki, self.nv, pool=b.pool, block=self.block, scores=b.cand_scores)
 
-    def scan_bytes(self):
+    def topk(self):
+        b = self.buf
+        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx, ws=b.topk_ws)
+
+    def attn(self):
+        b = self.buf
+        _C().csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, window=self.window, out=b.out,
+                              ws=b.attn_ws)
+
+    def pre(self):
+        self.write()
+
+    def post(self):
+        self.pool(); self.cand(); self.topk(); self.attn()
+
+    def launches_per_step(self):
+        return 10     # compress, pack, scan, pool chunk+merge, candidate scan, top-k chunk+merge, attention split+combine
+
+    def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
         once, plus the queries and head weights."""
         return self.B * self.V * 68 + self.B * self.H_I * (128 * 2 + 4)
+
+    def stages(self):
+        B, H = self.B, self.H
+        attn_bytes = B * (self.k * 288 + self.window * 1024 + H * 512 * 2 * 2)
+        attn_flops = B * H * (self.k + self.window) * 512 * 4
+        return [("write new rows", self.write, B * (2 * 1024 + 256 + 288 + 68), 0),
+                ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
+                ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
+                ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128),
+                ("top-512", self.topk, B * self.n_keep * 8 * 4, 0),
+                ("sparse attention", self.attn, attn_bytes, attn_flops)]
 
     def queries(self):
         return self.B
 
     def entries(self):
         return self.B * self.V
-
-    # --- end to end through the public API with host buffers
-    def e2e_inputs(self):
-        pin = lambda t: t.detach().cpu().pin_memory()
-        self.h_in = {"qI": pin(self.qI), "w": pin(self.w), "q": pin(self.q), "C_new": pin(self.C_new),
-                     "Z_new": pin(self.Z_new), "KI_new": pin(self.KI_new),
-                     "swa_row": pin(self.swa[:, self.t % 128].contiguous())}
-        self.h_out = torch.empty(self.buf.out.shape, dtype=self.buf.out.dtype).pin_memory()
-        self.h_idx = torch.empty(self.buf.idx.shape, dtype=self.buf.idx.dtype).pin_memory()
-        self.d_swa_row = torch.empty_like(self.h_in["swa_row"], device=self.qI.device)
-        return sum(v.numel() * v.element_size() for v in self.h_in.values()), \
-            self.h_out.numel() * self.h_out.element_size() + self.h_idx.numel() * self.h_idx.element_size()
-
-    def e2e_copy_in(self):
-        self.qI.copy_(self.h_in["qI"], non_blocking=True)
-        self.w.copy_(self.h_in["w"], non_blocking=True)
-        self.q.copy_(self.h_in["q"], non_blocking=True)
-        self.C_new.copy_(self.h_in["C_new"], non_blocking=True)
-        self.Z_new.copy_(self.h_in["Z_new"], non_blocking=True)
-        self.KI_new.copy_(self.h_in["KI_new"], non_blocking=True)
-        self.swa[:, self.t % 128].copy_(self.h_in["swa_row"], non_blocking=True)
-
-    def e2e_copy_out(self):
-        self.h_out.copy_(self.buf.out, non_blocking=True)
-        self.h_idx.copy_(self.buf.idx, non_blocking=True)
 
     # --- the oracle on a bounded sample (host cores)
     def oracle_prepare(self, b=0):
@@ -241,9 +306,7 @@ class FP4Decode:
         ki = torch.cat([W.fp4_rows("KI", self.seq0 + b, r0, min(1 << 18, N - r0), N, "cpu")
                         for r0 in range(0, N, 1 << 18)]).numpy()
         self.o_ki = O.mxfp4_pack(ki)
-        wl = self.wl if hasattr(self, "wl") else None
-        if wl is None:
-            wl = W.fp4_decode("cpu", B=self.B, N=N)
+        wl = self.wl if hasattr(self, "wl") else W.fp4_decode("cpu", B=self.B, N=N)
         self.o_q = dict(qI=wl["qI"][b, 0].double().cpu().numpy(), w=wl["w"][b, 0].double().cpu().numpy(),
                         q=wl["q"][b, 0].double().cpu().numpy(), swa=wl["swa"][b].double().cpu().numpy(),
                         sink=wl["sink"].double().cpu().numpy())
@@ -270,13 +333,303 @@ class FP4Decode:
         out, lse, _ = O.sparse_attn(o["q"], kv_sel, idx, o["swa"], 0, self.t, o["sink"], self.window)
         return out
 
+    def oracle_sample_text(self, n):
+        return (f"{n} query(ies) of sequence 0 (full pipeline per query: MXFP4 dequant of all {self.V} indexer "
+                f"rows, f64 scores, block max, pool, top-512, FP4 row gather, attention); numpy f64, BLAS threads "
+                f"for the score matmul, {os.uname().machine}")
+
+
+class DecodeBF16(Workload):
+    """Decoder Full-mode decode, bf16, batch 32 x 64K, with the pool."""
+    name = "decode_full_bf16"
+    main_name = "csa2_index_score (bf16 full scan, fused block max)"
+
+    def __init__(self, B=32, N=65536, seq0=0):
+        self.B, self.N = B, N
+        self.H_I, self.H, self.k, self.window, self.block, self.n_keep = 64, 64, 512, 128, 8, 2048
+        self.t, self.V = N - 1, N - 1
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "context": self.N, "m": 1, "indexer_heads": self.H_I,
+                "heads": self.H, "topk": self.k, "window": self.window, "pool": f"{self.n_keep} blocks of 8",
+                "cache": "bf16 main KV and indexer K", "l2": "inputs larger than L2 (2.5 GB of caches)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import pipeline as P
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        wl = W.decode_full_bf16(dev, B=self.B, N=self.N)
+        self.wl = wl
+        self.kv, self.KI, self.qI, self.w, self.q = wl["kv"], wl["KI"], wl["qI"], wl["w"], wl["q"]
+        self.swa, self.sink, self.C_new, self.Z_new = wl["swa"], wl["sink"], wl["C_new"], wl["Z_new"]
+        self.q_pos = wl.q_pos.clone()
+        self.pos_new = self.q_pos[:, 0].clone()
+        self.nv = P.visible_entries(self.q_pos, 1)
+        self.buf = P.alloc_decode(self.B, 1, self.N, self.H, 512, dev)
+        self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new]
+        self.e2e_out = [self.buf.out, self.buf.idx]
+
+    def write(self):
+        C = _C()
+        C.csa2_compress(self.C_new, self.Z_new, 1, pos0=self.pos_new, flags=C.W_ROPE, out=self.kv[:, self.t],
+                        out_seq_stride=self.N)
+
+    def main(self):
+        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, want_scores=False, want_block_max=True,
+                              block_max=self.buf.block_max)
+
+    def pool(self):
+        b = self.buf
+        _C().csa2_block_pool(b.block_max, self.nv, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
+
+    def cand(self):
+        b = self.buf
+        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, pool=b.pool, scores=b.cand_scores)
+
+    def topk(self):
+        b = self.buf
+        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, out_idx=b.idx, ws=b.topk_ws)
+
+    def attn(self):
+        b = self.buf
+        _C().csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, out=b.out, ws=b.attn_ws)
+
+    def pre(self):
+        self.write()
+
+    def post(self):
+        self.pool(); self.cand(); self.topk(); self.attn()
+
+    def launches_per_step(self):
+        return 9
+
+    def main_amount(self):
+        return self.B * self.V * 256 + self.B * self.H_I * (128 * 2 + 4)
+
+    def stages(self):
+        B, H = self.B, self.H
+        return [("write new row", self.write, B * 3 * 1024, 0),
+                ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
+                ("block pool", self.pool, B * (self.V // 8) * 4, 0),
+                ("candidate scan", self.cand, B * 16384 * 256, 2 * B * 16384 * 64 * 128),
+                ("top-512", self.topk, B * 16384 * 4, 0),
+                ("sparse attention", self.attn, B * (640 * 1024 + H * 512 * 4), B * H * 640 * 512 * 4)]
+
+    def queries(self):
+        return self.B
+
+    def entries(self):
+        return self.B * self.V
+
+
+class ReindexReuse(Workload):
+    """Reindex over the pooled 16,384 candidates + 3 Reuse layers, bf16, 64 x 256K."""
+    name = "reindex_reuse_bf16"
+    main_name = "csa2_index_score (bf16 candidate scan, 16,384 pooled entries per query)"
+
+    def __init__(self, B=64, N=262144, seq0=0):
+        self.B, self.N = B, N
+        self.t, self.V = N - 1, N - 1
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "context": self.N, "m": 1, "indexer_heads": 64,
+                "heads": 64, "topk": 512, "window": 128, "pool": "2048 given blocks of 8 (16,384 candidates)",
+                "layers": "Reindex + 3 Reuse", "l2": "inputs larger than L2 (20 GB of caches)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import pipeline as P
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        C = _C()
+        wl = W.reindex_reuse_bf16(dev, B=self.B, N=self.N)
+        self.wl = wl
+        self.nv = P.visible_entries(wl.q_pos, 1)
+        self.q_pos = wl.q_pos
+        self.cand_scores = torch.empty((self.B, 1, 16384), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((self.B, 1, 512), dtype=torch.int32, device=dev)
+        self.outs = [torch.empty((self.B, 1, 64, 512), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        self.topk_ws = C._ws(C.csa2_topk_workspace_bytes(self.B, 16384, 512), dev)
+        self.attn_ws = C._ws(C.csa2_sparse_attn_workspace_bytes(self.B, 1, 64, 512, 128), dev)
+        self.e2e_in = [wl["qI"], wl["w"]] + [wl[f"q{l}"] for l in range(4)]
+        self.e2e_out = self.outs + [self.idx]
+
+    def main(self):
+        wl = self.wl
+        _C().csa2_index_score(wl["qI"], wl["w"], wl["KI"], self.nv, pool=wl["pool"], scores=self.cand_scores)
+
+    def topk(self):
+        _C().csa2_topk(self.cand_scores, self.nv, 512, pool=self.wl["pool"], out_idx=self.idx, ws=self.topk_ws)
+
+    def attn_layer(self, l):
+        wl = self.wl
+        _C().csa2_sparse_attn(wl[f"q{l}"], wl["kv"], self.idx, wl[f"swa{l}"], self.q_pos, wl["sink"],
+                              out=self.outs[l], ws=self.attn_ws)
+
+    def post(self):
+        self.topk()
+        for l in range(4):
+            self.attn_layer(l)
+
+    def launches_per_step(self):
+        return 1 + 2 + 4 * 2
+
+    def main_amount(self):
+        return self.B * 16384 * 256 + self.B * 64 * (128 * 2 + 4)
+
+    def stages(self):
+        B = self.B
+        st = [("candidate scan", self.main, self.main_amount(), 2 * B * 16384 * 64 * 128),
+              ("top-512", self.topk, B * 16384 * 4, 0)]
+        for l in range(4):
+            st.append((f"attention layer {l}", (lambda l=l: self.attn_layer(l)), B * (640 * 1024 + 64 * 512 * 4),
+                       B * 64 * 640 * 512 * 4))
+        return st
+
+    def queries(self):
+        return self.B
+
+    def entries(self):
+        return self.B * 16384
+
+
+class PrefillChunk(Workload):
+    """Encoder prefill chunk: 8192 queries on a 131,072-token context (m=4 overlap)."""
+    name = "prefill_chunk_bf16"
+    main_name = "csa2_index_score (bf16 causal scan, 4 queries per key tile)"
+    main_bound = "tensor"
+
+    def __init__(self, n_new=8192, seq0=0, N=None):
+        self.n_new = n_new
+
+    def config(self):
+        return {"workload": self.name, "batch": 1, "queries": self.n_new, "context_tokens": 131072, "m": 4,
+                "entries": self.N, "indexer_heads": 64, "heads": 64, "topk": 512, "window": 128,
+                "compressor": "overlapped, carried previous-block state",
+                "l2": "scores (1.1 GB) and queries larger than L2"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import pipeline as P
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        wl = W.prefill_chunk_bf16(dev, n_new=self.n_new)
+        self.wl = wl
+        self.N, self.Q, self.m = wl.N, wl.Q, wl.m
+        self.nce = wl.meta["n_ctx_entries"]
+        self.kv = torch.empty((1, self.N, 512), dtype=torch.bfloat16, device=dev)
+        self.kv[0, :self.nce] = wl["kv_ctx"][0]
+        self.pos0 = torch.tensor([wl.meta["pos0"]], dtype=torch.int64, device=dev)
+        self.buf = P.alloc_prefill(self.Q, self.N, 64, 512, dev, wl.q_pos, self.m)
+        self.V_sum = int(self.buf.n_visible.sum())
+        self.e2e_in = [wl["Ca"], wl["Cb"], wl["Za"], wl["Zb"], wl["qI"], wl["w"], wl["q"]]
+        self.e2e_out = [self.buf.out, self.buf.idx]
+
+    def compress(self):
+        C = _C()
+        wl = self.wl
+        C.csa2_compress(wl["Ca"], wl["Za"], self.m, cb=wl["Cb"], zb=wl["Zb"], ba=wl["Ba"], bb=wl["Bb"],
+                        prev_cb=wl["prev_Cb"], prev_zb=wl["prev_Zb"], pos0=self.pos0, flags=C.W_NORM | C.W_ROPE,
+                        out=self.kv[0, self.nce:], out_seq_stride=0)
+
+    def main(self):
+        wl = self.wl
+        _C().csa2_index_score(wl["qI"], wl["w"], wl["KI"], self.buf.n_visible, scores=self.buf.scores)
+
+    def topk(self):
+        _C().csa2_topk(self.buf.scores, self.buf.n_visible, 512, out_idx=self.buf.idx, ws=self.buf.topk_ws)
+
+    def attn(self):
+        wl = self.wl
+        _C().csa2_sparse_attn(wl["q"], self.kv, self.buf.idx, wl["swa"], wl.q_pos, wl["sink"],
+                              swa_pos0=wl.meta["swa_pos0"], out=self.buf.out, ws=self.buf.attn_ws)
+
+    def pre(self):
+        self.compress()
+
+    def post(self):
+        self.topk(); self.attn()
+
+    def launches_per_step(self):
+        return 4
+
+    def main_amount(self):
+        return 2 * self.V_sum * 64 * 128          # flops of the causal indexer contraction
+
+    def stages(self):
+        Q = self.Q
+        return [("compress (overlap, m=4)", self.compress, self.n_new * 512 * 2 * 4 + 2048 * 1024, 0),
+                ("index scan", self.main, self.N * 256 + Q * 64 * 260 + Q * self.N * 4, self.main_amount()),
+                ("top-512", self.topk, Q * self.N * 4, 0),
+                ("sparse attention", self.attn, Q * (640 * 1024 + 64 * 512 * 4), Q * 64 * 640 * 512 * 4)]
+
+    def queries(self):
+        return self.Q
+
+    def entries(self):
+        return self.V_sum
+
+
+class TinyLayer(Workload):
+    """Tiny fp32 Full layer (CUDA-core path)."""
+    name = "tiny_full_layer_fp32"
+    main_name = "csa2_index_score (fp32, CUDA cores)"
+    dtype = "fp32"
+
+    def __init__(self, seq0=0, N=None):
+        pass
+
+    def config(self):
+        return {"workload": self.name, "tokens": 4096, "m": 2, "entries": 2048, "indexer_heads": 8, "heads": 16,
+                "queries": 4, "l2": "inputs fit in L2 (correctness workload)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import pipeline as P
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        wl = W.tiny_full_layer(dev)
+        self.wl = wl
+        self.kv = torch.empty((1, 2048, 512), dtype=torch.float32, device=dev)
+        self.nv = P.visible_entries(wl.q_pos, wl.m)
+        self.scores = torch.empty((1, 4, 2048), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((1, 4, 512), dtype=torch.int32, device=dev)
+        self.out = torch.empty((1, 4, 16, 512), dtype=torch.float32, device=dev)
+        self.e2e_in = [wl["qI"], wl["w"], wl["q"]]
+        self.e2e_out = [self.out, self.idx]
+
+    def compress(self):
+        C = _C()
+        wl = self.wl
+        C.csa2_compress(wl["Ca"], wl["Za"], wl.m, ba=wl["Ba"], flags=C.W_NORM | C.W_ROPE, out=self.kv[0])
+
+    def main(self):
+        wl = self.wl
+        _C().csa2_index_score(wl["qI"], wl["w"], wl["KI"], self.nv, scores=self.scores)
+
+    def post(self):
+        wl = self.wl
+        _C().csa2_topk(self.scores, self.nv, 512, out_idx=self.idx)
+        _C().csa2_sparse_attn(wl["q"], self.kv, self.idx, wl["swa"], wl.q_pos, wl["sink"], out=self.out)
+
+    def pre(self):
+        self.compress()
+
+    def launches_per_step(self):
+        return 5
+
+    def main_amount(self):
+        return 2048 * 128 * 4 * 4
+
+    def stages(self):
+        return [("compress", self.compress, 4096 * 512 * 8 + 2048 * 2048, 0),
+                ("index scan", self.main, self.main_amount(), 0)]
+
+    def queries(self):
+        return 4
+
+    def entries(self):
+        return int(self.nv.sum())
+
 
 class _RowMap:
     """Indexable view over a dict of gathered rows (the oracle indexes kv[s])."""
 
     def __init__(self, rows):
         self.rows = rows
-        self.shape = (max(rows) + 1 if rows else 0, 512)
 
     def __getitem__(self, s):
         return self.rows[int(s)]
@@ -294,7 +647,7 @@ def _offset_workload(fn, dev, B, N, seq0):
     return wl
 
 
-WORKLOADS = {"fp4_decode_1M": FP4Decode}
+WORKLOADS = {c.name: c for c in (FP4Decode, DecodeBF16, ReindexReuse, PrefillChunk, TinyLayer)}
 
 
 def _make(args, seq0=0):
@@ -305,6 +658,28 @@ def _make(args, seq0=0):
 
 
 # ----------------------------------------------------------------------------- arms
+def _time_stages(wl, stream, reps):
+    """Each stage alone, `reps` times, CUDA events around every launch (median)."""
+    hbm, bf16, _, _ = _peaks()
+    out = {}
+    for name, fn, nbytes, flops in wl.stages():
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in evs)[reps // 2]
+        d = {"ms": ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm}
+        if flops:
+            d["TFLOP_per_s"] = flops / (ms * 1e-3) / 1e12
+            d["tensor_frac"] = d["TFLOP_per_s"] / bf16
+        out[name] = d
+    return out
+
+
 def run_ours(args):
     rank, world, local = _env_rank()
     dist = None
@@ -318,17 +693,17 @@ def run_ours(args):
         build_lib.build()
     if dist is not None:
         dist.barrier()
-    from compressed_sparse_attention_06_gb300 import csa2 as C
+    C = _C()
     C.load()
     wl = _make(args, seq0=rank * 8)
     wl.setup(dev)
     stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(dev)
+    clocks.start()
 
     # warm-up (also sets kernel attributes before any graph capture)
     for _ in range(max(1, args.warmup)):
-        wl.write_new_rows()
-        wl.scan()
-        wl.select_and_attend()
+        wl.pre(); wl.main(); wl.post()
     C.csa2_ctx_check()
     g_pre = g_post = None
     if not args.no_graph:
@@ -337,37 +712,35 @@ def run_ours(args):
         s.wait_stream(stream)
         with torch.cuda.stream(s):
             with torch.cuda.graph(g_pre, stream=s):
-                wl.write_new_rows()
+                wl.pre()
             with torch.cuda.graph(g_post, stream=s):
-                wl.select_and_attend()
+                wl.post()
         stream.wait_stream(s)
         for _ in range(2):
-            g_pre.replay(); wl.scan(); g_post.replay()
+            g_pre.replay(); wl.main(); g_post.replay()
     torch.cuda.synchronize()
 
     def step(ev0=None, ev1=None):
         if g_pre is not None:
             g_pre.replay()
         else:
-            wl.write_new_rows()
+            wl.pre()
         if ev0 is not None:
             ev0.record(stream)
-        wl.scan()
+        wl.main()
         if ev1 is not None:
             ev1.record(stream)
         if g_post is not None:
             g_post.replay()
         else:
-            wl.select_and_attend()
+            wl.post()
 
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
     t0.record(stream)
     for i in range(K):
         step(*evs[i])
@@ -378,12 +751,15 @@ def run_ours(args):
         dist.barrier()
     C.csa2_ctx_check()
     ms_total = t0.elapsed_time(t1)
-    scan_ms = sum(a.elapsed_time(b) for a, b in evs) / K
+    main_ms = sum(a.elapsed_time(b) for a, b in evs) / K
     if dist is not None:
-        tt = torch.tensor([ms_total, scan_ms], dtype=torch.float64, device=dev)
+        tt = torch.tensor([ms_total, main_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, scan_ms = float(tt[0]), float(tt[1])
+        ms_total, main_ms = float(tt[0]), float(tt[1])
     ms_step = ms_total / K
+
+    stages = _time_stages(wl, stream, max(5, K))
+    C.csa2_ctx_check()
 
     # end to end: host inputs -> device, step, result -> host, every step
     h2d, d2h = wl.e2e_inputs()
@@ -405,25 +781,33 @@ def run_ours(args):
         e_s = float(tt[0])
 
     hbm, bf16, bf16s, src = _peaks()
-    achieved = wl.scan_bytes() / (scan_ms * 1e-3) / 1e9
-    traffic = _profile_traffic(wl.profile, _kernel_hash(wl.kernel_files))
+    if wl.main_bound == "hbm":
+        achieved = wl.main_amount() / (main_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "bytes_per_launch": wl.main_amount()}
+    else:
+        achieved = wl.main_amount() / (main_ms * 1e-3) / 1e12
+        peak = bf16s if ms_step > 5.0 else bf16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "flops_per_launch": wl.main_amount()}
+    traffic = _profile_traffic(wl.profile, _kernel_hash(wl.kernel_files)) if wl.profile else None
+    roof.update({"traffic": traffic, "kernel": wl.main_name, "kernel_ms": main_ms, "peak_source": src})
     value = world * wl.queries() / (ms_step * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp32", "data": "synthetic (seeded counter-based generator)",
+        "dtype": wl.dtype, "data": "synthetic (seeded counter-based generator)",
         "config": {**wl.config(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cuda_graph": g_pre is not None},
         "entries_per_s": world * wl.entries() / (ms_step * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "kernel": "csa2_index_score (full scan, fused block max)",
-                     "kernel_ms": scan_ms, "bytes_per_launch": wl.scan_bytes(), "peak_source": src},
+        "roofline": roof,
+        "stages": stages,
         "e2e": {"value": world * wl.queries() * K / e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": wl.launches_per_step * K,
+        "gpu_launches": wl.launches_per_step() * K,
         "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and hasattr(wl, "oracle_query"):
         res["cpu_baseline"] = cpu_baseline(wl, args)
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -431,24 +815,15 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(wl, args, n_queries=None):
+def cpu_baseline(wl, args):
     """The oracle, as it stands, on a bounded sample of the same workload."""
-    import numpy as np
     wl.oracle_prepare(0)
-    n = n_queries or args.cpu_queries
+    n = args.cpu_queries
     t0 = time.perf_counter()
     for _ in range(n):
         wl.oracle_query()
     dt = time.perf_counter() - t0
-    try:
-        import threadpoolctl
-        cores = max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
-    except Exception:
-        cores = os.cpu_count() or 1
-    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} query(ies) of sequence 0 (full pipeline per query: MXFP4 dequant of all "
-                      f"{wl.V} indexer rows, f64 scores, block max, pool, top-512, FP4 row gather, attention); "
-                      f"numpy f64, BLAS threads for the score matmul, {os.uname().machine}"}
+    return {"value": n / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle", "sample": wl.oracle_sample_text(n)}
 
 
 def run_reference(args):
@@ -456,6 +831,9 @@ def run_reference(args):
     if rank != 0:
         return
     wl = _make(args)
+    if not hasattr(wl, "oracle_query"):
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle sample defined for {wl.name}"}))
+        return
     wl.oracle_prepare(0)
     for _ in range(args.warmup):
         wl.oracle_query()
@@ -464,16 +842,11 @@ def run_reference(args):
         wl.oracle_query()
     dt = time.perf_counter() - t0
     v = args.steps / dt
-    try:
-        import threadpoolctl
-        cores = max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
-    except Exception:
-        cores = os.cpu_count() or 1
     res = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
            "config": wl.config(),
-           "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "cpu_baseline": {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle",
                             "sample": "each step = one query of sequence 0 through the whole oracle pipeline"},
            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)

@@ -93,10 +93,13 @@ __device__ __forceinline__ uint32_t key_of(const SelArgs& a, int64_t row, int64_
     return inf.valid ? order_key(a.vals[row * a.ld + e]) : 0u;
 }
 
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active) {
+// Add a digit to this warp's private histogram: lanes with the same digit are
+// counted once by their lowest lane, so no two lanes touch one bin in the same
+// instruction and no other warp touches this histogram.
+__device__ __forceinline__ void hist_add(uint32_t* whist, uint32_t digit, bool active) {
     const uint32_t d = active ? digit : 256u;
     const unsigned peers = __match_any_sync(0xffffffffu, d);
-    if (active && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+    if (active && (int)(threadIdx.x & 31) == __ffs(peers) - 1) whist[d] += (uint32_t)__popc(peers);
 }
 
 // Block-wide exclusive scan of a 0/1 flag; returns the prefix, writes the total.
@@ -131,6 +134,7 @@ struct SelState {
 };
 
 struct SelShared {
+    uint32_t whist[32][256];     // one histogram per warp (scores of a row share their top bits)
     uint32_t hist[256];
     int warp_tot[33];
     int digit, remaining, nvalid;
@@ -149,19 +153,27 @@ __device__ SelState block_radix_select(KeyAt key_at, int64_t n, int k, SelShared
     int remaining = k;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
+        const int nwarps = blockDim.x >> 5;
+        for (int i = tid; i < nwarps * 256; i += blockDim.x) sh.whist[i >> 8][i & 255] = 0;
         if (tid == 0) sh.nvalid = 0;
         __syncthreads();
         int local_valid = 0;
+        uint32_t* wh = sh.whist[tid >> 5];
         for (int64_t base = 0; base < n; base += blockDim.x) {
             const int64_t e = base + tid;
             const uint32_t key = e < n ? key_at(e) : 0u;
             local_valid += key != 0u;
-            hist_add(sh.hist, (key >> shift) & 255u, key != 0u && (key & pmask) == prefix);
+            hist_add(wh, (key >> shift) & 255u, key != 0u && (key & pmask) == prefix);
         }
         if (pass == 0) {
             const int w = __reduce_add_sync(0xffffffffu, local_valid);
             if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
+        }
+        __syncthreads();
+        for (int b = tid; b < 256; b += blockDim.x) {
+            uint32_t tot = 0;
+            for (int w = 0; w < nwarps; ++w) tot += sh.whist[w][b];
+            sh.hist[b] = tot;
         }
         __syncthreads();
         if (pass == 0 && sh.nvalid <= k) {
