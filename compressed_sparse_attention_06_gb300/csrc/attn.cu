@@ -13,7 +13,9 @@
 // partial (max, sum, unnormalised output) to the caller's workspace and
 // attn_combine_kernel merges them by log-sum-exp.
 #include <algorithm>
+#include <cstring>
 
+#include "attn_tc.cuh"
 #include "csa2_internal.cuh"
 
 namespace {
@@ -26,26 +28,6 @@ constexpr int ATT_PER_LANE = ATT_C / 32;
 constexpr int PART = ATT_C + 2;      // floats per partial: max, sum, output
 
 enum KvKind { KV_F32 = 0, KV_BF16 = 1, KV_FP4 = 2 };
-
-// Eight E2M1 codes (one 32-bit word, code 2i in the low nibble of byte i) -> f32,
-// through the exact E2M1 -> f16 conversion.
-__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&o)[8]) {
-    uint32_t h[4];
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __half22float2(*reinterpret_cast<__half2*>(&h[i]));
-        o[2 * i] = f.x;
-        o[2 * i + 1] = f.y;
-    }
-}
 
 // Load 16 channels [16*lane, 16*lane+16) of a row into f32 (exact for every format).
 template <int KIND>
@@ -333,6 +315,13 @@ csa2_status launch_attn(AttnArgs& a, int B, int Q, cudaStream_t s) {
     return csa2_launch_status();
 }
 
+template <typename TO>
+csa2_status launch_combine(const AttnArgs& a, int B, int Q, cudaStream_t s) {
+    const int64_t rows = (int64_t)B * Q * a.H;
+    attn_combine_kernel<TO><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, rows);
+    return csa2_launch_status();
+}
+
 template <typename TQ, int KVK, typename TS>
 csa2_status dispatch_out(csa2_dtype out_dt, AttnArgs& a, int B, int Q, cudaStream_t s) {
     if (out_dt == CSA2_F32) return launch_attn<TQ, KVK, TS, float>(a, B, Q, s);
@@ -362,12 +351,17 @@ int choose_splits(const csa2_ctx* ctx, int64_t groups, int n_slots_max, int64_t 
 
 }  // namespace
 
-extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
+size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
     if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0) return 0;
     const int64_t groups = (int64_t)B * Q * ((H + ATT_HG - 1) / ATT_HG);
     const int splits = choose_splits(ctx, groups, k + window, (int64_t)B * Q * H, SIZE_MAX / 2, true);
     if (splits <= 1) return 0;
     return (size_t)B * Q * H * splits * PART * sizeof(float);
+}
+
+extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
+    if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0) return 0;
+    return std::max(attn_simt_ws_bytes(ctx, B, Q, H, k, window), attn_tc_ws_bytes(ctx, B, Q, H, k, window));
 }
 
 extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
@@ -391,6 +385,50 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     if (window > 0 && (!swa || swa_cap < window)) return CSA2_ERR_INVALID_ARG;
     if (window == 0) swa_cap = 1;
     if (!aligned(kv, 16) || !aligned(swa, 16) || !aligned(q, 16) || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    // tensor-core path: bf16 query and window, bf16 or FP4 rows, both RMSNorms, <= 64 heads
+    AttnTcCall tc;
+    tc.q = q;
+    tc.q_dt = q_dt;
+    tc.kv = kv;
+    tc.kv_dt = kv_dt;
+    tc.N = N;
+    tc.idx = idx;
+    tc.k = k;
+    tc.swa = swa;
+    tc.swa_dt = swa_dt;
+    tc.swa_cap = swa_cap;
+    tc.swa_pos0 = swa_pos0;
+    tc.window = window;
+    tc.q_pos = q_pos;
+    tc.sink = sink;
+    tc.B = B;
+    tc.Q = Q;
+    tc.H = H;
+    tc.rope = make_rope_table(rope_base);
+    tc.flags = flags;
+    tc.out = out;
+    tc.out_dt = out_dt;
+    tc.lse = lse;
+    if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, H, k, window)) {
+        int ns = 1;
+        const csa2_status st = attn_tc_run(ctx, tc, ws, ws_bytes, s, &ns);
+        if (st != CSA2_OK || ns <= 1) return st;
+        AttnArgs c;
+        memset(&c, 0, sizeof(c));
+        c.q_pos = q_pos;
+        c.sink = sink;
+        c.Q = Q;
+        c.H = H;
+        c.rope = tc.rope;
+        c.flags = flags;
+        c.out = out;
+        c.lse = lse;
+        c.ws = reinterpret_cast<float*>(ws);
+        c.n_split = ns;
+        c.st = ctx->status;
+        return out_dt == CSA2_F32 ? launch_combine<float>(c, B, Q, s) : launch_combine<__nv_bfloat16>(c, B, Q, s);
+    }
     AttnArgs a;
     a.q = q;
     a.kv = kv;
@@ -417,7 +455,6 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     a.spl = ((n_slots_max + a.n_split - 1) / a.n_split + ATT_KC - 1) / ATT_KC * ATT_KC;
     if (a.spl == 0) a.spl = ATT_KC;
     a.n_split = std::max(1, (n_slots_max + a.spl - 1) / a.spl);
-    cudaStream_t s = as_stream(stream);
 #define CSA2_ATT(TQ, KVK) return dispatch_swa<TQ, KVK>(swa_dt, out_dt, a, B, Q, s)
     if (q_dt == CSA2_F32) {
         if (kv_dt == CSA2_F32) CSA2_ATT(float, KV_F32);

@@ -15,6 +15,7 @@
 // start at zero: every call rewrites each partial result it later reads.
 #include <mutex>
 
+#include "attn_tc.cuh"
 #include "csa2_internal.cuh"
 
 namespace {
@@ -55,8 +56,9 @@ extern "C" csa2_status csa2_sparse_attn_noalloc(csa2_ctx* ctx, const void* q, cs
                                                 unsigned flags, void* out, csa2_dtype out_dt, float* lse,
                                                 void* stream) {
     if (!ctx) return CSA2_ERR_INVALID_ARG;
-    // The split the regular entry point would use must fit the fixed array.
-    const size_t need = csa2_sparse_attn_workspace_bytes(ctx, B, Q, H, k, window);
+    // The CUDA-core key split must fit the fixed array; the tensor-core path is taken
+    // only when its larger workspace fits as well.
+    const size_t need = attn_simt_ws_bytes(ctx, B, Q, H, k, window);
     if (need > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_INVALID_ARG;
     void* scratch = nullptr;
     csa2_status st = scratch_address(ctx->device, &scratch);

@@ -1,0 +1,801 @@
+// Shared-KV MQA over the selected entries plus the sliding window on the tcgen05
+// tensor cores (DSA-to-CSA/HCA page eqs. (18)-(19) and (27); CSA2 page «保留了 CSA
+// 的骨架»): the same RMS-normalised row is key and value for all heads, the query
+// is RMS-normalised and rotated by RoPE_t on its last 64 dims, the output is
+// rotated back by RoPE_-t, and the sink adds e^{z'_h} to the denominator only.
+//
+// Work item = (query, range of 128-slot key tiles).  Per tile, two MMAs:
+//   S^T[128 slots x 64 heads]  = X[128 x 512] . Qhat[64 x 512]^T       (K-major A, B)
+//   O^T[512 dims x 64 heads]  += X^T[512 x 128] . P'[64 x 128]^T       (MN-major A, B)
+// X is the tile of raw key rows (bf16; FP4 rows dequantised exactly into bf16),
+// gathered once into shared memory in the 128-byte-swizzled layout and read by both
+// MMAs; S and O live in tensor memory.  Each row's RMS factor r_s is applied to the
+// logits and folded into the probabilities (P' = p r_s), so X is never rescaled.
+//
+// Softmax without a running maximum.  With both RMSNorms on, |qhat| and |xhat| are
+// at most sqrt(512), so every logit qhat.xhat / sqrt(512) lies in [-22.7, 22.7].
+// p = exp(logit - 24) is therefore in (e^-47, 1]: no overflow, no underflow in f32
+// or bf16, and O accumulates across tiles without rescaling.  The denominator is the
+// f32 sum of the unrounded p.  With several key splits each writes (24, sum,
+// unnormalised O) and the log-sum-exp combine merges them.
+//
+// Precision: the normalised query and P' are rounded to bf16 for the MMA (fp32
+// accumulation); key rows are exact.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over work items):
+//   warp 0     producer: the query image (one bulk copy) and the tile's bf16 rows
+//              (TMA gather of four rows per instruction, 128-byte swizzle)
+//   warp 1     MMA issuer; owns the tensor memory (O^T: columns 0-255, S^T: 256-319)
+//   warps 2-5  softmax: one thread per slot; then the output epilogue, one thread per
+//              output dim
+//   warps 6-9  loaders: FP4 rows dequantised into the tile, zero rows for empty slots,
+//              and every row's RMS factor
+// Every wait is bounded; a wait that expires flags a timeout and the roles wind down.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "attn_tc.cuh"
+#include "sm100_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace {
+
+using namespace sm100;
+
+constexpr int TC_C = 512;
+constexpr int TC_H = 64;
+constexpr int TC_TILE = 128;
+constexpr int TC_THREADS = 320;
+constexpr float TC_SHIFT = 24.0f;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int QIMG_BYTES = TC_H * TC_C * 2;     // 64 KB: 8 chunks of 64 rows x 128 B
+constexpr int CHUNK_Q = TC_H * 128;
+constexpr int CHUNK_K = TC_TILE * 128;          // 16 KB: 128 rows x 64 dims
+constexpr int PART = TC_C + 2;
+constexpr uint32_t DS_COL = 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr long long WAIT_BUDGET = 1ll << 31;
+constexpr unsigned FULL = 0xffffffffu;
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + QIMG_BYTES;
+constexpr int OFF_P = OFF_K + 8 * CHUNK_K;
+constexpr int OFF_RINV = OFF_P + TC_TILE * 128;
+constexpr int OFF_LW = OFF_RINV + TC_TILE * 4;
+constexpr int OFF_BAR = OFF_LW + 4 * TC_H * 4;
+constexpr int N_BAR = 16;
+constexpr int OFF_TMEMPTR = OFF_BAR + N_BAR * 8;
+constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+struct TcArgs {
+    const uint8_t* qimg;          // [B*Q] query images
+    const void* kv;               // bf16 [B, N, 512] or FP4 [B, N, 288]
+    int64_t N;
+    const int32_t* idx;           // [B*Q, k]
+    int k;
+    int64_t swa_cap, swa_pos0;
+    int window;
+    const int64_t* q_pos;
+    const float* sink;
+    int Q, H;
+    RopeTable rope;
+    unsigned flags;
+    void* out;
+    float* lse;
+    float* part;                  // [B*Q, H, n_split, PART] when n_split > 1
+    int n_split, tps;             // splits per query, tiles per split
+    int64_t items;
+    unsigned int* st;
+    long long budget;
+};
+
+struct ItemInfo {
+    int64_t bq, b, t;
+    int split, nw, n_slots, t0, nt;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const TcArgs& a, int64_t item) {
+    ItemInfo r;
+    r.bq = item / a.n_split;
+    r.split = (int)(item % a.n_split);
+    r.b = r.bq / a.Q;
+    r.t = a.q_pos[r.bq];
+    r.nw = (int)max((int64_t)0, min((int64_t)a.window, r.t + 1));
+    r.n_slots = a.k + r.nw;
+    const int n_tiles = (r.n_slots + TC_TILE - 1) / TC_TILE;
+    r.t0 = r.split * a.tps;
+    r.nt = max(0, min(n_tiles, r.t0 + a.tps) - r.t0);
+    return r;
+}
+
+// Source of a key slot: kind 0 = empty, 1 = selected cache row, 2 = window row.
+struct SlotSrc {
+    int kind;
+    int64_t row;
+};
+
+__device__ __forceinline__ SlotSrc slot_source(const TcArgs& a, const ItemInfo& it, int slot, bool flag_range) {
+    SlotSrc r;
+    r.kind = 0;
+    r.row = 0;
+    if (slot >= it.n_slots) return r;
+    if (slot < a.k) {
+        const int32_t id = a.idx[it.bq * a.k + slot];
+        if (id >= 0) {
+            if (id < a.N) {
+                r.kind = 1;
+                r.row = it.b * a.N + id;
+            } else if (flag_range) {
+                csa2_flag(a.st, CSA2_DEVBIT_RANGE);
+            }
+        }
+    } else {
+        const int64_t p = it.t - it.nw + 1 + (slot - a.k);
+        r.kind = 2;
+        r.row = it.b * a.swa_cap + (((p - a.swa_pos0) % a.swa_cap) + a.swa_cap) % a.swa_cap;
+    }
+    return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& ss) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+    }
+}
+
+// One FP4 row (256 code bytes, 32 E4M3 scales) into row r of the tile as bf16
+// (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits).
+// Returns the sum of squares of the dequantised values.
+__device__ __forceinline__ float fp4_row_to_tile(const uint8_t* kv, int64_t row, uint8_t* sK, int r) {
+    const uint4* src = reinterpret_cast<const uint4*>(kv + row * fp4_row_bytes(TC_C));
+    const uint4 sa = src[16], sb = src[17];
+    const uint32_t scw[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    float ss = 0.0f;
+#pragma unroll 2
+    for (int c = 0; c < 8; ++c) {
+        const uint4 ca = src[2 * c], cb = src[2 * c + 1];
+        const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = c * 4 + (u >> 1);                  // 16-dim scale group
+            const float s = e4m3_to_f32((scw[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+            float f[8];
+            e2m1x8_to_f32(cw[u], f);
+            uint32_t pk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = f[2 * i] * s, x1 = f[2 * i + 1] * s;
+                ss = fmaf(x0, x0, ss);
+                ss = fmaf(x1, x1, ss);
+                pk[i] = pack_bf16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+    return ss;
+}
+
+// Normalised, rotated query of every (query, head) as the bf16 image of the MMA's
+// B operand: 8 chunks of [64 heads x 64 dims], 128-byte swizzled; heads >= H are 0.
+template <typename TQ>
+__global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, RopeTable rope,
+                                                         unsigned flags, uint8_t* qimg) {
+    __shared__ float cs[32], sn[32];
+    const int64_t bq = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) rope_cos_sin(rope, q_pos[bq], threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
+    __syncthreads();
+    uint8_t* img = qimg + bq * (int64_t)QIMG_BYTES;
+    for (int h = warp; h < TC_H; h += 8) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        if (h < H) {
+            const TQ* src = q + ((bq * H + h) * (int64_t)TC_C + 16 * lane);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = to_f32<TQ>(src[i]);
+        }
+        if (flags & CSA2_QNORM) {
+            float ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+            ss = warp_sum(ss);
+            const float r = 1.0f / sqrtf(ss / (float)TC_C + 1e-6f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= r;
+        }
+        if ((flags & CSA2_ROPE) && lane >= 28) {      // dims 448..511, pairs (2j, 2j+1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = 8 * (lane - 28) + i;
+                const float c = cs[j], s = sn[j], x0 = v[2 * i], x1 = v[2 * i + 1];
+                v[2 * i] = x0 * c - x1 * s;
+                v[2 * i + 1] = x1 * c + x0 * s;
+            }
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        const int u0 = 2 * lane, chunk = u0 >> 3, uc = u0 & 7;
+        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(h, uc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(h, uc + 1)) =
+            make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+}
+
+// Output of a query whose split holds no key slot: the sink alone (O = 0).
+template <typename TO>
+__device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
+    for (int h = 0; h < a.H; ++h) {
+        for (int d = d0; d < TC_C; d += 128) {
+            if (a.n_split > 1)
+                a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + 2 + d] = 0.0f;
+            else
+                reinterpret_cast<TO*>(a.out)[(it.bq * a.H + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
+        }
+    }
+    if (d0 < a.H) {
+        const int h = d0;
+        if (a.n_split > 1) {
+            float* p = a.part + ((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART;
+            p[0] = -INFINITY;
+            p[1] = 0.0f;
+        } else if (a.lse) {
+            a.lse[it.bq * a.H + h] = a.sink ? a.sink[h] : -INFINITY;
+        }
+    }
+}
+
+template <bool FP4, typename TO>
+__global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a,
+                                                                const __grid_constant__ CUtensorMap tm_kv,
+                                                                const __grid_constant__ CUtensorMap tm_swa) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem + OFF_Q;
+    uint8_t* sK = smem + OFF_K;
+    uint8_t* sP = smem + OFF_P;
+    float* sRinv = reinterpret_cast<float*>(smem + OFF_RINV);
+    float* sLw = reinterpret_cast<float*>(smem + OFF_LW);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* qfull = bars + 0;
+    uint64_t* qempty = bars + 1;
+    uint64_t* kfull = bars + 2;        // [4] per 128-dim block of the tile
+    uint64_t* kempty = bars + 6;       // [4]
+    uint64_t* rfull = bars + 10;
+    uint64_t* sfull = bars + 11;
+    uint64_t* pfull = bars + 12;
+    uint64_t* ofull = bars + 13;
+    uint64_t* oempty = bars + 14;
+    uint64_t* lred = bars + 15;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qfull, 1);
+        mbar_init(qempty, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&kfull[i], 1 + 4);
+            mbar_init(&kempty[i], 1);
+        }
+        mbar_init(rfull, 4);
+        mbar_init(sfull, 1);
+        mbar_init(pfull, 4);
+        mbar_init(ofull, 1);
+        mbar_init(oempty, 4);
+        mbar_init(lred, 4);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sTmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sTmem;
+
+    if (warp == 0) {
+        // ============================ producer ============================
+        int g = 0, qi = 0;
+        int issued_g[4] = {-1, -1, -1, -1};
+        int issued_q = -1;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
+            const ItemInfo it = item_info(a, item);
+            if (it.nt == 0) continue;
+            if (lane == 0) {
+                if (qi > 0 && !mbar_wait(qempty, (qi - 1) & 1, a.budget, a.st)) {
+                    ok = false;
+                } else {
+                    mbar_arrive_expect_tx(qfull, QIMG_BYTES);
+                    bulk_g2s(sQ, a.qimg + it.bq * (int64_t)QIMG_BYTES, QIMG_BYTES, qfull);
+                    issued_q = qi;
+                }
+            }
+            ok = __shfl_sync(FULL, ok, 0);
+            for (int tt = 0; tt < it.nt && ok; ++tt, ++g) {
+                const int slot0 = (it.t0 + tt) * TC_TILE + 4 * lane;
+                int kind[4];
+                int32_t row[4];
+                int ntma = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const SlotSrc s = slot_source(a, it, slot0 + i, false);
+                    const bool tma = s.kind == 2 || (s.kind == 1 && !FP4);
+                    kind[i] = tma ? s.kind : 0;
+                    row[i] = (int32_t)s.row;
+                    ntma += tma ? 1 : 0;
+                }
+                const int tot = __reduce_add_sync(FULL, ntma);
+                const bool all_kv = kind[0] == 1 && kind[1] == 1 && kind[2] == 1 && kind[3] == 1;
+                const bool all_sw = kind[0] == 2 && kind[1] == 2 && kind[2] == 2 && kind[3] == 2;
+                for (int db = 0; db < 4; ++db) {
+                    if (lane == 0) {
+                        if (g > 0 && !mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st)) {
+                            ok = false;
+                        } else {
+                            mbar_arrive_expect_tx(&kfull[db], (uint32_t)tot * 256u);
+                            issued_g[db] = g;
+                        }
+                    }
+                    ok = __shfl_sync(FULL, ok, 0);
+                    if (!ok) break;
+#pragma unroll
+                    for (int ch = 2 * db; ch < 2 * db + 2; ++ch) {
+                        uint8_t* dst = sK + ch * CHUNK_K + 4 * lane * 128;
+                        if (all_kv) {
+                            tma_gather4(dst, &tm_kv, ch * 64, row[0], row[1], row[2], row[3], &kfull[db]);
+                        } else if (all_sw) {
+                            tma_gather4(dst, &tm_swa, ch * 64, row[0], row[1], row[2], row[3], &kfull[db]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                if (kind[i] == 1) tma_load_2d(dst + i * 128, &tm_kv, ch * 64, row[i], &kfull[db]);
+                                else if (kind[i] == 2) tma_load_2d(dst + i * 128, &tm_swa, ch * 64, row[i], &kfull[db]);
+                            }
+                        }
+                    }
+                }
+            }
+            if (ok) ++qi;
+        }
+        // copies still in flight must land before the CTA exits
+        if (lane == 0) {
+            for (int db = 0; db < 4; ++db)
+                if (issued_g[db] >= 0) mbar_wait(&kfull[db], issued_g[db] & 1, a.budget, a.st);
+            if (issued_q >= 0) mbar_wait(qfull, issued_q & 1, a.budget, a.st);
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ============================
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_f16(TC_TILE, TC_H, true);
+            constexpr uint32_t IDESC_PV = idesc_f16_major(128, TC_H, true, true, true);
+            const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), p_base = smem_u32(sP);
+            int g = 0, qi = 0;
+            bool ok = true;
+            uint64_t* last_bar = nullptr;
+            uint32_t last_par = 0;
+            for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
+                const ItemInfo it = item_info(a, item);
+                if (it.nt == 0) continue;
+                if (!mbar_wait(qfull, qi & 1, a.budget, a.st)) {
+                    ok = false;
+                    break;
+                }
+                for (int tt = 0; tt < it.nt; ++tt, ++g) {
+                    // logits: S^T = X . Qhat^T over 512 dims
+                    for (int db = 0; db < 4 && ok; ++db) {
+                        if (!mbar_wait(&kfull[db], g & 1, a.budget, a.st)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int ch = 2 * db + (kk >> 2);
+                            const uint32_t ko = (uint32_t)(kk & 3) * 32u;
+                            mma_ss(tmem + DS_COL, sdesc_sw128(k_base + ch * CHUNK_K + ko),
+                                   sdesc_sw128(q_base + ch * CHUNK_Q + ko), IDESC_QK, (db | kk) != 0);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(sfull);
+                    last_bar = sfull;
+                    last_par = g & 1;
+                    if (tt == it.nt - 1) {
+                        mma_commit(qempty);
+                        last_bar = qempty;
+                        last_par = qi & 1;
+                    }
+                    // output: O^T += X^T . P'^T over the tile's 128 slots
+                    if (!mbar_wait(pfull, g & 1, a.budget, a.st) ||
+                        (tt == 0 && qi > 0 && !mbar_wait(oempty, (qi - 1) & 1, a.budget, a.st))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int db = 0; db < 4; ++db) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            mma_ss(tmem + (uint32_t)db * TC_H,
+                                   sdesc_sw128_mn(k_base + 2 * db * CHUNK_K + ks * 2048, CHUNK_K, 1024),
+                                   sdesc_sw128_mn(p_base + ks * 2048, 1024, 1024), IDESC_PV, (tt > 0 || ks > 0));
+                        }
+                        mma_commit(&kempty[db]);
+                    }
+                    last_bar = &kempty[3];
+                    last_par = g & 1;
+                    if (tt == it.nt - 1) {
+                        mma_commit(ofull);
+                        last_bar = ofull;
+                        last_par = qi & 1;
+                    }
+                }
+                if (ok) ++qi;
+            }
+            // the MMAs must be complete before tensor memory is released
+            if (last_bar) mbar_wait(last_bar, last_par, a.budget, a.st);
+        }
+    } else if (warp < 6) {
+        // ============================ softmax + output ============================
+        const int qd = warp & 3;
+        const int r = qd * 32 + lane;                 // slot of the tile / dim of a 128-dim block
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const float c1_base = LOG2E / sqrtf((float)TC_C);
+        const float c0 = -TC_SHIFT * LOG2E;
+        int g = 0, qi = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
+            const ItemInfo it = item_info(a, item);
+            if (it.nt == 0) {
+                write_empty<TO>(a, it, r);
+                continue;
+            }
+            float lacc[TC_H];
+#pragma unroll
+            for (int h = 0; h < TC_H; ++h) lacc[h] = 0.0f;
+            for (int tt = 0; tt < it.nt; ++tt, ++g) {
+                bool w = mbar_wait(sfull, g & 1, a.budget, a.st) && mbar_wait(rfull, g & 1, a.budget, a.st);
+                if (!__all_sync(FULL, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s0[32], s1[32];
+                tmem_ld32(tmem + lane_base + DS_COL, s0);
+                tmem_ld32(tmem + lane_base + DS_COL + 32, s1);
+                tmem_wait_ld();
+                const float rinv = sRinv[r];
+                const float c1 = rinv * c1_base;
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(s0[2 * i]), c1, c0));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(s0[2 * i + 1]), c1, c0));
+                    if (rinv == 0.0f) p0 = p1 = 0.0f;
+                    lacc[2 * i] += p0;
+                    lacc[2 * i + 1] += p1;
+                    pk[i] = pack_bf16x2(p0 * rinv, p1 * rinv);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(s1[2 * i]), c1, c0));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(s1[2 * i + 1]), c1, c0));
+                    if (rinv == 0.0f) p0 = p1 = 0.0f;
+                    lacc[32 + 2 * i] += p0;
+                    lacc[33 + 2 * i] += p1;
+                    pk[16 + i] = pack_bf16x2(p0 * rinv, p1 * rinv);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(sP + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pfull);
+            }
+            if (!ok) break;
+            // denominators: sum of p over the 128 slots (reduce-scatter: lane l ends
+            // with heads 2l and 2l+1 of this warp's 32 slots)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const bool up = lane & 16;
+                const float send = up ? lacc[i] : lacc[i + 32], keep = up ? lacc[i + 32] : lacc[i];
+                lacc[i] = keep + __shfl_xor_sync(FULL, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const bool up = lane & 8;
+                const float send = up ? lacc[i] : lacc[i + 16], keep = up ? lacc[i + 16] : lacc[i];
+                lacc[i] = keep + __shfl_xor_sync(FULL, send, 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const bool up = lane & 4;
+                const float send = up ? lacc[i] : lacc[i + 8], keep = up ? lacc[i + 8] : lacc[i];
+                lacc[i] = keep + __shfl_xor_sync(FULL, send, 4);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool up = lane & 2;
+                const float send = up ? lacc[i] : lacc[i + 4], keep = up ? lacc[i + 4] : lacc[i];
+                lacc[i] = keep + __shfl_xor_sync(FULL, send, 2);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const bool up = lane & 1;
+                const float send = up ? lacc[i] : lacc[i + 2], keep = up ? lacc[i + 2] : lacc[i];
+                lacc[i] = keep + __shfl_xor_sync(FULL, send, 1);
+            }
+            sLw[qd * TC_H + 2 * lane] = lacc[0];
+            sLw[qd * TC_H + 2 * lane + 1] = lacc[1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(lred);
+            {
+                const bool w = mbar_wait(lred, qi & 1, a.budget, a.st);
+                if (!__all_sync(FULL, w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // per-head totals for heads lane and lane + 32; output scale and lse
+            float sc2[2], lse2[2], L2[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int h = lane + 32 * j;
+                const float L = sLw[h] + sLw[TC_H + h] + sLw[2 * TC_H + h] + sLw[3 * TC_H + h];
+                const float zs = (a.sink && h < a.H) ? a.sink[h] : -INFINITY;
+                float sc = 0.0f, ls = -INFINITY;
+                if (L > 0.0f) {
+                    const float M = fmaxf(TC_SHIFT, zs);
+                    const float e = expf(TC_SHIFT - M);
+                    const float den = L * e + ((zs == -INFINITY) ? 0.0f : expf(zs - M));
+                    sc = e / den;
+                    ls = M + logf(den);
+                } else if (zs != -INFINITY) {
+                    ls = zs;
+                }
+                sc2[j] = sc;
+                lse2[j] = ls;
+                L2[j] = L;
+            }
+            {
+                const bool w = mbar_wait(ofull, qi & 1, a.budget, a.st);
+                if (!__all_sync(FULL, w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            tc_fence_after();
+            const bool split = a.n_split > 1;
+            const bool rot = !split && (a.flags & CSA2_ROPE) && qd >= 2;
+            float rc = 1.0f, rs = 0.0f;
+            if (rot) rope_cos_sin(a.rope, it.t, (32 * qd + lane - 64) >> 1, rc, rs);
+            float scv[TC_H];
+#pragma unroll
+            for (int h = 0; h < TC_H; ++h) scv[h] = __shfl_sync(FULL, sc2[h >> 5], h & 31);
+            for (int db = 0; db < 4; ++db) {
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H, o0);
+                tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H + 32, o1);
+                tmem_wait_ld();
+                const int d = db * 128 + r;
+#pragma unroll
+                for (int h = 0; h < TC_H; ++h) {
+                    float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]);
+                    if (split) {
+                        if (h < a.H) a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + 2 + d] = v;
+                    } else {
+                        v *= scv[h];
+                        if (db == 3 && rot) {
+                            const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
+                            v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
+                        }
+                        if (h < a.H)
+                            reinterpret_cast<TO*>(a.out)[(it.bq * a.H + h) * (int64_t)TC_C + d] = from_f32<TO>(v);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(oempty);
+            if (qd == 0) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = lane + 32 * j;
+                    if (h >= a.H) continue;
+                    if (split) {
+                        float* p = a.part + ((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART;
+                        p[0] = L2[j] > 0.0f ? TC_SHIFT : -INFINITY;
+                        p[1] = L2[j];
+                    } else if (a.lse) {
+                        a.lse[it.bq * a.H + h] = lse2[j];
+                    }
+                }
+            }
+            ++qi;
+        }
+    } else {
+        // ============================ loaders ============================
+        const int r = threadIdx.x - 192;           // slot of the tile
+        int g = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
+            const ItemInfo it = item_info(a, item);
+            for (int tt = 0; tt < it.nt; ++tt, ++g) {
+                const SlotSrc s = slot_source(a, it, (it.t0 + tt) * TC_TILE + r, true);
+                const bool tma_row = s.kind == 2 || (s.kind == 1 && !FP4);
+                bool w = true;
+                if (g > 0)
+                    for (int db = 0; db < 4; ++db) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
+                if (!__all_sync(FULL, w)) {
+                    ok = false;
+                    break;
+                }
+                float ss = 0.0f;
+                if (!tma_row) {
+                    if (s.kind == 1) {
+                        ss = fp4_row_to_tile(reinterpret_cast<const uint8_t*>(a.kv), s.row, sK, r);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    for (int db = 0; db < 4; ++db) mbar_arrive(&kfull[db]);
+                if (tma_row) {
+                    for (int db = 0; db < 4; ++db) w = w && mbar_wait(&kfull[db], g & 1, a.budget, a.st);
+                    if (w) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                bf16x8_sumsq(*reinterpret_cast<const uint4*>(
+                                                 sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
+                                             ss);
+                    }
+                }
+                if (!__all_sync(FULL, w)) {
+                    ok = false;
+                    break;
+                }
+                sRinv[r] = s.kind != 0 ? 1.0f / sqrtf(ss / (float)TC_C + 1e-6f) : 0.0f;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rfull);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+void tc_splits(const csa2_ctx* ctx, int64_t n_bq, int k, int window, int& n_split, int& tps) {
+    const int n_tiles = std::max(1, (k + window + TC_TILE - 1) / TC_TILE);
+    int want = (int)std::min<int64_t>(n_tiles, std::max<int64_t>(1, (ctx->num_sms + n_bq - 1) / n_bq));
+    tps = (n_tiles + want - 1) / want;
+    n_split = (n_tiles + tps - 1) / tps;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <bool FP4, typename TO>
+csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, const CUtensorMap& m_kv, const CUtensorMap& m_swa,
+                      cudaStream_t s) {
+    auto kern = attn_tc_kernel<FP4, TO>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+            return CSA2_ERR_CUDA;
+        attr = true;
+    }
+    const int64_t grid = std::min<int64_t>(a.items, ctx->num_sms);
+    kern<<<(unsigned)grid, TC_THREADS, SMEM_BYTES, s>>>(a, m_kv, m_swa);
+    return csa2_launch_status();
+}
+
+}  // namespace
+
+bool attn_tc_applies(const AttnTcCall& c) {
+    if (c.q_dt != CSA2_BF16) return false;
+    if (c.kv_dt != CSA2_BF16 && c.kv_dt != CSA2_FP4_E4M3x16) return false;
+    if (c.window > 0 && c.swa_dt != CSA2_BF16) return false;
+    if ((c.flags & (CSA2_QNORM | CSA2_KVNORM)) != (CSA2_QNORM | CSA2_KVNORM)) return false;
+    if (c.H < 1 || c.H > TC_H) return false;
+    if (c.kv_dt == CSA2_BF16 && c.k > 0 && (int64_t)c.B * c.N > 0x7FFFFFFF) return false;   // map row coordinate
+    if (c.window > 0 && (int64_t)c.B * c.swa_cap > 0x7FFFFFFF) return false;
+    return true;
+}
+
+size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
+    if (!ctx || H < 1 || H > TC_H || B <= 0 || Q <= 0) return 0;
+    const int64_t n_bq = (int64_t)B * Q;
+    int ns = 1, tps = 1;
+    tc_splits(ctx, n_bq, k, window, ns, tps);
+    const size_t part = ns > 1 ? align_up((size_t)n_bq * H * ns * PART * sizeof(float), 1024) : 0;
+    return part + (size_t)n_bq * QIMG_BYTES;
+}
+
+csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
+                        int* n_split) {
+    const int64_t n_bq = (int64_t)c.B * c.Q;
+    int ns = 1, tps = 1;
+    tc_splits(ctx, n_bq, c.k, c.window, ns, tps);
+    const size_t part = ns > 1 ? align_up((size_t)n_bq * c.H * ns * PART * sizeof(float), 1024) : 0;
+    if (!ws || ws_bytes < part + (size_t)n_bq * QIMG_BYTES || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    uint8_t* qimg = reinterpret_cast<uint8_t*>(ws) + part;
+    if (c.q_dt == CSA2_BF16)
+        attn_qprep_kernel<__nv_bfloat16><<<(unsigned)n_bq, 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg);
+    else
+        attn_qprep_kernel<float><<<(unsigned)n_bq, 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
+                                                                c.rope, c.flags, qimg);
+    CUtensorMap m_kv, m_swa;
+    memset(&m_kv, 0, sizeof(m_kv));
+    memset(&m_swa, 0, sizeof(m_swa));
+    if (c.kv_dt == CSA2_BF16 && c.k > 0 && c.N > 0) {
+        if (!csa2_make_bf16_map(&m_kv, c.kv, (int64_t)c.B * c.N, TC_C, 64, 1)) return CSA2_ERR_CUDA;
+    }
+    if (c.window > 0) {
+        if (!csa2_make_bf16_map(&m_swa, c.swa, (int64_t)c.B * c.swa_cap, TC_C, 64, 1)) return CSA2_ERR_CUDA;
+    }
+    TcArgs a;
+    a.qimg = qimg;
+    a.kv = c.kv;
+    a.N = c.N;
+    a.idx = c.idx;
+    a.k = c.k;
+    a.swa_cap = c.swa_cap;
+    a.swa_pos0 = c.swa_pos0;
+    a.window = c.window;
+    a.q_pos = c.q_pos;
+    a.sink = c.sink;
+    a.Q = c.Q;
+    a.H = c.H;
+    a.rope = c.rope;
+    a.flags = c.flags;
+    a.out = c.out;
+    a.lse = c.lse;
+    a.part = reinterpret_cast<float*>(ws);
+    a.n_split = ns;
+    a.tps = tps;
+    a.items = n_bq * ns;
+    a.st = ctx->status;
+    a.budget = WAIT_BUDGET;
+    *n_split = ns;
+    const bool fp4 = c.kv_dt == CSA2_FP4_E4M3x16;
+    const bool f32o = c.out_dt == CSA2_F32;
+    if (fp4) return f32o ? launch_tc<true, float>(ctx, a, m_kv, m_swa, s)
+                         : launch_tc<true, __nv_bfloat16>(ctx, a, m_kv, m_swa, s);
+    return f32o ? launch_tc<false, float>(ctx, a, m_kv, m_swa, s)
+                : launch_tc<false, __nv_bfloat16>(ctx, a, m_kv, m_swa, s);
+}

@@ -1,0 +1,46 @@
+// Tensor-core (tcgen05) path of csa2_sparse_attn, used when the query and the
+// window are bf16, the selected rows are bf16 or FP4, both RMSNorms are on and the
+// heads fit one 64-wide MMA.  The caller (attn.cu) owns validation and the split
+// combine.
+#pragma once
+
+#include "csa2_internal.cuh"
+
+struct AttnTcCall {
+    const void* q;
+    csa2_dtype q_dt;
+    const void* kv;
+    csa2_dtype kv_dt;
+    int64_t N;
+    const int32_t* idx;
+    int k;
+    const void* swa;
+    csa2_dtype swa_dt;
+    int64_t swa_cap, swa_pos0;
+    int window;
+    const int64_t* q_pos;
+    const float* sink;
+    int B, Q, H;
+    RopeTable rope;
+    unsigned flags;
+    void* out;
+    csa2_dtype out_dt;
+    float* lse;
+};
+
+// Whether the tensor-core path handles these dtypes, flags and sizes.
+bool attn_tc_applies(const AttnTcCall& c);
+
+// Workspace bytes the tensor-core path needs for these sizes (query images plus,
+// when the keys are split, the per-split partials), or 0 when H > 64.
+size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window);
+
+// Workspace bytes of the CUDA-core path (attn.cu) for these sizes: its key-split
+// partials, 0 when it runs unsplit.
+size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window);
+
+// Runs the path.  On return *n_split > 1 means the output is still in per-split
+// partials at the start of `ws` (float [B*Q, H, n_split, 514]: max, sum, output),
+// to be merged by the caller's combine kernel.
+csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
+                        int* n_split);

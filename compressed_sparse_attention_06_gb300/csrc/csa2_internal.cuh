@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -127,6 +128,26 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
     uint32_t e = (nib >> 1) & 3u, mbit = nib & 1u;
     float mag = (e == 0) ? 0.5f * (float)mbit : ldexpf(1.0f + 0.5f * (float)mbit, (int)e - 1);
     return (nib & 8u) ? -mag : mag;
+}
+
+// Eight E2M1 codes (one 32-bit word, code 2i in the low nibble of byte i) -> f32,
+// through the exact E2M1 -> f16 conversion.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&o)[8]) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(*reinterpret_cast<__half2*>(&h[i]));
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
 }
 
 // Row bytes of the packed formats.

@@ -38,6 +38,7 @@
 
 #include "index_score_tc.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace {
 
@@ -123,6 +124,22 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t& o0, uint32
         "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
         : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
         : "r"(x));
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register) and their fused multiply-add,
+// each lane rounded exactly as a scalar fmaf.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -391,18 +408,30 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
             float sc[QT];
 #pragma unroll
             for (int qi = 0; qi < QT; ++qi) {
-                uint32_t d[32];
-                float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // four independent chains
+                uint32_t d0[32], d1[32];
                 const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + C::D_COL0 + j * C::N + qi * HEADS;
+                tmem_ld32(tb, d0);
+                tmem_ld32(tb + 32, d1);
+                tmem_wait_ld();
+                // four independent chains (head h feeds chain h mod 4), two per packed FMA
+                uint64_t c01 = 0, c23 = 0;
+                const float4* w4 = reinterpret_cast<const float4*>(sW + qi * HEADS);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    tmem_ld32(tb + hh * 32, d);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        a4[i & 3] = fmaf(sW[qi * HEADS + hh * 32 + i], fmaxf(__uint_as_float(d[i]), 0.0f), a4[i & 3]);
+                for (int i = 0; i < 16; ++i) {
+                    const float4 wv = w4[i];
+                    const uint32_t* dd = i < 8 ? d0 : d1;
+                    const int o = (i & 7) * 4;
+                    c01 = ffma2(f2pack(wv.x, wv.y),
+                                f2pack(fmaxf(__uint_as_float(dd[o]), 0.0f), fmaxf(__uint_as_float(dd[o + 1]), 0.0f)),
+                                c01);
+                    c23 = ffma2(f2pack(wv.z, wv.w),
+                                f2pack(fmaxf(__uint_as_float(dd[o + 2]), 0.0f), fmaxf(__uint_as_float(dd[o + 3]), 0.0f)),
+                                c23);
                 }
-                float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+                float a0, a1, a2, a3;
+                f2unpack(c01, a0, a1);
+                f2unpack(c23, a2, a3);
+                float acc = (a0 + a1) + (a2 + a3);
                 if (KF == KF_MX) acc = ldexpf(acc, rho);
                 const bool vis = sid < V[qi] && e < n_elems;
                 sc[qi] = vis ? acc : -INFINITY;
@@ -443,36 +472,9 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 // 2-D map over bf16 rows of 128 values: box of 64 values x box_rows rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)DIM, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)DIM * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return csa2_make_bf16_map(m, base, rows, DIM, 64, box_rows);
 }
 
 template <int KF, int QT, bool CAND>

@@ -83,6 +83,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// Four rows of a 2-D tensor (box of one row) gathered into consecutive rows of
+// shared memory: rows y0..y3, columns [x, x + box width).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -185,6 +196,26 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
     d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset: 8-row atoms
     d |= (uint64_t)1 << 46;                  // descriptor version for tcgen05
     d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor with the operand majors given: an MN-major A (or B) is
+// stored with M (or N) contiguous.
+__host__ __device__ constexpr uint32_t idesc_f16_major(int M, int N, bool bf16, bool a_mn, bool b_mn) {
+    return idesc_f16(M, N, bf16) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
+}
+
+// Descriptor for an MN-major operand with the 128-byte swizzle: rows of 128 B hold
+// 64 consecutive M (or N) elements, one row per K index; 8 consecutive K rows form
+// a 1024-byte atom.  `lbo` = bytes from one 64-element group of M (N) to the next,
+// `sbo` = bytes from one 8-row K group to the next.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
     return d;
 }
 

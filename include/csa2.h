@@ -228,12 +228,21 @@ size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, 
  *           lse = log(sum_j e^{z_j} + e^{sink_i})
  * c == 512, 1 <= H <= 128, 0 <= k <= 2048, 0 <= window <= 1024, B*Q <= 65535.
  *
- * Workspace: with few queries the keys of each query are split over several CTAs
- * whose partial results go to `ws` (caller-owned device memory, 16-byte aligned)
- * and are merged by log-sum-exp.  csa2_sparse_attn_workspace_bytes() gives the
- * size that enables the full split; a smaller (or NULL) workspace gives fewer
- * splits (same result, less parallelism).  Calls that share a workspace must not
- * overlap on the GPU.
+ * Two paths compute this.  The tensor-core path (tcgen05) runs when q and swa are
+ * BF16, kv is BF16 or FP4, both RMSNorm flags are set, H <= 64 and the workspace
+ * holds at least csa2_sparse_attn_workspace_bytes(); it rounds the normalised,
+ * rotated query and the probabilities to bf16 for the MMAs (fp32 accumulation) and,
+ * because both norms bound every logit by sqrt(c), uses the fixed softmax offset 24
+ * instead of a running maximum.  Every other call takes the CUDA-core path, which
+ * works in fp32 throughout.
+ *
+ * Workspace (caller-owned device memory, 16-byte aligned): the tensor-core path keeps
+ * each query's prepared bf16 image there (64 KB per query) and, with few queries,
+ * the per-split partial results of its key split; the CUDA-core path keeps only its
+ * key-split partials.  csa2_sparse_attn_workspace_bytes() gives the size that
+ * enables both; with less, the call falls back to the CUDA-core path with as many
+ * splits as fit (NULL: no split).  Calls that share a workspace must not overlap on
+ * the GPU.
  */
 size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window);
 csa2_status csa2_sparse_attn(csa2_ctx* ctx,
@@ -263,9 +272,11 @@ csa2_status csa2_sparse_attn(csa2_ctx* ctx,
  *     capture.
  *   - All calls share the array: calls whose kernels overlap on the GPU race.
  *     Nothing in it needs to start at zero (each call rewrites what it reads).
- *   - A call whose split would need more than CSA2_NOALLOC_SCRATCH_BYTES is rejected
- *     with CSA2_ERR_INVALID_ARG before anything is launched.
- * Results equal csa2_sparse_attn's with a full workspace.
+ *   - A call whose CUDA-core key split would need more than
+ *     CSA2_NOALLOC_SCRATCH_BYTES is rejected with CSA2_ERR_INVALID_ARG before
+ *     anything is launched.  The tensor-core path is taken when its workspace fits
+ *     the array, so results equal csa2_sparse_attn's with a full workspace whenever
+ *     that workspace is at most CSA2_NOALLOC_SCRATCH_BYTES.
  */
 #define CSA2_NOALLOC_SCRATCH_BYTES (24u << 20)
 csa2_status csa2_sparse_attn_noalloc(csa2_ctx* ctx,

@@ -314,13 +314,19 @@ def test_sparse_attn(kv_kind, flags):
                                   want_lse=True)
     out, lse = to_np(out), to_np(lse)
     tol = 1e-4 if kv_kind == "f32" else 2e-2
+    # The tensor-core path (bf16 query, both norms) rounds the normalised query to
+    # bf16: a logit q^.k^/sqrt(c) moves by about 2^-9 |q^||k^| / (sqrt(3) c) ~ 1e-3,
+    # and lse by the softmax-weighted mean of those moves, up to that size when few
+    # keys carry the mass; fp32 paths stay at 1e-5.
+    tc = kv_kind != "f32" and (flags & C.QNORM) and (flags & C.KVNORM)
+    lse_tol = 2e-3 if tc else 1e-5
     for b in range(B):
         for qq in range(Q):
             t = int(q_pos[b, qq])
             o, l, mass = O.sparse_attn(q[b, qq].double().cpu().numpy(), kv_np[b], to_np(idx[b, qq]),
                                        swa[b].double().cpu().numpy(), 0, t, sink.double().cpu().numpy(), 128, flags)
             assert_close(out[b, qq], o, tol, f"out b{b} q{qq}")
-            assert_close(lse[b, qq], l, 1e-5, "lse")
+            assert_close(lse[b, qq], l, lse_tol, "lse")
             assert np.all((mass > 0) & (mass < 1))
 
 
