@@ -126,22 +126,6 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t& o0, uint32
         : "r"(x));
 }
 
-// Packed fp32 pairs (two lanes of one 64-bit register) and their fused multiply-add,
-// each lane rounded exactly as a scalar fmaf.
-__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -413,25 +397,24 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                 tmem_ld32(tb, d0);
                 tmem_ld32(tb + 32, d1);
                 tmem_wait_ld();
-                // four independent chains (head h feeds chain h mod 4), two per packed FMA
-                uint64_t c01 = 0, c23 = 0;
+                // four independent chains (head h feeds chain h mod 4) of w_h * 2 ReLU(d_h):
+                // d + |d| is exactly 2 ReLU(d) (one add on the FMA pipe), and the final
+                // halving is exact, so the sum equals the one of w_h * ReLU(d_h)
+                float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 const float4* w4 = reinterpret_cast<const float4*>(sW + qi * HEADS);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float4 wv = w4[i];
                     const uint32_t* dd = i < 8 ? d0 : d1;
                     const int o = (i & 7) * 4;
-                    c01 = ffma2(f2pack(wv.x, wv.y),
-                                f2pack(fmaxf(__uint_as_float(dd[o]), 0.0f), fmaxf(__uint_as_float(dd[o + 1]), 0.0f)),
-                                c01);
-                    c23 = ffma2(f2pack(wv.z, wv.w),
-                                f2pack(fmaxf(__uint_as_float(dd[o + 2]), 0.0f), fmaxf(__uint_as_float(dd[o + 3]), 0.0f)),
-                                c23);
+                    const float x0 = __uint_as_float(dd[o]), x1 = __uint_as_float(dd[o + 1]);
+                    const float x2 = __uint_as_float(dd[o + 2]), x3 = __uint_as_float(dd[o + 3]);
+                    a4[0] = fmaf(wv.x, x0 + fabsf(x0), a4[0]);
+                    a4[1] = fmaf(wv.y, x1 + fabsf(x1), a4[1]);
+                    a4[2] = fmaf(wv.z, x2 + fabsf(x2), a4[2]);
+                    a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
                 }
-                float a0, a1, a2, a3;
-                f2unpack(c01, a0, a1);
-                f2unpack(c23, a2, a3);
-                float acc = (a0 + a1) + (a2 + a3);
+                float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
                 if (KF == KF_MX) acc = ldexpf(acc, rho);
                 const bool vis = sid < V[qi] && e < n_elems;
                 sc[qi] = vis ? acc : -INFINITY;

@@ -17,8 +17,10 @@
 //     same total order);
 //   * without a workspace a long row falls back to one CTA reading global memory
 //     on every pass.
-// Histogram increments are aggregated per warp (__match_any_sync), since scores of
-// one row often share their top key bits.
+// The threshold search takes a 12-bit histogram over every key, copies the keys of
+// the threshold bin aside and resolves the remaining 20 bits on that copy; a warp
+// whose keys share a digit (scores of one row often share their top bits) counts
+// them with one shared-memory atomic.
 #include <algorithm>
 
 #include "csa2_internal.cuh"
@@ -93,39 +95,10 @@ __device__ __forceinline__ uint32_t key_of(const SelArgs& a, int64_t row, int64_
     return inf.valid ? order_key(a.vals[row * a.ld + e]) : 0u;
 }
 
-// Add a digit to this warp's private histogram: lanes with the same digit are
-// counted once by their lowest lane, so no two lanes touch one bin in the same
-// instruction and no other warp touches this histogram.
-__device__ __forceinline__ void hist_add(uint32_t* whist, uint32_t digit, bool active) {
-    const uint32_t d = active ? digit : 256u;
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    if (active && (int)(threadIdx.x & 31) == __ffs(peers) - 1) whist[d] += (uint32_t)__popc(peers);
-}
-
-// Block-wide exclusive scan of a 0/1 flag; returns the prefix, writes the total.
-__device__ __forceinline__ int block_excl_scan(bool flag, int* warp_tot, int& total) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[wid] = __popc(bal);
-    __syncthreads();
-    if (wid == 0) {
-        const int v = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        warp_tot[lane] = incl - v;
-        if (lane == 31) warp_tot[32] = incl;
-    }
-    __syncthreads();
-    const int r = warp_tot[wid] + in_warp;
-    total = warp_tot[32];
-    __syncthreads();
-    return r;
-}
+constexpr unsigned FULL_MASK = 0xffffffffu;
+constexpr int NB_A = 4096;             // first digit: key bits 31..20
+constexpr int NB_B = 1024;             // then bits 19..10 and 9..0
+constexpr int CAND_CAP = 8192;         // keys of the threshold bin kept for the last two digits
 
 struct SelState {
     uint32_t T;
@@ -134,88 +107,170 @@ struct SelState {
 };
 
 struct SelShared {
-    uint32_t whist[32][256];     // one histogram per warp (scores of a row share their top bits)
-    uint32_t hist[256];
+    uint32_t hist[NB_A];
+    uint32_t wtot[32];
+    uint32_t wtot_all;
     int warp_tot[33];
-    int digit, remaining, nvalid;
+    int bin, nvalid, cand_n;
+    uint32_t above;
 };
 
-// Exact k-th largest key over n elements given by key_at(e) (0 = not a candidate).
+// Block-wide exclusive scan of one value per thread (thread order); `total` gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, SelShared& sh, uint32_t& total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) sh.wtot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const uint32_t t = lane < nw ? sh.wtot[lane] : 0u;
+        uint32_t ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(FULL_MASK, ti, o);
+            if (lane >= o) ti += u;
+        }
+        sh.wtot[lane] = ti - t;
+        if (lane == 31) sh.wtot_all = ti;
+    }
+    __syncthreads();
+    const uint32_t r = sh.wtot[wid] + incl - v;
+    total = sh.wtot_all;
+    __syncthreads();
+    return r;
+}
+
+// Histogram of digit (key >> shift) & dmask over the active keys (valid, and equal to
+// `prefix` on the bits of `pmask`).  A warp whose active lanes share one digit adds
+// once; otherwise each active lane adds its own (shared-memory atomics).
 template <class KeyAt>
-__device__ SelState block_radix_select(KeyAt key_at, int64_t n, int k, SelShared& sh) {
-    const int tid = threadIdx.x, lane = tid & 31;
+__device__ __forceinline__ void hist_pass(KeyAt key_at, int64_t n, uint32_t prefix, uint32_t pmask, int shift,
+                                          uint32_t dmask, uint32_t* hist, int* nvalid) {
+    const int lane = threadIdx.x & 31;
+    int local_valid = 0;
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+        const int64_t e = base + threadIdx.x;
+        const uint32_t key = e < n ? key_at(e) : 0u;
+        local_valid += key != 0u;
+        const bool act = key != 0u && (key & pmask) == prefix;
+        const unsigned am = __ballot_sync(FULL_MASK, act);
+        if (am == 0u) continue;
+        const uint32_t d = (key >> shift) & dmask;
+        const int leader = __ffs(am) - 1;
+        const uint32_t d0 = __shfl_sync(FULL_MASK, d, leader);
+        if (__all_sync(FULL_MASK, !act || d == d0)) {
+            if (lane == leader) atomicAdd(&hist[d0], (uint32_t)__popc(am));
+        } else if (act) {
+            atomicAdd(&hist[d], 1u);
+        }
+    }
+    if (nvalid) {
+        const int w = __reduce_add_sync(FULL_MASK, local_valid);
+        if (lane == 0 && w) atomicAdd(nvalid, w);
+    }
+}
+
+// The bin (searched from the top) that holds the `remaining`-th largest active key:
+// sh.bin = that bin, sh.above = active keys in the bins above it.  nb is a multiple
+// of the block size.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t remaining, SelShared& sh) {
+    const int per = nb / (int)blockDim.x;
+    const int top = nb - 1 - (int)threadIdx.x * per;
+    uint32_t loc = 0;
+    for (int j = 0; j < per; ++j) loc += hist[top - j];
+    uint32_t total;
+    const uint32_t excl = block_excl_scan_u32(loc, sh, total);
+    if (excl < remaining && remaining <= excl + loc) {
+        uint32_t cum = excl;
+        for (int j = 0; j < per; ++j) {
+            const uint32_t c = hist[top - j];
+            if (cum + c >= remaining) {
+                sh.bin = top - j;
+                sh.above = cum;
+                break;
+            }
+            cum += c;
+        }
+    }
+    __syncthreads();
+}
+
+// Unordered copy of the active keys into cand (sh.cand_n must start at 0).
+template <class KeyAt>
+__device__ __forceinline__ void compact_active(KeyAt key_at, int64_t n, uint32_t prefix, uint32_t pmask,
+                                               uint32_t* cand, SelShared& sh) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+        const int64_t e = base + threadIdx.x;
+        const uint32_t key = e < n ? key_at(e) : 0u;
+        const bool act = key != 0u && (key & pmask) == prefix;
+        const unsigned am = __ballot_sync(FULL_MASK, act);
+        if (am == 0u) continue;
+        const int leader = __ffs(am) - 1;
+        int off = 0;
+        if (lane == leader) off = atomicAdd(&sh.cand_n, __popc(am));
+        off = __shfl_sync(FULL_MASK, off, leader);
+        if (act) cand[off + __popc(am & lt)] = key;
+    }
+}
+
+// Exact k-th largest key over n elements given by key_at(e) (0 = not a candidate):
+// a 12-bit histogram over all keys picks the threshold bin; its keys (if at most
+// CAND_CAP) are copied aside and two 10-bit passes over them finish the key.
+template <class KeyAt>
+__device__ SelState block_radix_select(KeyAt key_at, int64_t n, int k, SelShared& sh, uint32_t* cand) {
+    const int tid = threadIdx.x;
     SelState r;
     r.take_all = false;
     r.T = 0xFFFFFFFFu;
     r.remaining = 0;
     if (k <= 0) return r;
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = k;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        const int nwarps = blockDim.x >> 5;
-        for (int i = tid; i < nwarps * 256; i += blockDim.x) sh.whist[i >> 8][i & 255] = 0;
-        if (tid == 0) sh.nvalid = 0;
+    for (int i = tid; i < NB_A; i += blockDim.x) sh.hist[i] = 0;
+    if (tid == 0) {
+        sh.nvalid = 0;
+        sh.cand_n = 0;
+    }
+    __syncthreads();
+    hist_pass(key_at, n, 0u, 0u, 20, 0xFFFu, sh.hist, &sh.nvalid);
+    __syncthreads();
+    if (sh.nvalid <= k) {
+        r.take_all = true;
+        r.T = 0;
+        return r;
+    }
+    find_bin(sh.hist, NB_A, (uint32_t)k, sh);
+    uint32_t prefix = (uint32_t)sh.bin << 20, pmask = 0xFFF00000u;
+    uint32_t remaining = (uint32_t)k - sh.above;
+    const uint32_t m = sh.hist[sh.bin];
+    __syncthreads();
+    const bool use_cand = m <= (uint32_t)CAND_CAP;
+    if (use_cand) {
+        compact_active(key_at, n, prefix, pmask, cand, sh);
         __syncthreads();
-        int local_valid = 0;
-        uint32_t* wh = sh.whist[tid >> 5];
-        for (int64_t base = 0; base < n; base += blockDim.x) {
-            const int64_t e = base + tid;
-            const uint32_t key = e < n ? key_at(e) : 0u;
-            local_valid += key != 0u;
-            hist_add(wh, (key >> shift) & 255u, key != 0u && (key & pmask) == prefix);
-        }
-        if (pass == 0) {
-            const int w = __reduce_add_sync(0xffffffffu, local_valid);
-            if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
-        }
+    }
+    auto cand_at = [&](int64_t i) -> uint32_t { return cand[i]; };
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        for (int i = tid; i < NB_B; i += blockDim.x) sh.hist[i] = 0;
         __syncthreads();
-        for (int b = tid; b < 256; b += blockDim.x) {
-            uint32_t tot = 0;
-            for (int w = 0; w < nwarps; ++w) tot += sh.whist[w][b];
-            sh.hist[b] = tot;
-        }
+        if (use_cand)
+            hist_pass(cand_at, (int64_t)m, prefix, pmask, shift, 0x3FFu, sh.hist, nullptr);
+        else
+            hist_pass(key_at, n, prefix, pmask, shift, 0x3FFu, sh.hist, nullptr);
         __syncthreads();
-        if (pass == 0 && sh.nvalid <= k) {
-            r.take_all = true;
-            r.T = 0;
-            return r;
-        }
-        if (tid < 32) {
-            uint32_t loc[8];
-            uint32_t lsum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                loc[j] = sh.hist[255 - 8 * lane - j];
-                lsum += loc[j];
-            }
-            uint32_t incl = lsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            const uint32_t excl = incl - lsum;
-            if (excl < (uint32_t)remaining && (uint32_t)remaining <= incl) {
-                uint32_t cum = excl;
-                for (int j = 0; j < 8; ++j) {
-                    if (cum + loc[j] >= (uint32_t)remaining) {
-                        sh.digit = 255 - 8 * lane - j;
-                        sh.remaining = remaining - (int)cum;
-                        break;
-                    }
-                    cum += loc[j];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)sh.digit << shift;
-        pmask |= 255u << shift;
-        remaining = sh.remaining;
+        find_bin(sh.hist, NB_B, remaining, sh);
+        prefix |= (uint32_t)sh.bin << shift;
+        pmask |= 0x3FFu << shift;
+        remaining -= sh.above;
         __syncthreads();
     }
     r.T = prefix;
-    r.remaining = remaining;
+    r.remaining = (int)remaining;
     return r;
 }
 
@@ -302,7 +357,7 @@ __device__ void finish_row(const SelArgs& a, int64_t row, int filled, int64_t n_
 // Stage 1 (or the whole selection when chunks == 1): a CTA per (chunk, row).
 template <int MODE, bool SMEM>
 __global__ void __launch_bounds__(SEL_THREADS) sel_chunk_kernel(SelArgs a) {
-    extern __shared__ uint32_t skey[];
+    extern __shared__ uint32_t skey[];     // [chunk_len] keys (SMEM) then [CAND_CAP] candidates
     __shared__ SelShared sh;
     const int64_t row = blockIdx.y;
     const int chunk = blockIdx.x;
@@ -316,7 +371,8 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_chunk_kernel(SelArgs a) {
         __syncthreads();
     }
     auto key_at = [&](int64_t i) -> uint32_t { return SMEM ? skey[i] : key_of<MODE>(a, row, c0 + i, V, n_elems); };
-    const SelState r = block_radix_select(key_at, n, a.k, sh);
+    uint32_t* cand = skey + (SMEM ? a.chunk_len : 0);
+    const SelState r = block_radix_select(key_at, n, a.k, sh, cand);
     if (a.chunks > 1) {
         const int64_t base = (row * a.chunks + chunk) * (int64_t)a.k;
         const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
@@ -347,7 +403,7 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_merge_kernel(SelArgs a) {
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) skey[i] = a.ws_key[base + i];
     __syncthreads();
     auto key_at = [&](int64_t i) -> uint32_t { return skey[i]; };
-    const SelState r = block_radix_select(key_at, n, a.k, sh);
+    const SelState r = block_radix_select(key_at, n, a.k, sh, skey + n);
     const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
         a.out_idx[row * a.out_len + pos] = a.ws_id[base + i];
         if (a.out_val) a.out_val[row * a.out_len + pos] = key_to_float(key);
@@ -393,9 +449,11 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
     }
     static bool attr = false;
     if (!attr) {
-        const int bytes = SEL_SMEM_CAP * (int)sizeof(uint32_t);
+        const int bytes = (SEL_SMEM_CAP + CAND_CAP) * (int)sizeof(uint32_t);
         if (cudaFuncSetAttribute(sel_chunk_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
                 cudaSuccess ||
+            cudaFuncSetAttribute(sel_chunk_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CAND_CAP * (int)sizeof(uint32_t)) != cudaSuccess ||
             cudaFuncSetAttribute(sel_merge_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
                 cudaSuccess)
             return CSA2_ERR_CUDA;
@@ -403,11 +461,12 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
     }
     dim3 grid((unsigned)a.chunks, (unsigned)rows);
     if (smem)
-        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, a.chunk_len * sizeof(uint32_t), s>>>(a);
+        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, (a.chunk_len + CAND_CAP) * sizeof(uint32_t), s>>>(a);
     else
-        sel_chunk_kernel<MODE, false><<<grid, SEL_THREADS, 0, s>>>(a);
+        sel_chunk_kernel<MODE, false><<<grid, SEL_THREADS, CAND_CAP * sizeof(uint32_t), s>>>(a);
     if (a.chunks > 1)
-        sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS, (size_t)a.chunks * a.k * sizeof(uint32_t), s>>>(a);
+        sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS, ((size_t)a.chunks * a.k + CAND_CAP) * sizeof(uint32_t),
+                                 s>>>(a);
     return csa2_launch_status();
 }
 
