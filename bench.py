@@ -447,7 +447,7 @@ class ReindexReuse(Workload):
         self.idx = torch.empty((self.B, 1, 512), dtype=torch.int32, device=dev)
         self.outs = [torch.empty((self.B, 1, 64, 512), dtype=torch.bfloat16, device=dev) for _ in range(4)]
         self.topk_ws = C._ws(C.csa2_topk_workspace_bytes(self.B, 16384, 512), dev)
-        self.attn_ws = C._ws(C.csa2_sparse_attn_workspace_bytes(self.B, 1, 64, 512, 128), dev)
+        self.attn_ws = C._ws(C.csa2_sparse_attn_workspace_bytes(self.B, 1, 64, 512, 128, N=self.N, swa_cap=128), dev)
         self.e2e_in = [wl["qI"], wl["w"]] + [wl[f"q{l}"] for l in range(4)]
         self.e2e_out = self.outs + [self.idx]
 
@@ -515,7 +515,7 @@ class PrefillChunk(Workload):
         self.kv = torch.empty((1, self.N, 512), dtype=torch.bfloat16, device=dev)
         self.kv[0, :self.nce] = wl["kv_ctx"][0]
         self.pos0 = torch.tensor([wl.meta["pos0"]], dtype=torch.int64, device=dev)
-        self.buf = P.alloc_prefill(self.Q, self.N, 64, 512, dev, wl.q_pos, self.m)
+        self.buf = P.alloc_prefill(self.Q, self.N, 64, 512, dev, wl.q_pos, self.m, swa_cap=wl.meta["swa_cap"])
         self.V_sum = int(self.buf.n_visible.sum())
         self.e2e_in = [wl["Ca"], wl["Cb"], wl["Za"], wl["Zb"], wl["qI"], wl["w"], wl["q"]]
         self.e2e_out = [self.buf.out, self.buf.idx]
@@ -659,7 +659,10 @@ def _make(args, seq0=0):
 
 # ----------------------------------------------------------------------------- arms
 def _time_stages(wl, stream, reps):
-    """Each stage alone, `reps` times, CUDA events around every launch (median)."""
+    """Each stage alone, `reps` times, CUDA events around every launch (median).
+    A GPU spin of about a millisecond is queued before each timed stage, so the
+    stage's launches are already queued when its start event runs: the interval is
+    GPU time, not host launch overhead."""
     hbm, bf16, _, _ = _peaks()
     out = {}
     for name, fn, nbytes, flops in wl.stages():
@@ -667,6 +670,7 @@ def _time_stages(wl, stream, reps):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda.synchronize()
         for a, b in evs:
+            torch.cuda._sleep(2_000_000)
             a.record(stream)
             fn()
             b.record(stream)

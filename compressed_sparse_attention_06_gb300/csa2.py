@@ -64,7 +64,7 @@ def _declare(lib):
         "csa2_block_pool_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
-        "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i]),
+        "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i, _i64, _i64]),
         "csa2_sparse_attn_noalloc": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                           _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp]),
     }
@@ -285,8 +285,8 @@ def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
 
 
 def csa2_sparse_attn_workspace_bytes(B: int, Q: int, H: int, k: int, window: int,
-                                     device: Optional[int] = None) -> int:
-    return int(_lib().csa2_sparse_attn_workspace_bytes(ctx(device), B, Q, H, k, window))
+                                     device: Optional[int] = None, N: int = 0, swa_cap: int = 0) -> int:
+    return int(_lib().csa2_sparse_attn_workspace_bytes(ctx(device), B, Q, H, k, window, N, swa_cap))
 
 
 def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_pos0: int = 0,
@@ -308,7 +308,7 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
     if want_lse and lse is None:
         lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
     if ws is None:
-        nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k, window, q.device.index)
+        nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k, window, q.device.index, N=N, swa_cap=swa_cap)
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
     st = _lib().csa2_sparse_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(idx), k, _p(swa), swa_dt,
                                  swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,

@@ -359,9 +359,11 @@ size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int w
     return (size_t)B * Q * H * splits * PART * sizeof(float);
 }
 
-extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
-    if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0) return 0;
-    return std::max(attn_simt_ws_bytes(ctx, B, Q, H, k, window), attn_tc_ws_bytes(ctx, B, Q, H, k, window));
+extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N,
+                                                   int64_t swa_cap) {
+    if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0 || N < 0 || swa_cap < 0) return 0;
+    return std::max(attn_simt_ws_bytes(ctx, B, Q, H, k, window),
+                    attn_tc_ws_bytes(ctx, B, Q, H, k, window, N, swa_cap));
 }
 
 extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
@@ -410,7 +412,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     tc.out = out;
     tc.out_dt = out_dt;
     tc.lse = lse;
-    if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, H, k, window)) {
+    if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, H, k, window, 0, 0)) {
         int ns = 1;
         const csa2_status st = attn_tc_run(ctx, tc, ws, ws_bytes, s, &ns);
         if (st != CSA2_OK || ns <= 1) return st;

@@ -23,22 +23,22 @@
 // accumulation); key rows are exact.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over work items):
-//   warp 0     producer: the query image (one bulk copy) and the tile's bf16 rows
-//              (TMA gather of four rows per instruction, 128-byte swizzle)
+//   warp 0     producer: the query image of each work item (one 64 KB bulk copy)
 //   warp 1     MMA issuer; owns the tensor memory (O^T: columns 0-255, S^T: 256-319)
 //   warps 2-5  softmax: one thread per slot; then the output epilogue, one thread per
 //              output dim
-//   warps 6-9  loaders: FP4 rows dequantised into the tile, zero rows for empty slots,
-//              and every row's RMS factor
+//   warps 6-9  loaders, one thread per slot: bf16 rows gathered with 16-byte cp.async
+//              straight into the swizzled tile (one commit group per 128-dim block, so
+//              the next tile streams in while the current PV finishes), FP4 rows
+//              dequantised exactly into bf16, zero rows for empty slots, and each row's
+//              RMS factor (read from a table precomputed once per call when rows are
+//              gathered many times over, as in prefill)
 // Every wait is bounded; a wait that expires flags a timeout and the roles wind down.
-#include <cuda.h>
-
 #include <algorithm>
 #include <cstring>
 
 #include "attn_tc.cuh"
 #include "sm100_ptx.cuh"
-#include "tma_host.cuh"
 
 namespace {
 
@@ -73,6 +73,9 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 struct TcArgs {
     const uint8_t* qimg;          // [B*Q] query images
     const void* kv;               // bf16 [B, N, 512] or FP4 [B, N, 288]
+    const uint8_t* swa;           // bf16 [B, swa_cap, 512]
+    const float* rinv_kv;         // precomputed RMS factors of the bf16 rows, or NULL
+    const float* rinv_swa;        // precomputed RMS factors of the window rows, or NULL
     int64_t N;
     const int32_t* idx;           // [B*Q, k]
     int k;
@@ -162,37 +165,37 @@ __device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& ss) {
     }
 }
 
-// One FP4 row (256 code bytes, 32 E4M3 scales) into row r of the tile as bf16
-// (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits).
-// Returns the sum of squares of the dequantised values.
-__device__ __forceinline__ float fp4_row_to_tile(const uint8_t* kv, int64_t row, uint8_t* sK, int r) {
-    const uint4* src = reinterpret_cast<const uint4*>(kv + row * fp4_row_bytes(TC_C));
-    const uint4 sa = src[16], sb = src[17];
-    const uint32_t scw[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-    float ss = 0.0f;
-#pragma unroll 2
-    for (int c = 0; c < 8; ++c) {
-        const uint4 ca = src[2 * c], cb = src[2 * c + 1];
-        const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16 (exact:
+// an E2M1 value times an E4M3 scale has at most 6 significant bits).  ca, cb: the
+// chunk's 32 code bytes; scw: its four scale bytes.  Adds the squares to ss.
+__device__ __forceinline__ void fp4_chunk_to_tile(const uint4& ca, const uint4& cb, uint32_t scw, uint8_t* sK,
+                                                  int c, int r, float& ss) {
+    const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = c * 4 + (u >> 1);                  // 16-dim scale group
-            const float s = e4m3_to_f32((scw[j >> 2] >> (8 * (j & 3))) & 0xFFu);
-            float f[8];
-            e2m1x8_to_f32(cw[u], f);
-            uint32_t pk[4];
+    for (int u = 0; u < 8; ++u) {
+        const float s = e4m3_to_f32((scw >> (8 * (u >> 1))) & 0xFFu);
+        float f[8];
+        e2m1x8_to_f32(cw[u], f);
+        uint32_t pk[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x0 = f[2 * i] * s, x1 = f[2 * i + 1] * s;
-                ss = fmaf(x0, x0, ss);
-                ss = fmaf(x1, x1, ss);
-                pk[i] = pack_bf16x2(x0, x1);
-            }
-            *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = f[2 * i] * s, x1 = f[2 * i + 1] * s;
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+            pk[i] = pack_bf16x2(x0, x1);
         }
+        *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-    return ss;
 }
 
 // Normalised, rotated query of every (query, head) as the bf16 image of the MMA's
@@ -243,6 +246,19 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
     }
 }
 
+// RMS factor 1/sqrt(mean(x^2) + 1e-6) of every bf16 row of 512 values (a warp per row).
+__global__ void __launch_bounds__(256) attn_rownorm_kernel(const uint8_t* rows, int64_t n_rows, float* rinv) {
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= n_rows) return;
+    const uint4* p = reinterpret_cast<const uint4*>(rows + row * (int64_t)(TC_C * 2)) + 2 * lane;
+    float ss = 0.0f;
+    bf16x8_sumsq(p[0], ss);
+    bf16x8_sumsq(p[1], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) rinv[row] = 1.0f / sqrtf(ss / (float)TC_C + 1e-6f);
+}
+
 // Output of a query whose split holds no key slot: the sink alone (O = 0).
 template <typename TO>
 __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
@@ -267,9 +283,7 @@ __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
 }
 
 template <bool FP4, typename TO>
-__global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a,
-                                                                const __grid_constant__ CUtensorMap tm_kv,
-                                                                const __grid_constant__ CUtensorMap tm_swa) {
+__global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + OFF_Q;
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a,
         mbar_init(qfull, 1);
         mbar_init(qempty, 1);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&kfull[i], 1 + 4);
+            mbar_init(&kfull[i], 4);
             mbar_init(&kempty[i], 1);
         }
         mbar_init(rfull, 4);
@@ -317,73 +331,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a,
 
     if (warp == 0) {
         // ============================ producer ============================
-        int g = 0, qi = 0;
-        int issued_g[4] = {-1, -1, -1, -1};
-        int issued_q = -1;
-        bool ok = true;
-        for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
-            const ItemInfo it = item_info(a, item);
-            if (it.nt == 0) continue;
-            if (lane == 0) {
-                if (qi > 0 && !mbar_wait(qempty, (qi - 1) & 1, a.budget, a.st)) {
-                    ok = false;
-                } else {
-                    mbar_arrive_expect_tx(qfull, QIMG_BYTES);
-                    bulk_g2s(sQ, a.qimg + it.bq * (int64_t)QIMG_BYTES, QIMG_BYTES, qfull);
-                    issued_q = qi;
-                }
-            }
-            ok = __shfl_sync(FULL, ok, 0);
-            for (int tt = 0; tt < it.nt && ok; ++tt, ++g) {
-                const int slot0 = (it.t0 + tt) * TC_TILE + 4 * lane;
-                int kind[4];
-                int32_t row[4];
-                int ntma = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const SlotSrc s = slot_source(a, it, slot0 + i, false);
-                    const bool tma = s.kind == 2 || (s.kind == 1 && !FP4);
-                    kind[i] = tma ? s.kind : 0;
-                    row[i] = (int32_t)s.row;
-                    ntma += tma ? 1 : 0;
-                }
-                const int tot = __reduce_add_sync(FULL, ntma);
-                const bool all_kv = kind[0] == 1 && kind[1] == 1 && kind[2] == 1 && kind[3] == 1;
-                const bool all_sw = kind[0] == 2 && kind[1] == 2 && kind[2] == 2 && kind[3] == 2;
-                for (int db = 0; db < 4; ++db) {
-                    if (lane == 0) {
-                        if (g > 0 && !mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st)) {
-                            ok = false;
-                        } else {
-                            mbar_arrive_expect_tx(&kfull[db], (uint32_t)tot * 256u);
-                            issued_g[db] = g;
-                        }
-                    }
-                    ok = __shfl_sync(FULL, ok, 0);
-                    if (!ok) break;
-#pragma unroll
-                    for (int ch = 2 * db; ch < 2 * db + 2; ++ch) {
-                        uint8_t* dst = sK + ch * CHUNK_K + 4 * lane * 128;
-                        if (all_kv) {
-                            tma_gather4(dst, &tm_kv, ch * 64, row[0], row[1], row[2], row[3], &kfull[db]);
-                        } else if (all_sw) {
-                            tma_gather4(dst, &tm_swa, ch * 64, row[0], row[1], row[2], row[3], &kfull[db]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                if (kind[i] == 1) tma_load_2d(dst + i * 128, &tm_kv, ch * 64, row[i], &kfull[db]);
-                                else if (kind[i] == 2) tma_load_2d(dst + i * 128, &tm_swa, ch * 64, row[i], &kfull[db]);
-                            }
-                        }
-                    }
-                }
-            }
-            if (ok) ++qi;
-        }
-        // copies still in flight must land before the CTA exits
         if (lane == 0) {
-            for (int db = 0; db < 4; ++db)
-                if (issued_g[db] >= 0) mbar_wait(&kfull[db], issued_g[db] & 1, a.budget, a.st);
+            int qi = 0, issued_q = -1;
+            for (int64_t item = blockIdx.x; item < a.items; item += gridDim.x) {
+                const ItemInfo it = item_info(a, item);
+                if (it.nt == 0) continue;
+                if (qi > 0 && !mbar_wait(qempty, (qi - 1) & 1, a.budget, a.st)) break;
+                mbar_arrive_expect_tx(qfull, QIMG_BYTES);
+                bulk_g2s(sQ, a.qimg + it.bq * (int64_t)QIMG_BYTES, QIMG_BYTES, qfull);
+                issued_q = qi++;
+            }
+            // the last copy must land before the CTA exits
             if (issued_q >= 0) mbar_wait(qfull, issued_q & 1, a.budget, a.st);
         }
     } else if (warp == 1) {
@@ -640,54 +598,94 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a,
     } else {
         // ============================ loaders ============================
         const int r = threadIdx.x - 192;           // slot of the tile
+        const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv);
         int g = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
             const ItemInfo it = item_info(a, item);
             for (int tt = 0; tt < it.nt; ++tt, ++g) {
                 const SlotSrc s = slot_source(a, it, (it.t0 + tt) * TC_TILE + r, true);
-                const bool tma_row = s.kind == 2 || (s.kind == 1 && !FP4);
-                bool w = true;
-                if (g > 0)
-                    for (int db = 0; db < 4; ++db) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
-                if (!__all_sync(FULL, w)) {
-                    ok = false;
-                    break;
+                const bool bf_row = s.kind == 2 || (s.kind == 1 && !FP4);
+                const uint8_t* src = s.kind == 2 ? a.swa + s.row * (int64_t)(TC_C * 2)
+                                                 : (bf_row ? kvb + s.row * (int64_t)(TC_C * 2) : nullptr);
+                const float* pre = s.kind == 2 ? a.rinv_swa : (bf_row ? a.rinv_kv : nullptr);
+                const float rpre = (pre && s.kind != 0) ? pre[s.row] : 0.0f;
+                uint4 fc[16];
+                uint4 fs0 = make_uint4(0u, 0u, 0u, 0u), fs1 = fs0;
+                const bool fp4_row = FP4 && s.kind == 1;
+                if (fp4_row) {
+                    const uint4* p = reinterpret_cast<const uint4*>(kvb + s.row * fp4_row_bytes(TC_C));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) fc[i] = p[i];
+                    fs0 = p[16];
+                    fs1 = p[17];
                 }
                 float ss = 0.0f;
-                if (!tma_row) {
-                    if (s.kind == 1) {
-                        ss = fp4_row_to_tile(reinterpret_cast<const uint8_t*>(a.kv), s.row, sK, r);
-                    } else {
+                bool w = true;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-#pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    for (int db = 0; db < 4; ++db) mbar_arrive(&kfull[db]);
-                if (tma_row) {
-                    for (int db = 0; db < 4; ++db) w = w && mbar_wait(&kfull[db], g & 1, a.budget, a.st);
+                for (int db = 0; db < 4; ++db) {
+                    if (g > 0) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
                     if (w) {
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
+                        for (int ch = 2 * db; ch < 2 * db + 2; ++ch) {
+                            uint8_t* dst = sK + ch * CHUNK_K;
+                            if (bf_row) {
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                bf16x8_sumsq(*reinterpret_cast<const uint4*>(
-                                                 sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
-                                             ss);
+                                for (int u = 0; u < 8; ++u)
+                                    cp_async16(dst + sw128_offset((uint32_t)r, (uint32_t)u), src + ch * 128 + u * 16);
+                            } else if (fp4_row) {
+                                const uint32_t scw = (ch < 4) ? (ch == 0 ? fs0.x : ch == 1 ? fs0.y : ch == 2 ? fs0.z : fs0.w)
+                                                              : (ch == 4 ? fs1.x : ch == 5 ? fs1.y : ch == 6 ? fs1.z : fs1.w);
+                                fp4_chunk_to_tile(fc[2 * ch], fc[2 * ch + 1], scw, sK, ch, r, ss);
+                            } else {
+#pragma unroll
+                                for (int u = 0; u < 8; ++u)
+                                    *reinterpret_cast<uint4*>(dst + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                                        make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        }
                     }
+                    cp_async_commit();
                 }
+                // each 128-dim block is complete once its copy group has landed
+                cp_async_wait<3>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kfull[0]);
+                cp_async_wait<2>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kfull[1]);
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kfull[2]);
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kfull[3]);
                 if (!__all_sync(FULL, w)) {
                     ok = false;
                     break;
                 }
-                sRinv[r] = s.kind != 0 ? 1.0f / sqrtf(ss / (float)TC_C + 1e-6f) : 0.0f;
+                float rv = 0.0f;
+                if (s.kind != 0) {
+                    if (pre) {
+                        rv = rpre;
+                    } else {
+                        if (bf_row) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                                for (int u = 0; u < 8; ++u)
+                                    bf16x8_sumsq(*reinterpret_cast<const uint4*>(
+                                                     sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
+                                                 ss);
+                        }
+                        rv = 1.0f / sqrtf(ss / (float)TC_C + 1e-6f);
+                    }
+                }
+                sRinv[r] = rv;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rfull);
             }
@@ -708,9 +706,35 @@ void tc_splits(const csa2_ctx* ctx, int64_t n_bq, int k, int window, int& n_spli
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Precomputed RMS factors pay off when the call gathers each cache row many times
+// over (prefill: thousands of queries over one cache), not in decode.
+bool want_row_table(int64_t n_bq, int k, int window, int64_t rows) {
+    return rows > 0 && n_bq * (int64_t)(k + window) >= 4 * rows;
+}
+
+struct WsLayout {
+    size_t part, qimg, rinv_kv, rinv_swa, total;
+    int n_split, tps;
+    bool table;
+};
+
+WsLayout ws_layout(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap) {
+    WsLayout L;
+    const int64_t n_bq = (int64_t)B * Q;
+    tc_splits(ctx, n_bq, k, window, L.n_split, L.tps);
+    const int64_t kv_rows = (k > 0) ? (int64_t)B * std::max<int64_t>(N, 0) : 0;
+    const int64_t sw_rows = (window > 0) ? (int64_t)B * std::max<int64_t>(swa_cap, 0) : 0;
+    L.table = want_row_table(n_bq, k, window, kv_rows + sw_rows);
+    L.part = 0;
+    L.qimg = L.n_split > 1 ? align_up((size_t)n_bq * H * L.n_split * PART * sizeof(float), 1024) : 0;
+    L.rinv_kv = L.qimg + (size_t)n_bq * QIMG_BYTES;
+    L.rinv_swa = align_up(L.rinv_kv + (L.table ? (size_t)kv_rows * sizeof(float) : 0), 256);
+    L.total = L.rinv_swa + (L.table ? (size_t)sw_rows * sizeof(float) : 0);
+    return L;
+}
+
 template <bool FP4, typename TO>
-csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, const CUtensorMap& m_kv, const CUtensorMap& m_swa,
-                      cudaStream_t s) {
+csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, cudaStream_t s) {
     auto kern = attn_tc_kernel<FP4, TO>;
     static bool attr = false;
     if (!attr) {
@@ -719,7 +743,7 @@ csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, const CUtensorMap& m_kv, c
         attr = true;
     }
     const int64_t grid = std::min<int64_t>(a.items, ctx->num_sms);
-    kern<<<(unsigned)grid, TC_THREADS, SMEM_BYTES, s>>>(a, m_kv, m_swa);
+    kern<<<(unsigned)grid, TC_THREADS, SMEM_BYTES, s>>>(a);
     return csa2_launch_status();
 }
 
@@ -731,46 +755,50 @@ bool attn_tc_applies(const AttnTcCall& c) {
     if (c.window > 0 && c.swa_dt != CSA2_BF16) return false;
     if ((c.flags & (CSA2_QNORM | CSA2_KVNORM)) != (CSA2_QNORM | CSA2_KVNORM)) return false;
     if (c.H < 1 || c.H > TC_H) return false;
-    if (c.kv_dt == CSA2_BF16 && c.k > 0 && (int64_t)c.B * c.N > 0x7FFFFFFF) return false;   // map row coordinate
-    if (c.window > 0 && (int64_t)c.B * c.swa_cap > 0x7FFFFFFF) return false;
     return true;
 }
 
-size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window) {
+size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap) {
     if (!ctx || H < 1 || H > TC_H || B <= 0 || Q <= 0) return 0;
-    const int64_t n_bq = (int64_t)B * Q;
-    int ns = 1, tps = 1;
-    tc_splits(ctx, n_bq, k, window, ns, tps);
-    const size_t part = ns > 1 ? align_up((size_t)n_bq * H * ns * PART * sizeof(float), 1024) : 0;
-    return part + (size_t)n_bq * QIMG_BYTES;
+    return ws_layout(ctx, B, Q, H, k, window, N, swa_cap).total;
 }
 
 csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
                         int* n_split) {
     const int64_t n_bq = (int64_t)c.B * c.Q;
-    int ns = 1, tps = 1;
-    tc_splits(ctx, n_bq, c.k, c.window, ns, tps);
-    const size_t part = ns > 1 ? align_up((size_t)n_bq * c.H * ns * PART * sizeof(float), 1024) : 0;
-    if (!ws || ws_bytes < part + (size_t)n_bq * QIMG_BYTES || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
-    uint8_t* qimg = reinterpret_cast<uint8_t*>(ws) + part;
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    if (!ws || !aligned(ws, 16) || ws_bytes < L.rinv_kv) return CSA2_ERR_INVALID_ARG;
+    uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+    uint8_t* qimg = base + L.qimg;
     if (c.q_dt == CSA2_BF16)
         attn_qprep_kernel<__nv_bfloat16><<<(unsigned)n_bq, 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg);
     else
         attn_qprep_kernel<float><<<(unsigned)n_bq, 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
                                                                 c.rope, c.flags, qimg);
-    CUtensorMap m_kv, m_swa;
-    memset(&m_kv, 0, sizeof(m_kv));
-    memset(&m_swa, 0, sizeof(m_swa));
-    if (c.kv_dt == CSA2_BF16 && c.k > 0 && c.N > 0) {
-        if (!csa2_make_bf16_map(&m_kv, c.kv, (int64_t)c.B * c.N, TC_C, 64, 1)) return CSA2_ERR_CUDA;
-    }
-    if (c.window > 0) {
-        if (!csa2_make_bf16_map(&m_swa, c.swa, (int64_t)c.B * c.swa_cap, TC_C, 64, 1)) return CSA2_ERR_CUDA;
-    }
     TcArgs a;
+    a.rinv_kv = nullptr;
+    a.rinv_swa = nullptr;
+    if (L.table && ws_bytes >= L.total) {
+        const bool kv_bf = c.kv_dt == CSA2_BF16 && c.k > 0 && c.N > 0;
+        if (kv_bf) {
+            float* t = reinterpret_cast<float*>(base + L.rinv_kv);
+            const int64_t rows = (int64_t)c.B * c.N;
+            attn_rownorm_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const uint8_t*>(c.kv),
+                                                                          rows, t);
+            a.rinv_kv = t;
+        }
+        if (c.window > 0) {
+            float* t = reinterpret_cast<float*>(base + L.rinv_swa);
+            const int64_t rows = (int64_t)c.B * c.swa_cap;
+            attn_rownorm_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const uint8_t*>(c.swa),
+                                                                          rows, t);
+            a.rinv_swa = t;
+        }
+    }
     a.qimg = qimg;
     a.kv = c.kv;
+    a.swa = reinterpret_cast<const uint8_t*>(c.swa);
     a.N = c.N;
     a.idx = c.idx;
     a.k = c.k;
@@ -785,17 +813,15 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.flags = c.flags;
     a.out = c.out;
     a.lse = c.lse;
-    a.part = reinterpret_cast<float*>(ws);
-    a.n_split = ns;
-    a.tps = tps;
-    a.items = n_bq * ns;
+    a.part = reinterpret_cast<float*>(base + L.part);
+    a.n_split = L.n_split;
+    a.tps = L.tps;
+    a.items = n_bq * L.n_split;
     a.st = ctx->status;
     a.budget = WAIT_BUDGET;
-    *n_split = ns;
+    *n_split = L.n_split;
     const bool fp4 = c.kv_dt == CSA2_FP4_E4M3x16;
     const bool f32o = c.out_dt == CSA2_F32;
-    if (fp4) return f32o ? launch_tc<true, float>(ctx, a, m_kv, m_swa, s)
-                         : launch_tc<true, __nv_bfloat16>(ctx, a, m_kv, m_swa, s);
-    return f32o ? launch_tc<false, float>(ctx, a, m_kv, m_swa, s)
-                : launch_tc<false, __nv_bfloat16>(ctx, a, m_kv, m_swa, s);
+    if (fp4) return f32o ? launch_tc<true, float>(ctx, a, s) : launch_tc<true, __nv_bfloat16>(ctx, a, s);
+    return f32o ? launch_tc<false, float>(ctx, a, s) : launch_tc<false, __nv_bfloat16>(ctx, a, s);
 }

@@ -31,9 +31,11 @@ struct AttnTcCall {
 // Whether the tensor-core path handles these dtypes, flags and sizes.
 bool attn_tc_applies(const AttnTcCall& c);
 
-// Workspace bytes the tensor-core path needs for these sizes (query images plus,
-// when the keys are split, the per-split partials), or 0 when H > 64.
-size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window);
+// Workspace bytes the tensor-core path uses for these sizes: per-split partials
+// (when the keys are split), the query images, and, when the call gathers each
+// row many times over, the rows' RMS factors (B*N + B*swa_cap floats); 0 when H > 64.
+// The path runs with any workspace that holds the partials and the images.
+size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap);
 
 // Workspace bytes of the CUDA-core path (attn.cu) for these sizes: its key-split
 // partials, 0 when it runs unsplit.

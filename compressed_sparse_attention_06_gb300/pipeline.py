@@ -52,7 +52,8 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
         idx=torch.empty((B, Q, k), dtype=torch.int32, device=device),
         out=torch.empty((B, Q, H, c), dtype=out_dtype, device=device),
         attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
-                                                                       torch.device(device).index)),
+                                                                       torch.device(device).index, N=N,
+                                                                       swa_cap=window)),
                             dtype=torch.uint8, device=device),
         pool_ws=C._ws(C.csa2_block_pool_workspace_bytes(B * Q, nb, n_keep, torch.device(device).index), device),
         topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_keep * block, k, torch.device(device).index), device),
@@ -110,14 +111,17 @@ class PrefillBuffers:
 
 
 def alloc_prefill(Q: int, N: int, H: int, c: int, device, q_pos: torch.Tensor, m: int,
-                  out_dtype=torch.bfloat16, k: int = TOPK, window: int = 128) -> PrefillBuffers:
+                  out_dtype=torch.bfloat16, k: int = TOPK, window: int = 128, swa_cap: int = 0) -> PrefillBuffers:
+    """swa_cap: rows of the window buffer the attention will read (sizes the workspace
+    for the per-call table of row RMS factors)."""
     return PrefillBuffers(
         scores=torch.empty((1, Q, N), dtype=torch.float32, device=device),
         idx=torch.empty((1, Q, k), dtype=torch.int32, device=device),
         out=torch.empty((1, Q, H, c), dtype=out_dtype, device=device),
         n_visible=visible_entries(q_pos, m),
         attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(1, Q, H, k, window,
-                                                                       torch.device(device).index)),
+                                                                       torch.device(device).index, N=N,
+                                                                       swa_cap=swa_cap)),
                             dtype=torch.uint8, device=device),
         topk_ws=C._ws(C.csa2_topk_workspace_bytes(Q, N, k, torch.device(device).index), device),
     )

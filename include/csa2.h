@@ -237,14 +237,18 @@ size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, 
  * works in fp32 throughout.
  *
  * Workspace (caller-owned device memory, 16-byte aligned): the tensor-core path keeps
- * each query's prepared bf16 image there (64 KB per query) and, with few queries,
- * the per-split partial results of its key split; the CUDA-core path keeps only its
- * key-split partials.  csa2_sparse_attn_workspace_bytes() gives the size that
- * enables both; with less, the call falls back to the CUDA-core path with as many
- * splits as fit (NULL: no split).  Calls that share a workspace must not overlap on
- * the GPU.
+ * each query's prepared bf16 image there (64 KB per query), with few queries the
+ * per-split partial results of its key split, and, when the call gathers each row
+ * many times over (B*Q*(k+window) >= 4*(B*N + B*swa_cap), as in prefill), the rows'
+ * RMS factors computed once per call; the CUDA-core path keeps only its key-split
+ * partials.  csa2_sparse_attn_workspace_bytes(), given the same N and swa_cap as the
+ * call, returns the size that enables all of it; the tensor-core path runs without
+ * the factor table when only it is missing, and with less than the images and
+ * partials the call falls back to the CUDA-core path with as many splits as fit
+ * (NULL: no split).  Calls that share a workspace must not overlap on the GPU.
  */
-size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window);
+size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N,
+                                        int64_t swa_cap);
 csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              const void* q, csa2_dtype q_dt,
                              const void* kv, csa2_dtype kv_dt, int64_t N,
