@@ -198,26 +198,53 @@ __device__ __forceinline__ void fp4_chunk_to_tile(const uint4& ca, const uint4& 
     }
 }
 
+template <typename TQ>
+__device__ __forceinline__ void load16(const TQ* src, float (&v)[16]);
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* src, float (&v)[16]) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint4 u = p[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+}
+template <>
+__device__ __forceinline__ void load16<float>(const float* src, float (&v)[16]) {
+    const float4* p = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 u = p[i];
+        v[4 * i] = u.x;
+        v[4 * i + 1] = u.y;
+        v[4 * i + 2] = u.z;
+        v[4 * i + 3] = u.w;
+    }
+}
+
 // Normalised, rotated query of every (query, head) as the bf16 image of the MMA's
 // B operand: 8 chunks of [64 heads x 64 dims], 128-byte swizzled; heads >= H are 0.
+// A CTA per (8 heads, query), a warp per head, 16 dims per lane.
 template <typename TQ>
 __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, RopeTable rope,
                                                          unsigned flags, uint8_t* qimg) {
     __shared__ float cs[32], sn[32];
-    const int64_t bq = blockIdx.x;
+    const int64_t bq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x < 32) rope_cos_sin(rope, q_pos[bq], threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
     __syncthreads();
     uint8_t* img = qimg + bq * (int64_t)QIMG_BYTES;
-    for (int h = warp; h < TC_H; h += 8) {
+    {
+        const int h = blockIdx.x * 8 + warp;
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-        if (h < H) {
-            const TQ* src = q + ((bq * H + h) * (int64_t)TC_C + 16 * lane);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = to_f32<TQ>(src[i]);
-        }
+        if (h < H) load16<TQ>(q + ((bq * H + h) * (int64_t)TC_C + 16 * lane), v);
         if (flags & CSA2_QNORM) {
             float ss = 0.0f;
 #pragma unroll
@@ -554,25 +581,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
             float scv[TC_H];
 #pragma unroll
             for (int h = 0; h < TC_H; ++h) scv[h] = __shfl_sync(FULL, sc2[h >> 5], h & 31);
+            // one base pointer per query; head h is a constant offset from it
+            TO* obase = reinterpret_cast<TO*>(a.out) + it.bq * a.H * (int64_t)TC_C + r;
+            float* pbase = a.part + ((it.bq * a.H) * a.n_split + it.split) * (int64_t)PART + 2 + r;
+            const int64_t pstride = (int64_t)a.n_split * PART;
             for (int db = 0; db < 4; ++db) {
                 uint32_t o0[32], o1[32];
                 tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H, o0);
                 tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H + 32, o1);
                 tmem_wait_ld();
-                const int d = db * 128 + r;
+                if (split) {
+                    float* pb = pbase + db * 128;
 #pragma unroll
-                for (int h = 0; h < TC_H; ++h) {
-                    float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]);
-                    if (split) {
-                        if (h < a.H) a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + 2 + d] = v;
-                    } else {
-                        v *= scv[h];
-                        if (db == 3 && rot) {
+                    for (int h = 0; h < TC_H; ++h) {
+                        if (h < a.H) pb[h * pstride] = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]);
+                    }
+                } else {
+                    TO* ob = obase + db * 128;
+                    const bool rot_here = db == 3 && rot;
+#pragma unroll
+                    for (int h = 0; h < TC_H; ++h) {
+                        float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]) * scv[h];
+                        if (rot_here) {
                             const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
                             v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
                         }
-                        if (h < a.H)
-                            reinterpret_cast<TO*>(a.out)[(it.bq * a.H + h) * (int64_t)TC_C + d] = from_f32<TO>(v);
+                        if (h < a.H) ob[h * TC_C] = from_f32<TO>(v);
                     }
                 }
             }
@@ -620,27 +654,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     fs0 = p[16];
                     fs1 = p[17];
                 }
+                // bf16 rows are copied cooperatively: per instruction the warp moves two of
+                // its 32 rows, 256 contiguous bytes each (16 lanes x 16 B per row)
+                const int wl = r >> 5, half = lane >> 4, piece = lane & 15;
+                const uint8_t* srcj[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint64_t p = __shfl_sync(FULL, (uint64_t)(uintptr_t)(bf_row ? src : nullptr), 2 * j + half);
+                    srcj[j] = reinterpret_cast<const uint8_t*>((uintptr_t)p);
+                }
                 float ss = 0.0f;
                 bool w = true;
 #pragma unroll
                 for (int db = 0; db < 4; ++db) {
                     if (g > 0) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
                     if (w) {
+                        const int ch = 2 * db + (piece >> 3), u = piece & 7;
 #pragma unroll
-                        for (int ch = 2 * db; ch < 2 * db + 2; ++ch) {
-                            uint8_t* dst = sK + ch * CHUNK_K;
-                            if (bf_row) {
+                        for (int j = 0; j < 16; ++j) {
+                            if (srcj[j])
+                                cp_async16(sK + ch * CHUNK_K + sw128_offset((uint32_t)(32 * wl + 2 * j + half), (uint32_t)u),
+                                           srcj[j] + ch * 128 + u * 16);
+                        }
 #pragma unroll
-                                for (int u = 0; u < 8; ++u)
-                                    cp_async16(dst + sw128_offset((uint32_t)r, (uint32_t)u), src + ch * 128 + u * 16);
-                            } else if (fp4_row) {
-                                const uint32_t scw = (ch < 4) ? (ch == 0 ? fs0.x : ch == 1 ? fs0.y : ch == 2 ? fs0.z : fs0.w)
-                                                              : (ch == 4 ? fs1.x : ch == 5 ? fs1.y : ch == 6 ? fs1.z : fs1.w);
-                                fp4_chunk_to_tile(fc[2 * ch], fc[2 * ch + 1], scw, sK, ch, r, ss);
-                            } else {
+                        for (int c2 = 2 * db; c2 < 2 * db + 2; ++c2) {
+                            if (fp4_row) {
+                                const uint32_t scw = (c2 < 4) ? (c2 == 0 ? fs0.x : c2 == 1 ? fs0.y : c2 == 2 ? fs0.z : fs0.w)
+                                                              : (c2 == 4 ? fs1.x : c2 == 5 ? fs1.y : c2 == 6 ? fs1.z : fs1.w);
+                                fp4_chunk_to_tile(fc[2 * c2], fc[2 * c2 + 1], scw, sK, c2, r, ss);
+                            } else if (!bf_row) {
 #pragma unroll
-                                for (int u = 0; u < 8; ++u)
-                                    *reinterpret_cast<uint4*>(dst + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                                for (int u2 = 0; u2 < 8; ++u2)
+                                    *reinterpret_cast<uint4*>(sK + c2 * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u2)) =
                                         make_uint4(0u, 0u, 0u, 0u);
                             }
                         }
@@ -771,10 +816,10 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     uint8_t* qimg = base + L.qimg;
     if (c.q_dt == CSA2_BF16)
-        attn_qprep_kernel<__nv_bfloat16><<<(unsigned)n_bq, 256, 0, s>>>(
+        attn_qprep_kernel<__nv_bfloat16><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(
             reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg);
     else
-        attn_qprep_kernel<float><<<(unsigned)n_bq, 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
+        attn_qprep_kernel<float><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
                                                                 c.rope, c.flags, qimg);
     TcArgs a;
     a.rinv_kv = nullptr;

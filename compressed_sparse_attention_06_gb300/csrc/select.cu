@@ -144,9 +144,22 @@ __device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, SelShared& s
     return r;
 }
 
-// Histogram of digit (key >> shift) & dmask over the active keys (valid, and equal to
-// `prefix` on the bits of `pmask`).  A warp whose active lanes share one digit adds
+// Count digit d of every active lane: a warp whose active lanes share one digit adds
 // once; otherwise each active lane adds its own (shared-memory atomics).
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t d, bool act) {
+    const unsigned am = __ballot_sync(FULL_MASK, act);
+    if (am == 0u) return;
+    const int leader = __ffs(am) - 1;
+    const uint32_t d0 = __shfl_sync(FULL_MASK, d, leader);
+    if (__all_sync(FULL_MASK, !act || d == d0)) {
+        if ((int)(threadIdx.x & 31) == leader) atomicAdd(&hist[d0], (uint32_t)__popc(am));
+    } else if (act) {
+        atomicAdd(&hist[d], 1u);
+    }
+}
+
+// Histogram of digit (key >> shift) & dmask over the active keys (valid, and equal to
+// `prefix` on the bits of `pmask`).
 template <class KeyAt>
 __device__ __forceinline__ void hist_pass(KeyAt key_at, int64_t n, uint32_t prefix, uint32_t pmask, int shift,
                                           uint32_t dmask, uint32_t* hist, int* nvalid) {
@@ -157,16 +170,7 @@ __device__ __forceinline__ void hist_pass(KeyAt key_at, int64_t n, uint32_t pref
         const uint32_t key = e < n ? key_at(e) : 0u;
         local_valid += key != 0u;
         const bool act = key != 0u && (key & pmask) == prefix;
-        const unsigned am = __ballot_sync(FULL_MASK, act);
-        if (am == 0u) continue;
-        const uint32_t d = (key >> shift) & dmask;
-        const int leader = __ffs(am) - 1;
-        const uint32_t d0 = __shfl_sync(FULL_MASK, d, leader);
-        if (__all_sync(FULL_MASK, !act || d == d0)) {
-            if (lane == leader) atomicAdd(&hist[d0], (uint32_t)__popc(am));
-        } else if (act) {
-            atomicAdd(&hist[d], 1u);
-        }
+        hist_add_warp(hist, (key >> shift) & dmask, act);
     }
     if (nvalid) {
         const int w = __reduce_add_sync(FULL_MASK, local_valid);
@@ -342,6 +346,157 @@ __device__ int block_ordered_emit(KeyAt key_at, int64_t n, const SelState& r, in
     return min(total, k);
 }
 
+constexpr int BM_WORDS = SEL_SMEM_CAP / 32;     // bitmap words for a staged row
+constexpr int CAND64_CAP = CAND_CAP / 2;        // (key, index) pairs in the candidate buffer
+
+// Selection over keys staged in shared memory, whose 12-bit histogram (sh.hist) and
+// valid count were built while staging and exceed k.  The threshold bin b is found
+// from the histogram; keys above b are winners outright, the keys of b (at most
+// CAND64_CAP) are copied with their index and two 10-bit histograms over the copy
+// give the exact threshold key T and how many ties at T are taken.  Winners and ties
+// are marked in two bitmaps (bmW, bmE: zeroed by the caller), and one ordered scan of
+// the bitmaps emits the winners in element order, the lowest-index ties first.
+// Returns -1 (nothing emitted) if bin b holds more than CAND64_CAP keys.
+template <class Emit>
+__device__ int staged_select(const uint32_t* skey, int n, int k, SelShared& sh, uint64_t* cand, uint32_t* bmW,
+                             uint32_t* bmE, Emit emit) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    find_bin(sh.hist, NB_A, (uint32_t)k, sh);
+    const uint32_t b = (uint32_t)sh.bin;
+    uint32_t remaining = (uint32_t)k - sh.above;
+    const uint32_t m = sh.hist[b];
+    if (tid == 0) sh.cand_n = 0;
+    __syncthreads();
+    if (m > (uint32_t)CAND64_CAP) return -1;
+    // classify: whole words of 32 elements per warp step
+    const int nwords = (n + 31) / 32;
+    for (int w = warp; w < nwords; w += nwarps) {
+        const int i = w * 32 + lane;
+        const uint32_t key = i < n ? skey[i] : 0u;
+        const uint32_t d = key >> 20;
+        const bool gt = key != 0u && d > b, eq = key != 0u && d == b;
+        const unsigned bg = __ballot_sync(FULL_MASK, gt);
+        if (lane == 0) bmW[w] = bg;
+        const unsigned be = __ballot_sync(FULL_MASK, eq);
+        if (be) {
+            const int leader = __ffs(be) - 1;
+            int off = 0;
+            if (lane == leader) off = atomicAdd(&sh.cand_n, __popc(be));
+            off = __shfl_sync(FULL_MASK, off, leader);
+            if (eq) cand[off + __popc(be & lt)] = ((uint64_t)key << 32) | (uint32_t)i;
+        }
+    }
+    __syncthreads();
+    // the low 20 bits of T among the bin's keys
+    auto cand_key = [&](int64_t j) -> uint32_t { return (uint32_t)(cand[j] >> 32); };
+    uint32_t prefix = b << 20, pmask = 0xFFF00000u;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        for (int i = tid; i < NB_B; i += blockDim.x) sh.hist[i] = 0;
+        __syncthreads();
+        hist_pass(cand_key, (int64_t)m, prefix, pmask, shift, 0x3FFu, sh.hist, nullptr);
+        __syncthreads();
+        find_bin(sh.hist, NB_B, remaining, sh);
+        prefix |= (uint32_t)sh.bin << shift;
+        pmask |= 0x3FFu << shift;
+        remaining -= sh.above;
+        __syncthreads();
+    }
+    const uint32_t T = prefix;
+    for (int j = tid; j < (int)m; j += blockDim.x) {
+        const uint64_t c = cand[j];
+        const uint32_t key = (uint32_t)(c >> 32), i = (uint32_t)c;
+        if (key > T) atomicOr(&bmW[i >> 5], 1u << (i & 31));
+        else if (key == T) atomicOr(&bmE[i >> 5], 1u << (i & 31));
+    }
+    __syncthreads();
+    // ordered emission: thread t owns a run of consecutive words
+    const int per = (nwords + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    uint32_t cg = 0, ce = 0;
+    for (int w = w0; w < w1; ++w) {
+        cg += __popc(bmW[w]);
+        ce += __popc(bmE[w]);
+    }
+    uint32_t tot;
+    uint32_t gb = block_excl_scan_u32(cg, sh, tot);
+    uint32_t eb = block_excl_scan_u32(ce, sh, tot);
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t wg = bmW[w], we = bmE[w];
+        uint32_t bits = wg | we;
+        while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int i = w * 32 + j;
+            if ((wg >> j) & 1u) {
+                emit((int64_t)i, (int)(gb + min(eb, remaining)), skey[i]);
+                ++gb;
+            } else {
+                if (eb < remaining) emit((int64_t)i, (int)(gb + eb), skey[i]);
+                ++eb;
+            }
+        }
+    }
+    __syncthreads();
+    return k;
+}
+
+// Stage n keys from load(i) into skey while building their 12-bit histogram and
+// valid count (eight loads in flight per thread); also zeroes the bitmaps.
+template <class Load>
+__device__ void stage_keys(Load load, int n, uint32_t* skey, SelShared& sh, uint32_t* bmW, uint32_t* bmE) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < NB_A; i += blockDim.x) sh.hist[i] = 0;
+    for (int i = tid; i < (n + 31) / 32; i += blockDim.x) {
+        bmW[i] = 0u;
+        bmE[i] = 0u;
+    }
+    if (tid == 0) {
+        sh.nvalid = 0;
+        sh.cand_n = 0;
+    }
+    __syncthreads();
+    int local_valid = 0;
+    for (int base = 0; base < n; base += (int)blockDim.x * 8) {
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = base + j * (int)blockDim.x + tid;
+            v[j] = i < n ? load(i) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = base + j * (int)blockDim.x + tid;
+            if (i < n) skey[i] = v[j];
+            local_valid += v[j] != 0u;
+            hist_add_warp(sh.hist, v[j] >> 20, v[j] != 0u);
+        }
+    }
+    const int w = __reduce_add_sync(FULL_MASK, local_valid);
+    if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
+    __syncthreads();
+}
+
+// Staged keys -> winners in element order through emit(i, pos, key); returns the
+// number emitted (min(valid, k)).
+template <class Emit>
+__device__ int select_staged_row(const uint32_t* skey, int n, int k, SelShared& sh, uint32_t* cand32,
+                                 uint32_t* bmW, uint32_t* bmE, Emit emit) {
+    auto key_at = [&](int64_t i) -> uint32_t { return skey[i]; };
+    if (sh.nvalid <= k) {
+        SelState r;
+        r.T = 0;
+        r.remaining = 0;
+        r.take_all = true;
+        return block_ordered_emit(key_at, (int64_t)n, r, k, sh, emit);
+    }
+    const int f = staged_select(skey, n, k, sh, reinterpret_cast<uint64_t*>(cand32), bmW, bmE, emit);
+    if (f >= 0) return f;
+    const SelState r = block_radix_select(key_at, (int64_t)n, k, sh, cand32);
+    return block_ordered_emit(key_at, (int64_t)n, r, k, sh, emit);
+}
+
 template <int MODE>
 __device__ void finish_row(const SelArgs& a, int64_t row, int filled, int64_t n_elems) {
     if (MODE == SEL_POOL && n_elems > 0) {
@@ -367,21 +522,32 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_chunk_kernel(SelArgs a) {
     const int64_t c1 = min(n_elems, c0 + a.chunk_len);
     const int64_t n = max((int64_t)0, c1 - c0);
     if (SMEM) {
-        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) skey[i] = key_of<MODE>(a, row, c0 + i, V, n_elems);
-        __syncthreads();
-    }
-    auto key_at = [&](int64_t i) -> uint32_t { return SMEM ? skey[i] : key_of<MODE>(a, row, c0 + i, V, n_elems); };
-    uint32_t* cand = skey + (SMEM ? a.chunk_len : 0);
-    const SelState r = block_radix_select(key_at, n, a.k, sh, cand);
-    if (a.chunks > 1) {
-        const int64_t base = (row * a.chunks + chunk) * (int64_t)a.k;
-        const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
-            a.ws_key[base + pos] = key;
-            a.ws_id[base + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+        __shared__ uint32_t bmW[BM_WORDS], bmE[BM_WORDS];
+        uint32_t* cand = skey + ((a.chunk_len + 1) & ~(int64_t)1);
+        stage_keys([&](int i) -> uint32_t { return key_of<MODE>(a, row, c0 + i, V, n_elems); }, (int)n, skey, sh,
+                   bmW, bmE);
+        if (a.chunks > 1) {
+            const int64_t base = (row * a.chunks + chunk) * (int64_t)a.k;
+            const int filled = select_staged_row(skey, (int)n, a.k, sh, cand, bmW, bmE,
+                                                 [&](int64_t i, int pos, uint32_t key) {
+                a.ws_key[base + pos] = key;
+                a.ws_id[base + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+            });
+            for (int i = filled + threadIdx.x; i < a.k; i += blockDim.x) a.ws_key[base + i] = 0u;
+            return;
+        }
+        const int filled = select_staged_row(skey, (int)n, a.k, sh, cand, bmW, bmE,
+                                             [&](int64_t i, int pos, uint32_t key) {
+            a.out_idx[row * a.out_len + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+            if (a.out_val) a.out_val[row * a.out_len + pos] = a.vals[row * a.ld + c0 + i];
         });
-        for (int i = filled + threadIdx.x; i < a.k; i += blockDim.x) a.ws_key[base + i] = 0u;
+        finish_row<MODE>(a, row, filled, n_elems);
         return;
     }
+    // long row without a workspace: every pass reads global memory
+    auto key_at = [&](int64_t i) -> uint32_t { return key_of<MODE>(a, row, c0 + i, V, n_elems); };
+    uint32_t* cand = skey;
+    const SelState r = block_radix_select(key_at, n, a.k, sh, cand);
     const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
         a.out_idx[row * a.out_len + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
         if (a.out_val) a.out_val[row * a.out_len + pos] = a.vals[row * a.ld + c0 + i];
@@ -398,13 +564,12 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_merge_kernel(SelArgs a) {
     const int64_t row = blockIdx.x;
     const int64_t V = a.nv[row];
     const int64_t n_elems = row_elems<MODE>(a, V);
-    const int64_t n = (int64_t)a.chunks * a.k;
-    const int64_t base = row * n;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) skey[i] = a.ws_key[base + i];
-    __syncthreads();
-    auto key_at = [&](int64_t i) -> uint32_t { return skey[i]; };
-    const SelState r = block_radix_select(key_at, n, a.k, sh, skey + n);
-    const int filled = block_ordered_emit(key_at, n, r, a.k, sh, [&](int64_t i, int pos, uint32_t key) {
+    const int n = a.chunks * a.k;
+    const int64_t base = row * (int64_t)n;
+    __shared__ uint32_t bmW[BM_WORDS], bmE[BM_WORDS];
+    uint32_t* cand = skey + ((n + 1) & ~1);
+    stage_keys([&](int i) -> uint32_t { return a.ws_key[base + i]; }, n, skey, sh, bmW, bmE);
+    const int filled = select_staged_row(skey, n, a.k, sh, cand, bmW, bmE, [&](int64_t i, int pos, uint32_t key) {
         a.out_idx[row * a.out_len + pos] = a.ws_id[base + i];
         if (a.out_val) a.out_val[row * a.out_len + pos] = key_to_float(key);
     });
@@ -449,7 +614,7 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
     }
     static bool attr = false;
     if (!attr) {
-        const int bytes = (SEL_SMEM_CAP + CAND_CAP) * (int)sizeof(uint32_t);
+        const int bytes = (SEL_SMEM_CAP + 2 + CAND_CAP) * (int)sizeof(uint32_t);
         if (cudaFuncSetAttribute(sel_chunk_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(sel_chunk_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -461,12 +626,13 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
     }
     dim3 grid((unsigned)a.chunks, (unsigned)rows);
     if (smem)
-        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, (a.chunk_len + CAND_CAP) * sizeof(uint32_t), s>>>(a);
+        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, (((a.chunk_len + 1) & ~(int64_t)1) + CAND_CAP) *
+                                                                   sizeof(uint32_t), s>>>(a);
     else
         sel_chunk_kernel<MODE, false><<<grid, SEL_THREADS, CAND_CAP * sizeof(uint32_t), s>>>(a);
     if (a.chunks > 1)
-        sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS, ((size_t)a.chunks * a.k + CAND_CAP) * sizeof(uint32_t),
-                                 s>>>(a);
+        sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS,
+                                 ((((size_t)a.chunks * a.k) + 1) / 2 * 2 + CAND_CAP) * sizeof(uint32_t), s>>>(a);
     return csa2_launch_status();
 }
 
