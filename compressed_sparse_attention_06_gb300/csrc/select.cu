@@ -347,6 +347,32 @@ __device__ int block_ordered_emit(KeyAt key_at, int64_t n, const SelState& r, in
 }
 
 constexpr int BM_WORDS = SEL_SMEM_CAP / 32;     // bitmap words for a staged row
+
+// Keys staged in shared memory (zero-padded to whole words of 32).
+struct SmemKeys {
+    const uint32_t* skey;
+    __device__ __forceinline__ uint4 piece(int w, int q) const {
+        return reinterpret_cast<const uint4*>(skey)[w * 8 + q];
+    }
+    __device__ __forceinline__ uint32_t key(int i) const { return skey[i]; }
+};
+
+// Keys computed on the fly from one row of scores in global memory (16-byte
+// aligned): element i < V (and < n) is visible.
+struct RowScores {
+    const float* rowp;
+    int n, V;
+    __device__ __forceinline__ uint32_t key(int i) const { return (i < V && i < n) ? order_key(rowp[i]) : 0u; }
+    __device__ __forceinline__ uint4 piece(int w, int q) const {
+        const int e = 32 * w + 4 * q;
+        const int lim = min(n, V);
+        if (e + 3 < lim) {
+            const float4 f = reinterpret_cast<const float4*>(rowp)[e >> 2];
+            return make_uint4(order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w));
+        }
+        return make_uint4(key(e), key(e + 1), key(e + 2), key(e + 3));
+    }
+};
 constexpr int CAND64_CAP = CAND_CAP / 2;        // (key, index) pairs in the candidate buffer
 
 // Selection over keys staged in shared memory, whose 12-bit histogram (sh.hist) and
@@ -357,11 +383,10 @@ constexpr int CAND64_CAP = CAND_CAP / 2;        // (key, index) pairs in the can
 // are marked in two bitmaps (bmW, bmE: zeroed by the caller), and one ordered scan of
 // the bitmaps emits the winners in element order, the lowest-index ties first.
 // Returns -1 (nothing emitted) if bin b holds more than CAND64_CAP keys.
-template <class Emit>
-__device__ int staged_select(const uint32_t* skey, int n, int k, SelShared& sh, uint64_t* cand, uint32_t* bmW,
+template <class Src, class Emit>
+__device__ int staged_select(const Src src, int n, int k, SelShared& sh, uint64_t* cand, uint32_t* bmW,
                              uint32_t* bmE, Emit emit) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const unsigned lt = (1u << lane) - 1u;
+    const int tid = threadIdx.x;
     find_bin(sh.hist, NB_A, (uint32_t)k, sh);
     const uint32_t b = (uint32_t)sh.bin;
     uint32_t remaining = (uint32_t)k - sh.above;
@@ -369,22 +394,44 @@ __device__ int staged_select(const uint32_t* skey, int n, int k, SelShared& sh, 
     if (tid == 0) sh.cand_n = 0;
     __syncthreads();
     if (m > (uint32_t)CAND64_CAP) return -1;
-    // classify: whole words of 32 elements per warp step
+    // classify: a thread per word of 32 keys (bit j of word w = key 32w + j), read as
+    // eight 16-byte pieces starting at a lane-dependent piece so that the lanes of a
+    // warp spread over the banks; skey is padded with zeros to a whole word
     const int nwords = (n + 31) / 32;
-    for (int w = warp; w < nwords; w += nwarps) {
-        const int i = w * 32 + lane;
-        const uint32_t key = i < n ? skey[i] : 0u;
-        const uint32_t d = key >> 20;
-        const bool gt = key != 0u && d > b, eq = key != 0u && d == b;
-        const unsigned bg = __ballot_sync(FULL_MASK, gt);
-        if (lane == 0) bmW[w] = bg;
-        const unsigned be = __ballot_sync(FULL_MASK, eq);
-        if (be) {
-            const int leader = __ffs(be) - 1;
-            int off = 0;
-            if (lane == leader) off = atomicAdd(&sh.cand_n, __popc(be));
-            off = __shfl_sync(FULL_MASK, off, leader);
-            if (eq) cand[off + __popc(be & lt)] = ((uint64_t)key << 32) | (uint32_t)i;
+    const int lane = tid & 31;
+    for (int w0 = 0; w0 < nwords; w0 += blockDim.x) {
+        const int w = w0 + tid;
+        uint32_t mgt = 0u, meq = 0u;
+        if (w < nwords) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int q = (t + w) & 7;
+                const uint4 k4 = src.piece(w, q);
+                const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t key = kk[c], d = key >> 20;
+                    if (key != 0u && d > b) mgt |= 1u << (4 * q + c);
+                    if (key != 0u && d == b) meq |= 1u << (4 * q + c);
+                }
+            }
+            bmW[w] = mgt;
+        }
+        // the bin's keys go to cand: one atomic per warp, offsets by a warp scan
+        const int cnt = __popc(meq);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int base = 0;
+        if (lane == 31 && incl) base = atomicAdd(&sh.cand_n, incl);
+        base = __shfl_sync(FULL_MASK, base, 31) + incl - cnt;
+        while (meq) {
+            const int j = __ffs(meq) - 1;
+            meq &= meq - 1;
+            cand[base++] = ((uint64_t)src.key(w * 32 + j) << 32) | (uint32_t)(w * 32 + j);
         }
     }
     __syncthreads();
@@ -430,10 +477,10 @@ __device__ int staged_select(const uint32_t* skey, int n, int k, SelShared& sh, 
             bits &= bits - 1;
             const int i = w * 32 + j;
             if ((wg >> j) & 1u) {
-                emit((int64_t)i, (int)(gb + min(eb, remaining)), skey[i]);
+                emit((int64_t)i, (int)(gb + min(eb, remaining)), src.key(i));
                 ++gb;
             } else {
-                if (eb < remaining) emit((int64_t)i, (int)(gb + eb), skey[i]);
+                if (eb < remaining) emit((int64_t)i, (int)(gb + eb), src.key(i));
                 ++eb;
             }
         }
@@ -473,6 +520,65 @@ __device__ void stage_keys(Load load, int n, uint32_t* skey, SelShared& sh, uint
             hist_add_warp(sh.hist, v[j] >> 20, v[j] != 0u);
         }
     }
+    for (int i = n + tid; i < (n + 31) / 32 * 32; i += blockDim.x) skey[i] = 0u;
+    const int w = __reduce_add_sync(FULL_MASK, local_valid);
+    if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
+    __syncthreads();
+}
+
+// Full-row top-k staging: scores[0..n) of one row, visible below V, into skey as keys,
+// with their 12-bit histogram and valid count (16-byte loads and stores when the row
+// is 16-byte aligned; spread scores, so the histogram takes plain atomics).
+__device__ void stage_scores(const float* rowp, int n, int V, uint32_t* skey, SelShared& sh, uint32_t* bmW,
+                             uint32_t* bmE) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < NB_A; i += blockDim.x) sh.hist[i] = 0;
+    for (int i = tid; i < (n + 31) / 32; i += blockDim.x) {
+        bmW[i] = 0u;
+        bmE[i] = 0u;
+    }
+    if (tid == 0) {
+        sh.nvalid = 0;
+        sh.cand_n = 0;
+    }
+    __syncthreads();
+    int local_valid = 0;
+    const bool vec = (reinterpret_cast<uintptr_t>(rowp) & 15u) == 0;
+    const int nq = vec ? n / 4 : 0;
+    for (int base = 0; base < nq; base += (int)blockDim.x * 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = base + j * (int)blockDim.x + tid;
+            v[j] = q < nq ? reinterpret_cast<const float4*>(rowp)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = base + j * (int)blockDim.x + tid;
+            if (q >= nq) continue;
+            const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t kk[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                kk[c] = (4 * q + c < V) ? order_key(f[c]) : 0u;
+                if (kk[c]) {
+                    ++local_valid;
+                    atomicAdd(&sh.hist[kk[c] >> 20], 1u);
+                }
+            }
+            if (skey) reinterpret_cast<uint4*>(skey)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        }
+    }
+    for (int i = 4 * nq + tid; i < n; i += blockDim.x) {
+        const uint32_t key = i < V ? order_key(rowp[i]) : 0u;
+        if (skey) skey[i] = key;
+        if (key) {
+            ++local_valid;
+            atomicAdd(&sh.hist[key >> 20], 1u);
+        }
+    }
+    if (skey)
+        for (int i = n + tid; i < (n + 31) / 32 * 32; i += blockDim.x) skey[i] = 0u;
     const int w = __reduce_add_sync(FULL_MASK, local_valid);
     if (lane == 0 && w) atomicAdd(&sh.nvalid, w);
     __syncthreads();
@@ -491,7 +597,9 @@ __device__ int select_staged_row(const uint32_t* skey, int n, int k, SelShared& 
         r.take_all = true;
         return block_ordered_emit(key_at, (int64_t)n, r, k, sh, emit);
     }
-    const int f = staged_select(skey, n, k, sh, reinterpret_cast<uint64_t*>(cand32), bmW, bmE, emit);
+    SmemKeys src;
+    src.skey = skey;
+    const int f = staged_select(src, n, k, sh, reinterpret_cast<uint64_t*>(cand32), bmW, bmE, emit);
     if (f >= 0) return f;
     const SelState r = block_radix_select(key_at, (int64_t)n, k, sh, cand32);
     return block_ordered_emit(key_at, (int64_t)n, r, k, sh, emit);
@@ -523,9 +631,13 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_chunk_kernel(SelArgs a) {
     const int64_t n = max((int64_t)0, c1 - c0);
     if (SMEM) {
         __shared__ uint32_t bmW[BM_WORDS], bmE[BM_WORDS];
-        uint32_t* cand = skey + ((a.chunk_len + 1) & ~(int64_t)1);
-        stage_keys([&](int i) -> uint32_t { return key_of<MODE>(a, row, c0 + i, V, n_elems); }, (int)n, skey, sh,
-                   bmW, bmE);
+        uint32_t* cand = skey + (a.chunk_len + 31) / 32 * 32;
+        if (MODE == SEL_TOPK)
+            stage_scores(a.vals + row * a.ld + c0, (int)n, (int)max((int64_t)0, min(V, n_elems) - c0), skey, sh, bmW,
+                         bmE);
+        else
+            stage_keys([&](int i) -> uint32_t { return key_of<MODE>(a, row, c0 + i, V, n_elems); }, (int)n, skey,
+                       sh, bmW, bmE);
         if (a.chunks > 1) {
             const int64_t base = (row * a.chunks + chunk) * (int64_t)a.k;
             const int filled = select_staged_row(skey, (int)n, a.k, sh, cand, bmW, bmE,
@@ -567,13 +679,53 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_merge_kernel(SelArgs a) {
     const int n = a.chunks * a.k;
     const int64_t base = row * (int64_t)n;
     __shared__ uint32_t bmW[BM_WORDS], bmE[BM_WORDS];
-    uint32_t* cand = skey + ((n + 1) & ~1);
+    uint32_t* cand = skey + (n + 31) / 32 * 32;
     stage_keys([&](int i) -> uint32_t { return a.ws_key[base + i]; }, n, skey, sh, bmW, bmE);
     const int filled = select_staged_row(skey, n, a.k, sh, cand, bmW, bmE, [&](int64_t i, int pos, uint32_t key) {
         a.out_idx[row * a.out_len + pos] = a.ws_id[base + i];
         if (a.out_val) a.out_val[row * a.out_len + pos] = key_to_float(key);
     });
     finish_row<MODE>(a, row, filled, n_elems);
+}
+
+// Full-row top-k for many rows of at most SEL_SMEM_CAP scores each (prefill): a
+// 512-thread CTA per row with no staged copy of the row, so two CTAs share an SM and
+// overlap their phases.  The histogram pass and the classify pass both read the
+// row's scores (the second read is served by L2).
+constexpr int STREAM_THREADS = 512;
+
+__global__ void __launch_bounds__(STREAM_THREADS, 2) sel_stream_kernel(SelArgs a) {
+    extern __shared__ uint32_t cand32[];          // [CAND_CAP]
+    __shared__ SelShared sh;
+    __shared__ uint32_t bmW[BM_WORDS], bmE[BM_WORDS];
+    const int64_t row = blockIdx.x;
+    const int n = (int)a.n;
+    const int V = (int)min((int64_t)n, max((int64_t)0, a.nv[row]));
+    RowScores src;
+    src.rowp = a.vals + row * a.ld;
+    src.n = n;
+    src.V = V;
+    stage_scores(src.rowp, n, V, nullptr, sh, bmW, bmE);
+    auto emit = [&](int64_t i, int pos, uint32_t key) {
+        a.out_idx[row * a.out_len + pos] = (int32_t)i;
+        if (a.out_val) a.out_val[row * a.out_len + pos] = src.rowp[i];
+    };
+    auto key_at = [&](int64_t i) -> uint32_t { return src.key((int)i); };
+    int filled;
+    if (sh.nvalid <= a.k) {
+        SelState r;
+        r.T = 0;
+        r.remaining = 0;
+        r.take_all = true;
+        filled = block_ordered_emit(key_at, (int64_t)n, r, a.k, sh, emit);
+    } else {
+        filled = staged_select(src, n, a.k, sh, reinterpret_cast<uint64_t*>(cand32), bmW, bmE, emit);
+        if (filled < 0) {
+            const SelState r = block_radix_select(key_at, (int64_t)n, a.k, sh, cand32);
+            filled = block_ordered_emit(key_at, (int64_t)n, r, a.k, sh, emit);
+        }
+    }
+    finish_row<SEL_TOPK>(a, row, filled, n);
 }
 
 // Chunking: enough CTAs for the GPU when rows are few, each chunk holding at least 4k
@@ -614,7 +766,7 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
     }
     static bool attr = false;
     if (!attr) {
-        const int bytes = (SEL_SMEM_CAP + 2 + CAND_CAP) * (int)sizeof(uint32_t);
+        const int bytes = (SEL_SMEM_CAP + 32 + CAND_CAP) * (int)sizeof(uint32_t);
         if (cudaFuncSetAttribute(sel_chunk_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(sel_chunk_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -624,15 +776,27 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
             return CSA2_ERR_CUDA;
         attr = true;
     }
+    if (MODE == SEL_TOPK && a.chunks == 1 && smem && rows >= 2LL * ctx->num_sms && n_max <= SEL_SMEM_CAP &&
+        (a.ld % 4) == 0 && aligned(a.vals, 16)) {
+        static bool sattr = false;
+        if (!sattr) {
+            if (cudaFuncSetAttribute(sel_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CAND_CAP * (int)sizeof(uint32_t)) != cudaSuccess)
+                return CSA2_ERR_CUDA;
+            sattr = true;
+        }
+        sel_stream_kernel<<<(unsigned)rows, STREAM_THREADS, CAND_CAP * sizeof(uint32_t), s>>>(a);
+        return csa2_launch_status();
+    }
     dim3 grid((unsigned)a.chunks, (unsigned)rows);
     if (smem)
-        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, (((a.chunk_len + 1) & ~(int64_t)1) + CAND_CAP) *
+        sel_chunk_kernel<MODE, true><<<grid, SEL_THREADS, ((a.chunk_len + 31) / 32 * 32 + CAND_CAP) *
                                                                    sizeof(uint32_t), s>>>(a);
     else
         sel_chunk_kernel<MODE, false><<<grid, SEL_THREADS, CAND_CAP * sizeof(uint32_t), s>>>(a);
     if (a.chunks > 1)
         sel_merge_kernel<MODE><<<(unsigned)rows, SEL_THREADS,
-                                 ((((size_t)a.chunks * a.k) + 1) / 2 * 2 + CAND_CAP) * sizeof(uint32_t), s>>>(a);
+                                 (((size_t)a.chunks * a.k + 31) / 32 * 32 + CAND_CAP) * sizeof(uint32_t), s>>>(a);
     return csa2_launch_status();
 }
 

@@ -231,6 +231,23 @@ def test_topk_bit_exact(n, k, ties):
         np.testing.assert_array_equal(val[r], exp_val)
 
 
+@pytest.mark.parametrize("n,k,ties", [(5000, 512, False), (5000, 512, True), (40960, 512, False), (2000, 64, True)])
+def test_topk_many_rows_bit_exact(n, k, ties):
+    """Enough rows (as in prefill) for the one-CTA-per-row streaming kernel; visible
+    counts cover full, partial, ragged and empty rows; all rows against the oracle."""
+    rows = 400
+    s = _score_rows(rows, n, 71 + n, ties)
+    nv = torch.tensor([(n - (37 * r) % (n + 1)) if r % 7 else (r % 3) * (k // 2) for r in range(rows)],
+                      dtype=torch.int64, device=DEV)
+    idx, val = C.csa2_topk(s, nv, k, want_scores=True)
+    idx, val, sn = to_np(idx), to_np(val), s.double().cpu().numpy()
+    for r in range(rows):
+        ref = O.topk(sn[r], int(nv[r]), k)
+        np.testing.assert_array_equal(idx[r], ref, err_msg=f"row {r}")
+        exp_val = np.where(ref >= 0, sn[r][np.maximum(ref, 0)], -np.inf)
+        np.testing.assert_array_equal(val[r], exp_val)
+
+
 def test_topk_all_equal_scores():
     s = torch.full((2, 10000), 3.25, device=DEV)
     nv = torch.tensor([10000, 600], dtype=torch.int64, device=DEV)
