@@ -25,7 +25,8 @@ constexpr int ATT_THREADS = 32 * ATT_HG;
 constexpr int ATT_KC = 32;           // key rows per staged chunk
 constexpr int ATT_C = 512;           // head dim this kernel is built for
 constexpr int ATT_PER_LANE = ATT_C / 32;
-constexpr int PART = ATT_C + 2;      // floats per partial: max, sum, output
+constexpr int PART = ATTN_PART;      // floats per partial (layout in attn_tc.cuh)
+constexpr int PO = ATTN_PART_O;
 
 enum KvKind { KV_F32 = 0, KV_BF16 = 1, KV_FP4 = 2 };
 
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
             part[1] = l_run;
         }
 #pragma unroll
-        for (int i = 0; i < ATT_PER_LANE; ++i) part[2 + lane + 32 * i] = acc[i];
+        for (int i = 0; i < ATT_PER_LANE; ++i) part[PO + lane + 32 * i] = acc[i];
         return;
     }
     // single split: sink, normalisation, inverse RoPE, store
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int
             const float e = expf(ms - M);
             denom = fmaf(part[s * PART + 1], e, denom);
 #pragma unroll
-            for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e, part[s * PART + 2 + lane + 32 * i], acc[i]);
+            for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e, part[s * PART + PO + lane + 32 * i], acc[i]);
         }
     }
     const float inv = denom > 0.0f ? 1.0f / denom : 0.0f;

@@ -53,7 +53,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr int QIMG_BYTES = TC_H * TC_C * 2;     // 64 KB: 8 chunks of 64 rows x 128 B
 constexpr int CHUNK_Q = TC_H * 128;
 constexpr int CHUNK_K = TC_TILE * 128;          // 16 KB: 128 rows x 64 dims
-constexpr int PART = TC_C + 2;
+constexpr int PART = ATTN_PART;
 constexpr uint32_t DS_COL = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr long long WAIT_BUDGET = 1ll << 31;
@@ -64,7 +64,8 @@ constexpr int OFF_K = OFF_Q + QIMG_BYTES;
 constexpr int OFF_P = OFF_K + 8 * CHUNK_K;
 constexpr int OFF_RINV = OFF_P + TC_TILE * 128;
 constexpr int OFF_LW = OFF_RINV + TC_TILE * 4;
-constexpr int OFF_BAR = OFF_LW + 4 * TC_H * 4;
+constexpr int OFF_SC = OFF_LW + 4 * TC_H * 4;        // [4 warps][64] output scale per head
+constexpr int OFF_BAR = OFF_SC + 4 * TC_H * 4;
 constexpr int N_BAR = 16;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BAR * 8;
 constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;
@@ -89,6 +90,7 @@ struct TcArgs {
     void* out;
     float* lse;
     float* part;                  // [B*Q, H, n_split, PART] when n_split > 1
+    const float* rope_cs;         // [B*Q, 64]: cos, sin of the 32 RoPE angles at the query position
     int n_split, tps;             // splits per query, tiles per split
     int64_t items;
     unsigned int* st;
@@ -232,11 +234,17 @@ __device__ __forceinline__ void load16<float>(const float* src, float (&v)[16]) 
 // A CTA per (8 heads, query), a warp per head, 16 dims per lane.
 template <typename TQ>
 __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, RopeTable rope,
-                                                         unsigned flags, uint8_t* qimg) {
+                                                         unsigned flags, uint8_t* qimg, float* rope_cs) {
     __shared__ float cs[32], sn[32];
     const int64_t bq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x < 32) rope_cos_sin(rope, q_pos[bq], threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
+    if (threadIdx.x < 32) {
+        rope_cos_sin(rope, q_pos[bq], threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
+        if (blockIdx.x == 0) {
+            rope_cs[bq * 64 + threadIdx.x] = cs[threadIdx.x];
+            rope_cs[bq * 64 + 32 + threadIdx.x] = sn[threadIdx.x];
+        }
+    }
     __syncthreads();
     uint8_t* img = qimg + bq * (int64_t)QIMG_BYTES;
     {
@@ -292,7 +300,7 @@ __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
     for (int h = 0; h < a.H; ++h) {
         for (int d = d0; d < TC_C; d += 128) {
             if (a.n_split > 1)
-                a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + 2 + d] = 0.0f;
+                a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + d] = 0.0f;
             else
                 reinterpret_cast<TO*>(a.out)[(it.bq * a.H + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
         }
@@ -318,6 +326,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     uint8_t* sP = smem + OFF_P;
     float* sRinv = reinterpret_cast<float*>(smem + OFF_RINV);
     float* sLw = reinterpret_cast<float*>(smem + OFF_LW);
+    float* sSc = reinterpret_cast<float*>(smem + OFF_SC);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* qfull = bars + 0;
     uint64_t* qempty = bars + 1;
@@ -577,13 +586,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
             const bool split = a.n_split > 1;
             const bool rot = !split && (a.flags & CSA2_ROPE) && qd >= 2;
             float rc = 1.0f, rs = 0.0f;
-            if (rot) rope_cos_sin(a.rope, it.t, (32 * qd + lane - 64) >> 1, rc, rs);
-            float scv[TC_H];
-#pragma unroll
-            for (int h = 0; h < TC_H; ++h) scv[h] = __shfl_sync(FULL, sc2[h >> 5], h & 31);
+            if (rot) {
+                const int j = (32 * qd + lane - 64) >> 1;
+                rc = a.rope_cs[it.bq * 64 + j];
+                rs = a.rope_cs[it.bq * 64 + 32 + j];
+            }
+            // this warp's copy of the 64 output scales (lane holds heads lane, lane + 32)
+            float* scw = sSc + qd * TC_H;
+            scw[lane] = sc2[0];
+            scw[lane + 32] = sc2[1];
+            __syncwarp();
             // one base pointer per query; head h is a constant offset from it
             TO* obase = reinterpret_cast<TO*>(a.out) + it.bq * a.H * (int64_t)TC_C + r;
-            float* pbase = a.part + ((it.bq * a.H) * a.n_split + it.split) * (int64_t)PART + 2 + r;
+            float* pbase = a.part + ((it.bq * a.H) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + r;
             const int64_t pstride = (int64_t)a.n_split * PART;
             for (int db = 0; db < 4; ++db) {
                 uint32_t o0[32], o1[32];
@@ -593,15 +608,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                 if (split) {
                     float* pb = pbase + db * 128;
 #pragma unroll
-                    for (int h = 0; h < TC_H; ++h) {
+                    for (int h = 0; h < TC_H; ++h)
                         if (h < a.H) pb[h * pstride] = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]);
-                    }
                 } else {
                     TO* ob = obase + db * 128;
                     const bool rot_here = db == 3 && rot;
+                    float sc4[4];
 #pragma unroll
                     for (int h = 0; h < TC_H; ++h) {
-                        float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]) * scv[h];
+                        if ((h & 3) == 0) {
+                            const float4 t4 = reinterpret_cast<const float4*>(scw)[h >> 2];
+                            sc4[0] = t4.x;
+                            sc4[1] = t4.y;
+                            sc4[2] = t4.z;
+                            sc4[3] = t4.w;
+                        }
+                        float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]) * sc4[h & 3];
                         if (rot_here) {
                             const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
                             v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
@@ -758,7 +780,7 @@ bool want_row_table(int64_t n_bq, int k, int window, int64_t rows) {
 }
 
 struct WsLayout {
-    size_t part, qimg, rinv_kv, rinv_swa, total;
+    size_t part, qimg, rope, rinv_kv, rinv_swa, total;
     int n_split, tps;
     bool table;
 };
@@ -772,7 +794,8 @@ WsLayout ws_layout(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, 
     L.table = want_row_table(n_bq, k, window, kv_rows + sw_rows);
     L.part = 0;
     L.qimg = L.n_split > 1 ? align_up((size_t)n_bq * H * L.n_split * PART * sizeof(float), 1024) : 0;
-    L.rinv_kv = L.qimg + (size_t)n_bq * QIMG_BYTES;
+    L.rope = L.qimg + (size_t)n_bq * QIMG_BYTES;
+    L.rinv_kv = align_up(L.rope + (size_t)n_bq * 64 * sizeof(float), 256);
     L.rinv_swa = align_up(L.rinv_kv + (L.table ? (size_t)kv_rows * sizeof(float) : 0), 256);
     L.total = L.rinv_swa + (L.table ? (size_t)sw_rows * sizeof(float) : 0);
     return L;
@@ -815,12 +838,13 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     if (!ws || !aligned(ws, 16) || ws_bytes < L.rinv_kv) return CSA2_ERR_INVALID_ARG;
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     uint8_t* qimg = base + L.qimg;
+    float* rope_cs = reinterpret_cast<float*>(base + L.rope);
     if (c.q_dt == CSA2_BF16)
         attn_qprep_kernel<__nv_bfloat16><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(
-            reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg);
+            reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs);
     else
         attn_qprep_kernel<float><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
-                                                                c.rope, c.flags, qimg);
+                                                                c.rope, c.flags, qimg, rope_cs);
     TcArgs a;
     a.rinv_kv = nullptr;
     a.rinv_swa = nullptr;
@@ -842,6 +866,7 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
         }
     }
     a.qimg = qimg;
+    a.rope_cs = rope_cs;
     a.kv = c.kv;
     a.swa = reinterpret_cast<const uint8_t*>(c.swa);
     a.N = c.N;

@@ -6,6 +6,12 @@
 
 #include "csa2_internal.cuh"
 
+// Per-split partial result of one (query, head): [0] = max logit (or the fixed
+// offset), [1] = sum of exponentials, [ATTN_PART_O ..] = the 512 unnormalised output
+// values.  Rows are 16-byte multiples so they can be written by bulk copies.
+constexpr int ATTN_PART = 516;
+constexpr int ATTN_PART_O = 4;
+
 struct AttnTcCall {
     const void* q;
     csa2_dtype q_dt;
@@ -42,7 +48,7 @@ size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int win
 size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window);
 
 // Runs the path.  On return *n_split > 1 means the output is still in per-split
-// partials at the start of `ws` (float [B*Q, H, n_split, 514]: max, sum, output),
+// partials at the start of `ws` (float [B*Q, H, n_split, ATTN_PART]),
 // to be merged by the caller's combine kernel.
 csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
                         int* n_split);
