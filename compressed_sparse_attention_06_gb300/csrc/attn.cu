@@ -84,6 +84,7 @@ struct AttnArgs {
     void* out;
     float* lse;
     float* ws;            // [B*Q, H, n_split, PART] partials (n_split > 1)
+    const float* rope_cs; // [B*Q, 64] RoPE cos, sin at the query position (tensor-core path), or NULL
     int n_split;
     int spl;              // key slots per split (multiple of ATT_KC)
     unsigned int* st;
@@ -252,7 +253,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
     if (a.lse && lane == 0) a.lse[bq * a.H + h] = (denom > 0.0f) ? m_fin + logf(denom) : -INFINITY;
 }
 
-// Merge the splits of one (query, head) per warp.
+// Merge the splits of one (query, head) per warp: the split maxima are read one per
+// lane, then four splits at a time are accumulated with all their loads in flight.
 template <typename TO>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int64_t rows) {
     __shared__ float cs_all[8][32], sn_all[8][32];
@@ -261,28 +263,44 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int
     if (r >= rows) return;
     const int64_t bq = r / a.H;
     const int h = (int)(r % a.H);
-    const int64_t t = a.q_pos[bq];
     float* cs = cs_all[warp];
     float* sn = sn_all[warp];
-    if (a.flags & CSA2_ROPE) rope_cos_sin(a.rope, t, lane, cs[lane], sn[lane]);
+    if (a.flags & CSA2_ROPE) {
+        if (a.rope_cs) {
+            cs[lane] = a.rope_cs[bq * 64 + lane];
+            sn[lane] = a.rope_cs[bq * 64 + 32 + lane];
+        } else {
+            rope_cos_sin(a.rope, a.q_pos[bq], lane, cs[lane], sn[lane]);
+        }
+    }
     __syncwarp();
-    const float* part = a.ws + r * (int64_t)a.n_split * PART;
+    const int ns = a.n_split;
+    const float* part = a.ws + r * (int64_t)ns * PART;
     const float zs = a.sink ? a.sink[h] : -INFINITY;
     float M = zs;
-    for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, part[s * PART]);
+    for (int s0 = 0; s0 < ns; s0 += 32) M = fmaxf(M, warp_max(s0 + lane < ns ? part[(s0 + lane) * PART] : -INFINITY));
     float acc[ATT_PER_LANE];
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = 0.0f;
     float denom = 0.0f;
     if (M != -INFINITY) {
         denom = (zs == -INFINITY) ? 0.0f : expf(zs - M);
-        for (int s = 0; s < a.n_split; ++s) {
-            const float ms = part[s * PART];
-            if (ms == -INFINITY) continue;
-            const float e = expf(ms - M);
-            denom = fmaf(part[s * PART + 1], e, denom);
+        for (int s = 0; s < ns; s += 4) {
+            float e[4], l[4];
 #pragma unroll
-            for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e, part[s * PART + PO + lane + 32 * i], acc[i]);
+            for (int j = 0; j < 4; ++j) {
+                const float ms = s + j < ns ? part[(s + j) * PART] : -INFINITY;
+                e[j] = (ms == -INFINITY) ? 0.0f : expf(ms - M);
+                l[j] = s + j < ns ? part[(s + j) * PART + 1] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (s + j >= ns) break;
+                denom = fmaf(l[j], e[j], denom);
+                const float* pj = part + (s + j) * PART + PO + lane;
+#pragma unroll
+                for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e[j], pj[32 * i], acc[i]);
+            }
         }
     }
     const float inv = denom > 0.0f ? 1.0f / denom : 0.0f;
@@ -428,6 +446,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
         c.out = out;
         c.lse = lse;
         c.ws = reinterpret_cast<float*>(ws);
+        c.rope_cs = attn_tc_rope_table(ctx, tc, ws);
         c.n_split = ns;
         c.st = ctx->status;
         return out_dt == CSA2_F32 ? launch_combine<float>(c, B, Q, s) : launch_combine<__nv_bfloat16>(c, B, Q, s);
@@ -451,6 +470,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     a.out = out;
     a.lse = lse;
     a.ws = reinterpret_cast<float*>(ws);
+    a.rope_cs = nullptr;
     a.st = ctx->status;
     const int64_t groups = (int64_t)B * Q * ((H + ATT_HG - 1) / ATT_HG);
     const int n_slots_max = k + window;

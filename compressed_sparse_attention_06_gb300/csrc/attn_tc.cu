@@ -831,6 +831,11 @@ size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int win
     return ws_layout(ctx, B, Q, H, k, window, N, swa_cap).total;
 }
 
+const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* ws) {
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    return reinterpret_cast<const float*>(reinterpret_cast<uint8_t*>(ws) + L.rope);
+}
+
 csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
                         int* n_split) {
     const int64_t n_bq = (int64_t)c.B * c.Q;

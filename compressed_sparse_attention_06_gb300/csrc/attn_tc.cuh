@@ -47,6 +47,9 @@ size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int win
 // partials, 0 when it runs unsplit.
 size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window);
 
+// The RoPE cos/sin table (float [B*Q, 64]) the path wrote into `ws` for this call.
+const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* ws);
+
 // Runs the path.  On return *n_split > 1 means the output is still in per-split
 // partials at the start of `ws` (float [B*Q, H, n_split, ATTN_PART]),
 // to be merged by the caller's combine kernel.

@@ -732,6 +732,13 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2) sel_stream_kernel(SelArgs a
 // elements, chunks that fit shared memory, and a merge that fits shared memory.
 void choose_chunks(const csa2_ctx* ctx, int64_t rows, int64_t n_max, int k, size_t ws_bytes, bool have_ws,
                    int& chunks, int64_t& chunk_len, bool& smem) {
+    // a row that fits on-chip is one CTA: its two passes cost less than a second launch
+    if (n_max <= SEL_SMEM_CAP) {
+        chunks = 1;
+        chunk_len = std::max<int64_t>(n_max, 1);
+        smem = true;
+        return;
+    }
     int64_t need = (n_max + SEL_SMEM_CAP - 1) / SEL_SMEM_CAP;
     int64_t want = std::max<int64_t>(need, std::min<int64_t>((2LL * ctx->num_sms + rows - 1) / rows,
                                                              n_max / std::max(1, 4 * k)));
