@@ -65,8 +65,9 @@ constexpr int OFF_P = OFF_K + 8 * CHUNK_K;
 constexpr int OFF_RINV = OFF_P + TC_TILE * 128;
 constexpr int OFF_LW = OFF_RINV + TC_TILE * 4;
 constexpr int OFF_SC = OFF_LW + 4 * TC_H * 4;        // [4 warps][64] output scale per head
-constexpr int OFF_BAR = OFF_SC + 4 * TC_H * 4;
-constexpr int N_BAR = 16;
+constexpr int OFF_SCL = OFF_SC + 4 * TC_H * 4;       // [2 items][64] scales for the loader warps
+constexpr int OFF_BAR = OFF_SCL + 2 * TC_H * 4;
+constexpr int N_BAR = 17;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BAR * 8;
 constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -317,6 +318,58 @@ __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
     }
 }
 
+// Output of heads [hbeg, hbeg + 32) of an item from O^T in tensor memory: the calling
+// warp reads its 32-lane quarter `quad` (dims 32 quad + lane of every 128-dim block),
+// scales by sc[h] (final output) and rotates back, or stores the unnormalised partial.
+template <typename TO>
+__device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& it, uint32_t tmem, int quad, int lane,
+                                               int hbeg, const float* sc) {
+    const bool split = a.n_split > 1;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int rr = quad * 32 + lane;
+    const bool rot = !split && (a.flags & CSA2_ROPE) && quad >= 2;
+    float rc = 1.0f, rs = 0.0f;
+    if (rot) {
+        const int j = (32 * quad + lane - 64) >> 1;
+        rc = a.rope_cs[it.bq * 64 + j];
+        rs = a.rope_cs[it.bq * 64 + 32 + j];
+    }
+    TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.H + hbeg) * (int64_t)TC_C + rr;
+    float* pbase = a.part + ((it.bq * a.H + hbeg) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + rr;
+    const int64_t pstride = (int64_t)a.n_split * PART;
+    for (int db = 0; db < 4; ++db) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + (uint32_t)(db * TC_H + hbeg), o);
+        tmem_wait_ld();
+        if (split) {
+            float* pb = pbase + db * 128;
+#pragma unroll
+            for (int h = 0; h < 32; ++h)
+                if (hbeg + h < a.H) pb[h * pstride] = __uint_as_float(o[h]);
+        } else {
+            TO* ob = obase + db * 128;
+            const bool rot_here = db == 3 && rot;
+            float sc4[4];
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+                if ((h & 3) == 0) {
+                    const float4 t4 = reinterpret_cast<const float4*>(sc + hbeg)[h >> 2];
+                    sc4[0] = t4.x;
+                    sc4[1] = t4.y;
+                    sc4[2] = t4.z;
+                    sc4[3] = t4.w;
+                }
+                float v = __uint_as_float(o[h]) * sc4[h & 3];
+                if (rot_here) {
+                    const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
+                    v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
+                }
+                if (hbeg + h < a.H) ob[h * TC_C] = from_f32<TO>(v);
+            }
+        }
+    }
+}
+
 template <bool FP4, typename TO>
 __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -327,6 +380,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     float* sRinv = reinterpret_cast<float*>(smem + OFF_RINV);
     float* sLw = reinterpret_cast<float*>(smem + OFF_LW);
     float* sSc = reinterpret_cast<float*>(smem + OFF_SC);
+    float* sScL = reinterpret_cast<float*>(smem + OFF_SCL);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* qfull = bars + 0;
     uint64_t* qempty = bars + 1;
@@ -338,6 +392,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     uint64_t* ofull = bars + 13;
     uint64_t* oempty = bars + 14;
     uint64_t* lred = bars + 15;
+    uint64_t* scready = bars + 16;     // an item's output scales are in sScL
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -352,7 +407,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         mbar_init(sfull, 1);
         mbar_init(pfull, 4);
         mbar_init(ofull, 1);
-        mbar_init(oempty, 4);
+        mbar_init(oempty, 8);
+        mbar_init(scready, 1);
         mbar_init(lred, 4);
         fence_mbar_init();
     }
@@ -584,54 +640,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
             }
             tc_fence_after();
             const bool split = a.n_split > 1;
-            const bool rot = !split && (a.flags & CSA2_ROPE) && qd >= 2;
-            float rc = 1.0f, rs = 0.0f;
-            if (rot) {
-                const int j = (32 * qd + lane - 64) >> 1;
-                rc = a.rope_cs[it.bq * 64 + j];
-                rs = a.rope_cs[it.bq * 64 + 32 + j];
-            }
-            // this warp's copy of the 64 output scales (lane holds heads lane, lane + 32)
+            // this warp's copy of the 64 output scales (lane holds heads lane, lane + 32);
+            // warp 0 also publishes them for the loader warps, which store heads 32..63
             float* scw = sSc + qd * TC_H;
             scw[lane] = sc2[0];
             scw[lane + 32] = sc2[1];
-            __syncwarp();
-            // one base pointer per query; head h is a constant offset from it
-            TO* obase = reinterpret_cast<TO*>(a.out) + it.bq * a.H * (int64_t)TC_C + r;
-            float* pbase = a.part + ((it.bq * a.H) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + r;
-            const int64_t pstride = (int64_t)a.n_split * PART;
-            for (int db = 0; db < 4; ++db) {
-                uint32_t o0[32], o1[32];
-                tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H, o0);
-                tmem_ld32(tmem + lane_base + (uint32_t)db * TC_H + 32, o1);
-                tmem_wait_ld();
-                if (split) {
-                    float* pb = pbase + db * 128;
-#pragma unroll
-                    for (int h = 0; h < TC_H; ++h)
-                        if (h < a.H) pb[h * pstride] = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]);
-                } else {
-                    TO* ob = obase + db * 128;
-                    const bool rot_here = db == 3 && rot;
-                    float sc4[4];
-#pragma unroll
-                    for (int h = 0; h < TC_H; ++h) {
-                        if ((h & 3) == 0) {
-                            const float4 t4 = reinterpret_cast<const float4*>(scw)[h >> 2];
-                            sc4[0] = t4.x;
-                            sc4[1] = t4.y;
-                            sc4[2] = t4.z;
-                            sc4[3] = t4.w;
-                        }
-                        float v = __uint_as_float(h < 32 ? o0[h] : o1[h - 32]) * sc4[h & 3];
-                        if (rot_here) {
-                            const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
-                            v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
-                        }
-                        if (h < a.H) ob[h * TC_C] = from_f32<TO>(v);
-                    }
-                }
+            if (qd == 0) {
+                sScL[(qi & 1) * TC_H + lane] = sc2[0];
+                sScL[(qi & 1) * TC_H + lane + 32] = sc2[1];
             }
+            __syncwarp();
+            if (qd == 0 && lane == 0) mbar_arrive(scready);
+            epilogue_heads<TO>(a, it, tmem, qd, lane, 0, scw);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(oempty);
@@ -654,12 +674,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     } else {
         // ============================ loaders ============================
         const int r = threadIdx.x - 192;           // slot of the tile
+        const int quad = warp & 3;                 // tensor-memory lane quarter of this warp
         const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv);
-        int g = 0;
+        int g = 0, qi = 0;
         bool ok = true;
+        // heads 32..63 of the previous item's output, stored once the next item's first
+        // tile is on its way (or after the last item)
+        ItemInfo pend;
+        bool have_pend = false;
+        auto run_pending = [&]() {
+            bool w = mbar_wait(scready, (qi - 1) & 1, a.budget, a.st) && mbar_wait(ofull, (qi - 1) & 1, a.budget, a.st);
+            if (!__all_sync(FULL, w)) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            epilogue_heads<TO>(a, pend, tmem, quad, lane, 32, sScL + ((qi - 1) & 1) * TC_H);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(oempty);
+            have_pend = false;
+        };
         for (int64_t item = blockIdx.x; item < a.items && ok; item += gridDim.x) {
             const ItemInfo it = item_info(a, item);
-            for (int tt = 0; tt < it.nt; ++tt, ++g) {
+            for (int tt = 0; tt < it.nt && ok; ++tt, ++g) {
                 const SlotSrc s = slot_source(a, it, (it.t0 + tt) * TC_TILE + r, true);
                 const bool bf_row = s.kind == 2 || (s.kind == 1 && !FP4);
                 const uint8_t* src = s.kind == 2 ? a.swa + s.row * (int64_t)(TC_C * 2)
@@ -755,8 +793,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                 sRinv[r] = rv;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rfull);
+                if (tt == 0 && have_pend) run_pending();
+            }
+            if (it.nt > 0 && ok) {
+                if (have_pend) run_pending();      // an item of a single tile: previous one first
+                pend = it;
+                have_pend = true;
+                ++qi;
             }
         }
+        if (have_pend && ok) run_pending();
     }
     tc_fence_before();
     __syncthreads();

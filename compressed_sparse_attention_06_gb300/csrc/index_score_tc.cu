@@ -341,8 +341,16 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                           e3 = (int)(sw >> 24);
                 const int emax = max(max(e0, e1), max(e2, e3));
                 // block exponent relative to the row's largest block, which lands at 2^13
-                const uint32_t m0 = f16_pow2_bits(e0 - emax + 13), m1 = f16_pow2_bits(e1 - emax + 13),
-                               m2 = f16_pow2_bits(e2 - emax + 13), m3 = f16_pow2_bits(e3 - emax + 13);
+                // the four block multipliers, each as a pair of f16 lanes
+                uint32_t m2[4];
+                {
+                    const uint32_t b0 = f16_pow2_bits(e0 - emax + 13), b1 = f16_pow2_bits(e1 - emax + 13),
+                                   b2 = f16_pow2_bits(e2 - emax + 13), b3 = f16_pow2_bits(e3 - emax + 13);
+                    m2[0] = b0 | (b0 << 16);
+                    m2[1] = b1 | (b1 << 16);
+                    m2[2] = b2 | (b2 << 16);
+                    m2[3] = b3 | (b3 << 16);
+                }
                 sRho[(li & 3) * TILE + row] = emax - 127 - 13;
                 uint32_t out[32];
                 const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + j * 64;
@@ -351,8 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
 #pragma unroll
                     for (int wi = 0; wi < 8; ++wi) {
                         const int wd = half * 8 + wi;
-                        const uint32_t mb = (wd < 4) ? m0 : (wd < 8) ? m1 : (wd < 12) ? m2 : m3;
-                        const uint32_t m2x = mb | (mb << 16);
+                        const uint32_t m2x = m2[wd >> 2];
                         uint32_t o0, o1, o2, o3;
                         e2m1x8_to_f16x2(cw[wd], o0, o1, o2, o3);
                         out[4 * wi + 0] = hmul2(o0, m2x);
@@ -415,7 +422,8 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                     a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
                 }
                 float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
-                if (KF == KF_MX) acc = ldexpf(acc, rho);
+                if (KF == KF_MX)      // exact power-of-two rescale (2^rho built from its bits when normal)
+                    acc = (rho >= -126 && rho <= 127) ? acc * __int_as_float((rho + 127) << 23) : ldexpf(acc, rho);
                 const bool vis = sid < V[qi] && e < n_elems;
                 sc[qi] = vis ? acc : -INFINITY;
             }
