@@ -184,7 +184,7 @@ class Workload:
 class FP4Decode(Workload):
     """FP4-cache long-context decode, B sequences x N entries (the headline)."""
     name = "fp4_decode_1M"
-    main_name = "csa2_index_score (MXFP4 full scan, fused block max)"
+    main_name = "csa2_index_score (FP4 QK full scan over MXFP4 keys, fused block max)"
     profile = "index_score_fp4_decode_1M.txt"
 
     def __init__(self, B=8, N=1 << 20, seq0=0):
@@ -223,6 +223,7 @@ class FP4Decode(Workload):
         self.nv = P.visible_entries(self.q_pos, 1)
         self.pos_new = self.q_pos[:, 0].clone()
         self.buf = P.alloc_decode(B, 1, N, self.H, 512, dev, out_dtype=torch.bfloat16)
+        self.qI_mx = self.buf.qI_mx
         self.swa_row = self.swa[:, self.t % 128]
         self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new, self.KI_new]
         self.e2e_out = [self.buf.out, self.buf.idx]
@@ -244,9 +245,10 @@ class FP4Decode(Workload):
         C.csa2_compress(self.C_new, self.Z_new, 1, pos0=self.pos_new, flags=C.W_ROPE, out=self.kv[:, t],
                         out_seq_stride=self.N)
         C.csa2_fp4_pack(self.KI_new, C.MXFP4_E8M0x32, out=self.ki[:, t], out_ld=self.N * 68)
+        C.csa2_fp4_pack(self.qI, C.MXFP4_E8M0x32, out=self.qI_mx)     # the QK path runs in FP4
 
     def main(self):
-        _C().csa2_index_score(self.qI, self.w, self.ki, self.nv, block=self.block, want_scores=False,
+        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, want_scores=False,
                               want_block_max=True, block_max=self.buf.block_max)
 
     def pool(self):
@@ -255,7 +257,8 @@ class FP4Decode(Workload):
 
     def cand(self):
         b = self.buf
-        _C().csa2_index_score(self.qI, self.w, self.ki, self.nv, pool=b.pool, block=self.block, scores=b.cand_scores)
+        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, pool=b.pool, block=self.block,
+                              scores=b.cand_scores)
 
     def topk(self):
         b = self.buf
@@ -273,18 +276,18 @@ class FP4Decode(Workload):
         self.pool(); self.cand(); self.topk(); self.attn()
 
     def launches_per_step(self):
-        return 10     # compress, pack, scan, pool chunk+merge, candidate scan, top-k chunk+merge, attention split+combine
+        return 11     # compress, 2 packs, scan, pool chunk+merge, candidate scan, top-k, attention qprep+main+combine
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
-        once, plus the queries and head weights."""
-        return self.B * self.V * 68 + self.B * self.H_I * (128 * 2 + 4)
+        once, plus the MXFP4 queries and the head weights."""
+        return self.B * self.V * 68 + self.B * self.H_I * (68 + 4)
 
     def stages(self):
         B, H = self.B, self.H
         attn_bytes = B * (self.k * 288 + self.window * 1024 + H * 512 * 2 * 2)
         attn_flops = B * H * (self.k + self.window) * 512 * 4
-        return [("write new rows", self.write, B * (2 * 1024 + 256 + 288 + 68), 0),
+        return [("write new rows", self.write, B * (2 * 1024 + 256 + 288 + 68 + self.H_I * (256 + 68)), 0),
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
                 ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
                 ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128),
@@ -307,7 +310,9 @@ class FP4Decode(Workload):
                         for r0 in range(0, N, 1 << 18)]).numpy()
         self.o_ki = O.mxfp4_pack(ki)
         wl = self.wl if hasattr(self, "wl") else W.fp4_decode("cpu", B=self.B, N=N)
-        self.o_q = dict(qI=wl["qI"][b, 0].double().cpu().numpy(), w=wl["w"][b, 0].double().cpu().numpy(),
+        # the indexer query as the FP4 QK path sees it: MXFP4-packed, dequantised
+        qI_mx = O.mxfp4_unpack(O.mxfp4_pack(wl["qI"][b, 0].float().cpu().numpy()))
+        self.o_q = dict(qI=qI_mx, w=wl["w"][b, 0].double().cpu().numpy(),
                         q=wl["q"][b, 0].double().cpu().numpy(), swa=wl["swa"][b].double().cpu().numpy(),
                         sink=wl["sink"].double().cpu().numpy())
         self.o_b = b
@@ -319,7 +324,8 @@ class FP4Decode(Workload):
                      for s in idx if s >= 0}
 
     def oracle_query(self):
-        """One query of the step through the oracle: dequantise the indexer cache, score,
+        """One query of the step through the oracle: dequantise the indexer cache (the
+        query was packed and dequantised the same way in oracle_prepare), score,
         block max, pool, top-512 inside the pool, gather + dequantise the selected
         main-KV rows, attend."""
         from oracle import csa2_oracle as O

@@ -212,9 +212,15 @@ def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=No
 def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=None, block: int = 8,
                      scores: Optional[torch.Tensor] = None, block_max: Optional[torch.Tensor] = None,
                      want_scores: bool = True, want_block_max: bool = False):
-    """qI [B,Q,H_I,d], w [B,Q,H_I], kI [B,N,d] (f32/bf16) or [B,N,row_bytes] uint8 (MXFP4),
-    n_visible [B,Q] int64.  Returns (scores, block_max); either may be None."""
+    """qI [B,Q,H_I,d] (f32/bf16) or [B,Q,H_I,68] uint8 (MXFP4, d = 128), w [B,Q,H_I],
+    kI [B,N,d] (f32/bf16) or [B,N,row_bytes] uint8 (MXFP4), n_visible [B,Q] int64.
+    MXFP4 queries over MXFP4 keys run the QK product in FP4 on the tensor cores.
+    Returns (scores, block_max); either may be None."""
     B, Q, H_I, d = qI.shape
+    if qI.dtype == torch.uint8:
+        q_dt, d = MXFP4_E8M0x32, 128
+    else:
+        q_dt = _dt(qI)
     N = kI.shape[1]
     if kI.dtype == torch.uint8:
         k_dt = MXFP4_E8M0x32 if k_fmt is None else k_fmt
@@ -230,7 +236,7 @@ def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=Non
             scores = torch.empty((B, Q, N), dtype=torch.float32, device=qI.device)
         if want_block_max and block_max is None:
             block_max = torch.empty((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
-    st = _lib().csa2_index_score(ctx(qI.device.index), _p(qI), _dt(qI), _p(w), _p(kI), k_dt, B, Q, N, H_I, d,
+    st = _lib().csa2_index_score(ctx(qI.device.index), _p(qI), q_dt, _p(w), _p(kI), k_dt, B, Q, N, H_I, d,
                                  _p(n_visible), _p(pool), n_pool, block, _p(scores), _p(block_max), _stream(qI))
     _check("csa2_index_score", st)
     return scores, block_max

@@ -1,0 +1,393 @@
+// Lightning-indexer scan with the QK product in FP4 (tcgen05 kind::mxf4, sm_103a).
+//
+// Computes eq. (16) of the DSA-to-CSA/HCA page,
+//     I[t, s] = sum_h w[t, h] * ReLU(q^I[t, h] . K^I[s]),
+// when both the indexer query and the indexer keys are MXFP4 (E2M1 codes, one E8M0
+// scale per 32 dims): the page runs the indexer QK path in FP4 (section «Lightning
+// Indexer：公式 (13)–(17)» and «系统收益从哪里来»), and the CSA2 page stores K^I as
+// 64 code bytes + 4 scale bytes per entry.  The block-scaled MMA multiplies the FP4
+// values with their scales applied, so no element is converted on the CUDA cores.
+//
+// Per tile of 128 entries: D[128 entries x 64 heads] = sum over two K=64 steps of
+// (A x SFA)(B x SFB)^T, A = the tile's key codes, B = the query's codes, SFA / SFB
+// their scales in tensor memory, D in fp32 tensor memory.  The block max over 8
+// entries (CSA2 page, «解码器里的分层索引») is fused into the epilogue, or the tile is
+// a list of pooled candidate blocks (Reindex).
+//
+// One CTA per SM (the grid splits each query's tiles over the SMs), 18 warps:
+//   warp 0       producer: bulk copies of 68-byte key rows into a 10-stage ring
+//   warp 1       MMA issuer (one lane); owns the tensor-memory allocation
+//   warps 2-9    two copy groups (alternate tiles): each thread moves its entry's 64
+//                code bytes into the MMA's no-swizzle K-major layout and the group
+//                writes the tile's scale bytes into tensor memory
+//   warps 10-17  two epilogue groups (alternate tiles): each thread reads its entry's
+//                64 head dots, applies ReLU and the head weights, sums, masks the
+//                invisible entries and writes the score / block max
+// Buffers: 4 A tiles (shared memory), 4 D tiles (tensor memory, 64 columns each).
+//
+// Exactness: E2M1 x E2M1 products and their per-block sums are exact; each block sum
+// is scaled by a power of two and accumulated in fp32.
+//
+// Every mbarrier wait is bounded; a wait that expires records CSA2_ERR_TIMEOUT and
+// the CTA winds down (copies and MMAs in flight are drained, tensor memory is freed).
+#include <algorithm>
+
+#include "index_score_tc.cuh"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+using namespace sm100;
+
+constexpr int TILE = 128;                    // entries per tile (MMA M)
+constexpr int HEADS = 64;                    // indexer heads (MMA N)
+constexpr int MX_ROW = 68;                   // bytes of an MXFP4 row of 128 dims
+constexpr int CODE_BYTES = 64;
+constexpr int MX_STAGE = TILE * MX_ROW;      // 8704 B, a multiple of 16
+constexpr long long WAIT_BUDGET = 1ll << 31;
+
+constexpr int CPY_GROUPS = 2, EPI_GROUPS = 2;
+constexpr int NWARPS = 2 + 4 * CPY_GROUPS + 4 * EPI_GROUPS;
+constexpr int THREADS = NWARPS * 32;
+constexpr int STAGES = 10, A_BUFS = 4, D_BUFS = 4;
+constexpr int A_BYTES = TILE * CODE_BYTES;   // 8 KB
+constexpr int B_BYTES = HEADS * CODE_BYTES;  // 4 KB
+
+// shared memory (offsets from a 128-byte aligned base)
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + A_BUFS * A_BYTES;
+constexpr int OFF_STAGE = OFF_B + B_BYTES;
+constexpr int OFF_W = OFF_STAGE + STAGES * MX_STAGE;
+constexpr int OFF_BAR = OFF_W + HEADS * 4;
+constexpr int N_BARS = 2 * STAGES + 2 * A_BUFS + 2 * D_BUFS;
+constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
+constexpr int SMEM = OFF_TMEMPTR + 16 + 128;
+// tensor memory: D tiles, then 4 scale columns per A tile, then the query's scales
+constexpr uint32_t D_COL0 = 0;
+constexpr uint32_t SFA_COL0 = D_COL0 + D_BUFS * 64;
+constexpr uint32_t SFB_COL = SFA_COL0 + A_BUFS * 4;
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(SFB_COL + 4 <= TMEM_COLS, "tensor memory");
+// more than half of the SM's shared memory: one CTA per SM, so the 512-column
+// allocation never waits on another CTA
+static_assert(SMEM > 114 * 1024 && SMEM <= 227 * 1024, "shared memory");
+static_assert(OFF_STAGE % 16 == 0 && MX_STAGE % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+
+struct FpArgs {
+    const uint8_t* qmx;           // MXFP4 queries [B, Q, 64, 68]
+    const float* w;               // [B, Q, 64]
+    const uint8_t* kmx;           // MXFP4 keys [B, N, 68]
+    const int64_t* nv;            // [B, Q]
+    const int32_t* pool;          // candidate mode: [B, Q, n_pool]
+    float* scores;                // full: [B, Q, N]; candidate: [B, Q, n_pool*8]
+    float* bmax;                  // full: [B, Q, ceil(N/8)]
+    unsigned int* st;
+    int B, Q, n_pool;
+    int64_t N;
+    int tiles;                    // tiles per query
+    int tiles_per_cta;
+    long long budget;
+    int stall;                    // test hook: the producer issues nothing
+};
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+template <bool CAND>
+__global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    uint8_t* sA = smem + OFF_A;
+    uint8_t* sB = smem + OFF_B;
+    uint8_t* sStage = smem + OFF_STAGE;
+    float* sW = reinterpret_cast<float*>(smem + OFF_W);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* full = bars;                   // [STAGES] rows landed
+    uint64_t* empty = full + STAGES;         // [STAGES] rows read by a copy group
+    uint64_t* afull = empty + STAGES;        // [A_BUFS] A tile + its scales written
+    uint64_t* adone = afull + A_BUFS;        // [A_BUFS] MMA done with the A tile
+    uint64_t* mdone = adone + A_BUFS;        // [D_BUFS] D tile ready
+    uint64_t* dempty = mdone + D_BUFS;       // [D_BUFS] D tile read by an epilogue group
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.y;                // b * Q + q
+    const int b = g / a.Q;
+    int64_t V = a.nv[g];
+    if (!CAND && V > a.N) V = a.N;
+    const int t_begin = blockIdx.x * a.tiles_per_cta;
+    const int t_end = min(a.tiles, t_begin + a.tiles_per_cta);
+    int t_act_end = t_end;
+    if (!CAND) t_act_end = min(t_end, (int)((V + TILE - 1) / TILE));
+    const int n_act = max(0, t_act_end - t_begin);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);
+        }
+        for (int j = 0; j < A_BUFS; ++j) {
+            mbar_init(&afull[j], 4);
+            mbar_init(&adone[j], 1);
+        }
+        for (int j = 0; j < D_BUFS; ++j) {
+            mbar_init(&mdone[j], 1);
+            mbar_init(&dempty[j], 4);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sTmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    // query codes -> the B tile: thread (head h, 16-byte unit u)
+    const uint8_t* qrow0 = a.qmx + (int64_t)g * HEADS * MX_ROW;
+    for (int t = threadIdx.x; t < HEADS * 4; t += THREADS) {
+        const int h = t >> 2, u = t & 3;
+        const uint8_t* src = qrow0 + h * MX_ROW + u * 16;
+        *reinterpret_cast<uint4*>(sB + kmajor64_offset(h, u)) =
+            make_uint4(ld_u32(src), ld_u32(src + 4), ld_u32(src + 8), ld_u32(src + 12));
+    }
+    for (int h = threadIdx.x; h < HEADS; h += THREADS) sW[h] = a.w[(int64_t)g * HEADS + h];
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sTmem;
+    // query scales -> tensor memory.  Scale-factor layout: the 32-bit cell at lane
+    // 32j' + l, column c + j holds the four block scales of row 32j + l (the same in
+    // each lane quarter); the query has 64 rows (heads), so columns c and c+1.
+    if (warp < 4) {
+        const uint32_t s0 = ld_u32(qrow0 + lane * MX_ROW + CODE_BYTES);
+        const uint32_t s1 = ld_u32(qrow0 + (lane + 32) * MX_ROW + CODE_BYTES);
+        tmem_st4(tmem + ((uint32_t)(warp * 32) << 16) + SFB_COL, s0, s1, 0u, 0u);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    bool ok = true;
+
+    if (warp == 0) {
+        // ============================ producer ============================
+        if (lane == 0) {
+            int issued = 0;
+            for (int li = 0; li < (a.stall ? 0 : n_act) && ok; ++li) {
+                const int s = li % STAGES, r = li / STAGES;
+                if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st)) {
+                    ok = false;
+                    break;
+                }
+                const int tile = t_begin + li;
+                uint8_t* dst = sStage + s * MX_STAGE;
+                if (!CAND) {
+                    const int64_t row0 = (int64_t)tile * TILE;
+                    const int64_t rows = min((int64_t)TILE, a.N - row0);
+                    const uint32_t bytes = (uint32_t)(rows * MX_ROW);
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    bulk_g2s(dst, a.kmx + ((int64_t)b * a.N + row0) * MX_ROW, bytes, &full[s]);
+                } else {
+                    const int32_t* pl = a.pool + (int64_t)g * a.n_pool + (int64_t)tile * 16;
+                    int32_t blk[16];
+                    uint32_t bytes = 0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        int32_t pb = pl[j];
+                        if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
+                        blk[j] = pb;
+                        if (pb >= 0) bytes += 8 * MX_ROW;
+                    }
+                    mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (blk[j] >= 0)
+                            bulk_g2s(dst + j * 8 * MX_ROW, a.kmx + ((int64_t)b * a.N + (int64_t)blk[j] * 8) * MX_ROW,
+                                     8 * MX_ROW, &full[s]);
+                }
+                ++issued;
+            }
+            // no copy may still be writing shared memory when the CTA exits
+            for (int li = max(0, issued - STAGES); li < issued; ++li)
+                mbar_wait(&full[li % STAGES], (li / STAGES) & 1, a.budget, a.st);
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ============================
+        if (lane == 0) {
+            int done = 0;
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            for (int li = 0; li < n_act && ok; ++li) {
+                const int ja = li % A_BUFS, jd = li % D_BUFS;
+                if (!mbar_wait(&afull[ja], (li / A_BUFS) & 1, a.budget, a.st)) {
+                    ok = false;
+                    break;
+                }
+                if (li >= D_BUFS && !mbar_wait(&dempty[jd], ((li / D_BUFS) - 1) & 1, a.budget, a.st)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    // K = 64 per step: 16-byte units 2kk, 2kk+1 (scale bytes 2kk, 2kk+1)
+                    const uint64_t ad = sdesc_kmajor_none(a_base + ja * A_BYTES + kk * 256, 128, 512);
+                    const uint64_t bd = sdesc_kmajor_none(b_base + kk * 256, 128, 512);
+                    mma_mxf4_ss(tmem + D_COL0 + jd * 64, ad, bd, idesc_mxf4(TILE, HEADS, 2 * kk, 2 * kk),
+                                tmem + SFA_COL0 + ja * 4, tmem + SFB_COL, kk);
+                }
+                mma_commit(&adone[ja]);
+                mma_commit(&mdone[jd]);
+                ++done;
+            }
+            // the last commit covers every MMA of this thread
+            if (done > 0) mbar_wait(&mdone[(done - 1) % D_BUFS], ((done - 1) / D_BUFS) & 1, a.budget, a.st);
+        }
+    } else if (warp < 2 + 4 * CPY_GROUPS) {
+        // ============================ copy groups ============================
+        const int cg = (warp - 2) >> 2, quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        for (int li = cg; li < n_act; li += CPY_GROUPS) {
+            const int s = li % STAGES, ja = li % A_BUFS;
+            bool w = mbar_wait(&full[s], (li / STAGES) & 1, a.budget, a.st);
+            if (li >= A_BUFS) w = w && mbar_wait(&adone[ja], ((li / A_BUFS) - 1) & 1, a.budget, a.st);
+            if (!__all_sync(0xffffffffu, w)) break;
+            tc_fence_after();
+            const uint8_t* st_base = sStage + s * MX_STAGE;
+            const uint8_t* src = st_base + row * MX_ROW;   // 68r: rows 17 words apart, no bank conflicts
+            uint32_t c[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) c[i] = ld_u32(src + 4 * i);
+            uint32_t sf[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sf[j] = ld_u32(st_base + (lane + 32 * j) * MX_ROW + CODE_BYTES);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            uint8_t* dA = sA + ja * A_BYTES;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(dA + kmajor64_offset(row, u)) =
+                    make_uint4(c[4 * u], c[4 * u + 1], c[4 * u + 2], c[4 * u + 3]);
+            tmem_st4(tmem + lane_base + SFA_COL0 + ja * 4, sf[0], sf[1], sf[2], sf[3]);
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[ja]);
+        }
+    } else {
+        // ============================ epilogue groups ============================
+        const int eg = (warp - 2 - 4 * CPY_GROUPS) >> 2, quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int64_t n_elems = CAND ? (int64_t)a.n_pool * 8 : a.N;
+        const int64_t nb = (a.N + 7) / 8;
+        const uint32_t tb0 = tmem + ((uint32_t)(quad * 32) << 16) + D_COL0;
+        for (int li = eg; li < n_act; li += EPI_GROUPS) {
+            const int jd = li % D_BUFS;
+            {
+                const bool w = mbar_wait(&mdone[jd], (li / D_BUFS) & 1, a.budget, a.st);
+                if (!__all_sync(0xffffffffu, w)) break;
+            }
+            tc_fence_after();
+            const int tile = t_begin + li;
+            const int64_t e = (int64_t)tile * TILE + row;
+            int64_t sid = e;
+            if (CAND) {
+                const int64_t pi = e >> 3;
+                const int32_t pb = pi < a.n_pool ? a.pool[(int64_t)g * a.n_pool + pi] : -1;
+                sid = (pb >= 0 && (int64_t)pb * 8 + 8 <= a.N) ? (int64_t)pb * 8 + (e & 7) : INT64_MAX;
+            }
+            uint32_t d0[32], d1[32];
+            tmem_ld32(tb0 + jd * 64, d0);
+            tmem_ld32(tb0 + jd * 64 + 32, d1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[jd]);
+            // four chains (head h feeds chain h mod 4) of w_h * 2 ReLU(d_h)
+            float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const float4* w4 = reinterpret_cast<const float4*>(sW);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 wv = w4[i];
+                const uint32_t* dd = i < 8 ? d0 : d1;
+                const int o = (i & 7) * 4;
+                const float x0 = __uint_as_float(dd[o]), x1 = __uint_as_float(dd[o + 1]);
+                const float x2 = __uint_as_float(dd[o + 2]), x3 = __uint_as_float(dd[o + 3]);
+                a4[0] = fmaf(wv.x, x0 + fabsf(x0), a4[0]);
+                a4[1] = fmaf(wv.y, x1 + fabsf(x1), a4[1]);
+                a4[2] = fmaf(wv.z, x2 + fabsf(x2), a4[2]);
+                a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
+            }
+            const float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
+            const bool vis = sid < V && e < n_elems;
+            const float sc = vis ? acc : -INFINITY;
+            if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = sc;
+            if (!CAND && a.bmax) {
+                float m = sc;
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                if ((lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = m;
+            }
+        }
+        // tiles of this CTA past every visible entry: -inf outputs
+        for (int tile = t_begin + n_act + eg; tile < t_end; tile += EPI_GROUPS) {
+            const int64_t e = (int64_t)tile * TILE + row;
+            if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = -INFINITY;
+            if (!CAND && a.bmax && (lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <bool CAND>
+csa2_status launch_fp4(csa2_ctx* ctx, FpArgs& a, cudaStream_t s) {
+    auto kern = index_scan_fp4_kernel<CAND>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+            return CSA2_ERR_CUDA;
+        attr = true;
+    }
+    const int groups = a.B * a.Q;
+    int splits = (int)std::min<int64_t>(a.tiles, std::max<int64_t>(1, ((int64_t)ctx->num_sms + groups - 1) / groups));
+    a.tiles_per_cta = (a.tiles + splits - 1) / splits;
+    splits = (a.tiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
+    kern<<<dim3((unsigned)splits, (unsigned)groups), THREADS, SMEM, s>>>(a);
+    return csa2_launch_status();
+}
+
+}  // namespace
+
+csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const float* w, const void* k_idx, int B,
+                                     int Q, int64_t N, int H_I, const int64_t* n_visible, const int32_t* pool,
+                                     int n_pool, int block, float* scores, float* block_max, cudaStream_t s) {
+    if (H_I != HEADS || block != 8 || (N % 8) != 0 || N == 0) return CSA2_ERR_UNSUPPORTED;
+    if (pool && (n_pool % 16) != 0) return CSA2_ERR_UNSUPPORTED;
+    FpArgs a;
+    a.qmx = reinterpret_cast<const uint8_t*>(q_idx);
+    a.w = w;
+    a.kmx = reinterpret_cast<const uint8_t*>(k_idx);
+    a.nv = n_visible;
+    a.pool = pool;
+    a.scores = scores;
+    a.bmax = block_max;
+    a.st = ctx->status;
+    a.B = B;
+    a.Q = Q;
+    a.N = N;
+    a.n_pool = n_pool;
+    a.tiles_per_cta = 0;
+    a.budget = WAIT_BUDGET;
+    a.stall = 0;
+    if (ctx->stall_next) {
+        a.stall = 1;
+        if (ctx->stall_budget > 0) a.budget = ctx->stall_budget;
+        ctx->stall_next = 0;
+    }
+    a.tiles = pool ? n_pool / 16 : (int)((N + TILE - 1) / TILE);
+    if (a.tiles == 0) return CSA2_OK;
+    return pool ? launch_fp4<true>(ctx, a, s) : launch_fp4<false>(ctx, a, s);
+}

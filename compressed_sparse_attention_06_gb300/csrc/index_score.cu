@@ -7,7 +7,10 @@
 // This file holds the CUDA-core kernel: one thread per entry, the entry's key row
 // in registers, the query's H_I x 128 indexer heads in shared memory (read as
 // warp-wide broadcasts), fp32 FMA over exact bf16 / FP4 products.  It serves f32
-// inputs and is the reference point for the tensor-core scan.
+// inputs, the shapes the tensor-core scans do not cover, and is the reference point
+// for them.  MXFP4 queries are dequantised into shared memory.
+#include <type_traits>
+
 #include "csa2_internal.cuh"
 #include "index_score_tc.cuh"
 
@@ -55,9 +58,27 @@ __device__ __forceinline__ void load_key_row(const void* kI, int64_t row, float 
     }
 }
 
+struct QMx {};   // query tag: MXFP4 rows of 68 bytes per head
+
+template <typename TQ>
+__device__ __forceinline__ void load_queries(const void* qI, int64_t bq, int H_I, float* qs) {
+    if constexpr (std::is_same<TQ, QMx>::value) {
+        const uint8_t* q8 = reinterpret_cast<const uint8_t*>(qI) + bq * (int64_t)H_I * mxfp4_row_bytes(D_IDX);
+        for (int i = threadIdx.x; i < H_I * D_IDX; i += blockDim.x) {
+            const int h = i / D_IDX, d = i % D_IDX;
+            const uint8_t* row = q8 + h * mxfp4_row_bytes(D_IDX);
+            const uint32_t code = (row[d >> 1] >> (4 * (d & 1))) & 0xF;
+            qs[i] = e2m1_to_f32(code) * e8m0_to_f32(row[D_IDX / 2 + d / 32]);
+        }
+    } else {
+        const TQ* qrow = reinterpret_cast<const TQ*>(qI) + bq * (int64_t)H_I * D_IDX;
+        for (int i = threadIdx.x; i < H_I * D_IDX; i += blockDim.x) qs[i] = to_f32<TQ>(qrow[i]);
+    }
+}
+
 template <typename TQ, int KF>
 __global__ void __launch_bounds__(SIMT_TILE) index_score_simt_kernel(
-    const TQ* __restrict__ qI, const float* __restrict__ w, const void* __restrict__ kI, int Q, int64_t N,
+    const void* __restrict__ qI, const float* __restrict__ w, const void* __restrict__ kI, int Q, int64_t N,
     int H_I, const int64_t* __restrict__ n_visible, const int32_t* __restrict__ pool, int n_pool, int block,
     float* __restrict__ scores, float* __restrict__ bmax, unsigned int* st) {
     extern __shared__ float smem[];
@@ -65,8 +86,7 @@ __global__ void __launch_bounds__(SIMT_TILE) index_score_simt_kernel(
     float* ws = smem + H_I * D_IDX;        // [H_I]
     const int64_t bq = blockIdx.y;         // b * Q + q
     const int64_t b = bq / Q;
-    const TQ* qrow = qI + bq * (int64_t)H_I * D_IDX;
-    for (int i = threadIdx.x; i < H_I * D_IDX; i += blockDim.x) qs[i] = to_f32<TQ>(qrow[i]);
+    load_queries<TQ>(qI, bq, H_I, qs);
     for (int i = threadIdx.x; i < H_I; i += blockDim.x) ws[i] = w[bq * H_I + i];
     __syncthreads();
 
@@ -123,7 +143,7 @@ void launch_simt(const void* qI, const float* w, const void* kI, int B, int Q, i
     size_t sm = (size_t)(H_I * D_IDX + H_I) * sizeof(float);
     if (sm > 48 * 1024)
         cudaFuncSetAttribute(index_score_simt_kernel<TQ, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    index_score_simt_kernel<TQ, KF><<<grid, SIMT_TILE, sm, s>>>((const TQ*)qI, w, kI, Q, N, H_I, nv, pool,
+    index_score_simt_kernel<TQ, KF><<<grid, SIMT_TILE, sm, s>>>(qI, w, kI, Q, N, H_I, nv, pool,
                                                                  n_pool, block, scores, bmax, st);
 }
 
@@ -137,7 +157,7 @@ extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_d
     if (d_I != D_IDX) return CSA2_ERR_UNSUPPORTED;
     if (block < 1 || block > 32 || (block & (block - 1))) return CSA2_ERR_INVALID_ARG;
     if (pool_blocks && (block_max || !scores || n_pool < 0)) return CSA2_ERR_INVALID_ARG;
-    if (q_dt != CSA2_F32 && q_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (q_dt != CSA2_F32 && q_dt != CSA2_BF16 && q_dt != CSA2_MXFP4_E8M0x32) return CSA2_ERR_UNSUPPORTED;
     if (k_dt != CSA2_F32 && k_dt != CSA2_BF16 && k_dt != CSA2_MXFP4_E8M0x32) return CSA2_ERR_UNSUPPORTED;
     if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;
     if (B == 0 || Q == 0) return CSA2_OK;
@@ -147,7 +167,13 @@ extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_d
     if (n_elems == 0) return CSA2_OK;
     cudaStream_t s = as_stream(stream);
 
-    // Tensor-core scan for bf16 queries over bf16 or MXFP4 keys.
+    // FP4 tensor-core scan for MXFP4 queries over MXFP4 keys; the kind::f16 scan for
+    // bf16 queries over bf16 or MXFP4 keys.
+    if (q_dt == CSA2_MXFP4_E8M0x32 && k_dt == CSA2_MXFP4_E8M0x32) {
+        csa2_status r = index_score_fp4_dispatch(ctx, q_idx, w, k_idx, B, Q, N, H_I, n_visible, pool_blocks, n_pool,
+                                                 block, scores, block_max, s);
+        if (r != CSA2_ERR_UNSUPPORTED) return r;
+    }
     if (q_dt == CSA2_BF16 && k_dt != CSA2_F32) {
         csa2_status r = index_score_tc_dispatch(ctx, q_idx, w, k_idx, k_dt, B, Q, N, H_I, n_visible,
                                                 pool_blocks, n_pool, block, scores, block_max, s);
@@ -156,7 +182,11 @@ extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_d
 #define CSA2_IS_LAUNCH(TQ, KF)                                                                            \
     launch_simt<TQ, KF>(q_idx, w, k_idx, B, Q, N, H_I, n_visible, pool_blocks, n_pool, block, scores,       \
                         block_max, ctx->status, s)
-    if (q_dt == CSA2_F32) {
+    if (q_dt == CSA2_MXFP4_E8M0x32) {
+        if (k_dt == CSA2_F32) CSA2_IS_LAUNCH(QMx, K_F32);
+        else if (k_dt == CSA2_BF16) CSA2_IS_LAUNCH(QMx, K_BF16);
+        else CSA2_IS_LAUNCH(QMx, K_MX);
+    } else if (q_dt == CSA2_F32) {
         if (k_dt == CSA2_F32) CSA2_IS_LAUNCH(float, K_F32);
         else if (k_dt == CSA2_BF16) CSA2_IS_LAUNCH(float, K_BF16);
         else CSA2_IS_LAUNCH(float, K_MX);

@@ -143,6 +143,21 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= (A[smem desc] x SFA) * (B[smem desc] x SFB)^T with MXFP4 operands:
+// E2M1 values packed two per byte, one UE8M0 scale per 32 K-elements, K = 64 per
+// instruction (kind::mxf4, block scale vector 2X).  sfa_tmem / sfb_tmem address the
+// scale factors in tensor memory; the instruction descriptor picks their byte.
+__device__ __forceinline__ void mma_mxf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Make `bar` track completion of all prior tcgen05 async operations of this thread.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -175,6 +190,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
         CSA2_W8(0), CSA2_W8(8), CSA2_W8(16), CSA2_W8(24)
         : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns (store).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
 }
 
 #undef CSA2_R8
@@ -220,6 +242,34 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t lbo, 
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Instruction descriptor, kind::mxf4 (block-scaled): A and B E2M1 (format 1), both
+// K-major, UE8M0 scales (bit 23), dense K = 64; b_sf_id at bits 4-5 and a_sf_id at
+// bits 29-30 pick the first scale byte of the 32-bit tensor-memory cell (0 or 2 for
+// the 2X scale vector).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t a_sf_id, uint32_t b_sf_id) {
+    return ((b_sf_id & 3u) << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | ((a_sf_id & 3u) << 29);
+}
+
+// Shared-memory descriptor for a K-major operand without swizzle: 8-row x 16-byte
+// core matrices (rows 16 B apart), `lbo` = bytes between core matrices along K,
+// `sbo` = bytes between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_kmajor_none(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;                  // descriptor version for tcgen05
+    return d;                                // layout type 0: no swizzle
+}
+
+// Byte offset of 16-byte unit `u` of row `r` in a no-swizzle K-major tile whose rows
+// are 4 units (64 B) long: core matrices of 128 B, K-adjacent ones 128 B apart
+// (LBO = 128), 8-row groups 512 B apart (SBO = 512).
+__host__ __device__ constexpr uint32_t kmajor64_offset(uint32_t r, uint32_t u) {
+    return (r >> 3) * 512u + u * 128u + (r & 7u) * 16u;
 }
 
 // Byte offset of 16-byte unit `u` (0..7) of row `r` in a 128B-swizzled K-major tile.

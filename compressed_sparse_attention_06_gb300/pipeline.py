@@ -39,11 +39,12 @@ class DecodeBuffers:
     attn_ws: torch.Tensor
     pool_ws: torch.Tensor
     topk_ws: torch.Tensor
+    qI_mx: torch.Tensor          # the indexer query packed to MXFP4 (FP4 QK path)
 
 
 def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch.bfloat16,
                  k: int = TOPK, block: int = POOL_BLOCK, n_keep: int = POOL_KEEP,
-                 window: int = 128) -> DecodeBuffers:
+                 window: int = 128, h_idx: int = 64) -> DecodeBuffers:
     nb = (N + block - 1) // block
     return DecodeBuffers(
         block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
@@ -57,6 +58,7 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
                             dtype=torch.uint8, device=device),
         pool_ws=C._ws(C.csa2_block_pool_workspace_bytes(B * Q, nb, n_keep, torch.device(device).index), device),
         topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_keep * block, k, torch.device(device).index), device),
+        qI_mx=torch.empty((B, Q, h_idx, C.mxfp4_row_bytes(128)), dtype=torch.uint8, device=device),
     )
 
 
@@ -66,7 +68,13 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     """Full layer with the hierarchical pool (CSA2 page, «解码器里的分层索引»):
     scan all visible entries keeping only block maxima, pick the pool, rescore its
     candidates, take the top-k (the top-k of all entries lies inside the pool), and
-    attend over the selected entries plus the window."""
+    attend over the selected entries plus the window.
+
+    With an MXFP4 indexer cache the QK product runs in FP4 (DSA-to-CSA/HCA page,
+    «Lightning Indexer：公式 (13)–(17)»): a bf16/f32 qI is first packed to MXFP4 by
+    the same rule as the keys (into buf.qI_mx); an already packed uint8 qI is used
+    as given."""
+    qI = mxfp4_query(qI, kI, buf.qI_mx)
     C.csa2_index_score(qI, w, kI, n_visible, block=block, want_scores=False, want_block_max=True,
                        block_max=buf.block_max)
     C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws)
@@ -77,8 +85,18 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     return buf
 
 
+def mxfp4_query(qI, kI, out=None):
+    """The indexer query as the scan takes it: packed to MXFP4 when the keys are
+    MXFP4 (uint8 rows) and the query is not packed yet; unchanged otherwise."""
+    if kI.dtype != torch.uint8 or qI.dtype == torch.uint8:
+        return qI
+    return C.csa2_fp4_pack(qI, C.MXFP4_E8M0x32, out=out)
+
+
 def reindex_step(qI, w, kI, pool, n_visible, cand_scores=None, idx=None, k: int = TOPK, block: int = POOL_BLOCK):
-    """Reindex layer: own indexer query over the pooled candidates, then top-k."""
+    """Reindex layer: own indexer query over the pooled candidates, then top-k
+    (FP4 QK product over an MXFP4 cache, as in full_decode_step)."""
+    qI = mxfp4_query(qI, kI)
     sc, _ = C.csa2_index_score(qI, w, kI, n_visible, pool=pool, block=block, scores=cand_scores)
     ids, _ = C.csa2_topk(sc, n_visible, k, pool=pool, block=block, out_idx=idx)
     return ids
@@ -94,7 +112,9 @@ def reuse_attention(q, kv, idx, swa, q_pos, sink, out=None, window: int = 128, s
 
 
 def full_topk_step(qI, w, kI, n_visible, k: int = TOPK, scores=None, idx=None):
-    """Full layer without a pool (encoder / prefill): full scores, then top-k."""
+    """Full layer without a pool (encoder / prefill): full scores, then top-k
+    (FP4 QK product over an MXFP4 cache, as in full_decode_step)."""
+    qI = mxfp4_query(qI, kI)
     sc, _ = C.csa2_index_score(qI, w, kI, n_visible, scores=scores)
     ids, _ = C.csa2_topk(sc, n_visible, k, out_idx=idx)
     return sc, ids
@@ -136,6 +156,7 @@ def prefill_chunk_step(Ca, Cb, Za, Zb, Ba, Bb, prev_Cb, prev_Zb, kv_cache, n_ctx
     over them plus its window."""
     C.csa2_compress(Ca, Za, m, cb=Cb, zb=Zb, ba=Ba, bb=Bb, prev_cb=prev_Cb, prev_zb=prev_Zb, pos0=pos0,
                     flags=write_flags, out=kv_cache[0, n_ctx_entries:], out_seq_stride=0)
+    qI = mxfp4_query(qI, kI)
     C.csa2_index_score(qI, w, kI, buf.n_visible, scores=buf.scores)
     C.csa2_topk(buf.scores, buf.n_visible, k, out_idx=buf.idx, ws=buf.topk_ws)
     C.csa2_sparse_attn(q, kv_cache, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, out=buf.out,

@@ -143,7 +143,8 @@ csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, in
  * with no scale and no softmax, for the entries visible to the query
  * (s < n_visible[b,q]; the causal rule t >= m(j+1) gives n_visible = floor(t/m)).
  *
- *   q_idx  : [B, Q, H_I, d_I] in q_dt (F32 or BF16)
+ *   q_idx  : [B, Q, H_I, d_I] in q_dt (F32 or BF16), or [B, Q, H_I, 68] B with
+ *            q_dt = CSA2_MXFP4_E8M0x32 (packed by csa2_fp4_pack like the keys)
  *   w      : [B, Q, H_I] f32
  *   k_idx  : [B, N, d_I] in k_dt (F32, BF16) or [B, N, d_I/2 + d_I/32] B (MXFP4)
  *   n_visible : [B, Q] int64, device
@@ -158,6 +159,13 @@ csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, in
  *                 pool[c/block]*block + c%block; invalid candidates get -inf
  *   block_max must be NULL.
  * d_I == 128, 1 <= H_I <= 128, block a power of two <= 32, B*Q <= 65535.
+ *
+ * Paths.  MXFP4 queries over MXFP4 keys with H_I == 64, block == 8, N % 8 == 0 (and
+ * n_pool % 16 == 0) run the QK product in FP4 on the tensor cores (the page puts the
+ * indexer QK path in FP4, «Lightning Indexer：公式 (13)–(17)»): E2M1 products with
+ * their E8M0 block scales, fp32 accumulation.  BF16 queries over BF16 or MXFP4 keys
+ * on the same shapes use the bf16/f16 tensor-core scan (exact products, fp32 sums).
+ * Everything else runs on the CUDA cores in fp32.
  */
 csa2_status csa2_index_score(csa2_ctx* ctx,
                              const void* q_idx, csa2_dtype q_dt, const float* w,

@@ -1,6 +1,9 @@
-"""GPU parity of the tensor-core indexer scan (64 heads, N a multiple of 8) against
+"""GPU parity of the tensor-core indexer scans (64 heads, N a multiple of 8) against
 the oracle: full scans with ragged visible counts, several queries sharing a key
-tile, pooled candidates, exact-grid inputs (bit-exact) and extreme MXFP4 scales."""
+tile, pooled candidates, exact-grid inputs (bit-exact) and extreme MXFP4 scales.
+Kinds: "bf16" (bf16 q and K), "mx" (bf16 q, MXFP4 K; kind::f16 scan) and "mxq"
+(MXFP4 q and K: the FP4 QK path, kind::mxf4), where the oracle scores the
+dequantised MXFP4 query."""
 import numpy as np
 import pytest
 import torch
@@ -32,7 +35,7 @@ def _keys(B, N, seed, kind, grid=False, extreme=False):
         KI = (KI.view(B, N, 4, 32) * torch.pow(2.0, e)).view(B, N, 128)
     if grid:
         KI = torch.clamp(torch.round(KI * 2) / 2, -4, 4)
-    if kind == "mx":
+    if kind in ("mx", "mxq"):
         kf = KI.float().reshape(B * N, 128)
         kI = C.csa2_fp4_pack(kf, C.MXFP4_E8M0x32).reshape(B, N, 68)
         K_np = O.mxfp4_unpack(O.mxfp4_pack(kf.cpu().numpy())).reshape(B, N, 128)
@@ -51,18 +54,31 @@ def _queries(B, Q, seed, grid=False):
     return qI.to(torch.bfloat16), w.float()
 
 
-@pytest.mark.parametrize("kind", ["mx", "bf16"])
+def _q_as(kind, qI):
+    """(query passed to the scan, its values for the oracle [B, Q, 64, 128] f64)."""
+    if kind != "mxq":
+        return qI, qI.double().cpu().numpy()
+    B, Q = qI.shape[:2]
+    qf = qI.float().reshape(-1, 128)
+    packed = C.csa2_fp4_pack(qf, C.MXFP4_E8M0x32).reshape(B, Q, 64, 68)
+    ref = O.mxfp4_pack(qf.cpu().numpy())
+    assert np.array_equal(packed.reshape(-1, 68).cpu().numpy(), ref)
+    return packed, O.mxfp4_unpack(ref).reshape(B, Q, 64, 128)
+
+
+@pytest.mark.parametrize("kind", ["mx", "bf16", "mxq"])
 @pytest.mark.parametrize("grid", [False, True])
 def test_full_scan_decode(kind, grid):
     B, Q, N = 4, 1, 128 * 37 + 24
     kI, K_np = _keys(B, N, 101, kind, grid)
     qI, w = _queries(B, Q, 102, grid)
+    qI, qn = _q_as(kind, qI)
     nv = torch.tensor([[N], [N - 3], [1], [129]], dtype=torch.int64, device=DEV)
     sc, bm = C.csa2_index_score(qI, w, kI, nv, want_block_max=True)
     sc, bm = to_np(sc), to_np(bm)
     for b in range(B):
         V = int(nv[b, 0])
-        ref = O.index_score(qI[b, 0].double().cpu().numpy(), w[b, 0].double().cpu().numpy(), K_np[b], V)
+        ref = O.index_score(qn[b, 0], w[b, 0].double().cpu().numpy(), K_np[b], V)
         full_bm = np.full((N + 7) // 8, -np.inf)
         rb = O.block_max(ref, V, 8)
         full_bm[: len(rb)] = rb
@@ -74,11 +90,13 @@ def test_full_scan_decode(kind, grid):
             assert_close(bm[b, 0], full_bm, 1e-5, f"block max {kind} b{b}")
 
 
-def test_full_scan_several_queries_share_tiles():
-    # bf16 keys with Q >= 4 queries per sequence: four queries per key tile, causal
+@pytest.mark.parametrize("kind", ["bf16", "mxq"])
+def test_full_scan_several_queries_share_tiles(kind):
+    # Q = 10 queries per sequence (bf16: four queries per key tile), causal
     B, Q, N = 2, 10, 128 * 9 + 16
-    kI, K_np = _keys(B, N, 111, "bf16")
+    kI, K_np = _keys(B, N, 111, kind)
     qI, w = _queries(B, Q, 112)
+    qI, qn = _q_as(kind, qI)
     nv = torch.tensor([[N, N - 1, N - 2, 900, 800, 128, 127, 1, 0, 555],
                        [5, 500, 1000, N, N, N, 64, 65, 66, 67]], dtype=torch.int64, device=DEV)
     sc, _ = C.csa2_index_score(qI, w, kI, nv)
@@ -86,37 +104,40 @@ def test_full_scan_several_queries_share_tiles():
     for b in range(B):
         for q in range(Q):
             V = int(nv[b, q])
-            ref = O.index_score(qI[b, q].double().cpu().numpy(), w[b, q].double().cpu().numpy(), K_np[b], V)
+            ref = O.index_score(qn[b, q], w[b, q].double().cpu().numpy(), K_np[b], V)
             assert_close(sc[b, q], ref, 1e-5, f"b{b} q{q}")
 
 
-def test_mx_extreme_block_scales():
+@pytest.mark.parametrize("kind", ["mx", "mxq"])
+def test_mx_extreme_block_scales(kind):
     B, N = 2, 1024
-    kI, K_np = _keys(B, N, 121, "mx", extreme=True)
+    kI, K_np = _keys(B, N, 121, kind, extreme=True)
     qI, w = _queries(B, 1, 122)
+    qI, qn = _q_as(kind, qI)
     nv = torch.tensor([[N], [N - 100]], dtype=torch.int64, device=DEV)
     sc, _ = C.csa2_index_score(qI, w, kI, nv)
     sc = to_np(sc)
     for b in range(B):
         V = int(nv[b, 0])
-        ref = O.index_score(qI[b, 0].double().cpu().numpy(), w[b, 0].double().cpu().numpy(), K_np[b], V)
+        ref = O.index_score(qn[b, 0], w[b, 0].double().cpu().numpy(), K_np[b], V)
         # each score is dominated by its largest block; per-element relative check
         fin = np.isfinite(ref)
         err = np.abs(sc[b, 0][fin] - ref[fin])
         scale = np.abs(ref[fin]) + 1e-30
-        bound = 1e-5 * np.maximum(scale, np.abs(O.index_score(np.abs(qI[b, 0].double().cpu().numpy()),
+        bound = 1e-5 * np.maximum(scale, np.abs(O.index_score(np.abs(qn[b, 0]),
                                                               np.abs(w[b, 0].double().cpu().numpy()),
                                                               np.abs(K_np[b]), V))[fin])
         assert np.all(err <= bound), f"worst {np.max(err / bound):.3e}"
         assert np.array_equal(np.isfinite(sc[b, 0]), fin)
 
 
-@pytest.mark.parametrize("kind", ["mx", "bf16"])
+@pytest.mark.parametrize("kind", ["mx", "bf16", "mxq"])
 @pytest.mark.parametrize("n_pool", [64, 2048])
 def test_candidates(kind, n_pool):
     B, N = 3, 8 * 4096
     kI, K_np = _keys(B, N, 131, kind)
     qI, w = _queries(B, 1, 132)
+    qI, qn = _q_as(kind, qI)
     nv = torch.tensor([[N - 1], [20001], [333]], dtype=torch.int64, device=DEV)
     pool = torch.full((B, 1, n_pool), -1, dtype=torch.int32)
     for b in range(B):
@@ -130,7 +151,7 @@ def test_candidates(kind, n_pool):
     sc = to_np(sc)
     for b in range(B):
         V = int(nv[b, 0])
-        full = O.index_score(qI[b, 0].double().cpu().numpy(), w[b, 0].double().cpu().numpy(), K_np[b], V)
+        full = O.index_score(qn[b, 0], w[b, 0].double().cpu().numpy(), K_np[b], V)
         pl = to_np(pool[b, 0])
         exp = np.full(n_pool * 8, -np.inf)
         for c_ in range(n_pool * 8):
@@ -141,25 +162,29 @@ def test_candidates(kind, n_pool):
         assert_close(sc[b, 0], exp, 1e-5, f"candidates {kind} b{b}")
 
 
-def test_tc_equals_cuda_core_on_grid():
+@pytest.mark.parametrize("kind", ["mx", "mxq"])
+def test_tc_equals_cuda_core_on_grid(kind):
     # the same exact-grid problem through the tensor-core path (N % 8 == 0) and the
     # CUDA-core path (N % 8 != 0, one extra invisible entry): identical scores
     B, N = 2, 128 * 5
-    kI, K_np = _keys(B, N + 1, 141, "mx", grid=True)
+    kI, K_np = _keys(B, N + 1, 141, kind, grid=True)
     qI, w = _queries(B, 1, 142, grid=True)
+    qI, _ = _q_as(kind, qI)
     nv = torch.tensor([[N], [N - 77]], dtype=torch.int64, device=DEV)
     sc_tc, _ = C.csa2_index_score(qI, w, kI[:, :N].contiguous(), nv)
     sc_cc, _ = C.csa2_index_score(qI, w, kI, nv)
     np.testing.assert_array_equal(to_np(sc_tc), to_np(sc_cc)[:, :, :N])
 
 
-def test_bounded_wait_times_out_and_context_recovers():
+@pytest.mark.parametrize("kind", ["mx", "mxq"])
+def test_bounded_wait_times_out_and_context_recovers(kind):
     """A producer that never signals (test hook): the consumers' bounded waits expire
     (about 2^27 cycles here), the kernel reports a timeout instead of hanging, and
     the next launch on the same context is correct."""
     B, N = 1, 1024
-    kI, K_np = _keys(B, N, 151, "mx")
+    kI, K_np = _keys(B, N, 151, kind)
     qI, w = _queries(B, 1, 152)
+    qI, qn = _q_as(kind, qI)
     nv = torch.tensor([[N]], dtype=torch.int64, device=DEV)
     C.csa2_ctx_test_stall_next(1 << 27)
     C.csa2_index_score(qI, w, kI, nv)
@@ -168,5 +193,5 @@ def test_bounded_wait_times_out_and_context_recovers():
     assert e.value.status == C.ERR_TIMEOUT
     sc, _ = C.csa2_index_score(qI, w, kI, nv)
     C.csa2_ctx_check()
-    ref = O.index_score(qI[0, 0].double().cpu().numpy(), w[0, 0].double().cpu().numpy(), K_np[0], N)
+    ref = O.index_score(qn[0, 0], w[0, 0].double().cpu().numpy(), K_np[0], N)
     assert_close(to_np(sc)[0, 0], ref, 1e-5, "after timeout")

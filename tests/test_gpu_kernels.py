@@ -125,27 +125,44 @@ def _index_inputs(B, Q, N, H_I, seed, q_dt, k_kind, grid=False):
         qI = torch.clamp(torch.round(qI * 8) / 8, -4, 4)
         KI = torch.clamp(torch.round(KI * 2) / 2, -4, 4)
         w = torch.round(w * 2) / 2
-    qI = qI.to(q_dt)
     w = w.float()
+    if q_dt == "mx":
+        # MXFP4 queries (the FP4 QK path); the oracle scores their dequantised values
+        qf = qI.float().reshape(-1, 128)
+        qI = C.csa2_fp4_pack(qf, C.MXFP4_E8M0x32).reshape(B, Q, H_I, 68)
+        q_ref = O.mxfp4_pack(qf.cpu().numpy())
+        assert np.array_equal(qI.reshape(-1, 68).cpu().numpy(), q_ref)
+        qn = O.mxfp4_unpack(q_ref).reshape(B, Q, H_I, 128)
+    else:
+        qI = qI.to(q_dt)
+        qn = qI.double().cpu().numpy()
     if k_kind == "mx":
         kI = C.csa2_fp4_pack(KI.float().reshape(B * N, 128), C.MXFP4_E8M0x32).reshape(B, N, 68)
         K_np = O.mxfp4_unpack(O.mxfp4_pack(KI.float().reshape(B * N, 128).cpu().numpy())).reshape(B, N, 128)
     else:
         kI = KI.to(torch.float32 if k_kind == "f32" else torch.bfloat16)
         K_np = kI.double().cpu().numpy()
-    return qI, w, kI, K_np
+    return qI, w, kI, K_np, qn
 
 
-@pytest.mark.parametrize("q_dt,k_kind", [(torch.float32, "f32"), (torch.bfloat16, "bf16"),
-                                         (torch.bfloat16, "mx"), (torch.float32, "mx")])
+@pytest.mark.parametrize("q_dt,k_kind,H_I", [(torch.float32, "f32", 8), (torch.bfloat16, "bf16", 64),
+                                             (torch.bfloat16, "mx", 64), (torch.float32, "mx", 8),
+                                             ("mx", "mx", 64), ("mx", "mx", 8), ("mx", "bf16", 8)])
 @pytest.mark.parametrize("grid", [False, True])
-def test_index_score_full_scan(q_dt, k_kind, grid):
-    B, Q, N, H_I = 2, 3, 1000 + 357, 64 if q_dt == torch.bfloat16 else 8
-    qI, w, kI, K_np = _index_inputs(B, Q, N, H_I, 31, q_dt, k_kind, grid)
+def test_index_score_full_scan(q_dt, k_kind, H_I, grid):
+    """N = 1357 (ten tiles and a ragged one; N % 8 != 0 takes the CUDA-core path, so
+    the 64-head MXFP4 cases also run N = 1352 on the tensor cores)."""
+    for N in ((1000 + 357, 1000 + 352) if H_I == 64 else (1000 + 357,)):
+        _full_scan_case(q_dt, k_kind, H_I, grid, N)
+
+
+def _full_scan_case(q_dt, k_kind, H_I, grid, N):
+    B, Q = 2, 3
+    qI, w, kI, K_np, qn = _index_inputs(B, Q, N, H_I, 31, q_dt, k_kind, grid)
     nv = torch.tensor([[N, N - 1, 0], [777, 1, N - 8]], dtype=torch.int64, device=DEV)
     sc, bm = C.csa2_index_score(qI, w, kI, nv, want_block_max=True)
     sc, bm = to_np(sc), to_np(bm)
-    qn, wn = qI.double().cpu().numpy(), w.double().cpu().numpy()
+    wn = w.double().cpu().numpy()
     for b in range(B):
         for q in range(Q):
             V = int(nv[b, q])
@@ -164,10 +181,10 @@ def test_index_score_full_scan(q_dt, k_kind, grid):
                 assert_close(bm[b, q], full, 1e-4, "block max")
 
 
-@pytest.mark.parametrize("k_kind", ["bf16", "mx"])
-def test_index_score_candidates(k_kind):
+@pytest.mark.parametrize("q_dt,k_kind", [(torch.bfloat16, "bf16"), (torch.bfloat16, "mx"), ("mx", "mx")])
+def test_index_score_candidates(q_dt, k_kind):
     B, Q, N, H_I = 2, 1, 5000, 64
-    qI, w, kI, K_np = _index_inputs(B, Q, N, H_I, 41, torch.bfloat16, k_kind)
+    qI, w, kI, K_np, qn = _index_inputs(B, Q, N, H_I, 41, q_dt, k_kind)
     nv = torch.tensor([[N - 3], [4000]], dtype=torch.int64, device=DEV)
     n_pool = 300
     pool = torch.full((B, Q, n_pool), -1, dtype=torch.int32)
@@ -180,7 +197,7 @@ def test_index_score_candidates(k_kind):
     sc, _ = C.csa2_index_score(qI, w, kI, nv, pool=pool)
     idx, val = C.csa2_topk(sc, nv, 512, pool=pool, want_scores=True)
     sc, idx = to_np(sc), to_np(idx)
-    qn, wn = qI.double().cpu().numpy(), w.double().cpu().numpy()
+    wn = w.double().cpu().numpy()
     for b in range(B):
         V = int(nv[b, 0])
         full = O.index_score(qn[b, 0], wn[b, 0], K_np[b], V)

@@ -117,7 +117,10 @@ def test_fp4_decode_1M_full_size():
         np.testing.assert_array_equal(to_np(ki[b]), ki_ref)            # cache bytes, bit-exact
         V = N - 1
         K_np = O.mxfp4_unpack(ki_ref[:V])
-        _, ref_idx = _check_decode_query(b, V, _np(wl["qI"][b, 0]), _np(wl["w"][b, 0]), K_np,
+        # the FP4 QK path: the step packed qI to MXFP4 (bytes bit-exact with the oracle's pack)
+        qI_ref = O.mxfp4_pack(wl["qI"][b, 0].float().cpu().numpy())
+        np.testing.assert_array_equal(to_np(buf.qI_mx[b, 0]), qI_ref)
+        _, ref_idx = _check_decode_query(b, V, O.mxfp4_unpack(qI_ref), _np(wl["w"][b, 0]), K_np,
                                          to_np(buf.idx[b, 0]), to_np(buf.pool[b, 0]), to_np(buf.block_max[b, 0]))
         rows = {int(s): O.nvfp4_unpack(O.nvfp4_pack(W.fp4_rows("kv", b, int(s), 1, N, "cpu").numpy()))[0]
                 for s in ref_idx if s >= 0}
