@@ -168,15 +168,6 @@ __device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& ss) {
     }
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16 (exact:
 // an E2M1 value times an E4M3 scale has at most 6 significant bits).  ca, cb: the
 // chunk's 32 code bytes; scw: its four scale bytes.  Adds the squares to ss.

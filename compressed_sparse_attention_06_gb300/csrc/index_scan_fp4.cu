@@ -8,22 +8,39 @@
 // 64 code bytes + 4 scale bytes per entry.  The block-scaled MMA multiplies the FP4
 // values with their scales applied, so no element is converted on the CUDA cores.
 //
-// Per tile of 128 entries: D[128 entries x 64 heads] = sum over two K=64 steps of
-// (A x SFA)(B x SFB)^T, A = the tile's key codes, B = the query's codes, SFA / SFB
-// their scales in tensor memory, D in fp32 tensor memory.  The block max over 8
-// entries (CSA2 page, «解码器里的分层索引») is fused into the epilogue, or the tile is
-// a list of pooled candidate blocks (Reindex).
+// The pipeline steps over tiles of 256 entries (two MMA sub-tiles of 128): every
+// per-step synchronisation (waits, commits) is paid once per 256 entries.  Per
+// sub-tile: D[128 entries x 64 heads] = sum over two K=64 steps of (A x SFA)(B x
+// SFB)^T, A = the sub-tile's key codes (tensor memory, one entry per lane), B = the
+// query's codes (shared memory), SFA / SFB their E8M0 scales in tensor memory, D in
+// fp32 tensor memory.  The block max over 8 entries (CSA2 page, «解码器里的分层索引»)
+// is fused into the epilogue, or the tile is a list of 32 pooled candidate blocks
+// (Reindex).
 //
 // One CTA per SM (the grid splits each query's tiles over the SMs), 18 warps:
-//   warp 0       producer: bulk copies of 68-byte key rows into a 10-stage ring
-//   warp 1       MMA issuer (one lane); owns the tensor-memory allocation
-//   warps 2-9    two copy groups (alternate tiles): each thread moves its entry's 64
-//                code bytes into the MMA's no-swizzle K-major layout and the group
-//                writes the tile's scale bytes into tensor memory
-//   warps 10-17  two epilogue groups (alternate tiles): each thread reads its entry's
-//                64 head dots, applies ReLU and the head weights, sums, masks the
-//                invisible entries and writes the score / block max
-// Buffers: 4 A tiles (shared memory), 4 D tiles (tensor memory, 64 columns each).
+//   warp 0       producer, into an 8-stage ring of tiles.  Full scan: a tile is
+//                17408 contiguous bytes, one bulk copy; four lanes issue them, lane p
+//                owning stages p and p+4 (one issuing thread alone sustains well under
+//                the HBM read rate).  Candidates: a tile is 32 blocks of 544 bytes,
+//                gathered by all 32 lanes with 16-byte cp.async (544-byte bulk copies
+//                run at a small fraction of the HBM rate), completion arriving on the
+//                stage barrier.
+//   warp 1       MMA issuer (one lane): 4 MMAs and one commit per tile; owns the
+//                tensor-memory allocation
+//   warps 2-9    two copy groups (alternate tiles): each thread stores the 16 code
+//                words of its two entries (one per sub-tile) into tensor memory, and
+//                the group stores the tile's scale bytes next to them
+//   warps 10-17  two epilogue groups (alternate tiles): each thread reads its two
+//                entries' 64 head dots, applies ReLU and the head weights, sums, masks
+//                the invisible entries and writes the scores / block max
+// Tensor memory: 3 D tiles (128 columns), 3 A tiles (32), their scales (8), the
+// query's scales (4) = 508 of 512 columns.
+//
+// Phase safety: every mbarrier is waited on in phase order by construction -- each
+// ring stage belongs to one producer lane and one copy group (the stage count is a
+// multiple of both), buffers >= groups, and the MMA lane waits in tile order -- so no
+// waiter can ask for phase k+1 while phase k is still open (the parity test would
+// pass early).
 //
 // Exactness: E2M1 x E2M1 products and their per-block sums are exact; each block sum
 // is scaled by a power of two and accumulated in fp32.
@@ -39,33 +56,37 @@ namespace {
 
 using namespace sm100;
 
-constexpr int TILE = 128;                    // entries per tile (MMA M)
+constexpr int SUB = 128;                     // entries per MMA (M)
+constexpr int TILE = 2 * SUB;                // entries per pipeline step
 constexpr int HEADS = 64;                    // indexer heads (MMA N)
 constexpr int MX_ROW = 68;                   // bytes of an MXFP4 row of 128 dims
 constexpr int CODE_BYTES = 64;
-constexpr int MX_STAGE = TILE * MX_ROW;      // 8704 B, a multiple of 16
+constexpr int MX_STAGE = TILE * MX_ROW;      // 17408 B, a multiple of 16
+constexpr int BLOCKS_PER_TILE = TILE / 8;    // candidate blocks of 8 entries per tile
 constexpr long long WAIT_BUDGET = 1ll << 31;
 
 constexpr int CPY_GROUPS = 2, EPI_GROUPS = 2;
 constexpr int NWARPS = 2 + 4 * CPY_GROUPS + 4 * EPI_GROUPS;
 constexpr int THREADS = NWARPS * 32;
-constexpr int STAGES = 10, A_BUFS = 4, D_BUFS = 4;
-constexpr int A_BYTES = TILE * CODE_BYTES;   // 8 KB
+constexpr int STAGES = 8, BUFS = 3;          // ring stages; A / D buffers (same index)
+constexpr int PROD_LANES = 4;                // bulk-copy issuers (full scan)
 constexpr int B_BYTES = HEADS * CODE_BYTES;  // 4 KB
+static_assert(STAGES % PROD_LANES == 0 && STAGES % CPY_GROUPS == 0, "stage ownership");
+static_assert(BUFS >= CPY_GROUPS && BUFS >= EPI_GROUPS, "buffer phases");
 
 // shared memory (offsets from a 128-byte aligned base)
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + A_BUFS * A_BYTES;
+constexpr int OFF_B = 0;
 constexpr int OFF_STAGE = OFF_B + B_BYTES;
 constexpr int OFF_W = OFF_STAGE + STAGES * MX_STAGE;
 constexpr int OFF_BAR = OFF_W + HEADS * 4;
-constexpr int N_BARS = 2 * STAGES + 2 * A_BUFS + 2 * D_BUFS;
+constexpr int N_BARS = 2 * STAGES + 3 * BUFS;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
 constexpr int SMEM = OFF_TMEMPTR + 16 + 128;
-// tensor memory: D tiles, then 4 scale columns per A tile, then the query's scales
-constexpr uint32_t D_COL0 = 0;
-constexpr uint32_t SFA_COL0 = D_COL0 + D_BUFS * 64;
-constexpr uint32_t SFB_COL = SFA_COL0 + A_BUFS * 4;
+// tensor memory
+constexpr uint32_t D_COL0 = 0;                          // D[j]: 2 sub-tiles x 64 columns
+constexpr uint32_t A_COL0 = D_COL0 + BUFS * 128;        // A[j]: 2 x 16 columns (128 E2M1 per lane)
+constexpr uint32_t SFA_COL0 = A_COL0 + BUFS * 32;       // SFA[j]: 2 x 4 columns
+constexpr uint32_t SFB_COL = SFA_COL0 + BUFS * 8;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SFB_COL + 4 <= TMEM_COLS, "tensor memory");
 // more than half of the SM's shared memory: one CTA per SM, so the 512-column
@@ -96,17 +117,15 @@ template <bool CAND>
 __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
-    uint8_t* sA = smem + OFF_A;
     uint8_t* sB = smem + OFF_B;
     uint8_t* sStage = smem + OFF_STAGE;
     float* sW = reinterpret_cast<float*>(smem + OFF_W);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* full = bars;                   // [STAGES] rows landed
     uint64_t* empty = full + STAGES;         // [STAGES] rows read by a copy group
-    uint64_t* afull = empty + STAGES;        // [A_BUFS] A tile + its scales written
-    uint64_t* adone = afull + A_BUFS;        // [A_BUFS] MMA done with the A tile
-    uint64_t* mdone = adone + A_BUFS;        // [D_BUFS] D tile ready
-    uint64_t* dempty = mdone + D_BUFS;       // [D_BUFS] D tile read by an epilogue group
+    uint64_t* afull = empty + STAGES;        // [BUFS] A tile + its scales stored
+    uint64_t* done = afull + BUFS;           // [BUFS] the tile's MMAs completed: D ready, A free
+    uint64_t* dempty = done + BUFS;          // [BUFS] D tile read by an epilogue group
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,15 +141,12 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], CAND ? 32 : 1);   // cp.async: one arrival per lane
             mbar_init(&empty[i], 4);
         }
-        for (int j = 0; j < A_BUFS; ++j) {
+        for (int j = 0; j < BUFS; ++j) {
             mbar_init(&afull[j], 4);
-            mbar_init(&adone[j], 1);
-        }
-        for (int j = 0; j < D_BUFS; ++j) {
-            mbar_init(&mdone[j], 1);
+            mbar_init(&done[j], 1);
             mbar_init(&dempty[j], 4);
         }
         fence_mbar_init();
@@ -165,175 +181,183 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    bool ok = true;
 
     if (warp == 0) {
         // ============================ producer ============================
-        if (lane == 0) {
-            int issued = 0;
-            for (int li = 0; li < (a.stall ? 0 : n_act) && ok; ++li) {
+        if (!CAND) {
+            // lane p issues tiles p, p+PL, ... (so it alone uses stages p, p+PL, ...);
+            // a bulk copy of rows*68 bytes (rows a multiple of 8: a multiple of 16 B)
+            constexpr int PL = PROD_LANES;
+            if (lane < PL) {
+                int last = -1;
+                for (int li = lane; li < (a.stall ? 0 : n_act); li += PL) {
+                    const int s = li % STAGES, r = li / STAGES;
+                    if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st)) break;
+                    const int64_t row0 = (int64_t)(t_begin + li) * TILE;
+                    const uint32_t bytes = (uint32_t)(min((int64_t)TILE, a.N - row0) * MX_ROW);
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    bulk_g2s(sStage + s * MX_STAGE, a.kmx + ((int64_t)b * a.N + row0) * MX_ROW, bytes, &full[s]);
+                    last = li;
+                }
+                // no copy may still be writing shared memory when the CTA exits: wait
+                // for this lane's tiles of the last STAGES (no later tile reuses their
+                // stages, so their phases are unambiguous; earlier ones were consumed)
+                for (int li = last; li >= 0 && li > n_act - 1 - STAGES; li -= PL)
+                    mbar_wait(&full[li % STAGES], (li / STAGES) & 1, a.budget, a.st);
+            }
+        } else {
+            for (int li = 0; li < (a.stall ? 0 : n_act); ++li) {
                 const int s = li % STAGES, r = li / STAGES;
-                if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st)) {
-                    ok = false;
-                    break;
-                }
-                const int tile = t_begin + li;
+                const bool w = r == 0 || mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st);
+                if (!__all_sync(0xffffffffu, w)) break;
                 uint8_t* dst = sStage + s * MX_STAGE;
-                if (!CAND) {
-                    const int64_t row0 = (int64_t)tile * TILE;
-                    const int64_t rows = min((int64_t)TILE, a.N - row0);
-                    const uint32_t bytes = (uint32_t)(rows * MX_ROW);
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    bulk_g2s(dst, a.kmx + ((int64_t)b * a.N + row0) * MX_ROW, bytes, &full[s]);
-                } else {
-                    const int32_t* pl = a.pool + (int64_t)g * a.n_pool + (int64_t)tile * 16;
-                    int32_t blk[16];
-                    uint32_t bytes = 0;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        int32_t pb = pl[j];
-                        if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
-                        blk[j] = pb;
-                        if (pb >= 0) bytes += 8 * MX_ROW;
-                    }
-                    mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (blk[j] >= 0)
-                            bulk_g2s(dst + j * 8 * MX_ROW, a.kmx + ((int64_t)b * a.N + (int64_t)blk[j] * 8) * MX_ROW,
-                                     8 * MX_ROW, &full[s]);
+                // 32 candidate blocks of 8 rows (544 contiguous bytes each); empty or
+                // out-of-range slots are skipped (their rows are masked in the epilogue)
+                int32_t pb = a.pool[(int64_t)g * a.n_pool + (int64_t)(t_begin + li) * BLOCKS_PER_TILE + lane];
+                if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
+#pragma unroll 2
+                for (int it = 0; it < BLOCKS_PER_TILE * 34 / 32; ++it) {
+                    const int p = it * 32 + lane;          // piece 0 .. 1087
+                    const int j = p / 34, o = p - 34 * j;
+                    const int32_t bj = __shfl_sync(0xffffffffu, pb, j);
+                    if (bj >= 0)
+                        cp_async16(dst + j * 544 + o * 16,
+                                   a.kmx + ((int64_t)b * a.N + (int64_t)bj * 8) * MX_ROW + o * 16);
                 }
-                ++issued;
+                cp_async_mbar_arrive_noinc(&full[s]);
             }
             // no copy may still be writing shared memory when the CTA exits
-            for (int li = max(0, issued - STAGES); li < issued; ++li)
-                mbar_wait(&full[li % STAGES], (li / STAGES) & 1, a.budget, a.st);
+            cp_async_wait_all();
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
-            int done = 0;
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-            for (int li = 0; li < n_act && ok; ++li) {
-                const int ja = li % A_BUFS, jd = li % D_BUFS;
-                if (!mbar_wait(&afull[ja], (li / A_BUFS) & 1, a.budget, a.st)) {
-                    ok = false;
-                    break;
-                }
-                if (li >= D_BUFS && !mbar_wait(&dempty[jd], ((li / D_BUFS) - 1) & 1, a.budget, a.st)) {
-                    ok = false;
-                    break;
-                }
+            int issued = 0;
+            const uint32_t b_base = smem_u32(sB);
+            for (int li = 0; li < n_act; ++li) {
+                const int j = li % BUFS, u = li / BUFS;
+                if (!mbar_wait(&afull[j], u & 1, a.budget, a.st)) break;
+                if (u > 0 && !mbar_wait(&dempty[j], (u - 1) & 1, a.budget, a.st)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    // K = 64 per step: 16-byte units 2kk, 2kk+1 (scale bytes 2kk, 2kk+1)
-                    const uint64_t ad = sdesc_kmajor_none(a_base + ja * A_BYTES + kk * 256, 128, 512);
-                    const uint64_t bd = sdesc_kmajor_none(b_base + kk * 256, 128, 512);
-                    mma_mxf4_ss(tmem + D_COL0 + jd * 64, ad, bd, idesc_mxf4(TILE, HEADS, 2 * kk, 2 * kk),
-                                tmem + SFA_COL0 + ja * 4, tmem + SFB_COL, kk);
+                for (int sub = 0; sub < 2; ++sub) {
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        // K = 64 per step: A columns 8kk .. 8kk+7, B's 16-byte units 2kk,
+                        // 2kk+1, scale bytes 2kk, 2kk+1
+                        const uint64_t bd = sdesc_kmajor_none(b_base + kk * 256, 128, 512);
+                        mma_mxf4_ts(tmem + D_COL0 + j * 128 + sub * 64, tmem + A_COL0 + j * 32 + sub * 16 + kk * 8, bd,
+                                    idesc_mxf4(SUB, HEADS, 2 * kk, 2 * kk), tmem + SFA_COL0 + j * 8 + sub * 4,
+                                    tmem + SFB_COL, kk);
+                    }
                 }
-                mma_commit(&adone[ja]);
-                mma_commit(&mdone[jd]);
-                ++done;
+                mma_commit(&done[j]);
+                ++issued;
             }
             // the last commit covers every MMA of this thread
-            if (done > 0) mbar_wait(&mdone[(done - 1) % D_BUFS], ((done - 1) / D_BUFS) & 1, a.budget, a.st);
+            if (issued > 0) mbar_wait(&done[(issued - 1) % BUFS], ((issued - 1) / BUFS) & 1, a.budget, a.st);
         }
     } else if (warp < 2 + 4 * CPY_GROUPS) {
         // ============================ copy groups ============================
         const int cg = (warp - 2) >> 2, quad = warp & 3;
-        const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         for (int li = cg; li < n_act; li += CPY_GROUPS) {
-            const int s = li % STAGES, ja = li % A_BUFS;
+            const int s = li % STAGES, j = li % BUFS, u = li / BUFS;
             bool w = mbar_wait(&full[s], (li / STAGES) & 1, a.budget, a.st);
-            if (li >= A_BUFS) w = w && mbar_wait(&adone[ja], ((li / A_BUFS) - 1) & 1, a.budget, a.st);
+            if (u > 0) w = w && mbar_wait(&done[j], (u - 1) & 1, a.budget, a.st);
             if (!__all_sync(0xffffffffu, w)) break;
             tc_fence_after();
             const uint8_t* st_base = sStage + s * MX_STAGE;
-            const uint8_t* src = st_base + row * MX_ROW;   // 68r: rows 17 words apart, no bank conflicts
-            uint32_t c[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) c[i] = ld_u32(src + 4 * i);
-            uint32_t sf[4];
+            for (int sub = 0; sub < 2; ++sub) {
+                // 68-byte rows are 17 words apart: a warp's 32 rows hit 32 banks
+                const uint8_t* src = st_base + (sub * SUB + quad * 32 + lane) * MX_ROW;
+                uint32_t c[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sf[j] = ld_u32(st_base + (lane + 32 * j) * MX_ROW + CODE_BYTES);
+                for (int i = 0; i < 16; ++i) c[i] = ld_u32(src + 4 * i);
+                uint32_t sf[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) sf[q4] = ld_u32(st_base + (sub * SUB + lane + 32 * q4) * MX_ROW + CODE_BYTES);
+                tmem_st16(tmem + lane_base + A_COL0 + j * 32 + sub * 16, c);
+                tmem_st4(tmem + lane_base + SFA_COL0 + j * 8 + sub * 4, sf[0], sf[1], sf[2], sf[3]);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            uint8_t* dA = sA + ja * A_BYTES;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<uint4*>(dA + kmajor64_offset(row, u)) =
-                    make_uint4(c[4 * u], c[4 * u + 1], c[4 * u + 2], c[4 * u + 3]);
-            tmem_st4(tmem + lane_base + SFA_COL0 + ja * 4, sf[0], sf[1], sf[2], sf[3]);
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[ja]);
+            if (lane == 0) mbar_arrive(&afull[j]);
         }
     } else {
         // ============================ epilogue groups ============================
         const int eg = (warp - 2 - 4 * CPY_GROUPS) >> 2, quad = warp & 3;
-        const int row = quad * 32 + lane;
         const int64_t n_elems = CAND ? (int64_t)a.n_pool * 8 : a.N;
         const int64_t nb = (a.N + 7) / 8;
         const uint32_t tb0 = tmem + ((uint32_t)(quad * 32) << 16) + D_COL0;
+        const float4* w4 = reinterpret_cast<const float4*>(sW);
         for (int li = eg; li < n_act; li += EPI_GROUPS) {
-            const int jd = li % D_BUFS;
+            const int j = li % BUFS;
             {
-                const bool w = mbar_wait(&mdone[jd], (li / D_BUFS) & 1, a.budget, a.st);
+                const bool w = mbar_wait(&done[j], (li / BUFS) & 1, a.budget, a.st);
                 if (!__all_sync(0xffffffffu, w)) break;
             }
             tc_fence_after();
             const int tile = t_begin + li;
-            const int64_t e = (int64_t)tile * TILE + row;
-            int64_t sid = e;
-            if (CAND) {
-                const int64_t pi = e >> 3;
-                const int32_t pb = pi < a.n_pool ? a.pool[(int64_t)g * a.n_pool + pi] : -1;
-                sid = (pb >= 0 && (int64_t)pb * 8 + 8 <= a.N) ? (int64_t)pb * 8 + (e & 7) : INT64_MAX;
-            }
-            uint32_t d0[32], d1[32];
-            tmem_ld32(tb0 + jd * 64, d0);
-            tmem_ld32(tb0 + jd * 64 + 32, d1);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[jd]);
-            // four chains (head h feeds chain h mod 4) of w_h * 2 ReLU(d_h)
-            float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const float4* w4 = reinterpret_cast<const float4*>(sW);
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+                const int64_t e = (int64_t)tile * TILE + sub * SUB + quad * 32 + lane;
+                int64_t sid = e;
+                if (CAND) {
+                    const int64_t pi = e >> 3;
+                    const int32_t pb = pi < a.n_pool ? a.pool[(int64_t)g * a.n_pool + pi] : -1;
+                    sid = (pb >= 0 && (int64_t)pb * 8 + 8 <= a.N) ? (int64_t)pb * 8 + (e & 7) : INT64_MAX;
+                }
+                // four chains (head h feeds chain h mod 4) of w_h * 2 ReLU(d_h), over the
+                // two 32-head halves of the sub-tile's D (32 registers at a time)
+                float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 wv = w4[i];
-                const uint32_t* dd = i < 8 ? d0 : d1;
-                const int o = (i & 7) * 4;
-                const float x0 = __uint_as_float(dd[o]), x1 = __uint_as_float(dd[o + 1]);
-                const float x2 = __uint_as_float(dd[o + 2]), x3 = __uint_as_float(dd[o + 3]);
-                a4[0] = fmaf(wv.x, x0 + fabsf(x0), a4[0]);
-                a4[1] = fmaf(wv.y, x1 + fabsf(x1), a4[1]);
-                a4[2] = fmaf(wv.z, x2 + fabsf(x2), a4[2]);
-                a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
-            }
-            const float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
-            const bool vis = sid < V && e < n_elems;
-            const float sc = vis ? acc : -INFINITY;
-            if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = sc;
-            if (!CAND && a.bmax) {
-                float m = sc;
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                if ((lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = m;
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t d[32];
+                    tmem_ld32(tb0 + j * 128 + sub * 64 + hh * 32, d);
+                    tmem_wait_ld();
+                    if (sub == 1 && hh == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&dempty[j]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 wv = w4[hh * 8 + i];
+                        const float x0 = __uint_as_float(d[4 * i]), x1 = __uint_as_float(d[4 * i + 1]);
+                        const float x2 = __uint_as_float(d[4 * i + 2]), x3 = __uint_as_float(d[4 * i + 3]);
+                        a4[0] = fmaf(wv.x, x0 + fabsf(x0), a4[0]);
+                        a4[1] = fmaf(wv.y, x1 + fabsf(x1), a4[1]);
+                        a4[2] = fmaf(wv.z, x2 + fabsf(x2), a4[2]);
+                        a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
+                    }
+                }
+                const float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
+                const bool vis = sid < V && e < n_elems;
+                const float sc = vis ? acc : -INFINITY;
+                if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = sc;
+                if (!CAND && a.bmax) {
+                    float m = sc;
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    if ((lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = m;
+                }
             }
         }
         // tiles of this CTA past every visible entry: -inf outputs
         for (int tile = t_begin + n_act + eg; tile < t_end; tile += EPI_GROUPS) {
-            const int64_t e = (int64_t)tile * TILE + row;
-            if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = -INFINITY;
-            if (!CAND && a.bmax && (lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = -INFINITY;
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+                const int64_t e = (int64_t)tile * TILE + sub * SUB + quad * 32 + lane;
+                if (a.scores && e < n_elems) a.scores[(int64_t)g * n_elems + e] = -INFINITY;
+                if (!CAND && a.bmax && (lane & 7) == 0 && (e >> 3) < nb)
+                    a.bmax[(int64_t)g * nb + (e >> 3)] = -INFINITY;
+            }
         }
     }
     tc_fence_before();
@@ -365,7 +389,7 @@ csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const flo
                                      int Q, int64_t N, int H_I, const int64_t* n_visible, const int32_t* pool,
                                      int n_pool, int block, float* scores, float* block_max, cudaStream_t s) {
     if (H_I != HEADS || block != 8 || (N % 8) != 0 || N == 0) return CSA2_ERR_UNSUPPORTED;
-    if (pool && (n_pool % 16) != 0) return CSA2_ERR_UNSUPPORTED;
+    if (pool && (n_pool % BLOCKS_PER_TILE) != 0) return CSA2_ERR_UNSUPPORTED;
     FpArgs a;
     a.qmx = reinterpret_cast<const uint8_t*>(q_idx);
     a.w = w;
@@ -387,7 +411,7 @@ csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const flo
         if (ctx->stall_budget > 0) a.budget = ctx->stall_budget;
         ctx->stall_next = 0;
     }
-    a.tiles = pool ? n_pool / 16 : (int)((N + TILE - 1) / TILE);
+    a.tiles = pool ? n_pool / BLOCKS_PER_TILE : (int)((N + TILE - 1) / TILE);
     if (a.tiles == 0) return CSA2_OK;
     return pool ? launch_fp4<true>(ctx, a, s) : launch_fp4<false>(ctx, a, s);
 }
