@@ -17,7 +17,7 @@
 // is fused into the epilogue, or the tile is a list of 32 pooled candidate blocks
 // (Reindex).
 //
-// One CTA per SM (the grid splits each query's tiles over the SMs), 18 warps:
+// One CTA per SM (the grid splits each query's tiles over the SMs), 22 warps:
 //   warp 0       producer, into an 8-stage ring of tiles.  Full scan: a tile is
 //                17408 contiguous bytes, one bulk copy; four lanes issue them, lane p
 //                owning stages p and p+4 (one issuing thread alone sustains well under
@@ -30,9 +30,10 @@
 //   warps 2-9    two copy groups (alternate tiles): each thread stores the 16 code
 //                words of its two entries (one per sub-tile) into tensor memory, and
 //                the group stores the tile's scale bytes next to them
-//   warps 10-17  two epilogue groups (alternate tiles): each thread reads its two
-//                entries' 64 head dots, applies ReLU and the head weights, sums, masks
-//                the invisible entries and writes the scores / block max
+//   warps 10-21  three epilogue groups (tiles in turn): each thread reads its two
+//                entries' 64 head dots, applies ReLU and the head weights (packed
+//                f32x2 FMAs), sums, masks the invisible entries and writes the scores /
+//                block max
 // Tensor memory: 3 D tiles (128 columns), 3 A tiles (32), their scales (8), the
 // query's scales (4) = 508 of 512 columns.
 //
@@ -65,7 +66,7 @@ constexpr int MX_STAGE = TILE * MX_ROW;      // 17408 B, a multiple of 16
 constexpr int BLOCKS_PER_TILE = TILE / 8;    // candidate blocks of 8 entries per tile
 constexpr long long WAIT_BUDGET = 1ll << 31;
 
-constexpr int CPY_GROUPS = 2, EPI_GROUPS = 2;
+constexpr int CPY_GROUPS = 2, EPI_GROUPS = 3;
 constexpr int NWARPS = 2 + 4 * CPY_GROUPS + 4 * EPI_GROUPS;
 constexpr int THREADS = NWARPS * 32;
 constexpr int STAGES = 8, BUFS = 3;          // ring stages; A / D buffers (same index)
@@ -112,6 +113,19 @@ struct FpArgs {
 };
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// (a0, a1) = (w0 * x0 + a0, w1 * x1 + a1), one packed f32x2 FMA (each lane rounds
+// like fmaf).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+    asm("{\n\t.reg .b64 acc, wv, xv;\n\t"
+        "mov.b64 acc, {%0, %1};\n\t"
+        "mov.b64 wv, {%2, %3};\n\t"
+        "mov.b64 xv, {%4, %5};\n\t"
+        "fma.rn.f32x2 acc, wv, xv, acc;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
 
 template <bool CAND>
 __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs a) {
@@ -330,10 +344,8 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
                         const float4 wv = w4[hh * 8 + i];
                         const float x0 = __uint_as_float(d[4 * i]), x1 = __uint_as_float(d[4 * i + 1]);
                         const float x2 = __uint_as_float(d[4 * i + 2]), x3 = __uint_as_float(d[4 * i + 3]);
-                        a4[0] = fmaf(wv.x, x0 + fabsf(x0), a4[0]);
-                        a4[1] = fmaf(wv.y, x1 + fabsf(x1), a4[1]);
-                        a4[2] = fmaf(wv.z, x2 + fabsf(x2), a4[2]);
-                        a4[3] = fmaf(wv.w, x3 + fabsf(x3), a4[3]);
+                        ffma2(a4[0], a4[1], wv.x, wv.y, x0 + fabsf(x0), x1 + fabsf(x1));
+                        ffma2(a4[2], a4[3], wv.z, wv.w, x2 + fabsf(x2), x3 + fabsf(x3));
                     }
                 }
                 const float acc = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * 0.5f;
