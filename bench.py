@@ -186,6 +186,7 @@ class FP4Decode(Workload):
     name = "fp4_decode_1M"
     main_name = "csa2_index_score (FP4 QK full scan over MXFP4 keys, fused block max)"
     profile = "index_score_fp4_decode_1M.txt"
+    kernel_files = ("index_scan_fp4.cu", "index_score.cu", "index_score_tc.cuh", "sm100_ptx.cuh", "csa2_internal.cuh")
 
     def __init__(self, B=8, N=1 << 20, seq0=0):
         self.B, self.N, self.seq0 = B, N, seq0
