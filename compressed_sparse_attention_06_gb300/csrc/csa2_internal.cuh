@@ -15,6 +15,7 @@ struct csa2_ctx {
     unsigned int* status;   // device word: bit 0 = out-of-range index, bit 1 = timeout
     int stall_next;         // test hook: next tensor-core scan runs with a silent producer
     long long stall_budget; // wait budget (cycles) for that launch
+    int cluster16;          // 16-CTA clusters of the selection kernel fit: -1 unknown, 0 no, 1 yes
 };
 
 #define CSA2_DEVBIT_RANGE 1u

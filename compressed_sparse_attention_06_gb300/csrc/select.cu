@@ -116,7 +116,8 @@ struct SelShared {
 };
 
 // Block-wide exclusive scan of one value per thread (thread order); `total` gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, SelShared& sh, uint32_t& total) {
+template <class Sh>
+__device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, Sh& sh, uint32_t& total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     uint32_t incl = v;
 #pragma unroll
@@ -758,9 +759,396 @@ void choose_chunks(const csa2_ctx* ctx, int64_t rows, int64_t n_max, int k, size
     smem = n_max <= SEL_SMEM_CAP;
 }
 
+// ---------------------------------------------------------------- cluster selection
+// Few long rows (the decode pool over 131,072 block maxima, the top-512 over 16,384
+// pooled candidates): one thread-block cluster of C CTAs per row.  Each CTA stages its
+// contiguous chunk of keys in shared memory.  The three radix digits (12, 10, 10 bits)
+// are counted per CTA and summed across the cluster through distributed shared
+// memory: each CTA sums one slice of the bins over the cluster, then every CTA reads
+// the slice totals and the one slice that holds the threshold, so all find the same
+// bin.  Finally each CTA emits its winners in index order, at the offset given by the
+// winner and tie counts of the CTAs before it (ties at T go to the lowest indices).
+// Every CTA runs the same sequence of cluster barriers whatever the data, so no
+// barrier can be left waiting for a CTA that took another path.
+constexpr int CL_THREADS = 512;
+constexpr int CL_MAX_CHUNK = 16384;        // keys per CTA (64 KB of shared memory)
+
+struct ClShared {
+    uint32_t hist[NB_A];                   // this CTA's histogram of the current digit
+    uint32_t full[NB_A];                   // the row's histogram (every owner pushes its slice)
+    uint32_t wtot[32];
+    uint32_t wtot_all;
+    uint32_t wgt[32], weq[32];             // per-warp winner / tie counts
+    uint32_t gt, eq;                       // this CTA's keys above T / equal to T
+    uint32_t total;                        // keys counted by the last search, whole row
+    int bin;
+    uint32_t above;
+    uint32_t off, take, nsel;              // emission: output offset, ties taken, row total
+};
+
+__device__ __forceinline__ uint32_t cl_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster; release / acquire orders shared memory.
+__device__ __forceinline__ void cl_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the word at `p` in the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    return ra;
+}
+__device__ __forceinline__ uint32_t cl_ld(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Sum of the words at offset `off` in the shared memory of CTAs 0..7 (bases b[]): the
+// eight loads are issued back to back, one round trip for all.
+__device__ __forceinline__ uint32_t cl_sum8(const uint32_t* b, uint32_t off) {
+    uint32_t v0, v1, v2, v3, v4, v5, v6, v7;
+    asm volatile(
+        "ld.shared::cluster.u32 %0, [%8];\n\t"
+        "ld.shared::cluster.u32 %1, [%9];\n\t"
+        "ld.shared::cluster.u32 %2, [%10];\n\t"
+        "ld.shared::cluster.u32 %3, [%11];\n\t"
+        "ld.shared::cluster.u32 %4, [%12];\n\t"
+        "ld.shared::cluster.u32 %5, [%13];\n\t"
+        "ld.shared::cluster.u32 %6, [%14];\n\t"
+        "ld.shared::cluster.u32 %7, [%15];"
+        : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3), "=r"(v4), "=r"(v5), "=r"(v6), "=r"(v7)
+        : "r"(b[0] + off), "r"(b[1] + off), "r"(b[2] + off), "r"(b[3] + off), "r"(b[4] + off), "r"(b[5] + off),
+          "r"(b[6] + off), "r"(b[7] + off)
+        : "memory");
+    return ((v0 + v1) + (v2 + v3)) + ((v4 + v5) + (v6 + v7));
+}
+
+__device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Cluster-wide: the bin (of nb, searched from the top) holding the remaining-th
+// largest key of the row, and the number of keys in the bins above it, from every
+// CTA's local histogram sh.hist.  CTA r sums bins [r*W, r*W+W) over the cluster and
+// pushes the sums into every CTA's sh.full, so after one more barrier each CTA holds
+// the row's histogram and searches it locally.  sh.total gets the number of keys
+// counted; if remaining exceeds it, bin = 0 and above = 0 (the caller takes all).
+// base[c] = the cluster address of CTA c's ClShared.  blockDim.x == CL_THREADS.
+__device__ void cl_find_bin(ClShared& sh, int nb, uint32_t remaining, uint32_t C, uint32_t rank,
+                            const uint32_t* base, int& bin, uint32_t& above) {
+    const int W = nb / (int)C;             // bins per slice, <= blockDim
+    const uint32_t hist_off = (uint32_t)offsetof(ClShared, hist);
+    const uint32_t full_off = (uint32_t)offsetof(ClShared, full);
+    cl_sync();                             // every CTA's histogram is complete, and every
+                                           // CTA has finished reading its sh.full
+    if ((int)threadIdx.x < W) {
+        const uint32_t off = 4u * (rank * (uint32_t)W + threadIdx.x);
+        uint32_t v = cl_sum8(base, hist_off + off);
+        if (C == 16) v += cl_sum8(base + 8, hist_off + off);
+        for (uint32_t c = 0; c < C; ++c) cl_st(base[c] + full_off + off, v);
+    }
+    cl_sync();                             // every slice is in every CTA's sh.full
+    // local search from the top: thread t sums `per` consecutive bins
+    const int per = nb / (int)blockDim.x;
+    const int top = nb - 1 - (int)threadIdx.x * per;
+    uint32_t loc = 0;
+    for (int j = 0; j < per; ++j) loc += sh.full[top - j];
+    uint32_t total;
+    const uint32_t excl = block_excl_scan_u32(loc, sh, total);
+    if (threadIdx.x == 0) {
+        sh.bin = 0;
+        sh.above = 0u;
+        sh.total = total;
+    }
+    __syncthreads();
+    if (excl < remaining && remaining <= excl + loc) {
+        uint32_t cum = excl;
+        for (int j = 0; j < per; ++j) {
+            const uint32_t c = sh.full[top - j];
+            if (cum + c >= remaining) {
+                sh.bin = top - j;
+                sh.above = cum;
+                break;
+            }
+            cum += c;
+        }
+    }
+    __syncthreads();
+    bin = sh.bin;
+    above = sh.above;
+}
+
+// Keys of elements c0 .. c0+n-1 of the row into skey, and the first digit's local
+// histogram; values are read four at a time when the chunk is 16-byte aligned.
+template <int MODE>
+__device__ void cl_stage(const SelArgs& a, int64_t row, int64_t c0, int n, int64_t V, int64_t n_elems,
+                         uint32_t* skey, uint32_t* hist) {
+    const int tid = threadIdx.x;
+    const float* rowp = a.vals + row * a.ld + c0;
+    const bool vec = (reinterpret_cast<uintptr_t>(rowp) & 15u) == 0;
+    const int nq = vec ? n / 4 : 0;
+    for (int base = 0; base < nq; base += (int)blockDim.x * 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = base + j * (int)blockDim.x + tid;
+            v[j] = q < nq ? reinterpret_cast<const float4*>(rowp)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = base + j * (int)blockDim.x + tid;
+            if (q >= nq) continue;
+            const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t kk[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                kk[c] = elem_info<MODE>(a, row, c0 + 4 * q + c, V, n_elems).valid ? order_key(f[c]) : 0u;
+                if (kk[c]) atomicAdd(&hist[kk[c] >> 20], 1u);
+            }
+            reinterpret_cast<uint4*>(skey)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        }
+    }
+    for (int i = 4 * nq + tid; i < n; i += blockDim.x) {
+        const uint32_t key = key_of<MODE>(a, row, c0 + i, V, n_elems);
+        skey[i] = key;
+        if (key) atomicAdd(&hist[key >> 20], 1u);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(CL_THREADS) sel_cluster_kernel(SelArgs a, int chunk) {
+    extern __shared__ uint32_t skey[];     // [chunk]
+    __shared__ ClShared sh;
+    const uint32_t C = cl_size(), rank = cl_rank();
+    const int64_t row = blockIdx.y;
+    const int64_t V = a.nv[row];
+    const int64_t n_elems = row_elems<MODE>(a, V);
+    const int64_t c0 = (int64_t)rank * chunk;
+    const int n = (int)max((int64_t)0, min((int64_t)chunk, n_elems - c0));
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int k = a.k;
+    uint32_t base[16];                     // cluster addresses of every CTA's ClShared
+#pragma unroll
+    for (int c = 0; c < 16; ++c) base[c] = cl_map(&sh, (uint32_t)c < C ? (uint32_t)c : 0u);
+
+    // stage the chunk's keys and count the first digit (bits 31..20)
+    for (int i = threadIdx.x; i < NB_A; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    cl_stage<MODE>(a, row, c0, n, V, n_elems, skey, sh.hist);
+    __syncthreads();
+    int b1, b2, b3;
+    uint32_t ab1, ab2, ab3;
+    cl_find_bin(sh, NB_A, (uint32_t)k, C, rank, base, b1, ab1);
+    const bool take_all = sh.total <= (uint32_t)k;
+    uint32_t prefix = (uint32_t)b1 << 20;
+    uint32_t rem = take_all ? 0u : (uint32_t)k - ab1;
+    // second digit (bits 19..10) over the keys of the threshold bin; the searches run
+    // (on empty histograms) even when every key is taken, keeping the barriers uniform
+    for (int i = threadIdx.x; i < NB_B; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const uint32_t key = i < n ? skey[i] : 0u;
+        hist_add_warp(sh.hist, (key >> 10) & 0x3FFu, !take_all && key != 0u && (key & 0xFFF00000u) == prefix);
+    }
+    __syncthreads();
+    cl_find_bin(sh, NB_B, take_all ? 1u : rem, C, rank, base, b2, ab2);
+    prefix |= (uint32_t)b2 << 10;
+    rem -= take_all ? 0u : ab2;
+    // third digit (bits 9..0)
+    for (int i = threadIdx.x; i < NB_B; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const uint32_t key = i < n ? skey[i] : 0u;
+        hist_add_warp(sh.hist, key & 0x3FFu, !take_all && key != 0u && (key & 0xFFFFFC00u) == prefix);
+    }
+    __syncthreads();
+    cl_find_bin(sh, NB_B, take_all ? 1u : rem, C, rank, base, b3, ab3);
+    prefix |= (uint32_t)b3;
+    rem -= take_all ? 0u : ab3;
+    // the k-th key T and the number of keys equal to T to take (lowest indices first);
+    // take_all: every valid key (keys are never 0)
+    const uint32_t T = take_all ? 0u : prefix;
+    const uint32_t r_ties = take_all ? 0u : rem;
+
+    // emission, pass 1: per-warp counts over a contiguous segment (32 keys per step)
+    const int seg = ((n + nwarps - 1) / nwarps + 31) / 32 * 32;
+    const int w0 = wid * seg, w1 = min(n, w0 + seg);
+    uint32_t cgt = 0, ceq = 0;
+    for (int j = w0; j < w1; j += 32) {
+        const int i = j + lane;
+        const uint32_t key = i < w1 ? skey[i] : 0u;
+        cgt += __popc(__ballot_sync(FULL_MASK, key > T));
+        ceq += __popc(__ballot_sync(FULL_MASK, T != 0u && key == T));
+    }
+    if (lane == 0) {
+        sh.wgt[wid] = cgt;
+        sh.weq[wid] = ceq;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        uint32_t g = lane < nwarps ? sh.wgt[lane] : 0u, e = lane < nwarps ? sh.weq[lane] : 0u;
+        uint32_t gi = g, ei = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t ug = __shfl_up_sync(FULL_MASK, gi, o), ue = __shfl_up_sync(FULL_MASK, ei, o);
+            if (lane >= o) {
+                gi += ug;
+                ei += ue;
+            }
+        }
+        if (lane < nwarps) {
+            sh.wgt[lane] = gi - g;         // exclusive: before this warp
+            sh.weq[lane] = ei - e;
+        }
+        if (lane == 31) {
+            sh.gt = gi;
+            sh.eq = ei;
+        }
+    }
+    cl_sync();                              // every CTA's counts are published
+    if (wid == 0) {
+        // offsets from the CTAs before this one (index order = rank order)
+        const uint32_t g = lane < C ? cl_ld(base[lane < C ? lane : 0] + (uint32_t)offsetof(ClShared, gt)) : 0u;
+        const uint32_t e = lane < C ? cl_ld(base[lane < C ? lane : 0] + (uint32_t)offsetof(ClShared, eq)) : 0u;
+        uint32_t ei = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(FULL_MASK, ei, o);
+            if (lane >= o) ei += u;
+        }
+        const uint32_t ties_before = ei - e;
+        const uint32_t take = r_ties > ties_before ? min(r_ties - ties_before, e) : 0u;
+        uint32_t sel = g + take, si = sel;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(FULL_MASK, si, o);
+            if (lane >= o) si += u;
+        }
+        if (lane == rank) {
+            sh.off = si - sel;
+            sh.take = take;
+        }
+        if (lane == 31) sh.nsel = si;
+    }
+    __syncthreads();
+    // pass 2: write the winners in index order
+    {
+        const uint32_t off = sh.off, take = sh.take;
+        uint32_t gb = sh.wgt[wid], eb = sh.weq[wid];
+        const unsigned lt = (1u << lane) - 1u;
+        for (int j = w0; j < w1; j += 32) {
+            const int i = j + lane;
+            const uint32_t key = i < w1 ? skey[i] : 0u;
+            const unsigned mg = __ballot_sync(FULL_MASK, key > T);
+            const unsigned me = __ballot_sync(FULL_MASK, T != 0u && key == T);
+            const uint32_t g_before = gb + __popc(mg & lt), e_before = eb + __popc(me & lt);
+            const bool isel = key > T || (T != 0u && key == T && e_before < take);
+            if (isel) {
+                const int64_t pos = (int64_t)off + g_before + min(e_before, take);
+                a.out_idx[row * a.out_len + pos] = (int32_t)elem_info<MODE>(a, row, c0 + i, V, n_elems).id;
+                if (a.out_val) a.out_val[row * a.out_len + pos] = a.vals[row * a.ld + c0 + i];
+            }
+            gb += __popc(mg);
+            eb += __popc(me);
+        }
+    }
+    // the rest of the row: the newest visible block (pool), then padding; spread over
+    // the cluster's threads
+    {
+        int64_t filled = sh.nsel;
+        if (MODE == SEL_POOL && n_elems > 0) {
+            if (rank == 0 && threadIdx.x == 0) a.out_idx[row * a.out_len + filled] = (int32_t)(n_elems - 1);
+            ++filled;
+        }
+        for (int64_t i = filled + (int64_t)rank * blockDim.x + threadIdx.x; i < a.out_len;
+             i += (int64_t)C * blockDim.x) {
+            a.out_idx[row * a.out_len + i] = -1;
+            if (a.out_val) a.out_val[row * a.out_len + i] = -INFINITY;
+        }
+    }
+    cl_sync();                              // no CTA leaves while another reads its counts
+}
+
+// Cluster size for the cluster path, or 0 when it does not apply: few rows, each split
+// into chunks of at most CL_MAX_CHUNK keys.
+int cluster_size_for(csa2_ctx* ctx, int64_t rows, int64_t n_max) {
+    if (n_max < 4096) return 0;
+    for (int c : {16, 8}) {
+        if (rows * c > ctx->num_sms) continue;
+        if (((n_max + c - 1) / c + 31) / 32 * 32 > CL_MAX_CHUNK) return 0;
+        return c;
+    }
+    return 0;
+}
+
+template <int MODE>
+csa2_status launch_cluster(csa2_ctx* ctx, const SelArgs& a, int64_t rows, int64_t n_max, int C, cudaStream_t s) {
+    auto kern = sel_cluster_kernel<MODE>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CL_MAX_CHUNK * 4) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return CSA2_ERR_CUDA;
+        attr = true;
+    }
+    const int chunk = (int)(((n_max + C - 1) / C + 31) / 32 * 32);   // 16-byte aligned chunk starts
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
+    cfg.blockDim = dim3(CL_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)chunk * sizeof(uint32_t);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
+    return csa2_launch_status();
+}
+
 template <int MODE>
 csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, void* ws, size_t ws_bytes,
                        cudaStream_t s) {
+    if (const int C = cluster_size_for(ctx, rows, n_max)) {
+        if (ctx->cluster16 < 0) {
+            // can a 16-CTA cluster of this kernel be resident at all?
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(16, 1, 1);
+            cfg.blockDim = dim3(CL_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = CL_MAX_CHUNK * sizeof(uint32_t);
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 16;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int ncl = 0;
+            cudaFuncSetAttribute(sel_cluster_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CL_MAX_CHUNK * 4);
+            cudaFuncSetAttribute(sel_cluster_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            const bool ok = cudaOccupancyMaxActiveClusters(&ncl, sel_cluster_kernel<MODE>, &cfg) == cudaSuccess &&
+                            ncl > 0;
+            (void)cudaGetLastError();
+            ctx->cluster16 = ok ? 1 : 0;
+        }
+        const int Cuse = (C == 16 && !ctx->cluster16) ? 8 : C;
+        if (((n_max + Cuse - 1) / Cuse + 31) / 32 * 32 <= CL_MAX_CHUNK && rows * Cuse <= ctx->num_sms)
+            return launch_cluster<MODE>(ctx, a, rows, n_max, Cuse, s);
+    }
     bool smem = false;
     choose_chunks(ctx, rows, n_max, a.k, ws_bytes, ws != nullptr, a.chunks, a.chunk_len, smem);
     if (a.chunks > 1) {

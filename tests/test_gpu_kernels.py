@@ -397,22 +397,77 @@ def test_out_of_range_index_is_flagged_not_faulted():
 
 @pytest.mark.parametrize("ties", [False, True])
 def test_selection_without_workspace_matches(ties):
-    """Long rows with no workspace take the one-CTA-per-row path through global
-    memory; the result is the same exact selection."""
+    """Rows too long for the cluster path (more than 16 x 16,384 elements) with no
+    workspace take the one-CTA-per-row path through global memory; with a
+    workspace, the chunk + merge path; the result is the same exact selection."""
     tiny = torch.empty(16, dtype=torch.uint8, device=DEV)
-    bm = _score_rows(2, 131072, 171, ties)
-    nv = torch.tensor([1048575, 700001], dtype=torch.int64, device=DEV)
-    pool = to_np(C.csa2_block_pool(bm, nv, 8, 2048, ws=tiny))
+    nbl = 300000
+    bm = _score_rows(2, nbl, 171, ties)
+    nv = torch.tensor([8 * nbl - 3, 700001], dtype=torch.int64, device=DEV)
     bmn = bm.double().cpu().numpy()
-    for r in range(2):
-        Vr = int(nv[r])
-        np.testing.assert_array_equal(pool[r], O.block_pool(bmn[r][: (Vr + 7) // 8], Vr, 8, 2048))
-    s = _score_rows(3, 70001, 172, ties)
-    nv = torch.tensor([70001, 45000, 100], dtype=torch.int64, device=DEV)
-    idx, _ = C.csa2_topk(s, nv, 512, ws=tiny)
+    for ws in (tiny, None):
+        pool = to_np(C.csa2_block_pool(bm, nv, 8, 2048, ws=ws))
+        for r in range(2):
+            Vr = int(nv[r])
+            np.testing.assert_array_equal(pool[r], O.block_pool(bmn[r][: (Vr + 7) // 8], Vr, 8, 2048))
+    s = _score_rows(3, nbl, 172, ties)
+    nv = torch.tensor([nbl, 45000, 100], dtype=torch.int64, device=DEV)
     sn = s.double().cpu().numpy()
-    for r in range(3):
-        np.testing.assert_array_equal(to_np(idx)[r], O.topk(sn[r], int(nv[r]), 512))
+    for ws in (tiny, None):
+        idx, _ = C.csa2_topk(s, nv, 512, ws=ws)
+        for r in range(3):
+            np.testing.assert_array_equal(to_np(idx)[r], O.topk(sn[r], int(nv[r]), 512))
+
+
+@pytest.mark.parametrize("rows,n,k", [(12, 20000, 512), (9, 131072, 2047), (3, 4096, 4096), (19, 9000, 100)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_cluster_rows_bit_exact(rows, n, k, ties):
+    """Few long rows: one thread-block cluster per row (16 CTAs for up to 9 rows, 8
+    for up to 19).  Visible counts cover full, ragged, tiny, empty and <= k rows."""
+    s = _score_rows(rows, n, 181 + n + rows, ties)
+    nv = torch.tensor([[n, n - 1, 1, 0, k, k + 1, n // 3][r % 7] for r in range(rows)], dtype=torch.int64,
+                      device=DEV)
+    idx, val = C.csa2_topk(s, nv, k, want_scores=True)
+    idx, val, sn = to_np(idx), to_np(val), s.double().cpu().numpy()
+    for r in range(rows):
+        ref = O.topk(sn[r], int(nv[r]), k)
+        np.testing.assert_array_equal(idx[r], ref, err_msg=f"row {r}")
+        exp_val = np.where(ref >= 0, sn[r][np.maximum(ref, 0)], -np.inf)
+        np.testing.assert_array_equal(val[r], exp_val)
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_candidates_cluster_bit_exact(ties):
+    """Top-512 over 2,048 pooled blocks x 8 candidates (the decode Reindex shape) on
+    the cluster path: empty slots (-1), blocks past the visible count, a partial last
+    block; compared with the oracle's restricted top-k."""
+    rows, n_pool, N = 6, 2048, 1 << 20
+    s = _score_rows(rows, n_pool * 8, 191, ties)
+    pool = torch.full((rows, n_pool), -1, dtype=torch.int32)
+    nv = [N - 1, 20000, 16383, 333, 9, 0]
+    for r in range(rows):
+        nb = (nv[r] + 7) // 8
+        if nb == 0:
+            continue
+        m = min(n_pool - 100 * (r % 2) - (r == 0), nb)
+        sel = W.distinct_sample(max(nb - 1, 1), m - 1, 193, r) if m > 1 else torch.empty(0, dtype=torch.int64)
+        blocks = torch.sort(torch.cat([sel, torch.tensor([nb - 1])])).values
+        pool[r, : len(blocks)] = blocks.to(torch.int32)
+        if r == 0:
+            pool[r, len(blocks)] = nb + 3          # a block past the visible count (pool stays ascending)
+    pool = pool.to(DEV)
+    nvt = torch.tensor(nv, dtype=torch.int64, device=DEV)
+    idx, _ = C.csa2_topk(s, nvt, 512, pool=pool)
+    idx, sn, pl = to_np(idx), s.double().cpu().numpy(), to_np(pool)
+    for r in range(rows):
+        full = np.full(max(nv[r], 1), -np.inf)
+        for c_ in range(n_pool * 8):
+            b = pl[r, c_ // 8]
+            e = int(b) * 8 + c_ % 8
+            if b >= 0 and e < nv[r]:
+                full[e] = sn[r, c_]
+        ref = O.reindex_topk(full, pl[r], nv[r], 512)
+        np.testing.assert_array_equal(idx[r], ref, err_msg=f"row {r}")
 
 
 @pytest.mark.parametrize("pos", [0, 1, 4095, 131072, (1 << 20) - 1, (1 << 31) - 7])
