@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
 template <typename TO>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int64_t rows) {
     __shared__ float cs_all[8][32], sn_all[8][32];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * 8 + warp;      // (bq, h)
     if (r >= rows) return;
@@ -337,8 +339,8 @@ csa2_status launch_attn(AttnArgs& a, int B, int Q, cudaStream_t s) {
 template <typename TO>
 csa2_status launch_combine(const AttnArgs& a, int B, int Q, cudaStream_t s) {
     const int64_t rows = (int64_t)B * Q * a.H;
-    attn_combine_kernel<TO><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, rows);
-    return csa2_launch_status();
+    const csa2_status r = launch_pdl(attn_combine_kernel<TO>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, a, rows);
+    return r != CSA2_OK ? r : csa2_launch_status();
 }
 
 template <typename TQ, int KVK, typename TS>

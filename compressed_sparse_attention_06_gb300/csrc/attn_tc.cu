@@ -228,6 +228,8 @@ template <typename TQ>
 __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, RopeTable rope,
                                                          unsigned flags, uint8_t* qimg, float* rope_cs) {
     __shared__ float cs[32], sn[32];
+    pdl_wait();
+    pdl_trigger();
     const int64_t bq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x < 32) {
@@ -275,6 +277,8 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
 
 // RMS factor 1/sqrt(mean(x^2) + 1e-6) of every bf16 row of 512 values (a warp per row).
 __global__ void __launch_bounds__(256) attn_rownorm_kernel(const uint8_t* rows, int64_t n_rows, float* rinv) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= n_rows) return;
@@ -364,6 +368,7 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
 template <bool FP4, typename TO>
 __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();                        // the query images, indices and rows are complete
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + OFF_Q;
     uint8_t* sK = smem + OFF_K;
@@ -798,6 +803,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_trigger();
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -848,8 +854,8 @@ csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, cudaStream_t s) {
         attr = true;
     }
     const int64_t grid = std::min<int64_t>(a.items, ctx->num_sms);
-    kern<<<(unsigned)grid, TC_THREADS, SMEM_BYTES, s>>>(a);
-    return csa2_launch_status();
+    const csa2_status r = launch_pdl(kern, dim3((unsigned)grid), dim3(TC_THREADS), SMEM_BYTES, s, a);
+    return r != CSA2_OK ? r : csa2_launch_status();
 }
 
 }  // namespace
@@ -881,12 +887,13 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     uint8_t* qimg = base + L.qimg;
     float* rope_cs = reinterpret_cast<float*>(base + L.rope);
-    if (c.q_dt == CSA2_BF16)
-        attn_qprep_kernel<__nv_bfloat16><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(
-            reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs);
-    else
-        attn_qprep_kernel<float><<<dim3(8, (unsigned)n_bq), 256, 0, s>>>(reinterpret_cast<const float*>(c.q), c.q_pos, c.H,
-                                                                c.rope, c.flags, qimg, rope_cs);
+    const csa2_status rq =
+        c.q_dt == CSA2_BF16
+            ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs)
+            : launch_pdl(attn_qprep_kernel<float>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs);
+    if (rq != CSA2_OK) return rq;
     TcArgs a;
     a.rinv_kv = nullptr;
     a.rinv_swa = nullptr;

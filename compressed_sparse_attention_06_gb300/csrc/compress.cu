@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(256) compress_kernel(
     const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
     const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
     int64_t out_seq_stride) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t i = blockIdx.x;            // entry within the stream
     const int64_t bseq = blockIdx.y;         // stream (sequence)
     const int t = threadIdx.x;
@@ -194,16 +196,17 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
     const T* zz = (const T*)zb;
     const T* p1 = (const T*)pcb;
     const T* p2 = (const T*)pzb;
+    csa2_status r;
     if (out_dt == CSA2_F32)
-        compress_kernel<T, OUT_F32><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
-                                                            flags, out, oss);
+        r = launch_pdl(compress_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+                       pos0, rope, flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        compress_kernel<T, OUT_BF16><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
-                                                             flags, out, oss);
+        r = launch_pdl(compress_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+                       pos0, rope, flags, out, oss);
     else
-        compress_kernel<T, OUT_FP4><<<grid, block, 0, s>>>(a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m, pos0, rope,
-                                                            flags, out, oss);
-    return csa2_launch_status();
+        r = launch_pdl(compress_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    return r != CSA2_OK ? r : csa2_launch_status();
 }
 
 }  // namespace

@@ -33,6 +33,31 @@ static inline csa2_status csa2_launch_status() {
 
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Programmatic dependent launch.  Kernels of the decode step are launched with
+// launch_pdl so a kernel's CTAs can be scheduled while the previous kernel on the
+// stream finishes; every such kernel calls pdl_wait() before its first global-memory
+// access (read or write), which returns once the previous kernel has completed and its
+// writes are visible, so stream order holds for every dependency.  pdl_trigger() lets
+// the next kernel's CTAs be scheduled.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static inline csa2_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
+
 static inline bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

@@ -15,6 +15,8 @@ namespace {
 template <typename T>
 __global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, uint8_t* __restrict__ out,
                                 int64_t out_ld) {
+    pdl_wait();
+    pdl_trigger();
     const int gpr = c / 16;
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= rows * gpr) return;
@@ -48,6 +50,8 @@ __global__ void fp4_pack_kernel(const T* __restrict__ x, int64_t rows, int c, ui
 template <typename T>
 __global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, uint8_t* __restrict__ out,
                                   int64_t out_ld) {
+    pdl_wait();
+    pdl_trigger();
     const int gpr = d / 32;
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= rows * gpr) return;
@@ -120,9 +124,11 @@ extern "C" csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_
         int64_t n = rows * (c / 16);
         dim3 grid((unsigned)((n + threads - 1) / threads));
         if (x_dt == CSA2_F32)
-            fp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out, out_ld);
+            return launch_pdl(fp4_pack_kernel<float>, dim3(grid), dim3(threads), 0, as_stream(stream), (const float*)x,
+                              rows, c, out, out_ld);
         else
-            fp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out, out_ld);
+            return launch_pdl(fp4_pack_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, as_stream(stream),
+                              (const __nv_bfloat16*)x, rows, c, out, out_ld);
     } else if (fmt == CSA2_MXFP4_E8M0x32) {
         if (c % 128) return CSA2_ERR_INVALID_ARG;  // keeps every row 4-byte aligned
         if (out_ld == 0) out_ld = mxfp4_row_bytes(c);
@@ -130,9 +136,11 @@ extern "C" csa2_status csa2_fp4_pack(csa2_ctx* ctx, const void* x, csa2_dtype x_
         int64_t n = rows * (c / 32);
         dim3 grid((unsigned)((n + threads - 1) / threads));
         if (x_dt == CSA2_F32)
-            mxfp4_pack_kernel<float><<<grid, threads, 0, as_stream(stream)>>>((const float*)x, rows, c, out, out_ld);
+            return launch_pdl(mxfp4_pack_kernel<float>, dim3(grid), dim3(threads), 0, as_stream(stream),
+                              (const float*)x, rows, c, out, out_ld);
         else
-            mxfp4_pack_kernel<__nv_bfloat16><<<grid, threads, 0, as_stream(stream)>>>((const __nv_bfloat16*)x, rows, c, out, out_ld);
+            return launch_pdl(mxfp4_pack_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, as_stream(stream),
+                              (const __nv_bfloat16*)x, rows, c, out, out_ld);
     } else {
         return CSA2_ERR_UNSUPPORTED;
     }

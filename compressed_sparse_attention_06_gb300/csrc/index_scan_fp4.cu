@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     uint64_t* dempty = done + BUFS;          // [BUFS] D tile read by an epilogue group
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
 
+    pdl_wait();                              // inputs of the previous kernel are complete
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y;                // b * Q + q
     const int b = g / a.Q;
@@ -372,6 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
             }
         }
     }
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -391,8 +393,8 @@ csa2_status launch_fp4(csa2_ctx* ctx, FpArgs& a, cudaStream_t s) {
     int splits = (int)std::min<int64_t>(a.tiles, std::max<int64_t>(1, ((int64_t)ctx->num_sms + groups - 1) / groups));
     a.tiles_per_cta = (a.tiles + splits - 1) / splits;
     splits = (a.tiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
-    kern<<<dim3((unsigned)splits, (unsigned)groups), THREADS, SMEM, s>>>(a);
-    return csa2_launch_status();
+    const csa2_status r = launch_pdl(kern, dim3((unsigned)splits, (unsigned)groups), dim3(THREADS), SMEM, s, a);
+    return r != CSA2_OK ? r : csa2_launch_status();
 }
 
 }  // namespace

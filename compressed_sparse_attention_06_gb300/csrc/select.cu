@@ -927,6 +927,7 @@ template <int MODE>
 __global__ void __launch_bounds__(CL_THREADS) sel_cluster_kernel(SelArgs a, int chunk) {
     extern __shared__ uint32_t skey[];     // [chunk]
     __shared__ ClShared sh;
+    pdl_wait();                            // the scores / block maxima are complete
     const uint32_t C = cl_size(), rank = cl_rank();
     const int64_t row = blockIdx.y;
     const int64_t V = a.nv[row];
@@ -1076,6 +1077,7 @@ __global__ void __launch_bounds__(CL_THREADS) sel_cluster_kernel(SelArgs a, int 
             if (a.out_val) a.out_val[row * a.out_len + i] = -INFINITY;
         }
     }
+    pdl_trigger();
     cl_sync();                              // no CTA leaves while another reads its counts
 }
 
@@ -1108,13 +1110,15 @@ csa2_status launch_cluster(csa2_ctx* ctx, const SelArgs& a, int64_t rows, int64_
     cfg.blockDim = dim3(CL_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)chunk * sizeof(uint32_t);
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)C;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait()
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
     return csa2_launch_status();
 }
