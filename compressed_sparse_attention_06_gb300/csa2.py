@@ -29,6 +29,7 @@ EXPORTS = (
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
+    "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed",
 )
 
 
@@ -54,6 +55,10 @@ def _declare(lib):
         "csa2_ctx_test_stall_next": (_i, [_vp, ctypes.c_longlong]),
         "csa2_compress": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _vp, _f, _u,
                                _vp, _i, _i64, _vp]),
+        "csa2_compress_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _f, _u, _vp, _i,
+                                    _i64, _vp]),
+        "csa2_compress_state_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+        "csa2_compress_state_seed": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _vp, _vp]),
         "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
@@ -179,11 +184,57 @@ def csa2_fp4_unpack(b: torch.Tensor, fmt: int, c: int, out_dtype=torch.float32,
     return out
 
 
+def _alloc_rows(shape, c, out_fmt, device):
+    if out_fmt == "fp4":
+        return torch.empty((*shape, fp4_row_bytes(c)), dtype=torch.uint8, device=device)
+    if out_fmt == "mxfp4":
+        return torch.empty((*shape, mxfp4_row_bytes(c)), dtype=torch.uint8, device=device)
+    return torch.empty((*shape, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16, device=device)
+
+
+def _out_dt(out, out_fmt):
+    if out.dtype == torch.uint8:
+        return MXFP4_E8M0x32 if out_fmt == "mxfp4" else FP4_E4M3x16
+    return _dt(out)
+
+
+def csa2_compress_state_bytes(B: int, c: int, m: int, dtype=torch.bfloat16, overlap: bool = True) -> int:
+    return int(_lib().csa2_compress_state_bytes(B, c, m, F32 if dtype == torch.float32 else BF16, int(overlap)))
+
+
+def csa2_compress_state(B: int, c: int, m: int, dtype, device, overlap: bool = True) -> torch.Tensor:
+    """Device buffer for the decode compressor state (no clearing needed)."""
+    return torch.empty(max(16, csa2_compress_state_bytes(B, c, m, dtype, overlap)), dtype=torch.uint8,
+                       device=device)
+
+
+def csa2_compress_step(ca, za, m: int, pos, state, cb=None, zb=None, ba=None, bb=None, rope_base: float = 10000.0,
+                       flags: int = 0, out: Optional[torch.Tensor] = None, out_fmt: str = "f32",
+                       out_seq_stride: int = 0):
+    """One decode step: ca/za (and cb/zb) [B, c] rows of the token at position pos[b]
+    ([B] int64; < 0 skips b).  The token that completes block i writes entry i to row
+    b*out_seq_stride + i of `out` (e.g. a cache [B, N, row])."""
+    B, c = ca.shape
+    st = _lib().csa2_compress_step(ctx(ca.device.index), _p(ca), _p(za), _p(cb), _p(zb), _dt(ca), _p(ba), _p(bb),
+                                   B, c, m, _p(pos), _p(state), rope_base, flags, _vp(out.data_ptr()),
+                                   _out_dt(out, out_fmt), out_seq_stride, _stream(ca))
+    _check("csa2_compress_step", st)
+    return out
+
+
+def csa2_compress_state_seed(ca, za, m: int, state, cb=None, zb=None):
+    """Seed the state from the first n tokens of each sequence ([B, n, c] rows)."""
+    B, n, c = ca.shape
+    st = _lib().csa2_compress_state_seed(ctx(ca.device.index), _p(ca), _p(za), _p(cb), _p(zb), _dt(ca), B, n, c, m,
+                                         _p(state), _stream(ca))
+    _check("csa2_compress_state_seed", st)
+
+
 def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=None, prev_zb=None,
                   pos0=0, rope_base: float = 10000.0, flags: int = 0, out_fmt: str = "f32",
                   out: Optional[torch.Tensor] = None, out_seq_stride: Optional[int] = None) -> torch.Tensor:
     """Compressed entries of one token stream [n, c] or a batch [B, n, c] -> [.., n/m, c]
-    (out_fmt 'f32', 'bf16') or packed FP4 rows ('fp4').  pos0: int or [B] int64 tensor
+    (out_fmt 'f32', 'bf16') or packed FP4 / MXFP4 rows ('fp4', 'mxfp4').  pos0: int or [B] int64 tensor
     (position of each stream's first token).  With `out` and `out_seq_stride`, entry i
     of stream b goes to row b*out_seq_stride + i of `out` (e.g. into a cache)."""
     batched = ca.dim() == 3
@@ -191,13 +242,9 @@ def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=No
     n_ent = n // m
     if out is None:
         shape = (B, n_ent) if batched else (n_ent,)
-        if out_fmt == "fp4":
-            out = torch.empty((*shape, fp4_row_bytes(c)), dtype=torch.uint8, device=ca.device)
-        else:
-            out = torch.empty((*shape, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16,
-                              device=ca.device)
+        out = _alloc_rows(shape, c, out_fmt, ca.device)
     oss = n_ent if out_seq_stride is None else out_seq_stride
-    out_dt = FP4_E4M3x16 if out.dtype == torch.uint8 else _dt(out)
+    out_dt = _out_dt(out, out_fmt)
     if isinstance(pos0, torch.Tensor):
         pos_t = pos0.to(device=ca.device, dtype=torch.int64).contiguous()
     else:

@@ -7,8 +7,16 @@
 // the last 64 channels at position pos0 + m*i -> f32 / bf16 / FP4 store.
 //
 // One CTA per compressed entry, c/4 threads, each owning 4 adjacent channels, so
-// loads are coalesced float4 / 8-byte vectors and a 16-channel FP4 group is 4
-// adjacent lanes.
+// loads are coalesced float4 / 8-byte vectors, a 16-channel FP4 group is 4 adjacent
+// lanes and a 32-channel MXFP4 group 8.
+//
+// Decode step (compress_step_kernel): the compressor state of the Attention-evolution
+// page §3.3 -- the unfinished block's projections and gate logits, and the previous
+// block's overlap half -- lives in a caller-owned buffer; each step stores the new
+// token's rows into its slot, and the token that completes a block emits the block's
+// entry into the cache (a compressed entry exists only once its block is complete,
+// DSA-to-CSA/HCA page «因果边界与短滑窗»), then keeps the block's overlap half for the
+// next one.
 #include "csa2_internal.cuh"
 
 namespace {
@@ -35,48 +43,25 @@ __device__ __forceinline__ float f4get(const float4& v, int k) {
     return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
-enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_FP4 = 2 };
+enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_FP4 = 2, OUT_MX = 3 };
 
+template <typename T>
+__device__ __forceinline__ void copy4(T* dst, const T* src) {
+    if (sizeof(T) == 4)
+        *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
+    else
+        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+}
+
+// One compressed entry; this thread's channels ch .. ch+3 (blockDim.x = c/4): the
+// softmax over the block's m rows (and the m history rows, if any) per channel, the
+// weighted sum, then RMSNorm -> RoPE at `pos` -> store as row `orow` of out.
 template <typename T, int OUT>
-__global__ void __launch_bounds__(256) compress_kernel(
-    const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
-    const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
-    const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
-    const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
-    int64_t out_seq_stride) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t i = blockIdx.x;            // entry within the stream
-    const int64_t bseq = blockIdx.y;         // stream (sequence)
+__device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, const T* hc, const T* hz,
+                                               const float* ba, const float* bb, int c, int m, int64_t pos,
+                                               const RopeTable& rope, unsigned flags, void* out, int64_t orow) {
     const int t = threadIdx.x;
     const int ch = 4 * t;
-    const bool overlap = cb != nullptr;
-    const int64_t in_off = bseq * n_tokens * (int64_t)c;
-    ca += in_off;
-    za += in_off;
-    if (overlap) {
-        cb += in_off;
-        zb += in_off;
-    }
-    if (prev_cb) {
-        prev_cb += bseq * (int64_t)m * c;
-        prev_zb += bseq * (int64_t)m * c;
-    }
-    const int64_t orow = bseq * out_seq_stride + i;
-    // history rows: block i-1 of (cb, zb), or the carried state for block 0
-    const T* hc = nullptr;
-    const T* hz = nullptr;
-    if (overlap) {
-        if (i > 0) {
-            hc = cb + (m * (i - 1)) * (int64_t)c;
-            hz = zb + (m * (i - 1)) * (int64_t)c;
-        } else if (prev_cb) {
-            hc = prev_cb;
-            hz = prev_zb;
-        }
-    }
-    const T* cur_c = ca + (m * i) * (int64_t)c;
-    const T* cur_z = za + (m * i) * (int64_t)c;
 
     // pass 1: per-channel max of the logits
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -143,7 +128,6 @@ __global__ void __launch_bounds__(256) compress_kernel(
     }
     // RoPE on the last 64 channels (interleaved pairs) at the entry's position
     if ((flags & CSA2_W_ROPE) && ch >= c - 64) {
-        const int64_t pos = (pos0_arr ? pos0_arr[bseq] : 0) + (int64_t)m * i;
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             int j = (ch + 2 * p - (c - 64)) >> 1;
@@ -166,7 +150,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
         u.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[2])) |
               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[3])) << 16);
         *reinterpret_cast<uint2*>(o) = u;
-    } else {
+    } else if (OUT == OUT_FP4) {
         // FP4: the 16-channel group is lanes 4g..4g+3 of this warp
         float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -180,6 +164,107 @@ __global__ void __launch_bounds__(256) compress_kernel(
         uint8_t* row = reinterpret_cast<uint8_t*>(out) + orow * fp4_row_bytes(c);
         *reinterpret_cast<uint16_t*>(row + ch / 2) = (uint16_t)codes;
         if ((t & 3) == 0) row[c / 2 + ch / 16] = (uint8_t)sb;
+    } else {
+        // MXFP4: the 32-channel group is lanes 8g..8g+7 of this warp
+        float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const uint32_t code = mx_scale_code(amax);
+        uint32_t codes = 0;
+        if (amax > 0.0f) {
+            const float X = e8m0_to_f32(code);
+            codes = e2m1x2(__fdiv_rn(y[0], X), __fdiv_rn(y[1], X)) | (e2m1x2(__fdiv_rn(y[2], X), __fdiv_rn(y[3], X)) << 8);
+        }
+        uint8_t* row = reinterpret_cast<uint8_t*>(out) + orow * mxfp4_row_bytes(c);
+        *reinterpret_cast<uint16_t*>(row + ch / 2) = (uint16_t)codes;
+        if ((t & 7) == 0) row[c / 2 + ch / 32] = (uint8_t)code;
+    }
+}
+
+template <typename T, int OUT>
+__global__ void __launch_bounds__(256) compress_kernel(
+    const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
+    const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
+    const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
+    const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
+    int64_t out_seq_stride) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = blockIdx.x;            // entry within the stream
+    const int64_t bseq = blockIdx.y;         // stream (sequence)
+    const bool overlap = cb != nullptr;
+    const int64_t in_off = bseq * n_tokens * (int64_t)c;
+    ca += in_off;
+    za += in_off;
+    if (overlap) {
+        cb += in_off;
+        zb += in_off;
+    }
+    if (prev_cb) {
+        prev_cb += bseq * (int64_t)m * c;
+        prev_zb += bseq * (int64_t)m * c;
+    }
+    // history rows: block i-1 of (cb, zb), or the carried state for block 0
+    const T* hc = nullptr;
+    const T* hz = nullptr;
+    if (overlap) {
+        if (i > 0) {
+            hc = cb + (m * (i - 1)) * (int64_t)c;
+            hz = zb + (m * (i - 1)) * (int64_t)c;
+        } else if (prev_cb) {
+            hc = prev_cb;
+            hz = prev_zb;
+        }
+    }
+    const int64_t pos = (pos0_arr ? pos0_arr[bseq] : 0) + (int64_t)m * i;
+    compress_entry<T, OUT>(ca + (m * i) * (int64_t)c, za + (m * i) * (int64_t)c, hc, hz, ba, bb, c, m, pos, rope,
+                           flags, out, bseq * out_seq_stride + i);
+}
+
+// One decode step for B sequences (a CTA each): the token at position pos[b] (< 0: no
+// token this step) is stored in slot pos % m of the state; when it completes block
+// i = pos / m, entry i (position m*i) is written to row b*out_seq_stride + i of out
+// and the block's overlap half becomes the history of block i+1.
+// state per sequence: [ca, za (, cb, zb, prev cb, prev zb)] x [m, c] in T.
+template <typename T, int OUT>
+__global__ void __launch_bounds__(256) compress_step_kernel(
+    const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
+    const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ pos_arr, T* state,
+    int c, int m, const RopeTable rope, unsigned flags, void* __restrict__ out, int64_t out_seq_stride) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t b = blockIdx.x;
+    const int ch = 4 * threadIdx.x;
+    const bool overlap = cb != nullptr;
+    const int64_t mc = (int64_t)m * c;
+    T* st = state + b * (overlap ? 6 : 2) * mc;
+    T* s_ca = st;
+    T* s_za = st + mc;
+    T* s_cb = st + 2 * mc;
+    T* s_zb = st + 3 * mc;
+    T* s_pcb = st + 4 * mc;
+    T* s_pzb = st + 5 * mc;
+    const int64_t p = pos_arr[b];
+    if (p < 0) return;                       // the whole CTA: no token for this sequence
+    const int j = (int)(p % m);
+    const int64_t i = p / m;
+    // each thread only ever touches its own 4 channels of every buffer
+    copy4<T>(s_ca + (int64_t)j * c + ch, ca + b * c + ch);
+    copy4<T>(s_za + (int64_t)j * c + ch, za + b * c + ch);
+    if (overlap) {
+        copy4<T>(s_cb + (int64_t)j * c + ch, cb + b * c + ch);
+        copy4<T>(s_zb + (int64_t)j * c + ch, zb + b * c + ch);
+    }
+    if (j != m - 1) return;                  // the block is not complete yet
+    const bool hist = overlap && i > 0;
+    compress_entry<T, OUT>(s_ca, s_za, hist ? s_pcb : nullptr, hist ? s_pzb : nullptr, ba, bb, c, m,
+                           (int64_t)m * i, rope, flags, out, b * out_seq_stride + i);
+    if (overlap) {
+        for (int r = 0; r < m; ++r) {
+            copy4<T>(s_pcb + (int64_t)r * c + ch, s_cb + (int64_t)r * c + ch);
+            copy4<T>(s_pzb + (int64_t)r * c + ch, s_zb + (int64_t)r * c + ch);
+        }
     }
 }
 
@@ -203,9 +288,39 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
     else if (out_dt == CSA2_BF16)
         r = launch_pdl(compress_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
-    else
+    else if (out_dt == CSA2_FP4_E4M3x16)
         r = launch_pdl(compress_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
+    else
+        r = launch_pdl(compress_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    return r != CSA2_OK ? r : csa2_launch_status();
+}
+
+template <typename T>
+csa2_status launch_step(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+                        const float* bb, const int64_t* pos, void* state, int B, int c, int m, float base,
+                        unsigned flags, void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
+    const RopeTable rope = make_rope_table(base);
+    const T* a = (const T*)ca;
+    const T* z = (const T*)za;
+    const T* b = (const T*)cb;
+    const T* zz = (const T*)zb;
+    T* st = (T*)state;
+    const dim3 grid((unsigned)B), block(c / 4);
+    csa2_status r;
+    if (out_dt == CSA2_F32)
+        r = launch_pdl(compress_step_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+                       flags, out, oss);
+    else if (out_dt == CSA2_BF16)
+        r = launch_pdl(compress_step_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+                       flags, out, oss);
+    else if (out_dt == CSA2_FP4_E4M3x16)
+        r = launch_pdl(compress_step_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+                       flags, out, oss);
+    else
+        r = launch_pdl(compress_step_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+                       flags, out, oss);
     return r != CSA2_OK ? r : csa2_launch_status();
 }
 
@@ -224,7 +339,8 @@ extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* 
     if (prev_cb && !cb) return CSA2_ERR_INVALID_ARG;
     if (flags & ~(CSA2_W_NORM | CSA2_W_ROPE)) return CSA2_ERR_INVALID_ARG;
     if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
-    if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16) return CSA2_ERR_UNSUPPORTED;
+    if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16 && out_dt != CSA2_MXFP4_E8M0x32)
+        return CSA2_ERR_UNSUPPORTED;
     if (n_tokens == 0 || B == 0) return CSA2_OK;
     if (out_seq_stride < n_tokens / m && B > 1) return CSA2_ERR_INVALID_ARG;
     if (!ca || !za || !out) return CSA2_ERR_INVALID_ARG;
@@ -240,4 +356,69 @@ extern "C" csa2_status csa2_compress(csa2_ctx* ctx, const void* ca, const void* 
                                       flags, out, out_dt, out_seq_stride, s);
     return launch_compress<__nv_bfloat16>(ca, za, cb, zb, ba, bb, prev_cb, prev_zb, B, n_tokens, c, m, pos0,
                                           rope_base, flags, out, out_dt, out_seq_stride, s);
+}
+
+extern "C" size_t csa2_compress_state_bytes(int B, int c, int m, csa2_dtype in_dt, int overlap) {
+    if (B <= 0 || c <= 0 || m < 1 || (in_dt != CSA2_F32 && in_dt != CSA2_BF16)) return 0;
+    return (size_t)B * (overlap ? 6 : 2) * (size_t)m * c * (in_dt == CSA2_F32 ? 4 : 2);
+}
+
+extern "C" csa2_status csa2_compress_step(csa2_ctx* ctx, const void* ca, const void* za, const void* cb,
+                                          const void* zb, csa2_dtype in_dt, const float* ba, const float* bb,
+                                          int B, int c, int m, const int64_t* pos, void* state, float rope_base,
+                                          unsigned flags, void* out, csa2_dtype out_dt, int64_t out_seq_stride,
+                                          void* stream) {
+    if (!ctx || B < 0 || B > 65535 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
+    if (c % 128 || c > 1024) return CSA2_ERR_INVALID_ARG;
+    if ((cb == nullptr) != (zb == nullptr)) return CSA2_ERR_INVALID_ARG;
+    if (flags & ~(CSA2_W_NORM | CSA2_W_ROPE)) return CSA2_ERR_INVALID_ARG;
+    if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16 && out_dt != CSA2_MXFP4_E8M0x32)
+        return CSA2_ERR_UNSUPPORTED;
+    if (B == 0) return CSA2_OK;
+    if (!ca || !za || !pos || !state || !out || out_seq_stride < 0) return CSA2_ERR_INVALID_ARG;
+    const size_t va = in_dt == CSA2_F32 ? 16 : 8;
+    if (!aligned(ca, va) || !aligned(za, va) || (cb && (!aligned(cb, va) || !aligned(zb, va))) ||
+        !aligned(state, 16) || (ba && !aligned(ba, 16)) || (bb && !aligned(bb, 16)) || !aligned(out, 16))
+        return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (in_dt == CSA2_F32)
+        return launch_step<float>(ca, za, cb, zb, ba, bb, pos, state, B, c, m, rope_base, flags, out, out_dt,
+                                  out_seq_stride, s);
+    return launch_step<__nv_bfloat16>(ca, za, cb, zb, ba, bb, pos, state, B, c, m, rope_base, flags, out, out_dt,
+                                      out_seq_stride, s);
+}
+
+extern "C" csa2_status csa2_compress_state_seed(csa2_ctx* ctx, const void* ca, const void* za, const void* cb,
+                                                const void* zb, csa2_dtype in_dt, int B, int64_t n_tokens, int c,
+                                                int m, void* state, void* stream) {
+    if (!ctx || B < 0 || n_tokens < 0 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
+    if ((cb == nullptr) != (zb == nullptr)) return CSA2_ERR_INVALID_ARG;
+    if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (B == 0 || n_tokens == 0) return CSA2_OK;
+    if (!ca || !za || !state) return CSA2_ERR_INVALID_ARG;
+    const size_t es = in_dt == CSA2_F32 ? 4 : 2;
+    const bool overlap = cb != nullptr;
+    const size_t row = (size_t)c * es, mc = (size_t)m * row;
+    const size_t spitch = (size_t)n_tokens * row, dpitch = (overlap ? 6 : 2) * mc;
+    const int64_t full = n_tokens / m, tail = n_tokens % m;
+    cudaStream_t s = as_stream(stream);
+    uint8_t* st = reinterpret_cast<uint8_t*>(state);
+    // the unfinished block's rows into slots 0 .. tail-1
+    if (tail > 0) {
+        const size_t off = (size_t)full * m * row, w = (size_t)tail * row;
+        const void* src[4] = {ca, za, cb, zb};
+        for (int k = 0; k < (overlap ? 4 : 2); ++k)
+            CSA2_CHECK_CUDA(cudaMemcpy2DAsync(st + k * mc, dpitch, reinterpret_cast<const uint8_t*>(src[k]) + off,
+                                              spitch, w, (size_t)B, cudaMemcpyDeviceToDevice, s));
+    }
+    // the last complete block's overlap half becomes the history
+    if (overlap && full > 0) {
+        const size_t off = (size_t)(full - 1) * m * row;
+        CSA2_CHECK_CUDA(cudaMemcpy2DAsync(st + 4 * mc, dpitch, reinterpret_cast<const uint8_t*>(cb) + off, spitch, mc,
+                                          (size_t)B, cudaMemcpyDeviceToDevice, s));
+        CSA2_CHECK_CUDA(cudaMemcpy2DAsync(st + 5 * mc, dpitch, reinterpret_cast<const uint8_t*>(zb) + off, spitch, mc,
+                                          (size_t)B, cudaMemcpyDeviceToDevice, s));
+    }
+    return CSA2_OK;
 }

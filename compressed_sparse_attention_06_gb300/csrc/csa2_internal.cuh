@@ -144,6 +144,17 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
 }
 
 // E8M0 byte -> float 2^(b-127) (exact, 2^-127 is a float subnormal).
+// MXFP4 block scale (OCP MX): E8M0 code of 2^(floor(log2 amax) - 2), clamped to
+// 0..254; amax == 0 (or not positive) gives code 0.
+__device__ __forceinline__ uint32_t mx_scale_code(float amax) {
+    if (!(amax > 0.0f)) return 0u;
+    const uint32_t bits = __float_as_uint(amax);
+    const int e = (int)((bits >> 23) & 0xFF);
+    const int fl = (e > 0) ? e - 127 : (31 - __clz((int)bits)) - 149;   // floor(log2 amax)
+    const int cc = fl - 2 + 127;
+    return (uint32_t)(cc < 0 ? 0 : (cc > 254 ? 254 : cc));
+}
+
 __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float((b & 0xFF) << 23);
 }

@@ -64,14 +64,7 @@ __global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, 
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    uint32_t code = 0;
-    if (amax > 0.0f) {
-        uint32_t bits = __float_as_uint(amax);
-        int e = (int)((bits >> 23) & 0xFF);
-        int fl = (e > 0) ? e - 127 : (31 - __clz((int)bits)) - 149;   // floor(log2 amax)
-        int cc = fl - 2 + 127;
-        code = (uint32_t)(cc < 0 ? 0 : (cc > 254 ? 254 : cc));
-    }
+    const uint32_t code = mx_scale_code(amax);
     uint32_t w[4] = {0, 0, 0, 0};
     if (amax > 0.0f) {
         float X = e8m0_to_f32(code);

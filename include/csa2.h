@@ -108,7 +108,8 @@ csa2_status csa2_ctx_test_stall_next(csa2_ctx* ctx, long long budget_cycles);
  *                    (NULL = 0); entry i of stream b sits at pos0[b] + m*i
  *   out            : entry i of stream b goes to row b*out_seq_stride + i of out,
  *                    rows of c values in out_dt (F32, BF16) or c/2 + c/16 bytes
- *                    (CSA2_FP4_E4M3x16); out_seq_stride >= n_tokens/m
+ *                    (CSA2_FP4_E4M3x16) or c/2 + c/32 bytes (CSA2_MXFP4_E8M0x32, the
+ *                    indexer-key format); out_seq_stride >= n_tokens/m
  * n_tokens % m == 0, c % 128 == 0, c <= 1024, m >= 1; RoPE acts on the last 64
  * channels.
  */
@@ -119,6 +120,43 @@ csa2_status csa2_compress(csa2_ctx* ctx,
                           int B, int64_t n_tokens, int c, int m, const int64_t* pos0,
                           float rope_base, unsigned flags, void* out, csa2_dtype out_dt,
                           int64_t out_seq_stride, void* stream);
+
+/*
+ * csa2_compress_step -- the compressor in decode, one token per sequence per call,
+ * with the compressor state of the Attention-evolution page §3.3 (the unfinished
+ * block's projections and gate logits; with overlap, the previous block's overlap
+ * half).  A compressed entry exists once its block is complete (DSA-to-CSA/HCA page
+ * «因果边界与短滑窗»): the token at position p goes to slot p % m of its sequence's
+ * state; if p % m == m-1 it completes block i = p/m, and entry i -- the same value
+ * csa2_compress computes for the whole sequence, at position m*i -- is written to row
+ * b*out_seq_stride + i of out (typically the cache), after which block i's overlap
+ * half becomes the history of block i+1.  Positions count from the sequence start.
+ *   ca, za, cb, zb : [B, c] this step's rows in in_dt (cb/zb NULL: non-overlap)
+ *   ba, bb         : [m, c] f32 or NULL
+ *   pos            : [B] int64 device array; pos[b] < 0 skips sequence b this step
+ *   state          : caller-owned device memory of csa2_compress_state_bytes()
+ *                    bytes (16-byte aligned), per sequence [ca, za (, cb, zb,
+ *                    prev cb, prev zb)] x [m, c] in in_dt.  It needs no clearing
+ *                    before position 0; csa2_compress_state_seed fills it from a
+ *                    prefix of the sequence.
+ *   out, out_dt    : as csa2_compress.
+ * Calls must be made in position order per sequence; the call only reads and
+ * writes device memory on `stream`.
+ */
+size_t csa2_compress_state_bytes(int B, int c, int m, csa2_dtype in_dt, int overlap);
+csa2_status csa2_compress_step(csa2_ctx* ctx,
+                               const void* ca, const void* za, const void* cb, const void* zb,
+                               csa2_dtype in_dt, const float* ba, const float* bb,
+                               int B, int c, int m, const int64_t* pos, void* state,
+                               float rope_base, unsigned flags, void* out, csa2_dtype out_dt,
+                               int64_t out_seq_stride, void* stream);
+/* Seed the state from the first n_tokens tokens of each sequence ([B, n_tokens, c]
+ * rows, e.g. a prefill compressed with csa2_compress): the unfinished block's rows
+ * and the last complete block's overlap half.  The next step is position n_tokens. */
+csa2_status csa2_compress_state_seed(csa2_ctx* ctx,
+                                     const void* ca, const void* za, const void* cb, const void* zb,
+                                     csa2_dtype in_dt, int B, int64_t n_tokens, int c, int m,
+                                     void* state, void* stream);
 
 /*
  * csa2_fp4_pack / csa2_fp4_unpack -- the two 4-bit cache formats.
