@@ -29,7 +29,7 @@ EXPORTS = (
     "csa2_compress", "csa2_fp4_pack", "csa2_fp4_unpack", "csa2_index_score", "csa2_topk",
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
-    "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed",
+    "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
 )
 
 
@@ -70,6 +70,8 @@ def _declare(lib):
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i, _i64, _i64]),
+        "csa2_dense_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
+                                 _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_sparse_attn_noalloc": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                           _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp]),
     }
@@ -367,6 +369,33 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
                                  swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
                                  _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
     _check("csa2_sparse_attn", st)
+    return out, lse
+
+
+def csa2_dense_attn(q, kv, n_visible, k_max: int, swa, q_pos, sink=None, window: int = 128, swa_pos0: int = 0,
+                    kv_fmt: Optional[int] = None, rope_base: float = 10000.0, flags: int = ATTN_DEFAULT,
+                    out_dtype=None, want_lse: bool = False, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None):
+    """HCA attention: each query over compressed entries 0 .. n_visible[b,q]-1 (all it
+    can see) plus the window.  n_visible [B,Q] int64 <= k_max; otherwise as
+    csa2_sparse_attn."""
+    B, Q, H, c = q.shape
+    N = kv.shape[1] if kv is not None else 0
+    kv_dt = (FP4_E4M3x16 if kv_fmt is None else kv_fmt) if kv is not None and kv.dtype == torch.uint8 else \
+        (_dt(kv) if kv is not None else F32)
+    swa_cap = swa.shape[1] if swa is not None else 0
+    swa_dt = _dt(swa) if swa is not None else F32
+    if out is None:
+        out = torch.empty((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k_max, window, q.device.index, N=N, swa_cap=swa_cap)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    st = _lib().csa2_dense_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(n_visible), k_max, _p(swa),
+                                swa_dt, swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
+                                _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
+    _check("csa2_dense_attn", st)
     return out, lse
 
 

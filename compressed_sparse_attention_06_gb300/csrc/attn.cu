@@ -73,6 +73,7 @@ struct AttnArgs {
     int64_t N;
     const int32_t* idx;
     int k;
+    const int64_t* dense_nv;  // dense mode (idx NULL): entries 0 .. dense_nv[bq]-1
     const void* swa;
     int64_t swa_cap, swa_pos0;
     int window;
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
     if (a.flags & CSA2_ROPE) rope_lanes(qv, lane, cs, sn, 1.0f);
 
     const int nw = (int)max((int64_t)0, min((int64_t)a.window, t + 1));   // window rows (positions >= 0)
-    const int n_slots = a.k + nw;
+    const int kq = a.dense_nv ? (int)max((int64_t)0, min((int64_t)a.k, a.dense_nv[bq])) : a.k;
+    const int n_slots = kq + nw;
     const int s_begin = split * a.spl;
     const int s_end = min(n_slots, s_begin + a.spl);
     float m_run = -INFINITY, l_run = 0.0f;
@@ -155,14 +157,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnAr
             bool from_window = false;
             int64_t row = 0;
             if (sl < s_end) {
-                if (sl < a.k) {
-                    const int32_t id = a.idx[bq * a.k + sl];
+                if (sl < kq) {
+                    const int32_t id = a.dense_nv ? sl : a.idx[bq * a.k + sl];
                     if (id >= 0) {
                         if (id < a.N) { ok = 1; row = b * a.N + id; }
                         else if (lane == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
                     }
                 } else {
-                    const int64_t p = t - nw + 1 + (sl - a.k);
+                    const int64_t p = t - nw + 1 + (sl - kq);
                     const int64_t slot = ((p - a.swa_pos0) % a.swa_cap + a.swa_cap) % a.swa_cap;
                     ok = 1;
                     from_window = true;
@@ -387,13 +389,13 @@ extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, 
                     attn_tc_ws_bytes(ctx, B, Q, H, k, window, N, swa_cap));
 }
 
-extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
-                                        csa2_dtype kv_dt, int64_t N, const int32_t* idx, int k, const void* swa,
-                                        csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0, int window,
-                                        const int64_t* q_pos, const float* sink, int B, int Q, int H, int c,
-                                        float rope_base, unsigned flags, void* out, csa2_dtype out_dt, float* lse,
-                                        void* ws, size_t ws_bytes, void* stream) {
-    if (!ctx || B < 0 || Q < 0 || N < 0 || k < 0 || k > 2048 || window < 0 || window > 1024) return CSA2_ERR_INVALID_ARG;
+// Sparse (idx) or dense (dense_nv: entries 0 .. dense_nv[bq]-1, at most k) attention.
+static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv, csa2_dtype kv_dt,
+                             int64_t N, const int32_t* idx, const int64_t* dense_nv, int k, const void* swa,
+                             csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0, int window, const int64_t* q_pos,
+                             const float* sink, int B, int Q, int H, int c, float rope_base, unsigned flags, void* out,
+                             csa2_dtype out_dt, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (!ctx || B < 0 || Q < 0 || N < 0 || k < 0 || window < 0 || window > 1024) return CSA2_ERR_INVALID_ARG;
     if (H < 1 || H > 128) return CSA2_ERR_INVALID_ARG;
     if (c != ATT_C) return CSA2_ERR_UNSUPPORTED;
     if (flags & ~(CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE)) return CSA2_ERR_INVALID_ARG;
@@ -404,7 +406,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;     // one grid.z slice per query
     if (B == 0 || Q == 0) return CSA2_OK;
     if (!q || !q_pos || !out) return CSA2_ERR_INVALID_ARG;
-    if (k > 0 && (!idx || !kv)) return CSA2_ERR_INVALID_ARG;
+    if (k > 0 && ((!idx && !dense_nv) || !kv)) return CSA2_ERR_INVALID_ARG;
     if (window > 0 && (!swa || swa_cap < window)) return CSA2_ERR_INVALID_ARG;
     if (window == 0) swa_cap = 1;
     if (!aligned(kv, 16) || !aligned(swa, 16) || !aligned(q, 16) || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
@@ -418,6 +420,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     tc.N = N;
     tc.idx = idx;
     tc.k = k;
+    tc.dense_nv = dense_nv;
     tc.swa = swa;
     tc.swa_dt = swa_dt;
     tc.swa_cap = swa_cap;
@@ -459,6 +462,7 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
     a.N = N;
     a.idx = idx;
     a.k = k;
+    a.dense_nv = dense_nv;
     a.swa = swa;
     a.swa_cap = swa_cap;
     a.swa_pos0 = swa_pos0;
@@ -491,4 +495,26 @@ extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype
         CSA2_ATT(__nv_bfloat16, KV_FP4);
     }
 #undef CSA2_ATT
+}
+
+extern "C" csa2_status csa2_sparse_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
+                                        csa2_dtype kv_dt, int64_t N, const int32_t* idx, int k, const void* swa,
+                                        csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0, int window,
+                                        const int64_t* q_pos, const float* sink, int B, int Q, int H, int c,
+                                        float rope_base, unsigned flags, void* out, csa2_dtype out_dt, float* lse,
+                                        void* ws, size_t ws_bytes, void* stream) {
+    if (k > 2048) return CSA2_ERR_INVALID_ARG;
+    return attn_impl(ctx, q, q_dt, kv, kv_dt, N, idx, nullptr, k, swa, swa_dt, swa_cap, swa_pos0, window, q_pos, sink,
+                     B, Q, H, c, rope_base, flags, out, out_dt, lse, ws, ws_bytes, stream);
+}
+
+extern "C" csa2_status csa2_dense_attn(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const void* kv,
+                                       csa2_dtype kv_dt, int64_t N, const int64_t* n_visible, int k_max,
+                                       const void* swa, csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0,
+                                       int window, const int64_t* q_pos, const float* sink, int B, int Q, int H,
+                                       int c, float rope_base, unsigned flags, void* out, csa2_dtype out_dt,
+                                       float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (k_max < 0 || k_max > (1 << 22) || (k_max > 0 && !n_visible)) return CSA2_ERR_INVALID_ARG;
+    return attn_impl(ctx, q, q_dt, kv, kv_dt, N, nullptr, n_visible, k_max, swa, swa_dt, swa_cap, swa_pos0, window,
+                     q_pos, sink, B, Q, H, c, rope_base, flags, out, out_dt, lse, ws, ws_bytes, stream);
 }

@@ -81,6 +81,7 @@ struct TcArgs {
     int64_t N;
     const int32_t* idx;           // [B*Q, k]
     int k;
+    const int64_t* dense_nv;      // dense mode: entries 0 .. dense_nv[bq]-1 (idx unused)
     int64_t swa_cap, swa_pos0;
     int window;
     const int64_t* q_pos;
@@ -100,7 +101,7 @@ struct TcArgs {
 
 struct ItemInfo {
     int64_t bq, b, t;
-    int split, nw, n_slots, t0, nt;
+    int split, nw, kq, n_slots, t0, nt;   // kq: cache slots of this query, then nw window slots
 };
 
 __device__ __forceinline__ ItemInfo item_info(const TcArgs& a, int64_t item) {
@@ -110,7 +111,8 @@ __device__ __forceinline__ ItemInfo item_info(const TcArgs& a, int64_t item) {
     r.b = r.bq / a.Q;
     r.t = a.q_pos[r.bq];
     r.nw = (int)max((int64_t)0, min((int64_t)a.window, r.t + 1));
-    r.n_slots = a.k + r.nw;
+    r.kq = a.dense_nv ? (int)max((int64_t)0, min((int64_t)a.k, a.dense_nv[r.bq])) : a.k;
+    r.n_slots = r.kq + r.nw;
     const int n_tiles = (r.n_slots + TC_TILE - 1) / TC_TILE;
     r.t0 = r.split * a.tps;
     r.nt = max(0, min(n_tiles, r.t0 + a.tps) - r.t0);
@@ -128,8 +130,8 @@ __device__ __forceinline__ SlotSrc slot_source(const TcArgs& a, const ItemInfo& 
     r.kind = 0;
     r.row = 0;
     if (slot >= it.n_slots) return r;
-    if (slot < a.k) {
-        const int32_t id = a.idx[it.bq * a.k + slot];
+    if (slot < it.kq) {
+        const int32_t id = a.dense_nv ? slot : a.idx[it.bq * a.k + slot];
         if (id >= 0) {
             if (id < a.N) {
                 r.kind = 1;
@@ -139,7 +141,7 @@ __device__ __forceinline__ SlotSrc slot_source(const TcArgs& a, const ItemInfo& 
             }
         }
     } else {
-        const int64_t p = it.t - it.nw + 1 + (slot - a.k);
+        const int64_t p = it.t - it.nw + 1 + (slot - it.kq);
         r.kind = 2;
         r.row = it.b * a.swa_cap + (((p - a.swa_pos0) % a.swa_cap) + a.swa_cap) % a.swa_cap;
     }
@@ -921,6 +923,7 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.N = c.N;
     a.idx = c.idx;
     a.k = c.k;
+    a.dense_nv = c.dense_nv;
     a.swa_cap = c.swa_cap;
     a.swa_pos0 = c.swa_pos0;
     a.window = c.window;

@@ -19,7 +19,8 @@ struct AttnTcCall {
     csa2_dtype kv_dt;
     int64_t N;
     const int32_t* idx;
-    int k;
+    int k;                 // idx row length, or (dense_nv) the most entries a query takes
+    const int64_t* dense_nv; // dense mode (idx NULL): query bq takes entries 0 .. dense_nv[bq]-1
     const void* swa;
     csa2_dtype swa_dt;
     int64_t swa_cap, swa_pos0;

@@ -307,6 +307,30 @@ csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * csa2_dense_attn -- the HCA attention (DSA-to-CSA/HCA page «HCA：公式 (20)–(26)»,
+ * eq. (26); window of «因果边界与短滑窗»): with the heavily compressed cache (m' = 128,
+ * produced by csa2_compress), each query attends densely over every visible
+ * compressed entry instead of an indexer's selection.  The computation is exactly
+ * csa2_sparse_attn with idx = 0 .. n_visible[b,q]-1, plus the same window, sink,
+ * norms and rotations.
+ *   n_visible : [B, Q] int64, entries 0 .. n_visible-1 of sequence b are taken (the
+ *               causal rule gives n_visible = floor(t/m'))
+ *   k_max     : an upper bound of n_visible (at most 4,194,304); it sizes the key
+ *               splits, so csa2_sparse_attn_workspace_bytes(ctx, B, Q, H, k_max, window,
+ *               N, swa_cap) gives the workspace
+ * Every other argument, layout and error as csa2_sparse_attn.
+ */
+csa2_status csa2_dense_attn(csa2_ctx* ctx,
+                            const void* q, csa2_dtype q_dt,
+                            const void* kv, csa2_dtype kv_dt, int64_t N,
+                            const int64_t* n_visible, int k_max,
+                            const void* swa, csa2_dtype swa_dt, int64_t swa_cap, int64_t swa_pos0,
+                            int window, const int64_t* q_pos, const float* sink,
+                            int B, int Q, int H, int c, float rope_base, unsigned flags,
+                            void* out, csa2_dtype out_dt, float* lse,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
  * csa2_sparse_attn_noalloc -- csa2_sparse_attn for callers that may not allocate
  * device memory.  The paper has no counterpart: this is a deployment convenience.
  *

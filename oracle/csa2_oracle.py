@@ -509,6 +509,17 @@ def sparse_attn(q, kv_entries, idx, swa, swa_pos0: int, t: int, sink=None, windo
 # Whole-layer helpers (loops over batch and queries)
 # =============================================================================
 
+def dense_attn(q, kv_entries, swa, swa_pos0: int, t: int, m: int, sink=None, window: int = 128,
+               flags: int = QNORM | KVNORM | ROPE, base: float = ROPE_BASE):
+    """HCA attention (DSA-to-CSA/HCA page «HCA：公式 (20)–(26)», eq. 26): every compressed
+    entry visible to query t (floor(t/m) of them, m = m' = 128 in V4) is key and
+    value, together with the window (section «因果边界与短滑窗»).  The selection step
+    of CSA is simply absent, so this is sparse_attn with the index list 0..V-1."""
+    V = visible_entries(int(t), m)
+    idx = np.arange(V, dtype=np.int64)
+    return sparse_attn(q, kv_entries, idx, swa, swa_pos0, t, sink, window, flags, base)
+
+
 def full_layer_decode(qI, w, KI, q, kv_entries, swa, swa_pos0, q_pos, m, sink, k=512,
                       window=128, use_pool=False, block=8, n_keep=2048, flags=QNORM | KVNORM | ROPE):
     """One Full-mode layer for the queries of one sequence: score, [pool], top-k,

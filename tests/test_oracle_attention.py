@@ -170,3 +170,39 @@ def test_full_layer_decode_tiny_workload():
         assert np.all(np.diff(ids) > 0)
         assert np.all((res[i]["mass"] > 0) & (res[i]["mass"] < 1))
         assert res[i]["out"].shape == (16, 512)
+
+
+def test_hca_dense_attention_identical_rows_closed_form():
+    """HCA (DSA-to-CSA/HCA page eq. 26): when every visible entry and every window row
+    is the same vector x, the weights do not matter -- without a sink the output is
+    the inverse rotation of the normalised row, RoPE_{-t}(x / rms(x)), for any query."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(512)
+    m, t, H = 128, 128 * 9 + 40, 3
+    kv = np.tile(x, (20, 1))
+    swa = np.tile(x, (128, 1))
+    q = rng.standard_normal((H, 512))
+    out, lse, mass = O.dense_attn(q, kv, swa, 0, t, m, None, 128)
+    expect = O.rope(O.rms_norm(x), t, inverse=True)
+    for h in range(H):
+        np.testing.assert_allclose(out[h], expect, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(mass, 1.0, rtol=1e-12)
+
+
+def test_hca_dense_attention_sees_exactly_the_completed_blocks():
+    """Query t sees entries 0 .. floor(t/m)-1 (t >= m(j+1)): changing the first entry
+    it cannot see leaves the output unchanged, changing the last one it can see
+    changes it, and so does changing entry 0."""
+    rng = np.random.default_rng(6)
+    m, H = 128, 2
+    kv = rng.standard_normal((12, 512))
+    swa = rng.standard_normal((128, 512))
+    q = rng.standard_normal((H, 512))
+    for t in (128 * 5 - 1, 128 * 5, 128 * 5 + 77):
+        V = t // m
+        base, _, _ = O.dense_attn(q, kv, swa, 0, t, m)
+        for j, changes in ((V, False), (V - 1, True), (0, True)):
+            kv2 = kv.copy()
+            kv2[j] = rng.standard_normal(512) * 3
+            o2, _, _ = O.dense_attn(q, kv2, swa, 0, t, m)
+            assert (np.max(np.abs(o2 - base)) > 1e-6) == changes, (t, j)
