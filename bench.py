@@ -9,7 +9,8 @@ rescoring, top-512, sparse shared-KV attention.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload fp4_decode_1M|decode_full_bf16|reindex_reuse_bf16|
-                              prefill_chunk_bf16|tiny_full_layer_fp32]
+                              prefill_chunk_bf16|tiny_full_layer_fp32|hca_decode_1M|compress_step_m4|
+                              fp4_decode_1M_v4pro]
 
 Besides the step rate, the line carries each stage's time (timed separately with
 CUDA events after the main loop) against its own roofline.  With torchrun (N > 1)
@@ -151,6 +152,7 @@ class Workload:
     main_bound = "hbm"
     kernel_files = ("index_score_tc.cu", "index_score.cu", "sm100_ptx.cuh", "csa2_internal.cuh")
     profile = None
+    flush_l2 = False          # True: the step's data fit in L2, flush it before every timed step
     dtype = "f16/bf16 MMA, fp32 accumulate"
 
     def pre(self):
@@ -188,9 +190,12 @@ class FP4Decode(Workload):
     profile = "index_score_fp4_decode_1M.txt"
     kernel_files = ("index_scan_fp4.cu", "index_score.cu", "index_score_tc.cuh", "sm100_ptx.cuh", "csa2_internal.cuh")
 
+    H, K = 64, 512                            # query heads, top-k
+
     def __init__(self, B=8, N=1 << 20, seq0=0):
         self.B, self.N, self.seq0 = B, N, seq0
-        self.H_I, self.H, self.k, self.window, self.block, self.n_keep = 64, 64, 512, 128, 8, 2048
+        self.H_I, self.window, self.block, self.n_keep = 64, 128, 8, 2048
+        self.k = self.K
         self.t = N - 1                        # query position; m = 1 so V = t entries are visible
         self.V = self.t
 
@@ -216,14 +221,15 @@ class FP4Decode(Workload):
                                 out=self.kv[b, r0:r0 + n])
                 C.csa2_fp4_pack(W.fp4_rows("KI", self.seq0 + b, r0, n, N, dev), C.MXFP4_E8M0x32,
                                 out=self.ki[b, r0:r0 + n])
-        wl = W.fp4_decode(dev, B=B, N=N) if self.seq0 == 0 else _offset_workload(W.fp4_decode, dev, B, N, self.seq0)
+        wl = W.fp4_decode(dev, B=B, N=N, H=self.H) if self.seq0 == 0 else \
+            _offset_workload(lambda d, B, N: W.fp4_decode(d, B=B, N=N, H=self.H), dev, B, N, self.seq0)
         self.wl = wl
         self.qI, self.w, self.q, self.swa, self.sink = wl["qI"], wl["w"], wl["q"], wl["swa"], wl["sink"]
         self.C_new, self.Z_new, self.KI_new = wl["C_new"], wl["Z_new"], wl["KI_new"].reshape(B, 128)
         self.q_pos = wl.q_pos.clone()
         self.nv = P.visible_entries(self.q_pos, 1)
         self.pos_new = self.q_pos[:, 0].clone()
-        self.buf = P.alloc_decode(B, 1, N, self.H, 512, dev, out_dtype=torch.bfloat16)
+        self.buf = P.alloc_decode(B, 1, N, self.H, 512, dev, out_dtype=torch.bfloat16, k=self.k)
         self.qI_mx = self.buf.qI_mx
         self.swa_row = self.swa[:, self.t % 128]
         self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new, self.KI_new]
@@ -277,7 +283,9 @@ class FP4Decode(Workload):
         self.pool(); self.cand(); self.topk(); self.attn()
 
     def launches_per_step(self):
-        return 11     # compress, 2 packs, scan, pool chunk+merge, candidate scan, top-k, attention qprep+main+combine
+        # compress, 2 packs, scan, pool, candidate scan, top-k, then per 64-head pass of the
+        # attention: query prep, attention, split combine
+        return 7 + 3 * ((self.H + 63) // 64)
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
@@ -292,7 +300,7 @@ class FP4Decode(Workload):
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
                 ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
                 ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128),
-                ("top-512", self.topk, B * self.n_keep * 8 * 4, 0),
+                (f"top-{self.k}", self.topk, B * self.n_keep * 8 * 4, 0),
                 ("sparse attention", self.attn, attn_bytes, attn_flops)]
 
     def queries(self):
@@ -344,6 +352,13 @@ class FP4Decode(Workload):
         return (f"{n} query(ies) of sequence 0 (full pipeline per query: MXFP4 dequant of all {self.V} indexer "
                 f"rows, f64 scores, block max, pool, top-512, FP4 row gather, attention); numpy f64, BLAS threads "
                 f"for the score matmul, {os.uname().machine}")
+
+
+class V4ProDecode(FP4Decode):
+    """The FP4 decode step with the V4-Pro configuration of the DSA-to-CSA/HCA page's
+    table («两个已公开配置»): CSA top-1024 and 128 query heads (64 indexer heads)."""
+    name = "fp4_decode_1M_v4pro"
+    H, K = 128, 1024
 
 
 class DecodeBF16(Workload):
@@ -495,6 +510,184 @@ class ReindexReuse(Workload):
 
     def entries(self):
         return self.B * 16384
+
+
+class HCADecode(Workload):
+    """HCA layer decode (DSA-to-CSA/HCA page, «HCA：公式 (20)–(26)»): 8 sequences at
+    1M tokens, m' = 128 -> 8,192 FP4 compressed entries each; the step writes the
+    entry completed by the new token (decode compressor with its state) and attends
+    densely over every visible entry plus the 128-token window."""
+    name = "hca_decode_1M"
+    main_name = "csa2_dense_attn (tcgen05, 8,191 FP4 entries + 128 window rows per query)"
+    main_bound = "tensor"
+    kernel_files = ("attn_tc.cu", "attn.cu", "sm100_ptx.cuh", "csa2_internal.cuh")
+    flush_l2 = True
+
+    def __init__(self, B=8, N=1 << 20, seq0=0):
+        self.B, self.tokens, self.seq0 = B, N, seq0
+        self.m = 128
+        self.N = N // self.m                  # HCA entries in the cache
+        self.t = N - 1                        # the new token completes block N/m - 1
+        self.V = self.t // self.m             # entries visible to the query (the new one is not)
+        self.H = 64
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "context_tokens": self.tokens, "m": self.m,
+                "entries": self.N, "heads": self.H, "head_dim": 512, "window": 128, "attention": "dense over all "
+                "visible entries (no indexer)", "cache": "main KV FP4 E2M1+E4M3/16 (288 B/entry)",
+                "l2": "L2 flushed before every timed step (the 19 MB FP4 cache fits in L2)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        C = _C()
+        B, N = self.B, self.N
+        self.kv = torch.empty((B, N, 288), dtype=torch.uint8, device=dev)
+        for b in range(B):
+            C.csa2_fp4_pack(W.fp4_rows("kv", self.seq0 + b, 0, N, N, dev),
+                            C.FP4_E4M3x16, out=self.kv[b])
+        self.q = W.normal_tensor((B, 1, self.H, 512), 6001, 0, torch.bfloat16, dev)
+        self.swa = W.normal_tensor((B, 128, 512), 6002, 0, torch.bfloat16, dev)
+        self.sink = W.normal_tensor((self.H,), 6003, 0, torch.float32, dev)
+        self.q_pos = torch.full((B, 1), self.t, dtype=torch.int64, device=dev)
+        self.nv = torch.full((B, 1), self.V, dtype=torch.int64, device=dev)
+        # decode compressor: the block's first 127 tokens are in the state, the step brings the 128th
+        m = self.m
+        pre_c = W.normal_tensor((B, m - 1, 512), 6004, 0, torch.bfloat16, dev)
+        pre_z = W.normal_tensor((B, m - 1, 512), 6005, 0, torch.bfloat16, dev)
+        self.state = C.csa2_compress_state(B, 512, m, torch.bfloat16, dev, overlap=False)
+        C.csa2_compress_state_seed(pre_c, pre_z, m, self.state)
+        self.c_new = W.normal_tensor((B, 512), 6006, 0, torch.bfloat16, dev)
+        self.z_new = W.normal_tensor((B, 512), 6007, 0, torch.bfloat16, dev)
+        self.pos_new = torch.full((B,), self.t, dtype=torch.int64, device=dev)
+        self.out = torch.empty((B, 1, self.H, 512), dtype=torch.bfloat16, device=dev)
+        self.ws = C._ws(C.csa2_sparse_attn_workspace_bytes(B, 1, self.H, N, 128, N=N, swa_cap=128), dev)
+        self.e2e_in = [self.q, self.c_new, self.z_new]
+        self.e2e_out = [self.out]
+        torch.cuda.synchronize()
+
+    def write(self):
+        C = _C()
+        C.csa2_compress_step(self.c_new, self.z_new, self.m, self.pos_new, self.state, flags=C.W_NORM | C.W_ROPE,
+                             out=self.kv, out_fmt="fp4", out_seq_stride=self.N)
+
+    def main(self):
+        _C().csa2_dense_attn(self.q, self.kv, self.nv, self.N, self.swa, self.q_pos, self.sink, window=128,
+                             out=self.out, ws=self.ws)
+
+    def pre(self):
+        self.write()
+
+    def launches_per_step(self):
+        return 1 + 3              # compress step; query prep, attention, split combine
+
+    def main_amount(self):
+        """FLOPs of one attention launch: QK and PV over (V + 128) rows, 64 heads."""
+        return self.B * self.H * (self.V + 128) * 512 * 4
+
+    def stages(self):
+        B = self.B
+        return [("compress step (m' = 128, FP4 row)", self.write, B * (2 * 1024 + 2 * 128 * 1024 + 288), 0),
+                ("dense attention", self.main, B * ((self.V) * 288 + 128 * 1024 + self.H * 1024 * 2),
+                 self.main_amount())]
+
+    def queries(self):
+        return self.B
+
+    def entries(self):
+        return self.B * self.V
+
+    def oracle_prepare(self, b=0):
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        from oracle import csa2_oracle as O
+        self.o_kv = O.nvfp4_unpack(O.nvfp4_pack(W.fp4_rows("kv", self.seq0 + b, 0, self.N, self.N, "cpu").numpy()))
+        self.o_q = (self.q[b, 0].double().cpu().numpy(), self.swa[b].double().cpu().numpy(),
+                    self.sink.double().cpu().numpy())
+
+    def oracle_query(self):
+        from oracle import csa2_oracle as O
+        q, swa, sink = self.o_q
+        return O.dense_attn(q, self.o_kv, swa, 0, self.t, self.m, sink, 128)[0]
+
+    def oracle_sample_text(self, n):
+        return (f"{n} query(ies) of sequence 0 (oracle dense attention over {self.V} dequantised FP4 entries + "
+                f"128 window rows, 64 heads; numpy f64), {os.uname().machine}")
+
+
+class CompressStepM4(Workload):
+    """The CSA compressor in decode (overlapped, m = 4) for 64 sequences: every step
+    stores the new token's rows in the compressor state and, for the token that
+    completes a block, writes the FP4 main-KV row and the MXFP4 indexer-key row."""
+    name = "compress_step_m4"
+    main_name = "csa2_compress_step (overlap m=4, c=512 FP4 row + c=128 MXFP4 row)"
+    kernel_files = ("compress.cu", "csa2_internal.cuh")
+    flush_l2 = True
+
+    def __init__(self, B=64, N=None, seq0=0):
+        self.B, self.m = B, 4
+        self.t = 4 * 4096 - 1                 # completes a block at every timed step
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "m": self.m, "overlap": True,
+                "rows": "main KV c=512 -> FP4 288 B; indexer K c=128 -> MXFP4 68 B", "flags": "RMSNorm + RoPE",
+                "l2": "L2 flushed before every timed step (state and rows fit in L2)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        C = _C()
+        B, m = self.B, self.m
+        self.new = {c: [W.normal_tensor((B, c), 6100 + c, k, torch.bfloat16, dev) for k in range(4)]
+                    for c in (512, 128)}
+        self.bias = {c: (W.normal_tensor((m, c), 6200 + c, 0, torch.float32, dev, std=0.1),
+                         W.normal_tensor((m, c), 6200 + c, 1, torch.float32, dev, std=0.1)) for c in (512, 128)}
+        self.state = {}
+        for c in (512, 128):
+            self.state[c] = C.csa2_compress_state(B, c, m, torch.bfloat16, dev)
+            pre = [W.normal_tensor((B, 2 * m - 1, c), 6300 + c, k, torch.bfloat16, dev) for k in range(4)]
+            C.csa2_compress_state_seed(pre[0], pre[1], m, self.state[c], cb=pre[2], zb=pre[3])
+        self.kv = torch.empty((B, 4096, 288), dtype=torch.uint8, device=dev)
+        self.ki = torch.empty((B, 4096, 68), dtype=torch.uint8, device=dev)
+        self.pos = torch.full((B,), self.t, dtype=torch.int64, device=dev)
+        self.e2e_in = self.new[512] + self.new[128]
+        self.e2e_out = [self.kv[:, -1].contiguous()]
+        torch.cuda.synchronize()
+
+    def step_kv(self):
+        C = _C()
+        a = self.new[512]
+        C.csa2_compress_step(a[0], a[1], self.m, self.pos, self.state[512], cb=a[2], zb=a[3], ba=self.bias[512][0],
+                             bb=self.bias[512][1], flags=C.W_NORM | C.W_ROPE, out=self.kv, out_fmt="fp4",
+                             out_seq_stride=4096)
+
+    def step_ki(self):
+        C = _C()
+        a = self.new[128]
+        C.csa2_compress_step(a[0], a[1], self.m, self.pos, self.state[128], cb=a[2], zb=a[3], ba=self.bias[128][0],
+                             bb=self.bias[128][1], flags=C.W_NORM | C.W_ROPE, out=self.ki, out_fmt="mxfp4",
+                             out_seq_stride=4096)
+
+    def main(self):
+        self.step_kv()
+
+    def post(self):
+        self.step_ki()
+
+    def launches_per_step(self):
+        return 2
+
+    def main_amount(self):
+        """Bytes of one main-KV step: the token's four rows in, the block's 4 x 4 state
+        rows read and 2 x 4 written back, the FP4 row out."""
+        return self.B * (4 * 1024 + 16 * 1024 + 8 * 1024 + 288)
+
+    def stages(self):
+        return [("compress step, main KV (FP4)", self.step_kv, self.main_amount(), 0),
+                ("compress step, indexer K (MXFP4)", self.step_ki, self.B * (4 * 256 + 24 * 256 + 68), 0)]
+
+    def queries(self):
+        return self.B
+
+    def entries(self):
+        return self.B
 
 
 class PrefillChunk(Workload):
@@ -654,7 +847,8 @@ def _offset_workload(fn, dev, B, N, seq0):
     return wl
 
 
-WORKLOADS = {c.name: c for c in (FP4Decode, DecodeBF16, ReindexReuse, PrefillChunk, TinyLayer)}
+WORKLOADS = {c.name: c for c in (FP4Decode, DecodeBF16, ReindexReuse, PrefillChunk, TinyLayer, HCADecode,
+                                  CompressStepM4, V4ProDecode)}
 
 
 def _make(args, seq0=0):
@@ -749,19 +943,29 @@ def run_ours(args):
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # workloads whose data fit in L2 flush it before every step (a 256 MB write, outside
+    # the step's own event interval); the others stream more than L2 per step
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if wl.flush_l2 else None
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)] \
+        if flush is not None else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(K):
+        if flush is not None:
+            flush.zero_()
+            sevs[i][0].record(stream)
         step(*evs[i])
+        if flush is not None:
+            sevs[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if dist is not None:
         dist.barrier()
     C.csa2_ctx_check()
-    ms_total = t0.elapsed_time(t1)
+    ms_total = t0.elapsed_time(t1) if flush is None else sum(a.elapsed_time(b) for a, b in sevs)
     main_ms = sum(a.elapsed_time(b) for a, b in evs) / K
     if dist is not None:
         tt = torch.tensor([ms_total, main_ms], dtype=torch.float64, device=dev)

@@ -80,6 +80,7 @@ struct AttnArgs {
     const int64_t* q_pos;
     const float* sink;
     int Q, H;
+    int Hs;               // heads per query in out / lse (combine of a tensor-core head pass; else H)
     RopeTable rope;
     unsigned flags;
     void* out;
@@ -311,10 +312,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] *= inv;
     if (a.flags & CSA2_ROPE) rope_lanes(acc, lane, cs, sn, -1.0f);
-    TO* o = reinterpret_cast<TO*>(a.out) + r * (int64_t)ATT_C;
+    const int64_t ro = bq * a.Hs + h;                      // row of out / lse
+    TO* o = reinterpret_cast<TO*>(a.out) + ro * (int64_t)ATT_C;
 #pragma unroll
     for (int i = 0; i < ATT_PER_LANE; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
-    if (a.lse && lane == 0) a.lse[r] = (denom > 0.0f) ? M + logf(denom) : -INFINITY;
+    if (a.lse && lane == 0) a.lse[ro] = (denom > 0.0f) ? M + logf(denom) : -INFINITY;
 }
 
 constexpr size_t ATT_SMEM = (size_t)ATT_KC * ATT_C * sizeof(float) + ATT_KC * sizeof(float) + ATT_KC * sizeof(int) +
@@ -411,7 +413,8 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     if (window == 0) swa_cap = 1;
     if (!aligned(kv, 16) || !aligned(swa, 16) || !aligned(q, 16) || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
-    // tensor-core path: bf16 query and window, bf16 or FP4 rows, both RMSNorms, <= 64 heads
+    // tensor-core path: bf16 query and window, bf16 or FP4 rows, both RMSNorms; heads
+    // in passes of at most 64 (each pass gathers the rows once)
     AttnTcCall tc;
     tc.q = q;
     tc.q_dt = q_dt;
@@ -430,31 +433,46 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     tc.sink = sink;
     tc.B = B;
     tc.Q = Q;
-    tc.H = H;
+    tc.H = std::min(H, 64);
+    tc.Hs = H;
     tc.rope = make_rope_table(rope_base);
     tc.flags = flags;
     tc.out = out;
     tc.out_dt = out_dt;
     tc.lse = lse;
-    if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, H, k, window, 0, 0)) {
-        int ns = 1;
-        const csa2_status st = attn_tc_run(ctx, tc, ws, ws_bytes, s, &ns);
-        if (st != CSA2_OK || ns <= 1) return st;
-        AttnArgs c;
-        memset(&c, 0, sizeof(c));
-        c.q_pos = q_pos;
-        c.sink = sink;
-        c.Q = Q;
-        c.H = H;
-        c.rope = tc.rope;
-        c.flags = flags;
-        c.out = out;
-        c.lse = lse;
-        c.ws = reinterpret_cast<float*>(ws);
-        c.rope_cs = attn_tc_rope_table(ctx, tc, ws);
-        c.n_split = ns;
-        c.st = ctx->status;
-        return out_dt == CSA2_F32 ? launch_combine<float>(c, B, Q, s) : launch_combine<__nv_bfloat16>(c, B, Q, s);
+    if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, tc.H, k, window, 0, 0)) {
+        const size_t qsz = q_dt == CSA2_F32 ? 4 : 2, osz = out_dt == CSA2_F32 ? 4 : 2;
+        for (int h0 = 0; h0 < H; h0 += 64) {
+            AttnTcCall p = tc;
+            p.H = std::min(64, H - h0);
+            p.q = reinterpret_cast<const uint8_t*>(q) + (size_t)h0 * ATT_C * qsz;
+            p.out = reinterpret_cast<uint8_t*>(out) + (size_t)h0 * ATT_C * osz;
+            p.lse = lse ? lse + h0 : nullptr;
+            p.sink = sink ? sink + h0 : nullptr;
+            int ns = 1;
+            const csa2_status st = attn_tc_run(ctx, p, ws, ws_bytes, s, &ns);
+            if (st != CSA2_OK) return st;
+            if (ns <= 1) continue;
+            AttnArgs c;
+            memset(&c, 0, sizeof(c));
+            c.q_pos = q_pos;
+            c.sink = p.sink;
+            c.Q = Q;
+            c.H = p.H;
+            c.Hs = H;
+            c.rope = tc.rope;
+            c.flags = flags;
+            c.out = p.out;
+            c.lse = p.lse;
+            c.ws = reinterpret_cast<float*>(ws);
+            c.rope_cs = attn_tc_rope_table(ctx, p, ws);
+            c.n_split = ns;
+            c.st = ctx->status;
+            const csa2_status sc =
+                out_dt == CSA2_F32 ? launch_combine<float>(c, B, Q, s) : launch_combine<__nv_bfloat16>(c, B, Q, s);
+            if (sc != CSA2_OK) return sc;
+        }
+        return CSA2_OK;
     }
     AttnArgs a;
     a.q = q;
@@ -471,6 +489,7 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     a.sink = sink;
     a.Q = Q;
     a.H = H;
+    a.Hs = H;
     a.rope = make_rope_table(rope_base);
     a.flags = flags;
     a.out = out;

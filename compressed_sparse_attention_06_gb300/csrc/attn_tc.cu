@@ -87,6 +87,7 @@ struct TcArgs {
     const int64_t* q_pos;
     const float* sink;
     int Q, H;
+    int Hs;                       // heads per query in out / lse (out, lse, sink start at this pass's head 0)
     RopeTable rope;
     unsigned flags;
     void* out;
@@ -227,8 +228,9 @@ __device__ __forceinline__ void load16<float>(const float* src, float (&v)[16]) 
 // B operand: 8 chunks of [64 heads x 64 dims], 128-byte swizzled; heads >= H are 0.
 // A CTA per (8 heads, query), a warp per head, 16 dims per lane.
 template <typename TQ>
-__global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, RopeTable rope,
-                                                         unsigned flags, uint8_t* qimg, float* rope_cs) {
+__global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int64_t* q_pos, int H, int Hs,
+                                                         RopeTable rope, unsigned flags, uint8_t* qimg,
+                                                         float* rope_cs) {
     __shared__ float cs[32], sn[32];
     pdl_wait();
     pdl_trigger();
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-        if (h < H) load16<TQ>(q + ((bq * H + h) * (int64_t)TC_C + 16 * lane), v);
+        if (h < H) load16<TQ>(q + ((bq * Hs + h) * (int64_t)TC_C + 16 * lane), v);
         if (flags & CSA2_QNORM) {
             float ss = 0.0f;
 #pragma unroll
@@ -300,7 +302,7 @@ __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
             if (a.n_split > 1)
                 a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + d] = 0.0f;
             else
-                reinterpret_cast<TO*>(a.out)[(it.bq * a.H + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
+                reinterpret_cast<TO*>(a.out)[(it.bq * a.Hs + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
         }
     }
     if (d0 < a.H) {
@@ -310,7 +312,7 @@ __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
             p[0] = -INFINITY;
             p[1] = 0.0f;
         } else if (a.lse) {
-            a.lse[it.bq * a.H + h] = a.sink ? a.sink[h] : -INFINITY;
+            a.lse[it.bq * a.Hs + h] = a.sink ? a.sink[h] : -INFINITY;
         }
     }
 }
@@ -331,7 +333,7 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
         rc = a.rope_cs[it.bq * 64 + j];
         rs = a.rope_cs[it.bq * 64 + 32 + j];
     }
-    TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.H + hbeg) * (int64_t)TC_C + rr;
+    TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + hbeg) * (int64_t)TC_C + rr;
     float* pbase = a.part + ((it.bq * a.H + hbeg) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + rr;
     const int64_t pstride = (int64_t)a.n_split * PART;
     for (int db = 0; db < 4; ++db) {
@@ -663,7 +665,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                         p[0] = L2[j] > 0.0f ? TC_SHIFT : -INFINITY;
                         p[1] = L2[j];
                     } else if (a.lse) {
-                        a.lse[it.bq * a.H + h] = lse2[j];
+                        a.lse[it.bq * a.Hs + h] = lse2[j];
                     }
                 }
             }
@@ -872,8 +874,8 @@ bool attn_tc_applies(const AttnTcCall& c) {
 }
 
 size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap) {
-    if (!ctx || H < 1 || H > TC_H || B <= 0 || Q <= 0) return 0;
-    return ws_layout(ctx, B, Q, H, k, window, N, swa_cap).total;
+    if (!ctx || H < 1 || B <= 0 || Q <= 0) return 0;
+    return ws_layout(ctx, B, Q, std::min(H, TC_H), k, window, N, swa_cap).total;
 }
 
 const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* ws) {
@@ -892,9 +894,10 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     const csa2_status rq =
         c.q_dt == CSA2_BF16
             ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs)
+                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg,
+                         rope_cs)
             : launch_pdl(attn_qprep_kernel<float>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.rope, c.flags, qimg, rope_cs);
+                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg, rope_cs);
     if (rq != CSA2_OK) return rq;
     TcArgs a;
     a.rinv_kv = nullptr;
@@ -931,6 +934,7 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.sink = c.sink;
     a.Q = c.Q;
     a.H = c.H;
+    a.Hs = c.Hs;
     a.rope = c.rope;
     a.flags = c.flags;
     a.out = c.out;

@@ -27,7 +27,9 @@ struct AttnTcCall {
     int window;
     const int64_t* q_pos;
     const float* sink;
-    int B, Q, H;
+    int B, Q, H;           // H: heads of this pass (<= 64)
+    int Hs;                // heads per query in q / out / lse (q, out, lse, sink point at this
+                           // pass's first head)
     RopeTable rope;
     unsigned flags;
     void* out;
@@ -40,7 +42,8 @@ bool attn_tc_applies(const AttnTcCall& c);
 
 // Workspace bytes the tensor-core path uses for these sizes: per-split partials
 // (when the keys are split), the query images, and, when the call gathers each
-// row many times over, the rows' RMS factors (B*N + B*swa_cap floats); 0 when H > 64.
+// row many times over, the rows' RMS factors (B*N + B*swa_cap floats).  More than 64
+// heads run in passes of 64 that reuse the workspace, so H is capped at 64 here.
 // The path runs with any workspace that holds the partials and the images.
 size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap);
 

@@ -65,6 +65,7 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
 
     // pass 1: per-channel max of the logits
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 8
     for (int j = 0; j < m; ++j) {
         float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
         float4 b = load4_bias(ba, (int64_t)j * c + ch);
@@ -72,7 +73,8 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
         for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], f4get(z, k) + f4get(b, k));
     }
     if (hz) {
-        for (int j = 0; j < m; ++j) {
+    #pragma unroll 8
+    for (int j = 0; j < m; ++j) {
             float4 z = load4<T>(hz + (int64_t)j * c + ch);
             float4 b = load4_bias(bb, (int64_t)j * c + ch);
 #pragma unroll
@@ -81,6 +83,7 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
     }
     // pass 2: softmax-weighted sum
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int j = 0; j < m; ++j) {
         float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
         float4 b = load4_bias(ba, (int64_t)j * c + ch);
@@ -93,7 +96,8 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
         }
     }
     if (hz) {
-        for (int j = 0; j < m; ++j) {
+    #pragma unroll 8
+    for (int j = 0; j < m; ++j) {
             float4 z = load4<T>(hz + (int64_t)j * c + ch);
             float4 b = load4_bias(bb, (int64_t)j * c + ch);
             float4 v = load4<T>(hc + (int64_t)j * c + ch);

@@ -272,12 +272,13 @@ def fp4_rows(kind: str, b: int, row0: int, rows: int, N: int, device="cpu") -> t
     return (x.view(rows, width) * r.view(rows, 1)).to(torch.float32)
 
 
-def fp4_decode(device="cpu", B: int = 8, N: int = 1 << 20) -> Workload:
+def fp4_decode(device="cpu", B: int = 8, N: int = 1 << 20, H: int = 64) -> Workload:
     """FP4-cache long-context decode: B sequences of N entries (m=1); query at
     t = N-1.  The main-KV and indexer-K caches are drawn with `fp4_rows` and
-    packed by the caller (FP4 E2M1+E4M3/16 and MXFP4 respectively)."""
+    packed by the caller (FP4 E2M1+E4M3/16 and MXFP4 respectively).  H query heads
+    (64; 128 for the V4-Pro configuration)."""
     wid = 4
-    m, H_I, H, Q = 1, 64, 64, 1
+    m, H_I, Q = 1, 64, 1
     t = {}
     t["qI"] = normal_tensor((B, Q, H_I, D_INDEX), _wid_seed(wid, 5), 0, torch.bfloat16, device)
     t["w"] = normal_tensor((B, Q, H_I), _wid_seed(wid, 6), 0, torch.float32, device)

@@ -104,3 +104,39 @@ def test_tensor_core_out_of_range_index_is_flagged():
     assert e.value.status == C.ERR_DEVICE
     C.csa2_ctx_check()
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("H,k", [(128, 1024), (100, 512)])
+@pytest.mark.parametrize("kv_kind", ["bf16", "fp4"])
+def test_more_than_64_heads_in_passes(H, k, kv_kind):
+    """More than 64 heads (V4-Pro: 128): the tensor-core path runs 64-head passes over
+    the same rows (the second one ragged for H = 100); against the oracle and against
+    the CUDA-core path of the same call."""
+    B, Q, N, window = 2, 2, 6000, 128
+    pos = [[N, N + 300], [700, 5000]]
+    q = W.normal_tensor((B, Q, H, 512), 341, 1, torch.bfloat16, DEV)
+    kv_f = W.normal_tensor((B, N, 512), 341, 2, torch.float32, DEV) * 1.3
+    if kv_kind == "fp4":
+        kv = C.csa2_fp4_pack(kv_f)
+        kv_np = O.nvfp4_unpack(O.nvfp4_pack(kv_f.reshape(-1, 512).cpu().numpy())).reshape(B, N, 512)
+    else:
+        kv = kv_f.to(torch.bfloat16)
+        kv_np = kv.double().cpu().numpy()
+    swa = W.normal_tensor((B, 128, 512), 341, 3, torch.bfloat16, DEV)
+    q_pos = torch.tensor(pos, dtype=torch.int64, device=DEV)
+    idx = torch.full((B, Q, k), -1, dtype=torch.int32)
+    for b in range(B):
+        for qq in range(Q):
+            n = k - (37 if (b + qq) % 2 else 0)
+            idx[b, qq, :n] = W.distinct_sample(N, n, 342 + b, qq).to(torch.int32)
+    idx = idx.to(DEV)
+    sink = W.normal_tensor((H,), 343, 0, torch.float32, DEV)
+    tc, tc_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
+                                    want_lse=True)
+    tiny = torch.empty(16, dtype=torch.uint8, device=DEV)
+    cc, cc_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
+                                    want_lse=True, ws=tiny)
+    C.csa2_ctx_check()
+    assert_close(to_np(tc), to_np(cc), 2e-2, "tensor-core vs CUDA-core output")
+    assert_close(to_np(tc_lse), to_np(cc_lse), 2e-3, "tensor-core vs CUDA-core lse")
+    _check(q, kv_np, idx, swa, q_pos, sink, window, to_np(tc), to_np(tc_lse), [(0, 1), (1, 0)])

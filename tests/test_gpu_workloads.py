@@ -232,3 +232,64 @@ def test_prefill_chunk_full_size():
                                 _np(wl["sink"]), 128)
         g = _gpu_attn_one(wl["q"][0, qi], kv[0], ref_idx, wl["swa"][0], t, wl["sink"], wl.meta["swa_pos0"])
         assert_close(g, o, 2e-2, f"attention q{qi}")
+
+
+def test_fp4_decode_v4pro_variant():
+    """The V4-Pro configuration (DSA-to-CSA/HCA page, «两个已公开配置»): CSA top-1024,
+    128 query heads (two 64-head tensor-core passes over the same selected rows),
+    64 indexer heads; FP4 caches, 4 sequences of 262,144 entries; sampled sequences
+    through the oracle."""
+    B, N, H, k = 4, 1 << 18, 128, 1024
+    wl = W.fp4_decode(DEV, B=B, N=N, H=H)
+    kv = torch.empty((B, N, 288), dtype=torch.uint8, device=DEV)
+    ki = torch.empty((B, N, 68), dtype=torch.uint8, device=DEV)
+    for b in range(B):
+        C.csa2_fp4_pack(W.fp4_rows("kv", b, 0, N, N, DEV), C.FP4_E4M3x16, out=kv[b])
+        C.csa2_fp4_pack(W.fp4_rows("KI", b, 0, N, N, DEV), C.MXFP4_E8M0x32, out=ki[b])
+    nv = P.visible_entries(wl.q_pos, 1)
+    sink = W.normal_tensor((H,), 4109, 0, torch.float32, DEV)
+    buf = P.alloc_decode(B, 1, N, H, 512, DEV, out_dtype=torch.float32, k=k)
+    P.full_decode_step(wl["qI"], wl["w"], ki, wl["q"], kv, wl["swa"], wl.q_pos, nv, sink, buf, k=k)
+    C.csa2_ctx_check()
+    t = N - 1
+    for b in (0, B - 1):
+        ki_ref = O.mxfp4_pack(W.fp4_rows("KI", b, 0, N, N, "cpu").numpy())
+        qI_ref = O.mxfp4_pack(wl["qI"][b, 0].float().cpu().numpy())
+        V = N - 1
+        _, ref_idx = _check_decode_query(b, V, O.mxfp4_unpack(qI_ref), _np(wl["w"][b, 0]),
+                                         O.mxfp4_unpack(ki_ref[:V]), to_np(buf.idx[b, 0]), to_np(buf.pool[b, 0]),
+                                         to_np(buf.block_max[b, 0]), k=k)
+        rows = {int(s): O.nvfp4_unpack(O.nvfp4_pack(W.fp4_rows("kv", b, int(s), 1, N, "cpu").numpy()))[0]
+                for s in ref_idx if s >= 0}
+        o, _, _ = O.sparse_attn(_np(wl["q"][b, 0]), _RowMap(rows), ref_idx, _np(wl["swa"][b]), 0, t, _np(sink), 128)
+        assert o.shape[0] == H
+        if np.array_equal(to_np(buf.idx[b, 0]), ref_idx):
+            assert_close(to_np(buf.out[b, 0]), o, 2e-2, f"attention (pipeline) b{b}")
+        g = _gpu_attn_one(wl["q"][b, 0], kv[b], ref_idx, wl["swa"][b], t, sink)
+        assert_close(g, o, 2e-2, f"attention b{b}")
+
+
+def test_dsa_token_level_top2048():
+    """DSA-style selection (DSA-to-CSA/HCA page, the DSA baseline: top-2048 tokens,
+    m = 1) and attention over the 2,048 selected rows plus the window, bf16, 64 heads."""
+    B, N, k = 2, 100000, 2048
+    qI = W.normal_tensor((B, 1, 64, 128), 4201, 0, torch.bfloat16, DEV)
+    w = W.normal_tensor((B, 1, 64), 4202, 0, torch.float32, DEV)
+    KI = W.normal_tensor((B, N, 128), 4203, 0, torch.bfloat16, DEV)
+    kv = W.normal_tensor((B, N, 512), 4204, 0, torch.bfloat16, DEV)
+    q = W.normal_tensor((B, 1, 64, 512), 4205, 0, torch.bfloat16, DEV)
+    swa = W.normal_tensor((B, 128, 512), 4206, 0, torch.bfloat16, DEV)
+    sink = W.normal_tensor((64,), 4207, 0, torch.float32, DEV)
+    q_pos = torch.tensor([[N - 1], [61234]], dtype=torch.int64, device=DEV)
+    nv = P.visible_entries(q_pos, 1)
+    sc, idx = P.full_topk_step(qI, w, KI, nv, k=k)
+    out, _ = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=128, out_dtype=torch.float32)
+    C.csa2_ctx_check()
+    for b in range(B):
+        V = int(nv[b, 0])
+        ref_sc = O.index_score(_np(qI[b, 0]), _np(w[b, 0]), _np(KI[b]), V)
+        topk_swaps(to_np(idx[b, 0]), ref_sc, V, k)
+        ref_idx = O.topk(ref_sc, V, k)
+        o, _, _ = O.sparse_attn(_np(q[b, 0]), _np(kv[b]), ref_idx, _np(swa[b]), 0, int(q_pos[b, 0]), _np(sink), 128)
+        g = _gpu_attn_one(q[b, 0], kv[b], ref_idx, swa[b], int(q_pos[b, 0]), sink)
+        assert_close(g, o, 2e-2, f"attention b{b}")
