@@ -30,6 +30,7 @@ EXPORTS = (
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
     "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
+    "csa2_compress_varlen",
 )
 
 
@@ -58,6 +59,8 @@ def _declare(lib):
         "csa2_compress_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _f, _u, _vp, _i,
                                     _i64, _vp]),
         "csa2_compress_state_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+        "csa2_compress_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _i64, _i, _i, _vp, _f, _u, _vp,
+                                      _i, _i64, _vp]),
         "csa2_compress_state_seed": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _vp, _vp]),
         "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
@@ -198,6 +201,26 @@ def _out_dt(out, out_fmt):
     if out.dtype == torch.uint8:
         return MXFP4_E8M0x32 if out_fmt == "mxfp4" else FP4_E4M3x16
     return _dt(out)
+
+
+def csa2_compress_varlen(ca, za, m: int, cu_tokens, max_tokens: int, cb=None, zb=None, ba=None, bb=None, pos0=None,
+                         rope_base: float = 10000.0, flags: int = 0, out_fmt: str = "f32",
+                         out: Optional[torch.Tensor] = None, out_seq_stride: Optional[int] = None):
+    """Packed samples: ca/za (cb/zb) [T, c] hold S samples back to back, sample s at
+    tokens cu_tokens[s] .. cu_tokens[s+1]-1 ([S+1] int64 device tensor).  Returns (or
+    fills) [S, max_tokens // m, row]: entry i of sample s in row s, i; each sample is
+    compressed alone (no shared window, tails left out)."""
+    T, c = ca.shape
+    S = cu_tokens.shape[0] - 1
+    n_ent = max_tokens // m
+    if out is None:
+        out = _alloc_rows((S, n_ent), c, out_fmt, ca.device)
+    oss = n_ent if out_seq_stride is None else out_seq_stride
+    st = _lib().csa2_compress_varlen(ctx(ca.device.index), _p(ca), _p(za), _p(cb), _p(zb), _dt(ca), _p(ba), _p(bb), S,
+                                     _p(cu_tokens), max_tokens, c, m, _p(pos0), rope_base, flags,
+                                     _vp(out.data_ptr()), _out_dt(out, out_fmt), oss, _stream(ca))
+    _check("csa2_compress_varlen", st)
+    return out
 
 
 def csa2_compress_state_bytes(B: int, c: int, m: int, dtype=torch.bfloat16, overlap: bool = True) -> int:

@@ -226,6 +226,37 @@ __global__ void __launch_bounds__(256) compress_kernel(
                            flags, out, bseq * out_seq_stride + i);
 }
 
+// Packed samples (varlen): the tokens of S samples lie back to back in one stream,
+// sample s at tokens cu_tokens[s] .. cu_tokens[s+1]-1.  Each sample is compressed on
+// its own -- its blocks start at its first token, its first block has no history, and
+// a tail shorter than m is left out rather than completed by the next sample's tokens
+// (DSA-to-CSA/HCA page, the note under the compressor code and «算法语义») -- and
+// entry i of sample s goes to row s*out_seq_stride + i at position pos0[s] + m*i.
+// Grid: (max entries per sample, S); CTAs past their sample's entry count exit.
+template <typename T, int OUT>
+__global__ void __launch_bounds__(256) compress_varlen_kernel(
+    const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
+    const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ cu_tokens, int c, int m,
+    const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
+    int64_t out_seq_stride) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = blockIdx.x;
+    const int64_t smp = blockIdx.y;
+    const int64_t t0 = cu_tokens[smp], n = cu_tokens[smp + 1] - t0;
+    if (i >= n / m) return;                  // the whole CTA: past this sample's complete blocks
+    const bool overlap = cb != nullptr;
+    const int64_t r0 = (t0 + m * i) * (int64_t)c;
+    const T* hc = nullptr;
+    const T* hz = nullptr;
+    if (overlap && i > 0) {
+        hc = cb + r0 - (int64_t)m * c;
+        hz = zb + r0 - (int64_t)m * c;
+    }
+    const int64_t pos = (pos0_arr ? pos0_arr[smp] : 0) + (int64_t)m * i;
+    compress_entry<T, OUT>(ca + r0, za + r0, hc, hz, ba, bb, c, m, pos, rope, flags, out, smp * out_seq_stride + i);
+}
+
 // One decode step for B sequences (a CTA each): the token at position pos[b] (< 0: no
 // token this step) is stored in slot pos % m of the state; when it completes block
 // i = pos / m, entry i (position m*i) is written to row b*out_seq_stride + i of out
@@ -297,6 +328,33 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
                        pos0, rope, flags, out, oss);
     else
         r = launch_pdl(compress_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    return r != CSA2_OK ? r : csa2_launch_status();
+}
+
+template <typename T>
+csa2_status launch_varlen(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+                          const float* bb, const int64_t* cu_tokens, int S, int64_t max_entries, int c, int m,
+                          const int64_t* pos0, float base, unsigned flags, void* out, csa2_dtype out_dt, int64_t oss,
+                          cudaStream_t s) {
+    const RopeTable rope = make_rope_table(base);
+    const T* a = (const T*)ca;
+    const T* z = (const T*)za;
+    const T* b = (const T*)cb;
+    const T* zz = (const T*)zb;
+    const dim3 grid((unsigned)max_entries, (unsigned)S), block(c / 4);
+    csa2_status r;
+    if (out_dt == CSA2_F32)
+        r = launch_pdl(compress_varlen_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    else if (out_dt == CSA2_BF16)
+        r = launch_pdl(compress_varlen_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    else if (out_dt == CSA2_FP4_E4M3x16)
+        r = launch_pdl(compress_varlen_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+                       pos0, rope, flags, out, oss);
+    else
+        r = launch_pdl(compress_varlen_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
                        pos0, rope, flags, out, oss);
     return r != CSA2_OK ? r : csa2_launch_status();
 }
@@ -425,4 +483,32 @@ extern "C" csa2_status csa2_compress_state_seed(csa2_ctx* ctx, const void* ca, c
                                           (size_t)B, cudaMemcpyDeviceToDevice, s));
     }
     return CSA2_OK;
+}
+
+extern "C" csa2_status csa2_compress_varlen(csa2_ctx* ctx, const void* ca, const void* za, const void* cb,
+                                            const void* zb, csa2_dtype in_dt, const float* ba, const float* bb,
+                                            int S, const int64_t* cu_tokens, int64_t max_tokens, int c, int m,
+                                            const int64_t* pos0, float rope_base, unsigned flags, void* out,
+                                            csa2_dtype out_dt, int64_t out_seq_stride, void* stream) {
+    if (!ctx || S < 0 || S > 65535 || max_tokens < 0 || m < 1 || c <= 0) return CSA2_ERR_INVALID_ARG;
+    if (c % 128 || c > 1024) return CSA2_ERR_INVALID_ARG;
+    if ((cb == nullptr) != (zb == nullptr)) return CSA2_ERR_INVALID_ARG;
+    if (flags & ~(CSA2_W_NORM | CSA2_W_ROPE)) return CSA2_ERR_INVALID_ARG;
+    if (in_dt != CSA2_F32 && in_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (out_dt != CSA2_F32 && out_dt != CSA2_BF16 && out_dt != CSA2_FP4_E4M3x16 && out_dt != CSA2_MXFP4_E8M0x32)
+        return CSA2_ERR_UNSUPPORTED;
+    const int64_t max_entries = max_tokens / m;
+    if (S == 0 || max_entries == 0) return CSA2_OK;
+    if (max_entries > 0x7FFFFFFF) return CSA2_ERR_INVALID_ARG;
+    if (!ca || !za || !cu_tokens || !out || out_seq_stride < (S > 1 ? max_entries : 0)) return CSA2_ERR_INVALID_ARG;
+    const size_t va = in_dt == CSA2_F32 ? 16 : 8;
+    if (!aligned(ca, va) || !aligned(za, va) || (cb && (!aligned(cb, va) || !aligned(zb, va))) ||
+        (ba && !aligned(ba, 16)) || (bb && !aligned(bb, 16)) || !aligned(out, 16))
+        return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (in_dt == CSA2_F32)
+        return launch_varlen<float>(ca, za, cb, zb, ba, bb, cu_tokens, S, max_entries, c, m, pos0, rope_base, flags,
+                                    out, out_dt, out_seq_stride, s);
+    return launch_varlen<__nv_bfloat16>(ca, za, cb, zb, ba, bb, cu_tokens, S, max_entries, c, m, pos0, rope_base,
+                                        flags, out, out_dt, out_seq_stride, s);
 }

@@ -122,6 +122,27 @@ csa2_status csa2_compress(csa2_ctx* ctx,
                           int64_t out_seq_stride, void* stream);
 
 /*
+ * csa2_compress_varlen -- csa2_compress over packed samples (a varlen batch): the
+ * tokens of S samples lie back to back, sample s at tokens cu_tokens[s] ..
+ * cu_tokens[s+1]-1 of ca/za/cb/zb ([total tokens, c] in in_dt).  Samples never share a
+ * compression window (DSA-to-CSA/HCA page, the note under the compressor code and
+ * «算法语义»): each is compressed as if alone -- blocks start at its first token, its
+ * first block has no history, a tail shorter than m is left out (it is not completed
+ * by the next sample).  Entry i of sample s goes to row s*out_seq_stride + i of out at
+ * position pos0[s] + m*i (pos0 NULL = 0), so each sample's cache row is its own and the
+ * window and the indexer's visible range stay inside the sample.
+ *   cu_tokens  : [S+1] int64 device array, non-decreasing, cu_tokens[0] = 0
+ *   max_tokens : an upper bound of the tokens of any one sample (sizes the grid)
+ *   out_seq_stride >= max_tokens/m when S > 1.  Other arguments as csa2_compress.
+ */
+csa2_status csa2_compress_varlen(csa2_ctx* ctx,
+                                 const void* ca, const void* za, const void* cb, const void* zb,
+                                 csa2_dtype in_dt, const float* ba, const float* bb,
+                                 int S, const int64_t* cu_tokens, int64_t max_tokens, int c, int m,
+                                 const int64_t* pos0, float rope_base, unsigned flags, void* out,
+                                 csa2_dtype out_dt, int64_t out_seq_stride, void* stream);
+
+/*
  * csa2_compress_step -- the compressor in decode, one token per sequence per call,
  * with the compressor state of the Attention-evolution page §3.3 (the unfinished
  * block's projections and gate logits; with overlap, the previous block's overlap
