@@ -10,7 +10,7 @@ rescoring, top-512, sparse shared-KV attention.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload fp4_decode_1M|decode_full_bf16|reindex_reuse_bf16|
                               prefill_chunk_bf16|tiny_full_layer_fp32|hca_decode_1M|compress_step_m4|
-                              fp4_decode_1M_v4pro]
+                              fp4_decode_1M_v4pro|prefill_varlen_compress]
 
 Besides the step rate, the line carries each stage's time (timed separately with
 CUDA events after the main loop) against its own roofline.  With torchrun (N > 1)
@@ -32,6 +32,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "decode queries/s & indexer entries/s at 1M ctx; % of HBM roofline (1 GB300)"
@@ -690,6 +691,73 @@ class CompressStepM4(Workload):
         return self.B
 
 
+class PrefillVarlenCompress(Workload):
+    """Packed-sample prefill write path: 32 samples of 1,000 .. 4,000 tokens back to
+    back (cu_tokens offsets), overlapped compressor m = 4, each sample compressed alone
+    into its own cache rows: FP4 main KV (c = 512) and MXFP4 indexer keys (c = 128)."""
+    name = "prefill_varlen_compress"
+    main_name = "csa2_compress_varlen (overlap m=4, c=512 -> FP4 rows)"
+    kernel_files = ("compress.cu", "csa2_internal.cuh")
+
+    def __init__(self, B=32, N=None, seq0=0):
+        self.S, self.m = B, 4
+
+    def config(self):
+        return {"workload": self.name, "samples": self.S, "tokens": self.T, "m": self.m, "overlap": True,
+                "rows": "main KV c=512 -> FP4 288 B; indexer K c=128 -> MXFP4 68 B", "flags": "RMSNorm + RoPE",
+                "l2": f"inputs larger than L2 ({self.T * (4 * 512 + 4 * 128) * 2 / 1e6:.0f} MB of token rows)"}
+
+    def setup(self, dev):
+        from compressed_sparse_attention_06_gb300 import workloads as W
+        C = _C()
+        u = W.uniform(self.S, 6401, 0, "cpu")
+        self.lens = [int(1000 + 3000 * float(x)) for x in u]
+        self.T, self.maxlen = sum(self.lens), max(self.lens)
+        self.cu = torch.tensor([0] + list(np.cumsum(self.lens)), dtype=torch.int64, device=dev)
+        self.rows = {c: [W.normal_tensor((self.T, c), 6410 + c, k, torch.bfloat16, dev) for k in range(4)]
+                     for c in (512, 128)}
+        self.bias = {c: (W.normal_tensor((4, c), 6420 + c, 0, torch.float32, dev, std=0.1),
+                         W.normal_tensor((4, c), 6420 + c, 1, torch.float32, dev, std=0.1)) for c in (512, 128)}
+        ne = self.maxlen // self.m
+        self.kv = torch.empty((self.S, ne, 288), dtype=torch.uint8, device=dev)
+        self.ki = torch.empty((self.S, ne, 68), dtype=torch.uint8, device=dev)
+        self.entries_total = sum(n // self.m for n in self.lens)
+        self.e2e_in = self.rows[512] + self.rows[128]
+        self.e2e_out = [self.kv]
+        torch.cuda.synchronize()
+
+    def write(self, c):
+        C = _C()
+        a = self.rows[c]
+        C.csa2_compress_varlen(a[0], a[1], self.m, self.cu, self.maxlen, cb=a[2], zb=a[3], ba=self.bias[c][0],
+                               bb=self.bias[c][1], flags=C.W_NORM | C.W_ROPE, out_fmt="fp4" if c == 512 else "mxfp4",
+                               out=self.kv if c == 512 else self.ki)
+
+    def main(self):
+        self.write(512)
+
+    def post(self):
+        self.write(128)
+
+    def launches_per_step(self):
+        return 2
+
+    def main_amount(self):
+        """Bytes of the main-KV launch: four bf16 token rows in (each read once: a
+        block's rows and, for the next block, its overlap half), FP4 rows out."""
+        return self.T * 4 * 1024 + self.entries_total * 288
+
+    def stages(self):
+        return [("compress varlen, main KV (FP4)", self.main, self.main_amount(), 0),
+                ("compress varlen, indexer K (MXFP4)", self.post, self.T * 4 * 256 + self.entries_total * 68, 0)]
+
+    def queries(self):
+        return self.T
+
+    def entries(self):
+        return self.entries_total
+
+
 class PrefillChunk(Workload):
     """Encoder prefill chunk: 8192 queries on a 131,072-token context (m=4 overlap)."""
     name = "prefill_chunk_bf16"
@@ -848,7 +916,7 @@ def _offset_workload(fn, dev, B, N, seq0):
 
 
 WORKLOADS = {c.name: c for c in (FP4Decode, DecodeBF16, ReindexReuse, PrefillChunk, TinyLayer, HCADecode,
-                                  CompressStepM4, V4ProDecode)}
+                                  CompressStepM4, V4ProDecode, PrefillVarlenCompress)}
 
 
 def _make(args, seq0=0):
