@@ -770,7 +770,7 @@ void choose_chunks(const csa2_ctx* ctx, int64_t rows, int64_t n_max, int k, size
 // winner and tie counts of the CTAs before it (ties at T go to the lowest indices).
 // Every CTA runs the same sequence of cluster barriers whatever the data, so no
 // barrier can be left waiting for a CTA that took another path.
-constexpr int CL_THREADS = 512;
+constexpr int CL_THREADS = 1024;           // most threads per CTA (chunks of >= 8,192 keys; 512 below)
 constexpr int CL_MAX_CHUNK = 16384;        // keys per CTA (64 KB of shared memory)
 
 struct ClShared {
@@ -1082,12 +1082,13 @@ __global__ void __launch_bounds__(CL_THREADS) sel_cluster_kernel(SelArgs a, int 
 }
 
 // Cluster size for the cluster path, or 0 when it does not apply: few rows, each split
-// into chunks of at most CL_MAX_CHUNK keys.
+// into chunks of at most CL_MAX_CHUNK keys.  8 CTAs when the chunks fit (measured: the
+// cluster barriers of 8 CTAs are cheaper than those of 16), else 16.
 int cluster_size_for(csa2_ctx* ctx, int64_t rows, int64_t n_max) {
     if (n_max < 4096) return 0;
-    for (int c : {16, 8}) {
-        if (rows * c > ctx->num_sms) continue;
-        if (((n_max + c - 1) / c + 31) / 32 * 32 > CL_MAX_CHUNK) return 0;
+    for (int c : {8, 16}) {
+        if (rows * c > ctx->num_sms) return 0;
+        if (((n_max + c - 1) / c + 31) / 32 * 32 > CL_MAX_CHUNK) continue;
         return c;
     }
     return 0;
@@ -1107,7 +1108,7 @@ csa2_status launch_cluster(csa2_ctx* ctx, const SelArgs& a, int64_t rows, int64_
     const int chunk = (int)(((n_max + C - 1) / C + 31) / 32 * 32);   // 16-byte aligned chunk starts
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
-    cfg.blockDim = dim3(CL_THREADS, 1, 1);
+    cfg.blockDim = dim3(chunk >= 8192 ? 1024 : 512, 1, 1);   // >= the 512 bins of a 12-bit slice at C = 8
     cfg.dynamicSmemBytes = (size_t)chunk * sizeof(uint32_t);
     cfg.stream = s;
     cudaLaunchAttribute at[2];
@@ -1131,7 +1132,7 @@ csa2_status run_select(csa2_ctx* ctx, SelArgs a, int64_t rows, int64_t n_max, vo
             // can a 16-CTA cluster of this kernel be resident at all?
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(16, 1, 1);
-            cfg.blockDim = dim3(CL_THREADS, 1, 1);
+            cfg.blockDim = dim3(CL_THREADS, 1, 1);                 // the largest block the path launches
             cfg.dynamicSmemBytes = CL_MAX_CHUNK * sizeof(uint32_t);
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;

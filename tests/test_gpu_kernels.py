@@ -419,11 +419,13 @@ def test_selection_without_workspace_matches(ties):
             np.testing.assert_array_equal(to_np(idx)[r], O.topk(sn[r], int(nv[r]), 512))
 
 
-@pytest.mark.parametrize("rows,n,k", [(12, 20000, 512), (9, 131072, 2047), (3, 4096, 4096), (19, 9000, 100)])
+@pytest.mark.parametrize("rows,n,k", [(12, 20000, 512), (9, 131072, 2047), (3, 4096, 4096), (19, 9000, 100),
+                                      (3, 200000, 512)])
 @pytest.mark.parametrize("ties", [False, True])
 def test_topk_cluster_rows_bit_exact(rows, n, k, ties):
-    """Few long rows: one thread-block cluster per row (16 CTAs for up to 9 rows, 8
-    for up to 19).  Visible counts cover full, ragged, tiny, empty and <= k rows."""
+    """Few long rows: one thread-block cluster per row (8 CTAs; 16 when a row needs more
+    than 8 x 16,384 keys, here 200,000).  Visible counts cover full, ragged, tiny, empty
+    and <= k rows."""
     s = _score_rows(rows, n, 181 + n + rows, ties)
     nv = torch.tensor([[n, n - 1, 1, 0, k, k + 1, n // 3][r % 7] for r in range(rows)], dtype=torch.int64,
                       device=DEV)
