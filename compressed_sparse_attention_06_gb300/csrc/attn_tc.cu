@@ -372,7 +372,6 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
 template <bool FP4, typename TO>
 __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    pdl_wait();                        // the query images, indices and rows are complete
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + OFF_Q;
     uint8_t* sK = smem + OFF_K;
@@ -416,6 +415,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         tmem_alloc(sTmem, TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above touches no global memory; the previous kernels (and their tensor
+    // memory) are done before these CTAs can start, see pdl_wait()
+    pdl_wait();                        // the query images, indices and rows are complete
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -142,18 +142,14 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     uint64_t* dempty = done + BUFS;          // [BUFS] D tile read by an epilogue group
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
 
-    pdl_wait();                              // inputs of the previous kernel are complete
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y;                // b * Q + q
     const int b = g / a.Q;
-    int64_t V = a.nv[g];
-    if (!CAND && V > a.N) V = a.N;
-    const int t_begin = blockIdx.x * a.tiles_per_cta;
-    const int t_end = min(a.tiles, t_begin + a.tiles_per_cta);
-    int t_act_end = t_end;
-    if (!CAND) t_act_end = min(t_end, (int)((V + TILE - 1) / TILE));
-    const int n_act = max(0, t_act_end - t_begin);
 
+    // setup that touches no global memory runs before the wait for the previous
+    // kernel (which, like every kernel before it, has released its tensor memory by the
+    // time these CTAs can start: a kernel lets its successor start only after its own
+    // wait returned)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], CAND ? 32 : 1);   // cp.async: one arrival per lane
@@ -170,6 +166,14 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
         tmem_alloc(sTmem, TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_wait();                              // inputs of the previous kernel are complete
+    int64_t V = a.nv[g];
+    if (!CAND && V > a.N) V = a.N;
+    const int t_begin = blockIdx.x * a.tiles_per_cta;
+    const int t_end = min(a.tiles, t_begin + a.tiles_per_cta);
+    int t_act_end = t_end;
+    if (!CAND) t_act_end = min(t_end, (int)((V + TILE - 1) / TILE));
+    const int n_act = max(0, t_act_end - t_begin);
     // query codes -> the B tile: thread (head h, 16-byte unit u)
     const uint8_t* qrow0 = a.qmx + (int64_t)g * HEADS * MX_ROW;
     for (int t = threadIdx.x; t < HEADS * 4; t += THREADS) {
