@@ -171,24 +171,38 @@ __device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& ss) {
     }
 }
 
-// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16 (exact:
-// an E2M1 value times an E4M3 scale has at most 6 significant bits).  ca, cb: the
-// chunk's 32 code bytes; scw: its four scale bytes.  Adds the squares to ss.
+// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16.  Each
+// E2M1 pair becomes an f16x2 and is multiplied by its E4M3 block scale in f16: exact,
+// since an E2M1 value times an E4M3 scale has at most 6 significant bits and lies in
+// [2^-10, 2688]; the bf16 image is then the upper half of the exact f32.  ca, cb: the
+// chunk's 32 code bytes; scw: its four scale bytes.  The squares go to eight partial
+// sums (short dependency chains).
 __device__ __forceinline__ void fp4_chunk_to_tile(const uint4& ca, const uint4& cb, uint32_t scw, uint8_t* sK,
-                                                  int c, int r, float& ss) {
+                                                  int c, int r, float (&ss)[8]) {
     const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const float s = e4m3_to_f32((scw >> (8 * (u >> 1))) & 0xFFu);
-        float f[8];
-        e2m1x8_to_f32(cw[u], f);
+        uint32_t s2;                              // the block scale in both f16 halves
+        const unsigned short sb = (unsigned short)(((scw >> (8 * (u >> 1))) & 0xFFu) * 0x101u);
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sb));
+        uint32_t h[4];
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+            "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+            : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+            : "r"(cw[u]));
         uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float x0 = f[2 * i] * s, x1 = f[2 * i + 1] * s;
-            ss = fmaf(x0, x0, ss);
-            ss = fmaf(x1, x1, ss);
-            pk[i] = pack_bf16x2(x0, x1);
+            uint32_t x;
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(h[i]), "r"(s2));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x));
+            ss[2 * i] = fmaf(f.x, f.x, ss[2 * i]);
+            ss[2 * i + 1] = fmaf(f.y, f.y, ss[2 * i + 1]);
+            pk[i] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
         }
         *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -725,7 +739,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     const uint64_t p = __shfl_sync(FULL, (uint64_t)(uintptr_t)(bf_row ? src : nullptr), 2 * j + half);
                     srcj[j] = reinterpret_cast<const uint8_t*>((uintptr_t)p);
                 }
-                float ss = 0.0f;
+                float ss = 0.0f, ss8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
                 bool w = true;
 #pragma unroll
                 for (int db = 0; db < 4; ++db) {
@@ -743,7 +757,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                             if (fp4_row) {
                                 const uint32_t scw = (c2 < 4) ? (c2 == 0 ? fs0.x : c2 == 1 ? fs0.y : c2 == 2 ? fs0.z : fs0.w)
                                                               : (c2 == 4 ? fs1.x : c2 == 5 ? fs1.y : c2 == 6 ? fs1.z : fs1.w);
-                                fp4_chunk_to_tile(fc[2 * c2], fc[2 * c2 + 1], scw, sK, c2, r, ss);
+                                fp4_chunk_to_tile(fc[2 * c2], fc[2 * c2 + 1], scw, sK, c2, r, ss8);
                             } else if (!bf_row) {
 #pragma unroll
                                 for (int u2 = 0; u2 < 8; ++u2)
@@ -789,6 +803,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                                                      sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
                                                  ss);
                         }
+                        if (fp4_row)
+                            ss = ((ss8[0] + ss8[1]) + (ss8[2] + ss8[3])) + ((ss8[4] + ss8[5]) + (ss8[6] + ss8[7]));
                         rv = 1.0f / sqrtf(ss / (float)TC_C + 1e-6f);
                     }
                 }

@@ -17,6 +17,8 @@
 // entry into the cache (a compressed entry exists only once its block is complete,
 // DSA-to-CSA/HCA page «因果边界与短滑窗»), then keeps the block's overlap half for the
 // next one.
+#include <algorithm>
+
 #include "csa2_internal.cuh"
 
 namespace {
@@ -45,6 +47,17 @@ __device__ __forceinline__ float f4get(const float4& v, int k) {
 
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_FP4 = 2, OUT_MX = 3 };
 
+constexpr int CMP_MAX_THREADS = 512;
+
+// Row groups of one entry's CTA: a long block (HCA's m' = 128) would leave each
+// thread a serial walk over m rows, so blocks of 16 rows or more are split into up to
+// m/8 groups of c/4 threads (at most CMP_MAX_THREADS threads); short blocks (CSA's
+// m = 4) keep one group.
+int compress_row_groups(int m, int c) {
+    if (m < 16) return 1;
+    return std::max(1, std::min(m / 8, CMP_MAX_THREADS / (c / 4)));
+}
+
 template <typename T>
 __device__ __forceinline__ void copy4(T* dst, const T* src) {
     if (sizeof(T) == 4)
@@ -53,38 +66,59 @@ __device__ __forceinline__ void copy4(T* dst, const T* src) {
         *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
 }
 
-// One compressed entry; this thread's channels ch .. ch+3 (blockDim.x = c/4): the
-// softmax over the block's m rows (and the m history rows, if any) per channel, the
-// weighted sum, then RMSNorm -> RoPE at `pos` -> store as row `orow` of out.
+// One compressed entry; this thread's channels ch .. ch+3.  blockDim.x = R * c/4: R
+// row groups (R = compress_row_groups(m, c)), group rg taking rows rg, rg+R, ... of the
+// block (and of the history).  The softmax over the block's m rows (and the m history
+// rows, if any) per channel, the weighted sum, then RMSNorm -> RoPE at `pos` -> store
+// as row `orow` of out.  The groups share the per-channel maximum, so every row's
+// weight exp(z + b - max) is the same for any R; their partial sums are added in group
+// order.  Every kernel that writes entries takes its R from compress_row_groups, so an
+// entry is the same bits whichever kernel (whole sequence, packed samples, decode
+// step) produced it.
 template <typename T, int OUT>
 __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, const T* hc, const T* hz,
                                                const float* ba, const float* bb, int c, int m, int64_t pos,
                                                const RopeTable& rope, unsigned flags, void* out, int64_t orow) {
-    const int t = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int cq = c >> 2;
+    const int R = (int)blockDim.x / cq;
+    const int t = tid % cq, rg = tid / cq;
     const int ch = 4 * t;
+    __shared__ float4 xb[2 * CMP_MAX_THREADS];
 
     // pass 1: per-channel max of the logits
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 8
-    for (int j = 0; j < m; ++j) {
+    for (int j = rg; j < m; j += R) {
         float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
         float4 b = load4_bias(ba, (int64_t)j * c + ch);
 #pragma unroll
         for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], f4get(z, k) + f4get(b, k));
     }
     if (hz) {
-    #pragma unroll 8
-    for (int j = 0; j < m; ++j) {
+#pragma unroll 8
+        for (int j = rg; j < m; j += R) {
             float4 z = load4<T>(hz + (int64_t)j * c + ch);
             float4 b = load4_bias(bb, (int64_t)j * c + ch);
 #pragma unroll
             for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], f4get(z, k) + f4get(b, k));
         }
     }
+    if (R > 1) {
+        xb[tid] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+        __syncthreads();
+        for (int g = 0; g < R; ++g) {
+            const float4 o = xb[g * cq + t];
+            mx[0] = fmaxf(mx[0], o.x);
+            mx[1] = fmaxf(mx[1], o.y);
+            mx[2] = fmaxf(mx[2], o.z);
+            mx[3] = fmaxf(mx[3], o.w);
+        }
+    }
     // pass 2: softmax-weighted sum
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-    for (int j = 0; j < m; ++j) {
+    for (int j = rg; j < m; j += R) {
         float4 z = load4<T>(cur_z + (int64_t)j * c + ch);
         float4 b = load4_bias(ba, (int64_t)j * c + ch);
         float4 v = load4<T>(cur_c + (int64_t)j * c + ch);
@@ -96,8 +130,8 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
         }
     }
     if (hz) {
-    #pragma unroll 8
-    for (int j = 0; j < m; ++j) {
+#pragma unroll 8
+        for (int j = rg; j < m; j += R) {
             float4 z = load4<T>(hz + (int64_t)j * c + ch);
             float4 b = load4_bias(bb, (int64_t)j * c + ch);
             float4 v = load4<T>(hc + (int64_t)j * c + ch);
@@ -109,27 +143,45 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
             }
         }
     }
+    if (R > 1) {
+        // group partials in group order (xb's first half is free: every thread has
+        // read the maxima before it passed this barrier)
+        __syncthreads();
+        xb[tid] = make_float4(num[0], num[1], num[2], num[3]);
+        xb[CMP_MAX_THREADS + tid] = make_float4(den[0], den[1], den[2], den[3]);
+        __syncthreads();
+        float4 n4 = xb[t], d4 = xb[CMP_MAX_THREADS + t];
+        for (int g = 1; g < R; ++g) {
+            const float4 o = xb[g * cq + t], e = xb[CMP_MAX_THREADS + g * cq + t];
+            n4.x += o.x; n4.y += o.y; n4.z += o.z; n4.w += o.w;
+            d4.x += e.x; d4.y += e.y; d4.z += e.z; d4.w += e.w;
+        }
+        num[0] = n4.x; num[1] = n4.y; num[2] = n4.z; num[3] = n4.w;
+        den[0] = d4.x; den[1] = d4.y; den[2] = d4.z; den[3] = d4.w;
+    }
     float y[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] = num[k] / den[k];
 
-    // RMSNorm over the c channels of the entry
+    // RMSNorm over the c channels of the entry (row group 0 holds the entry; the other
+    // groups only take part in the barriers)
     if (flags & CSA2_W_NORM) {
         __shared__ float red[32];
-        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+        float ss = rg == 0 ? y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3] : 0.0f;
         ss = warp_sum(ss);
-        if ((t & 31) == 0) red[t >> 5] = ss;
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
         __syncthreads();
-        if (t < 32) {
-            float v = (t < (int)(blockDim.x >> 5)) ? red[t] : 0.f;
+        if (tid < 32) {
+            float v = (tid < (int)(blockDim.x >> 5)) ? red[tid] : 0.f;
             v = warp_sum(v);
-            if (t == 0) red[0] = v;
+            if (tid == 0) red[0] = v;
         }
         __syncthreads();
         float r = 1.0f / sqrtf(red[0] / (float)c + 1e-6f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) y[k] *= r;
     }
+    if (rg != 0) return;
     // RoPE on the last 64 channels (interleaved pairs) at the entry's position
     if ((flags & CSA2_W_ROPE) && ch >= c - 64) {
 #pragma unroll
@@ -187,7 +239,7 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
 }
 
 template <typename T, int OUT>
-__global__ void __launch_bounds__(256) compress_kernel(
+__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
     const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
     const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
@@ -234,7 +286,7 @@ __global__ void __launch_bounds__(256) compress_kernel(
 // entry i of sample s goes to row s*out_seq_stride + i at position pos0[s] + m*i.
 // Grid: (max entries per sample, S); CTAs past their sample's entry count exit.
 template <typename T, int OUT>
-__global__ void __launch_bounds__(256) compress_varlen_kernel(
+__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_varlen_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
     const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ cu_tokens, int c, int m,
     const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
@@ -263,14 +315,17 @@ __global__ void __launch_bounds__(256) compress_varlen_kernel(
 // and the block's overlap half becomes the history of block i+1.
 // state per sequence: [ca, za (, cb, zb, prev cb, prev zb)] x [m, c] in T.
 template <typename T, int OUT>
-__global__ void __launch_bounds__(256) compress_step_kernel(
+__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_step_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
     const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ pos_arr, T* state,
     int c, int m, const RopeTable rope, unsigned flags, void* __restrict__ out, int64_t out_seq_stride) {
     pdl_wait();
     pdl_trigger();
     const int64_t b = blockIdx.x;
-    const int ch = 4 * threadIdx.x;
+    const int cq = c >> 2;
+    const int R = (int)blockDim.x / cq;
+    const int rg = (int)threadIdx.x / cq;
+    const int ch = 4 * ((int)threadIdx.x % cq);
     const bool overlap = cb != nullptr;
     const int64_t mc = (int64_t)m * c;
     T* st = state + b * (overlap ? 6 : 2) * mc;
@@ -284,19 +339,26 @@ __global__ void __launch_bounds__(256) compress_step_kernel(
     if (p < 0) return;                       // the whole CTA: no token for this sequence
     const int j = (int)(p % m);
     const int64_t i = p / m;
-    // each thread only ever touches its own 4 channels of every buffer
-    copy4<T>(s_ca + (int64_t)j * c + ch, ca + b * c + ch);
-    copy4<T>(s_za + (int64_t)j * c + ch, za + b * c + ch);
-    if (overlap) {
-        copy4<T>(s_cb + (int64_t)j * c + ch, cb + b * c + ch);
-        copy4<T>(s_zb + (int64_t)j * c + ch, zb + b * c + ch);
+    // row group 0 stores the token; each thread touches only its own 4 channels of a
+    // row, and the rows of a group's turn below are read after the barrier
+    if (rg == 0) {
+        copy4<T>(s_ca + (int64_t)j * c + ch, ca + b * c + ch);
+        copy4<T>(s_za + (int64_t)j * c + ch, za + b * c + ch);
+        if (overlap) {
+            copy4<T>(s_cb + (int64_t)j * c + ch, cb + b * c + ch);
+            copy4<T>(s_zb + (int64_t)j * c + ch, zb + b * c + ch);
+        }
     }
     if (j != m - 1) return;                  // the block is not complete yet
+    if (R > 1) __syncthreads();
     const bool hist = overlap && i > 0;
     compress_entry<T, OUT>(s_ca, s_za, hist ? s_pcb : nullptr, hist ? s_pzb : nullptr, ba, bb, c, m,
                            (int64_t)m * i, rope, flags, out, b * out_seq_stride + i);
     if (overlap) {
-        for (int r = 0; r < m; ++r) {
+        // every group has passed compress_entry's last barrier, so the history rows
+        // are read; the new block's rows were stored before the barrier above
+        __syncthreads();
+        for (int r = rg; r < m; r += R) {
             copy4<T>(s_pcb + (int64_t)r * c + ch, s_cb + (int64_t)r * c + ch);
             copy4<T>(s_pzb + (int64_t)r * c + ch, s_zb + (int64_t)r * c + ch);
         }
@@ -308,7 +370,7 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
                             const float* ba, const float* bb, const void* pcb, const void* pzb, int B,
                             int64_t n_tokens, int c, int m, const int64_t* pos0, float base, unsigned flags,
                             void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
-    dim3 grid((unsigned)(n_tokens / m), (unsigned)B), block(c / 4);
+    dim3 grid((unsigned)(n_tokens / m), (unsigned)B), block((c / 4) * compress_row_groups(m, c));
     const RopeTable rope = make_rope_table(base);
     const T* a = (const T*)ca;
     const T* z = (const T*)za;
@@ -342,7 +404,7 @@ csa2_status launch_varlen(const void* ca, const void* za, const void* cb, const 
     const T* z = (const T*)za;
     const T* b = (const T*)cb;
     const T* zz = (const T*)zb;
-    const dim3 grid((unsigned)max_entries, (unsigned)S), block(c / 4);
+    const dim3 grid((unsigned)max_entries, (unsigned)S), block((c / 4) * compress_row_groups(m, c));
     csa2_status r;
     if (out_dt == CSA2_F32)
         r = launch_pdl(compress_varlen_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
@@ -369,7 +431,7 @@ csa2_status launch_step(const void* ca, const void* za, const void* cb, const vo
     const T* b = (const T*)cb;
     const T* zz = (const T*)zb;
     T* st = (T*)state;
-    const dim3 grid((unsigned)B), block(c / 4);
+    const dim3 grid((unsigned)B), block((c / 4) * compress_row_groups(m, c));
     csa2_status r;
     if (out_dt == CSA2_F32)
         r = launch_pdl(compress_step_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,

@@ -225,28 +225,30 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
                     mbar_wait(&full[li % STAGES], (li / STAGES) & 1, a.budget, a.st);
             }
         } else {
+            // lane j copies candidate block j of each tile: its 8 rows are 544 contiguous
+            // bytes (a multiple of 16, at a 16-byte aligned offset since N is a multiple
+            // of 8) in one bulk copy; empty or out-of-range slots copy nothing (their
+            // rows are masked in the epilogue) and only arrive
+            int last = -1;
             for (int li = 0; li < (a.stall ? 0 : n_act); ++li) {
                 const int s = li % STAGES, r = li / STAGES;
                 const bool w = r == 0 || mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st);
                 if (!__all_sync(0xffffffffu, w)) break;
-                uint8_t* dst = sStage + s * MX_STAGE;
-                // 32 candidate blocks of 8 rows (544 contiguous bytes each); empty or
-                // out-of-range slots are skipped (their rows are masked in the epilogue)
                 int32_t pb = a.pool[(int64_t)g * a.n_pool + (int64_t)(t_begin + li) * BLOCKS_PER_TILE + lane];
                 if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
-#pragma unroll 2
-                for (int it = 0; it < BLOCKS_PER_TILE * 34 / 32; ++it) {
-                    const int p = it * 32 + lane;          // piece 0 .. 1087
-                    const int j = p / 34, o = p - 34 * j;
-                    const int32_t bj = __shfl_sync(0xffffffffu, pb, j);
-                    if (bj >= 0)
-                        cp_async16(dst + j * 544 + o * 16,
-                                   a.kmx + ((int64_t)b * a.N + (int64_t)bj * 8) * MX_ROW + o * 16);
+                if (pb >= 0) {
+                    mbar_arrive_expect_tx(&full[s], 8 * MX_ROW);
+                    bulk_g2s(sStage + s * MX_STAGE + lane * (8 * MX_ROW),
+                             a.kmx + ((int64_t)b * a.N + (int64_t)pb * 8) * MX_ROW, 8 * MX_ROW, &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);
                 }
-                cp_async_mbar_arrive_noinc(&full[s]);
+                last = li;
             }
-            // no copy may still be writing shared memory when the CTA exits
-            cp_async_wait_all();
+            // no copy may still be writing shared memory when the CTA exits (the last
+            // STAGES tiles hold distinct stages, so their phases are unambiguous)
+            for (int li = last; li >= 0 && li > last - STAGES; --li)
+                mbar_wait(&full[li % STAGES], (li / STAGES) & 1, a.budget, a.st);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================

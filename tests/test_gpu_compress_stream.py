@@ -62,7 +62,7 @@ def _oracle_entries(ca, za, cb, zb, m, ba, bb, flags, b):
 
 
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("overlap,m", [(True, 4), (False, 2), (True, 1)])
+@pytest.mark.parametrize("overlap,m", [(True, 4), (False, 2), (True, 1), (True, 16), (False, 128)])
 def test_stream_equals_whole_sequence(dt, overlap, m):
     B, c = 3, 512
     n = 5 * m + (m - 1)                     # five complete blocks and an unfinished one

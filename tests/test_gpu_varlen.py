@@ -28,9 +28,9 @@ def _packed(seed, lens, c, dt, overlap=True):
 
 @pytest.mark.parametrize("fmt,c,dt", [("f32", 512, torch.float32), ("fp4", 512, torch.bfloat16),
                                       ("mxfp4", 128, torch.bfloat16), ("bf16", 512, torch.bfloat16)])
-@pytest.mark.parametrize("overlap", [True, False])
-def test_varlen_equals_each_sample_alone(fmt, c, dt, overlap):
-    m = 4
+@pytest.mark.parametrize("overlap,m", [(True, 4), (False, 4), (True, 32)])
+def test_varlen_equals_each_sample_alone(fmt, c, dt, overlap, m):
+    """m = 32 splits each entry's rows over several row groups of the CTA."""
     ca, za, cb, zb, cu = _packed(601, LENS, c, dt, overlap)
     ba = W.normal_tensor((m, c), 602, 1, torch.float32, DEV, std=0.1)
     bb = W.normal_tensor((m, c), 602, 2, torch.float32, DEV, std=0.1) if overlap else None
