@@ -67,9 +67,10 @@ constexpr int OFF_LW = OFF_RINV + TC_TILE * 4;
 constexpr int OFF_SC = OFF_LW + 4 * TC_H * 4;        // [4 warps][64] output scale per head
 constexpr int OFF_SCL = OFF_SC + 4 * TC_H * 4;       // [2 items][64] scales for the loader warps
 constexpr int OFF_BAR = OFF_SCL + 2 * TC_H * 4;
-constexpr int N_BAR = 17;
+constexpr int N_BAR = 19;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BAR * 8;
-constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;
+constexpr int OFF_STGSC = (OFF_TMEMPTR + 16 + 15) / 16 * 16;   // [128 rows][32 B] staged FP4 scales
+constexpr int SMEM_BYTES = OFF_STGSC + TC_TILE * 32 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 struct TcArgs {
@@ -171,42 +172,63 @@ __device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& ss) {
     }
 }
 
-// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16.  Each
-// E2M1 pair becomes an f16x2 and is multiplied by its E4M3 block scale in f16: exact,
-// since an E2M1 value times an E4M3 scale has at most 6 significant bits and lies in
-// [2^-10, 2688]; the bf16 image is then the upper half of the exact f32.  ca, cb: the
-// chunk's 32 code bytes; scw: its four scale bytes.  The squares go to eight partial
-// sums (short dependency chains).
-__device__ __forceinline__ void fp4_chunk_to_tile(const uint4& ca, const uint4& cb, uint32_t scw, uint8_t* sK,
-                                                  int c, int r, float (&ss)[8]) {
+// Staged FP4 codes: 16-byte piece i (0..15) of row r, XOR-swizzled so that the eight
+// rows a quarter-warp touches at once sit in eight different bank groups.
+__device__ __forceinline__ uint32_t stg_code_offset(int r, int i) {
+    return (uint32_t)r * 256u + ((uint32_t)(i ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16, by table
+// lookup rather than per-value conversion.  Per 16-dim block, the eight E2M1
+// magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are multiplied by the block's E4M3 scale as
+// bf16 pairs (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits),
+// then split into a low-byte and a high-byte table; each code's 3 magnitude bits pick
+// its two bytes with a byte permute, and its sign bit is XORed into the bf16 sign.  The
+// squares (for the row's RMS) come from a byte table of 4 x magnitude^2 summed with
+// dp4a, times scale^2 / 4 per block; the chunk's sum of squares is returned.  ca, cb:
+// the chunk's 32 code bytes (value 2k in the low nibble of byte k); scw: its four
+// scale bytes.  Not inlined: one copy of the code serves the eight chunks, which keeps
+// a CTA's single pass over a tile (decode) from stalling on instruction fetch.
+__device__ __noinline__ float fp4_chunk_to_tile(uint4 ca, uint4 cb, uint32_t scw, uint8_t* sK, int c, int r) {
     const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+    float ss[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        uint32_t s2;                              // the block scale in both f16 halves
-        const unsigned short sb = (unsigned short)(((scw >> (8 * (u >> 1))) & 0xFFu) * 0x101u);
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sb));
-        uint32_t h[4];
-        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-            "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-            "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-            "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-            : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-            : "r"(cw[u]));
-        uint32_t pk[4];
+    for (int blk = 0; blk < 4; ++blk) {
+        const float sc = e4m3_to_f32((scw >> (8 * blk)) & 0xFFu);
+        const uint32_t s2 = __byte_perm(__float_as_uint(sc), 0u, 0x3232);     // (bf16 scale, bf16 scale)
+        const uint32_t t01 = bf16x2_mul(0x3F000000u, s2);                     // (0, 0.5) x scale
+        const uint32_t t23 = bf16x2_mul(0x3FC03F80u, s2);                     // (1, 1.5)
+        const uint32_t t45 = bf16x2_mul(0x40404000u, s2);                     // (2, 3)
+        const uint32_t t67 = bf16x2_mul(0x40C04080u, s2);                     // (4, 6)
+        const uint32_t lo0 = __byte_perm(t01, t23, 0x6420), hi0 = __byte_perm(t01, t23, 0x7531);
+        const uint32_t lo1 = __byte_perm(t45, t67, 0x6420), hi1 = __byte_perm(t45, t67, 0x7531);
+        uint32_t q = 0u;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t x;
-            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(h[i]), "r"(s2));
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x));
-            ss[2 * i] = fmaf(f.x, f.x, ss[2 * i]);
-            ss[2 * i + 1] = fmaf(f.y, f.y, ss[2 * i + 1]);
-            pk[i] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+        for (int h = 0; h < 2; ++h) {
+            const int u = 2 * blk + h;                   // 16-byte unit of the tile row: 8 values
+            const uint32_t w = cw[u];
+            const uint32_t m = w & 0x77777777u, mh = m >> 16, w4 = w << 4;
+            uint32_t lo = __byte_perm(lo0, lo1, m), hi = __byte_perm(hi0, hi1, m);
+            const uint32_t p0 = __byte_perm(lo, hi, 0x5140) ^ (__byte_perm(w4, w, 0x4000) & 0x80008000u);
+            const uint32_t p1 = __byte_perm(lo, hi, 0x7362) ^ (__byte_perm(w4, w, 0x5010) & 0x80008000u);
+            lo = __byte_perm(lo0, lo1, mh);
+            hi = __byte_perm(hi0, hi1, mh);
+            const uint32_t p2 = __byte_perm(lo, hi, 0x5140) ^ (__byte_perm(w4, w, 0x6020) & 0x80008000u);
+            const uint32_t p3 = __byte_perm(lo, hi, 0x7362) ^ (__byte_perm(w4, w, 0x7030) & 0x80008000u);
+            q = __dp4a(__byte_perm(0x09040100u, 0x90402410u, m), 0x01010101u, q);
+            q = __dp4a(__byte_perm(0x09040100u, 0x90402410u, mh), 0x01010101u, q);
+            *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                make_uint4(p0, p1, p2, p3);
         }
-        *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        ss[blk] = (float)q * 0.25f * (sc * sc);
     }
+    return (ss[0] + ss[1]) + (ss[2] + ss[3]);
 }
 
 template <typename TQ>
@@ -350,6 +372,8 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
     TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + hbeg) * (int64_t)TC_C + rr;
     float* pbase = a.part + ((it.bq * a.H + hbeg) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + rr;
     const int64_t pstride = (int64_t)a.n_split * PART;
+    // not unrolled: a CTA often runs this once (one item), from a cold instruction cache
+#pragma unroll 1
     for (int db = 0; db < 4; ++db) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + (uint32_t)(db * TC_H + hbeg), o);
@@ -406,7 +430,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     uint64_t* oempty = bars + 14;
     uint64_t* lred = bars + 15;
     uint64_t* scready = bars + 16;     // an item's output scales are in sScL
+    uint64_t* stg = bars + 17;         // the tile's FP4 rows are staged (one arrival per loader thread)
+    uint64_t* stgread = bars + 18;     // every loader warp has read its rows' first block
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+    uint8_t* sStgSc = smem + OFF_STGSC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -423,6 +450,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         mbar_init(oempty, 8);
         mbar_init(scready, 1);
         mbar_init(lred, 4);
+        mbar_init(stg, TC_TILE);
+        mbar_init(stgread, 4);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -470,8 +499,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     break;
                 }
                 for (int tt = 0; tt < it.nt; ++tt, ++g) {
-                    // logits: S^T = X . Qhat^T over 512 dims
-                    for (int db = 0; db < 4 && ok; ++db) {
+                    // logits: S^T = X . Qhat^T over 512 dims, the 128-dim blocks in the
+                    // order the loaders produce them
+                    for (int dbi = 0; dbi < 4 && ok; ++dbi) {
+                        const int db = FP4 ? (dbi + 1) & 3 : dbi;
                         if (!mbar_wait(&kfull[db], g & 1, a.budget, a.st)) {
                             ok = false;
                             break;
@@ -482,7 +513,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                             const int ch = 2 * db + (kk >> 2);
                             const uint32_t ko = (uint32_t)(kk & 3) * 32u;
                             mma_ss(tmem + DS_COL, sdesc_sw128(k_base + ch * CHUNK_K + ko),
-                                   sdesc_sw128(q_base + ch * CHUNK_Q + ko), IDESC_QK, (db | kk) != 0);
+                                   sdesc_sw128(q_base + ch * CHUNK_Q + ko), IDESC_QK, (dbi | kk) != 0);
                         }
                     }
                     if (!ok) break;
@@ -720,16 +751,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                                                  : (bf_row ? kvb + s.row * (int64_t)(TC_C * 2) : nullptr);
                 const float* pre = s.kind == 2 ? a.rinv_swa : (bf_row ? a.rinv_kv : nullptr);
                 const float rpre = (pre && s.kind != 0) ? pre[s.row] : 0.0f;
-                uint4 fc[16];
-                uint4 fs0 = make_uint4(0u, 0u, 0u, 0u), fs1 = fs0;
                 const bool fp4_row = FP4 && s.kind == 1;
-                if (fp4_row) {
-                    const uint4* p = reinterpret_cast<const uint4*>(kvb + s.row * fp4_row_bytes(TC_C));
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) fc[i] = p[i];
-                    fs0 = p[16];
-                    fs1 = p[17];
-                }
+                const uint8_t* frow = fp4_row ? kvb + s.row * fp4_row_bytes(TC_C) : nullptr;
                 // bf16 rows are copied cooperatively: per instruction the warp moves two of
                 // its 32 rows, 256 contiguous bytes each (16 lanes x 16 B per row)
                 const int wl = r >> 5, half = lane >> 4, piece = lane & 15;
@@ -741,9 +764,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                 }
                 float ss = 0.0f, ss8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
                 bool w = true;
+                if (FP4) {
+                    // the tile's FP4 rows are staged whole (codes in the space of the first
+                    // 128-dim block, whose PV reads finish first; scales beside): each
+                    // thread's 18 copies are in flight together.  Blocks 1..3 are produced
+                    // from the staging, block 0 last, from registers.
+                    if (g > 0) w = w && mbar_wait(&kempty[0], (g - 1) & 1, a.budget, a.st);
+                    if (w && fp4_row) {
 #pragma unroll
-                for (int db = 0; db < 4; ++db) {
-                    if (g > 0) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
+                        for (int i = 0; i < 16; ++i) cp_async16(sK + stg_code_offset(r, i), frow + 16 * i);
+                        cp_async16(sStgSc + r * 32, frow + 256);
+                        cp_async16(sStgSc + r * 32 + 16, frow + 272);
+                    }
+                    cp_async_mbar_arrive_noinc(stg);
+                }
+#pragma unroll
+                for (int dbi = 0; dbi < 4; ++dbi) {
+                    const int db = FP4 ? (dbi + 1) & 3 : dbi;
+                    if (g > 0 && !(FP4 && db == 0)) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
+                    if (FP4 && dbi == 0) w = w && mbar_wait(stg, g & 1, a.budget, a.st);
+                    uint4 rc[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                                   make_uint4(0u, 0u, 0u, 0u)};
+                    uint32_t rs[2] = {0u, 0u};
+                    if (FP4 && db == 0) {
+                        // this row's raw block 0 into registers; the staging is overwritten
+                        // only after every loader warp has read its rows
+                        if (w && fp4_row) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) rc[i] = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, i));
+                            rs[0] = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32);
+                            rs[1] = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32 + 4);
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(stgread);
+                        w = w && mbar_wait(stgread, g & 1, a.budget, a.st);
+                    }
                     if (w) {
                         const int ch = 2 * db + (piece >> 3), u = piece & 7;
 #pragma unroll
@@ -755,9 +810,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
 #pragma unroll
                         for (int c2 = 2 * db; c2 < 2 * db + 2; ++c2) {
                             if (fp4_row) {
-                                const uint32_t scw = (c2 < 4) ? (c2 == 0 ? fs0.x : c2 == 1 ? fs0.y : c2 == 2 ? fs0.z : fs0.w)
-                                                              : (c2 == 4 ? fs1.x : c2 == 5 ? fs1.y : c2 == 6 ? fs1.z : fs1.w);
-                                fp4_chunk_to_tile(fc[2 * c2], fc[2 * c2 + 1], scw, sK, c2, r, ss8);
+                                if (db == 0) {
+                                    ss8[c2] = fp4_chunk_to_tile(rc[2 * c2], rc[2 * c2 + 1], rs[c2], sK, c2, r);
+                                } else {
+                                    const uint4 ca = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 2 * c2));
+                                    const uint4 cb = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 2 * c2 + 1));
+                                    const uint32_t scw = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32 + 4 * c2);
+                                    ss8[c2] = fp4_chunk_to_tile(ca, cb, scw, sK, c2, r);
+                                }
                             } else if (!bf_row) {
 #pragma unroll
                                 for (int u2 = 0; u2 < 8; ++u2)
@@ -768,23 +828,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     }
                     cp_async_commit();
                 }
-                // each 128-dim block is complete once its copy group has landed
+                // each 128-dim block is complete once its copy group has landed (blocks in
+                // the order they were produced)
                 cp_async_wait<3>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[0]);
+                if (lane == 0) mbar_arrive(&kfull[FP4 ? 1 : 0]);
                 cp_async_wait<2>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[1]);
+                if (lane == 0) mbar_arrive(&kfull[FP4 ? 2 : 1]);
                 cp_async_wait<1>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[2]);
+                if (lane == 0) mbar_arrive(&kfull[FP4 ? 3 : 2]);
                 cp_async_wait<0>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[3]);
+                if (lane == 0) mbar_arrive(&kfull[FP4 ? 0 : 3]);
                 if (!__all_sync(FULL, w)) {
                     ok = false;
                     break;
@@ -795,7 +856,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                         rv = rpre;
                     } else {
                         if (bf_row) {
-#pragma unroll
+                            // not unrolled, for the same reason as the FP4 chunks
+#pragma unroll 1
                             for (int c = 0; c < 8; ++c)
 #pragma unroll
                                 for (int u = 0; u < 8; ++u)
