@@ -47,7 +47,7 @@ __device__ __forceinline__ float f4get(const float4& v, int k) {
 
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_FP4 = 2, OUT_MX = 3 };
 
-constexpr int CMP_MAX_THREADS = 512;
+constexpr int CMP_MAX_THREADS = 1024;
 
 // Row groups of one entry's CTA: a long block (HCA's m' = 128) would leave each
 // thread a serial walk over m rows, so blocks of 16 rows or more are split into up to
@@ -56,6 +56,12 @@ constexpr int CMP_MAX_THREADS = 512;
 int compress_row_groups(int m, int c) {
     if (m < 16) return 1;
     return std::max(1, std::min(m / 8, CMP_MAX_THREADS / (c / 4)));
+}
+
+// Dynamic shared memory of an entry's CTA: the groups' exchange buffer, none for one group.
+size_t compress_smem(int m, int c) {
+    const int R = compress_row_groups(m, c);
+    return R > 1 ? (size_t)2 * R * (c / 4) * sizeof(float4) : 0;
 }
 
 template <typename T>
@@ -75,16 +81,17 @@ __device__ __forceinline__ void copy4(T* dst, const T* src) {
 // order.  Every kernel that writes entries takes its R from compress_row_groups, so an
 // entry is the same bits whichever kernel (whole sequence, packed samples, decode
 // step) produced it.
-template <typename T, int OUT>
+template <typename T, int OUT, int MAXT>
 __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, const T* hc, const T* hz,
                                                const float* ba, const float* bb, int c, int m, int64_t pos,
                                                const RopeTable& rope, unsigned flags, void* out, int64_t orow) {
     const int tid = threadIdx.x;
     const int cq = c >> 2;
-    const int R = (int)blockDim.x / cq;
-    const int t = tid % cq, rg = tid / cq;
+    const int R = MAXT > 256 ? (int)blockDim.x / cq : 1;   // CTAs of up to 256 threads: one group
+    const int t = MAXT > 256 ? tid % cq : tid, rg = MAXT > 256 ? tid / cq : 0;
     const int ch = 4 * t;
-    __shared__ float4 xb[2 * CMP_MAX_THREADS];
+    extern __shared__ float4 xb[];             // [2][blockDim.x] when R > 1 (dynamic, compress_smem)
+    const int nt = (int)blockDim.x;
 
     // pass 1: per-channel max of the logits
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -148,11 +155,11 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
         // read the maxima before it passed this barrier)
         __syncthreads();
         xb[tid] = make_float4(num[0], num[1], num[2], num[3]);
-        xb[CMP_MAX_THREADS + tid] = make_float4(den[0], den[1], den[2], den[3]);
+        xb[nt + tid] = make_float4(den[0], den[1], den[2], den[3]);
         __syncthreads();
-        float4 n4 = xb[t], d4 = xb[CMP_MAX_THREADS + t];
+        float4 n4 = xb[t], d4 = xb[nt + t];
         for (int g = 1; g < R; ++g) {
-            const float4 o = xb[g * cq + t], e = xb[CMP_MAX_THREADS + g * cq + t];
+            const float4 o = xb[g * cq + t], e = xb[nt + g * cq + t];
             n4.x += o.x; n4.y += o.y; n4.z += o.z; n4.w += o.w;
             d4.x += e.x; d4.y += e.y; d4.z += e.z; d4.w += e.w;
         }
@@ -238,8 +245,8 @@ __device__ __forceinline__ void compress_entry(const T* cur_c, const T* cur_z, c
     }
 }
 
-template <typename T, int OUT>
-__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_kernel(
+template <typename T, int OUT, int MAXT>
+__global__ void __launch_bounds__(MAXT) compress_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb,
     const T* __restrict__ zb, const float* __restrict__ ba, const float* __restrict__ bb,
     const T* __restrict__ prev_cb, const T* __restrict__ prev_zb, int64_t n_tokens, int c, int m,
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_kernel(
         }
     }
     const int64_t pos = (pos0_arr ? pos0_arr[bseq] : 0) + (int64_t)m * i;
-    compress_entry<T, OUT>(ca + (m * i) * (int64_t)c, za + (m * i) * (int64_t)c, hc, hz, ba, bb, c, m, pos, rope,
+    compress_entry<T, OUT, MAXT>(ca + (m * i) * (int64_t)c, za + (m * i) * (int64_t)c, hc, hz, ba, bb, c, m, pos, rope,
                            flags, out, bseq * out_seq_stride + i);
 }
 
@@ -285,8 +292,8 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_kernel(
 // (DSA-to-CSA/HCA page, the note under the compressor code and «算法语义») -- and
 // entry i of sample s goes to row s*out_seq_stride + i at position pos0[s] + m*i.
 // Grid: (max entries per sample, S); CTAs past their sample's entry count exit.
-template <typename T, int OUT>
-__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_varlen_kernel(
+template <typename T, int OUT, int MAXT>
+__global__ void __launch_bounds__(MAXT) compress_varlen_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
     const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ cu_tokens, int c, int m,
     const int64_t* __restrict__ pos0_arr, const RopeTable rope, unsigned flags, void* __restrict__ out,
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_varlen_kernel(
         hz = zb + r0 - (int64_t)m * c;
     }
     const int64_t pos = (pos0_arr ? pos0_arr[smp] : 0) + (int64_t)m * i;
-    compress_entry<T, OUT>(ca + r0, za + r0, hc, hz, ba, bb, c, m, pos, rope, flags, out, smp * out_seq_stride + i);
+    compress_entry<T, OUT, MAXT>(ca + r0, za + r0, hc, hz, ba, bb, c, m, pos, rope, flags, out, smp * out_seq_stride + i);
 }
 
 // One decode step for B sequences (a CTA each): the token at position pos[b] (< 0: no
@@ -314,8 +321,8 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_varlen_kernel(
 // i = pos / m, entry i (position m*i) is written to row b*out_seq_stride + i of out
 // and the block's overlap half becomes the history of block i+1.
 // state per sequence: [ca, za (, cb, zb, prev cb, prev zb)] x [m, c] in T.
-template <typename T, int OUT>
-__global__ void __launch_bounds__(CMP_MAX_THREADS) compress_step_kernel(
+template <typename T, int OUT, int MAXT>
+__global__ void __launch_bounds__(MAXT) compress_step_kernel(
     const T* __restrict__ ca, const T* __restrict__ za, const T* __restrict__ cb, const T* __restrict__ zb,
     const float* __restrict__ ba, const float* __restrict__ bb, const int64_t* __restrict__ pos_arr, T* state,
     int c, int m, const RopeTable rope, unsigned flags, void* __restrict__ out, int64_t out_seq_stride) {
@@ -323,9 +330,9 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_step_kernel(
     pdl_trigger();
     const int64_t b = blockIdx.x;
     const int cq = c >> 2;
-    const int R = (int)blockDim.x / cq;
-    const int rg = (int)threadIdx.x / cq;
-    const int ch = 4 * ((int)threadIdx.x % cq);
+    const int R = MAXT > 256 ? (int)blockDim.x / cq : 1;
+    const int rg = MAXT > 256 ? (int)threadIdx.x / cq : 0;
+    const int ch = 4 * (MAXT > 256 ? (int)threadIdx.x % cq : (int)threadIdx.x);
     const bool overlap = cb != nullptr;
     const int64_t mc = (int64_t)m * c;
     T* st = state + b * (overlap ? 6 : 2) * mc;
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_step_kernel(
     if (j != m - 1) return;                  // the block is not complete yet
     if (R > 1) __syncthreads();
     const bool hist = overlap && i > 0;
-    compress_entry<T, OUT>(s_ca, s_za, hist ? s_pcb : nullptr, hist ? s_pzb : nullptr, ba, bb, c, m,
+    compress_entry<T, OUT, MAXT>(s_ca, s_za, hist ? s_pcb : nullptr, hist ? s_pzb : nullptr, ba, bb, c, m,
                            (int64_t)m * i, rope, flags, out, b * out_seq_stride + i);
     if (overlap) {
         // every group has passed compress_entry's last barrier, so the history rows
@@ -365,8 +372,8 @@ __global__ void __launch_bounds__(CMP_MAX_THREADS) compress_step_kernel(
     }
 }
 
-template <typename T>
-csa2_status launch_compress(const void* ca, const void* za, const void* cb, const void* zb,
+template <typename T, int MAXT>
+csa2_status launch_compress_t(const void* ca, const void* za, const void* cb, const void* zb,
                             const float* ba, const float* bb, const void* pcb, const void* pzb, int B,
                             int64_t n_tokens, int c, int m, const int64_t* pos0, float base, unsigned flags,
                             void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
@@ -380,22 +387,22 @@ csa2_status launch_compress(const void* ca, const void* za, const void* cb, cons
     const T* p2 = (const T*)pzb;
     csa2_status r;
     if (out_dt == CSA2_F32)
-        r = launch_pdl(compress_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+        r = launch_pdl(compress_kernel<T, OUT_F32, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        r = launch_pdl(compress_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+        r = launch_pdl(compress_kernel<T, OUT_BF16, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else if (out_dt == CSA2_FP4_E4M3x16)
-        r = launch_pdl(compress_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+        r = launch_pdl(compress_kernel<T, OUT_FP4, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else
-        r = launch_pdl(compress_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
+        r = launch_pdl(compress_kernel<T, OUT_MX, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, p1, p2, n_tokens, c, m,
                        pos0, rope, flags, out, oss);
     return r != CSA2_OK ? r : csa2_launch_status();
 }
 
-template <typename T>
-csa2_status launch_varlen(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+template <typename T, int MAXT>
+csa2_status launch_varlen_t(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
                           const float* bb, const int64_t* cu_tokens, int S, int64_t max_entries, int c, int m,
                           const int64_t* pos0, float base, unsigned flags, void* out, csa2_dtype out_dt, int64_t oss,
                           cudaStream_t s) {
@@ -407,22 +414,22 @@ csa2_status launch_varlen(const void* ca, const void* za, const void* cb, const 
     const dim3 grid((unsigned)max_entries, (unsigned)S), block((c / 4) * compress_row_groups(m, c));
     csa2_status r;
     if (out_dt == CSA2_F32)
-        r = launch_pdl(compress_varlen_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+        r = launch_pdl(compress_varlen_kernel<T, OUT_F32, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, cu_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        r = launch_pdl(compress_varlen_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+        r = launch_pdl(compress_varlen_kernel<T, OUT_BF16, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, cu_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else if (out_dt == CSA2_FP4_E4M3x16)
-        r = launch_pdl(compress_varlen_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+        r = launch_pdl(compress_varlen_kernel<T, OUT_FP4, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, cu_tokens, c, m,
                        pos0, rope, flags, out, oss);
     else
-        r = launch_pdl(compress_varlen_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, cu_tokens, c, m,
+        r = launch_pdl(compress_varlen_kernel<T, OUT_MX, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, cu_tokens, c, m,
                        pos0, rope, flags, out, oss);
     return r != CSA2_OK ? r : csa2_launch_status();
 }
 
-template <typename T>
-csa2_status launch_step(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+template <typename T, int MAXT>
+csa2_status launch_step_t(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
                         const float* bb, const int64_t* pos, void* state, int B, int c, int m, float base,
                         unsigned flags, void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
     const RopeTable rope = make_rope_table(base);
@@ -434,18 +441,47 @@ csa2_status launch_step(const void* ca, const void* za, const void* cb, const vo
     const dim3 grid((unsigned)B), block((c / 4) * compress_row_groups(m, c));
     csa2_status r;
     if (out_dt == CSA2_F32)
-        r = launch_pdl(compress_step_kernel<T, OUT_F32>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+        r = launch_pdl(compress_step_kernel<T, OUT_F32, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
                        flags, out, oss);
     else if (out_dt == CSA2_BF16)
-        r = launch_pdl(compress_step_kernel<T, OUT_BF16>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+        r = launch_pdl(compress_step_kernel<T, OUT_BF16, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
                        flags, out, oss);
     else if (out_dt == CSA2_FP4_E4M3x16)
-        r = launch_pdl(compress_step_kernel<T, OUT_FP4>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+        r = launch_pdl(compress_step_kernel<T, OUT_FP4, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
                        flags, out, oss);
     else
-        r = launch_pdl(compress_step_kernel<T, OUT_MX>, grid, block, 0, s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
+        r = launch_pdl(compress_step_kernel<T, OUT_MX, MAXT>, grid, block, compress_smem(m, c), s, a, z, b, zz, ba, bb, pos, st, c, m, rope,
                        flags, out, oss);
     return r != CSA2_OK ? r : csa2_launch_status();
+}
+
+template <typename T>
+csa2_status launch_compress(const void* ca, const void* za, const void* cb, const void* zb,
+                            const float* ba, const float* bb, const void* pcb, const void* pzb, int B,
+                            int64_t n_tokens, int c, int m, const int64_t* pos0, float base, unsigned flags,
+                            void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
+    // long blocks run their row groups in up to CMP_MAX_THREADS threads; one group keeps
+    // the small CTA (and its register budget)
+    return compress_row_groups(m, c) > 1 ? launch_compress_t<T, CMP_MAX_THREADS>(ca, za, cb, zb, ba, bb, pcb, pzb, B, n_tokens, c, m, pos0, base, flags, out, out_dt, oss, s) : launch_compress_t<T, 256>(ca, za, cb, zb, ba, bb, pcb, pzb, B, n_tokens, c, m, pos0, base, flags, out, out_dt, oss, s);
+}
+
+template <typename T>
+csa2_status launch_varlen(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+                          const float* bb, const int64_t* cu_tokens, int S, int64_t max_entries, int c, int m,
+                          const int64_t* pos0, float base, unsigned flags, void* out, csa2_dtype out_dt, int64_t oss,
+                          cudaStream_t s) {
+    // long blocks run their row groups in up to CMP_MAX_THREADS threads; one group keeps
+    // the small CTA (and its register budget)
+    return compress_row_groups(m, c) > 1 ? launch_varlen_t<T, CMP_MAX_THREADS>(ca, za, cb, zb, ba, bb, cu_tokens, S, max_entries, c, m, pos0, base, flags, out, out_dt, oss, s) : launch_varlen_t<T, 256>(ca, za, cb, zb, ba, bb, cu_tokens, S, max_entries, c, m, pos0, base, flags, out, out_dt, oss, s);
+}
+
+template <typename T>
+csa2_status launch_step(const void* ca, const void* za, const void* cb, const void* zb, const float* ba,
+                        const float* bb, const int64_t* pos, void* state, int B, int c, int m, float base,
+                        unsigned flags, void* out, csa2_dtype out_dt, int64_t oss, cudaStream_t s) {
+    // long blocks run their row groups in up to CMP_MAX_THREADS threads; one group keeps
+    // the small CTA (and its register budget)
+    return compress_row_groups(m, c) > 1 ? launch_step_t<T, CMP_MAX_THREADS>(ca, za, cb, zb, ba, bb, pos, state, B, c, m, base, flags, out, out_dt, oss, s) : launch_step_t<T, 256>(ca, za, cb, zb, ba, bb, pos, state, B, c, m, base, flags, out, out_dt, oss, s);
 }
 
 }  // namespace
