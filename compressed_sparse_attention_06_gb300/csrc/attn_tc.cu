@@ -184,23 +184,28 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-// Chunk c (dims 64c .. 64c+63) of an FP4 row into row r of the tile as bf16, by table
-// lookup rather than per-value conversion.  Per 16-dim block, the eight E2M1
-// magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are multiplied by the block's E4M3 scale as
-// bf16 pairs (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits),
-// then split into a low-byte and a high-byte table; each code's 3 magnitude bits pick
-// its two bytes with a byte permute, and its sign bit is XORed into the bf16 sign.  The
-// squares (for the row's RMS) come from a byte table of 4 x magnitude^2 summed with
-// dp4a, times scale^2 / 4 per block; the chunk's sum of squares is returned.  ca, cb:
-// the chunk's 32 code bytes (value 2k in the low nibble of byte k); scw: its four
-// scale bytes.  Not inlined: one copy of the code serves the eight chunks, which keeps
-// a CTA's single pass over a tile (decode) from stalling on instruction fetch.
-__device__ __noinline__ float fp4_chunk_to_tile(uint4 ca, uint4 cb, uint32_t scw, uint8_t* sK, int c, int r) {
-    const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-    float ss[4];
+// 128-dim block db (chunks 2db, 2db+1: dims 128db .. 128db+127) of an FP4 row into row
+// r of the tile as bf16, by table lookup rather than per-value conversion.  Per 16-dim
+// scale block, the eight E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are multiplied by
+// the block's E4M3 scale as bf16 pairs (exact: an E2M1 value times an E4M3 scale has at
+// most 6 significant bits), then split into a low-byte and a high-byte table; each
+// code's 3 magnitude bits pick its two bytes with a byte permute, and its sign bit is
+// XORed into the bf16 sign.  The squares (for the row's RMS) come from a byte table of
+// 4 x magnitude^2 summed with dp4a, times scale^2 / 4 per scale block; the block's sum
+// of squares is returned.  code[4]: the block's 64 code bytes (value 2k in the low
+// nibble of byte k); sc0, sc1: the four scale bytes of each chunk.  The eight scale
+// blocks are independent chains, unrolled together for the latency; not inlined: one
+// copy of the code serves the four blocks, which keeps a CTA's single pass over a tile
+// (decode) from stalling on instruction fetch.
+__device__ __noinline__ float fp4_block_to_tile(uint4 k0, uint4 k1, uint4 k2, uint4 k3, uint32_t sc0, uint32_t sc1,
+                                                uint8_t* sK, int db, int r) {
+    const uint32_t cw[16] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w,
+                             k2.x, k2.y, k2.z, k2.w, k3.x, k3.y, k3.z, k3.w};
+    float ss[8];
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-        const float sc = e4m3_to_f32((scw >> (8 * blk)) & 0xFFu);
+    for (int sb = 0; sb < 8; ++sb) {                    // scale block: chunk sb / 4, 16 dims
+        const uint32_t scw = sb < 4 ? sc0 : sc1;
+        const float sc = e4m3_to_f32((scw >> (8 * (sb & 3))) & 0xFFu);
         const uint32_t s2 = __byte_perm(__float_as_uint(sc), 0u, 0x3232);     // (bf16 scale, bf16 scale)
         const uint32_t t01 = bf16x2_mul(0x3F000000u, s2);                     // (0, 0.5) x scale
         const uint32_t t23 = bf16x2_mul(0x3FC03F80u, s2);                     // (1, 1.5)
@@ -211,8 +216,8 @@ __device__ __noinline__ float fp4_chunk_to_tile(uint4 ca, uint4 cb, uint32_t scw
         uint32_t q = 0u;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int u = 2 * blk + h;                   // 16-byte unit of the tile row: 8 values
-            const uint32_t w = cw[u];
+            const int u = 2 * (sb & 3) + h;              // 16-byte unit of the chunk row: 8 values
+            const uint32_t w = cw[2 * sb + h];
             const uint32_t m = w & 0x77777777u, mh = m >> 16, w4 = w << 4;
             uint32_t lo = __byte_perm(lo0, lo1, m), hi = __byte_perm(hi0, hi1, m);
             const uint32_t p0 = __byte_perm(lo, hi, 0x5140) ^ (__byte_perm(w4, w, 0x4000) & 0x80008000u);
@@ -223,12 +228,12 @@ __device__ __noinline__ float fp4_chunk_to_tile(uint4 ca, uint4 cb, uint32_t scw
             const uint32_t p3 = __byte_perm(lo, hi, 0x7362) ^ (__byte_perm(w4, w, 0x7030) & 0x80008000u);
             q = __dp4a(__byte_perm(0x09040100u, 0x90402410u, m), 0x01010101u, q);
             q = __dp4a(__byte_perm(0x09040100u, 0x90402410u, mh), 0x01010101u, q);
-            *reinterpret_cast<uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
+            *reinterpret_cast<uint4*>(sK + (2 * db + (sb >> 2)) * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)) =
                 make_uint4(p0, p1, p2, p3);
         }
-        ss[blk] = (float)q * 0.25f * (sc * sc);
+        ss[sb] = (float)q * 0.25f * (sc * sc);
     }
-    return (ss[0] + ss[1]) + (ss[2] + ss[3]);
+    return ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
 }
 
 template <typename TQ>
@@ -807,23 +812,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                                 cp_async16(sK + ch * CHUNK_K + sw128_offset((uint32_t)(32 * wl + 2 * j + half), (uint32_t)u),
                                            srcj[j] + ch * 128 + u * 16);
                         }
+                        if (fp4_row) {
+                            if (db == 0) {
+                                ss8[0] = fp4_block_to_tile(rc[0], rc[1], rc[2], rc[3], rs[0], rs[1], sK, 0, r);
+                            } else {
+                                const uint4 k0 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db));
+                                const uint4 k1 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 1));
+                                const uint4 k2 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 2));
+                                const uint4 k3 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 3));
+                                const uint2 scw = *reinterpret_cast<const uint2*>(sStgSc + r * 32 + 8 * db);
+                                ss8[db] = fp4_block_to_tile(k0, k1, k2, k3, scw.x, scw.y, sK, db, r);
+                            }
+                        } else if (!bf_row) {
 #pragma unroll
-                        for (int c2 = 2 * db; c2 < 2 * db + 2; ++c2) {
-                            if (fp4_row) {
-                                if (db == 0) {
-                                    ss8[c2] = fp4_chunk_to_tile(rc[2 * c2], rc[2 * c2 + 1], rs[c2], sK, c2, r);
-                                } else {
-                                    const uint4 ca = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 2 * c2));
-                                    const uint4 cb = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 2 * c2 + 1));
-                                    const uint32_t scw = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32 + 4 * c2);
-                                    ss8[c2] = fp4_chunk_to_tile(ca, cb, scw, sK, c2, r);
-                                }
-                            } else if (!bf_row) {
+                            for (int c2 = 2 * db; c2 < 2 * db + 2; ++c2)
 #pragma unroll
                                 for (int u2 = 0; u2 < 8; ++u2)
                                     *reinterpret_cast<uint4*>(sK + c2 * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u2)) =
                                         make_uint4(0u, 0u, 0u, 0u);
-                            }
                         }
                     }
                     cp_async_commit();
