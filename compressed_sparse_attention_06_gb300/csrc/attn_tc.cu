@@ -47,7 +47,7 @@ using namespace sm100;
 constexpr int TC_C = 512;
 constexpr int TC_H = 64;
 constexpr int TC_TILE = 128;
-constexpr int TC_THREADS = 320;
+constexpr int TC_THREADS = 448;
 constexpr float TC_SHIFT = 24.0f;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int QIMG_BYTES = TC_H * TC_C * 2;     // 64 KB: 8 chunks of 64 rows x 128 B
@@ -67,10 +67,11 @@ constexpr int OFF_LW = OFF_RINV + TC_TILE * 4;
 constexpr int OFF_SC = OFF_LW + 4 * TC_H * 4;        // [4 warps][64] output scale per head
 constexpr int OFF_SCL = OFF_SC + 4 * TC_H * 4;       // [2 items][64] scales for the loader warps
 constexpr int OFF_BAR = OFF_SCL + 2 * TC_H * 4;
-constexpr int N_BAR = 19;
+constexpr int N_BAR = 20;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BAR * 8;
 constexpr int OFF_STGSC = (OFF_TMEMPTR + 16 + 15) / 16 * 16;   // [128 rows][32 B] staged FP4 scales
-constexpr int SMEM_BYTES = OFF_STGSC + TC_TILE * 32 + 1024;
+constexpr int OFF_SS = OFF_STGSC + TC_TILE * 32;              // [128] loader group 1's sums of squares
+constexpr int SMEM_BYTES = OFF_SS + TC_TILE * 4 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 struct TcArgs {
@@ -413,6 +414,7 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
 }
 
 template <bool FP4, typename TO>
+// 14 warps: at most 128 registers a thread (four warps share one SM sub-partition's 16K registers)
 __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -436,9 +438,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     uint64_t* lred = bars + 15;
     uint64_t* scready = bars + 16;     // an item's output scales are in sScL
     uint64_t* stg = bars + 17;         // the tile's FP4 rows are staged (one arrival per loader thread)
-    uint64_t* stgread = bars + 18;     // every loader warp has read its rows' first block
+    uint64_t* stgread = bars + 18;     // every loader warp has taken its rows' codes from the staging
+    uint64_t* ssrdy = bars + 19;       // loader group 1's sums of squares are in sSS
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
     uint8_t* sStgSc = smem + OFF_STGSC;
+    float* sSS = reinterpret_cast<float*>(smem + OFF_SS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -455,8 +459,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         mbar_init(oempty, 8);
         mbar_init(scready, 1);
         mbar_init(lred, 4);
-        mbar_init(stg, TC_TILE);
-        mbar_init(stgread, 4);
+        mbar_init(stg, 2 * TC_TILE);
+        mbar_init(stgread, 8);
+        mbar_init(ssrdy, 4);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -584,35 +589,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     break;
                 }
                 tc_fence_after();
-                uint32_t s0[32], s1[32];
-                tmem_ld32(tmem + lane_base + DS_COL, s0);
-                tmem_ld32(tmem + lane_base + DS_COL + 32, s1);
-                tmem_wait_ld();
                 const float rinv = sRinv[r];
                 const float c1 = rinv * c1_base;
-                uint32_t pk[32];
+                // heads 0..31, then 32..63 (half the logits live at a time)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(s0[2 * i]), c1, c0));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(s0[2 * i + 1]), c1, c0));
-                    if (rinv == 0.0f) p0 = p1 = 0.0f;
-                    lacc[2 * i] += p0;
-                    lacc[2 * i + 1] += p1;
-                    pk[i] = pack_bf16x2(p0 * rinv, p1 * rinv);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t sv[32];
+                    tmem_ld32(tmem + lane_base + DS_COL + 32 * hh, sv);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c1, c0));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c1, c0));
+                        if (rinv == 0.0f) p0 = p1 = 0.0f;
+                        lacc[32 * hh + 2 * i] += p0;
+                        lacc[32 * hh + 2 * i + 1] += p1;
+                        pk[i] = pack_bf16x2(p0 * rinv, p1 * rinv);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4*>(sP + sw128_offset((uint32_t)r, (uint32_t)(4 * hh + u))) =
+                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(s1[2 * i]), c1, c0));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(s1[2 * i + 1]), c1, c0));
-                    if (rinv == 0.0f) p0 = p1 = 0.0f;
-                    lacc[32 + 2 * i] += p0;
-                    lacc[33 + 2 * i] += p1;
-                    pk[16 + i] = pack_bf16x2(p0 * rinv, p1 * rinv);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<uint4*>(sP + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -725,13 +724,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         }
     } else {
         // ============================ loaders ============================
-        const int r = threadIdx.x - 192;           // slot of the tile
+        // two groups of four warps share the tile's slots, a thread per slot in each:
+        // group 0 produces the 128-dim blocks {1, 0} of FP4 tiles ({0, 1} of bf16 tiles)
+        // and the slot's RMS factor, group 1 the blocks {2, 3} and half of the squares
+        const int lt = threadIdx.x - 192;
+        const int hf = lt / TC_TILE;               // loader group
+        const int r = lt % TC_TILE;                // slot of the tile
         const int quad = warp & 3;                 // tensor-memory lane quarter of this warp
+        const int dbA = hf == 0 ? (FP4 ? 1 : 0) : 2;   // this group's blocks, in production order
+        const int dbB = hf == 0 ? (FP4 ? 0 : 1) : 3;
         const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv);
         int g = 0, qi = 0;
         bool ok = true;
-        // heads 32..63 of the previous item's output, stored once the next item's first
-        // tile is on its way (or after the last item)
+        // heads 32..63 of the previous item's output (group 0), stored once the next
+        // item's first tile is on its way (or after the last item)
         ItemInfo pend;
         bool have_pend = false;
         auto run_pending = [&]() {
@@ -755,7 +761,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                 const uint8_t* src = s.kind == 2 ? a.swa + s.row * (int64_t)(TC_C * 2)
                                                  : (bf_row ? kvb + s.row * (int64_t)(TC_C * 2) : nullptr);
                 const float* pre = s.kind == 2 ? a.rinv_swa : (bf_row ? a.rinv_kv : nullptr);
-                const float rpre = (pre && s.kind != 0) ? pre[s.row] : 0.0f;
+                const float rpre = (hf == 0 && pre && s.kind != 0) ? pre[s.row] : 0.0f;
                 const bool fp4_row = FP4 && s.kind == 1;
                 const uint8_t* frow = fp4_row ? kvb + s.row * fp4_row_bytes(TC_C) : nullptr;
                 // bf16 rows are copied cooperatively: per instruction the warp moves two of
@@ -767,43 +773,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     const uint64_t p = __shfl_sync(FULL, (uint64_t)(uintptr_t)(bf_row ? src : nullptr), 2 * j + half);
                     srcj[j] = reinterpret_cast<const uint8_t*>((uintptr_t)p);
                 }
-                float ss = 0.0f, ss8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                float ss = 0.0f;
                 bool w = true;
+                uint4 kc[8];
+                uint32_t ks[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) kc[i] = make_uint4(0u, 0u, 0u, 0u);
                 if (FP4) {
-                    // the tile's FP4 rows are staged whole (codes in the space of the first
-                    // 128-dim block, whose PV reads finish first; scales beside): each
-                    // thread's 18 copies are in flight together.  Blocks 1..3 are produced
-                    // from the staging, block 0 last, from registers.
+                    // the tile's FP4 rows are staged whole (codes in the space of block 0,
+                    // whose PV reads finish first; scales beside), each group copying half
+                    // of every row so that all copies are in flight together; each thread
+                    // then takes its two blocks' codes into registers, and block 0 is
+                    // written only after every loader warp has done so
                     if (g > 0) w = w && mbar_wait(&kempty[0], (g - 1) & 1, a.budget, a.st);
                     if (w && fp4_row) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) cp_async16(sK + stg_code_offset(r, i), frow + 16 * i);
-                        cp_async16(sStgSc + r * 32, frow + 256);
-                        cp_async16(sStgSc + r * 32 + 16, frow + 272);
+                        for (int i = 0; i < 8; ++i)
+                            cp_async16(sK + stg_code_offset(r, 8 * hf + i), frow + 16 * (8 * hf + i));
+                        cp_async16(sStgSc + r * 32 + 16 * hf, frow + 256 + 16 * hf);
                     }
                     cp_async_mbar_arrive_noinc(stg);
+                    w = w && mbar_wait(stg, g & 1, a.budget, a.st);
+                    if (w && fp4_row) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            kc[i] = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * dbA + i));
+                            kc[4 + i] = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * dbB + i));
+                        }
+                        const uint2 sa = *reinterpret_cast<const uint2*>(sStgSc + r * 32 + 8 * dbA);
+                        const uint2 sb = *reinterpret_cast<const uint2*>(sStgSc + r * 32 + 8 * dbB);
+                        ks[0] = sa.x;
+                        ks[1] = sa.y;
+                        ks[2] = sb.x;
+                        ks[3] = sb.y;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(stgread);
                 }
 #pragma unroll
-                for (int dbi = 0; dbi < 4; ++dbi) {
-                    const int db = FP4 ? (dbi + 1) & 3 : dbi;
+                for (int bi = 0; bi < 2; ++bi) {
+                    const int db = bi == 0 ? dbA : dbB;
                     if (g > 0 && !(FP4 && db == 0)) w = w && mbar_wait(&kempty[db], (g - 1) & 1, a.budget, a.st);
-                    if (FP4 && dbi == 0) w = w && mbar_wait(stg, g & 1, a.budget, a.st);
-                    uint4 rc[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                                   make_uint4(0u, 0u, 0u, 0u)};
-                    uint32_t rs[2] = {0u, 0u};
-                    if (FP4 && db == 0) {
-                        // this row's raw block 0 into registers; the staging is overwritten
-                        // only after every loader warp has read its rows
-                        if (w && fp4_row) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) rc[i] = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, i));
-                            rs[0] = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32);
-                            rs[1] = *reinterpret_cast<const uint32_t*>(sStgSc + r * 32 + 4);
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(stgread);
-                        w = w && mbar_wait(stgread, g & 1, a.budget, a.st);
-                    }
+                    if (FP4 && db == 0) w = w && mbar_wait(stgread, g & 1, a.budget, a.st);
                     if (w) {
                         const int ch = 2 * db + (piece >> 3), u = piece & 7;
 #pragma unroll
@@ -813,16 +824,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                                            srcj[j] + ch * 128 + u * 16);
                         }
                         if (fp4_row) {
-                            if (db == 0) {
-                                ss8[0] = fp4_block_to_tile(rc[0], rc[1], rc[2], rc[3], rs[0], rs[1], sK, 0, r);
-                            } else {
-                                const uint4 k0 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db));
-                                const uint4 k1 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 1));
-                                const uint4 k2 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 2));
-                                const uint4 k3 = *reinterpret_cast<const uint4*>(sK + stg_code_offset(r, 4 * db + 3));
-                                const uint2 scw = *reinterpret_cast<const uint2*>(sStgSc + r * 32 + 8 * db);
-                                ss8[db] = fp4_block_to_tile(k0, k1, k2, k3, scw.x, scw.y, sK, db, r);
-                            }
+                            ss += fp4_block_to_tile(kc[4 * bi], kc[4 * bi + 1], kc[4 * bi + 2], kc[4 * bi + 3], ks[2 * bi],
+                                                    ks[2 * bi + 1], sK, db, r);
                         } else if (!bf_row) {
 #pragma unroll
                             for (int c2 = 2 * db; c2 < 2 * db + 2; ++c2)
@@ -834,61 +837,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                     }
                     cp_async_commit();
                 }
-                // each 128-dim block is complete once its copy group has landed (blocks in
-                // the order they were produced)
-                cp_async_wait<3>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[FP4 ? 1 : 0]);
-                cp_async_wait<2>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[FP4 ? 2 : 1]);
+                // each 128-dim block is complete once its copy group has landed
                 cp_async_wait<1>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[FP4 ? 3 : 2]);
+                if (lane == 0) mbar_arrive(&kfull[dbA]);
                 cp_async_wait<0>();
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kfull[FP4 ? 0 : 3]);
+                if (lane == 0) mbar_arrive(&kfull[dbB]);
                 if (!__all_sync(FULL, w)) {
                     ok = false;
                     break;
                 }
-                float rv = 0.0f;
-                if (s.kind != 0) {
-                    if (pre) {
-                        rv = rpre;
-                    } else {
-                        if (bf_row) {
-                            // not unrolled, for the same reason as the FP4 chunks
+                // squares of a bf16 row over this group's four 64-dim chunks (their copies
+                // were made by this warp); not unrolled, for the same reason as the FP4 blocks
+                if (bf_row && !pre) {
 #pragma unroll 1
-                            for (int c = 0; c < 8; ++c)
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int c = 2 * (ci < 2 ? dbA : dbB) + (ci & 1);
 #pragma unroll
-                                for (int u = 0; u < 8; ++u)
-                                    bf16x8_sumsq(*reinterpret_cast<const uint4*>(
-                                                     sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
-                                                 ss);
-                        }
-                        if (fp4_row)
-                            ss = ((ss8[0] + ss8[1]) + (ss8[2] + ss8[3])) + ((ss8[4] + ss8[5]) + (ss8[6] + ss8[7]));
-                        rv = 1.0f / sqrtf(ss / (float)TC_C + 1e-6f);
+                        for (int u = 0; u < 8; ++u)
+                            bf16x8_sumsq(*reinterpret_cast<const uint4*>(sK + c * CHUNK_K + sw128_offset((uint32_t)r, (uint32_t)u)),
+                                         ss);
                     }
                 }
+                if (hf == 1) {
+                    sSS[r] = ss;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ssrdy);
+                    continue;
+                }
+                {
+                    const bool w2 = mbar_wait(ssrdy, g & 1, a.budget, a.st);
+                    if (!__all_sync(FULL, w2)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                float rv = 0.0f;
+                if (s.kind != 0) rv = pre ? rpre : 1.0f / sqrtf((ss + sSS[r]) / (float)TC_C + 1e-6f);
                 sRinv[r] = rv;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rfull);
                 if (tt == 0 && have_pend) run_pending();
             }
-            if (it.nt > 0 && ok) {
+            if (hf == 0 && it.nt > 0 && ok) {
                 if (have_pend) run_pending();      // an item of a single tile: previous one first
                 pend = it;
                 have_pend = true;
                 ++qi;
             }
         }
-        if (have_pend && ok) run_pending();
+        if (hf == 0 && have_pend && ok) run_pending();
     }
     tc_fence_before();
     __syncthreads();
