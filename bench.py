@@ -161,8 +161,8 @@ class Workload:
 
     def side(self):
         """Work of the step that nothing later in the step reads (cache rows written for
-        the next steps): it runs on a second stream, beside the scan and the rest, and
-        the step ends only when it has finished."""
+        the next steps): it runs on a second stream once the scan is done, beside the
+        selections and the attention, and the step ends only when it has finished."""
         pass
 
     has_side = False
@@ -997,7 +997,8 @@ def run_ours(args):
     clocks.start()
 
     # the step's side work (cache rows for later steps) forks onto a second stream after
-    # the query pack and joins at the end of the step
+    # the scan (beside the selections and the attention, which leave SMs free) and joins
+    # at the end of the step
     side_stream = torch.cuda.Stream(dev) if wl.has_side else None
     g_side = None
 
@@ -1017,7 +1018,7 @@ def run_ours(args):
 
     # warm-up (also sets kernel attributes before any graph capture)
     for _ in range(max(1, args.warmup)):
-        wl.pre(); fork_side(); wl.main(); wl.post(); join_side()
+        wl.pre(); wl.main(); fork_side(); wl.post(); join_side()
     C.csa2_ctx_check()
     g_pre = g_post = None
     if not args.no_graph:
@@ -1037,7 +1038,7 @@ def run_ours(args):
         if side_stream is not None:
             g_side = g_side_new
         for _ in range(2):
-            g_pre.replay(); fork_side(); wl.main(); g_post.replay(); join_side()
+            g_pre.replay(); wl.main(); fork_side(); g_post.replay(); join_side()
     torch.cuda.synchronize()
 
     def step(ev0=None, ev1=None):
@@ -1045,12 +1046,12 @@ def run_ours(args):
             g_pre.replay()
         else:
             wl.pre()
-        fork_side()
         if ev0 is not None:
             ev0.record(stream)
         wl.main()
         if ev1 is not None:
             ev1.record(stream)
+        fork_side()
         if g_post is not None:
             g_post.replay()
         else:
@@ -1103,8 +1104,8 @@ def run_ours(args):
     def e2e_step():
         wl.e2e_copy_in()
         wl.pre()
-        fork_side()
         wl.main()
+        fork_side()
         wl.post()
         join_side()
         wl.e2e_copy_out()
