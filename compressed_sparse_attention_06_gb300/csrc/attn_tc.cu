@@ -22,17 +22,19 @@
 // Precision: the normalised query and P' are rounded to bf16 for the MMA (fp32
 // accumulation); key rows are exact.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work items):
-//   warp 0     producer: the query image of each work item (one 64 KB bulk copy)
-//   warp 1     MMA issuer; owns the tensor memory (O^T: columns 0-255, S^T: 256-319)
-//   warps 2-5  softmax: one thread per slot; then the output epilogue, one thread per
-//              output dim
-//   warps 6-9  loaders, one thread per slot: bf16 rows gathered with 16-byte cp.async
-//              straight into the swizzled tile (one commit group per 128-dim block, so
-//              the next tile streams in while the current PV finishes), FP4 rows
-//              dequantised exactly into bf16, zero rows for empty slots, and each row's
-//              RMS factor (read from a table precomputed once per call when rows are
-//              gathered many times over, as in prefill)
+// Warp roles (448 threads, one CTA per SM, persistent over work items):
+//   warp 0      producer: the query image of each work item (one 64 KB bulk copy)
+//   warp 1      MMA issuer; owns the tensor memory (O^T: columns 0-255, S^T: 256-319)
+//   warps 2-5   softmax: one thread per slot; then the output epilogue, one thread per
+//               output dim
+//   warps 6-13  loaders, two groups of four warps with one thread per slot each, group
+//               0 producing the 128-dim blocks {1, 0} ({0, 1} for bf16 tiles) and group
+//               1 the blocks {2, 3}: bf16 rows gathered with 16-byte cp.async straight
+//               into the swizzled tile (one commit group per block, so the next tile
+//               streams in while the current PV finishes), FP4 rows staged in shared
+//               memory and dequantised exactly into bf16, zero rows for empty slots,
+//               and each row's RMS factor (group 0; read from a table precomputed once
+//               per call when rows are gathered many times over, as in prefill)
 // Every wait is bounded; a wait that expires flags a timeout and the roles wind down.
 #include <algorithm>
 #include <cstring>
