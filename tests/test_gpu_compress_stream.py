@@ -87,12 +87,13 @@ def test_stream_equals_whole_sequence(dt, overlap, m):
                      f"entries b{b}")
 
 
-@pytest.mark.parametrize("fmt,c", [("fp4", 512), ("mxfp4", 128)])
-def test_stream_packed_cache_rows(fmt, c):
+@pytest.mark.parametrize("fmt,c,m", [("fp4", 512, 4), ("mxfp4", 128, 4), ("mxfp4", 128, 128)])
+def test_stream_packed_cache_rows(fmt, c, m):
     """FP4 main-KV rows (c = 512) and MXFP4 indexer-key rows (c = 128) written straight
     into a cache: identical bytes to the whole-sequence kernel, and within the
-    format's rounding of the oracle's entries."""
-    B, m = 2, 4
+    format's rounding of the oracle's entries (m = 128 with c = 128: sixteen row
+    groups per entry)."""
+    B = 2
     n = 6 * m
     ca, za, cb, zb = _rows(B, n, c, 411, torch.bfloat16, True)
     ba, bb = _bias(m, c, 412, 1), _bias(m, c, 412, 2)
