@@ -261,6 +261,16 @@ class FP4Decode(Workload):
             v.copy_(t)
             setattr(self, n, v)
         self.e2e_in = [self.in_buf]
+        # the step's results (attention output, selected indices) likewise share one
+        # buffer, read back with one copy
+        b = self.buf
+        ob = b.out.numel() * b.out.element_size()
+        ob_pad = (ob + 255) // 256 * 256
+        self.out_buf = torch.empty(ob_pad + b.idx.numel() * b.idx.element_size(), dtype=torch.uint8,
+                                   device=b.out.device)
+        b.out = self.out_buf[:ob].view(b.out.dtype).view(b.out.shape)
+        b.idx = self.out_buf[ob_pad:].view(b.idx.dtype).view(b.idx.shape)
+        self.e2e_out = [self.out_buf]
         torch.cuda.synchronize()
         h2d, d2h = super().e2e_inputs()
         self.h_swa = self.swa_row.detach().cpu().pin_memory()
