@@ -37,6 +37,7 @@ import torch  # noqa: E402
 
 METRIC = "decode queries/s & indexer entries/s at 1M ctx; % of HBM roofline (1 GB300)"
 UNIT = "queries/s"
+FP4_PER_BF16 = 13.5 / 2.25      # nominal dense tensor rates per GPU, FP4 over bf16
 
 
 # ----------------------------------------------------------------------------- utils
@@ -198,6 +199,8 @@ class FP4Decode(Workload):
     main_name = "csa2_index_score (FP4 QK full scan over MXFP4 keys, fused block max)"
     profile = "index_score_fp4_decode_1M.txt"
     kernel_files = ("index_scan_fp4.cu", "index_score.cu", "index_score_tc.cuh", "sm100_ptx.cuh", "csa2_internal.cuh")
+    dtype = ("indexer QK MXFP4 x MXFP4 (tcgen05 kind::mxf4, E8M0 block scales, fp32 accumulate); "
+             "attention bf16 MMA over FP4 E2M1+E4M3 rows, fp32 accumulate")
 
     H, K = 64, 512                            # query heads, top-k
 
@@ -302,6 +305,15 @@ class FP4Decode(Workload):
         _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, want_scores=False,
                               want_block_max=True, block_max=self.buf.block_max)
 
+    def scan_bf16_query(self):
+        """The other reading of the pages: the bf16 indexer query over the same MXFP4
+        keys (keys dequantised exactly to f16 in tensor memory, f16 MMA).  Timed as a
+        stage for comparison; the step runs the FP4 QK path."""
+        if not hasattr(self, "bmax_bf16q"):
+            self.bmax_bf16q = torch.empty_like(self.buf.block_max)
+        _C().csa2_index_score(self.qI, self.w, self.ki, self.nv, block=self.block, want_scores=False,
+                              want_block_max=True, block_max=self.bmax_bf16q)
+
     def pool(self):
         b = self.buf
         _C().csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
@@ -346,9 +358,11 @@ class FP4Decode(Workload):
         attn_bytes = B * (self.k * 288 + self.window * 1024 + H * 512 * 2 * 2)
         attn_flops = B * H * (self.k + self.window) * 512 * 4
         return [("write new rows", self.write, B * (2 * 1024 + 256 + 288 + 68 + self.H_I * (256 + 68)), 0),
-                ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
+                ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128, "fp4"),
+                ("index scan (bf16 q)", self.scan_bf16_query, B * self.V * 68 + B * self.H_I * (256 + 4),
+                 2 * B * self.V * 64 * 128, "bf16"),
                 ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
-                ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128),
+                ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128, "fp4"),
                 (f"top-{self.k}", self.topk, B * self.n_keep * 8 * 4, 0),
                 ("sparse attention", self.attn, attn_bytes, attn_flops)]
 
@@ -971,6 +985,10 @@ def _make(args, seq0=0):
     kw = {"seq0": seq0}
     if args.n_ctx:
         kw["N"] = args.n_ctx
+    if args.n_new:
+        if args.workload != "prefill_chunk_bf16":
+            raise SystemExit("--n-new applies to prefill_chunk_bf16 only")
+        kw["n_new"] = args.n_new
     return WORKLOADS[args.workload](**kw)
 
 
@@ -982,7 +1000,9 @@ def _time_stages(wl, stream, reps):
     GPU time, not host launch overhead."""
     hbm, bf16, _, _ = _peaks()
     out = {}
-    for name, fn, nbytes, flops in wl.stages():
+    for st in wl.stages():
+        name, fn, nbytes, flops = st[:4]
+        kind = st[4] if len(st) > 4 else "bf16"
         fn()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda.synchronize()
@@ -996,7 +1016,11 @@ def _time_stages(wl, stream, reps):
         d = {"ms": ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm}
         if flops:
             d["TFLOP_per_s"] = flops / (ms * 1e-3) / 1e12
-            d["tensor_frac"] = d["TFLOP_per_s"] / bf16
+            # a kind::mxf4 MMA runs at the FP4 rate: the measured bf16 peak times the
+            # nominal dense FP4 / bf16 ratio (13.5 / 2.25 PFLOP/s)
+            peak = bf16 * FP4_PER_BF16 if kind == "fp4" else bf16
+            d["tensor_frac"] = d["TFLOP_per_s"] / peak
+            d["tensor_peak"] = {"TFLOP_per_s": peak, "dtype": kind}
         out[name] = d
     return out
 
@@ -1244,6 +1268,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-queries", type=int, default=3)
     ap.add_argument("--n-ctx", type=int, default=None, help="override the context length (quick checks only)")
+    ap.add_argument("--n-new", type=int, default=None,
+                    help="prefill_chunk_bf16: queries of the chunk (default 8192; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -429,6 +429,13 @@ def csa2_sparse_attn_noalloc(q, kv, idx, swa, q_pos, out: torch.Tensor, sink=Non
     memory: the library keeps the partial results in its own fixed device array.
     The caller passes every tensor, outputs included; nothing is allocated here."""
     B, Q, H, c = q.shape
+    # the kernels write B*Q*H rows of c values (and B*Q*H lse values): a smaller
+    # buffer would be overrun, so its shape, dtype and device are checked first
+    if tuple(out.shape) != (B, Q, H, c) or out.device != q.device or out.dtype not in (torch.float32,
+                                                                                      torch.bfloat16):
+        raise ValueError(f"out must be a float32/bfloat16 tensor of shape {(B, Q, H, c)} on {q.device}")
+    if lse is not None and (tuple(lse.shape) != (B, Q, H) or lse.dtype != torch.float32 or lse.device != q.device):
+        raise ValueError(f"lse must be None or a float32 tensor of shape {(B, Q, H)} on {q.device}")
     k = idx.shape[-1] if idx is not None else 0
     N = kv.shape[1] if kv is not None else 0
     kv_dt = (FP4_E4M3x16 if kv_fmt is None else kv_fmt) if kv is not None and kv.dtype == torch.uint8 else \

@@ -13,36 +13,31 @@
 // GPU that loads the library holds it until the process exits.  All calls share
 // it, so calls whose kernels overlap on the GPU race on it.  Nothing in it has to
 // start at zero: every call rewrites each partial result it later reads.
-#include <mutex>
-
 #include "attn_tc.cuh"
 #include "csa2_internal.cuh"
 
 namespace {
 
-constexpr int MAX_DEVICES = 64;
-
 static __device__ __align__(256) unsigned char g_attn_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_attn_scratch on `device`.  In host code the array's name is
-// only a host-side stand-in, so the address is looked up once per device, with
-// that device current.
-csa2_status scratch_address(int device, void** out) {
-    static std::mutex mu;
-    static void* addr[MAX_DEVICES] = {nullptr};
-    if (device < 0 || device >= MAX_DEVICES) return CSA2_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[device]) {
+// Device address of g_attn_scratch on the context's device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with that
+// device current, once per context (the set-up of the first call), and kept in the
+// context: it lives exactly as long as the context.  A device reset unloads the
+// module and may move the array; the context (whose status word the reset frees as
+// well) must then be destroyed and created again.
+csa2_status scratch_address(csa2_ctx* ctx, void** out) {
+    if (!ctx->noalloc_scratch) {
         int prev = 0;
         if (cudaGetDevice(&prev) != cudaSuccess) return CSA2_ERR_CUDA;
-        if (prev != device && cudaSetDevice(device) != cudaSuccess) return CSA2_ERR_CUDA;
+        if (prev != ctx->device && cudaSetDevice(ctx->device) != cudaSuccess) return CSA2_ERR_CUDA;
         void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
-        if (prev != device) cudaSetDevice(prev);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (prev != ctx->device && cudaSetDevice(prev) != cudaSuccess) return CSA2_ERR_CUDA;
         if (e != cudaSuccess || !p) return CSA2_ERR_CUDA;
-        addr[device] = p;
+        ctx->noalloc_scratch = p;
     }
-    *out = addr[device];
+    *out = ctx->noalloc_scratch;
     return CSA2_OK;
 }
 
@@ -61,7 +56,7 @@ extern "C" csa2_status csa2_sparse_attn_noalloc(csa2_ctx* ctx, const void* q, cs
     const size_t need = attn_simt_ws_bytes(ctx, B, Q, H, k, window);
     if (need > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_INVALID_ARG;
     void* scratch = nullptr;
-    csa2_status st = scratch_address(ctx->device, &scratch);
+    csa2_status st = scratch_address(ctx, &scratch);
     if (st != CSA2_OK) return st;
     return csa2_sparse_attn(ctx, q, q_dt, kv, kv_dt, N, idx, k, swa, swa_dt, swa_cap, swa_pos0, window, q_pos, sink,
                             B, Q, H, c, rope_base, flags, out, out_dt, lse, scratch,

@@ -34,6 +34,7 @@ extern "C" csa2_status csa2_ctx_create(int device, csa2_ctx** out) {
     c->stall_next = 0;
     c->stall_budget = 0;
     c->cluster16 = -1;
+    c->noalloc_scratch = nullptr;
     cudaError_t e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = cudaMalloc(&c->status, sizeof(unsigned int));
     if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(unsigned int));

@@ -16,6 +16,8 @@ struct csa2_ctx {
     int stall_next;         // test hook: next tensor-core scan runs with a silent producer
     long long stall_budget; // wait budget (cycles) for that launch
     int cluster16;          // 16-CTA clusters of the selection kernel fit: -1 unknown, 0 no, 1 yes
+    void* noalloc_scratch;  // device address of the allocation-free entry point's array (looked up
+                            // on its first call with this context; NULL until then)
 };
 
 #define CSA2_DEVBIT_RANGE 1u

@@ -21,10 +21,10 @@
 //   warp 0       producer, into an 8-stage ring of tiles.  Full scan: a tile is
 //                17408 contiguous bytes, one bulk copy; four lanes issue them, lane p
 //                owning stages p and p+4 (one issuing thread alone sustains well under
-//                the HBM read rate).  Candidates: a tile is 32 blocks of 544 bytes,
-//                gathered by all 32 lanes with 16-byte cp.async (544-byte bulk copies
-//                run at a small fraction of the HBM rate), completion arriving on the
-//                stage barrier.
+//                the HBM read rate).  Candidates: a tile is 32 blocks of 544 bytes;
+//                each of the 32 lanes issues one 544-byte bulk copy with its own
+//                expect-tx arrival on the stage barrier (an empty pool slot only
+//                arrives).
 //   warp 1       MMA issuer (one lane): 4 MMAs and one commit per tile; owns the
 //                tensor-memory allocation
 //   warps 2-9    two copy groups (alternate tiles): each thread stores the 16 code

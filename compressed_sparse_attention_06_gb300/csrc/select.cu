@@ -2,9 +2,10 @@
 //
 // Top-k (DSA-to-CSA/HCA page eq. (17)) and the pool (CSA2 page,
 // «解码器里的分层索引»; Attention-evolution page §4.4) share one exact radix select:
-// every score becomes an order-preserving uint32 key, four 8-bit histogram passes
-// find the k-th largest key T, and one ordered pass emits the keys above T plus the
-// first (lowest-index) keys equal to T.  The result is the top-k in the order
+// every score becomes an order-preserving uint32 key, a 12-bit histogram and two
+// 10-bit histograms (the last two over the keys of the threshold bin only) find the
+// k-th largest key T, and one ordered pass emits the keys above T plus the first
+// (lowest-index) keys equal to T.  The result is the top-k in the order
 // (score desc, index asc), independent of thread timing.
 //
 // Layouts:

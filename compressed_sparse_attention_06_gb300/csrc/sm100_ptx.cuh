@@ -86,17 +86,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
-// Four rows of a 2-D tensor (box of one row) gathered into consecutive rows of
-// shared memory: rows y0..y3, columns [x, x + box width).
-__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
-                                            int32_t y2, int32_t y3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -115,6 +115,28 @@ def distinct_sample(population: int, k: int, seed: int, stream: int, device="cpu
     return torch.sort(sel).values
 
 
+def snap(x: torch.Tensor, step: float, lim: float) -> torch.Tensor:
+    """Round values to the nearest multiple of `step` and clip them to [-lim, lim]:
+    the exact-grid variant of a workload (every product and partial sum of the
+    indexer is then exact in fp32, so scores and selections must match bit for bit)."""
+    return torch.clamp(torch.round(x.double() / step) * step, -lim, lim)
+
+
+# Exact-grid FP4 rows: values from this signed set, with the first value of every
+# 32-value block set to 4, so each block's largest magnitude is 4 and its MXFP4
+# scale is 2^0: every value is then stored exactly.
+_FP4_GRID = (-4.0, -3.0, -2.0, -1.5, -1.0, -0.5, 0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0)
+
+
+def fp4_grid_rows(seed: int, stream: int, row0: int, rows: int, width: int, device="cpu") -> torch.Tensor:
+    """[rows, width] f32 rows of the exact-grid FP4 workload (rows row0 .. of a stream)."""
+    u = uniform(rows * width, seed, stream, device, offset=row0 * width)
+    vals = torch.tensor(_FP4_GRID, dtype=torch.float64, device=device)
+    x = vals[torch.clamp((u * len(_FP4_GRID)).long(), max=len(_FP4_GRID) - 1)].view(rows, width // 32, 32)
+    x[:, :, 0] = 4.0
+    return x.reshape(rows, width).to(torch.float32)
+
+
 # ----------------------------------------------------------------------------------
 # The five workloads.  Shapes, dtypes and distributions are those of the workload
 # descriptions; `scale` knobs shrink a workload for the fast tests while keeping
@@ -192,10 +214,14 @@ PLANT_BETA = math.ceil(12.0 * math.sqrt(D_INDEX) * 4.0) / 4.0
 N_PLANTED = 16
 
 
-def decode_full_bf16(device="cpu", B: int = 32, N: int = 65536, with_main_kv: bool = True) -> Workload:
+def decode_full_bf16(device="cpu", B: int = 32, N: int = 65536, with_main_kv: bool = True,
+                     grid: bool = False) -> Workload:
     """Decoder Full-mode decode, bf16: B sequences, N entries (m=1), query at
     t = N-1 (V = N-1), 64 indexer heads, 64 core heads, 16 planted keys per
-    sequence at seeded positions in [0, V-129), 128-token window ring, sink 0."""
+    sequence at seeded positions in [0, V-129), 128-token window ring, sink 0.
+
+    grid=True: the exact-grid variant -- q^I and K^I on multiples of 2^-3 in
+    [-4, 4], w on multiples of 2^-1 in [-4, 4], no planted keys (they are off grid)."""
     wid = 2
     m, H_I, H, Q = 1, 64, 64, 1
     t = {}
@@ -204,6 +230,10 @@ def decode_full_bf16(device="cpu", B: int = 32, N: int = 65536, with_main_kv: bo
     KI = normal_tensor((B, N, D_INDEX), _wid_seed(wid, 2), 0, torch.bfloat16, device)
     t["qI"] = normal_tensor((B, Q, H_I, D_INDEX), _wid_seed(wid, 3), 0, torch.bfloat16, device)
     t["w"] = normal_tensor((B, Q, H_I), _wid_seed(wid, 4), 0, torch.float32, device)
+    if grid:
+        KI = snap(KI, 0.125, 4.0).to(torch.bfloat16)
+        t["qI"] = snap(t["qI"], 0.125, 4.0).to(torch.bfloat16)
+        t["w"] = snap(t["w"], 0.5, 4.0).to(torch.float32)
     t["q"] = normal_tensor((B, Q, H, C_MAIN), _wid_seed(wid, 5), 0, torch.bfloat16, device)
     t["swa"] = normal_tensor((B, WINDOW, C_MAIN), _wid_seed(wid, 6), 0, torch.bfloat16, device)
     t["sink"] = torch.zeros(H, dtype=torch.float32, device=device)
@@ -211,26 +241,30 @@ def decode_full_bf16(device="cpu", B: int = 32, N: int = 65536, with_main_kv: bo
     span = max(V - 129, 1)
     planted = torch.empty((B, N_PLANTED), dtype=torch.int64, device=device)
     u_dir = plant_direction(t["qI"][:, 0], t["w"][:, 0])            # [B, 128]
-    for b in range(B):
+    for b in range(0 if grid else B):
         pos = distinct_sample(span, min(N_PLANTED, span), _wid_seed(wid, 7) + 17 * b, b, device)
         planted[b, :pos.numel()] = pos
         KI[b, pos] = (PLANT_BETA * u_dir[b]).to(torch.bfloat16).unsqueeze(0).expand(pos.numel(), -1)
     t["KI"] = KI
-    t["planted"] = planted
+    if not grid:
+        t["planted"] = planted
     # the new token's compressor inputs (m = 1: one row) and its indexer key row
     t["C_new"] = normal_tensor((B, 1, C_MAIN), _wid_seed(wid, 8), 0, torch.bfloat16, device)
     t["Z_new"] = normal_tensor((B, 1, C_MAIN), _wid_seed(wid, 9), 0, torch.bfloat16, device)
     t["KI_new"] = normal_tensor((B, 1, D_INDEX), _wid_seed(wid, 10), 0, torch.bfloat16, device)
     q_pos = torch.full((B, Q), N - 1, dtype=torch.int64, device=device)
-    return Workload("decode_full_bf16", B, Q, N, m, H_I, H, q_pos, t,
+    return Workload("decode_full_bf16" + ("_grid" if grid else ""), B, Q, N, m, H_I, H, q_pos, t,
                     dict(swa_pos0=0, swa_cap=WINDOW, dtype="bf16"))
 
 
 def reindex_reuse_bf16(device="cpu", B: int = 64, N: int = 262144, n_reuse: int = 3,
-                       with_main_kv: bool = True) -> Workload:
+                       with_main_kv: bool = True, grid: bool = False) -> Workload:
     """Reindex + Reuse decode, bf16: each query rescores its 2048 pooled blocks
     (16,384 candidates) with its own indexer q/w, takes top-512, then the Reindex
-    layer and three Reuse layers each attend with their own q and window."""
+    layer and three Reuse layers each attend with their own q and window.
+
+    grid=True: the exact-grid variant (q^I, K^I on multiples of 2^-3 in [-4, 4],
+    w on multiples of 2^-1 in [-4, 4])."""
     wid = 3
     m, H_I, H, Q = 1, 64, 64, 1
     t = {}
@@ -239,6 +273,10 @@ def reindex_reuse_bf16(device="cpu", B: int = 64, N: int = 262144, n_reuse: int 
     t["KI"] = normal_tensor((B, N, D_INDEX), _wid_seed(wid, 2), 0, torch.bfloat16, device)
     t["qI"] = normal_tensor((B, Q, H_I, D_INDEX), _wid_seed(wid, 3), 0, torch.bfloat16, device)
     t["w"] = normal_tensor((B, Q, H_I), _wid_seed(wid, 4), 0, torch.float32, device)
+    if grid:
+        for nm in ("KI", "qI"):
+            t[nm] = snap(t[nm], 0.125, 4.0).to(torch.bfloat16)
+        t["w"] = snap(t["w"], 0.5, 4.0).to(torch.float32)
     V = N - 1
     b_new = (V - 1) // POOL_BLOCK
     n_keep = min(POOL_KEEP, b_new + 1)
@@ -255,7 +293,7 @@ def reindex_reuse_bf16(device="cpu", B: int = 64, N: int = 262144, n_reuse: int 
                                          torch.bfloat16, device)
     t["sink"] = torch.zeros(H, dtype=torch.float32, device=device)
     q_pos = torch.full((B, Q), N - 1, dtype=torch.int64, device=device)
-    return Workload("reindex_reuse_bf16", B, Q, N, m, H_I, H, q_pos, t,
+    return Workload("reindex_reuse_bf16" + ("_grid" if grid else ""), B, Q, N, m, H_I, H, q_pos, t,
                     dict(swa_pos0=0, swa_cap=WINDOW, n_layers=1 + n_reuse, dtype="bf16"))
 
 
@@ -272,16 +310,24 @@ def fp4_rows(kind: str, b: int, row0: int, rows: int, N: int, device="cpu") -> t
     return (x.view(rows, width) * r.view(rows, 1)).to(torch.float32)
 
 
-def fp4_decode(device="cpu", B: int = 8, N: int = 1 << 20, H: int = 64) -> Workload:
+def fp4_decode(device="cpu", B: int = 8, N: int = 1 << 20, H: int = 64, grid: bool = False) -> Workload:
     """FP4-cache long-context decode: B sequences of N entries (m=1); query at
     t = N-1.  The main-KV and indexer-K caches are drawn with `fp4_rows` and
     packed by the caller (FP4 E2M1+E4M3/16 and MXFP4 respectively).  H query heads
-    (64; 128 for the V4-Pro configuration)."""
+    (64; 128 for the V4-Pro configuration).
+
+    grid=True: the exact-grid variant -- the indexer query from `fp4_grid_rows`
+    (stored exactly by MXFP4), w on multiples of 2^-1 in [-4, 4]; the caller
+    draws the indexer keys with `fp4_grid_rows` too."""
     wid = 4
     m, H_I, Q = 1, 64, 1
     t = {}
     t["qI"] = normal_tensor((B, Q, H_I, D_INDEX), _wid_seed(wid, 5), 0, torch.bfloat16, device)
     t["w"] = normal_tensor((B, Q, H_I), _wid_seed(wid, 6), 0, torch.float32, device)
+    if grid:
+        t["qI"] = fp4_grid_rows(_wid_seed(wid, 12), 0, 0, B * Q * H_I, D_INDEX, device).to(
+            torch.bfloat16).view(B, Q, H_I, D_INDEX)
+        t["w"] = snap(t["w"], 0.5, 4.0).to(torch.float32)
     t["q"] = normal_tensor((B, Q, H, C_MAIN), _wid_seed(wid, 7), 0, torch.bfloat16, device)
     t["swa"] = normal_tensor((B, WINDOW, C_MAIN), _wid_seed(wid, 8), 0, torch.bfloat16, device)
     t["sink"] = torch.zeros(H, dtype=torch.float32, device=device)

@@ -362,16 +362,20 @@ csa2_status csa2_dense_attn(csa2_ctx* ctx,
  * workspace and keeps the partial results in a device array compiled into the
  * library, CSA2_NOALLOC_SCRATCH_BYTES large; every GPU that loads the library holds
  * that array until the process exits.  It calls no allocator.
- *   - The first call on a device looks up the array's device address (a one-time
- *     set-up that allocates nothing); make that first call before any stream
- *     capture.
+ *   - The first call with a context looks up the array's device address on the
+ *     context's device (a one-time set-up that allocates nothing) and keeps it in
+ *     the context; make that first call before any stream capture.  After a device
+ *     reset the context must be created again (the array may have moved).
  *   - All calls share the array: calls whose kernels overlap on the GPU race.
  *     Nothing in it needs to start at zero (each call rewrites what it reads).
- *   - A call whose CUDA-core key split would need more than
+ *   - The tensor-core path is taken when its workspace fits the array, so results
+ *     equal csa2_sparse_attn's with a full workspace whenever that workspace is at
+ *     most CSA2_NOALLOC_SCRATCH_BYTES.  Otherwise the CUDA-core path runs with its
+ *     key split in the array; that split needs fewer than
+ *     2 * (4 * SMs) * 8 * 516 * 4 bytes (20,078,592 on a 152-SM part), so it always
+ *     fits there.  On a part with more SMs, a call whose split would need more than
  *     CSA2_NOALLOC_SCRATCH_BYTES is rejected with CSA2_ERR_INVALID_ARG before
- *     anything is launched.  The tensor-core path is taken when its workspace fits
- *     the array, so results equal csa2_sparse_attn's with a full workspace whenever
- *     that workspace is at most CSA2_NOALLOC_SCRATCH_BYTES.
+ *     anything is launched.
  */
 #define CSA2_NOALLOC_SCRATCH_BYTES (24u << 20)
 csa2_status csa2_sparse_attn_noalloc(csa2_ctx* ctx,

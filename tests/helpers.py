@@ -1,4 +1,5 @@
 """Comparison helpers shared by the GPU parity tests."""
+import math
 import numpy as np
 import torch
 
@@ -62,3 +63,59 @@ def pool_swaps(gpu_pool, oracle_bmax, V, block, n_keep, rel_eps=1e-5):
     for b in set(gpu) ^ set(ref):
         assert abs(bm[b] - kth) <= eps, f"block {b}: {bm[b]} vs {kth}"
     return len(set(gpu) ^ set(ref)) // 2
+
+
+def valid_topk_sets(scores, cand, k, rms, rel_eps=1e-5, limit=64):
+    """Every index set that the tie-window rule accepts as a top-k of the
+    candidate ids `cand` under the oracle's scores: all candidates scoring above
+    the window around the oracle's k-th score, plus any choice of the remaining
+    count among the window's members (|score - kth| <= rel_eps * rms).  Each set
+    is ascending and -1 padded to k.  These are the results that are equally
+    correct; the list is built from the oracle's scores alone.  Returns None when
+    the window allows more than `limit` sets."""
+    import itertools
+    cand = np.asarray(cand, dtype=np.int64)
+    s = np.asarray(scores, dtype=np.float64)[cand]
+    n = min(k, cand.shape[0])
+    out_pad = np.full(k, -1, dtype=np.int64)
+    if n == 0:
+        return [out_pad]
+    kth = np.sort(s)[::-1][n - 1]
+    eps = rel_eps * rms
+    above = cand[s > kth + eps]
+    window = cand[np.abs(s - kth) <= eps]
+    need = n - above.shape[0]
+    if math.comb(window.shape[0], need) > limit:
+        return None
+    sets = []
+    for comb in itertools.combinations(window.tolist(), need):
+        sel = np.sort(np.concatenate([above, np.asarray(comb, dtype=np.int64)]))
+        o = out_pad.copy()
+        o[:n] = sel
+        sets.append(o)
+    return sets
+
+
+def check_step_attention(gpu_out, gpu_idx, sets, oracle_attn, tol, what):
+    """Check the attention a whole step produced (gpu_out, computed on the step's
+    own selection gpu_idx) against the oracle.  `sets` are the equally correct
+    selections the oracle enumerates (valid_topk_sets); the step's selection must
+    be one of them (topk_swaps has checked that), and its output must match the
+    oracle's attention over that set: oracle_attn(set) -> [H, c]."""
+    gpu_idx = np.asarray(gpu_idx, dtype=np.int64)
+    assert sets is not None, f"{what}: tie window too wide to enumerate the valid selections"
+    match = [s for s in sets if np.array_equal(s, gpu_idx)]
+    assert match, f"{what}: the step's selection is none of the oracle's valid selections"
+    assert_close(gpu_out, oracle_attn(match[0]), tol, what)
+    return len(sets)
+
+
+def assert_exact_grid_scores(qI, w, KI, V, p):
+    """Exact-grid precondition: every term w_h q_hd K_sd is a multiple of 2^-p and
+    the magnitudes of one score's terms total less than 2^(24-p), so every partial
+    sum is exact in fp32 in any order (and so equal to the f64 result)."""
+    qI = np.asarray(qI, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    K = np.asarray(KI, dtype=np.float64)[:V]
+    tot = np.abs(K) @ np.abs(qI).T @ np.abs(w)                 # [V]
+    assert tot.max() < 2.0 ** (24 - p), f"term sums up to {tot.max()} exceed 2^{24 - p}"

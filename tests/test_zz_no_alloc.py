@@ -1,25 +1,30 @@
-"""The allocation-free attention entry point (for callers that may not allocate
-device memory, so cannot pass a workspace) must give the same result as the
-regular entry point with a full workspace.  Decode-sized shapes are used so the
-keys really are split and the library's fixed device array is used; two calls in
-a row with different inputs check that a call does not depend on what the
-previous one left in that array.  This file is collected last on purpose."""
-import numpy as np
+"""The allocation-free attention entry point must give the same result as the
+regular entry point with a full workspace.
+
+Some callers cannot allocate device memory (a serving engine that owns one arena
+for the whole GPU and forbids cudaMalloc in plugins, or a latency-critical loop),
+so they cannot pass a workspace; csa2_sparse_attn_noalloc keeps its partial
+results in a fixed array inside the library instead.  Decode-sized shapes are used
+so the keys really are split and that array is used; two calls in a row with
+different inputs check that a call does not depend on what the previous one left
+in the array.  Both kernel paths are covered: the tensor-core path (bf16 query,
+FP4 rows, both norms) and the CUDA-core path (fp32 query), each bit for bit
+against the regular entry point, since both calls run the same kernels with the
+same key split.  This file is collected last on purpose."""
 import pytest
 import torch
 
 from compressed_sparse_attention_06_gb300 import csa2 as C
 from compressed_sparse_attention_06_gb300 import workloads as W
-from tests.helpers import assert_close, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _inputs(seed, B=8, N=20000, H=64):
-    q = W.normal_tensor((B, 1, H, 512), seed, 1, torch.bfloat16, DEV)
+def _inputs(seed, q_dtype, B=8, N=20000, H=64):
+    q = W.normal_tensor((B, 1, H, 512), seed, 1, q_dtype, DEV)
     kv = C.csa2_fp4_pack(W.normal_tensor((B, N, 512), seed, 2, torch.float32, DEV))
-    swa = W.normal_tensor((B, 128, 512), seed, 3, torch.bfloat16, DEV)
+    swa = W.normal_tensor((B, 128, 512), seed, 3, q_dtype, DEV)
     idx = torch.stack([W.distinct_sample(N - 1, 512, seed, b, DEV) for b in range(B)]).to(torch.int32)
     idx = idx.view(B, 1, 512).contiguous()
     q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=DEV)
@@ -27,18 +32,33 @@ def _inputs(seed, B=8, N=20000, H=64):
     return q, kv, idx, swa, q_pos, sink
 
 
-def test_noalloc_matches_regular_entry_point_twice():
+@pytest.mark.parametrize("q_dtype", [torch.bfloat16, torch.float32], ids=["tensor_core", "cuda_core"])
+def test_noalloc_matches_regular_entry_point_twice(q_dtype):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     C.load()
     B, H = 8, 64
     assert C.csa2_sparse_attn_workspace_bytes(B, 1, H, 512, 128) > 0      # the key split is in use
     for seed in (9101, 9102):
-        q, kv, idx, swa, q_pos, sink = _inputs(seed)
+        q, kv, idx, swa, q_pos, sink = _inputs(seed, q_dtype)
         ref, ref_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, out_dtype=torch.float32, want_lse=True)
-        out = torch.empty((B, 1, H, 512), dtype=torch.float32, device=DEV)
-        lse = torch.empty((B, 1, H), dtype=torch.float32, device=DEV)
+        out = torch.full((B, 1, H, 512), float("nan"), dtype=torch.float32, device=DEV)
+        lse = torch.full((B, 1, H), float("nan"), dtype=torch.float32, device=DEV)
         C.csa2_sparse_attn_noalloc(q, kv, idx, swa, q_pos, out, sink, lse=lse)
         C.csa2_ctx_check()
-        assert_close(to_np(out), to_np(ref), 2e-2, f"noalloc output, call {seed}")
-        assert_close(to_np(lse), to_np(ref_lse), 1e-5, f"noalloc lse, call {seed}")
+        assert torch.equal(out, ref), f"noalloc output differs from csa2_sparse_attn, call {seed}"
+        assert torch.equal(lse, ref_lse), f"noalloc lse differs from csa2_sparse_attn, call {seed}"
+
+
+def test_noalloc_rejects_wrong_output_buffer():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    C.load()
+    q, kv, idx, swa, q_pos, sink = _inputs(9103, torch.bfloat16, B=2, N=4096)
+    small = torch.empty((2, 1, 32, 512), dtype=torch.float32, device=DEV)
+    with pytest.raises(ValueError):
+        C.csa2_sparse_attn_noalloc(q, kv, idx, swa, q_pos, small, sink)
+    out = torch.empty((2, 1, 64, 512), dtype=torch.float32, device=DEV)
+    with pytest.raises(ValueError):
+        C.csa2_sparse_attn_noalloc(q, kv, idx, swa, q_pos, out, sink,
+                                   lse=torch.empty((2, 1, 64), dtype=torch.bfloat16, device=DEV))
