@@ -208,6 +208,7 @@ class FP4Decode(Workload):
         self.B, self.N, self.seq0 = B, N, seq0
         self.H_I, self.window, self.block, self.n_keep = 64, 128, 8, 2048
         self.k = self.K
+        self.n_top = (self.k + 31) // 32 * 32     # blocks rescored for the top-k
         self.t = N - 1                        # query position; m = 1 so V = t entries are visible
         self.V = self.t
 
@@ -303,7 +304,7 @@ class FP4Decode(Workload):
 
     def main(self):
         _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, want_scores=False,
-                              want_block_max=True, block_max=self.buf.block_max)
+                              want_block_max=True, block_max=self.buf.block_max, block_hist=self.buf.block_hist)
 
     def scan_bf16_query(self):
         """The other reading of the pages: the bf16 indexer query over the same MXFP4
@@ -316,16 +317,18 @@ class FP4Decode(Workload):
 
     def pool(self):
         b = self.buf
-        _C().csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
+        _C().csa2_block_pool(b.block_max, self.nv, block=self.block, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws,
+                             block_hist=b.block_hist, n_top=b.top_blocks.shape[-1], out_top=b.top_blocks)
 
     def cand(self):
         b = self.buf
-        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, pool=b.pool, block=self.block,
+        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, pool=b.top_blocks, block=self.block,
                               scores=b.cand_scores)
 
     def topk(self):
         b = self.buf
-        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, block=self.block, out_idx=b.idx, ws=b.topk_ws)
+        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.top_blocks, block=self.block, out_idx=b.idx,
+                       ws=b.topk_ws)
 
     def attn(self):
         b = self.buf
@@ -362,8 +365,8 @@ class FP4Decode(Workload):
                 ("index scan (bf16 q)", self.scan_bf16_query, B * self.V * 68 + B * self.H_I * (256 + 4),
                  2 * B * self.V * 64 * 128, "bf16"),
                 ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
-                ("candidate scan", self.cand, B * self.n_keep * 8 * 68, 2 * B * self.n_keep * 8 * 64 * 128, "fp4"),
-                (f"top-{self.k}", self.topk, B * self.n_keep * 8 * 4, 0),
+                ("candidate scan", self.cand, B * self.n_top * 8 * 68, 2 * B * self.n_top * 8 * 64 * 128, "fp4"),
+                (f"top-{self.k}", self.topk, B * self.n_top * 8 * 4, 0),
                 ("sparse attention", self.attn, attn_bytes, attn_flops)]
 
     def queries(self):
@@ -460,19 +463,20 @@ class DecodeBF16(Workload):
 
     def main(self):
         _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, want_scores=False, want_block_max=True,
-                              block_max=self.buf.block_max)
+                              block_max=self.buf.block_max, block_hist=self.buf.block_hist)
 
     def pool(self):
         b = self.buf
-        _C().csa2_block_pool(b.block_max, self.nv, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws)
+        _C().csa2_block_pool(b.block_max, self.nv, n_keep=self.n_keep, out=b.pool, ws=b.pool_ws,
+                             block_hist=b.block_hist, n_top=b.top_blocks.shape[-1], out_top=b.top_blocks)
 
     def cand(self):
         b = self.buf
-        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, pool=b.pool, scores=b.cand_scores)
+        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, pool=b.top_blocks, scores=b.cand_scores)
 
     def topk(self):
         b = self.buf
-        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.pool, out_idx=b.idx, ws=b.topk_ws)
+        _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.top_blocks, out_idx=b.idx, ws=b.topk_ws)
 
     def attn(self):
         b = self.buf
@@ -495,8 +499,8 @@ class DecodeBF16(Workload):
         return [("write new row", self.write, B * 3 * 1024, 0),
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
                 ("block pool", self.pool, B * (self.V // 8) * 4, 0),
-                ("candidate scan", self.cand, B * 16384 * 256, 2 * B * 16384 * 64 * 128),
-                ("top-512", self.topk, B * 16384 * 4, 0),
+                ("candidate scan", self.cand, B * 4096 * 256, 2 * B * 4096 * 64 * 128),
+                ("top-512", self.topk, B * 4096 * 4, 0),
                 ("sparse attention", self.attn, B * (640 * 1024 + H * 512 * 4), B * H * 640 * 512 * 4)]
 
     def queries(self):

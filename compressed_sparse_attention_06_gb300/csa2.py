@@ -21,6 +21,7 @@ F32, BF16, FP4_E4M3x16, MXFP4_E8M0x32 = range(4)
 QNORM, KVNORM, ROPE = 1, 2, 4
 ATTN_DEFAULT = QNORM | KVNORM | ROPE
 W_NORM, W_ROPE = 1, 2
+BLOCK_HIST_BINS = 4096          # words per row of csa2_index_score's block histogram
 
 # symbols declared in include/csa2.h
 EXPORTS = (
@@ -65,10 +66,11 @@ def _declare(lib):
         "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
-                                  _vp, _vp]),
+                                  _vp, _vp, _vp]),
         "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_topk_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
-        "csa2_block_pool": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+        "csa2_block_pool": (_i, [_vp, _vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp, _i, _vp, ctypes.c_size_t,
+                                 _vp]),
         "csa2_block_pool_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -283,10 +285,13 @@ def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=No
 
 def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=None, block: int = 8,
                      scores: Optional[torch.Tensor] = None, block_max: Optional[torch.Tensor] = None,
-                     want_scores: bool = True, want_block_max: bool = False):
+                     want_scores: bool = True, want_block_max: bool = False,
+                     block_hist: Optional[torch.Tensor] = None):
     """qI [B,Q,H_I,d] (f32/bf16) or [B,Q,H_I,68] uint8 (MXFP4, d = 128), w [B,Q,H_I],
     kI [B,N,d] (f32/bf16) or [B,N,row_bytes] uint8 (MXFP4), n_visible [B,Q] int64.
     MXFP4 queries over MXFP4 keys run the QK product in FP4 on the tensor cores.
+    block_hist ([B,Q,BLOCK_HIST_BINS] int32 storage, full scan with block_max only)
+    receives the block maxima's summary for csa2_block_pool.
     Returns (scores, block_max); either may be None."""
     B, Q, H_I, d = qI.shape
     if qI.dtype == torch.uint8:
@@ -309,7 +314,8 @@ def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=Non
         if want_block_max and block_max is None:
             block_max = torch.empty((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
     st = _lib().csa2_index_score(ctx(qI.device.index), _p(qI), q_dt, _p(w), _p(kI), k_dt, B, Q, N, H_I, d,
-                                 _p(n_visible), _p(pool), n_pool, block, _p(scores), _p(block_max), _stream(qI))
+                                 _p(n_visible), _p(pool), n_pool, block, _p(scores), _p(block_max),
+                                 _p(block_hist), _stream(qI))
     _check("csa2_index_score", st)
     return scores, block_max
 
@@ -348,18 +354,25 @@ def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores:
 
 
 def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
-                    out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+                    out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                    block_hist: Optional[torch.Tensor] = None, n_top: int = 0,
+                    out_top: Optional[torch.Tensor] = None):
+    """The pool ([..., n_keep] int32).  With n_top > 0 also the n_top best blocks
+    ([..., n_top] int32, ascending): returns (pool, top) then."""
     ld = block_max.shape[-1]
     rows = block_max.numel() // ld if ld else 0
     if out is None:
         out = torch.empty((*block_max.shape[:-1], n_keep), dtype=torch.int32, device=block_max.device)
+    if n_top > 0 and out_top is None:
+        out_top = torch.empty((*block_max.shape[:-1], n_top), dtype=torch.int32, device=block_max.device)
     if ws is None:
         ws = _ws(csa2_block_pool_workspace_bytes(rows, ld, n_keep, block_max.device.index) if rows else 0,
                  block_max.device)
-    st = _lib().csa2_block_pool(ctx(block_max.device.index), _p(block_max), rows, ld, _p(n_visible), block, n_keep,
-                                _p(out), _p(ws), ws.numel(), _stream(block_max))
+    st = _lib().csa2_block_pool(ctx(block_max.device.index), _p(block_max), _p(block_hist), rows, ld, _p(n_visible),
+                                block, n_keep, _p(out), _p(out_top) if n_top > 0 else None, n_top, _p(ws),
+                                ws.numel(), _stream(block_max))
     _check("csa2_block_pool", st)
-    return out
+    return (out, out_top) if n_top > 0 else out
 
 
 def csa2_sparse_attn_workspace_bytes(B: int, Q: int, H: int, k: int, window: int,

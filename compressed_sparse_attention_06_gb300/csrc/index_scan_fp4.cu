@@ -82,7 +82,8 @@ constexpr int OFF_W = OFF_STAGE + STAGES * MX_STAGE;
 constexpr int OFF_BAR = OFF_W + HEADS * 4;
 constexpr int N_BARS = 2 * STAGES + 3 * BUFS;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
-constexpr int SMEM = OFF_TMEMPTR + 16 + 128;
+constexpr int OFF_HIST = OFF_TMEMPTR + 16;               // [CSA2_BLOCK_HIST_BINS] block-max digit counts
+constexpr int SMEM = OFF_HIST + CSA2_BLOCK_HIST_BINS * 4 + 128;
 // tensor memory
 constexpr uint32_t D_COL0 = 0;                          // D[j]: 2 sub-tiles x 64 columns
 constexpr uint32_t A_COL0 = D_COL0 + BUFS * 128;        // A[j]: 2 x 16 columns (128 E2M1 per lane)
@@ -103,6 +104,7 @@ struct FpArgs {
     const int32_t* pool;          // candidate mode: [B, Q, n_pool]
     float* scores;                // full: [B, Q, N]; candidate: [B, Q, n_pool*8]
     float* bmax;                  // full: [B, Q, ceil(N/8)]
+    uint32_t* hist;               // full: [B, Q, CSA2_BLOCK_HIST_BINS] (zeroed before), or NULL
     unsigned int* st;
     int B, Q, n_pool;
     int64_t N;
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     uint64_t* done = afull + BUFS;           // [BUFS] the tile's MMAs completed: D ready, A free
     uint64_t* dempty = done + BUFS;          // [BUFS] D tile read by an epilogue group
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+    uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + OFF_HIST);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y;                // b * Q + q
@@ -183,6 +186,8 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
             make_uint4(ld_u32(src), ld_u32(src + 4), ld_u32(src + 8), ld_u32(src + 12));
     }
     for (int h = threadIdx.x; h < HEADS; h += THREADS) sW[h] = a.w[(int64_t)g * HEADS + h];
+    if (!CAND && a.hist)
+        for (int i = threadIdx.x; i < CSA2_BLOCK_HIST_BINS; i += THREADS) sHist[i] = 0u;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -364,7 +369,11 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    if ((lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = m;
+                    if ((lane & 7) == 0 && (e >> 3) < nb) {
+                        a.bmax[(int64_t)g * nb + (e >> 3)] = m;
+                        // the pool's first radix digit of every visible block's maximum
+                        if (a.hist && m != -INFINITY) atomicAdd(&sHist[order_key(m) >> 20], 1u);
+                    }
                 }
             }
         }
@@ -384,6 +393,12 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    // this CTA's block-max digit counts into the row's histogram
+    if (!CAND && a.hist) {
+        uint32_t* hrow = a.hist + (int64_t)g * CSA2_BLOCK_HIST_BINS;
+        for (int i = threadIdx.x; i < CSA2_BLOCK_HIST_BINS; i += THREADS)
+            if (const uint32_t v = sHist[i]) atomicAdd(&hrow[i], v);
+    }
 }
 
 template <bool CAND>
@@ -407,7 +422,8 @@ csa2_status launch_fp4(csa2_ctx* ctx, FpArgs& a, cudaStream_t s) {
 
 csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const float* w, const void* k_idx, int B,
                                      int Q, int64_t N, int H_I, const int64_t* n_visible, const int32_t* pool,
-                                     int n_pool, int block, float* scores, float* block_max, cudaStream_t s) {
+                                     int n_pool, int block, float* scores, float* block_max, uint32_t* hist,
+                                     cudaStream_t s) {
     if (H_I != HEADS || block != 8 || (N % 8) != 0 || N == 0) return CSA2_ERR_UNSUPPORTED;
     if (pool && (n_pool % BLOCKS_PER_TILE) != 0) return CSA2_ERR_UNSUPPORTED;
     FpArgs a;
@@ -418,6 +434,7 @@ csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const flo
     a.pool = pool;
     a.scores = scores;
     a.bmax = block_max;
+    a.hist = pool ? nullptr : hist;
     a.st = ctx->status;
     a.B = B;
     a.Q = Q;

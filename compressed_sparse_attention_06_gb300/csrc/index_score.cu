@@ -152,11 +152,13 @@ void launch_simt(const void* qI, const float* w, const void* kI, int B, int Q, i
 extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_dtype q_dt, const float* w,
                                         const void* k_idx, csa2_dtype k_dt, int B, int Q, int64_t N, int H_I,
                                         int d_I, const int64_t* n_visible, const int32_t* pool_blocks,
-                                        int n_pool, int block, float* scores, float* block_max, void* stream) {
+                                        int n_pool, int block, float* scores, float* block_max,
+                                        uint32_t* block_hist, void* stream) {
     if (!ctx || B < 0 || Q < 0 || N < 0 || H_I < 1 || H_I > 128) return CSA2_ERR_INVALID_ARG;
     if (d_I != D_IDX) return CSA2_ERR_UNSUPPORTED;
     if (block < 1 || block > 32 || (block & (block - 1))) return CSA2_ERR_INVALID_ARG;
     if (pool_blocks && (block_max || !scores || n_pool < 0)) return CSA2_ERR_INVALID_ARG;
+    if (block_hist && (pool_blocks || !block_max)) return CSA2_ERR_INVALID_ARG;
     if (q_dt != CSA2_F32 && q_dt != CSA2_BF16 && q_dt != CSA2_MXFP4_E8M0x32) return CSA2_ERR_UNSUPPORTED;
     if (k_dt != CSA2_F32 && k_dt != CSA2_BF16 && k_dt != CSA2_MXFP4_E8M0x32) return CSA2_ERR_UNSUPPORTED;
     if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;
@@ -165,19 +167,31 @@ extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_d
     if (!aligned(q_idx, 16) || !aligned(k_idx, 16)) return CSA2_ERR_INVALID_ARG;
     const int64_t n_elems = pool_blocks ? (int64_t)n_pool * block : N;
     if (n_elems == 0) return CSA2_OK;
+    if (block_hist && !aligned(block_hist, 16)) return CSA2_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
+    const int64_t rows = (int64_t)B * Q;
+    if (block_hist) {
+        const csa2_status z = block_hist_zero(block_hist, rows, s);
+        if (z != CSA2_OK) return z;
+    }
+    // the histogram of the block maxima: built by the FP4 scan itself, else counted
+    // from the written maxima once the scan is done
+    auto hist_after = [&](csa2_status r) -> csa2_status {
+        if (r != CSA2_OK || !block_hist) return r;
+        return block_hist_from_max(block_max, rows, (N + block - 1) / block, n_visible, block, block_hist, s);
+    };
 
     // FP4 tensor-core scan for MXFP4 queries over MXFP4 keys; the kind::f16 scan for
     // bf16 queries over bf16 or MXFP4 keys.
     if (q_dt == CSA2_MXFP4_E8M0x32 && k_dt == CSA2_MXFP4_E8M0x32) {
         csa2_status r = index_score_fp4_dispatch(ctx, q_idx, w, k_idx, B, Q, N, H_I, n_visible, pool_blocks, n_pool,
-                                                 block, scores, block_max, s);
+                                                 block, scores, block_max, block_hist, s);
         if (r != CSA2_ERR_UNSUPPORTED) return r;
     }
     if (q_dt == CSA2_BF16 && k_dt != CSA2_F32) {
         csa2_status r = index_score_tc_dispatch(ctx, q_idx, w, k_idx, k_dt, B, Q, N, H_I, n_visible,
                                                 pool_blocks, n_pool, block, scores, block_max, s);
-        if (r != CSA2_ERR_UNSUPPORTED) return r;
+        if (r != CSA2_ERR_UNSUPPORTED) return hist_after(r);
     }
 #define CSA2_IS_LAUNCH(TQ, KF)                                                                            \
     launch_simt<TQ, KF>(q_idx, w, k_idx, B, Q, N, H_I, n_visible, pool_blocks, n_pool, block, scores,       \
@@ -196,5 +210,5 @@ extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_d
         else CSA2_IS_LAUNCH(__nv_bfloat16, K_MX);
     }
 #undef CSA2_IS_LAUNCH
-    return csa2_launch_status();
+    return hist_after(csa2_launch_status());
 }

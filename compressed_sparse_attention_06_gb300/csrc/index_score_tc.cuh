@@ -13,4 +13,15 @@ csa2_status index_score_tc_dispatch(csa2_ctx* ctx, const void* q_idx, const floa
 // Same contract as index_score_tc_dispatch.
 csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const float* w, const void* k_idx, int B,
                                      int Q, int64_t N, int H_I, const int64_t* n_visible, const int32_t* pool,
-                                     int n_pool, int block, float* scores, float* block_max, cudaStream_t s);
+                                     int n_pool, int block, float* scores, float* block_max, uint32_t* hist,
+                                     cudaStream_t s);
+// hist != NULL: the scan adds every visible block maximum's first radix digit to
+// hist ([B*Q, CSA2_BLOCK_HIST_BINS], zeroed beforehand).  The other scans leave it
+// to block_hist_from_max (select.cu).
+
+// Pool histogram helpers (select.cu): zero rows x CSA2_BLOCK_HIST_BINS words; count
+// the first radix digit of the visible block maxima of each row (n_visible entries
+// per row, blocks of `block`).
+csa2_status block_hist_zero(uint32_t* hist, int64_t rows, cudaStream_t s);
+csa2_status block_hist_from_max(const float* bmax, int64_t rows, int64_t ld, const int64_t* n_visible, int block,
+                                uint32_t* hist, cudaStream_t s);

@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "csa2_internal.cuh"
+#include "index_score_tc.cuh"
 
 namespace {
 
@@ -183,7 +184,8 @@ __device__ __forceinline__ void hist_pass(KeyAt key_at, int64_t n, uint32_t pref
 // The bin (searched from the top) that holds the `remaining`-th largest active key:
 // sh.bin = that bin, sh.above = active keys in the bins above it.  nb is a multiple
 // of the block size.
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t remaining, SelShared& sh) {
+template <class Sh>
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t remaining, Sh& sh) {
     const int per = nb / (int)blockDim.x;
     const int top = nb - 1 - (int)threadIdx.x * per;
     uint32_t loc = 0;
@@ -836,6 +838,8 @@ __device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+__device__ void cl_search_full(ClShared& sh, int nb, uint32_t remaining, int& bin, uint32_t& above);
+
 // Cluster-wide: the bin (of nb, searched from the top) holding the remaining-th
 // largest key of the row, and the number of keys in the bins above it, from every
 // CTA's local histogram sh.hist.  CTA r sums bins [r*W, r*W+W) over the cluster and
@@ -852,12 +856,24 @@ __device__ void cl_find_bin(ClShared& sh, int nb, uint32_t remaining, uint32_t C
                                            // CTA has finished reading its sh.full
     if ((int)threadIdx.x < W) {
         const uint32_t off = 4u * (rank * (uint32_t)W + threadIdx.x);
-        uint32_t v = cl_sum8(base, hist_off + off);
-        if (C == 16) v += cl_sum8(base + 8, hist_off + off);
+        uint32_t v = 0u;
+        if (C == 8 || C == 16) {
+            v = cl_sum8(base, hist_off + off);
+            if (C == 16) v += cl_sum8(base + 8, hist_off + off);
+        } else {
+            for (uint32_t c = 0; c < C; ++c) v += cl_ld(base[c] + hist_off + off);
+        }
         for (uint32_t c = 0; c < C; ++c) cl_st(base[c] + full_off + off, v);
     }
     cl_sync();                             // every slice is in every CTA's sh.full
-    // local search from the top: thread t sums `per` consecutive bins
+    cl_search_full(sh, nb, remaining, bin, above);
+}
+
+// Search sh.full (a whole row's histogram of nb bins) from the top for the bin holding
+// the remaining-th largest key: bin, and the keys in the bins above it; sh.total gets
+// the keys counted (bin = 0, above = 0 if remaining exceeds it).  nb is a multiple of
+// the block size.
+__device__ void cl_search_full(ClShared& sh, int nb, uint32_t remaining, int& bin, uint32_t& above) {
     const int per = nb / (int)blockDim.x;
     const int top = nb - 1 - (int)threadIdx.x * per;
     uint32_t loc = 0;
@@ -1086,7 +1102,7 @@ __global__ void __launch_bounds__(CL_THREADS) sel_cluster_kernel(SelArgs a, int 
 // into chunks of at most CL_MAX_CHUNK keys.  8 CTAs when the chunks fit (measured: the
 // cluster barriers of 8 CTAs are cheaper than those of 16), else 16.
 int cluster_size_for(csa2_ctx* ctx, int64_t rows, int64_t n_max) {
-    if (n_max < 4096) return 0;
+    if (n_max <= 8192) return 0;           // one CTA stages the row: no cluster barriers
     for (int c : {8, 16}) {
         if (rows * c > ctx->num_sms) return 0;
         if (((n_max + c - 1) / c + 31) / 32 * 32 > CL_MAX_CHUNK) continue;
@@ -1122,6 +1138,392 @@ csa2_status launch_cluster(csa2_ctx* ctx, const SelArgs& a, int64_t rows, int64_
     cfg.attrs = at;
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
+    return csa2_launch_status();
+}
+
+// ---------------------------------------------------------------- pool from a histogram
+// The decode pool (CSA2 page, «解码器里的分层索引») with the first radix digit already
+// counted: the indexer scan adds every visible block maximum's leading 12 key bits to
+// a per-row histogram, so the threshold bin of the pool (rank n_keep-1 among the
+// blocks other than the newest) and of the top blocks (rank n_top among all blocks)
+// are read off that histogram.  One thread-block cluster per row; each CTA loads its
+// chunk of block maxima (every load in flight at once, beside the histogram's) and
+// classifies them: above the threshold bin -> winner, in it -> candidate.  The
+// candidates of the whole row are few (a few hundred on Gaussian scores: a bin is 1/8
+// of an octave wide), so every CTA gathers all of them through distributed shared
+// memory and ranks its own ones against them in the order (key desc, index asc): a
+// candidate wins if fewer than the remaining count rank above it.  Only a threshold
+// bin of more than PH_CAP keys takes cluster-wide radix passes (a threshold key T,
+// ties at T taken lowest index first).  Each CTA then pushes its winner and tie
+// counts into every CTA of the cluster, and after one more cluster barrier emits its
+// winners in index order at its offset.  The barrier sequence depends only on the
+// row's histogram, so every CTA of a cluster runs the same one.
+constexpr int PH_CAP = 2048;               // candidates a selection gathers on every CTA
+constexpr int PH_MAX_C = 16;
+constexpr int PH_KPT = CL_MAX_CHUNK / CL_THREADS;   // keys a thread loads (16)
+
+struct PoolArgs {
+    const float* bmax;        // [rows, ld]
+    int64_t ld;
+    const int64_t* nv;        // [rows] visible entries
+    const uint32_t* hist;     // [rows, NB_A] first-digit counts of the visible block maxima
+    int block;
+    int n_keep;               // pool size: the newest block + n_keep - 1 others
+    int32_t* out_pool;        // [rows, n_keep]
+    int n_top;                // 0: no top list
+    int32_t* out_top;         // [rows, n_top]
+    unsigned int* st;
+};
+
+struct PhShared {
+    uint32_t nloc[2];                      // candidates in this CTA's list, per selection
+    uint32_t start[PH_MAX_C + 1];          // the gathered list: where each CTA's candidates begin
+    uint32_t cnt[2][PH_MAX_C][2];          // pushed by every CTA: its (winners, ties at T), per selection
+    uint32_t rem[2];                       // ties at T to take (cluster-wide radix passes only)
+};
+
+// Ordered emission of one selection from the CTA's bitmaps: winners (bmW) in index
+// order, ties (bmE) while fewer than `quota` have been taken, at out[off + rank].
+__device__ void ph_emit(const uint32_t* bmW, const uint32_t* bmE, int nwords, int64_t c0, uint32_t off,
+                        uint32_t quota, int32_t* out, uint32_t out_len, ClShared& sh) {
+    const int tid = threadIdx.x;
+    const int per = (nwords + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    uint32_t cg = 0, ce = 0;
+    for (int w = w0; w < w1; ++w) {
+        cg += __popc(bmW[w]);
+        ce += __popc(bmE[w]);
+    }
+    uint32_t tot;
+    uint32_t gb = block_excl_scan_u32(cg, sh, tot);
+    uint32_t eb = block_excl_scan_u32(ce, sh, tot);
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t wg = bmW[w], we = bmE[w];
+        uint32_t bits = wg | we;
+        while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int32_t id = (int32_t)(c0 + w * 32 + j);
+            if ((wg >> j) & 1u) {
+                const uint32_t pos = off + gb + min(eb, quota);
+                if (pos < out_len) out[pos] = id;
+                ++gb;
+            } else {
+                if (eb < quota && off + gb + eb < out_len) out[off + gb + eb] = id;
+                ++eb;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int chunk) {
+    extern __shared__ __align__(16) uint32_t dyn[];
+    __shared__ ClShared sh;
+    __shared__ PhShared px;
+    pdl_wait();                            // the block maxima and the histogram are complete
+    const uint32_t C = cl_size(), rank = cl_rank();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t row = blockIdx.y;
+    const int64_t V = a.nv[row];
+    int64_t nb = V > 0 ? (V + a.block - 1) / a.block : 0;
+    if (nb > a.ld) {
+        if (tid == 0 && rank == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
+        nb = a.ld;
+    }
+    const bool doT = a.out_top != nullptr && a.n_top > 0;
+    const bool allP = nb <= a.n_keep, allT = !doT || nb <= a.n_top;
+    int32_t* outP = a.out_pool + row * a.n_keep;
+    int32_t* outT = doT ? a.out_top + row * a.n_top : nullptr;
+    const int bd = CL_THREADS;
+    // every visible block fits: ascending ids, then -1
+    if (allP)
+        for (int64_t i = (int64_t)rank * bd + tid; i < a.n_keep; i += (int64_t)C * bd) outP[i] = i < nb ? (int32_t)i : -1;
+    if (doT && allT)
+        for (int64_t i = (int64_t)rank * bd + tid; i < a.n_top; i += (int64_t)C * bd) outT[i] = i < nb ? (int32_t)i : -1;
+    if (allP && allT) {                    // the same for every CTA of the row: no barrier used
+        pdl_trigger();
+        return;
+    }
+    // every load of the phase in flight together: this thread's keys (key i of the
+    // chunk is loaded by thread i % 1024), the histogram, the newest block's maximum
+    const int64_t newest = nb - 1;
+    const int64_t c0 = (int64_t)rank * chunk;
+    const int n = (int)max((int64_t)0, min((int64_t)chunk, nb - c0));
+    const float* rowp = a.bmax + row * a.ld + c0;
+    float v[PH_KPT];
+#pragma unroll
+    for (int j = 0; j < PH_KPT; ++j) {
+        const int i = tid + j * bd;
+        v[j] = i < n ? rowp[i] : 0.0f;
+    }
+    const uint32_t* hrow = a.hist + row * NB_A;
+    uint32_t hv[NB_A / CL_THREADS];
+#pragma unroll
+    for (int j = 0; j < NB_A / CL_THREADS; ++j) hv[j] = hrow[tid + j * bd];
+    const uint32_t knew = order_key(a.bmax[row * a.ld + newest]);
+#pragma unroll
+    for (int j = 0; j < NB_A / CL_THREADS; ++j) sh.full[tid + j * bd] = hv[j];
+    if (tid < 2) px.nloc[tid] = 0u;
+    __syncthreads();
+    // the threshold bins of both selections
+    const uint32_t k[2] = {(uint32_t)a.n_keep - 1u, (uint32_t)a.n_top};
+    const bool act[2] = {!allP, !allT};
+    int bin[2] = {0, 0};
+    uint32_t above[2] = {0u, 0u}, m[2] = {0u, 0u};
+    if (act[1]) {
+        cl_search_full(sh, NB_A, k[1], bin[1], above[1]);
+        m[1] = sh.full[bin[1]];
+    }
+    if (act[0]) {                          // the newest block is not among the pool's candidates
+        __syncthreads();                   // every thread has read m[1] before the count changes
+        if (tid == 0) sh.full[knew >> 20] -= 1u;
+        __syncthreads();
+        cl_search_full(sh, NB_A, k[0], bin[0], above[0]);
+        m[0] = sh.full[bin[0]];
+    }
+    // classify: the 32 keys of word w = i / 32 are lanes of one warp in one step
+    const int cw = chunk / 32;
+    const int nwords = (n + 31) / 32;
+    uint32_t* skey = dyn;                                  // [chunk]
+    uint32_t* bmW = dyn + chunk;                           // [2][cw]
+    uint32_t* bmE = bmW + 2 * cw;                          // [2][cw]
+    uint64_t* loc = reinterpret_cast<uint64_t*>(bmE + 2 * cw);   // [2][PH_CAP] this CTA's candidates
+    uint64_t* all = loc + 2 * PH_CAP;                      // [2][PH_CAP] every CTA's, gathered
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < PH_KPT; ++j) {
+        const int i = tid + j * bd;
+        const int w = i >> 5;
+        if (w >= cw) break;                                // the same for the whole warp
+        const uint32_t key = i < n ? order_key(v[j]) : 0u;
+        skey[i] = key;
+        const int d = (int)(key >> 20);
+        const bool v0 = act[0] && key != 0u && c0 + i != newest, v1 = act[1] && key != 0u;
+        const unsigned g0 = __ballot_sync(FULL_MASK, v0 && d > bin[0]);
+        const unsigned e0 = __ballot_sync(FULL_MASK, v0 && d == bin[0]);
+        const unsigned g1 = __ballot_sync(FULL_MASK, v1 && d > bin[1]);
+        const unsigned e1 = __ballot_sync(FULL_MASK, v1 && d == bin[1]);
+        if (lane == 0) {
+            bmW[w] = g0;
+            bmW[cw + w] = g1;
+            bmE[w] = 0u;
+            bmE[cw + w] = 0u;
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            const unsigned e = s2 == 0 ? e0 : e1;
+            if (!e) continue;
+            uint32_t o = 0u;
+            if (lane == 0) o = atomicAdd(&px.nloc[s2], (uint32_t)__popc(e));
+            o = __shfl_sync(FULL_MASK, o, 0) + __popc(e & lt);
+            if (((e >> lane) & 1u) && o < PH_CAP) loc[s2 * PH_CAP + o] = ((uint64_t)key << 32) | (uint32_t)(c0 + i);
+        }
+    }
+    cl_sync();                             // (1) every CTA's candidate list is complete
+#pragma unroll 1
+    for (int s2 = 0; s2 < 2; ++s2) {
+        if (!act[s2]) continue;
+        uint32_t* W = bmW + s2 * cw;
+        uint32_t* E = bmE + s2 * cw;
+        const uint32_t r = k[s2] - above[s2];              // winners still to find in the bin
+        uint32_t rem_ties = 0u;
+        if (m[s2] <= (uint32_t)PH_CAP) {
+            // gather every CTA's candidates (one remote load each, all in flight), then
+            // rank this CTA's own candidates against them: (key desc, index asc)
+            uint64_t* A = all + s2 * PH_CAP;
+            if (tid < 32) {
+                const uint32_t nc = tid < (int)C ? min(cl_ld(cl_map(&px, tid) + (uint32_t)offsetof(PhShared, nloc) +
+                                                             4u * s2), (uint32_t)PH_CAP) : 0u;
+                uint32_t incl = nc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t u = __shfl_up_sync(FULL_MASK, incl, o);
+                    if (tid >= o) incl += u;
+                }
+                if (tid <= (int)C) px.start[tid] = incl - nc;     // start[C]: the total
+            }
+            __syncthreads();
+            const uint32_t mm = min(px.start[C], (uint32_t)PH_CAP);
+            for (uint32_t j = tid; j < mm; j += bd) {
+                uint32_t c = 0;
+                while (c + 1 < C && j >= px.start[c + 1]) ++c;
+                const uint32_t src = cl_map(loc + s2 * PH_CAP, c) + 8u * (j - px.start[c]);
+                uint32_t lo, hi;
+                asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(src) : "memory");
+                A[j] = (((uint64_t)hi << 32) | lo) ^ 0xFFFFFFFFull;   // larger = earlier in the order
+            }
+            __syncthreads();
+            const uint32_t nl = min(px.nloc[s2], (uint32_t)PH_CAP);
+            for (uint32_t ci = wid; ci < nl; ci += CL_THREADS / 32) {
+                const uint64_t x = loc[s2 * PH_CAP + ci] ^ 0xFFFFFFFFull;
+                uint32_t ahead = 0u;
+                for (uint32_t j = lane; j < mm; j += 32) ahead += A[j] > x;
+                ahead = __reduce_add_sync(FULL_MASK, ahead);
+                if (lane == 0 && ahead < r) {
+                    const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - c0);
+                    atomicOr(&W[li >> 5], 1u << (li & 31));
+                }
+            }
+        } else {
+            // a crowded threshold bin: the remaining two digits cluster-wide, then the
+            // ties at T by index
+            uint32_t prefix = (uint32_t)bin[s2] << 20, rr = r;
+            for (int pass = 0; pass < 2; ++pass) {
+                const int shift = pass == 0 ? 10 : 0;
+                const uint32_t pm = pass == 0 ? 0xFFF00000u : 0xFFFFFC00u;
+                for (int i = tid; i < NB_B; i += bd) sh.hist[i] = 0u;
+                __syncthreads();
+                for (int i0 = 0; i0 < nwords * 32; i0 += bd) {
+                    const int i = i0 + tid;
+                    const uint32_t key = i < nwords * 32 ? skey[i] : 0u;
+                    const bool ok = key != 0u && (key & pm) == prefix && !(s2 == 0 && c0 + i == newest);
+                    hist_add_warp(sh.hist, (key >> shift) & 0x3FFu, ok);
+                }
+                __syncthreads();
+                uint32_t base[PH_MAX_C];
+#pragma unroll
+                for (int c = 0; c < PH_MAX_C; ++c) base[c] = cl_map(&sh, (uint32_t)c < C ? (uint32_t)c : 0u);
+                int b2;
+                uint32_t ab;
+                cl_find_bin(sh, NB_B, rr, C, rank, base, b2, ab);
+                prefix |= (uint32_t)b2 << shift;
+                rr -= ab;
+            }
+            rem_ties = rr;
+            for (int i = tid; i < n; i += bd) {
+                const uint32_t key = skey[i];
+                if (key == 0u || (key >> 20) != (uint32_t)bin[s2] || (s2 == 0 && c0 + i == newest)) continue;
+                if (key > prefix) atomicOr(&W[i >> 5], 1u << (i & 31));
+                else if (key == prefix) atomicOr(&E[i >> 5], 1u << (i & 31));
+            }
+        }
+        if (s2 == 0 && newest >= c0 && newest < c0 + n) {   // the pool always keeps the newest block
+            const int li = (int)(newest - c0);
+            if (tid == 0) atomicOr(&W[li >> 5], 1u << (li & 31));
+        }
+        __syncthreads();
+        // this CTA's winner and tie counts, pushed into every CTA of the cluster
+        uint32_t cwin = 0u, ctie = 0u;
+        for (int w = tid; w < nwords; w += bd) {
+            cwin += __popc(W[w]);
+            ctie += __popc(E[w]);
+        }
+        cwin = __reduce_add_sync(FULL_MASK, cwin);
+        ctie = __reduce_add_sync(FULL_MASK, ctie);
+        __shared__ uint32_t wsum[2][CL_THREADS / 32];
+        if (lane == 0) {
+            wsum[0][wid] = cwin;
+            wsum[1][wid] = ctie;
+        }
+        if (tid == 0) px.rem[s2] = rem_ties;
+        __syncthreads();
+        if (tid < (int)C) {
+            uint32_t tw = 0u, tt = 0u;
+            for (int i = 0; i < CL_THREADS / 32; ++i) {
+                tw += wsum[0][i];
+                tt += wsum[1][i];
+            }
+            const uint32_t dst = cl_map(&px.cnt[s2][rank][0], (uint32_t)tid);
+            cl_st(dst, tw);
+            cl_st(dst + 4u, tt);
+        }
+        __syncthreads();
+    }
+    cl_sync();                             // (2) every CTA's counts are in every CTA
+#pragma unroll 1
+    for (int s2 = 0; s2 < 2; ++s2) {
+        if (!act[s2]) continue;
+        uint32_t off = 0u, ties_before = 0u, total = 0u, quota = 0u;
+        const uint32_t rem = px.rem[s2];
+        for (uint32_t c = 0; c < C; ++c) {
+            const uint32_t wc = px.cnt[s2][c][0], tc = px.cnt[s2][c][1];
+            const uint32_t take = rem > ties_before ? min(rem - ties_before, tc) : 0u;
+            if (c < rank) off += wc + take;
+            if (c == rank) quota = take;
+            total += wc + take;
+            ties_before += tc;
+        }
+        int32_t* out = s2 == 0 ? outP : outT;
+        const int out_len = s2 == 0 ? a.n_keep : a.n_top;
+        ph_emit(bmW + s2 * cw, bmE + s2 * cw, nwords, c0, off, quota, out, (uint32_t)out_len, sh);
+        for (int64_t i = (int64_t)total + (int64_t)rank * bd + tid; i < out_len; i += (int64_t)C * bd) out[i] = -1;
+        __syncthreads();
+    }
+    pdl_trigger();
+    // no CTA touches another's shared memory after barrier (2): each may leave now
+}
+
+// Counts of the first radix digit of the visible block maxima (a CTA per chunk of a
+// row, atomics into the zeroed row histogram).
+constexpr int HIST_CHUNK = 8192;
+
+__global__ void __launch_bounds__(256) block_hist_zero_kernel(uint32_t* hist, int64_t words) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i * 4 < words) reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void __launch_bounds__(256) block_hist_kernel(const float* bmax, int64_t ld, const int64_t* nv, int block,
+                                                         uint32_t* hist) {
+    __shared__ uint32_t h[NB_A];
+    pdl_wait();
+    const int64_t row = blockIdx.y;
+    const int64_t V = nv[row];
+    const int64_t nb = min(ld, V > 0 ? (V + block - 1) / block : (int64_t)0);
+    const int64_t c0 = (int64_t)blockIdx.x * HIST_CHUNK, c1 = min(nb, c0 + HIST_CHUNK);
+    for (int i = threadIdx.x; i < NB_A; i += 256) h[i] = 0u;
+    __syncthreads();
+    for (int64_t i = c0 + threadIdx.x; i < c1; i += 256) atomicAdd(&h[order_key(bmax[row * ld + i]) >> 20], 1u);
+    __syncthreads();
+    pdl_trigger();
+    if (c0 >= c1) return;
+    for (int i = threadIdx.x; i < NB_A; i += 256)
+        if (h[i]) atomicAdd(&hist[row * NB_A + i], h[i]);
+}
+
+int pool_cluster_size(const csa2_ctx* ctx, int64_t rows, int64_t ld) {
+    for (int c : {8, 16, 4, 2, 1}) {
+        if (((ld + c - 1) / c + CL_THREADS - 1) / CL_THREADS * CL_THREADS > CL_MAX_CHUNK) continue;
+        if (c > 1 && rows * c > ctx->num_sms) continue;
+        return c;
+    }
+    return 16;
+}
+
+size_t pool_hist_smem(int chunk) {
+    return (size_t)chunk * 4 + (size_t)chunk / 32 * 16 + 4ull * PH_CAP * 8;
+}
+
+csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cudaStream_t s) {
+    const int C = pool_cluster_size(ctx, rows, a.ld);
+    const int chunk = (int)(((a.ld + C - 1) / C + CL_THREADS - 1) / CL_THREADS * CL_THREADS);
+    if (chunk > CL_MAX_CHUNK) return CSA2_ERR_UNSUPPORTED;
+    const size_t smem = pool_hist_smem(chunk);
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(pool_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pool_hist_smem(CL_MAX_CHUNK)) != cudaSuccess ||
+            cudaFuncSetAttribute(pool_hist_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess)
+            return CSA2_ERR_CUDA;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
+    cfg.blockDim = dim3(CL_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, pool_hist_kernel, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
     return csa2_launch_status();
 }
 
@@ -1217,9 +1619,11 @@ extern "C" size_t csa2_topk_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t
     return select_ws_bytes(ctx, rows, n, k);
 }
 
+// The workspace of csa2_block_pool: the row histograms when the caller passes none,
+// or the general path's chunk winners, whichever is larger.
 extern "C" size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, int n_keep) {
     if (!ctx || rows <= 0 || ld <= 0 || n_keep < 2 || rows > 65535) return 0;
-    return select_ws_bytes(ctx, rows, ld, n_keep - 1);
+    return std::max(select_ws_bytes(ctx, rows, ld, n_keep - 1), (size_t)rows * NB_A * sizeof(uint32_t));
 }
 
 extern "C" csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t rows, int64_t n, int64_t ld,
@@ -1254,13 +1658,44 @@ extern "C" csa2_status csa2_topk(csa2_ctx* ctx, const float* scores, int64_t row
     return run_select<SEL_TOPK>(ctx, a, rows, n, ws, ws_bytes, s);
 }
 
-extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
-                                       const int64_t* n_visible, int block, int n_keep, int32_t* out_blocks,
-                                       void* ws, size_t ws_bytes, void* stream) {
+extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, const uint32_t* block_hist,
+                                       int64_t rows, int64_t ld, const int64_t* n_visible, int block, int n_keep,
+                                       int32_t* out_blocks, int32_t* out_top, int n_top, void* ws,
+                                       size_t ws_bytes, void* stream) {
     if (!ctx || rows < 0 || ld < 0 || block < 1 || n_keep < 1 || n_keep > 4096) return CSA2_ERR_INVALID_ARG;
+    if (n_top < 0 || n_top > 4096 || (n_top > 0 && !out_top)) return CSA2_ERR_INVALID_ARG;
     if (rows == 0) return CSA2_OK;
     if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
-    if (!block_max || !n_visible || !out_blocks || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    if (!block_max || !n_visible || !out_blocks || !aligned(ws, 16) || !aligned(block_hist, 16))
+        return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    // with the row histograms (given, or built here in the workspace) the selection
+    // reads the maxima once; without them the general radix select runs
+    const uint32_t* hist = block_hist;
+    const size_t hbytes = (size_t)rows * NB_A * sizeof(uint32_t);
+    const bool fits = ld > 0 && ((ld + PH_MAX_C - 1) / PH_MAX_C + CL_THREADS - 1) / CL_THREADS * CL_THREADS <= CL_MAX_CHUNK;
+    if (!hist && fits && ws && ws_bytes >= hbytes) {
+        uint32_t* h = reinterpret_cast<uint32_t*>(ws);
+        csa2_status r = block_hist_zero(h, rows, s);
+        if (r == CSA2_OK) r = block_hist_from_max(block_max, rows, ld, n_visible, block, h, s);
+        if (r != CSA2_OK) return r;
+        hist = h;
+    }
+    if (hist && fits && n_keep >= 2) {
+        PoolArgs p;
+        p.bmax = block_max;
+        p.ld = ld;
+        p.nv = n_visible;
+        p.hist = hist;
+        p.block = block;
+        p.n_keep = n_keep;
+        p.out_pool = out_blocks;
+        p.n_top = n_top;
+        p.out_top = n_top > 0 ? out_top : nullptr;
+        p.st = ctx->status;
+        return launch_pool_hist(ctx, p, rows, s);
+    }
+    if (n_top > 0) return CSA2_ERR_UNSUPPORTED;   // the top blocks need a histogram
     SelArgs a;
     a.vals = block_max;
     a.n = ld;
@@ -1274,5 +1709,20 @@ extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, in
     a.out_idx = out_blocks;
     a.out_val = nullptr;
     a.st = ctx->status;
-    return run_select<SEL_POOL>(ctx, a, rows, ld, ws, ws_bytes, as_stream(stream));
+    return run_select<SEL_POOL>(ctx, a, rows, ld, ws, ws_bytes, s);
+}
+
+csa2_status block_hist_zero(uint32_t* hist, int64_t rows, cudaStream_t s) {
+    const int64_t words = rows * NB_A;
+    const csa2_status r = launch_pdl(block_hist_zero_kernel, dim3((unsigned)((words / 4 + 255) / 256)), dim3(256), 0,
+                                     s, hist, words);
+    return r != CSA2_OK ? r : csa2_launch_status();
+}
+
+csa2_status block_hist_from_max(const float* bmax, int64_t rows, int64_t ld, const int64_t* n_visible, int block,
+                                uint32_t* hist, cudaStream_t s) {
+    if (ld <= 0) return CSA2_OK;
+    const csa2_status r = launch_pdl(block_hist_kernel, dim3((unsigned)((ld + HIST_CHUNK - 1) / HIST_CHUNK), (unsigned)rows),
+                                     dim3(256), 0, s, bmax, ld, n_visible, block, hist);
+    return r != CSA2_OK ? r : csa2_launch_status();
 }

@@ -32,7 +32,9 @@ def visible_entries(q_pos: torch.Tensor, m: int) -> torch.Tensor:
 class DecodeBuffers:
     """Preallocated outputs of a Full-mode decode step (reused across steps)."""
     block_max: torch.Tensor
+    block_hist: torch.Tensor     # the scan's summary of the block maxima, for the pool
     pool: torch.Tensor
+    top_blocks: torch.Tensor     # the best top_n blocks: the top-k entries lie in them
     cand_scores: torch.Tensor
     idx: torch.Tensor
     out: torch.Tensor
@@ -42,14 +44,24 @@ class DecodeBuffers:
     qI_mx: torch.Tensor          # the indexer query packed to MXFP4 (FP4 QK path)
 
 
+def top_blocks_for(k: int) -> int:
+    """Blocks the top-k selection rescores: the k best blocks hold the top-k entries
+    (every block ranked above a block b holds its maximum, which ranks above every
+    entry of b), rounded up to a whole candidate tile of 32 blocks."""
+    return (k + 31) // 32 * 32
+
+
 def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch.bfloat16,
                  k: int = TOPK, block: int = POOL_BLOCK, n_keep: int = POOL_KEEP,
                  window: int = 128, h_idx: int = 64) -> DecodeBuffers:
     nb = (N + block - 1) // block
+    n_top = top_blocks_for(k)
     return DecodeBuffers(
         block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
+        block_hist=torch.empty((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=device),
         pool=torch.empty((B, Q, n_keep), dtype=torch.int32, device=device),
-        cand_scores=torch.empty((B, Q, n_keep * block), dtype=torch.float32, device=device),
+        top_blocks=torch.empty((B, Q, n_top), dtype=torch.int32, device=device),
+        cand_scores=torch.empty((B, Q, n_top * block), dtype=torch.float32, device=device),
         idx=torch.empty((B, Q, k), dtype=torch.int32, device=device),
         out=torch.empty((B, Q, H, c), dtype=out_dtype, device=device),
         attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
@@ -57,7 +69,7 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
                                                                        swa_cap=window)),
                             dtype=torch.uint8, device=device),
         pool_ws=C._ws(C.csa2_block_pool_workspace_bytes(B * Q, nb, n_keep, torch.device(device).index), device),
-        topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_keep * block, k, torch.device(device).index), device),
+        topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_top * block, k, torch.device(device).index), device),
         qI_mx=torch.empty((B, Q, h_idx, C.mxfp4_row_bytes(128)), dtype=torch.uint8, device=device),
     )
 
@@ -66,9 +78,11 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
                      window: int = 128, swa_pos0: int = 0, k: int = TOPK, block: int = POOL_BLOCK,
                      n_keep: int = POOL_KEEP, flags: int = C.ATTN_DEFAULT):
     """Full layer with the hierarchical pool (CSA2 page, «解码器里的分层索引»):
-    scan all visible entries keeping only block maxima, pick the pool, rescore its
-    candidates, take the top-k (the top-k of all entries lies inside the pool), and
-    attend over the selected entries plus the window.
+    scan all visible entries keeping only block maxima (and their histogram), pick
+    the pool (for the Reindex layers that follow) together with the layer's own best
+    blocks, rescore those blocks' entries, take the top-k (the top-k of all entries
+    lies inside the k best blocks, which lie inside the pool), and attend over the
+    selected entries plus the window.
 
     With an MXFP4 indexer cache the QK product runs in FP4 (DSA-to-CSA/HCA page,
     «Lightning Indexer：公式 (13)–(17)»): a bf16/f32 qI is first packed to MXFP4 by
@@ -76,10 +90,11 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     as given."""
     qI = mxfp4_query(qI, kI, buf.qI_mx)
     C.csa2_index_score(qI, w, kI, n_visible, block=block, want_scores=False, want_block_max=True,
-                       block_max=buf.block_max)
-    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws)
-    C.csa2_index_score(qI, w, kI, n_visible, pool=buf.pool, block=block, scores=buf.cand_scores)
-    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.pool, block=block, out_idx=buf.idx, ws=buf.topk_ws)
+                       block_max=buf.block_max, block_hist=buf.block_hist)
+    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws,
+                      block_hist=buf.block_hist, n_top=buf.top_blocks.shape[-1], out_top=buf.top_blocks)
+    C.csa2_index_score(qI, w, kI, n_visible, pool=buf.top_blocks, block=block, scores=buf.cand_scores)
+    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.top_blocks, block=block, out_idx=buf.idx, ws=buf.topk_ws)
     C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
                        out=buf.out, ws=buf.attn_ws)
     return buf

@@ -212,6 +212,10 @@ csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, in
  *   block_max : [B, Q, ceil(N/block)] f32 or NULL: max over the visible members of
  *               each block of `block` entries (CSA2 page, «解码器里的分层索引»);
  *               blocks with no visible member get -inf
+ *   block_hist: [B, Q, CSA2_BLOCK_HIST_BINS] uint32 or NULL (needs block_max): a
+ *               summary of each row's visible block maxima that csa2_block_pool
+ *               takes to pick its pool with fewer passes (opaque: counts of the
+ *               maxima by their leading bits).  Written in full by this call.
  * Candidate mode (Reindex, CSA2 page «三种模式» and «解码器里的分层索引»):
  *   pool_blocks : [B, Q, n_pool] int32 block ids (-1 = empty slot)
  *   scores      : [B, Q, n_pool*block] f32 (required); candidate c is entry
@@ -226,13 +230,14 @@ csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, in
  * on the same shapes use the bf16/f16 tensor-core scan (exact products, fp32 sums).
  * Everything else runs on the CUDA cores in fp32.
  */
+#define CSA2_BLOCK_HIST_BINS 4096
 csa2_status csa2_index_score(csa2_ctx* ctx,
                              const void* q_idx, csa2_dtype q_dt, const float* w,
                              const void* k_idx, csa2_dtype k_dt,
                              int B, int Q, int64_t N, int H_I, int d_I,
                              const int64_t* n_visible,
                              const int32_t* pool_blocks, int n_pool, int block,
-                             float* scores, float* block_max, void* stream);
+                             float* scores, float* block_max, uint32_t* block_hist, void* stream);
 
 /*
  * csa2_topk -- top-k selection (DSA-to-CSA/HCA page eq. (17)) in one total order:
@@ -265,12 +270,24 @@ size_t csa2_topk_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t n, int k);
  * other blocks by (block max desc, block id asc).  If ceil(V/block) <= n_keep,
  * every visible block is kept; V == 0 gives an all -1 row.
  *   block_max  : [rows, ld] f32 (first ceil(V/block) used)
+ *   block_hist : [rows, CSA2_BLOCK_HIST_BINS] from csa2_index_score over the same
+ *                block maxima, or NULL (then the call builds it in `ws`, if it fits)
  *   n_visible  : [rows] int64 (V per row)
  *   out_blocks : [rows, n_keep] int32 ascending, -1 padded.   1 <= n_keep <= 4096.
+ *   out_top    : [rows, n_top] int32 or NULL: the n_top best visible blocks by
+ *                (block max desc, block asc) -- no block is forced in -- ascending,
+ *                -1 padded.  The top-k entries of the row (k <= n_top) all lie in these
+ *                blocks: every block ranked above a block b holds an entry, its
+ *                maximum, that ranks above every entry of b.  So csa2_topk over the
+ *                candidates of out_top gives the row's top-k.  Needs a histogram
+ *                (block_hist or a workspace that holds one); n_top <= n_keep - 1.
+ * With a histogram the selection reads the maxima once and resolves the threshold
+ * from the histogram; without one it runs the general radix select.
  */
-csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
-                            const int64_t* n_visible, int block, int n_keep,
-                            int32_t* out_blocks, void* ws, size_t ws_bytes, void* stream);
+csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, const uint32_t* block_hist,
+                            int64_t rows, int64_t ld, const int64_t* n_visible, int block, int n_keep,
+                            int32_t* out_blocks, int32_t* out_top, int n_top,
+                            void* ws, size_t ws_bytes, void* stream);
 size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, int n_keep);
 
 /*

@@ -49,7 +49,10 @@ def test_status_strings(lib):
 def test_host_validation_rejects_before_launch(lib):
     # a NULL context is rejected on the host; nothing touches a device
     assert lib.csa2_topk(None, None, 1, 8, 8, None, None, 0, 8, 4, None, None, None, 0, None) == C.ERR_INVALID_ARG
-    assert lib.csa2_block_pool(None, None, 1, 8, None, 8, 16, None, None, 0, None) == C.ERR_INVALID_ARG
+    assert lib.csa2_block_pool(None, None, None, 1, 8, None, 8, 16, None, None, 0, None, 0, None) == \
+        C.ERR_INVALID_ARG
+    assert lib.csa2_index_score(None, None, 0, None, None, 0, 1, 1, 8, 64, 128, None, None, 0, 8, None, None, None,
+                                None) == C.ERR_INVALID_ARG
     assert lib.csa2_topk_workspace_bytes(None, 8, 16384, 512) == 0
     assert lib.csa2_sparse_attn(None, None, 0, None, 0, 0, None, 0, None, 0, 0, 0, 0, None, None, 1, 1, 64, 512,
                                 10000.0, 7, None, 0, None, None, 0, None) == C.ERR_INVALID_ARG

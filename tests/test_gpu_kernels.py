@@ -272,19 +272,51 @@ def test_topk_all_equal_scores():
     np.testing.assert_array_equal(to_np(idx), np.stack([np.arange(512), np.arange(512)]))
 
 
-@pytest.mark.parametrize("V", [0, 1, 8, 9, 100, 8 * 2048, 8 * 2048 + 1, 131071, 1048575])
+@pytest.mark.parametrize("V", [0, 1, 8, 9, 100, 4097, 8 * 2048, 8 * 2048 + 1, 131071, 1048575])
 @pytest.mark.parametrize("ties", [False, True])
-def test_block_pool_bit_exact(V, ties):
+@pytest.mark.parametrize("path", ["histogram", "general"])
+def test_block_pool_bit_exact(V, ties, path):
+    """Both pool selections: from the row histograms (built in the workspace here; the
+    decode step takes them from the scan) with the n_top best blocks as well, and the
+    general radix select (a workspace too small for the histograms).  With ties the
+    threshold bin is crowded, which takes the histogram path's cluster-wide passes."""
     nb_max = (1048575 + 7) // 8
-    n_keep = 2048
+    n_keep, n_top = 2048, 512
     bm = _score_rows(2, nb_max, 71, ties)
     nv = torch.tensor([V, max(V - 5, 0)], dtype=torch.int64, device=DEV)
-    pool = to_np(C.csa2_block_pool(bm, nv, 8, n_keep))
     bmn = bm.double().cpu().numpy()
+    if path == "histogram":
+        pool, top = C.csa2_block_pool(bm, nv, 8, n_keep, n_top=n_top)
+        pool, top = to_np(pool), to_np(top)
+    else:
+        pool = to_np(C.csa2_block_pool(bm, nv, 8, n_keep, ws=torch.empty(16, dtype=torch.uint8, device=DEV)))
     for r in range(2):
         Vr = int(nv[r])
-        ref = O.block_pool(bmn[r][: (Vr + 7) // 8], Vr, 8, n_keep)
+        nb = (Vr + 7) // 8
+        ref = O.block_pool(bmn[r][:nb], Vr, 8, n_keep)
         np.testing.assert_array_equal(pool[r], ref)
+        if path == "histogram":
+            # the n_top best blocks: top-k over the block maxima as scores
+            np.testing.assert_array_equal(top[r], O.topk(bmn[r][:nb], nb, n_top))
+            assert set(top[r][top[r] >= 0].tolist()) <= set(ref[ref >= 0].tolist())
+
+
+def test_block_hist_from_scan_equals_from_maxima():
+    """The FP4 scan's own histogram of the block maxima drives the same selections as
+    the histogram built from the written maxima (the selections themselves are held to
+    the oracle by test_block_pool_bit_exact and the full-size workload tests)."""
+    B, N = 2, 1 << 18
+    ki = torch.stack([C.csa2_fp4_pack(W.fp4_rows("KI", b, 0, N, N, DEV), C.MXFP4_E8M0x32) for b in range(B)])
+    qI = C.csa2_fp4_pack(W.normal_tensor((B, 1, 64, 128), 4301, 0, torch.float32, DEV), C.MXFP4_E8M0x32)
+    w = W.normal_tensor((B, 1, 64), 4302, 0, torch.float32, DEV)
+    nv = torch.tensor([[N - 1], [N - 70000]], dtype=torch.int64, device=DEV)
+    hist = torch.empty((B, 1, C.BLOCK_HIST_BINS), dtype=torch.int32, device=DEV)
+    _, bm = C.csa2_index_score(qI, w, ki, nv, want_scores=False, want_block_max=True, block_hist=hist)
+    p1, t1 = C.csa2_block_pool(bm, nv, 8, 2048, block_hist=hist, n_top=512)
+    p2, t2 = C.csa2_block_pool(bm, nv, 8, 2048, n_top=512)
+    C.csa2_ctx_check()
+    np.testing.assert_array_equal(to_np(p1), to_np(p2))
+    np.testing.assert_array_equal(to_np(t1), to_np(t2))
 
 
 def test_sink_and_worked_example_through_abi(golden):

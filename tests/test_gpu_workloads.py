@@ -235,9 +235,13 @@ def _run_decode_bf16(grid):
         sc = O.index_score(qI, w, K_np, V)
         if grid:
             assert_exact_grid_scores(qI, w, K_np, V, 7)
-            cand = O.pool_candidates(to_np(buf.pool[b, 0]), V)
-            np.testing.assert_array_equal(to_np(buf.cand_scores[b, 0]).reshape(-1)[_cand_slots(buf.pool[b, 0], V)],
+            # the step rescored the entries of its best blocks (buf.top_blocks)
+            cand = O.pool_candidates(to_np(buf.top_blocks[b, 0]), V)
+            np.testing.assert_array_equal(to_np(buf.cand_scores[b, 0]).reshape(-1)[_cand_slots(buf.top_blocks[b, 0], V)],
                                           sc[cand], err_msg=f"{what}: candidate scores")
+            nb = (V + 7) // 8
+            np.testing.assert_array_equal(to_np(buf.top_blocks[b, 0]), O.topk(O.block_max(sc, V, 8), nb, 512),
+                                          err_msg=f"{what}: best blocks")
         sets = _check_selection(what, sc, V, to_np(buf.idx[b, 0]), 512, to_np(buf.pool[b, 0]),
                                 to_np(buf.block_max[b, 0]), exact=grid)
         if not grid:
