@@ -303,8 +303,13 @@ class FP4Decode(Workload):
         C.csa2_fp4_pack(self.qI, C.MXFP4_E8M0x32, out=self.qI_mx)     # the QK path runs in FP4
 
     def main(self):
-        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, want_scores=False,
+        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, scores=self.buf.scores,
                               want_block_max=True, block_max=self.buf.block_max, block_hist=self.buf.block_hist)
+
+    def select(self):
+        b = self.buf
+        _C().csa2_pool_topk(b.block_max, b.block_hist, b.scores, self.nv, self.k, block=self.block,
+                            n_keep=self.n_keep, out=b.pool, out_idx=b.idx)
 
     def scan_bf16_query(self):
         """The other reading of the pages: the bf16 indexer query over the same MXFP4
@@ -344,12 +349,12 @@ class FP4Decode(Workload):
         self.write_rows()
 
     def post(self):
-        self.pool(); self.cand(); self.topk(); self.attn()
+        self.select(); self.attn()
 
     def launches_per_step(self):
-        # compress, 2 packs, scan, pool, candidate scan, top-k, then per 64-head pass of the
-        # attention: query prep, attention, split combine
-        return 7 + 3 * ((self.H + 63) // 64)
+        # compress, 2 packs, histogram zeroing, scan, pool + top-k, then per 64-head pass
+        # of the attention: query prep, attention, split combine
+        return 6 + 3 * ((self.H + 63) // 64)
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
@@ -364,9 +369,8 @@ class FP4Decode(Workload):
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128, "fp4"),
                 ("index scan (bf16 q)", self.scan_bf16_query, B * self.V * 68 + B * self.H_I * (256 + 4),
                  2 * B * self.V * 64 * 128, "bf16"),
-                ("block pool", self.pool, B * ((self.V + 7) // 8) * 4, 0),
-                ("candidate scan", self.cand, B * self.n_top * 8 * 68, 2 * B * self.n_top * 8 * 64 * 128, "fp4"),
-                (f"top-{self.k}", self.topk, B * self.n_top * 8 * 4, 0),
+                (f"pool + top-{self.k}", self.select, B * ((self.V + 7) // 8) * 4 + B * self.n_top * 8 * 4, 0),
+                ("block pool alone", self.pool, B * ((self.V + 7) // 8) * 4, 0),
                 ("sparse attention", self.attn, attn_bytes, attn_flops)]
 
     def queries(self):
@@ -462,8 +466,13 @@ class DecodeBF16(Workload):
                         out_seq_stride=self.N)
 
     def main(self):
-        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, want_scores=False, want_block_max=True,
+        _C().csa2_index_score(self.qI, self.w, self.KI, self.nv, scores=self.buf.scores, want_block_max=True,
                               block_max=self.buf.block_max, block_hist=self.buf.block_hist)
+
+    def select(self):
+        b = self.buf
+        _C().csa2_pool_topk(b.block_max, b.block_hist, b.scores, self.nv, self.k, n_keep=self.n_keep, out=b.pool,
+                            out_idx=b.idx)
 
     def pool(self):
         b = self.buf
@@ -486,10 +495,10 @@ class DecodeBF16(Workload):
         self.write()
 
     def post(self):
-        self.pool(); self.cand(); self.topk(); self.attn()
+        self.select(); self.attn()
 
     def launches_per_step(self):
-        return 9
+        return 8          # compress, zeroing, scan, histogram, pool + top-k, query prep, attention, combine
 
     def main_amount(self):
         return self.B * self.V * 256 + self.B * self.H_I * (128 * 2 + 4)
@@ -498,9 +507,7 @@ class DecodeBF16(Workload):
         B, H = self.B, self.H
         return [("write new row", self.write, B * 3 * 1024, 0),
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128),
-                ("block pool", self.pool, B * (self.V // 8) * 4, 0),
-                ("candidate scan", self.cand, B * 4096 * 256, 2 * B * 4096 * 64 * 128),
-                ("top-512", self.topk, B * 4096 * 4, 0),
+                ("pool + top-512", self.select, B * (self.V // 8) * 4 + B * 4096 * 4, 0),
                 ("sparse attention", self.attn, B * (640 * 1024 + H * 512 * 4), B * H * 640 * 512 * 4)]
 
     def queries(self):

@@ -31,7 +31,7 @@ EXPORTS = (
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
     "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
-    "csa2_compress_varlen",
+    "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist",
 )
 
 
@@ -72,6 +72,8 @@ def _declare(lib):
         "csa2_block_pool": (_i, [_vp, _vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp, _i, _vp, ctypes.c_size_t,
                                  _vp]),
         "csa2_block_pool_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
+        "csa2_block_hist": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _vp, _vp]),
+        "csa2_pool_topk": (_i, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
                                   _i, _i, _i, _i, _f, _u, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
         "csa2_sparse_attn_workspace_bytes": (ctypes.c_size_t, [_vp, _i, _i, _i, _i, _i, _i64, _i64]),
@@ -373,6 +375,42 @@ def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
                                 ws.numel(), _stream(block_max))
     _check("csa2_block_pool", st)
     return (out, out_top) if n_top > 0 else out
+
+
+def csa2_block_hist(block_max, n_visible, block: int = 8, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The histogram of block maxima [..., ld] that csa2_block_pool / csa2_pool_topk take
+    ([..., BLOCK_HIST_BINS] int32 storage)."""
+    ld = block_max.shape[-1]
+    rows = block_max.numel() // ld if ld else 0
+    if out is None:
+        out = torch.empty((*block_max.shape[:-1], BLOCK_HIST_BINS), dtype=torch.int32, device=block_max.device)
+    st = _lib().csa2_block_hist(ctx(block_max.device.index), _p(block_max), rows, ld, _p(n_visible), block, _p(out),
+                                _stream(block_max))
+    _check("csa2_block_hist", st)
+    return out
+
+
+def csa2_pool_topk(block_max, block_hist, scores, n_visible, k: int, block: int = 8, n_keep: int = 2048,
+                   out: Optional[torch.Tensor] = None, out_idx: Optional[torch.Tensor] = None,
+                   out_score: Optional[torch.Tensor] = None, want_scores: bool = False):
+    """Pool and top-k of a Full decode layer from the scan's block maxima [..., ld],
+    their histogram [..., BLOCK_HIST_BINS] and the full scores [..., n_ent]:
+    returns (pool [..., n_keep], idx [..., k], scores of idx or None)."""
+    ld = block_max.shape[-1]
+    rows = block_max.numel() // ld if ld else 0
+    lead = block_max.shape[:-1]
+    n_ent = scores.shape[-1]
+    if out is None:
+        out = torch.empty((*lead, n_keep), dtype=torch.int32, device=block_max.device)
+    if out_idx is None:
+        out_idx = torch.empty((*lead, k), dtype=torch.int32, device=block_max.device)
+    if want_scores and out_score is None:
+        out_score = torch.empty((*lead, k), dtype=torch.float32, device=block_max.device)
+    st = _lib().csa2_pool_topk(ctx(block_max.device.index), _p(block_max), _p(block_hist), _p(scores), rows, ld, n_ent,
+                               _p(n_visible), block, n_keep, k, _p(out), _p(out_idx), _p(out_score),
+                               _stream(block_max))
+    _check("csa2_pool_topk", st)
+    return out, out_idx, out_score
 
 
 def csa2_sparse_attn_workspace_bytes(B: int, Q: int, H: int, k: int, window: int,

@@ -1170,9 +1170,15 @@ struct PoolArgs {
     int block;
     int n_keep;               // pool size: the newest block + n_keep - 1 others
     int32_t* out_pool;        // [rows, n_keep]
-    int n_top;                // 0: no top list
-    int32_t* out_top;         // [rows, n_top]
+    int n_top;                // 0: no top list (with ENTRY: k, the blocks that hold the top-k)
+    int32_t* out_top;         // [rows, n_top] or NULL
     unsigned int* st;
+    // ENTRY: the row's top-k entries from the stored scores of its k best blocks
+    const float* scores;      // [rows, n_ent]
+    int64_t n_ent;            // row stride of scores (>= ld * block)
+    int k;
+    int32_t* out_idx;         // [rows, k]
+    float* out_val;           // [rows, k] or NULL
 };
 
 struct PhShared {
@@ -1180,7 +1186,15 @@ struct PhShared {
     uint32_t start[PH_MAX_C + 1];          // the gathered list: where each CTA's candidates begin
     uint32_t cnt[2][PH_MAX_C][2];          // pushed by every CTA: its (winners, ties at T), per selection
     uint32_t rem[2];                       // ties at T to take (cluster-wide radix passes only)
+    uint32_t tkey;                         // ENTRY: the smallest block maximum among the best blocks
+    uint32_t ecnt;                         // ENTRY: entry candidates pushed into this CTA
+    uint32_t ewin[PH_MAX_C];               // ENTRY: every CTA's number of winning entries
+    uint32_t nown;                         // ENTRY: this CTA's best blocks / own candidates
 };
+constexpr int PH_ECAP = 8192;              // ENTRY: entry candidates a CTA receives (64 KB)
+// ENTRY reuses the two candidate-list arrays: `all` holds PH_ECAP words of indices,
+// `loc` the bitmap of a chunk's entries
+static_assert(2 * PH_CAP * 2 >= PH_ECAP, "the entry lists fit the candidate space");
 
 // Ordered emission of one selection from the CTA's bitmaps: winners (bmW) in index
 // order, ties (bmE) while fewer than `quota` have been taken, at out[off + rank].
@@ -1216,11 +1230,45 @@ __device__ void ph_emit(const uint32_t* bmW, const uint32_t* bmE, int nwords, in
     }
 }
 
+// Remote atomic add in CTA `rank`'s shared memory (cluster address from cl_map).
+__device__ __forceinline__ uint32_t cl_atomic_add(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
+// One selection pass over bitmap words in index order: thread t owns a run of words;
+// bit j of word w (id base + 32 w + j) goes to out[off + its rank] while below out_len.
+__device__ void ph_emit_bits(const uint32_t* bm, int nwords, int64_t base, uint32_t off, int32_t* out,
+                             float* outv, const float* vals, uint32_t out_len, ClShared& sh) {
+    const int tid = threadIdx.x;
+    const int per = (nwords + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    uint32_t cg = 0;
+    for (int w = w0; w < w1; ++w) cg += __popc(bm[w]);
+    uint32_t tot;
+    uint32_t pos = off + block_excl_scan_u32(cg, sh, tot);
+    for (int w = w0; w < w1; ++w) {
+        uint32_t bits = bm[w];
+        while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (pos < out_len) {
+                const int64_t id = base + w * 32 + j;
+                out[pos] = (int32_t)id;
+                if (outv) outv[pos] = vals[id];
+            }
+            ++pos;
+        }
+    }
+}
+
+template <bool ENTRY>
 __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int chunk) {
     extern __shared__ __align__(16) uint32_t dyn[];
     __shared__ ClShared sh;
     __shared__ PhShared px;
-    pdl_wait();                            // the block maxima and the histogram are complete
+    pdl_wait();                            // the block maxima, histogram and scores are complete
     const uint32_t C = cl_size(), rank = cl_rank();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t row = blockIdx.y;
@@ -1230,17 +1278,17 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         if (tid == 0 && rank == 0) csa2_flag(a.st, CSA2_DEVBIT_RANGE);
         nb = a.ld;
     }
-    const bool doT = a.out_top != nullptr && a.n_top > 0;
+    const bool doT = ENTRY || (a.out_top != nullptr && a.n_top > 0);
     const bool allP = nb <= a.n_keep, allT = !doT || nb <= a.n_top;
     int32_t* outP = a.out_pool + row * a.n_keep;
-    int32_t* outT = doT ? a.out_top + row * a.n_top : nullptr;
+    int32_t* outT = a.out_top ? a.out_top + row * a.n_top : nullptr;
     const int bd = CL_THREADS;
     // every visible block fits: ascending ids, then -1
     if (allP)
         for (int64_t i = (int64_t)rank * bd + tid; i < a.n_keep; i += (int64_t)C * bd) outP[i] = i < nb ? (int32_t)i : -1;
-    if (doT && allT)
+    if (outT && allT)
         for (int64_t i = (int64_t)rank * bd + tid; i < a.n_top; i += (int64_t)C * bd) outT[i] = i < nb ? (int32_t)i : -1;
-    if (allP && allT) {                    // the same for every CTA of the row: no barrier used
+    if (!ENTRY && allP && allT) {          // the same for every CTA of the row: no barrier used
         pdl_trigger();
         return;
     }
@@ -1256,14 +1304,19 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         const int i = tid + j * bd;
         v[j] = i < n ? rowp[i] : 0.0f;
     }
+    const bool need_hist = !allP || !allT;
     const uint32_t* hrow = a.hist + row * NB_A;
     uint32_t hv[NB_A / CL_THREADS];
 #pragma unroll
-    for (int j = 0; j < NB_A / CL_THREADS; ++j) hv[j] = hrow[tid + j * bd];
-    const uint32_t knew = order_key(a.bmax[row * a.ld + newest]);
+    for (int j = 0; j < NB_A / CL_THREADS; ++j) hv[j] = need_hist ? hrow[tid + j * bd] : 0u;
+    const uint32_t knew = nb > 0 ? order_key(a.bmax[row * a.ld + newest]) : 0u;
 #pragma unroll
     for (int j = 0; j < NB_A / CL_THREADS; ++j) sh.full[tid + j * bd] = hv[j];
     if (tid < 2) px.nloc[tid] = 0u;
+    if (tid == 0) {
+        px.ecnt = 0u;
+        px.tkey = 1u;                      // take-all: every valid key (keys are never 0)
+    }
     __syncthreads();
     // the threshold bins of both selections
     const uint32_t k[2] = {(uint32_t)a.n_keep - 1u, (uint32_t)a.n_top};
@@ -1284,8 +1337,9 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     // classify: the 32 keys of word w = i / 32 are lanes of one warp in one step
     const int cw = chunk / 32;
     const int nwords = (n + 31) / 32;
-    uint32_t* skey = dyn;                                  // [chunk]
-    uint32_t* bmW = dyn + chunk;                           // [2][cw]
+    const int skey_words = ENTRY ? max(chunk, 2 * PH_ECAP) : chunk;
+    uint32_t* skey = dyn;                                  // [skey_words]; ENTRY: then the received entries
+    uint32_t* bmW = dyn + skey_words;                      // [2][cw]
     uint32_t* bmE = bmW + 2 * cw;                          // [2][cw]
     uint64_t* loc = reinterpret_cast<uint64_t*>(bmE + 2 * cw);   // [2][PH_CAP] this CTA's candidates
     uint64_t* all = loc + 2 * PH_CAP;                      // [2][PH_CAP] every CTA's, gathered
@@ -1301,7 +1355,8 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         const bool v0 = act[0] && key != 0u && c0 + i != newest, v1 = act[1] && key != 0u;
         const unsigned g0 = __ballot_sync(FULL_MASK, v0 && d > bin[0]);
         const unsigned e0 = __ballot_sync(FULL_MASK, v0 && d == bin[0]);
-        const unsigned g1 = __ballot_sync(FULL_MASK, v1 && d > bin[1]);
+        // ENTRY with every block among the best: every visible block of the chunk is one
+        const unsigned g1 = __ballot_sync(FULL_MASK, (v1 && d > bin[1]) || (ENTRY && !act[1] && key != 0u));
         const unsigned e1 = __ballot_sync(FULL_MASK, v1 && d == bin[1]);
         if (lane == 0) {
             bmW[w] = g0;
@@ -1320,6 +1375,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         }
     }
     cl_sync();                             // (1) every CTA's candidate list is complete
+    bool any_radix = false;
 #pragma unroll 1
     for (int s2 = 0; s2 < 2; ++s2) {
         if (!act[s2]) continue;
@@ -1364,9 +1420,20 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                     atomicOr(&W[li >> 5], 1u << (li & 31));
                 }
             }
+            // the last winner may be another CTA's candidate: every CTA ranks the whole
+            // gathered list for it (a few hundred keys)
+            if (ENTRY && s2 == 1) {
+                for (uint32_t j = tid; j < mm; j += bd) {
+                    const uint64_t x = A[j];
+                    uint32_t ahead = 0u;
+                    for (uint32_t i = 0; i < mm; ++i) ahead += A[i] > x;
+                    if (ahead == r - 1) px.tkey = (uint32_t)(x >> 32);
+                }
+            }
         } else {
             // a crowded threshold bin: the remaining two digits cluster-wide, then the
             // ties at T by index
+            any_radix = true;
             uint32_t prefix = (uint32_t)bin[s2] << 20, rr = r;
             for (int pass = 0; pass < 2; ++pass) {
                 const int shift = pass == 0 ? 10 : 0;
@@ -1396,6 +1463,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                 if (key > prefix) atomicOr(&W[i >> 5], 1u << (i & 31));
                 else if (key == prefix) atomicOr(&E[i >> 5], 1u << (i & 31));
             }
+            if (ENTRY && s2 == 1 && tid == 0) px.tkey = prefix;
         }
         if (s2 == 0 && newest >= c0 && newest < c0 + n) {   // the pool always keeps the newest block
             const int li = (int)(newest - c0);
@@ -1429,10 +1497,89 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         }
         __syncthreads();
     }
-    cl_sync();                             // (2) every CTA's counts are in every CTA
+    if (ENTRY) {
+        // ---- the row's top-k entries: every entry of this CTA's best blocks that
+        // scores at least the smallest best-block maximum is a candidate; each CTA
+        // pushes its candidates into every CTA, then ranks its own against all of them
+        uint32_t* W = bmW + cw;
+        if (any_radix) {
+            // the crowded case: the ties at T taken (lowest index first) become best
+            // blocks once every CTA's counts are in; the barrier also ends every use of
+            // skey before entries are pushed into it
+            cl_sync();
+            if (act[1] && m[1] > (uint32_t)PH_CAP && tid == 0) {
+                uint32_t tb = 0u;
+                for (uint32_t c = 0; c < rank; ++c) tb += px.cnt[1][c][1];
+                const uint32_t rem = px.rem[1];
+                uint32_t quota = rem > tb ? min(rem - tb, px.cnt[1][rank][1]) : 0u;
+                const uint32_t* E = bmE + cw;
+                for (int w = 0; w < nwords && quota; ++w) {
+                    uint32_t e = E[w];
+                    while (e && quota) {
+                        const int j = __ffs(e) - 1;
+                        e &= e - 1;
+                        W[w] |= 1u << j;
+                        --quota;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        // this CTA's best blocks, compacted into `all` (free now) in index order
+        uint32_t* blist = reinterpret_cast<uint32_t*>(all);
+        {
+            const int per = (nwords + bd - 1) / bd;
+            const int w0 = tid * per, w1 = min(nwords, w0 + per);
+            uint32_t cnt = 0;
+            for (int w = w0; w < w1; ++w) cnt += __popc(W[w]);
+            uint32_t tot;
+            uint32_t o = block_excl_scan_u32(cnt, sh, tot);
+            for (int w = w0; w < w1; ++w) {
+                uint32_t bits = W[w];
+                while (bits) {
+                    const int j = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    if (o < 2u * PH_CAP) blist[o] = (uint32_t)(w * 32 + j);
+                    ++o;
+                }
+            }
+            if (tid == 0) px.nown = min(tot, 2u * (uint32_t)PH_CAP);
+        }
+        __syncthreads();
+        const uint32_t tkey = px.tkey, nown = px.nown;
+        const float* srow = a.scores + row * a.n_ent;
+        for (uint32_t t0 = 0; t0 < nown * (uint32_t)a.block; t0 += bd) {
+            const uint32_t t = t0 + tid;
+            bool keep = false;
+            uint32_t key = 0u;
+            int64_t e = 0;
+            if (t < nown * (uint32_t)a.block) {
+                e = (c0 + blist[t / a.block]) * a.block + t % a.block;
+                if (e < V) {
+                    key = order_key(srow[e]);
+                    keep = key >= tkey;
+                }
+            }
+            const unsigned km = __ballot_sync(FULL_MASK, keep);
+            if (!km) continue;
+            const uint64_t cand = ((uint64_t)key << 32) | (uint32_t)e;
+            for (uint32_t c = 0; c < C; ++c) {
+                uint32_t o = 0u;
+                if (lane == 0) o = cl_atomic_add(cl_map(&px.ecnt, c), (uint32_t)__popc(km));
+                o = __shfl_sync(FULL_MASK, o, 0) + __popc(km & lt);
+                if (keep && o < (uint32_t)PH_ECAP) {
+                    const uint32_t dst = cl_map(skey, c) + 8u * o;
+                    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"((uint32_t)cand),
+                                 "r"((uint32_t)(cand >> 32)) : "memory");
+                }
+            }
+        }
+    }
+    cl_sync();                             // (2) every CTA's counts (and entry candidates) are in every CTA
 #pragma unroll 1
     for (int s2 = 0; s2 < 2; ++s2) {
         if (!act[s2]) continue;
+        if (s2 == 1 && !outT) continue;
         uint32_t off = 0u, ties_before = 0u, total = 0u, quota = 0u;
         const uint32_t rem = px.rem[s2];
         for (uint32_t c = 0; c < C; ++c) {
@@ -1449,8 +1596,66 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         for (int64_t i = (int64_t)total + (int64_t)rank * bd + tid; i < out_len; i += (int64_t)C * bd) out[i] = -1;
         __syncthreads();
     }
+    if (ENTRY) {
+        // rank this CTA's own entry candidates (entries of its chunk) against all
+        // received ones; the winners go to a bitmap over the chunk's entries (in `loc`,
+        // which no CTA reads after barrier (2))
+        const uint32_t me = min(px.ecnt, (uint32_t)PH_ECAP);
+        const uint64_t* ec = reinterpret_cast<const uint64_t*>(skey);
+        uint32_t* ebm = reinterpret_cast<uint32_t*>(loc);
+        const int ew = (chunk * a.block + 31) / 32;
+        for (int i = tid; i < ew; i += bd) ebm[i] = 0u;
+        if (tid == 0) px.nown = 0u;
+        __syncthreads();
+        const int64_t e0 = c0 * a.block, e1 = (c0 + n) * a.block;
+        uint32_t* olist = reinterpret_cast<uint32_t*>(all);     // this CTA's candidates (slots of ec)
+        for (uint32_t j = tid; j < me; j += bd) {
+            const int64_t e = (int64_t)(uint32_t)ec[j];
+            if (e >= e0 && e < e1) {
+                const uint32_t o = atomicAdd(&px.nown, 1u);
+                if (o < (uint32_t)PH_ECAP) olist[o] = j;          // `all` holds PH_ECAP words
+            }
+        }
+        __syncthreads();
+        const uint32_t no = min(px.nown, (uint32_t)PH_ECAP);
+        for (uint32_t ci = wid; ci < no; ci += CL_THREADS / 32) {
+            const uint64_t x = ec[olist[ci]] ^ 0xFFFFFFFFull;
+            uint32_t ahead = 0u;
+            for (uint32_t j = lane; j < me; j += 32) ahead += (ec[j] ^ 0xFFFFFFFFull) > x;
+            ahead = __reduce_add_sync(FULL_MASK, ahead);
+            if (lane == 0 && ahead < (uint32_t)a.k) {
+                const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - e0);
+                atomicOr(&ebm[li >> 5], 1u << (li & 31));
+            }
+        }
+        __syncthreads();
+        uint32_t cwin = 0u;
+        for (int w = tid; w < ew; w += bd) cwin += __popc(ebm[w]);
+        cwin = __reduce_add_sync(FULL_MASK, cwin);
+        __shared__ uint32_t esum[CL_THREADS / 32];
+        if (lane == 0) esum[wid] = cwin;
+        __syncthreads();
+        if (tid < (int)C) {
+            uint32_t tw = 0u;
+            for (int i = 0; i < CL_THREADS / 32; ++i) tw += esum[i];
+            cl_st(cl_map(&px.ewin[rank], (uint32_t)tid), tw);
+        }
+        cl_sync();                         // (3) every CTA's winner count is in every CTA
+        uint32_t off = 0u, total = 0u;
+        for (uint32_t c = 0; c < C; ++c) {
+            if (c < rank) off += px.ewin[c];
+            total += px.ewin[c];
+        }
+        int32_t* oi = a.out_idx + row * a.k;
+        float* ov = a.out_val ? a.out_val + row * a.k : nullptr;
+        ph_emit_bits(ebm, ew, e0, off, oi, ov, a.scores + row * a.n_ent, (uint32_t)a.k, sh);
+        for (int64_t i = (int64_t)total + (int64_t)rank * bd + tid; i < a.k; i += (int64_t)C * bd) {
+            oi[i] = -1;
+            if (ov) ov[i] = -INFINITY;
+        }
+    }
     pdl_trigger();
-    // no CTA touches another's shared memory after barrier (2): each may leave now
+    // no CTA touches another's shared memory after its last barrier: each may leave now
 }
 
 // Counts of the first radix digit of the visible block maxima (a CTA per chunk of a
@@ -1491,21 +1696,25 @@ int pool_cluster_size(const csa2_ctx* ctx, int64_t rows, int64_t ld) {
     return 16;
 }
 
-size_t pool_hist_smem(int chunk) {
-    return (size_t)chunk * 4 + (size_t)chunk / 32 * 16 + 4ull * PH_CAP * 8;
+size_t pool_hist_smem(int chunk, bool entry) {
+    const int skey_words = entry ? std::max(chunk, 2 * PH_ECAP) : chunk;
+    return (size_t)skey_words * 4 + (size_t)chunk / 32 * 16 + 4ull * PH_CAP * 8;
 }
 
+template <bool ENTRY>
 csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cudaStream_t s) {
     const int C = pool_cluster_size(ctx, rows, a.ld);
     const int chunk = (int)(((a.ld + C - 1) / C + CL_THREADS - 1) / CL_THREADS * CL_THREADS);
     if (chunk > CL_MAX_CHUNK) return CSA2_ERR_UNSUPPORTED;
-    const size_t smem = pool_hist_smem(chunk);
+    // ENTRY: the bitmap of a chunk's entries lives in the candidate lists' space
+    if (ENTRY && ((size_t)chunk * a.block + 31) / 32 * 4 > 2ull * PH_CAP * 8) return CSA2_ERR_UNSUPPORTED;
+    const size_t smem = pool_hist_smem(chunk, ENTRY);
+    auto kern = pool_hist_kernel<ENTRY>;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(pool_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pool_hist_smem(CL_MAX_CHUNK)) != cudaSuccess ||
-            cudaFuncSetAttribute(pool_hist_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pool_hist_smem(CL_MAX_CHUNK, ENTRY)) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return CSA2_ERR_CUDA;
         attr = true;
     }
@@ -1523,7 +1732,7 @@ csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cud
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, pool_hist_kernel, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, a, chunk) != cudaSuccess) return CSA2_ERR_CUDA;
     return csa2_launch_status();
 }
 
@@ -1693,7 +1902,12 @@ extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, co
         p.n_top = n_top;
         p.out_top = n_top > 0 ? out_top : nullptr;
         p.st = ctx->status;
-        return launch_pool_hist(ctx, p, rows, s);
+        p.scores = nullptr;
+        p.n_ent = 0;
+        p.k = 0;
+        p.out_idx = nullptr;
+        p.out_val = nullptr;
+        return launch_pool_hist<false>(ctx, p, rows, s);
     }
     if (n_top > 0) return CSA2_ERR_UNSUPPORTED;   // the top blocks need a histogram
     SelArgs a;
@@ -1710,6 +1924,51 @@ extern "C" csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, co
     a.out_val = nullptr;
     a.st = ctx->status;
     return run_select<SEL_POOL>(ctx, a, rows, ld, ws, ws_bytes, s);
+}
+
+extern "C" csa2_status csa2_pool_topk(csa2_ctx* ctx, const float* block_max, const uint32_t* block_hist,
+                                      const float* scores, int64_t rows, int64_t ld, int64_t n_ent,
+                                      const int64_t* n_visible, int block, int n_keep, int k, int32_t* out_blocks,
+                                      int32_t* out_idx, float* out_score, void* stream) {
+    if (!ctx || rows < 0 || ld < 0 || block < 1 || block > 32 || n_keep < 2 || n_keep > 4096 || k < 1)
+        return CSA2_ERR_INVALID_ARG;
+    if (rows == 0) return CSA2_OK;
+    if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (!block_max || !block_hist || !scores || !n_visible || !out_blocks || !out_idx || ld <= 0 ||
+        n_ent < ld * block || !aligned(block_hist, 16))
+        return CSA2_ERR_INVALID_ARG;
+    // every entry of the k best blocks may be a candidate: they must fit the receive buffer
+    if ((int64_t)k * block > PH_ECAP || k > n_keep - 1) return CSA2_ERR_UNSUPPORTED;
+    if (((ld + PH_MAX_C - 1) / PH_MAX_C + CL_THREADS - 1) / CL_THREADS * CL_THREADS > CL_MAX_CHUNK)
+        return CSA2_ERR_UNSUPPORTED;
+    PoolArgs p;
+    p.bmax = block_max;
+    p.ld = ld;
+    p.nv = n_visible;
+    p.hist = block_hist;
+    p.block = block;
+    p.n_keep = n_keep;
+    p.out_pool = out_blocks;
+    p.n_top = k;
+    p.out_top = nullptr;
+    p.st = ctx->status;
+    p.scores = scores;
+    p.n_ent = n_ent;
+    p.k = k;
+    p.out_idx = out_idx;
+    p.out_val = out_score;
+    return launch_pool_hist<true>(ctx, p, rows, as_stream(stream));
+}
+
+extern "C" csa2_status csa2_block_hist(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
+                                       const int64_t* n_visible, int block, uint32_t* block_hist, void* stream) {
+    if (!ctx || rows < 0 || ld < 0 || block < 1) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0) return CSA2_OK;
+    if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (!block_max || !n_visible || !block_hist || !aligned(block_hist, 16)) return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    const csa2_status r = block_hist_zero(block_hist, rows, s);
+    return r != CSA2_OK ? r : block_hist_from_max(block_max, rows, ld, n_visible, block, block_hist, s);
 }
 
 csa2_status block_hist_zero(uint32_t* hist, int64_t rows, cudaStream_t s) {

@@ -31,6 +31,7 @@ def visible_entries(q_pos: torch.Tensor, m: int) -> torch.Tensor:
 @dataclass
 class DecodeBuffers:
     """Preallocated outputs of a Full-mode decode step (reused across steps)."""
+    scores: torch.Tensor         # the full scan's scores (the top-k reads its best blocks' entries)
     block_max: torch.Tensor
     block_hist: torch.Tensor     # the scan's summary of the block maxima, for the pool
     pool: torch.Tensor
@@ -57,6 +58,7 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
     nb = (N + block - 1) // block
     n_top = top_blocks_for(k)
     return DecodeBuffers(
+        scores=torch.empty((B, Q, N), dtype=torch.float32, device=device),
         block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
         block_hist=torch.empty((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=device),
         pool=torch.empty((B, Q, n_keep), dtype=torch.int32, device=device),
@@ -78,26 +80,37 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
                      window: int = 128, swa_pos0: int = 0, k: int = TOPK, block: int = POOL_BLOCK,
                      n_keep: int = POOL_KEEP, flags: int = C.ATTN_DEFAULT):
     """Full layer with the hierarchical pool (CSA2 page, «解码器里的分层索引»):
-    scan all visible entries keeping only block maxima (and their histogram), pick
-    the pool (for the Reindex layers that follow) together with the layer's own best
-    blocks, rescore those blocks' entries, take the top-k (the top-k of all entries
-    lies inside the k best blocks, which lie inside the pool), and attend over the
-    selected entries plus the window.
+    scan all visible entries (scores, block maxima and their histogram), pick the
+    pool (for the Reindex layers that follow) and the layer's own top-k in one call
+    (the top-k of all entries lies inside the k best blocks, which lie inside the
+    pool), and attend over the selected entries plus the window.  Shapes that call
+    does not take run the pool, the best blocks' rescoring and the top-k one by one.
 
     With an MXFP4 indexer cache the QK product runs in FP4 (DSA-to-CSA/HCA page,
     «Lightning Indexer：公式 (13)–(17)»): a bf16/f32 qI is first packed to MXFP4 by
     the same rule as the keys (into buf.qI_mx); an already packed uint8 qI is used
     as given."""
     qI = mxfp4_query(qI, kI, buf.qI_mx)
-    C.csa2_index_score(qI, w, kI, n_visible, block=block, want_scores=False, want_block_max=True,
+    C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores, want_block_max=True,
                        block_max=buf.block_max, block_hist=buf.block_hist)
-    C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws,
-                      block_hist=buf.block_hist, n_top=buf.top_blocks.shape[-1], out_top=buf.top_blocks)
-    C.csa2_index_score(qI, w, kI, n_visible, pool=buf.top_blocks, block=block, scores=buf.cand_scores)
-    C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.top_blocks, block=block, out_idx=buf.idx, ws=buf.topk_ws)
+    if pool_topk_applies(k, block, n_keep, buf.block_max.shape[-1]):
+        C.csa2_pool_topk(buf.block_max, buf.block_hist, buf.scores, n_visible, k, block=block, n_keep=n_keep,
+                         out=buf.pool, out_idx=buf.idx)
+    else:
+        C.csa2_block_pool(buf.block_max, n_visible, block=block, n_keep=n_keep, out=buf.pool, ws=buf.pool_ws,
+                          block_hist=buf.block_hist, n_top=buf.top_blocks.shape[-1], out_top=buf.top_blocks)
+        C.csa2_index_score(qI, w, kI, n_visible, pool=buf.top_blocks, block=block, scores=buf.cand_scores)
+        C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.top_blocks, block=block, out_idx=buf.idx,
+                    ws=buf.topk_ws)
     C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
                        out=buf.out, ws=buf.attn_ws)
     return buf
+
+
+def pool_topk_applies(k: int, block: int, n_keep: int, n_blocks: int) -> bool:
+    """The shapes csa2_pool_topk takes (its header states them)."""
+    chunk = -(-(-(-n_blocks // 16)) // 1024) * 1024
+    return 1 <= k <= n_keep - 1 and k * block <= 8192 and block <= 16 and chunk <= 16384
 
 
 def mxfp4_query(qI, kI, out=None):

@@ -290,6 +290,34 @@ csa2_status csa2_block_pool(csa2_ctx* ctx, const float* block_max, const uint32_
                             void* ws, size_t ws_bytes, void* stream);
 size_t csa2_block_pool_workspace_bytes(csa2_ctx* ctx, int64_t rows, int64_t ld, int n_keep);
 
+/* The histogram csa2_index_score writes beside the block maxima, built from block
+   maxima that came from elsewhere ([rows, ld] f32, n_visible entries per row):
+   block_hist [rows, CSA2_BLOCK_HIST_BINS] uint32 (16-byte aligned), written in full. */
+csa2_status csa2_block_hist(csa2_ctx* ctx, const float* block_max, int64_t rows, int64_t ld,
+                            const int64_t* n_visible, int block, uint32_t* block_hist, void* stream);
+
+/*
+ * csa2_pool_topk -- the selections of a Full decode layer in one call: the block pool
+ * of csa2_block_pool (for the Reindex layers that follow) and the layer's own top-k
+ * entries (DSA-to-CSA/HCA page eq. (17); CSA2 page, «解码器里的分层索引»), from the
+ * scan's block maxima, their histogram and the stored entry scores.  The top-k entries
+ * lie in the k best blocks (every block ranked above a block b holds an entry, its
+ * maximum, that ranks above every entry of b), and each of them scores at least the
+ * smallest of those k maxima, so only those blocks' entries above that value are
+ * ranked; the result equals csa2_topk over all the row's scores.
+ *   block_max, block_hist : as csa2_block_pool (block_hist from csa2_index_score)
+ *   scores     : [rows, n_ent] f32, the full-scan scores (entries < n_visible read)
+ *   out_blocks : [rows, n_keep] int32 (the pool);  out_idx : [rows, k] int32 entry
+ *                ids ascending, -1 padded;  out_score : [rows, k] f32 or NULL
+ * 2 <= n_keep <= 4096, 1 <= k <= n_keep - 1, k * block <= 8192, block <= 16,
+ * ld <= 262,144.  Other shapes return CSA2_ERR_UNSUPPORTED (csa2_block_pool and
+ * csa2_topk serve them).
+ */
+csa2_status csa2_pool_topk(csa2_ctx* ctx, const float* block_max, const uint32_t* block_hist,
+                           const float* scores, int64_t rows, int64_t ld, int64_t n_ent,
+                           const int64_t* n_visible, int block, int n_keep, int k,
+                           int32_t* out_blocks, int32_t* out_idx, float* out_score, void* stream);
+
 /*
  * csa2_sparse_attn -- shared-KV MQA over the selected compressed entries plus the
  * sliding window (DSA-to-CSA/HCA page eqs. (18)-(19), (27), «因果边界与短滑窗»;

@@ -516,3 +516,28 @@ def test_rope_angles_at_large_positions(pos):
     for b in range(B):
         ref = O.rope(C_[b, 0].double().cpu().numpy(), int(pos0[b]))
         np.testing.assert_allclose(to_np(out)[b, 0], ref, rtol=0, atol=2e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("V", [1, 9, 4000, 4097, 8 * 2048, 8 * 2048 + 1, 262143])
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("k", [512, 1024])
+def test_pool_topk_bit_exact(V, ties, k):
+    """csa2_pool_topk: the pool and the top-k entries from block maxima, their
+    histogram and the full scores -- both bit-exact with the oracle's block_pool and
+    topk over the same scores, ties and crowded threshold bins included."""
+    N = 262144
+    s = _score_rows(3, N, 81 + V, ties)
+    nv = torch.tensor([V, max(V - 7, 0), min(V + 3, N)], dtype=torch.int64, device=DEV)
+    sn = s.double().cpu().numpy()
+    # the block maxima are the oracle's own; the library summarises them
+    bm = torch.tensor(np.stack([O.block_max(np.where(np.arange(N) < int(nv[r]), sn[r], -np.inf), N, 8)
+                                for r in range(3)]), dtype=torch.float32, device=DEV)
+    hist = C.csa2_block_hist(bm, nv, 8)
+    pool, idx, val = C.csa2_pool_topk(bm, hist, s, nv, k, want_scores=True)
+    C.csa2_ctx_check()
+    for r in range(3):
+        Vr = int(nv[r])
+        np.testing.assert_array_equal(to_np(pool)[r], O.block_pool(O.block_max(sn[r], Vr, 8), Vr, 8, 2048))
+        ref = O.topk(sn[r], Vr, k)
+        np.testing.assert_array_equal(to_np(idx)[r], ref, err_msg=f"row {r} V {Vr}")
+        np.testing.assert_array_equal(to_np(val)[r], np.where(ref >= 0, sn[r][np.maximum(ref, 0)], -np.inf))

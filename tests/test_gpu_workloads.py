@@ -145,9 +145,9 @@ def _fp4_kv_row(b, N):
 
 
 def _run_fp4_decode(B, N, H, k, grid):
-    """The bench's FP4 decode step (new-token rows, query pack, full scan with block
-    max, pool, candidate rescoring, top-k, attention into bf16), then every sequence
-    through the oracle."""
+    """The bench's FP4 decode step (new-token rows, query pack, full scan with scores,
+    block maxima and their histogram, pool + top-k, attention into bf16), then every
+    sequence through the oracle."""
     wl = W.fp4_decode(DEV, B=B, N=N, H=H, grid=grid)
     kv, ki = _fp4_caches(B, N, grid)
     t = N - 1
@@ -175,6 +175,9 @@ def _run_fp4_decode(B, N, H, k, grid):
         np.testing.assert_array_equal(to_np(buf.qI_mx[b, 0]), qI_ref, err_msg=f"{what}: MXFP4 query bytes")
         if grid:
             assert_exact_grid_scores(O.mxfp4_unpack(qI_ref), _np(wl["w"][b, 0]), O.mxfp4_unpack(ki_ref), V, 3)
+            np.testing.assert_array_equal(to_np(buf.scores[b, 0])[:V], sc[:V], err_msg=f"{what}: scores")
+        else:
+            assert_close(to_np(buf.scores[b, 0])[:V], sc[:V], 1e-5, f"{what}: scores")
         sets = _check_selection(what, sc, V, to_np(buf.idx[b, 0]), k, to_np(buf.pool[b, 0]),
                                 to_np(buf.block_max[b, 0]), exact=grid)
         rows = _RowMap(_fp4_kv_row(b, N))
@@ -233,15 +236,12 @@ def _run_decode_bf16(grid):
         K_np = _np(wl["KI"][b])
         qI, w = _np(wl["qI"][b, 0]), _np(wl["w"][b, 0])
         sc = O.index_score(qI, w, K_np, V)
+        # the step's full scan scores (the top-k reads its best blocks' entries from them)
         if grid:
             assert_exact_grid_scores(qI, w, K_np, V, 7)
-            # the step rescored the entries of its best blocks (buf.top_blocks)
-            cand = O.pool_candidates(to_np(buf.top_blocks[b, 0]), V)
-            np.testing.assert_array_equal(to_np(buf.cand_scores[b, 0]).reshape(-1)[_cand_slots(buf.top_blocks[b, 0], V)],
-                                          sc[cand], err_msg=f"{what}: candidate scores")
-            nb = (V + 7) // 8
-            np.testing.assert_array_equal(to_np(buf.top_blocks[b, 0]), O.topk(O.block_max(sc, V, 8), nb, 512),
-                                          err_msg=f"{what}: best blocks")
+            np.testing.assert_array_equal(to_np(buf.scores[b, 0])[:V], sc[:V], err_msg=f"{what}: scores")
+        else:
+            assert_close(to_np(buf.scores[b, 0])[:V], sc[:V], 1e-5, f"{what}: scores")
         sets = _check_selection(what, sc, V, to_np(buf.idx[b, 0]), 512, to_np(buf.pool[b, 0]),
                                 to_np(buf.block_max[b, 0]), exact=grid)
         if not grid:
