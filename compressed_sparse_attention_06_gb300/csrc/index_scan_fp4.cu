@@ -15,7 +15,9 @@
 // query's codes (shared memory), SFA / SFB their E8M0 scales in tensor memory, D in
 // fp32 tensor memory.  The block max over 8 entries (CSA2 page, «解码器里的分层索引»)
 // is fused into the epilogue, or the tile is a list of 32 pooled candidate blocks
-// (Reindex).
+// (Reindex).  On request each CTA ends by counting the leading 12 key bits of its
+// visible block maxima into a per-row histogram, which the pool's selection starts
+// from.
 //
 // One CTA per SM (the grid splits each query's tiles over the SMs), 22 warps:
 //   warp 0       producer, into an 8-stage ring of tiles.  Full scan: a tile is
@@ -186,8 +188,6 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
             make_uint4(ld_u32(src), ld_u32(src + 4), ld_u32(src + 8), ld_u32(src + 12));
     }
     for (int h = threadIdx.x; h < HEADS; h += THREADS) sW[h] = a.w[(int64_t)g * HEADS + h];
-    if (!CAND && a.hist)
-        for (int i = threadIdx.x; i < CSA2_BLOCK_HIST_BINS; i += THREADS) sHist[i] = 0u;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -369,11 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    if ((lane & 7) == 0 && (e >> 3) < nb) {
-                        a.bmax[(int64_t)g * nb + (e >> 3)] = m;
-                        // the pool's first radix digit of every visible block's maximum
-                        if (a.hist && m != -INFINITY) atomicAdd(&sHist[order_key(m) >> 20], 1u);
-                    }
+                    if ((lane & 7) == 0 && (e >> 3) < nb) a.bmax[(int64_t)g * nb + (e >> 3)] = m;
                 }
             }
         }
@@ -393,8 +389,27 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
-    // this CTA's block-max digit counts into the row's histogram
+    // the first radix digit of this CTA's visible block maxima, counted once every tile
+    // is done (counting them in the epilogue stalled the pipeline), into the row's
+    // histogram: the maxima are read back eight at a time, all in flight together
     if (!CAND && a.hist) {
+        for (int i = threadIdx.x; i < CSA2_BLOCK_HIST_BINS; i += THREADS) sHist[i] = 0u;
+        __syncthreads();
+        const int64_t nbv = (V + 7) / 8, b0 = (int64_t)t_begin * (TILE / 8);
+        const int64_t b1 = min(nbv, (int64_t)t_end * (TILE / 8));
+        const float* brow = a.bmax + (int64_t)g * ((a.N + 7) / 8);
+        for (int64_t base = b0; base < b1; base += 8 * THREADS) {
+            float mv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int64_t bi = base + j * THREADS + threadIdx.x;
+                mv[j] = bi < b1 ? brow[bi] : -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (mv[j] != -INFINITY) atomicAdd(&sHist[order_key(mv[j]) >> 20], 1u);
+        }
+        __syncthreads();
         uint32_t* hrow = a.hist + (int64_t)g * CSA2_BLOCK_HIST_BINS;
         for (int i = threadIdx.x; i < CSA2_BLOCK_HIST_BINS; i += THREADS)
             if (const uint32_t v = sHist[i]) atomicAdd(&hrow[i], v);
