@@ -94,18 +94,6 @@ struct AttnArgs {
 
 // Rotate this warp's channels 448..511 (lanes hold lane+448 and lane+480) by +t
 // (sign = 1) or -t (sign = -1); pairs are (even lane, odd lane).
-__device__ __forceinline__ void rope_lanes(float (&x)[ATT_PER_LANE], int lane, const float* cs, const float* sn,
-                                           float sign) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int j = (lane + 32 * i) >> 1;
-        const float c = cs[j], s = sign * sn[j];
-        float v = x[14 + i];
-        float p = __shfl_xor_sync(0xffffffffu, v, 1);
-        x[14 + i] = (lane & 1) ? fmaf(p, s, v * c) : fmaf(-p, s, v * c);
-    }
-}
-
 template <typename TQ, int KVK, typename TS, typename TO>
 __global__ void __launch_bounds__(ATT_THREADS, 2) attn_split_kernel(const AttnArgs a) {
     extern __shared__ float smem[];
@@ -280,43 +268,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int
     }
     __syncwarp();
     const int ns = a.n_split;
-    const float* part = a.ws + r * (int64_t)ns * PART;
-    const float zs = a.sink ? a.sink[h] : -INFINITY;
-    float M = zs;
-    for (int s0 = 0; s0 < ns; s0 += 32) M = fmaxf(M, warp_max(s0 + lane < ns ? part[(s0 + lane) * PART] : -INFINITY));
-    float acc[ATT_PER_LANE];
-#pragma unroll
-    for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = 0.0f;
-    float denom = 0.0f;
-    if (M != -INFINITY) {
-        denom = (zs == -INFINITY) ? 0.0f : expf(zs - M);
-        for (int s = 0; s < ns; s += 4) {
-            float e[4], l[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float ms = s + j < ns ? part[(s + j) * PART] : -INFINITY;
-                e[j] = (ms == -INFINITY) ? 0.0f : expf(ms - M);
-                l[j] = s + j < ns ? part[(s + j) * PART + 1] : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (s + j >= ns) break;
-                denom = fmaf(l[j], e[j], denom);
-                const float* pj = part + (s + j) * PART + PO + lane;
-#pragma unroll
-                for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] = fmaf(e[j], pj[32 * i], acc[i]);
-            }
-        }
-    }
-    const float inv = denom > 0.0f ? 1.0f / denom : 0.0f;
-#pragma unroll
-    for (int i = 0; i < ATT_PER_LANE; ++i) acc[i] *= inv;
-    if (a.flags & CSA2_ROPE) rope_lanes(acc, lane, cs, sn, -1.0f);
     const int64_t ro = bq * a.Hs + h;                      // row of out / lse
-    TO* o = reinterpret_cast<TO*>(a.out) + ro * (int64_t)ATT_C;
-#pragma unroll
-    for (int i = 0; i < ATT_PER_LANE; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
-    if (a.lse && lane == 0) a.lse[ro] = (denom > 0.0f) ? M + logf(denom) : -INFINITY;
+    attn_combine_row<TO>(a.ws + r * (int64_t)ns * PART, ns, a.sink ? a.sink[h] : -INFINITY,
+                         (a.flags & CSA2_ROPE) ? cs : nullptr, sn, reinterpret_cast<TO*>(a.out) + ro * (int64_t)ATT_C,
+                         a.lse ? a.lse + ro : nullptr);
 }
 
 constexpr size_t ATT_SMEM = (size_t)ATT_KC * ATT_C * sizeof(float) + ATT_KC * sizeof(float) + ATT_KC * sizeof(int) +

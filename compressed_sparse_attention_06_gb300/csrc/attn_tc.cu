@@ -102,6 +102,8 @@ struct TcArgs {
     int64_t items;
     unsigned int* st;
     long long budget;
+    int cluster;                  // 1: a query's splits are one thread-block cluster (one item per
+                                  // CTA) and merge their partials at the end of the kernel
 };
 
 struct ItemInfo {
@@ -898,6 +900,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
     tc_fence_after();
     pdl_trigger();
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    if (a.cluster) {
+        // the query's splits merge here instead of in a combine kernel: once every CTA of
+        // the cluster has written its partials (fence, then the cluster barrier), this
+        // CTA merges its share of the heads from them, a warp per head
+        __threadfence();
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+        const ItemInfo it = item_info(a, blockIdx.x);
+        const int ns = a.n_split;
+        const int hs = (a.H + ns - 1) / ns;
+        const int h0 = it.split * hs, h1 = min(a.H, h0 + hs);
+        const float* cs = (a.flags & CSA2_ROPE) ? a.rope_cs + it.bq * 64 : nullptr;
+        for (int h = h0 + warp; h < h1; h += TC_THREADS / 32)
+            attn_combine_row<TO>(a.part + (it.bq * a.H + h) * (int64_t)ns * PART, ns, a.sink ? a.sink[h] : -INFINITY,
+                                 cs, cs ? cs + 32 : nullptr,
+                                 reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + h) * (int64_t)TC_C,
+                                 a.lse ? a.lse + it.bq * a.Hs + h : nullptr);
+    }
 }
 
 void tc_splits(const csa2_ctx* ctx, int64_t n_bq, int k, int window, int& n_split, int& tps) {
@@ -937,6 +956,30 @@ WsLayout ws_layout(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, 
     return L;
 }
 
+// Whether clusters of ns CTAs of this kernel can be resident (asked once per size).
+template <bool FP4, typename TO>
+bool tc_cluster_ok(int ns) {
+    static int ok[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (ns < 2 || ns > 8) return false;
+    if (ok[ns] < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ns);
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)ns;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        ok[ns] = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<FP4, TO>, &cfg) == cudaSuccess && n > 0;
+        (void)cudaGetLastError();
+    }
+    return ok[ns] == 1;
+}
+
 template <bool FP4, typename TO>
 csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, cudaStream_t s) {
     auto kern = attn_tc_kernel<FP4, TO>;
@@ -946,9 +989,30 @@ csa2_status launch_tc(const csa2_ctx* ctx, TcArgs& a, cudaStream_t s) {
             return CSA2_ERR_CUDA;
         attr = true;
     }
+    // few queries (decode): one item per CTA, and a query's splits as one cluster that
+    // merges its partials in the kernel
+    a.cluster = a.n_split > 1 && a.n_split <= 8 && a.items <= ctx->num_sms && tc_cluster_ok<FP4, TO>(a.n_split);
     const int64_t grid = std::min<int64_t>(a.items, ctx->num_sms);
-    const csa2_status r = launch_pdl(kern, dim3((unsigned)grid), dim3(TC_THREADS), SMEM_BYTES, s, a);
-    return r != CSA2_OK ? r : csa2_launch_status();
+    if (!a.cluster) {
+        const csa2_status r = launch_pdl(kern, dim3((unsigned)grid), dim3(TC_THREADS), SMEM_BYTES, s, a);
+        return r != CSA2_OK ? r : csa2_launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)a.n_split;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait()
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return CSA2_ERR_CUDA;
+    return csa2_launch_status();
 }
 
 }  // namespace
@@ -1035,8 +1099,11 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.st = ctx->status;
     a.budget = WAIT_BUDGET;
     *n_split = L.n_split;
+    a.cluster = 0;
     const bool fp4 = c.kv_dt == CSA2_FP4_E4M3x16;
     const bool f32o = c.out_dt == CSA2_F32;
-    if (fp4) return f32o ? launch_tc<true, float>(ctx, a, s) : launch_tc<true, __nv_bfloat16>(ctx, a, s);
-    return f32o ? launch_tc<false, float>(ctx, a, s) : launch_tc<false, __nv_bfloat16>(ctx, a, s);
+    const csa2_status r = fp4 ? (f32o ? launch_tc<true, float>(ctx, a, s) : launch_tc<true, __nv_bfloat16>(ctx, a, s))
+                              : (f32o ? launch_tc<false, float>(ctx, a, s) : launch_tc<false, __nv_bfloat16>(ctx, a, s));
+    if (a.cluster) *n_split = 1;           // merged in the kernel
+    return r;
 }

@@ -12,6 +12,65 @@
 constexpr int ATTN_PART = 516;
 constexpr int ATTN_PART_O = 4;
 
+// Inverse (sign -1) or forward RoPE on a warp's copy of one 512-dim row, lane l
+// holding dims l + 32 i: dims 448..511 are x[14], x[15]; pair (2j, 2j+1) sits in
+// lanes (2j, 2j+1) mod 32.  cs / sn: cos / sin of the 32 angles.
+__device__ __forceinline__ void rope_lanes(float (&x)[16], int lane, const float* cs, const float* sn, float sign) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int j = (lane + 32 * i) >> 1;
+        const float c = cs[j], s = sign * sn[j];
+        float v = x[14 + i];
+        float p = __shfl_xor_sync(0xffffffffu, v, 1);
+        x[14 + i] = (lane & 1) ? fmaf(p, s, v * c) : fmaf(-p, s, v * c);
+    }
+}
+
+// Merge of the key splits of one (query, head) by one warp (DSA-to-CSA/HCA page eq.
+// (27) over the union of the splits' keys): part = the ns partials of the row (max or
+// offset, sum of exponentials, unnormalised output), zs = the sink logit (-inf: none),
+// cs / sn = RoPE at the query position (NULL: no rotation).  Writes the 512 outputs
+// to o and, if lse is not NULL, log(sum e^z + e^zs) to *lse.
+template <typename TO>
+__device__ __forceinline__ void attn_combine_row(const float* part, int ns, float zs, const float* cs,
+                                                 const float* sn, TO* o, float* lse) {
+    const int lane = threadIdx.x & 31;
+    float M = zs;
+    for (int s0 = 0; s0 < ns; s0 += 32)
+        M = fmaxf(M, warp_max(s0 + lane < ns ? part[(s0 + lane) * ATTN_PART] : -INFINITY));
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+    float denom = 0.0f;
+    if (M != -INFINITY) {
+        denom = (zs == -INFINITY) ? 0.0f : expf(zs - M);
+        for (int s = 0; s < ns; s += 4) {
+            float e[4], l[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float ms = s + j < ns ? part[(s + j) * ATTN_PART] : -INFINITY;
+                e[j] = (ms == -INFINITY) ? 0.0f : expf(ms - M);
+                l[j] = s + j < ns ? part[(s + j) * ATTN_PART + 1] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (s + j >= ns) break;
+                denom = fmaf(l[j], e[j], denom);
+                const float* pj = part + (s + j) * ATTN_PART + ATTN_PART_O + lane;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = fmaf(e[j], pj[32 * i], acc[i]);
+            }
+        }
+    }
+    const float inv = denom > 0.0f ? 1.0f / denom : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] *= inv;
+    if (cs) rope_lanes(acc, lane, cs, sn, -1.0f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
+    if (lse && lane == 0) *lse = (denom > 0.0f) ? M + logf(denom) : -INFINITY;
+}
+
 struct AttnTcCall {
     const void* q;
     csa2_dtype q_dt;
