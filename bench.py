@@ -247,6 +247,7 @@ class FP4Decode(Workload):
         self.swa_row = self.swa[:, self.t % 128]
         self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new, self.KI_new]
         self.e2e_out = [self.buf.out, self.buf.idx]
+        self.qstream = torch.cuda.Stream(dev)
         torch.cuda.synchronize()
 
     def e2e_inputs(self):
@@ -335,13 +336,31 @@ class FP4Decode(Workload):
         _C().csa2_topk(b.cand_scores, self.nv, self.k, pool=b.top_blocks, block=self.block, out_idx=b.idx,
                        ws=b.topk_ws)
 
-    def attn(self):
+    def attn(self, prepared=False):
         b = self.buf
+        C = _C()
         _C().csa2_sparse_attn(self.q, self.kv, b.idx, self.swa, self.q_pos, self.sink, window=self.window, out=b.out,
-                              ws=b.attn_ws)
+                              ws=b.attn_ws, flags=C.ATTN_DEFAULT | (C.ATTN_PREPARED if prepared else 0))
+
+    def prepare(self):
+        """The attention's query half (depends only on q and its position)."""
+        _C().csa2_attn_prepare(self.q, self.q_pos, self.buf.attn_ws, self.k, window=self.window, N=self.N,
+                               swa_cap=128)
+
+    # True: the attention's query half beside the query pack on a second stream
+    # (measured: no faster than the attention call preparing it)
+    prep_early = False
 
     def pre(self):
-        self.pack_query()
+        if self.prep_early and self.H <= 64:
+            cur = torch.cuda.current_stream()
+            self.qstream.wait_stream(cur)
+            with torch.cuda.stream(self.qstream):
+                self.prepare()
+            self.pack_query()
+            cur.wait_stream(self.qstream)
+        else:
+            self.pack_query()
 
     has_side = True
 
@@ -349,12 +368,12 @@ class FP4Decode(Workload):
         self.write_rows()
 
     def post(self):
-        self.select(); self.attn()
+        self.select(); self.attn(prepared=self.prep_early)
 
     def launches_per_step(self):
         # compress, 2 packs, histogram zeroing, scan, pool + top-k, then per 64-head pass
-        # of the attention: query prep, attention, split combine
-        return 6 + 3 * ((self.H + 63) // 64)
+        # of the attention: query prep, attention (its key splits merged in the kernel)
+        return 6 + 2 * ((self.H + 63) // 64)
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
@@ -365,13 +384,17 @@ class FP4Decode(Workload):
         B, H = self.B, self.H
         attn_bytes = B * (self.k * 288 + self.window * 1024 + H * 512 * 2 * 2)
         attn_flops = B * H * (self.k + self.window) * 512 * 4
+        extra = []
+        if self.H <= 64:
+            extra = [("sparse attention (query half prepared)", lambda: self.attn(prepared=True), attn_bytes, attn_flops),
+                     ("attention query half", self.prepare, B * H * 512 * 2 * 2, 0)]
         return [("write new rows", self.write, B * (2 * 1024 + 256 + 288 + 68 + self.H_I * (256 + 68)), 0),
                 ("index scan", self.main, self.main_amount(), 2 * B * self.V * 64 * 128, "fp4"),
                 ("index scan (bf16 q)", self.scan_bf16_query, B * self.V * 68 + B * self.H_I * (256 + 4),
                  2 * B * self.V * 64 * 128, "bf16"),
                 (f"pool + top-{self.k}", self.select, B * ((self.V + 7) // 8) * 4 + B * self.n_top * 8 * 4, 0),
                 ("block pool alone", self.pool, B * ((self.V + 7) // 8) * 4, 0),
-                ("sparse attention", self.attn, attn_bytes, attn_flops)]
+                ("sparse attention", self.attn, attn_bytes, attn_flops)] + extra
 
     def queries(self):
         return self.B

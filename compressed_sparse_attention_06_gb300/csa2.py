@@ -20,6 +20,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(
 F32, BF16, FP4_E4M3x16, MXFP4_E8M0x32 = range(4)
 QNORM, KVNORM, ROPE = 1, 2, 4
 ATTN_DEFAULT = QNORM | KVNORM | ROPE
+ATTN_PREPARED = 8               # csa2_attn_prepare already wrote the query half into the workspace
 W_NORM, W_ROPE = 1, 2
 BLOCK_HIST_BINS = 4096          # words per row of csa2_index_score's block histogram
 
@@ -31,7 +32,7 @@ EXPORTS = (
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
     "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
-    "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist",
+    "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist", "csa2_attn_prepare",
 )
 
 
@@ -72,6 +73,8 @@ def _declare(lib):
         "csa2_block_pool": (_i, [_vp, _vp, _vp, _i64, _i64, _vp, _i, _i, _vp, _vp, _i, _vp, ctypes.c_size_t,
                                  _vp]),
         "csa2_block_pool_workspace_bytes": (ctypes.c_size_t, [_vp, _i64, _i64, _i]),
+        "csa2_attn_prepare": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i64, _i64, _f, _u, _vp,
+                                   ctypes.c_size_t, _vp]),
         "csa2_block_hist": (_i, [_vp, _vp, _i64, _i64, _vp, _i, _vp, _vp]),
         "csa2_pool_topk": (_i, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
         "csa2_sparse_attn": (_i, [_vp, _vp, _i, _vp, _i, _i64, _vp, _i, _vp, _i, _i64, _i64, _i, _vp, _vp,
@@ -444,6 +447,16 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
                                  _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
     _check("csa2_sparse_attn", st)
     return out, lse
+
+
+def csa2_attn_prepare(q, q_pos, ws: torch.Tensor, k: int, window: int = 128, N: int = 0, swa_cap: int = 0,
+                      rope_base: float = 10000.0, flags: int = ATTN_DEFAULT) -> None:
+    """The query half of a later csa2_sparse_attn / csa2_dense_attn call with the same
+    sizes, flags | ATTN_PREPARED and the same workspace `ws` (q [B,Q,H<=64,c])."""
+    B, Q, H, c = q.shape
+    st = _lib().csa2_attn_prepare(ctx(q.device.index), _p(q), _dt(q), _p(q_pos), B, Q, H, c, k, window, N, swa_cap,
+                                  rope_base, flags, _p(ws), ws.numel() * ws.element_size(), _stream(q))
+    _check("csa2_attn_prepare", st)
 
 
 def csa2_dense_attn(q, kv, n_visible, k_max: int, swa, q_pos, sink=None, window: int = 128, swa_pos0: int = 0,

@@ -355,7 +355,10 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     if (!ctx || B < 0 || Q < 0 || N < 0 || k < 0 || window < 0 || window > 1024) return CSA2_ERR_INVALID_ARG;
     if (H < 1 || H > 128) return CSA2_ERR_INVALID_ARG;
     if (c != ATT_C) return CSA2_ERR_UNSUPPORTED;
-    if (flags & ~(CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE)) return CSA2_ERR_INVALID_ARG;
+    if (flags & ~(CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE | CSA2_ATTN_PREPARED)) return CSA2_ERR_INVALID_ARG;
+    // a prepared query image is used only by a single tensor-core pass (<= 64 heads);
+    // otherwise the call prepares its own
+    if (H > 64) flags &= ~CSA2_ATTN_PREPARED;
     if (q_dt != CSA2_F32 && q_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
     if (kv_dt != CSA2_F32 && kv_dt != CSA2_BF16 && kv_dt != CSA2_FP4_E4M3x16) return CSA2_ERR_UNSUPPORTED;
     if (swa_dt != CSA2_F32 && swa_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
@@ -446,7 +449,7 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     a.H = H;
     a.Hs = H;
     a.rope = make_rope_table(rope_base);
-    a.flags = flags;
+    a.flags = flags & ~CSA2_ATTN_PREPARED;
     a.out = out;
     a.lse = lse;
     a.ws = reinterpret_cast<float*>(ws);
@@ -491,4 +494,33 @@ extern "C" csa2_status csa2_dense_attn(csa2_ctx* ctx, const void* q, csa2_dtype 
     if (k_max < 0 || k_max > (1 << 22) || (k_max > 0 && !n_visible)) return CSA2_ERR_INVALID_ARG;
     return attn_impl(ctx, q, q_dt, kv, kv_dt, N, nullptr, n_visible, k_max, swa, swa_dt, swa_cap, swa_pos0, window,
                      q_pos, sink, B, Q, H, c, rope_base, flags, out, out_dt, lse, ws, ws_bytes, stream);
+}
+
+extern "C" csa2_status csa2_attn_prepare(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const int64_t* q_pos, int B,
+                                         int Q, int H, int c, int k, int window, int64_t N, int64_t swa_cap,
+                                         float rope_base, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+    if (!ctx || B < 0 || Q < 0 || k < 0 || window < 0 || window > 1024 || H < 1 || H > 64) return CSA2_ERR_INVALID_ARG;
+    if (c != ATT_C) return CSA2_ERR_UNSUPPORTED;
+    if (flags & ~(CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE)) return CSA2_ERR_INVALID_ARG;
+    if (q_dt != CSA2_F32 && q_dt != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+    if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (B == 0 || Q == 0) return CSA2_OK;
+    if (!q || !q_pos || !aligned(q, 16) || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    if (window == 0) swa_cap = 1;
+    AttnTcCall tc;
+    memset(&tc, 0, sizeof(tc));
+    tc.q = q;
+    tc.q_dt = q_dt;
+    tc.N = N;
+    tc.k = k;
+    tc.window = window;
+    tc.swa_cap = swa_cap;
+    tc.q_pos = q_pos;
+    tc.B = B;
+    tc.Q = Q;
+    tc.H = H;
+    tc.Hs = H;
+    tc.rope = make_rope_table(rope_base);
+    tc.flags = flags;
+    return attn_tc_prepare(ctx, tc, ws, ws_bytes, as_stream(stream));
 }

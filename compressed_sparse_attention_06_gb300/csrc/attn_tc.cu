@@ -417,6 +417,45 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
     }
 }
 
+// Merge of one (query, head)'s key splits by one warp, for this path's partials: every
+// non-empty split used the same fixed offset (TC_SHIFT), so the unnormalised outputs
+// and the sums of exponentials simply add up (an empty split holds zeros) and the
+// output is scaled once, as a single split's epilogue does.  Every partial value is
+// loaded in one batch (no pass over the splits' maxima first).  cs: RoPE cos, then
+// sin, at the query position (NULL: no rotation).
+template <typename TO>
+__device__ __forceinline__ void tc_merge_row(const float* part, int ns, float zs, const float* cs, TO* o,
+                                             float* lse) {
+    const int lane = threadIdx.x & 31;
+    float L = 0.0f, acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int sp = 0; sp < 8; ++sp) {
+        if (sp >= ns) break;
+        const float* pp = part + sp * (int64_t)PART;
+        L += pp[1];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += pp[ATTN_PART_O + lane + 32 * i];
+    }
+    float sc = 0.0f, ls = -INFINITY;
+    if (L > 0.0f) {
+        const float M = fmaxf(TC_SHIFT, zs);
+        const float e = expf(TC_SHIFT - M);
+        const float den = L * e + ((zs == -INFINITY) ? 0.0f : expf(zs - M));
+        sc = e / den;
+        ls = M + logf(den);
+    } else if (zs != -INFINITY) {
+        ls = zs;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] *= sc;
+    if (cs) rope_lanes(acc, lane, cs, cs + 32, -1.0f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[lane + 32 * i] = from_f32<TO>(acc[i]);
+    if (lse && lane == 0) *lse = ls;
+}
+
 template <bool FP4, typename TO>
 // 14 warps: at most 128 registers a thread (four warps share one SM sub-partition's 16K registers)
 __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) {
@@ -912,10 +951,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         const int h0 = it.split * hs, h1 = min(a.H, h0 + hs);
         const float* cs = (a.flags & CSA2_ROPE) ? a.rope_cs + it.bq * 64 : nullptr;
         for (int h = h0 + warp; h < h1; h += TC_THREADS / 32)
-            attn_combine_row<TO>(a.part + (it.bq * a.H + h) * (int64_t)ns * PART, ns, a.sink ? a.sink[h] : -INFINITY,
-                                 cs, cs ? cs + 32 : nullptr,
-                                 reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + h) * (int64_t)TC_C,
-                                 a.lse ? a.lse + it.bq * a.Hs + h : nullptr);
+            tc_merge_row<TO>(a.part + (it.bq * a.H + h) * (int64_t)ns * PART, ns, a.sink ? a.sink[h] : -INFINITY, cs,
+                             reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + h) * (int64_t)TC_C,
+                             a.lse ? a.lse + it.bq * a.Hs + h : nullptr);
     }
 }
 
@@ -1036,6 +1074,29 @@ const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* 
     return reinterpret_cast<const float*>(reinterpret_cast<uint8_t*>(ws) + L.rope);
 }
 
+namespace {
+
+csa2_status attn_tc_prepare_into(const AttnTcCall& c, uint8_t* qimg, float* rope_cs, cudaStream_t s) {
+    const int64_t n_bq = (int64_t)c.B * c.Q;
+    const csa2_status rq =
+        c.q_dt == CSA2_BF16
+            ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg,
+                         rope_cs)
+            : launch_pdl(attn_qprep_kernel<float>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg, rope_cs);
+    return rq != CSA2_OK ? rq : csa2_launch_status();
+}
+
+}  // namespace
+
+csa2_status attn_tc_prepare(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s) {
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    if (!ws || !aligned(ws, 16) || ws_bytes < L.rinv_kv) return CSA2_ERR_INVALID_ARG;
+    uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+    return attn_tc_prepare_into(c, base + L.qimg, reinterpret_cast<float*>(base + L.rope), s);
+}
+
 csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
                         int* n_split) {
     const int64_t n_bq = (int64_t)c.B * c.Q;
@@ -1044,14 +1105,11 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     uint8_t* qimg = base + L.qimg;
     float* rope_cs = reinterpret_cast<float*>(base + L.rope);
-    const csa2_status rq =
-        c.q_dt == CSA2_BF16
-            ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg,
-                         rope_cs)
-            : launch_pdl(attn_qprep_kernel<float>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg, rope_cs);
-    if (rq != CSA2_OK) return rq;
+    // the query images and RoPE table (unless csa2_attn_prepare wrote them already)
+    if (!(c.flags & CSA2_ATTN_PREPARED)) {
+        const csa2_status rq = attn_tc_prepare_into(c, qimg, rope_cs, s);
+        if (rq != CSA2_OK) return rq;
+    }
     TcArgs a;
     a.rinv_kv = nullptr;
     a.rinv_swa = nullptr;

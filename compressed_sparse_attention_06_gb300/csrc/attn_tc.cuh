@@ -113,6 +113,10 @@ size_t attn_simt_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int w
 // The RoPE cos/sin table (float [B*Q, 64]) the path wrote into `ws` for this call.
 const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* ws);
 
+// The query half of the path alone (query images and RoPE table into `ws`), for a
+// later attn_tc_run with CSA2_ATTN_PREPARED in the flags and the same sizes.
+csa2_status attn_tc_prepare(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // Runs the path.  On return *n_split > 1 means the output is still in per-split
 // partials at the start of `ws` (float [B*Q, H, n_split, ATTN_PART]),
 // to be merged by the caller's combine kernel.

@@ -1189,16 +1189,20 @@ struct PhShared {
     uint32_t tkey;                         // ENTRY: the smallest block maximum among the best blocks
     uint32_t ecnt;                         // ENTRY: entry candidates pushed into this CTA
     uint32_t ewin[PH_MAX_C];               // ENTRY: every CTA's number of winning entries
-    uint32_t nown;                         // ENTRY: this CTA's best blocks / own candidates
+    uint32_t nown;                         // ENTRY: this CTA's best blocks
+    uint32_t tmin_local;                   // ENTRY: the smallest maximum among this CTA's in-bin best blocks
+    uint32_t tmin[PH_MAX_C];               // ENTRY: every CTA's tmin_local (pushed)
+    uint32_t ndense;                       // ENTRY: received entries scoring at least the threshold
 };
-constexpr int PH_ECAP = 8192;              // ENTRY: entry candidates a CTA receives (64 KB)
-// ENTRY reuses the two candidate-list arrays: `all` holds PH_ECAP words of indices,
-// `loc` the bitmap of a chunk's entries
-static_assert(2 * PH_CAP * 2 >= PH_ECAP, "the entry lists fit the candidate space");
+constexpr int PH_ECAP = 8192;              // ENTRY: entry candidates a CTA can receive (64 KB)
+// ENTRY reuses the two candidate-list arrays once the block selections are done:
+// `all` holds the received entries at or above the threshold (2 * PH_CAP of them, the
+// limit k * block <= 2 * PH_CAP keeps them within), `loc` the bitmap of a chunk's entries
+static_assert(2 * PH_CAP <= PH_ECAP, "every entry of the best blocks fits the receive buffer");
 
 // Ordered emission of one selection from the CTA's bitmaps: winners (bmW) in index
 // order, ties (bmE) while fewer than `quota` have been taken, at out[off + rank].
-__device__ void ph_emit(const uint32_t* bmW, const uint32_t* bmE, int nwords, int64_t c0, uint32_t off,
+__device__ __noinline__ void ph_emit(const uint32_t* bmW, const uint32_t* bmE, int nwords, int64_t c0, uint32_t off,
                         uint32_t quota, int32_t* out, uint32_t out_len, ClShared& sh) {
     const int tid = threadIdx.x;
     const int per = (nwords + (int)blockDim.x - 1) / (int)blockDim.x;
@@ -1239,7 +1243,7 @@ __device__ __forceinline__ uint32_t cl_atomic_add(uint32_t addr, uint32_t v) {
 
 // One selection pass over bitmap words in index order: thread t owns a run of words;
 // bit j of word w (id base + 32 w + j) goes to out[off + its rank] while below out_len.
-__device__ void ph_emit_bits(const uint32_t* bm, int nwords, int64_t base, uint32_t off, int32_t* out,
+__device__ __noinline__ void ph_emit_bits(const uint32_t* bm, int nwords, int64_t base, uint32_t off, int32_t* out,
                              float* outv, const float* vals, uint32_t out_len, ClShared& sh) {
     const int tid = threadIdx.x;
     const int per = (nwords + (int)blockDim.x - 1) / (int)blockDim.x;
@@ -1316,6 +1320,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     if (tid == 0) {
         px.ecnt = 0u;
         px.tkey = 1u;                      // take-all: every valid key (keys are never 0)
+        px.tmin_local = 0xFFFFFFFFu;
     }
     __syncthreads();
     // the threshold bins of both selections
@@ -1344,34 +1349,61 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     uint64_t* loc = reinterpret_cast<uint64_t*>(bmE + 2 * cw);   // [2][PH_CAP] this CTA's candidates
     uint64_t* all = loc + 2 * PH_CAP;                      // [2][PH_CAP] every CTA's, gathered
     const unsigned lt = (1u << lane) - 1u;
+    // the chunk's keys into shared memory (key i from thread i % 1024: coalesced loads)
 #pragma unroll
     for (int j = 0; j < PH_KPT; ++j) {
         const int i = tid + j * bd;
-        const int w = i >> 5;
-        if (w >= cw) break;                                // the same for the whole warp
-        const uint32_t key = i < n ? order_key(v[j]) : 0u;
-        skey[i] = key;
-        const int d = (int)(key >> 20);
-        const bool v0 = act[0] && key != 0u && c0 + i != newest, v1 = act[1] && key != 0u;
-        const unsigned g0 = __ballot_sync(FULL_MASK, v0 && d > bin[0]);
-        const unsigned e0 = __ballot_sync(FULL_MASK, v0 && d == bin[0]);
-        // ENTRY with every block among the best: every visible block of the chunk is one
-        const unsigned g1 = __ballot_sync(FULL_MASK, (v1 && d > bin[1]) || (ENTRY && !act[1] && key != 0u));
-        const unsigned e1 = __ballot_sync(FULL_MASK, v1 && d == bin[1]);
-        if (lane == 0) {
-            bmW[w] = g0;
-            bmW[cw + w] = g1;
-            bmE[w] = 0u;
-            bmE[cw + w] = 0u;
+        if (i >= chunk) break;
+        skey[i] = i < n ? order_key(v[j]) : 0u;
+    }
+    __syncthreads();
+    // classify: a thread per word of 32 keys, read as eight 16-byte pieces starting at a
+    // word-dependent piece (the lanes of a warp then spread over the banks)
+    for (int w = tid; w < nwords; w += bd) {
+        uint32_t g0 = 0u, e0 = 0u, g1 = 0u, e1 = 0u, vm = 0u;
+        // not unrolled: each CTA runs this once, from a cold instruction cache, and
+        // straight-line code there costs more in instruction fetch than the loop does
+#pragma unroll 1
+        for (int t = 0; t < 8; ++t) {
+            const int q = (t + w) & 7;
+            const uint4 k4 = *reinterpret_cast<const uint4*>(skey + w * 32 + 4 * q);
+            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t key = kk[c], bit = 1u << (4 * q + c);
+                const int d = (int)(key >> 20);
+                if (key != 0u) {
+                    vm |= bit;
+                    if (d > bin[0]) g0 |= bit;
+                    if (d == bin[0]) e0 |= bit;
+                    if (d > bin[1]) g1 |= bit;
+                    if (d == bin[1]) e1 |= bit;
+                }
+            }
         }
+        const int64_t nw_ = newest - c0 - (int64_t)w * 32;      // the newest block is not a pool candidate
+        const uint32_t notnew = (nw_ >= 0 && nw_ < 32) ? ~(1u << nw_) : 0xFFFFFFFFu;
+        g0 = act[0] ? g0 & notnew : 0u;
+        e0 = act[0] ? e0 & notnew : 0u;
+        // ENTRY with every block among the best: every visible block of the chunk is one
+        g1 = act[1] ? g1 : (ENTRY ? vm : 0u);
+        e1 = act[1] ? e1 : 0u;
+        bmW[w] = g0;
+        bmW[cw + w] = g1;
+        bmE[w] = 0u;
+        bmE[cw + w] = 0u;
+        // the threshold bins' keys go to this CTA's candidate lists (key, index)
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
-            const unsigned e = s2 == 0 ? e0 : e1;
+            uint32_t e = s2 == 0 ? e0 : e1;
             if (!e) continue;
-            uint32_t o = 0u;
-            if (lane == 0) o = atomicAdd(&px.nloc[s2], (uint32_t)__popc(e));
-            o = __shfl_sync(FULL_MASK, o, 0) + __popc(e & lt);
-            if (((e >> lane) & 1u) && o < PH_CAP) loc[s2 * PH_CAP + o] = ((uint64_t)key << 32) | (uint32_t)(c0 + i);
+            uint32_t o = atomicAdd(&px.nloc[s2], (uint32_t)__popc(e));
+            while (e) {
+                const int j = __ffs(e) - 1;
+                e &= e - 1;
+                if (o < PH_CAP) loc[s2 * PH_CAP + o] = ((uint64_t)skey[w * 32 + j] << 32) | (uint32_t)(c0 + w * 32 + j);
+                ++o;
+            }
         }
     }
     cl_sync();                             // (1) every CTA's candidate list is complete
@@ -1418,16 +1450,9 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                 if (lane == 0 && ahead < r) {
                     const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - c0);
                     atomicOr(&W[li >> 5], 1u << (li & 31));
-                }
-            }
-            // the last winner may be another CTA's candidate: every CTA ranks the whole
-            // gathered list for it (a few hundred keys)
-            if (ENTRY && s2 == 1) {
-                for (uint32_t j = tid; j < mm; j += bd) {
-                    const uint64_t x = A[j];
-                    uint32_t ahead = 0u;
-                    for (uint32_t i = 0; i < mm; ++i) ahead += A[i] > x;
-                    if (ahead == r - 1) px.tkey = (uint32_t)(x >> 32);
+                    // ENTRY: the smallest best-block maximum is the smallest in-bin winner
+                    // of the whole row, the minimum over the CTAs of this local one
+                    if (ENTRY && s2 == 1) atomicMin(&px.tmin_local, (uint32_t)(x >> 32));
                 }
             }
         } else {
@@ -1494,13 +1519,16 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             const uint32_t dst = cl_map(&px.cnt[s2][rank][0], (uint32_t)tid);
             cl_st(dst, tw);
             cl_st(dst + 4u, tt);
+            if (ENTRY && s2 == 1) cl_st(cl_map(&px.tmin[rank], (uint32_t)tid), px.tmin_local);
         }
         __syncthreads();
     }
     if (ENTRY) {
-        // ---- the row's top-k entries: every entry of this CTA's best blocks that
-        // scores at least the smallest best-block maximum is a candidate; each CTA
-        // pushes its candidates into every CTA, then ranks its own against all of them
+        // ---- the row's top-k entries: every entry of the best blocks that scores at
+        // least the smallest best-block maximum is a candidate.  Each CTA pushes every
+        // visible entry of its best blocks into every CTA (the threshold is known only
+        // after the next barrier), then each filters the received ones and ranks its
+        // own candidates against the rest
         uint32_t* W = bmW + cw;
         if (any_radix) {
             // the crowded case: the ties at T taken (lowest index first) become best
@@ -1546,7 +1574,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             if (tid == 0) px.nown = min(tot, 2u * (uint32_t)PH_CAP);
         }
         __syncthreads();
-        const uint32_t tkey = px.tkey, nown = px.nown;
+        const uint32_t nown = px.nown;
         const float* srow = a.scores + row * a.n_ent;
         for (uint32_t t0 = 0; t0 < nown * (uint32_t)a.block; t0 += bd) {
             const uint32_t t = t0 + tid;
@@ -1557,16 +1585,17 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                 e = (c0 + blist[t / a.block]) * a.block + t % a.block;
                 if (e < V) {
                     key = order_key(srow[e]);
-                    keep = key >= tkey;
+                    keep = true;
                 }
             }
             const unsigned km = __ballot_sync(FULL_MASK, keep);
             if (!km) continue;
             const uint64_t cand = ((uint64_t)key << 32) | (uint32_t)e;
+            // one slot reservation per destination CTA, lanes 0 .. C-1 at once
+            uint32_t rsv = 0u;
+            if (lane < (int)C) rsv = cl_atomic_add(cl_map(&px.ecnt, (uint32_t)lane), (uint32_t)__popc(km));
             for (uint32_t c = 0; c < C; ++c) {
-                uint32_t o = 0u;
-                if (lane == 0) o = cl_atomic_add(cl_map(&px.ecnt, c), (uint32_t)__popc(km));
-                o = __shfl_sync(FULL_MASK, o, 0) + __popc(km & lt);
+                const uint32_t o = __shfl_sync(FULL_MASK, rsv, (int)c) + __popc(km & lt);
                 if (keep && o < (uint32_t)PH_ECAP) {
                     const uint32_t dst = cl_map(skey, c) + 8u * o;
                     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"((uint32_t)cand),
@@ -1605,26 +1634,40 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         uint32_t* ebm = reinterpret_cast<uint32_t*>(loc);
         const int ew = (chunk * a.block + 31) / 32;
         for (int i = tid; i < ew; i += bd) ebm[i] = 0u;
-        if (tid == 0) px.nown = 0u;
+        // the threshold: the minimum of the CTAs' smallest in-bin winners (a crowded bin:
+        // T itself; every block among the best: any valid key)
+        uint32_t tkey = px.tkey;
+        if (act[1] && m[1] <= (uint32_t)PH_CAP) {
+            tkey = 0xFFFFFFFFu;
+            for (uint32_t c = 0; c < C; ++c) tkey = min(tkey, px.tmin[c]);
+        }
+        if (tid == 0) px.ndense = 0u;
         __syncthreads();
-        const int64_t e0 = c0 * a.block, e1 = (c0 + n) * a.block;
-        uint32_t* olist = reinterpret_cast<uint32_t*>(all);     // this CTA's candidates (slots of ec)
-        for (uint32_t j = tid; j < me; j += bd) {
-            const int64_t e = (int64_t)(uint32_t)ec[j];
-            if (e >= e0 && e < e1) {
-                const uint32_t o = atomicAdd(&px.nown, 1u);
-                if (o < (uint32_t)PH_ECAP) olist[o] = j;          // `all` holds PH_ECAP words
-            }
+        // the received entries at or above the threshold, as (order value, entry), in `all`
+        uint64_t* dense = all;
+        for (uint32_t j0 = 0; j0 < me; j0 += bd) {
+            const uint32_t j = j0 + tid;
+            const bool keep = j < me && (uint32_t)(ec[j] >> 32) >= tkey;
+            const unsigned km = __ballot_sync(FULL_MASK, keep);
+            if (!km) continue;
+            uint32_t o = 0u;
+            if (lane == 0) o = atomicAdd(&px.ndense, (uint32_t)__popc(km));
+            o = __shfl_sync(FULL_MASK, o, 0) + __popc(km & lt);
+            if (keep && o < 2u * PH_CAP) dense[o] = ec[j] ^ 0xFFFFFFFFull;     // larger = earlier in the order
         }
         __syncthreads();
-        const uint32_t no = min(px.nown, (uint32_t)PH_ECAP);
-        for (uint32_t ci = wid; ci < no; ci += CL_THREADS / 32) {
-            const uint64_t x = ec[olist[ci]] ^ 0xFFFFFFFFull;
+        const uint32_t md = min(px.ndense, 2u * (uint32_t)PH_CAP);
+        const int64_t e0 = c0 * a.block, e1 = (c0 + n) * a.block;
+        // a warp per candidate of this CTA's chunk: winners rank below k
+        for (uint32_t ci = wid; ci < md; ci += CL_THREADS / 32) {
+            const uint64_t x = dense[ci];
+            const int64_t e = (int64_t)(uint32_t)(x ^ 0xFFFFFFFFull);
+            if (e < e0 || e >= e1) continue;                     // the same for the whole warp
             uint32_t ahead = 0u;
-            for (uint32_t j = lane; j < me; j += 32) ahead += (ec[j] ^ 0xFFFFFFFFull) > x;
+            for (uint32_t j = lane; j < md; j += 32) ahead += dense[j] > x;
             ahead = __reduce_add_sync(FULL_MASK, ahead);
             if (lane == 0 && ahead < (uint32_t)a.k) {
-                const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - e0);
+                const uint32_t li = (uint32_t)(e - e0);
                 atomicOr(&ebm[li >> 5], 1u << (li & 31));
             }
         }
@@ -1701,14 +1744,32 @@ size_t pool_hist_smem(int chunk, bool entry) {
     return (size_t)skey_words * 4 + (size_t)chunk / 32 * 16 + 4ull * PH_CAP * 8;
 }
 
+// Whether 16-CTA clusters of the pool kernel can be resident (asked once).
+template <bool ENTRY>
+bool pool_cluster16_ok() {
+    static int ok = -1;
+    if (ok < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(CL_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = pool_hist_smem(CL_MAX_CHUNK, ENTRY);
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 16;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, pool_hist_kernel<ENTRY>, &cfg) == cudaSuccess && n > 0;
+        (void)cudaGetLastError();
+    }
+    return ok == 1;
+}
+
 template <bool ENTRY>
 csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cudaStream_t s) {
-    const int C = pool_cluster_size(ctx, rows, a.ld);
-    const int chunk = (int)(((a.ld + C - 1) / C + CL_THREADS - 1) / CL_THREADS * CL_THREADS);
-    if (chunk > CL_MAX_CHUNK) return CSA2_ERR_UNSUPPORTED;
-    // ENTRY: the bitmap of a chunk's entries lives in the candidate lists' space
-    if (ENTRY && ((size_t)chunk * a.block + 31) / 32 * 4 > 2ull * PH_CAP * 8) return CSA2_ERR_UNSUPPORTED;
-    const size_t smem = pool_hist_smem(chunk, ENTRY);
+    int C = pool_cluster_size(ctx, rows, a.ld);
     auto kern = pool_hist_kernel<ENTRY>;
     static bool attr = false;
     if (!attr) {
@@ -1718,6 +1779,12 @@ csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cud
             return CSA2_ERR_CUDA;
         attr = true;
     }
+    if (C == 16 && !pool_cluster16_ok<ENTRY>()) C = 8;
+    const int chunk = (int)(((a.ld + C - 1) / C + CL_THREADS - 1) / CL_THREADS * CL_THREADS);
+    if (chunk > CL_MAX_CHUNK) return CSA2_ERR_UNSUPPORTED;
+    // ENTRY: the bitmap of a chunk's entries lives in the candidate lists' space
+    if (ENTRY && ((size_t)chunk * a.block + 31) / 32 * 4 > 2ull * PH_CAP * 8) return CSA2_ERR_UNSUPPORTED;
+    const size_t smem = pool_hist_smem(chunk, ENTRY);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
     cfg.blockDim = dim3(CL_THREADS, 1, 1);
@@ -1937,8 +2004,9 @@ extern "C" csa2_status csa2_pool_topk(csa2_ctx* ctx, const float* block_max, con
     if (!block_max || !block_hist || !scores || !n_visible || !out_blocks || !out_idx || ld <= 0 ||
         n_ent < ld * block || !aligned(block_hist, 16))
         return CSA2_ERR_INVALID_ARG;
-    // every entry of the k best blocks may be a candidate: they must fit the receive buffer
-    if ((int64_t)k * block > PH_ECAP || k > n_keep - 1) return CSA2_ERR_UNSUPPORTED;
+    // every entry of the k best blocks is pushed to every CTA of the row's cluster and
+    // may be a candidate: they must fit the receive buffer and the candidate list
+    if ((int64_t)k * block > 2 * PH_CAP || k > n_keep - 1) return CSA2_ERR_UNSUPPORTED;
     if (((ld + PH_MAX_C - 1) / PH_MAX_C + CL_THREADS - 1) / CL_THREADS * CL_THREADS > CL_MAX_CHUNK)
         return CSA2_ERR_UNSUPPORTED;
     PoolArgs p;

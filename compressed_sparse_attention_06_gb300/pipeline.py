@@ -78,7 +78,8 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
 
 def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeBuffers, *,
                      window: int = 128, swa_pos0: int = 0, k: int = TOPK, block: int = POOL_BLOCK,
-                     n_keep: int = POOL_KEEP, flags: int = C.ATTN_DEFAULT):
+                     n_keep: int = POOL_KEEP, flags: int = C.ATTN_DEFAULT,
+                     side_stream: Optional[torch.cuda.Stream] = None):
     """Full layer with the hierarchical pool (CSA2 page, «解码器里的分层索引»):
     scan all visible entries (scores, block maxima and their histogram), pick the
     pool (for the Reindex layers that follow) and the layer's own top-k in one call
@@ -89,10 +90,20 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     With an MXFP4 indexer cache the QK product runs in FP4 (DSA-to-CSA/HCA page,
     «Lightning Indexer：公式 (13)–(17)»): a bf16/f32 qI is first packed to MXFP4 by
     the same rule as the keys (into buf.qI_mx); an already packed uint8 qI is used
-    as given."""
+    as given.
+
+    side_stream: the attention's query half (csa2_attn_prepare) runs there, beside
+    the selection, after the scan (which fills the GPU by itself)."""
     qI = mxfp4_query(qI, kI, buf.qI_mx)
     C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores, want_block_max=True,
                        block_max=buf.block_max, block_hist=buf.block_hist)
+    B, Q, H = q.shape[:3]
+    prepared = side_stream is not None and H <= 64
+    if prepared:
+        side_stream.wait_stream(torch.cuda.current_stream(q.device))
+        with torch.cuda.stream(side_stream):
+            C.csa2_attn_prepare(q, q_pos, buf.attn_ws, k, window=window, N=kv.shape[1], swa_cap=swa.shape[1],
+                                flags=flags)
     if pool_topk_applies(k, block, n_keep, buf.block_max.shape[-1]):
         C.csa2_pool_topk(buf.block_max, buf.block_hist, buf.scores, n_visible, k, block=block, n_keep=n_keep,
                          out=buf.pool, out_idx=buf.idx)
@@ -102,15 +113,17 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
         C.csa2_index_score(qI, w, kI, n_visible, pool=buf.top_blocks, block=block, scores=buf.cand_scores)
         C.csa2_topk(buf.cand_scores, n_visible, k, pool=buf.top_blocks, block=block, out_idx=buf.idx,
                     ws=buf.topk_ws)
-    C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0, flags=flags,
-                       out=buf.out, ws=buf.attn_ws)
+    if prepared:
+        torch.cuda.current_stream(q.device).wait_stream(side_stream)
+    C.csa2_sparse_attn(q, kv, buf.idx, swa, q_pos, sink, window=window, swa_pos0=swa_pos0,
+                       flags=flags | (C.ATTN_PREPARED if prepared else 0), out=buf.out, ws=buf.attn_ws)
     return buf
 
 
 def pool_topk_applies(k: int, block: int, n_keep: int, n_blocks: int) -> bool:
     """The shapes csa2_pool_topk takes (its header states them)."""
     chunk = -(-(-(-n_blocks // 16)) // 1024) * 1024
-    return 1 <= k <= n_keep - 1 and k * block <= 8192 and block <= 16 and chunk <= 16384
+    return 1 <= k <= n_keep - 1 and k * block <= 4096 and block <= 16 and chunk <= 16384
 
 
 def mxfp4_query(qI, kI, out=None):

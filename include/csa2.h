@@ -60,6 +60,7 @@ typedef enum {
 #define CSA2_KVNORM 2u   /* RMSNorm each key/value row (compressed and window)    */
 #define CSA2_ROPE   4u   /* RoPE_t on the query's last 64 dims, RoPE_-t on output */
 #define CSA2_ATTN_DEFAULT (CSA2_QNORM | CSA2_KVNORM | CSA2_ROPE)
+#define CSA2_ATTN_PREPARED 8u  /* csa2_attn_prepare already wrote the query half into ws */
 
 /* compressor write-epilogue flags */
 #define CSA2_W_NORM 1u   /* RMSNorm of each compressed entry (kv_norm)            */
@@ -309,7 +310,7 @@ csa2_status csa2_block_hist(csa2_ctx* ctx, const float* block_max, int64_t rows,
  *   scores     : [rows, n_ent] f32, the full-scan scores (entries < n_visible read)
  *   out_blocks : [rows, n_keep] int32 (the pool);  out_idx : [rows, k] int32 entry
  *                ids ascending, -1 padded;  out_score : [rows, k] f32 or NULL
- * 2 <= n_keep <= 4096, 1 <= k <= n_keep - 1, k * block <= 8192, block <= 16,
+ * 2 <= n_keep <= 4096, 1 <= k <= n_keep - 1, k * block <= 4096, block <= 16,
  * ld <= 262,144.  Other shapes return CSA2_ERR_UNSUPPORTED (csa2_block_pool and
  * csa2_topk serve them).
  */
@@ -371,6 +372,21 @@ csa2_status csa2_sparse_attn(csa2_ctx* ctx,
                              int B, int Q, int H, int c, float rope_base, unsigned flags,
                              void* out, csa2_dtype out_dt, float* lse,
                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * csa2_attn_prepare -- the query half of csa2_sparse_attn / csa2_dense_attn ahead of
+ * time: each query head RMS-normalised and rotated by RoPE_t (the q^ of the
+ * attention), as the tensor-core path's bf16 operand image, and the RoPE table of
+ * the query positions, into `ws`.  It depends only on q and q_pos, so it can run
+ * beside the indexer and the selection (another stream) instead of after them.  The
+ * attention call then passes the same sizes, flags | CSA2_ATTN_PREPARED and the same
+ * workspace, which must not be touched in between.  Sizes and flags as the attention
+ * call (its k, window, N and swa_cap place the image in the workspace); H <= 64.
+ * When that call does not take the tensor-core path it ignores the prepared image.
+ */
+csa2_status csa2_attn_prepare(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, const int64_t* q_pos,
+                              int B, int Q, int H, int c, int k, int window, int64_t N, int64_t swa_cap,
+                              float rope_base, unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * csa2_dense_attn -- the HCA attention (DSA-to-CSA/HCA page «HCA：公式 (20)–(26)»,

@@ -140,3 +140,33 @@ def test_more_than_64_heads_in_passes(H, k, kv_kind):
     assert_close(to_np(tc), to_np(cc), 2e-2, "tensor-core vs CUDA-core output")
     assert_close(to_np(tc_lse), to_np(cc_lse), 2e-3, "tensor-core vs CUDA-core lse")
     _check(q, kv_np, idx, swa, q_pos, sink, window, to_np(tc), to_np(tc_lse), [(0, 1), (1, 0)])
+
+
+@pytest.mark.parametrize("B", [8, 200])
+def test_prepared_query_half_equals_one_call(B):
+    """csa2_attn_prepare on another stream, then csa2_sparse_attn with ATTN_PREPARED on
+    the same workspace, gives the one-call result bit for bit: decode shapes (a query's
+    key splits merged in one cluster) and many queries (persistent CTAs)."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    C.load()
+    N, H = 20000, 64
+    q = W.normal_tensor((B, 1, H, 512), 7301, 0, torch.bfloat16, DEV)
+    kv = C.csa2_fp4_pack(W.normal_tensor((B, N, 512), 7302, 0, torch.float32, DEV))
+    swa = W.normal_tensor((B, 128, 512), 7303, 0, torch.bfloat16, DEV)
+    idx = torch.stack([W.distinct_sample(N - 1, 512, 7304, b, DEV) for b in range(B)]).to(torch.int32).view(B, 1, 512)
+    q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=DEV)
+    sink = W.normal_tensor((H,), 7305, 0, torch.float32, DEV)
+    ref, ref_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, out_dtype=torch.float32, want_lse=True)
+    ws = torch.empty(C.csa2_sparse_attn_workspace_bytes(B, 1, H, 512, 128, N=N, swa_cap=128), dtype=torch.uint8,
+                     device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        C.csa2_attn_prepare(q, q_pos, ws, 512, window=128, N=N, swa_cap=128)
+    torch.cuda.current_stream().wait_stream(side)
+    out, lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, out_dtype=torch.float32, want_lse=True, ws=ws,
+                                  flags=C.ATTN_DEFAULT | C.ATTN_PREPARED)
+    C.csa2_ctx_check()
+    assert torch.equal(out, ref)
+    assert torch.equal(lse, ref_lse)

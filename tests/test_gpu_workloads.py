@@ -165,7 +165,9 @@ def _run_fp4_decode(B, N, H, k, grid):
     sink = wl["sink"] if H == 64 else W.normal_tensor((H,), 4109, 0, torch.float32, DEV)
     nv = P.visible_entries(wl.q_pos, 1)
     buf = P.alloc_decode(B, 1, N, H, 512, DEV, out_dtype=torch.bfloat16, k=k)
-    P.full_decode_step(wl["qI"], wl["w"], ki, wl["q"], kv, wl["swa"], wl.q_pos, nv, sink, buf, k=k)
+    # as bench.py runs it: the attention's query half on a second stream beside the selection
+    P.full_decode_step(wl["qI"], wl["w"], ki, wl["q"], kv, wl["swa"], wl.q_pos, nv, sink, buf, k=k,
+                       side_stream=torch.cuda.Stream())
     C.csa2_ctx_check()
     n_sets = []
     for b in range(B):
