@@ -144,6 +144,13 @@ def _dt(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+def alloc(shape, dtype, device) -> torch.Tensor:
+    """Every output and workspace this module (and pipeline.py) allocates comes from
+    here: uninitialised device memory, like torch.empty.  The tests replace it with an
+    allocator that puts guard bytes before and after each buffer."""
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
 def _check(fn: str, st: int):
     if st != OK:
         raise Csa2Error(fn, st)
@@ -178,7 +185,7 @@ def csa2_fp4_pack(x: torch.Tensor, fmt: int = FP4_E4M3x16, out: Optional[torch.T
     rows = x.numel() // c if c else 0
     rb = fp4_row_bytes(c) if fmt == FP4_E4M3x16 else mxfp4_row_bytes(c)
     if out is None:
-        out = torch.empty((*x.shape[:-1], rb), dtype=torch.uint8, device=x.device)
+        out = alloc((*x.shape[:-1], rb), dtype=torch.uint8, device=x.device)
         out_ld = 0
     ptr = _vp(out.data_ptr()) if out_ld else _p(out)
     _check("csa2_fp4_pack", _lib().csa2_fp4_pack(ctx(x.device.index), _p(x), _dt(x), rows, c, fmt, ptr, out_ld,
@@ -190,7 +197,7 @@ def csa2_fp4_unpack(b: torch.Tensor, fmt: int, c: int, out_dtype=torch.float32,
                     out: Optional[torch.Tensor] = None) -> torch.Tensor:
     rows = b.numel() // b.shape[-1] if b.shape[-1] else 0
     if out is None:
-        out = torch.empty((*b.shape[:-1], c), dtype=out_dtype, device=b.device)
+        out = alloc((*b.shape[:-1], c), dtype=out_dtype, device=b.device)
     _check("csa2_fp4_unpack", _lib().csa2_fp4_unpack(ctx(b.device.index), _p(b), fmt, rows, c, _p(out), _dt(out),
                                                      _stream(b)))
     return out
@@ -198,10 +205,10 @@ def csa2_fp4_unpack(b: torch.Tensor, fmt: int, c: int, out_dtype=torch.float32,
 
 def _alloc_rows(shape, c, out_fmt, device):
     if out_fmt == "fp4":
-        return torch.empty((*shape, fp4_row_bytes(c)), dtype=torch.uint8, device=device)
+        return alloc((*shape, fp4_row_bytes(c)), dtype=torch.uint8, device=device)
     if out_fmt == "mxfp4":
-        return torch.empty((*shape, mxfp4_row_bytes(c)), dtype=torch.uint8, device=device)
-    return torch.empty((*shape, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16, device=device)
+        return alloc((*shape, mxfp4_row_bytes(c)), dtype=torch.uint8, device=device)
+    return alloc((*shape, c), dtype=torch.float32 if out_fmt == "f32" else torch.bfloat16, device=device)
 
 
 def _out_dt(out, out_fmt):
@@ -236,7 +243,7 @@ def csa2_compress_state_bytes(B: int, c: int, m: int, dtype=torch.bfloat16, over
 
 def csa2_compress_state(B: int, c: int, m: int, dtype, device, overlap: bool = True) -> torch.Tensor:
     """Device buffer for the decode compressor state (no clearing needed)."""
-    return torch.empty(max(16, csa2_compress_state_bytes(B, c, m, dtype, overlap)), dtype=torch.uint8,
+    return alloc(max(16, csa2_compress_state_bytes(B, c, m, dtype, overlap)), dtype=torch.uint8,
                        device=device)
 
 
@@ -312,12 +319,12 @@ def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=Non
     if pool is not None:
         n_pool = pool.shape[-1]
         if scores is None:
-            scores = torch.empty((B, Q, n_pool * block), dtype=torch.float32, device=qI.device)
+            scores = alloc((B, Q, n_pool * block), dtype=torch.float32, device=qI.device)
     else:
         if want_scores and scores is None:
-            scores = torch.empty((B, Q, N), dtype=torch.float32, device=qI.device)
+            scores = alloc((B, Q, N), dtype=torch.float32, device=qI.device)
         if want_block_max and block_max is None:
-            block_max = torch.empty((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
+            block_max = alloc((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
     st = _lib().csa2_index_score(ctx(qI.device.index), _p(qI), q_dt, _p(w), _p(kI), k_dt, B, Q, N, H_I, d,
                                  _p(n_visible), _p(pool), n_pool, block, _p(scores), _p(block_max),
                                  _p(block_hist), _stream(qI))
@@ -334,7 +341,7 @@ def csa2_block_pool_workspace_bytes(rows: int, ld: int, n_keep: int, device: Opt
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    return alloc(max(int(nbytes), 16), dtype=torch.uint8, device=device)
 
 
 def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores: bool = False,
@@ -346,9 +353,9 @@ def csa2_topk(scores, n_visible, k: int, pool=None, block: int = 8, want_scores:
     rows = scores.numel() // n if n else 0
     lead = scores.shape[:-1]
     if out_idx is None:
-        out_idx = torch.empty((*lead, k), dtype=torch.int32, device=scores.device)
+        out_idx = alloc((*lead, k), dtype=torch.int32, device=scores.device)
     if want_scores and out_score is None:
-        out_score = torch.empty((*lead, k), dtype=torch.float32, device=scores.device)
+        out_score = alloc((*lead, k), dtype=torch.float32, device=scores.device)
     n_pool = pool.shape[-1] if pool is not None else 0
     if ws is None:
         ws = _ws(csa2_topk_workspace_bytes(rows, n, k, scores.device.index) if rows else 0, scores.device)
@@ -367,9 +374,9 @@ def csa2_block_pool(block_max, n_visible, block: int = 8, n_keep: int = 2048,
     ld = block_max.shape[-1]
     rows = block_max.numel() // ld if ld else 0
     if out is None:
-        out = torch.empty((*block_max.shape[:-1], n_keep), dtype=torch.int32, device=block_max.device)
+        out = alloc((*block_max.shape[:-1], n_keep), dtype=torch.int32, device=block_max.device)
     if n_top > 0 and out_top is None:
-        out_top = torch.empty((*block_max.shape[:-1], n_top), dtype=torch.int32, device=block_max.device)
+        out_top = alloc((*block_max.shape[:-1], n_top), dtype=torch.int32, device=block_max.device)
     if ws is None:
         ws = _ws(csa2_block_pool_workspace_bytes(rows, ld, n_keep, block_max.device.index) if rows else 0,
                  block_max.device)
@@ -386,7 +393,7 @@ def csa2_block_hist(block_max, n_visible, block: int = 8, out: Optional[torch.Te
     ld = block_max.shape[-1]
     rows = block_max.numel() // ld if ld else 0
     if out is None:
-        out = torch.empty((*block_max.shape[:-1], BLOCK_HIST_BINS), dtype=torch.int32, device=block_max.device)
+        out = alloc((*block_max.shape[:-1], BLOCK_HIST_BINS), dtype=torch.int32, device=block_max.device)
     st = _lib().csa2_block_hist(ctx(block_max.device.index), _p(block_max), rows, ld, _p(n_visible), block, _p(out),
                                 _stream(block_max))
     _check("csa2_block_hist", st)
@@ -404,11 +411,11 @@ def csa2_pool_topk(block_max, block_hist, scores, n_visible, k: int, block: int 
     lead = block_max.shape[:-1]
     n_ent = scores.shape[-1]
     if out is None:
-        out = torch.empty((*lead, n_keep), dtype=torch.int32, device=block_max.device)
+        out = alloc((*lead, n_keep), dtype=torch.int32, device=block_max.device)
     if out_idx is None:
-        out_idx = torch.empty((*lead, k), dtype=torch.int32, device=block_max.device)
+        out_idx = alloc((*lead, k), dtype=torch.int32, device=block_max.device)
     if want_scores and out_score is None:
-        out_score = torch.empty((*lead, k), dtype=torch.float32, device=block_max.device)
+        out_score = alloc((*lead, k), dtype=torch.float32, device=block_max.device)
     st = _lib().csa2_pool_topk(ctx(block_max.device.index), _p(block_max), _p(block_hist), _p(scores), rows, ld, n_ent,
                                _p(n_visible), block, n_keep, k, _p(out), _p(out_idx), _p(out_score),
                                _stream(block_max))
@@ -436,12 +443,12 @@ def csa2_sparse_attn(q, kv, idx, swa, q_pos, sink=None, window: int = 128, swa_p
     swa_cap = swa.shape[1] if swa is not None else 0
     swa_dt = _dt(swa) if swa is not None else F32
     if out is None:
-        out = torch.empty((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
+        out = alloc((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
     if want_lse and lse is None:
-        lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
+        lse = alloc((B, Q, H), dtype=torch.float32, device=q.device)
     if ws is None:
         nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k, window, q.device.index, N=N, swa_cap=swa_cap)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        ws = alloc(max(nb, 16), dtype=torch.uint8, device=q.device)
     st = _lib().csa2_sparse_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(idx), k, _p(swa), swa_dt,
                                  swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
                                  _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))
@@ -473,12 +480,12 @@ def csa2_dense_attn(q, kv, n_visible, k_max: int, swa, q_pos, sink=None, window:
     swa_cap = swa.shape[1] if swa is not None else 0
     swa_dt = _dt(swa) if swa is not None else F32
     if out is None:
-        out = torch.empty((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
+        out = alloc((B, Q, H, c), dtype=out_dtype or q.dtype, device=q.device)
     if want_lse and lse is None:
-        lse = torch.empty((B, Q, H), dtype=torch.float32, device=q.device)
+        lse = alloc((B, Q, H), dtype=torch.float32, device=q.device)
     if ws is None:
         nb = csa2_sparse_attn_workspace_bytes(B, Q, H, k_max, window, q.device.index, N=N, swa_cap=swa_cap)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        ws = alloc(max(nb, 16), dtype=torch.uint8, device=q.device)
     st = _lib().csa2_dense_attn(ctx(q.device.index), _p(q), _dt(q), _p(kv), kv_dt, N, _p(n_visible), k_max, _p(swa),
                                 swa_dt, swa_cap, swa_pos0, window, _p(q_pos), _p(sink), B, Q, H, c, rope_base, flags,
                                 _p(out), _dt(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream(q))

@@ -102,6 +102,7 @@ struct TcArgs {
     int64_t items;
     unsigned int* st;
     long long budget;
+    int stall;                    // test hook: the query-image producer issues nothing
     int cluster;                  // 1: a query's splits are one thread-block cluster (one item per
                                   // CTA) and merge their partials at the end of the kernel
 };
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         // ============================ producer ============================
         if (lane == 0) {
             int qi = 0, issued_q = -1;
-            for (int64_t item = blockIdx.x; item < a.items; item += gridDim.x) {
+            for (int64_t item = blockIdx.x; item < a.items && !a.stall; item += gridDim.x) {
                 const ItemInfo it = item_info(a, item);
                 if (it.nt == 0) continue;
                 if (qi > 0 && !mbar_wait(qempty, (qi - 1) & 1, a.budget, a.st)) break;
@@ -1156,6 +1157,12 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.items = n_bq * L.n_split;
     a.st = ctx->status;
     a.budget = WAIT_BUDGET;
+    a.stall = 0;
+    if (ctx->stall_next) {
+        a.stall = 1;
+        if (ctx->stall_budget > 0) a.budget = ctx->stall_budget;
+        ctx->stall_next = 0;
+    }
     *n_split = L.n_split;
     a.cluster = 0;
     const bool fp4 = c.kv_dt == CSA2_FP4_E4M3x16;

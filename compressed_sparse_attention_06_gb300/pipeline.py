@@ -58,21 +58,21 @@ def alloc_decode(B: int, Q: int, N: int, H: int, c: int, device, out_dtype=torch
     nb = (N + block - 1) // block
     n_top = top_blocks_for(k)
     return DecodeBuffers(
-        scores=torch.empty((B, Q, N), dtype=torch.float32, device=device),
-        block_max=torch.empty((B, Q, nb), dtype=torch.float32, device=device),
-        block_hist=torch.empty((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=device),
-        pool=torch.empty((B, Q, n_keep), dtype=torch.int32, device=device),
-        top_blocks=torch.empty((B, Q, n_top), dtype=torch.int32, device=device),
-        cand_scores=torch.empty((B, Q, n_top * block), dtype=torch.float32, device=device),
-        idx=torch.empty((B, Q, k), dtype=torch.int32, device=device),
-        out=torch.empty((B, Q, H, c), dtype=out_dtype, device=device),
-        attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
+        scores=C.alloc((B, Q, N), dtype=torch.float32, device=device),
+        block_max=C.alloc((B, Q, nb), dtype=torch.float32, device=device),
+        block_hist=C.alloc((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=device),
+        pool=C.alloc((B, Q, n_keep), dtype=torch.int32, device=device),
+        top_blocks=C.alloc((B, Q, n_top), dtype=torch.int32, device=device),
+        cand_scores=C.alloc((B, Q, n_top * block), dtype=torch.float32, device=device),
+        idx=C.alloc((B, Q, k), dtype=torch.int32, device=device),
+        out=C.alloc((B, Q, H, c), dtype=out_dtype, device=device),
+        attn_ws=C.alloc(max(16, C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window,
                                                                        torch.device(device).index, N=N,
                                                                        swa_cap=window)),
                             dtype=torch.uint8, device=device),
         pool_ws=C._ws(C.csa2_block_pool_workspace_bytes(B * Q, nb, n_keep, torch.device(device).index), device),
         topk_ws=C._ws(C.csa2_topk_workspace_bytes(B * Q, n_top * block, k, torch.device(device).index), device),
-        qI_mx=torch.empty((B, Q, h_idx, C.mxfp4_row_bytes(128)), dtype=torch.uint8, device=device),
+        qI_mx=C.alloc((B, Q, h_idx, C.mxfp4_row_bytes(128)), dtype=torch.uint8, device=device),
     )
 
 
@@ -176,11 +176,11 @@ def alloc_prefill(Q: int, N: int, H: int, c: int, device, q_pos: torch.Tensor, m
     """swa_cap: rows of the window buffer the attention will read (sizes the workspace
     for the per-call table of row RMS factors)."""
     return PrefillBuffers(
-        scores=torch.empty((1, Q, N), dtype=torch.float32, device=device),
-        idx=torch.empty((1, Q, k), dtype=torch.int32, device=device),
-        out=torch.empty((1, Q, H, c), dtype=out_dtype, device=device),
+        scores=C.alloc((1, Q, N), dtype=torch.float32, device=device),
+        idx=C.alloc((1, Q, k), dtype=torch.int32, device=device),
+        out=C.alloc((1, Q, H, c), dtype=out_dtype, device=device),
         n_visible=visible_entries(q_pos, m),
-        attn_ws=torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(1, Q, H, k, window,
+        attn_ws=C.alloc(max(16, C.csa2_sparse_attn_workspace_bytes(1, Q, H, k, window,
                                                                        torch.device(device).index, N=N,
                                                                        swa_cap=swa_cap)),
                             dtype=torch.uint8, device=device),

@@ -154,9 +154,9 @@ def rank_select(qI, w, kI_local, lo: int, n_visible: torch.Tensor, k: int = 512,
     qI = P.mxfp4_query(qI, kI_local)
     nb = (N_r + block - 1) // block
     dev = n_visible.device
-    bmax = torch.empty((B, Q, nb), dtype=torch.float32, device=dev)
+    bmax = C.alloc((B, Q, nb), dtype=torch.float32, device=dev)
     C.csa2_index_score(qI, w, kI_local, nv, block=block, want_scores=False, want_block_max=True, block_max=bmax)
-    pool = torch.empty((B, Q, n_keep), dtype=torch.int32, device=dev)
+    pool = C.alloc((B, Q, n_keep), dtype=torch.int32, device=dev)
     C.csa2_block_pool(bmax, nv, block=block, n_keep=n_keep, out=pool)
     sc, _ = C.csa2_index_score(qI, w, kI_local, nv, pool=pool, block=block)
     ids, top_sc = C.csa2_topk(sc, nv, k, pool=pool, block=block, want_scores=True)

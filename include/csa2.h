@@ -80,11 +80,15 @@ csa2_status csa2_ctx_destroy(csa2_ctx* ctx);
    itself reports an error. */
 csa2_status csa2_ctx_check(csa2_ctx* ctx, void* stream);
 
-/* Failure-detection test hook.  The next tensor-core indexer launch on this
-   context runs with a producer that never signals its consumers, whose bounded
-   waits then expire after `budget_cycles` (0 = the default of 2^31 cycles) and
-   record CSA2_ERR_TIMEOUT; the kernel frees its tensor memory and exits, and the
-   context stays usable.  The flag clears after that one launch. */
+/* Failure-detection test hook.  The next tensor-core launch on this context (an
+   indexer scan, or the sparse attention's tensor-core kernel) runs with a producer
+   that never signals its consumers (the scan's key copies, the attention's query
+   images), whose bounded waits then expire after `budget_cycles` (0 = the default
+   of 2^31 cycles) and record CSA2_ERR_TIMEOUT; the kernel waits for the copies it
+   did issue, frees its tensor memory and exits, and the context stays usable.  The
+   flag clears after that one launch.  The selection kernels have no waits to
+   expire: their only synchronisation is the hardware barrier of a co-scheduled
+   thread-block cluster. */
 csa2_status csa2_ctx_test_stall_next(csa2_ctx* ctx, long long budget_cycles);
 
 /*

@@ -119,3 +119,46 @@ def assert_exact_grid_scores(qI, w, KI, V, p):
     K = np.asarray(KI, dtype=np.float64)[:V]
     tot = np.abs(K) @ np.abs(qI).T @ np.abs(w)                 # [V]
     assert tot.max() < 2.0 ** (24 - p), f"term sums up to {tot.max()} exceed 2^{24 - p}"
+
+
+GUARD_BYTES = 4096          # keeps the 256-byte alignment of the allocation it sits in
+GUARD_FILL = 0xA5
+
+
+class GuardedAlloc:
+    """Stand-in for the binding's allocator in the GPU tests: every buffer the
+    binding (or pipeline.py) allocates sits between two guard regions filled with
+    GUARD_FILL, and verify() checks on the host that no call wrote outside its
+    buffer.  Only buffers still alive are checked (a freed one may be reused)."""
+
+    def __init__(self):
+        import weakref
+        self._weakref = weakref
+        self.live = []
+        self.checked = 0
+
+    def alloc(self, shape, dtype, device):
+        shape = (int(shape),) if isinstance(shape, int) else tuple(int(s) for s in shape)
+        n = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        raw = torch.full((GUARD_BYTES + n + GUARD_BYTES,), GUARD_FILL, dtype=torch.uint8, device=device)
+        view = raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+        view._guard_raw = raw                        # the whole allocation lives as long as the view
+        self.live.append((self._weakref.ref(view), n))
+        return view
+
+    def verify(self, what=""):
+        keep, bad = [], []
+        if any(r() is not None and r().is_cuda for r, _ in self.live):
+            torch.cuda.synchronize()
+        for r, n in self.live:
+            v = r()
+            if v is None:
+                continue
+            keep.append((r, n))
+            raw = v._guard_raw
+            head, tail = raw[:GUARD_BYTES], raw[GUARD_BYTES + n:]
+            if not (bool((head == GUARD_FILL).all()) and bool((tail == GUARD_FILL).all())):
+                bad.append((tuple(v.shape), v.dtype))
+            self.checked += 1
+        self.live = keep
+        assert not bad, f"{what}: a call wrote outside its buffer(s) {bad}"

@@ -170,3 +170,32 @@ def test_prepared_query_half_equals_one_call(B):
     C.csa2_ctx_check()
     assert torch.equal(out, ref)
     assert torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("shape", ["one_split", "key_splits"])
+def test_bounded_wait_times_out_and_context_recovers(shape):
+    """The attention kernel with a query-image producer that never signals (test
+    hook): its consumers' bounded waits expire (about 2^27 cycles), the call reports
+    a timeout instead of hanging, and the next call on the same context returns the
+    same bits as a call made before the stall.  key_splits runs the splits of a
+    query as one thread-block cluster (merged in the kernel)."""
+    if shape == "one_split":
+        B, Q, H, N, k, window, cap = 1, 4, 64, 3000, 300, 128, 128
+        pos = [[N + 5 * i for i in range(Q)]]
+    else:
+        B, Q, H, N, k, window, cap = 2, 2, 64, 2500, 200, 300, 320
+        pos = [[10, 5000], [299, 4000]]
+    q, kv, kv_np, idx, swa, q_pos, sink = _case(311, B, Q, H, N, k, window, cap, pos, "fp4", n_pad=13)
+    ref, ref_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
+                                      want_lse=True)
+    C.csa2_ctx_check()
+    C.csa2_ctx_test_stall_next(1 << 27)
+    C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32, want_lse=True)
+    with pytest.raises(C.Csa2Error) as e:
+        C.csa2_ctx_check()
+    assert e.value.status == C.ERR_TIMEOUT
+    out, lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
+                                  want_lse=True)
+    C.csa2_ctx_check()
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    _check(q, kv_np, idx, swa, q_pos, sink, window, to_np(out), to_np(lse), [(0, 0), (B - 1, Q - 1)])
