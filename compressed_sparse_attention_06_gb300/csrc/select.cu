@@ -17,7 +17,13 @@
 //     those (the union of per-chunk top-k lists contains the row's top-k under the
 //     same total order);
 //   * without a workspace a long row falls back to one CTA reading global memory
-//     on every pass.
+//     on every pass;
+//   * few long rows (decode) run as one thread-block cluster per row, the digits
+//     counted per CTA and combined through distributed shared memory (cluster
+//     selection, below);
+//   * the decode pool, and the pool fused with the top-k of the best blocks' entries
+//     (csa2_pool_topk), start from the first-digit histogram the indexer scan counted
+//     (pool from a histogram, below).
 // The threshold search takes a 12-bit histogram over every key, copies the keys of
 // the threshold bin aside and resolves the remaining 20 bits on that copy; a warp
 // whose keys share a digit (scores of one row often share their top bits) counts

@@ -8,8 +8,10 @@ Two errors per point:
     scores (relative to their rms), the top-512 (exact up to the tie window) and
     the attention output (the parity rule, 2e-2 for a bf16 output path).  Asserted.
   * format error -- the same step against the oracle on the unquantised inputs (f32
-    rows, the oracle's own selection on unquantised scores): what FP4 or bf16
-    storage costs.  Reported, not asserted (it is a property of the format).
+    rows): with the step's own selection (what the row format costs the attention)
+    and with the oracle's own selection on unquantised scores (what the format costs
+    the whole layer, selection changes included), as relative L2 errors, plus the
+    overlap of the two selections.  Reported, not asserted (a property of the format).
 With CSA2_ERROR_REPORT set, each point is appended to that file as a JSON line."""
 import json
 import os
@@ -34,6 +36,12 @@ def _rel(g, o):
     """max |g - o| / (|o| + rms(o)): the parity rule's measure."""
     g, o = np.asarray(g, dtype=np.float64), np.asarray(o, dtype=np.float64)
     return float(np.max(np.abs(g - o) / (np.abs(o) + np.sqrt(np.mean(o ** 2)))))
+
+
+def _l2(g, o):
+    """||g - o|| / ||o|| over every head and dimension."""
+    g, o = np.asarray(g, dtype=np.float64), np.asarray(o, dtype=np.float64)
+    return float(np.linalg.norm(g - o) / np.linalg.norm(o))
 
 
 def _oracle_scores(qI, w, rows_f32, V, fmt):
@@ -108,13 +116,15 @@ def test_error_by_context_length(path, N):
     kernel_err = _rel(g_out, o_ref)
     assert_close(g_out, o_ref, 2e-2, f"{path} {N}: attention")
     # the oracle on unquantised inputs: what the storage format costs
+    o_same, _, _ = O.sparse_attn(q, _rows(kv_h, g_idx[g_idx >= 0], "f32"), g_idx, swa, 0, tpos, sink, 128)
     sc_f = _oracle_scores(qI_bf.astype(np.float64), w, ki_h, V, "f32")
     idx_f = O.topk(sc_f, V, 512)
     o_f, _, _ = O.sparse_attn(q, _rows(kv_h, idx_f[idx_f >= 0], "f32"), idx_f, swa, 0, tpos, sink, 128)
     overlap = len(set(g_idx.tolist()) & set(idx_f.tolist())) / 512.0
     rec = dict(path=path, N=N, visible=V, score_err_rel_rms=score_err, topk_tie_swaps=swaps,
-               attn_kernel_err=kernel_err, attn_format_err=_rel(g_out, o_f), topk_overlap_with_f32=overlap,
-               score_format_err_rel_rms=float(np.max(np.abs(sc[:V] - sc_f[:V]))) / rms)
+               attn_kernel_err_max=kernel_err, attn_kernel_err_l2=_l2(g_out, o_ref),
+               attn_format_err_l2_same_selection=_l2(g_out, o_same), attn_format_err_l2=_l2(g_out, o_f),
+               topk_overlap_with_f32=overlap, score_format_err_rel_rms=float(np.max(np.abs(sc[:V] - sc_f[:V]))) / rms)
     print(json.dumps(rec))
     path_out = os.environ.get("CSA2_ERROR_REPORT")
     if path_out:
