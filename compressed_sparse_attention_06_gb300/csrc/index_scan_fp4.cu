@@ -21,9 +21,10 @@
 //
 // One CTA per SM (the grid splits each query's tiles over the SMs), 22 warps:
 //   warp 0       producer, into an 8-stage ring of tiles.  Full scan: a tile is
-//                17408 contiguous bytes, one bulk copy; four lanes issue them, lane p
-//                owning stages p and p+4 (one issuing thread alone sustains well under
-//                the HBM read rate).  Candidates: a tile is 32 blocks of 544 bytes;
+//                17408 contiguous bytes, one bulk copy with an evict-first L2 policy
+//                (the keys are read once); four lanes issue them, lane p owning stages
+//                p and p+4 (one issuing thread alone sustains well under the HBM read
+//                rate).  Candidates: a tile is 32 blocks of 544 bytes;
 //                each of the 32 lanes issues one 544-byte bulk copy with its own
 //                expect-tx arrival on the stage barrier (an empty pool slot only
 //                arrives).
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
             // lane p issues tiles p, p+PL, ... (so it alone uses stages p, p+PL, ...);
             // a bulk copy of rows*68 bytes (rows a multiple of 8: a multiple of 16 B)
             constexpr int PL = PROD_LANES;
+            const uint64_t pol = policy_evict_first();
             if (lane < PL) {
                 int last = -1;
                 for (int li = lane; li < (a.stall ? 0 : n_act); li += PL) {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
                     const int64_t row0 = (int64_t)(t_begin + li) * TILE;
                     const uint32_t bytes = (uint32_t)(min((int64_t)TILE, a.N - row0) * MX_ROW);
                     mbar_arrive_expect_tx(&full[s], bytes);
-                    bulk_g2s(sStage + s * MX_STAGE, a.kmx + ((int64_t)b * a.N + row0) * MX_ROW, bytes, &full[s]);
+                    bulk_g2s_hint(sStage + s * MX_STAGE, a.kmx + ((int64_t)b * a.N + row0) * MX_ROW, bytes, &full[s], pol);
                     last = li;
                 }
                 // no copy may still be writing shared memory when the CTA exits: wait
