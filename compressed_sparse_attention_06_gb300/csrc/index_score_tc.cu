@@ -11,6 +11,8 @@
 //
 // Warp roles (320 threads):
 //   warp 0     producer: bulk / TMA copies of key tiles into a shared-memory ring
+//              (bf16 candidates: the 32 lanes each issue one of the tile's 32 tensor
+//              copies, 1 KB each, a third faster than one lane issuing all of them)
 //   warp 1     MMA issuer (one lane); owns the tensor-memory allocation
 //   warps 2-5  converters (MXFP4 keys only): each thread takes one entry row of the
 //              staged tile, turns its 128 E2M1 codes into f16 with the block scale
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
     // ---- set-up: barriers, tensor memory, the B operand (queries) and head weights
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], (CAND && KF == KF_BF16) ? 32 : 1);
             mbar_init(&empty[i], KF == KF_MX ? 4 : 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -232,7 +234,35 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
 
     if (warp == 0) {
         // ============================ producer ============================
-        if (lane == 0) {
+        if (CAND && KF == KF_BF16) {
+            // 16 pooled blocks per tile, two 64-dim halves each: lane l copies half l / 16
+            // of block l % 16 (one 1 KB tensor copy), with its own arrival on the stage
+            // barrier; an empty pool slot only arrives
+            int issued = 0;
+            const int j = lane & 15, hf = lane >> 4;
+            const int64_t gq = (int64_t)b * a.Q + q0;
+            for (int li = 0; li < (a.stall ? 0 : n_act); ++li) {
+                const int s = li % C::STAGES, r = li / C::STAGES;
+                const bool w = r == 0 || mbar_wait(&empty[s], (r - 1) & 1, a.budget, a.st);
+                if (!__all_sync(0xffffffffu, w)) break;
+                const int tile = t_begin + li;
+                uint8_t* dst = sStage + s * C::STAGE_BYTES;
+                const int64_t pi = (int64_t)tile * 16 + j;
+                int32_t pb = pi < a.n_pool ? a.pool[gq * a.n_pool + pi] : -1;
+                if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
+                if (pb >= 0) {
+                    mbar_arrive_expect_tx(&full[s], 1024);
+                    tma_load_2d(dst + hf * (BF_STAGE / 2) + j * 1024, &tmap_blk, 64 * hf,
+                                (int32_t)((int64_t)b * a.N + (int64_t)pb * 8), &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);
+                }
+                ++issued;
+            }
+            if (lane == 0)
+                for (int li = max(0, issued - C::STAGES); li < issued; ++li)
+                    mbar_wait(&full[li % C::STAGES], (li / C::STAGES) & 1, a.budget, a.st);
+        } else if (lane == 0) {
             int issued = 0;
             for (int li = 0; li < (a.stall ? 0 : n_act) && ok; ++li) {
                 const int s = li % C::STAGES, r = li / C::STAGES;
