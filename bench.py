@@ -304,13 +304,28 @@ class FP4Decode(Workload):
         C.csa2_fp4_pack(self.qI, C.MXFP4_E8M0x32, out=self.qI_mx)     # the QK path runs in FP4
 
     def main(self):
-        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block, scores=self.buf.scores,
+        # every score is stored only for the fused selection, which reads those of the
+        # best blocks
+        fused = self.fused_select()
+        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block,
+                              scores=self.buf.scores if fused else None, want_scores=fused,
                               want_block_max=True, block_max=self.buf.block_max, block_hist=self.buf.block_hist)
 
+    def fused_select(self):
+        from compressed_sparse_attention_06_gb300 import pipeline as P
+        return P.pool_topk_applies(self.k, self.block, self.n_keep, self.buf.block_max.shape[-1])
+
     def select(self):
+        """The pool and the layer's top-k: one cluster kernel from the stored scores of
+        the k best blocks where that kernel takes the shape (k * block <= 4,096), else
+        the pool with its best-block list, the candidate scan of those blocks and the
+        cluster top-k (V4-Pro's top-1024)."""
         b = self.buf
-        _C().csa2_pool_topk(b.block_max, b.block_hist, b.scores, self.nv, self.k, block=self.block,
-                            n_keep=self.n_keep, out=b.pool, out_idx=b.idx)
+        if self.fused_select():
+            _C().csa2_pool_topk(b.block_max, b.block_hist, b.scores, self.nv, self.k, block=self.block,
+                                n_keep=self.n_keep, out=b.pool, out_idx=b.idx)
+        else:
+            self.pool(); self.cand(); self.topk()
 
     def scan_bf16_query(self):
         """The other reading of the pages: the bf16 indexer query over the same MXFP4
@@ -371,9 +386,10 @@ class FP4Decode(Workload):
         self.select(); self.attn(prepared=self.prep_early)
 
     def launches_per_step(self):
-        # compress, 2 packs, histogram zeroing, scan, pool + top-k, then per 64-head pass
-        # of the attention: query prep, attention (its key splits merged in the kernel)
-        return 6 + 2 * ((self.H + 63) // 64)
+        # compress, 2 packs, histogram zeroing, scan, pool + top-k (or pool, candidate
+        # scan, top-k), then per 64-head pass of the attention: query prep, attention
+        # (its key splits merged in the kernel)
+        return (6 if self.fused_select() else 8) + 2 * ((self.H + 63) // 64)
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row

@@ -32,7 +32,7 @@ EXPORTS = (
     "csa2_block_pool", "csa2_sparse_attn", "csa2_sparse_attn_workspace_bytes", "csa2_sparse_attn_noalloc",
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
     "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
-    "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist", "csa2_attn_prepare",
+    "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist", "csa2_attn_prepare", "csa2_visible_entries",
 )
 
 
@@ -66,6 +66,7 @@ def _declare(lib):
         "csa2_compress_state_seed": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _vp, _vp]),
         "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
+        "csa2_visible_entries": (_i, [_vp, _vp, _i64, _i, _vp, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
                                   _vp, _vp, _vp]),
         "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -292,6 +293,23 @@ def csa2_compress(ca, za, m: int, cb=None, zb=None, ba=None, bb=None, prev_cb=No
                               _p(prev_cb), _p(prev_zb), B, n, c, m, _p(pos_t), rope_base, flags,
                               _vp(out.data_ptr()), out_dt, oss, _stream(ca))
     _check("csa2_compress", st)
+    return out
+
+
+def csa2_visible_entries(q_pos: torch.Tensor, m: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Entries visible to each query position, floor(t / m) (0 for t < 0): the causal
+    rule of the compressed cache (DSA-to-CSA/HCA page, «因果边界与短滑窗»).  q_pos:
+    int64 device tensor of any shape; returns the same shape."""
+    if q_pos.dtype != torch.int64 or not q_pos.is_cuda:
+        raise ValueError("q_pos must be an int64 CUDA tensor")
+    q_pos = q_pos.contiguous()
+    if out is None:
+        out = alloc(tuple(q_pos.shape), dtype=torch.int64, device=q_pos.device)
+    if out.shape != q_pos.shape or out.dtype != torch.int64 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int64 tensor shaped like q_pos")
+    st = _lib().csa2_visible_entries(ctx(q_pos.device.index), _p(q_pos), q_pos.numel(), int(m), _p(out),
+                                     _stream(q_pos))
+    _check("csa2_visible_entries", st)
     return out
 
 

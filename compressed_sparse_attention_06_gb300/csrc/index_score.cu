@@ -11,6 +11,8 @@
 // for them.  MXFP4 queries are dequantised into shared memory.
 #include <type_traits>
 
+#include <algorithm>
+
 #include "csa2_internal.cuh"
 #include "index_score_tc.cuh"
 
@@ -147,7 +149,28 @@ void launch_simt(const void* qI, const float* w, const void* kI, int B, int Q, i
                                                                  n_pool, block, scores, bmax, st);
 }
 
+// Entries visible to each query: entry j needs t >= m(j+1), so floor(t/m) of them
+// (a negative position sees none).
+__global__ void visible_kernel(const int64_t* q_pos, int64_t rows, int m, int64_t* nv) {
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = q_pos[i];
+        nv[i] = t >= 0 ? t / m : 0;
+    }
+    pdl_trigger();
+}
+
 }  // namespace
+
+extern "C" csa2_status csa2_visible_entries(csa2_ctx* ctx, const int64_t* q_pos, int64_t rows, int m,
+                                            int64_t* n_visible, void* stream) {
+    if (!ctx || rows < 0 || m < 1) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0) return CSA2_OK;
+    if (!q_pos || !n_visible) return CSA2_ERR_INVALID_ARG;
+    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 4 * (int64_t)ctx->num_sms);
+    return launch_pdl(visible_kernel, dim3((unsigned)blocks), dim3(256), 0, as_stream(stream), q_pos, rows, m,
+                      n_visible);
+}
 
 extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_dtype q_dt, const float* w,
                                         const void* k_idx, csa2_dtype k_dt, int B, int Q, int64_t N, int H_I,

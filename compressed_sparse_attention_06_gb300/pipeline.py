@@ -24,8 +24,8 @@ POOL_KEEP = 2048
 
 def visible_entries(q_pos: torch.Tensor, m: int) -> torch.Tensor:
     """Entries visible to each query: entry j needs t >= m(j+1), so floor(t/m)
-    (DSA-to-CSA/HCA page, «因果边界与短滑窗»)."""
-    return torch.div(q_pos, m, rounding_mode="floor")
+    (DSA-to-CSA/HCA page, «因果边界与短滑窗»); computed by csa2_visible_entries."""
+    return C.csa2_visible_entries(q_pos, m)
 
 
 @dataclass
@@ -95,8 +95,9 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
     side_stream: the attention's query half (csa2_attn_prepare) runs there, beside
     the selection, after the scan (which fills the GPU by itself)."""
     qI = mxfp4_query(qI, kI, buf.qI_mx)
-    C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores, want_block_max=True,
-                       block_max=buf.block_max, block_hist=buf.block_hist)
+    fused = pool_topk_applies(k, block, n_keep, buf.block_max.shape[-1])
+    C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores if fused else None, want_scores=fused,
+                       want_block_max=True, block_max=buf.block_max, block_hist=buf.block_hist)
     B, Q, H = q.shape[:3]
     prepared = side_stream is not None and H <= 64
     if prepared:
@@ -104,7 +105,7 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
         with torch.cuda.stream(side_stream):
             C.csa2_attn_prepare(q, q_pos, buf.attn_ws, k, window=window, N=kv.shape[1], swa_cap=swa.shape[1],
                                 flags=flags)
-    if pool_topk_applies(k, block, n_keep, buf.block_max.shape[-1]):
+    if fused:
         C.csa2_pool_topk(buf.block_max, buf.block_hist, buf.scores, n_visible, k, block=block, n_keep=n_keep,
                          out=buf.pool, out_idx=buf.idx)
     else:

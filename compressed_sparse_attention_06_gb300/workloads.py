@@ -167,10 +167,6 @@ class Workload:
     def __getitem__(self, k):
         return self.tensors[k]
 
-    def n_visible(self) -> torch.Tensor:
-        """Entries visible to each query, floor(t / m), as the causal rule states."""
-        return torch.div(self.q_pos, self.m, rounding_mode="floor")
-
 
 def _wid_seed(wid: int, stream: int) -> int:
     return wid * 1000 + stream

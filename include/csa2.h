@@ -202,6 +202,20 @@ csa2_status csa2_fp4_unpack(csa2_ctx* ctx, const uint8_t* in, csa2_dtype fmt, in
                             int c, void* out, csa2_dtype out_dt, void* stream);
 
 /*
+ * csa2_visible_entries -- the causal rule of the compressed cache (DSA-to-CSA/HCA
+ * page, «因果边界与短滑窗»): compressed entry j (made from tokens mj .. mj+m-1) is
+ * visible to the query at position t iff t >= m(j+1), so a query sees
+ *     n_visible[i] = floor(q_pos[i] / m)      (0 for a negative position)
+ * entries.  The n_visible arrays the indexer, the selections and the dense attention
+ * take are this.
+ *   q_pos     : [rows] int64, device
+ *   n_visible : [rows] int64, device (may alias q_pos)
+ *   m >= 1.  Asynchronous on `stream`; invalid arguments return before any launch.
+ */
+csa2_status csa2_visible_entries(csa2_ctx* ctx, const int64_t* q_pos, int64_t rows, int m, int64_t* n_visible,
+                                 void* stream);
+
+/*
  * csa2_index_score -- Lightning-indexer scores (DSA-to-CSA/HCA page eq. (16)):
  *     I[b,q,s] = sum_h w[b,q,h] * ReLU(q_idx[b,q,h,:] . k_idx[b,s,:])
  * with no scale and no softmax, for the entries visible to the query

@@ -57,6 +57,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.csa2_sparse_attn(None, None, 0, None, 0, 0, None, 0, None, 0, 0, 0, 0, None, None, 1, 1, 64, 512,
                                 10000.0, 7, None, 0, None, None, 0, None) == C.ERR_INVALID_ARG
     assert lib.csa2_sparse_attn_workspace_bytes(None, 8, 1, 64, 512, 128, 1000, 128) == 0
+    assert lib.csa2_visible_entries(None, None, 4, 2, None, None) == C.ERR_INVALID_ARG
     assert lib.csa2_ctx_destroy(None) == C.ERR_INVALID_ARG
     assert lib.csa2_ctx_check(None, None) == C.ERR_INVALID_ARG
 

@@ -554,3 +554,20 @@ def test_pool_topk_rejects_too_many_candidates():
     hist = C.csa2_block_hist(bm, nv, 8)
     with pytest.raises(C.Csa2Error):
         C.csa2_pool_topk(bm, hist, s, nv, 1024)
+
+
+def test_visible_entries_causal_rule():
+    """floor(t / m) per query position, the oracle's visibility rule, over positions
+    around every block edge, far positions and negative ones (which see nothing)."""
+    pos = [-5, -1, 0, 1, 3, 4, 5, 127, 128, 129, 4095, 4096, 1 << 20, (1 << 20) - 1, (1 << 40) + 3]
+    for m in (1, 2, 4, 128):
+        t = torch.tensor(pos, dtype=torch.int64, device="cuda")
+        nv = C.csa2_visible_entries(t.view(3, 5), m)
+        C.csa2_ctx_check()
+        ref = [O.visible_entries(p, m) if p >= 0 else 0 for p in pos]
+        assert nv.view(-1).cpu().tolist() == ref, m
+        # in place
+        C.csa2_visible_entries(t, m, out=t)
+        assert t.cpu().tolist() == ref
+    with pytest.raises(ValueError):
+        C.csa2_visible_entries(torch.zeros(3, dtype=torch.int32, device="cuda"), 2)

@@ -175,7 +175,14 @@ def _run_fp4_decode(B, N, H, k, grid):
         ki_ref, qI_ref, sc = futs[b].result()
         np.testing.assert_array_equal(to_np(ki[b]), ki_ref, err_msg=f"{what}: MXFP4 cache bytes")
         np.testing.assert_array_equal(to_np(buf.qI_mx[b, 0]), qI_ref, err_msg=f"{what}: MXFP4 query bytes")
-        if grid:
+        if not P.pool_topk_applies(k, 8, 2048, buf.block_max.shape[-1]):
+            # top-1024: the step rescored its best blocks with the candidate scan
+            tb = to_np(buf.top_blocks[b, 0]).astype(np.int64)
+            ids = (tb[:, None] * 8 + np.arange(8)).reshape(-1)
+            ok = np.repeat(tb >= 0, 8) & (ids < V)
+            assert ok.sum() >= k
+            assert_close(to_np(buf.cand_scores[b, 0])[ok], sc[ids[ok]], 1e-5, f"{what}: best blocks' scores")
+        elif grid:
             assert_exact_grid_scores(O.mxfp4_unpack(qI_ref), _np(wl["w"][b, 0]), O.mxfp4_unpack(ki_ref), V, 3)
             np.testing.assert_array_equal(to_np(buf.scores[b, 0])[:V], sc[:V], err_msg=f"{what}: scores")
         else:
