@@ -436,7 +436,7 @@ class FP4Decode(Workload):
                         swa=wl["swa"][b].double().cpu().numpy(), sink=wl["sink"].double().cpu().numpy())
         # the selection is the top-k of all scores (the pool lemma), so the rows to hand
         # over are known before the timed queries
-        sc = NO.index_score(NO.mxfp4_unpack(self.o_qmx), self.o_q["w"], NO.mxfp4_unpack(self.o_ki[:V]), V)
+        sc = O.index_score(NO.mxfp4_unpack(self.o_qmx), self.o_q["w"], NO.mxfp4_unpack(self.o_ki[:V]), V)
         ids = O.topk(sc, V, self.k)
         self.o_ids = ids[ids >= 0]
         self.o_kv = np.concatenate([NO.nvfp4_pack(W.fp4_rows("kv", self.seq0 + b, int(s), 1, N, "cpu").numpy())
