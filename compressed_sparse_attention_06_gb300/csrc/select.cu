@@ -476,9 +476,10 @@ __device__ int staged_select(const Src src, int n, int k, SelShared& sh, uint64_
         cg += __popc(bmW[w]);
         ce += __popc(bmE[w]);
     }
+    // both counts in one scan: a chunk holds fewer than 2^16 keys, so neither half carries
     uint32_t tot;
-    uint32_t gb = block_excl_scan_u32(cg, sh, tot);
-    uint32_t eb = block_excl_scan_u32(ce, sh, tot);
+    const uint32_t both = block_excl_scan_u32(cg | (ce << 16), sh, tot);
+    uint32_t gb = both & 0xFFFFu, eb = both >> 16;
     for (int w = w0; w < w1; ++w) {
         const uint32_t wg = bmW[w], we = bmE[w];
         uint32_t bits = wg | we;
@@ -1199,8 +1200,14 @@ struct PhShared {
     uint32_t tmin_local;                   // ENTRY: the smallest maximum among this CTA's in-bin best blocks
     uint32_t tmin[PH_MAX_C];               // ENTRY: every CTA's tmin_local (pushed)
     uint32_t ndense;                       // ENTRY: received entries scoring at least the threshold
+    uint32_t nwin;                         // ENTRY: this CTA's winning entries
+    uint32_t nown_e;                       // ENTRY: received entries of this CTA's chunk
+    uint32_t wsum[2][32];                  // threshold search: per-warp bin sums (pool, best blocks)
+    int sbin[2];                           // threshold search: the bin, the keys above it, the keys in it
+    uint32_t sabove[2], sm[2];
 };
 constexpr int PH_ECAP = 8192;              // ENTRY: entry candidates a CTA can receive (64 KB)
+constexpr int PH_WCAP = 1024;              // ENTRY: winners emitted from a list (more: from the bitmap)
 // ENTRY reuses the two candidate-list arrays once the block selections are done:
 // `all` holds the received entries at or above the threshold (2 * PH_CAP of them, the
 // limit k * block <= 2 * PH_CAP keeps them within), `loc` the bitmap of a chunk's entries
@@ -1273,10 +1280,88 @@ __device__ __noinline__ void ph_emit_bits(const uint32_t* bm, int nwords, int64_
     }
 }
 
+// The threshold bins of both selections, searched from the top of the row's histogram
+// (NB_A bins in `full`): index 0 the pool (rank kP among the blocks other than the
+// newest, whose bin knew_bin counts one block less), index 1 the best blocks (rank kT);
+// a rank of 0 skips that search.  Thread t holds bins NB_A-1-4t .. NB_A-4-4t; the warps'
+// sums meet in shared memory and the thread whose bins hold the rank walks them.  Each
+// result: the bin, the keys in the bins above it, the keys in it (bin 0, 0, 0 when the
+// rank exceeds the count).  Two block barriers; blockDim.x * 4 == NB_A.
+__device__ __noinline__ void ph_search2(const uint32_t* full, uint32_t knew_bin, uint32_t kP, uint32_t kT,
+                                        PhShared& px) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int top = NB_A - 1 - 4 * tid;
+    const uint4 q = *reinterpret_cast<const uint4*>(full + top - 3);
+    const uint32_t cT[4] = {q.w, q.z, q.y, q.x};        // bins top, top-1, top-2, top-3
+    uint32_t cP[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cP[j] = cT[j] - ((uint32_t)(top - j) == knew_bin ? 1u : 0u);
+    const uint32_t sT = (cT[0] + cT[1]) + (cT[2] + cT[3]), sP = (cP[0] + cP[1]) + (cP[2] + cP[3]);
+    uint32_t iT = sT, iP = sP;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t uT = __shfl_up_sync(FULL_MASK, iT, o), uP = __shfl_up_sync(FULL_MASK, iP, o);
+        if (lane >= o) {
+            iT += uT;
+            iP += uP;
+        }
+    }
+    if (lane == 31) {
+        px.wsum[0][wid] = iP;
+        px.wsum[1][wid] = iT;
+    }
+    if (tid < 2) {
+        px.sbin[tid] = 0;
+        px.sabove[tid] = 0u;
+        px.sm[tid] = 0u;
+    }
+    __syncthreads();
+    // keys in the warps' bins above this warp's (every warp scans the 32 sums)
+    uint32_t wP = px.wsum[0][lane], wT = px.wsum[1][lane];
+    uint32_t jP = wP, jT = wT;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t uT = __shfl_up_sync(FULL_MASK, jT, o), uP = __shfl_up_sync(FULL_MASK, jP, o);
+        if (lane >= o) {
+            jT += uT;
+            jP += uP;
+        }
+    }
+    const uint32_t preP = __shfl_sync(FULL_MASK, jP - wP, wid), preT = __shfl_sync(FULL_MASK, jT - wT, wid);
+    const uint32_t exP = preP + iP - sP, exT = preT + iT - sT;
+    if (kT > 0u && exT < kT && kT <= exT + sT) {
+        uint32_t cum = exT;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (cum + cT[j] >= kT) {
+                px.sbin[1] = top - j;
+                px.sabove[1] = cum;
+                px.sm[1] = cT[j];
+                break;
+            }
+            cum += cT[j];
+        }
+    }
+    if (kP > 0u && exP < kP && kP <= exP + sP) {
+        uint32_t cum = exP;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (cum + cP[j] >= kP) {
+                px.sbin[0] = top - j;
+                px.sabove[0] = cum;
+                px.sm[0] = cP[j];
+                break;
+            }
+            cum += cP[j];
+        }
+    }
+    __syncthreads();
+}
+
 template <bool ENTRY>
 __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int chunk) {
     extern __shared__ __align__(16) uint32_t dyn[];
-    __shared__ ClShared sh;
+    __shared__ __align__(16) ClShared sh;
     __shared__ PhShared px;
     pdl_wait();                            // the block maxima, histogram and scores are complete
     const uint32_t C = cl_size(), rank = cl_rank();
@@ -1332,19 +1417,10 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     // the threshold bins of both selections
     const uint32_t k[2] = {(uint32_t)a.n_keep - 1u, (uint32_t)a.n_top};
     const bool act[2] = {!allP, !allT};
-    int bin[2] = {0, 0};
-    uint32_t above[2] = {0u, 0u}, m[2] = {0u, 0u};
-    if (act[1]) {
-        cl_search_full(sh, NB_A, k[1], bin[1], above[1]);
-        m[1] = sh.full[bin[1]];
-    }
-    if (act[0]) {                          // the newest block is not among the pool's candidates
-        __syncthreads();                   // every thread has read m[1] before the count changes
-        if (tid == 0) sh.full[knew >> 20] -= 1u;
-        __syncthreads();
-        cl_search_full(sh, NB_A, k[0], bin[0], above[0]);
-        m[0] = sh.full[bin[0]];
-    }
+    // (the newest block is not among the pool's candidates: its bin counts one less)
+    ph_search2(sh.full, knew >> 20, act[0] ? k[0] : 0u, act[1] ? k[1] : 0u, px);
+    int bin[2] = {px.sbin[0], px.sbin[1]};
+    uint32_t above[2] = {px.sabove[0], px.sabove[1]}, m[2] = {px.sm[0], px.sm[1]};
     // classify: the 32 keys of word w = i / 32 are lanes of one warp in one step
     const int cw = chunk / 32;
     const int nwords = (n + 31) / 32;
@@ -1451,6 +1527,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             for (uint32_t ci = wid; ci < nl; ci += CL_THREADS / 32) {
                 const uint64_t x = loc[s2 * PH_CAP + ci] ^ 0xFFFFFFFFull;
                 uint32_t ahead = 0u;
+#pragma unroll 4
                 for (uint32_t j = lane; j < mm; j += 32) ahead += A[j] > x;
                 ahead = __reduce_add_sync(FULL_MASK, ahead);
                 if (lane == 0 && ahead < r) {
@@ -1635,6 +1712,8 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         // rank this CTA's own entry candidates (entries of its chunk) against all
         // received ones; the winners go to a bitmap over the chunk's entries (in `loc`,
         // which no CTA reads after barrier (2))
+        __shared__ uint32_t wlist[PH_WCAP];  // this CTA's winners (entry offsets in the chunk), unordered
+        __shared__ uint32_t olist[PH_WCAP];  // where this CTA's own entries sit in `dense`
         const uint32_t me = min(px.ecnt, (uint32_t)PH_ECAP);
         const uint64_t* ec = reinterpret_cast<const uint64_t*>(skey);
         uint32_t* ebm = reinterpret_cast<uint32_t*>(loc);
@@ -1647,8 +1726,13 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             tkey = 0xFFFFFFFFu;
             for (uint32_t c = 0; c < C; ++c) tkey = min(tkey, px.tmin[c]);
         }
-        if (tid == 0) px.ndense = 0u;
+        if (tid == 0) {
+            px.ndense = 0u;
+            px.nwin = 0u;
+            px.nown_e = 0u;
+        }
         __syncthreads();
+        const int64_t e0 = c0 * a.block, e1 = (c0 + n) * a.block;
         // the received entries at or above the threshold, as (order value, entry), in `all`
         uint64_t* dense = all;
         for (uint32_t j0 = 0; j0 < me; j0 += bd) {
@@ -1659,36 +1743,39 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             uint32_t o = 0u;
             if (lane == 0) o = atomicAdd(&px.ndense, (uint32_t)__popc(km));
             o = __shfl_sync(FULL_MASK, o, 0) + __popc(km & lt);
-            if (keep && o < 2u * PH_CAP) dense[o] = ec[j] ^ 0xFFFFFFFFull;     // larger = earlier in the order
+            if (keep && o < 2u * PH_CAP) {
+                dense[o] = ec[j] ^ 0xFFFFFFFFull;     // larger = earlier in the order
+                const int64_t e = (int64_t)(uint32_t)ec[j];
+                if (e >= e0 && e < e1) {
+                    const uint32_t q = atomicAdd(&px.nown_e, 1u);
+                    if (q < (uint32_t)PH_WCAP) olist[q] = o;
+                }
+            }
         }
         __syncthreads();
         const uint32_t md = min(px.ndense, 2u * (uint32_t)PH_CAP);
-        const int64_t e0 = c0 * a.block, e1 = (c0 + n) * a.block;
-        // a warp per candidate of this CTA's chunk: winners rank below k
-        for (uint32_t ci = wid; ci < md; ci += CL_THREADS / 32) {
-            const uint64_t x = dense[ci];
+        // a warp per candidate of this CTA's chunk (from the list of them, else picked out
+        // of all received entries): winners rank below k
+        const uint32_t no = px.nown_e;
+        const bool listed = no <= (uint32_t)PH_WCAP;
+        for (uint32_t ci = wid; ci < (listed ? no : md); ci += CL_THREADS / 32) {
+            const uint64_t x = dense[listed ? olist[ci] : ci];
             const int64_t e = (int64_t)(uint32_t)(x ^ 0xFFFFFFFFull);
             if (e < e0 || e >= e1) continue;                     // the same for the whole warp
             uint32_t ahead = 0u;
+#pragma unroll 4
             for (uint32_t j = lane; j < md; j += 32) ahead += dense[j] > x;
             ahead = __reduce_add_sync(FULL_MASK, ahead);
             if (lane == 0 && ahead < (uint32_t)a.k) {
                 const uint32_t li = (uint32_t)(e - e0);
                 atomicOr(&ebm[li >> 5], 1u << (li & 31));
+                const uint32_t o = atomicAdd(&px.nwin, 1u);
+                if (o < (uint32_t)PH_WCAP) wlist[o] = li;
             }
         }
         __syncthreads();
-        uint32_t cwin = 0u;
-        for (int w = tid; w < ew; w += bd) cwin += __popc(ebm[w]);
-        cwin = __reduce_add_sync(FULL_MASK, cwin);
-        __shared__ uint32_t esum[CL_THREADS / 32];
-        if (lane == 0) esum[wid] = cwin;
-        __syncthreads();
-        if (tid < (int)C) {
-            uint32_t tw = 0u;
-            for (int i = 0; i < CL_THREADS / 32; ++i) tw += esum[i];
-            cl_st(cl_map(&px.ewin[rank], (uint32_t)tid), tw);
-        }
+        const uint32_t nwin = px.nwin;
+        if (tid < (int)C) cl_st(cl_map(&px.ewin[rank], (uint32_t)tid), nwin);
         cl_sync();                         // (3) every CTA's winner count is in every CTA
         uint32_t off = 0u, total = 0u;
         for (uint32_t c = 0; c < C; ++c) {
@@ -1697,7 +1784,23 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         }
         int32_t* oi = a.out_idx + row * a.k;
         float* ov = a.out_val ? a.out_val + row * a.k : nullptr;
-        ph_emit_bits(ebm, ew, e0, off, oi, ov, a.scores + row * a.n_ent, (uint32_t)a.k, sh);
+        if (nwin <= (uint32_t)PH_WCAP) {
+            // few winners: each one's place among this CTA's is the count of smaller ids
+            const float* vals = a.scores + row * a.n_ent;
+            for (uint32_t i = tid; i < nwin; i += bd) {
+                const uint32_t li = wlist[i];
+                uint32_t pos = 0u;
+                for (uint32_t j = 0; j < nwin; ++j) pos += wlist[j] < li;
+                pos += off;
+                if (pos < (uint32_t)a.k) {
+                    const int64_t id = e0 + li;
+                    oi[pos] = (int32_t)id;
+                    if (ov) ov[pos] = vals[id];
+                }
+            }
+        } else {
+            ph_emit_bits(ebm, ew, e0, off, oi, ov, a.scores + row * a.n_ent, (uint32_t)a.k, sh);
+        }
         for (int64_t i = (int64_t)total + (int64_t)rank * bd + tid; i < a.k; i += (int64_t)C * bd) {
             oi[i] = -1;
             if (ov) ov[i] = -INFINITY;

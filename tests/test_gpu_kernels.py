@@ -544,6 +544,35 @@ def test_pool_topk_bit_exact(V, ties, k):
 
 
 
+@pytest.mark.parametrize("order", ["rising", "falling", "random"])
+def test_pool_topk_blocks_of_one_many_winners(order):
+    """Blocks of one entry and k = 3,000: with rising scores every winner lies in the
+    last CTA's chunk (more winners than one CTA lists, so they are emitted from its
+    bitmap), with falling scores in the first, at random everywhere; pool and top-k
+    bit-exact with the oracle, equal scores included."""
+    N, k, n_keep = 131072, 3000, 4096
+    g = torch.Generator().manual_seed(7)
+    base = torch.arange(N, dtype=torch.float64)
+    if order == "falling":
+        base = -base
+    elif order == "random":
+        base = torch.randn(N, generator=g, dtype=torch.float64)
+    sc = torch.floor(base * 4) / 4                       # many equal scores
+    s = sc.to(torch.float32).view(1, N).to(DEV)
+    nv = torch.tensor([N - 5], dtype=torch.int64, device=DEV)
+    sn = s.double().cpu().numpy()[0]
+    V = int(nv[0])
+    bm = torch.tensor(O.block_max(np.where(np.arange(N) < V, sn, -np.inf), N, 1), dtype=torch.float32,
+                      device=DEV).view(1, N)
+    hist = C.csa2_block_hist(bm, nv, 1)
+    pool, idx, val = C.csa2_pool_topk(bm, hist, s, nv, k, block=1, n_keep=n_keep, want_scores=True)
+    C.csa2_ctx_check()
+    np.testing.assert_array_equal(to_np(pool)[0], O.block_pool(O.block_max(sn, V, 1), V, 1, n_keep))
+    ref = O.topk(sn, V, k)
+    np.testing.assert_array_equal(to_np(idx)[0], ref)
+    np.testing.assert_array_equal(to_np(val)[0], sn[ref])
+
+
 def test_pool_topk_rejects_too_many_candidates():
     """k * block above the candidate capacity is refused on the host (the decode step
     then takes the pool, the best blocks' rescoring and csa2_topk one by one)."""
