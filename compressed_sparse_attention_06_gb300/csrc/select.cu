@@ -1439,53 +1439,65 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         skey[i] = i < n ? order_key(v[j]) : 0u;
     }
     __syncthreads();
-    // classify: a thread per word of 32 keys, read as eight 16-byte pieces starting at a
-    // word-dependent piece (the lanes of a warp then spread over the banks)
-    for (int w = tid; w < nwords; w += bd) {
-        uint32_t g0 = 0u, e0 = 0u, g1 = 0u, e1 = 0u, vm = 0u;
-        // not unrolled: each CTA runs this once, from a cold instruction cache, and
-        // straight-line code there costs more in instruction fetch than the loop does
+    // classify: two threads per word of 32 keys (threads 2w and 2w+1 take its halves),
+    // each half read as four 16-byte pieces starting at a word-dependent piece (the
+    // lanes of a warp then spread over the banks); the halves' bits meet by shuffle
+    const int np2 = 2 * nwords;
+    for (int p0 = 0; p0 < np2; p0 += bd) {                 // the same bounds for every thread
+        const int pw = p0 + tid;
+        const bool on = pw < np2;
+        const int w = pw >> 1, h = pw & 1;
+        uint32_t g0 = 0u, g1 = 0u;
+        if (on) {
+            uint32_t e0 = 0u, e1 = 0u, vm = 0u;
+            // not unrolled: each CTA runs this once, from a cold instruction cache, and
+            // straight-line code there costs more in instruction fetch than the loop does
 #pragma unroll 1
-        for (int t = 0; t < 8; ++t) {
-            const int q = (t + w) & 7;
-            const uint4 k4 = *reinterpret_cast<const uint4*>(skey + w * 32 + 4 * q);
-            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            for (int t = 0; t < 4; ++t) {
+                const int q = 4 * h + ((t + w) & 3);
+                const uint4 k4 = *reinterpret_cast<const uint4*>(skey + w * 32 + 4 * q);
+                const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t key = kk[c], bit = 1u << (4 * q + c);
-                const int d = (int)(key >> 20);
-                if (key != 0u) {
-                    vm |= bit;
-                    if (d > bin[0]) g0 |= bit;
-                    if (d == bin[0]) e0 |= bit;
-                    if (d > bin[1]) g1 |= bit;
-                    if (d == bin[1]) e1 |= bit;
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t key = kk[c], bit = 1u << (4 * q + c);
+                    const int d = (int)(key >> 20);
+                    if (key != 0u) {
+                        vm |= bit;
+                        if (d > bin[0]) g0 |= bit;
+                        if (d == bin[0]) e0 |= bit;
+                        if (d > bin[1]) g1 |= bit;
+                        if (d == bin[1]) e1 |= bit;
+                    }
+                }
+            }
+            const int64_t nw_ = newest - c0 - (int64_t)w * 32;      // the newest block is not a pool candidate
+            const uint32_t notnew = (nw_ >= 0 && nw_ < 32) ? ~(1u << nw_) : 0xFFFFFFFFu;
+            g0 = act[0] ? g0 & notnew : 0u;
+            e0 = act[0] ? e0 & notnew : 0u;
+            // ENTRY with every block among the best: every visible block of the chunk is one
+            g1 = act[1] ? g1 : (ENTRY ? vm : 0u);
+            e1 = act[1] ? e1 : 0u;
+            // the threshold bins' keys go to this CTA's candidate lists (key, index)
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                uint32_t e = s2 == 0 ? e0 : e1;
+                if (!e) continue;
+                uint32_t o = atomicAdd(&px.nloc[s2], (uint32_t)__popc(e));
+                while (e) {
+                    const int j = __ffs(e) - 1;
+                    e &= e - 1;
+                    if (o < PH_CAP) loc[s2 * PH_CAP + o] = ((uint64_t)skey[w * 32 + j] << 32) | (uint32_t)(c0 + w * 32 + j);
+                    ++o;
                 }
             }
         }
-        const int64_t nw_ = newest - c0 - (int64_t)w * 32;      // the newest block is not a pool candidate
-        const uint32_t notnew = (nw_ >= 0 && nw_ < 32) ? ~(1u << nw_) : 0xFFFFFFFFu;
-        g0 = act[0] ? g0 & notnew : 0u;
-        e0 = act[0] ? e0 & notnew : 0u;
-        // ENTRY with every block among the best: every visible block of the chunk is one
-        g1 = act[1] ? g1 : (ENTRY ? vm : 0u);
-        e1 = act[1] ? e1 : 0u;
-        bmW[w] = g0;
-        bmW[cw + w] = g1;
-        bmE[w] = 0u;
-        bmE[cw + w] = 0u;
-        // the threshold bins' keys go to this CTA's candidate lists (key, index)
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-            uint32_t e = s2 == 0 ? e0 : e1;
-            if (!e) continue;
-            uint32_t o = atomicAdd(&px.nloc[s2], (uint32_t)__popc(e));
-            while (e) {
-                const int j = __ffs(e) - 1;
-                e &= e - 1;
-                if (o < PH_CAP) loc[s2 * PH_CAP + o] = ((uint64_t)skey[w * 32 + j] << 32) | (uint32_t)(c0 + w * 32 + j);
-                ++o;
-            }
+        g0 |= __shfl_xor_sync(FULL_MASK, g0, 1);
+        g1 |= __shfl_xor_sync(FULL_MASK, g1, 1);
+        if (on && h == 0) {
+            bmW[w] = g0;
+            bmW[cw + w] = g1;
+            bmE[w] = 0u;
+            bmE[cw + w] = 0u;
         }
     }
     cl_sync();                             // (1) every CTA's candidate list is complete
@@ -1608,10 +1620,11 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     }
     if (ENTRY) {
         // ---- the row's top-k entries: every entry of the best blocks that scores at
-        // least the smallest best-block maximum is a candidate.  Each CTA pushes every
-        // visible entry of its best blocks into every CTA (the threshold is known only
-        // after the next barrier), then each filters the received ones and ranks its
-        // own candidates against the rest
+        // least the smallest best-block maximum is a candidate.  Each CTA pushes the
+        // visible entries of its best blocks at or above the best blocks' threshold bin
+        // into every CTA (the exact threshold is known only after the next barrier),
+        // then each filters the received ones and ranks its own candidates against the
+        // rest
         uint32_t* W = bmW + cw;
         if (any_radix) {
             // the crowded case: the ties at T taken (lowest index first) become best
@@ -1659,6 +1672,9 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         __syncthreads();
         const uint32_t nown = px.nown;
         const float* srow = a.scores + row * a.n_ent;
+        // the threshold is the maximum of a best block, so at least the best blocks'
+        // threshold bin's lower edge: an entry below that edge is never a candidate
+        const uint32_t edge = (uint32_t)bin[1] << 20;
         for (uint32_t t0 = 0; t0 < nown * (uint32_t)a.block; t0 += bd) {
             const uint32_t t = t0 + tid;
             bool keep = false;
@@ -1668,7 +1684,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                 e = (c0 + blist[t / a.block]) * a.block + t % a.block;
                 if (e < V) {
                     key = order_key(srow[e]);
-                    keep = true;
+                    keep = key >= edge;
                 }
             }
             const unsigned km = __ballot_sync(FULL_MASK, keep);
