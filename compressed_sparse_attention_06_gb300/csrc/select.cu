@@ -1358,6 +1358,65 @@ __device__ __noinline__ void ph_search2(const uint32_t* full, uint32_t knew_bin,
     __syncthreads();
 }
 
+// The winners among this CTA's candidates of a threshold bin.  A: every CTA's
+// candidates of the bin (mm of them, as (key, index) flipped so that larger is earlier
+// in the order key desc, index asc); own: this CTA's nl candidates (unflipped); r: the
+// winners still to take from the bin.  A histogram of A's next 10 key bits finds the
+// sub-bin holding the r-th: own candidates above it win, below it lose, and those in it
+// are ranked against all of A.  Winners set their bit in W (chunk offset from c0); with
+// track_min, px.tmin_local gets the smallest winning key.  blockDim.x == 1024.
+__device__ __noinline__ void ph_rank_bin(const uint64_t* A, uint32_t mm, const uint64_t* own, uint32_t nl, uint32_t r,
+                                         int64_t c0, uint32_t* W, bool track_min, ClShared& sh, PhShared& px) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t* h = sh.hist;                                 // 1,024 sub-bins: key bits 19..10
+    h[tid] = 0u;
+    if (tid == 0) px.sbin[0] = -1;                         // r beyond the bin: nobody wins from it
+    __syncthreads();
+    for (uint32_t j = tid; j < mm; j += CL_THREADS) atomicAdd(&h[(uint32_t)(A[j] >> 42) & 0x3FFu], 1u);
+    __syncthreads();
+    // thread t holds sub-bin 1023 - t: the keys above it are the sum over the threads before it
+    const int b = CL_THREADS - 1 - tid;
+    const uint32_t c = h[b];
+    uint32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(FULL_MASK, inc, o);
+        if (lane >= o) inc += u;
+    }
+    if (lane == 31) px.wsum[0][wid] = inc;
+    __syncthreads();
+    const uint32_t ws = px.wsum[0][lane];
+    uint32_t wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(FULL_MASK, wi, o);
+        if (lane >= o) wi += u;
+    }
+    const uint32_t ex = __shfl_sync(FULL_MASK, wi - ws, wid) + inc - c;
+    if (ex < r && r <= ex + c) px.sbin[0] = b;
+    __syncthreads();
+    const int sb = px.sbin[0];
+    auto win = [&](uint64_t x) {
+        const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - c0);
+        atomicOr(&W[li >> 5], 1u << (li & 31));
+        if (track_min) atomicMin(&px.tmin_local, (uint32_t)(x >> 32));
+    };
+    for (uint32_t ci = tid; ci < nl; ci += CL_THREADS) {
+        const uint64_t x = own[ci] ^ 0xFFFFFFFFull;
+        if ((int)((x >> 42) & 0x3FFu) > sb) win(x);
+    }
+    // the sub-bin of the r-th: a warp per own candidate in it, ranked against all of A
+    for (uint32_t ci = wid; ci < nl; ci += CL_THREADS / 32) {
+        const uint64_t x = own[ci] ^ 0xFFFFFFFFull;
+        if ((int)((x >> 42) & 0x3FFu) != sb) continue;           // the same for the whole warp
+        uint32_t ahead = 0u;
+#pragma unroll 4
+        for (uint32_t j = lane; j < mm; j += 32) ahead += A[j] > x;
+        ahead = __reduce_add_sync(FULL_MASK, ahead);
+        if (lane == 0 && ahead < r) win(x);
+    }
+}
+
 template <bool ENTRY>
 __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int chunk) {
     extern __shared__ __align__(16) uint32_t dyn[];
@@ -1535,21 +1594,10 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
                 A[j] = (((uint64_t)hi << 32) | lo) ^ 0xFFFFFFFFull;   // larger = earlier in the order
             }
             __syncthreads();
-            const uint32_t nl = min(px.nloc[s2], (uint32_t)PH_CAP);
-            for (uint32_t ci = wid; ci < nl; ci += CL_THREADS / 32) {
-                const uint64_t x = loc[s2 * PH_CAP + ci] ^ 0xFFFFFFFFull;
-                uint32_t ahead = 0u;
-#pragma unroll 4
-                for (uint32_t j = lane; j < mm; j += 32) ahead += A[j] > x;
-                ahead = __reduce_add_sync(FULL_MASK, ahead);
-                if (lane == 0 && ahead < r) {
-                    const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - c0);
-                    atomicOr(&W[li >> 5], 1u << (li & 31));
-                    // ENTRY: the smallest best-block maximum is the smallest in-bin winner
-                    // of the whole row, the minimum over the CTAs of this local one
-                    if (ENTRY && s2 == 1) atomicMin(&px.tmin_local, (uint32_t)(x >> 32));
-                }
-            }
+            // ENTRY: the smallest best-block maximum is the smallest in-bin winner of the
+            // whole row, the minimum over the CTAs of each one's local minimum
+            ph_rank_bin(A, mm, loc + s2 * PH_CAP, min(px.nloc[s2], (uint32_t)PH_CAP), r, c0, W,
+                        ENTRY && s2 == 1, sh, px);
         } else {
             // a crowded threshold bin: the remaining two digits cluster-wide, then the
             // ties at T by index
