@@ -1358,23 +1358,26 @@ __device__ __noinline__ void ph_search2(const uint32_t* full, uint32_t knew_bin,
     __syncthreads();
 }
 
-// The winners among this CTA's candidates of a threshold bin.  A: every CTA's
-// candidates of the bin (mm of them, as (key, index) flipped so that larger is earlier
-// in the order key desc, index asc); own: this CTA's nl candidates (unflipped); r: the
-// winners still to take from the bin.  A histogram of A's next 10 key bits finds the
-// sub-bin holding the r-th: own candidates above it win, below it lose, and those in it
-// are ranked against all of A.  Winners set their bit in W (chunk offset from c0); with
-// track_min, px.tmin_local gets the smallest winning key.  blockDim.x == 1024.
-__device__ __noinline__ void ph_rank_bin(const uint64_t* A, uint32_t mm, const uint64_t* own, uint32_t nl, uint32_t r,
-                                         int64_t c0, uint32_t* W, bool track_min, ClShared& sh, PhShared& px) {
+// Bucket of an entry (flipped (key, index) value): min(1023, (key >> shift) - base),
+// 0 below base -- non-decreasing in the key, so any bucket above the one holding the
+// r-th largest entry holds only entries ranked above it.
+__device__ __forceinline__ int ph_bucket(uint64_t x, int shift, uint32_t base) {
+    const uint32_t k = (uint32_t)(x >> 32) >> shift;
+    return k <= base ? 0 : (int)min(k - base, 1023u);
+}
+
+// The bucket (of 1,024) holding the r-th largest of the mm entries of A (flipped
+// values), searched from the top; -1 if r exceeds mm.  blockDim.x == 1024.
+__device__ __noinline__ int ph_bucket_of_rank(const uint64_t* A, uint32_t mm, uint32_t r, int shift, uint32_t base,
+                                              ClShared& sh, PhShared& px) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    uint32_t* h = sh.hist;                                 // 1,024 sub-bins: key bits 19..10
+    uint32_t* h = sh.hist;
     h[tid] = 0u;
-    if (tid == 0) px.sbin[0] = -1;                         // r beyond the bin: nobody wins from it
+    if (tid == 0) px.sbin[0] = -1;
     __syncthreads();
-    for (uint32_t j = tid; j < mm; j += CL_THREADS) atomicAdd(&h[(uint32_t)(A[j] >> 42) & 0x3FFu], 1u);
+    for (uint32_t j = tid; j < mm; j += CL_THREADS) atomicAdd(&h[ph_bucket(A[j], shift, base)], 1u);
     __syncthreads();
-    // thread t holds sub-bin 1023 - t: the keys above it are the sum over the threads before it
+    // thread t holds bucket 1023 - t: the entries above it are the sum over the threads before it
     const int b = CL_THREADS - 1 - tid;
     const uint32_t c = h[b];
     uint32_t inc = c;
@@ -1395,7 +1398,21 @@ __device__ __noinline__ void ph_rank_bin(const uint64_t* A, uint32_t mm, const u
     const uint32_t ex = __shfl_sync(FULL_MASK, wi - ws, wid) + inc - c;
     if (ex < r && r <= ex + c) px.sbin[0] = b;
     __syncthreads();
-    const int sb = px.sbin[0];
+    return px.sbin[0];
+}
+
+// The winners among this CTA's candidates of a threshold bin.  A: every CTA's
+// candidates of the bin (mm of them, flipped so that larger is earlier in the order
+// key desc, index asc); own: this CTA's nl candidates (unflipped); r: the winners
+// still to take from the bin.  Bucketed by the next 10 key bits: own candidates above
+// the bucket of the r-th win, below it lose, and those in it are ranked against all
+// of A.  Winners set their bit in W (chunk offset from c0); with track_min,
+// px.tmin_local gets the smallest winning key.  blockDim.x == 1024.
+__device__ __noinline__ void ph_rank_bin(const uint64_t* A, uint32_t mm, const uint64_t* own, uint32_t nl, uint32_t r,
+                                         int64_t c0, uint32_t* W, bool track_min, ClShared& sh, PhShared& px) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const uint32_t base = ((uint32_t)(A[0] >> 32) >> 20) << 10;   // the bin's keys share their top 12 bits
+    const int sb = mm ? ph_bucket_of_rank(A, mm, r, 10, base, sh, px) : -1;
     auto win = [&](uint64_t x) {
         const uint32_t li = (uint32_t)((int64_t)(uint32_t)(x ^ 0xFFFFFFFFull) - c0);
         atomicOr(&W[li >> 5], 1u << (li & 31));
@@ -1403,12 +1420,12 @@ __device__ __noinline__ void ph_rank_bin(const uint64_t* A, uint32_t mm, const u
     };
     for (uint32_t ci = tid; ci < nl; ci += CL_THREADS) {
         const uint64_t x = own[ci] ^ 0xFFFFFFFFull;
-        if ((int)((x >> 42) & 0x3FFu) > sb) win(x);
+        if (ph_bucket(x, 10, base) > sb) win(x);
     }
-    // the sub-bin of the r-th: a warp per own candidate in it, ranked against all of A
+    // the bucket of the r-th: a warp per own candidate in it, ranked against all of A
     for (uint32_t ci = wid; ci < nl; ci += CL_THREADS / 32) {
         const uint64_t x = own[ci] ^ 0xFFFFFFFFull;
-        if ((int)((x >> 42) & 0x3FFu) != sb) continue;           // the same for the whole warp
+        if (ph_bucket(x, 10, base) != sb) continue;              // the same for the whole warp
         uint32_t ahead = 0u;
 #pragma unroll 4
         for (uint32_t j = lane; j < mm; j += 32) ahead += A[j] > x;
@@ -1818,24 +1835,34 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
         }
         __syncthreads();
         const uint32_t md = min(px.ndense, 2u * (uint32_t)PH_CAP);
-        // a warp per candidate of this CTA's chunk (from the list of them, else picked out
-        // of all received entries): winners rank below k
+        // the winners rank below k among the received entries: bucketed by key bits 29..15
+        // above the threshold bin's edge (every received key is at least that edge), own
+        // entries above the bucket of the k-th win, and those in it are ranked against all
+        // (from the list of own entries, else picked out of all received ones)
+        const uint32_t ebase = (uint32_t)bin[1] << 5;
+        const int sbe = ph_bucket_of_rank(dense, md, (uint32_t)a.k, 15, ebase, sh, px);
         const uint32_t no = px.nown_e;
         const bool listed = no <= (uint32_t)PH_WCAP;
+        auto ewin = [&](int64_t e) {
+            const uint32_t li = (uint32_t)(e - e0);
+            atomicOr(&ebm[li >> 5], 1u << (li & 31));
+            const uint32_t o = atomicAdd(&px.nwin, 1u);
+            if (o < (uint32_t)PH_WCAP) wlist[o] = li;
+        };
+        for (uint32_t ci = tid; ci < (listed ? no : md); ci += CL_THREADS) {
+            const uint64_t x = dense[listed ? olist[ci] : ci];
+            const int64_t e = (int64_t)(uint32_t)(x ^ 0xFFFFFFFFull);
+            if (e >= e0 && e < e1 && ph_bucket(x, 15, ebase) > sbe) ewin(e);
+        }
         for (uint32_t ci = wid; ci < (listed ? no : md); ci += CL_THREADS / 32) {
             const uint64_t x = dense[listed ? olist[ci] : ci];
             const int64_t e = (int64_t)(uint32_t)(x ^ 0xFFFFFFFFull);
-            if (e < e0 || e >= e1) continue;                     // the same for the whole warp
+            if (e < e0 || e >= e1 || ph_bucket(x, 15, ebase) != sbe) continue;   // the same for the whole warp
             uint32_t ahead = 0u;
 #pragma unroll 4
             for (uint32_t j = lane; j < md; j += 32) ahead += dense[j] > x;
             ahead = __reduce_add_sync(FULL_MASK, ahead);
-            if (lane == 0 && ahead < (uint32_t)a.k) {
-                const uint32_t li = (uint32_t)(e - e0);
-                atomicOr(&ebm[li >> 5], 1u << (li & 31));
-                const uint32_t o = atomicAdd(&px.nwin, 1u);
-                if (o < (uint32_t)PH_WCAP) wlist[o] = li;
-            }
+            if (lane == 0 && ahead < (uint32_t)a.k) ewin(e);
         }
         __syncthreads();
         const uint32_t nwin = px.nwin;
