@@ -247,7 +247,6 @@ class FP4Decode(Workload):
         self.swa_row = self.swa[:, self.t % 128]
         self.e2e_in = [self.qI, self.w, self.q, self.C_new, self.Z_new, self.KI_new]
         self.e2e_out = [self.buf.out, self.buf.idx]
-        self.qstream = torch.cuda.Stream(dev)
         torch.cuda.synchronize()
 
     def e2e_inputs(self):
@@ -288,7 +287,6 @@ class FP4Decode(Workload):
     # stages
     def write(self):
         self.write_rows()
-        self.pack_query()
 
     def write_rows(self):
         """The new token's main-KV and indexer-key rows (entry t; the step's query sees
@@ -299,17 +297,16 @@ class FP4Decode(Workload):
                         out_seq_stride=self.N)
         C.csa2_fp4_pack(self.KI_new, C.MXFP4_E8M0x32, out=self.ki[:, t], out_ld=self.N * 68)
 
-    def pack_query(self):
-        C = _C()
-        C.csa2_fp4_pack(self.qI, C.MXFP4_E8M0x32, out=self.qI_mx)     # the QK path runs in FP4
 
     def main(self):
-        # every score is stored only for the fused selection, which reads those of the
-        # best blocks
+        # the FP4 QK path with the bf16 query packed to MXFP4 inside the scan (the packed
+        # bytes kept for the candidate scan of the top-1024 path); every score is stored
+        # only for the fused selection, which reads those of the best blocks
         fused = self.fused_select()
-        _C().csa2_index_score(self.qI_mx, self.w, self.ki, self.nv, block=self.block,
-                              scores=self.buf.scores if fused else None, want_scores=fused,
-                              want_block_max=True, block_max=self.buf.block_max, block_hist=self.buf.block_hist)
+        _C().csa2_index_score_mxq(self.qI, self.w, self.ki, self.nv, block=self.block,
+                                  scores=self.buf.scores if fused else None, want_scores=fused,
+                                  want_block_max=True, block_max=self.buf.block_max,
+                                  block_hist=self.buf.block_hist, q_mx_out=self.qI_mx)
 
     def fused_select(self):
         from compressed_sparse_attention_06_gb300 import pipeline as P
@@ -362,20 +359,8 @@ class FP4Decode(Workload):
         _C().csa2_attn_prepare(self.q, self.q_pos, self.buf.attn_ws, self.k, window=self.window, N=self.N,
                                swa_cap=128)
 
-    # True: the attention's query half beside the query pack on a second stream
-    # (measured: no faster than the attention call preparing it)
-    prep_early = False
-
     def pre(self):
-        if self.prep_early and self.H <= 64:
-            cur = torch.cuda.current_stream()
-            self.qstream.wait_stream(cur)
-            with torch.cuda.stream(self.qstream):
-                self.prepare()
-            self.pack_query()
-            cur.wait_stream(self.qstream)
-        else:
-            self.pack_query()
+        pass
 
     has_side = True
 
@@ -383,18 +368,18 @@ class FP4Decode(Workload):
         self.write_rows()
 
     def post(self):
-        self.select(); self.attn(prepared=self.prep_early)
+        self.select(); self.attn()
 
     def launches_per_step(self):
-        # compress, 2 packs, histogram zeroing, scan, pool + top-k (or pool, candidate
-        # scan, top-k), then per 64-head pass of the attention: query prep, attention
-        # (its key splits merged in the kernel)
-        return (6 if self.fused_select() else 8) + 2 * ((self.H + 63) // 64)
+        # compress, the new indexer-key row's pack, histogram zeroing, scan (packing the
+        # query), pool + top-k (or pool, candidate scan, top-k), then per 64-head pass of
+        # the attention: query prep, attention (its key splits merged in the kernel)
+        return (5 if self.fused_select() else 7) + 2 * ((self.H + 63) // 64)
 
     def main_amount(self):
         """Algorithmic bytes of one full-scan launch: every visible MXFP4 indexer row
-        once, plus the MXFP4 queries and the head weights."""
-        return self.B * self.V * 68 + self.B * self.H_I * (68 + 4)
+        once, plus the bf16 queries and the head weights."""
+        return self.B * self.V * 68 + self.B * self.H_I * (256 + 4)
 
     def stages(self):
         B, H = self.B, self.H

@@ -33,6 +33,7 @@ EXPORTS = (
     "csa2_topk_workspace_bytes", "csa2_block_pool_workspace_bytes",
     "csa2_compress_step", "csa2_compress_state_bytes", "csa2_compress_state_seed", "csa2_dense_attn",
     "csa2_compress_varlen", "csa2_pool_topk", "csa2_block_hist", "csa2_attn_prepare", "csa2_visible_entries",
+    "csa2_index_score_mxq",
 )
 
 
@@ -67,6 +68,7 @@ def _declare(lib):
         "csa2_fp4_pack": (_i, [_vp, _vp, _i, _i64, _i, _i, _vp, _i64, _vp]),
         "csa2_fp4_unpack": (_i, [_vp, _vp, _i, _i64, _i, _vp, _i, _vp]),
         "csa2_visible_entries": (_i, [_vp, _vp, _i64, _i, _vp, _vp]),
+        "csa2_index_score_mxq": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp]),
         "csa2_index_score": (_i, [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i64, _i, _i, _vp, _vp, _i, _i, _vp,
                                   _vp, _vp, _vp]),
         "csa2_topk": (_i, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -311,6 +313,31 @@ def csa2_visible_entries(q_pos: torch.Tensor, m: int, out: Optional[torch.Tensor
                                      _stream(q_pos))
     _check("csa2_visible_entries", st)
     return out
+
+
+def csa2_index_score_mxq(qI, w, kI, n_visible, block: int = 8, scores: Optional[torch.Tensor] = None,
+                         block_max: Optional[torch.Tensor] = None, want_scores: bool = True,
+                         want_block_max: bool = False, block_hist: Optional[torch.Tensor] = None,
+                         q_mx_out: Optional[torch.Tensor] = None):
+    """Full scan on the FP4 QK path from a bf16 indexer query qI [B,Q,64,128], packed to
+    MXFP4 inside the scan (by csa2_fp4_pack's rule; the packed bytes go to q_mx_out
+    [B,Q,64,68] uint8 if given); kI [B,N,68] MXFP4.  Outputs as csa2_index_score's full
+    scan.  Returns (scores, block_max)."""
+    if qI.dtype != torch.bfloat16 or kI.dtype != torch.uint8:
+        raise ValueError("csa2_index_score_mxq takes a bf16 query and MXFP4 keys")
+    B, Q, H_I, d = qI.shape
+    N = kI.shape[1]
+    if want_scores and scores is None:
+        scores = alloc((B, Q, N), dtype=torch.float32, device=qI.device)
+    if want_block_max and block_max is None:
+        block_max = alloc((B, Q, (N + block - 1) // block), dtype=torch.float32, device=qI.device)
+    if q_mx_out is not None and (q_mx_out.dtype != torch.uint8 or q_mx_out.shape != (B, Q, H_I, mxfp4_row_bytes(d))):
+        raise ValueError("q_mx_out must be uint8 [B, Q, H_I, 68]")
+    st = _lib().csa2_index_score_mxq(ctx(qI.device.index), _p(qI), _p(w), _p(kI), B, Q, N, H_I, d, _p(n_visible),
+                                     block, _p(scores) if want_scores else None, _p(block_max), _p(block_hist),
+                                     _p(q_mx_out), _stream(qI))
+    _check("csa2_index_score_mxq", st)
+    return scores, block_max
 
 
 def csa2_index_score(qI, w, kI, n_visible, k_fmt: Optional[int] = None, pool=None, block: int = 8,

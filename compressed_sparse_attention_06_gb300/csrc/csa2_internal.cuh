@@ -161,6 +161,26 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float((b & 0xFF) << 23);
 }
 
+// One MXFP4 block of 32 values (OCP MX): the E8M0 scale code (returned) and the 32
+// E2M1 codes E2M1_RNE(x / X), X = 2^(code - 127), value 2i in the low nibble of byte i;
+// all codes 0 when amax == 0.  X is a power of two, so x / X is taken as x * 2^(127 -
+// code): that factor is exact in fp32 (2^-127 as a subnormal), and the product rounds
+// exactly as the quotient would (the same real number, rounded once).
+__device__ __forceinline__ uint32_t mxfp4_block32(const float (&v)[32], uint32_t (&w)[4]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t code = mx_scale_code(amax);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = 0u;
+    if (amax > 0.0f) {
+        const float rX = code == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - code) << 23);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) w[i / 8] |= e2m1x2(v[i] * rX, v[i + 1] * rX) << (4 * (i % 8));
+    }
+    return code;
+}
+
 // Magnitudes of the 8 E2M1 codes (format definition: 2 exponent bits with bias
 // 1, one mantissa bit).
 __device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {

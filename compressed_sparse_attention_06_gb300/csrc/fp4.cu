@@ -61,17 +61,8 @@ __global__ void mxfp4_pack_kernel(const T* __restrict__ x, int64_t rows, int d, 
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = to_f32<T>(src[i]);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const uint32_t code = mx_scale_code(amax);
-    uint32_t w[4] = {0, 0, 0, 0};
-    if (amax > 0.0f) {
-        float X = e8m0_to_f32(code);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2)
-            w[i / 8] |= e2m1x2(__fdiv_rn(v[i], X), __fdiv_rn(v[i + 1], X)) << (4 * (i % 8));
-    }
+    uint32_t w[4];
+    const uint32_t code = mxfp4_block32(v, w);
     uint8_t* row = out + r * out_ld;
     uint32_t* codes = reinterpret_cast<uint32_t*>(row + gi * 16);
 #pragma unroll

@@ -82,7 +82,8 @@ static_assert(BUFS >= CPY_GROUPS && BUFS >= EPI_GROUPS, "buffer phases");
 constexpr int OFF_B = 0;
 constexpr int OFF_STAGE = OFF_B + B_BYTES;
 constexpr int OFF_W = OFF_STAGE + STAGES * MX_STAGE;
-constexpr int OFF_BAR = OFF_W + HEADS * 4;
+constexpr int OFF_QS = OFF_W + HEADS * 4;                // the query's scale bytes, packed here
+constexpr int OFF_BAR = OFF_QS + HEADS * 4;
 constexpr int N_BARS = 2 * STAGES + 3 * BUFS;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
 constexpr int OFF_HIST = OFF_TMEMPTR + 16;               // [CSA2_BLOCK_HIST_BINS] block-max digit counts
@@ -100,7 +101,9 @@ static_assert(SMEM > 114 * 1024 && SMEM <= 227 * 1024, "shared memory");
 static_assert(OFF_STAGE % 16 == 0 && MX_STAGE % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
 struct FpArgs {
-    const uint8_t* qmx;           // MXFP4 queries [B, Q, 64, 68]
+    const uint8_t* qmx;           // MXFP4 queries [B, Q, 64, 68], or NULL with qbf
+    const __nv_bfloat16* qbf;     // bf16 queries [B, Q, 64, 128], packed to MXFP4 here (or NULL)
+    uint8_t* qmx_out;             // with qbf: the packed queries [B, Q, 64, 68], or NULL
     const float* w;               // [B, Q, 64]
     const uint8_t* kmx;           // MXFP4 keys [B, N, 68]
     const int64_t* nv;            // [B, Q]
@@ -180,32 +183,72 @@ __global__ void __launch_bounds__(THREADS, 1) index_scan_fp4_kernel(const FpArgs
     int t_act_end = t_end;
     if (!CAND) t_act_end = min(t_end, (int)((V + TILE - 1) / TILE));
     const int n_act = max(0, t_act_end - t_begin);
-    // query codes -> the B tile: thread (head h, 16-byte unit u)
-    const uint8_t* qrow0 = a.qmx + (int64_t)g * HEADS * MX_ROW;
-    for (int t = threadIdx.x; t < HEADS * 4; t += THREADS) {
-        const int h = t >> 2, u = t & 3;
-        const uint8_t* src = qrow0 + h * MX_ROW + u * 16;
-        *reinterpret_cast<uint4*>(sB + kmajor64_offset(h, u)) =
-            make_uint4(ld_u32(src), ld_u32(src + 4), ld_u32(src + 8), ld_u32(src + 12));
+    __syncthreads();                         // the barrier initialisations are visible to every warp
+    // the query is prepared by warps 1.. while the producer (warp 0) already streams
+    // keys: the B tile (query codes, thread = (head h, 16-byte unit u = MX block u)), its
+    // scale bytes (sQS, then tensor memory) and the head weights
+    uint8_t* sQS = smem + OFF_QS;
+    uint32_t tmem = 0u;
+    if (warp != 0) {
+        constexpr int NT = THREADS - 32;
+        const int tq = threadIdx.x - 32;
+        if (a.qbf) {
+            // pack the bf16 query here, by the rule of csa2_fp4_pack (one MX block a thread)
+            for (int t = tq; t < HEADS * 4; t += NT) {
+                const int h = t >> 2, u = t & 3;
+                const uint4* src = reinterpret_cast<const uint4*>(a.qbf + ((int64_t)g * HEADS + h) * 128 + u * 32);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 p = src[i];
+                    const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        v[8 * i + 2 * j] = __uint_as_float(pw[j] << 16);
+                        v[8 * i + 2 * j + 1] = __uint_as_float(pw[j] & 0xFFFF0000u);
+                    }
+                }
+                uint32_t w4[4];
+                const uint32_t code = mxfp4_block32(v, w4);
+                *reinterpret_cast<uint4*>(sB + kmajor64_offset(h, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                sQS[h * 4 + u] = (uint8_t)code;
+                if (a.qmx_out && blockIdx.x == 0) {
+                    uint8_t* dst = a.qmx_out + ((int64_t)g * HEADS + h) * MX_ROW;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) reinterpret_cast<uint32_t*>(dst + u * 16)[i] = w4[i];
+                    dst[CODE_BYTES + u] = (uint8_t)code;
+                }
+            }
+        } else {
+            const uint8_t* qrow0 = a.qmx + (int64_t)g * HEADS * MX_ROW;
+            for (int t = tq; t < HEADS * 4; t += NT) {
+                const int h = t >> 2, u = t & 3;
+                const uint8_t* src = qrow0 + h * MX_ROW + u * 16;
+                *reinterpret_cast<uint4*>(sB + kmajor64_offset(h, u)) =
+                    make_uint4(ld_u32(src), ld_u32(src + 4), ld_u32(src + 8), ld_u32(src + 12));
+            }
+            for (int h = tq; h < HEADS; h += NT) reinterpret_cast<uint32_t*>(sQS)[h] = ld_u32(qrow0 + h * MX_ROW + CODE_BYTES);
+        }
+        for (int h = tq; h < HEADS; h += NT) sW[h] = a.w[(int64_t)g * HEADS + h];
+        fence_proxy_async_smem();
+        tc_fence_before();
+        bar_sync_named(1, NT);
+        tc_fence_after();
+        tmem = *sTmem;
+        // query scales -> tensor memory (warps 4..7: warp w reaches lane quarter w % 4).
+        // Scale-factor layout: the 32-bit cell at lane 32j' + l, column c + j holds the
+        // four block scales of row 32j + l (the same in each lane quarter); the query has
+        // 64 rows (heads), so columns c and c+1.
+        if (warp >= 4 && warp < 8) {
+            const uint32_t s0 = reinterpret_cast<const uint32_t*>(sQS)[lane];
+            const uint32_t s1 = reinterpret_cast<const uint32_t*>(sQS)[lane + 32];
+            tmem_st4(tmem + ((uint32_t)((warp & 3) * 32) << 16) + SFB_COL, s0, s1, 0u, 0u);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        bar_sync_named(1, NT);
+        tc_fence_after();
     }
-    for (int h = threadIdx.x; h < HEADS; h += THREADS) sW[h] = a.w[(int64_t)g * HEADS + h];
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *sTmem;
-    // query scales -> tensor memory.  Scale-factor layout: the 32-bit cell at lane
-    // 32j' + l, column c + j holds the four block scales of row 32j + l (the same in
-    // each lane quarter); the query has 64 rows (heads), so columns c and c+1.
-    if (warp < 4) {
-        const uint32_t s0 = ld_u32(qrow0 + lane * MX_ROW + CODE_BYTES);
-        const uint32_t s1 = ld_u32(qrow0 + (lane + 32) * MX_ROW + CODE_BYTES);
-        tmem_st4(tmem + ((uint32_t)(warp * 32) << 16) + SFB_COL, s0, s1, 0u, 0u);
-        tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 
     if (warp == 0) {
         // ============================ producer ============================
@@ -440,11 +483,13 @@ csa2_status launch_fp4(csa2_ctx* ctx, FpArgs& a, cudaStream_t s) {
 csa2_status index_score_fp4_dispatch(csa2_ctx* ctx, const void* q_idx, const float* w, const void* k_idx, int B,
                                      int Q, int64_t N, int H_I, const int64_t* n_visible, const int32_t* pool,
                                      int n_pool, int block, float* scores, float* block_max, uint32_t* hist,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, const void* q_bf16, uint8_t* q_mx_out) {
     if (H_I != HEADS || block != 8 || (N % 8) != 0 || N == 0) return CSA2_ERR_UNSUPPORTED;
     if (pool && (n_pool % BLOCKS_PER_TILE) != 0) return CSA2_ERR_UNSUPPORTED;
     FpArgs a;
     a.qmx = reinterpret_cast<const uint8_t*>(q_idx);
+    a.qbf = reinterpret_cast<const __nv_bfloat16*>(q_bf16);
+    a.qmx_out = q_mx_out;
     a.w = w;
     a.kmx = reinterpret_cast<const uint8_t*>(k_idx);
     a.nv = n_visible;

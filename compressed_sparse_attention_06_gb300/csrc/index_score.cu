@@ -172,6 +172,28 @@ extern "C" csa2_status csa2_visible_entries(csa2_ctx* ctx, const int64_t* q_pos,
                       n_visible);
 }
 
+extern "C" csa2_status csa2_index_score_mxq(csa2_ctx* ctx, const void* q_bf16, const float* w, const void* k_idx,
+                                            int B, int Q, int64_t N, int H_I, int d_I, const int64_t* n_visible,
+                                            int block, float* scores, float* block_max, uint32_t* block_hist,
+                                            uint8_t* q_mx_out, void* stream) {
+    if (!ctx || B < 0 || Q < 0 || N < 0 || H_I < 1) return CSA2_ERR_INVALID_ARG;
+    if (d_I != D_IDX || H_I != 64 || block != 8 || (N % 8) != 0) return CSA2_ERR_UNSUPPORTED;
+    if (block_hist && !block_max) return CSA2_ERR_INVALID_ARG;
+    if ((int64_t)B * Q > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (B == 0 || Q == 0 || N == 0) return CSA2_OK;
+    if (!q_bf16 || !w || !n_visible || !k_idx) return CSA2_ERR_INVALID_ARG;
+    if (!aligned(q_bf16, 16) || !aligned(k_idx, 16) || (block_hist && !aligned(block_hist, 16)))
+        return CSA2_ERR_INVALID_ARG;
+    if (q_mx_out && !aligned(q_mx_out, 4)) return CSA2_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (block_hist) {
+        const csa2_status z = block_hist_zero(block_hist, (int64_t)B * Q, s);
+        if (z != CSA2_OK) return z;
+    }
+    return index_score_fp4_dispatch(ctx, nullptr, w, k_idx, B, Q, N, H_I, n_visible, nullptr, 0, block, scores,
+                                    block_max, block_hist, s, q_bf16, q_mx_out);
+}
+
 extern "C" csa2_status csa2_index_score(csa2_ctx* ctx, const void* q_idx, csa2_dtype q_dt, const float* w,
                                         const void* k_idx, csa2_dtype k_dt, int B, int Q, int64_t N, int H_I,
                                         int d_I, const int64_t* n_visible, const int32_t* pool_blocks,

@@ -66,6 +66,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     return true;
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads (a multiple
+// of 32): the warps that take part wait until all of them have arrived.
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------- copies
 // 1-D bulk copy global -> shared, completing on an mbarrier (size % 16 == 0,
 // both addresses 16-byte aligned).

@@ -94,10 +94,18 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
 
     side_stream: the attention's query half (csa2_attn_prepare) runs there, beside
     the selection, after the scan (which fills the GPU by itself)."""
-    qI = mxfp4_query(qI, kI, buf.qI_mx)
     fused = pool_topk_applies(k, block, n_keep, buf.block_max.shape[-1])
-    C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores if fused else None, want_scores=fused,
-                       want_block_max=True, block_max=buf.block_max, block_hist=buf.block_hist)
+    if mxq_applies(qI, kI, block):
+        # the FP4 QK path with the query packed inside the scan (packed bytes kept in buf)
+        C.csa2_index_score_mxq(qI, w, kI, n_visible, block=block, scores=buf.scores if fused else None,
+                               want_scores=fused, want_block_max=True, block_max=buf.block_max,
+                               block_hist=buf.block_hist, q_mx_out=buf.qI_mx)
+        qI = buf.qI_mx
+    else:
+        qI = mxfp4_query(qI, kI, buf.qI_mx)
+        C.csa2_index_score(qI, w, kI, n_visible, block=block, scores=buf.scores if fused else None,
+                           want_scores=fused, want_block_max=True, block_max=buf.block_max,
+                           block_hist=buf.block_hist)
     B, Q, H = q.shape[:3]
     prepared = side_stream is not None and H <= 64
     if prepared:
@@ -125,6 +133,13 @@ def pool_topk_applies(k: int, block: int, n_keep: int, n_blocks: int) -> bool:
     """The shapes csa2_pool_topk takes (its header states them)."""
     chunk = -(-(-(-n_blocks // 16)) // 1024) * 1024
     return 1 <= k <= n_keep - 1 and k * block <= 4096 and block <= 16 and chunk <= 16384
+
+
+def mxq_applies(qI, kI, block: int) -> bool:
+    """Shapes csa2_index_score_mxq takes: a bf16 query of 64 heads x 128 over MXFP4 keys,
+    blocks of 8, a cache length that is a multiple of 8."""
+    return (qI.dtype == torch.bfloat16 and kI.dtype == torch.uint8 and tuple(qI.shape[2:]) == (64, 128)
+            and block == 8 and kI.shape[1] % 8 == 0)
 
 
 def mxfp4_query(qI, kI, out=None):

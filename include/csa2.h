@@ -259,6 +259,26 @@ csa2_status csa2_index_score(csa2_ctx* ctx,
                              float* scores, float* block_max, uint32_t* block_hist, void* stream);
 
 /*
+ * csa2_index_score_mxq -- the full scan of csa2_index_score on its FP4 QK path
+ * (DSA-to-CSA/HCA page, «Lightning Indexer：公式 (13)–(17)»: the indexer QK product in
+ * FP4) from a bf16 indexer query: each query head row is packed to MXFP4 inside the
+ * scan by the rule of csa2_fp4_pack (so no separate packing launch), then scored as
+ * csa2_index_score scores a packed query, with the same outputs.
+ *   q_bf16   : [B, Q, 64, 128] bf16 (16-byte aligned)
+ *   k_idx    : [B, N, 68] B MXFP4 indexer keys; N a multiple of 8; block == 8
+ *   q_mx_out : [B, Q, 64, 68] B or NULL: the packed query bytes, as csa2_fp4_pack
+ *              writes them (4-byte aligned)
+ * w, n_visible, scores, block_max, block_hist: as csa2_index_score's full scan.
+ * Other head counts, head sizes or blocks return CSA2_ERR_UNSUPPORTED (pack the query
+ * with csa2_fp4_pack and call csa2_index_score).
+ */
+csa2_status csa2_index_score_mxq(csa2_ctx* ctx, const void* q_bf16, const float* w, const void* k_idx,
+                                 int B, int Q, int64_t N, int H_I, int d_I, const int64_t* n_visible,
+                                 int block, float* scores, float* block_max, uint32_t* block_hist,
+                                 uint8_t* q_mx_out, void* stream);
+
+/*
+ * csa2_topk -- top-k selection/*
  * csa2_topk -- top-k selection (DSA-to-CSA/HCA page eq. (17)) in one total order:
  * score descending, entry index ascending (the lower index wins a tie).
  * Row r of `scores` (stride ld floats) covers:

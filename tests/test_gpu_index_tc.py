@@ -195,3 +195,35 @@ def test_bounded_wait_times_out_and_context_recovers(kind):
     C.csa2_ctx_check()
     ref = O.index_score(qn[0, 0], w[0, 0].double().cpu().numpy(), K_np[0], N)
     assert_close(to_np(sc)[0, 0], ref, 1e-5, "after timeout")
+
+
+@pytest.mark.parametrize("B,Q,N", [(1, 1, 8), (2, 3, 4096), (8, 1, 131072)])
+def test_in_scan_query_packing_equals_separate_pack(B, Q, N):
+    """csa2_index_score_mxq (the bf16 query packed to MXFP4 inside the FP4 scan) gives
+    the bytes of csa2_fp4_pack and then the same scores, block maxima and histogram as
+    csa2_index_score on that packed query, bit for bit; the scores match the oracle on
+    the dequantised packed query.  Visible counts ragged, some 0, some past N."""
+    kI, K_np = _keys(B, N, 171 + N, "mx")
+    qI, w = _queries(B, Q, 172 + N)
+    vis = [(N * (3 * i + 1)) // (3 * B * Q) for i in range(B * Q)]
+    vis[0] = 0 if B * Q > 1 else N
+    vis[-1] = N + 5
+    nv = torch.tensor(vis, dtype=torch.int64, device=DEV).view(B, Q)
+    nb = N // 8
+    packed = torch.empty((B, Q, 64, 68), dtype=torch.uint8, device=DEV)
+    sc1, bm1 = C.csa2_index_score_mxq(qI, w, kI, nv, want_block_max=True, q_mx_out=packed,
+                                      block_hist=torch.empty((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=DEV))
+    qmx = C.csa2_fp4_pack(qI, C.MXFP4_E8M0x32)
+    hist2 = torch.empty((B, Q, C.BLOCK_HIST_BINS), dtype=torch.int32, device=DEV)
+    sc2, bm2 = C.csa2_index_score(qmx, w, kI, nv, want_block_max=True, block_hist=hist2)
+    # the histogram of the first call, read back through a second call into its own buffer
+    hist1 = torch.empty_like(hist2)
+    C.csa2_index_score_mxq(qI, w, kI, nv, want_block_max=True, block_hist=hist1)
+    C.csa2_ctx_check()
+    assert torch.equal(packed, qmx)
+    assert torch.equal(sc1, sc2) and torch.equal(bm1, bm2) and torch.equal(hist1, hist2)
+    q_np = O.mxfp4_unpack(qmx.reshape(-1, 68).cpu().numpy()).reshape(B, Q, 64, 128)
+    for b, q in [(0, 0), (B - 1, Q - 1)]:
+        V = min(int(nv[b, q]), N)
+        ref = O.index_score(q_np[b, q], w[b, q].double().cpu().numpy(), K_np[b], V)
+        assert_close(to_np(sc1[b, q]), ref, 1e-5, f"b{b} q{q}")
