@@ -960,7 +960,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
 
 void tc_splits(const csa2_ctx* ctx, int64_t n_bq, int k, int window, int& n_split, int& tps) {
     const int n_tiles = std::max(1, (k + window + TC_TILE - 1) / TC_TILE);
-    int want = (int)std::min<int64_t>(n_tiles, std::max<int64_t>(1, (ctx->num_sms + n_bq - 1) / n_bq));
+    // as many key splits as keep every (query, split) item in one wave of CTAs: a second
+    // wave would put two items' tiles in a row on some SMs, and one wave lets a query's
+    // splits run as one cluster that merges in the kernel
+    int want = (int)std::min<int64_t>(n_tiles, std::max<int64_t>(1, ctx->num_sms / n_bq));
     tps = (n_tiles + want - 1) / want;
     n_split = (n_tiles + tps - 1) / tps;
 }
