@@ -283,6 +283,12 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
     pdl_trigger();
     const int64_t bq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the head row is loaded first, so its load and the position's overlap
+    const int h = blockIdx.x * 8 + warp;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    if (h < H) load16<TQ>(q + ((bq * Hs + h) * (int64_t)TC_C + 16 * lane), v);
     if (threadIdx.x < 32) {
         rope_cos_sin(rope, q_pos[bq], threadIdx.x, cs[threadIdx.x], sn[threadIdx.x]);
         if (blockIdx.x == 0) {
@@ -293,11 +299,6 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
     __syncthreads();
     uint8_t* img = qimg + bq * (int64_t)QIMG_BYTES;
     {
-        const int h = blockIdx.x * 8 + warp;
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-        if (h < H) load16<TQ>(q + ((bq * Hs + h) * (int64_t)TC_C + 16 * lane), v);
         if (flags & CSA2_QNORM) {
             float ss = 0.0f;
 #pragma unroll

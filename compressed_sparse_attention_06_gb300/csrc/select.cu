@@ -1209,9 +1209,13 @@ struct PhShared {
 constexpr int PH_ECAP = 8192;              // ENTRY: entry candidates a CTA can receive (64 KB)
 constexpr int PH_WCAP = 1024;              // ENTRY: winners emitted from a list (more: from the bitmap)
 // ENTRY reuses the two candidate-list arrays once the block selections are done:
-// `all` holds the received entries at or above the threshold (2 * PH_CAP of them, the
-// limit k * block <= 2 * PH_CAP keeps them within), `loc` the bitmap of a chunk's entries
+// `all` (sized for max(2 * PH_CAP, k * block) entries) holds the received entries at or
+// above the threshold (at most k * block of them: the entries of the k best blocks),
+// `loc` the bitmap of a chunk's entries; the receive buffer holds PH_ECAP entries, so
+// k * block <= PH_ECAP.
 static_assert(2 * PH_CAP <= PH_ECAP, "every entry of the best blocks fits the receive buffer");
+// capacity of `all` for k best blocks of `block` entries
+__host__ __device__ inline int ph_dense_cap(int k, int block) { return k * block > 2 * PH_CAP ? k * block : 2 * PH_CAP; }
 
 // Ordered emission of one selection from the CTA's bitmaps: winners (bmW) in index
 // order, ties (bmE) while fewer than `quota` have been taken, at out[off + rank].
@@ -1505,7 +1509,8 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
     uint32_t* bmW = dyn + skey_words;                      // [2][cw]
     uint32_t* bmE = bmW + 2 * cw;                          // [2][cw]
     uint64_t* loc = reinterpret_cast<uint64_t*>(bmE + 2 * cw);   // [2][PH_CAP] this CTA's candidates
-    uint64_t* all = loc + 2 * PH_CAP;                      // [2][PH_CAP] every CTA's, gathered
+    uint64_t* all = loc + 2 * PH_CAP;                      // [2][PH_CAP] every CTA's, gathered (ENTRY: more)
+    const uint32_t dcap = ENTRY ? (uint32_t)ph_dense_cap(a.k, a.block) : 2u * PH_CAP;
     const unsigned lt = (1u << lane) - 1u;
     // the chunk's keys into shared memory (key i from thread i % 1024: coalesced loads)
 #pragma unroll
@@ -1824,7 +1829,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             uint32_t o = 0u;
             if (lane == 0) o = atomicAdd(&px.ndense, (uint32_t)__popc(km));
             o = __shfl_sync(FULL_MASK, o, 0) + __popc(km & lt);
-            if (keep && o < 2u * PH_CAP) {
+            if (keep && o < dcap) {
                 dense[o] = ec[j] ^ 0xFFFFFFFFull;     // larger = earlier in the order
                 const int64_t e = (int64_t)(uint32_t)ec[j];
                 if (e >= e0 && e < e1) {
@@ -1834,7 +1839,7 @@ __global__ void __launch_bounds__(CL_THREADS) pool_hist_kernel(PoolArgs a, int c
             }
         }
         __syncthreads();
-        const uint32_t md = min(px.ndense, 2u * (uint32_t)PH_CAP);
+        const uint32_t md = min(px.ndense, dcap);
         // the winners rank below k among the received entries: bucketed by key bits 29..15
         // above the threshold bin's edge (every received key is at least that edge), own
         // entries above the bucket of the k-th win, and those in it are ranked against all
@@ -1939,9 +1944,9 @@ int pool_cluster_size(const csa2_ctx* ctx, int64_t rows, int64_t ld) {
     return 16;
 }
 
-size_t pool_hist_smem(int chunk, bool entry) {
+size_t pool_hist_smem(int chunk, bool entry, int dense_cap = 2 * PH_CAP) {
     const int skey_words = entry ? std::max(chunk, 2 * PH_ECAP) : chunk;
-    return (size_t)skey_words * 4 + (size_t)chunk / 32 * 16 + 4ull * PH_CAP * 8;
+    return (size_t)skey_words * 4 + (size_t)chunk / 32 * 16 + (2ull * PH_CAP + (entry ? dense_cap : 2 * PH_CAP)) * 8;
 }
 
 // Whether 16-CTA clusters of the pool kernel can be resident (asked once).
@@ -1952,7 +1957,7 @@ bool pool_cluster16_ok() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16, 1, 1);
         cfg.blockDim = dim3(CL_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = pool_hist_smem(CL_MAX_CHUNK, ENTRY);
+        cfg.dynamicSmemBytes = pool_hist_smem(CL_MAX_CHUNK, ENTRY, PH_ECAP);
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = 16;
@@ -1974,7 +1979,7 @@ csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cud
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pool_hist_smem(CL_MAX_CHUNK, ENTRY)) != cudaSuccess ||
+                                 (int)pool_hist_smem(CL_MAX_CHUNK, ENTRY, PH_ECAP)) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return CSA2_ERR_CUDA;
         attr = true;
@@ -1984,7 +1989,7 @@ csa2_status launch_pool_hist(csa2_ctx* ctx, const PoolArgs& a, int64_t rows, cud
     if (chunk > CL_MAX_CHUNK) return CSA2_ERR_UNSUPPORTED;
     // ENTRY: the bitmap of a chunk's entries lives in the candidate lists' space
     if (ENTRY && ((size_t)chunk * a.block + 31) / 32 * 4 > 2ull * PH_CAP * 8) return CSA2_ERR_UNSUPPORTED;
-    const size_t smem = pool_hist_smem(chunk, ENTRY);
+    const size_t smem = pool_hist_smem(chunk, ENTRY, ENTRY ? ph_dense_cap(a.k, a.block) : 2 * PH_CAP);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
     cfg.blockDim = dim3(CL_THREADS, 1, 1);
@@ -2206,7 +2211,7 @@ extern "C" csa2_status csa2_pool_topk(csa2_ctx* ctx, const float* block_max, con
         return CSA2_ERR_INVALID_ARG;
     // every entry of the k best blocks is pushed to every CTA of the row's cluster and
     // may be a candidate: they must fit the receive buffer and the candidate list
-    if ((int64_t)k * block > 2 * PH_CAP || k > n_keep - 1) return CSA2_ERR_UNSUPPORTED;
+    if ((int64_t)k * block > PH_ECAP || k > n_keep - 1) return CSA2_ERR_UNSUPPORTED;
     if (((ld + PH_MAX_C - 1) / PH_MAX_C + CL_THREADS - 1) / CL_THREADS * CL_THREADS > CL_MAX_CHUNK)
         return CSA2_ERR_UNSUPPORTED;
     PoolArgs p;

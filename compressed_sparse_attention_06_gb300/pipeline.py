@@ -132,7 +132,7 @@ def full_decode_step(qI, w, kI, q, kv, swa, q_pos, n_visible, sink, buf: DecodeB
 def pool_topk_applies(k: int, block: int, n_keep: int, n_blocks: int) -> bool:
     """The shapes csa2_pool_topk takes (its header states them)."""
     chunk = -(-(-(-n_blocks // 16)) // 1024) * 1024
-    return 1 <= k <= n_keep - 1 and k * block <= 4096 and block <= 16 and chunk <= 16384
+    return 1 <= k <= n_keep - 1 and k * block <= 8192 and block <= 16 and chunk <= 16384
 
 
 def mxq_applies(qI, kI, block: int) -> bool:

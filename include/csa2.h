@@ -348,7 +348,7 @@ csa2_status csa2_block_hist(csa2_ctx* ctx, const float* block_max, int64_t rows,
  *   scores     : [rows, n_ent] f32, the full-scan scores (entries < n_visible read)
  *   out_blocks : [rows, n_keep] int32 (the pool);  out_idx : [rows, k] int32 entry
  *                ids ascending, -1 padded;  out_score : [rows, k] f32 or NULL
- * 2 <= n_keep <= 4096, 1 <= k <= n_keep - 1, k * block <= 4096, block <= 16,
+ * 2 <= n_keep <= 4096, 1 <= k <= n_keep - 1, k * block <= 8192, block <= 16,
  * ld <= 262,144.  Other shapes return CSA2_ERR_UNSUPPORTED (csa2_block_pool and
  * csa2_topk serve them).
  */

@@ -520,7 +520,7 @@ def test_rope_angles_at_large_positions(pos):
 
 @pytest.mark.parametrize("V", [1, 9, 4000, 4097, 8 * 2048, 8 * 2048 + 1, 262143])
 @pytest.mark.parametrize("ties", [False, True])
-@pytest.mark.parametrize("k", [100, 512])
+@pytest.mark.parametrize("k", [100, 512, 1024])
 def test_pool_topk_bit_exact(V, ties, k):
     """csa2_pool_topk: the pool and the top-k entries from block maxima, their
     histogram and the full scores -- both bit-exact with the oracle's block_pool and
@@ -574,15 +574,16 @@ def test_pool_topk_blocks_of_one_many_winners(order):
 
 
 def test_pool_topk_rejects_too_many_candidates():
-    """k * block above the candidate capacity is refused on the host (the decode step
-    then takes the pool, the best blocks' rescoring and csa2_topk one by one)."""
-    N = 8192
+    """k * block above the receive capacity (8,192 entries) is refused on the host (the
+    decode step then takes the pool, the best blocks' rescoring and csa2_topk one by
+    one)."""
+    N = 16384
     s = _score_rows(1, N, 91, False)
     nv = torch.tensor([N], dtype=torch.int64, device=DEV)
     bm = torch.zeros((1, N // 8), dtype=torch.float32, device=DEV)
     hist = C.csa2_block_hist(bm, nv, 8)
     with pytest.raises(C.Csa2Error):
-        C.csa2_pool_topk(bm, hist, s, nv, 1024)
+        C.csa2_pool_topk(bm, hist, s, nv, 1100)
 
 
 def test_visible_entries_causal_rule():
