@@ -343,7 +343,8 @@ extern "C" size_t csa2_sparse_attn_workspace_bytes(csa2_ctx* ctx, int B, int Q, 
                                                    int64_t swa_cap) {
     if (!ctx || B <= 0 || Q <= 0 || H <= 0 || k < 0 || window < 0 || N < 0 || swa_cap < 0) return 0;
     return std::max(attn_simt_ws_bytes(ctx, B, Q, H, k, window),
-                    attn_tc_ws_bytes(ctx, B, Q, H, k, window, N, swa_cap));
+                    H > 64 ? attn_tc_ws_bytes_all_passes(ctx, B, Q, H, k, window, N, swa_cap)
+                           : attn_tc_ws_bytes(ctx, B, Q, H, k, window, N, swa_cap));
 }
 
 // Sparse (idx) or dense (dense_nv: entries 0 .. dense_nv[bq]-1, at most k) attention.
@@ -398,8 +399,42 @@ static csa2_status attn_impl(csa2_ctx* ctx, const void* q, csa2_dtype q_dt, cons
     tc.out = out;
     tc.out_dt = out_dt;
     tc.lse = lse;
+    const size_t qsz = q_dt == CSA2_F32 ? 4 : 2, osz = out_dt == CSA2_F32 ? 4 : 2;
+    // more than 64 heads: every pass in one launch when the workspace holds them all
+    // (the passes' items then share one wave of CTAs); the per-pass partials merge in
+    // the kernel (cluster) or in one combine launch per pass
+    const int n_pass = (H + 63) / 64;
+    if (attn_tc_applies(tc) && ws && n_pass > 1 &&
+        ws_bytes >= attn_tc_ws_bytes_all_passes(ctx, B, Q, H, k, window, 0, 0)) {
+        AttnTcCall p = tc;
+        p.n_pass = n_pass;
+        int ns = 1;
+        const csa2_status st = attn_tc_run(ctx, p, ws, ws_bytes, s, &ns);
+        if (st != CSA2_OK || ns <= 1) return st;
+        const int64_t n_bq = (int64_t)B * Q;
+        for (int h0 = 0; h0 < H; h0 += 64) {
+            AttnArgs c;
+            memset(&c, 0, sizeof(c));
+            c.q_pos = q_pos;
+            c.sink = sink ? sink + h0 : nullptr;
+            c.Q = Q;
+            c.H = std::min(64, H - h0);
+            c.Hs = H;
+            c.rope = tc.rope;
+            c.flags = flags;
+            c.out = reinterpret_cast<uint8_t*>(out) + (size_t)h0 * ATT_C * osz;
+            c.lse = lse ? lse + h0 : nullptr;
+            c.ws = reinterpret_cast<float*>(ws) + (size_t)h0 * n_bq * ns * PART;
+            c.rope_cs = attn_tc_rope_table(ctx, p, ws);
+            c.n_split = ns;
+            c.st = ctx->status;
+            const csa2_status sc =
+                out_dt == CSA2_F32 ? launch_combine<float>(c, B, Q, s) : launch_combine<__nv_bfloat16>(c, B, Q, s);
+            if (sc != CSA2_OK) return sc;
+        }
+        return CSA2_OK;
+    }
     if (attn_tc_applies(tc) && ws && ws_bytes >= attn_tc_ws_bytes(ctx, B, Q, tc.H, k, window, 0, 0)) {
-        const size_t qsz = q_dt == CSA2_F32 ? 4 : 2, osz = out_dt == CSA2_F32 ? 4 : 2;
         for (int h0 = 0; h0 < H; h0 += 64) {
             AttnTcCall p = tc;
             p.H = std::min(64, H - h0);
@@ -509,6 +544,7 @@ extern "C" csa2_status csa2_attn_prepare(csa2_ctx* ctx, const void* q, csa2_dtyp
     if (window == 0) swa_cap = 1;
     AttnTcCall tc;
     memset(&tc, 0, sizeof(tc));
+    tc.n_pass = 1;
     tc.q = q;
     tc.q_dt = q_dt;
     tc.N = N;

@@ -99,6 +99,9 @@ struct TcArgs {
     float* part;                  // [B*Q, H, n_split, PART] when n_split > 1
     const float* rope_cs;         // [B*Q, 64]: cos, sin of the 32 RoPE angles at the query position
     int n_split, tps;             // splits per query, tiles per split
+    int n_pass;                   // head passes of H (<= 64) heads in this launch (out, lse, sink
+                                  // and q are then not offset: pass p takes heads 64p ..)
+    int64_t n_bq;                 // queries (B * Q)
     int64_t items;
     unsigned int* st;
     long long budget;
@@ -109,13 +112,21 @@ struct TcArgs {
 
 struct ItemInfo {
     int64_t bq, b, t;
+    int64_t v;                            // pass * n_bq + bq: the query image, the partials' block
+    int64_t prow;                         // first row of this item's heads in the partials
+    int pass, h0, H;                      // head pass, its first head, its heads
     int split, nw, kq, n_slots, t0, nt;   // kq: cache slots of this query, then nw window slots
 };
 
 __device__ __forceinline__ ItemInfo item_info(const TcArgs& a, int64_t item) {
     ItemInfo r;
-    r.bq = item / a.n_split;
+    r.v = item / a.n_split;
     r.split = (int)(item % a.n_split);
+    r.pass = (int)(r.v / a.n_bq);
+    r.bq = r.v % a.n_bq;
+    r.h0 = r.pass * TC_H;
+    r.H = min(a.H, a.Hs - r.h0);
+    r.prow = (int64_t)r.pass * TC_H * a.n_bq + r.bq * r.H;
     r.b = r.bq / a.Q;
     r.t = a.q_pos[r.bq];
     r.nw = (int)max((int64_t)0, min((int64_t)a.window, r.t + 1));
@@ -297,7 +308,8 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
         }
     }
     __syncthreads();
-    uint8_t* img = qimg + bq * (int64_t)QIMG_BYTES;
+    // the image of (pass h / 64, query bq): passes side by side, gridDim.y queries each
+    uint8_t* img = qimg + ((int64_t)(h >> 6) * gridDim.y + bq) * (int64_t)QIMG_BYTES;
     {
         if (flags & CSA2_QNORM) {
             float ss = 0.0f;
@@ -321,8 +333,9 @@ __global__ void __launch_bounds__(256) attn_qprep_kernel(const TQ* q, const int6
 #pragma unroll
         for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
         const int u0 = 2 * lane, chunk = u0 >> 3, uc = u0 & 7;
-        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(h, uc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(h, uc + 1)) =
+        const uint32_t hr = (uint32_t)(h & (TC_H - 1));     // row within the pass's image
+        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(hr, uc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(img + chunk * CHUNK_Q + sw128_offset(hr, uc + 1)) =
             make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
 }
@@ -345,22 +358,22 @@ __global__ void __launch_bounds__(256) attn_rownorm_kernel(const uint8_t* rows, 
 // Output of a query whose split holds no key slot: the sink alone (O = 0).
 template <typename TO>
 __device__ void write_empty(const TcArgs& a, const ItemInfo& it, int d0) {
-    for (int h = 0; h < a.H; ++h) {
+    for (int h = 0; h < it.H; ++h) {
         for (int d = d0; d < TC_C; d += 128) {
             if (a.n_split > 1)
-                a.part[((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + d] = 0.0f;
+                a.part[((it.prow + h) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + d] = 0.0f;
             else
-                reinterpret_cast<TO*>(a.out)[(it.bq * a.Hs + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
+                reinterpret_cast<TO*>(a.out)[(it.bq * a.Hs + it.h0 + h) * (int64_t)TC_C + d] = from_f32<TO>(0.0f);
         }
     }
-    if (d0 < a.H) {
+    if (d0 < it.H) {
         const int h = d0;
         if (a.n_split > 1) {
-            float* p = a.part + ((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART;
+            float* p = a.part + ((it.prow + h) * a.n_split + it.split) * (int64_t)PART;
             p[0] = -INFINITY;
             p[1] = 0.0f;
         } else if (a.lse) {
-            a.lse[it.bq * a.Hs + h] = a.sink ? a.sink[h] : -INFINITY;
+            a.lse[it.bq * a.Hs + it.h0 + h] = a.sink ? a.sink[it.h0 + h] : -INFINITY;
         }
     }
 }
@@ -381,8 +394,8 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
         rc = a.rope_cs[it.bq * 64 + j];
         rs = a.rope_cs[it.bq * 64 + 32 + j];
     }
-    TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + hbeg) * (int64_t)TC_C + rr;
-    float* pbase = a.part + ((it.bq * a.H + hbeg) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + rr;
+    TO* obase = reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + it.h0 + hbeg) * (int64_t)TC_C + rr;
+    float* pbase = a.part + ((it.prow + hbeg) * a.n_split + it.split) * (int64_t)PART + ATTN_PART_O + rr;
     const int64_t pstride = (int64_t)a.n_split * PART;
     // not unrolled: a CTA often runs this once (one item), from a cold instruction cache
 #pragma unroll 1
@@ -394,7 +407,7 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
             float* pb = pbase + db * 128;
 #pragma unroll
             for (int h = 0; h < 32; ++h)
-                if (hbeg + h < a.H) pb[h * pstride] = __uint_as_float(o[h]);
+                if (hbeg + h < it.H) pb[h * pstride] = __uint_as_float(o[h]);
         } else {
             TO* ob = obase + db * 128;
             const bool rot_here = db == 3 && rot;
@@ -413,7 +426,7 @@ __device__ __forceinline__ void epilogue_heads(const TcArgs& a, const ItemInfo& 
                     const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
                     v = (lane & 1) ? v * rc - pv * rs : v * rc + pv * rs;
                 }
-                if (hbeg + h < a.H) ob[h * TC_C] = from_f32<TO>(v);
+                if (hbeg + h < it.H) ob[h * TC_C] = from_f32<TO>(v);
             }
         }
     }
@@ -530,7 +543,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
                 if (it.nt == 0) continue;
                 if (qi > 0 && !mbar_wait(qempty, (qi - 1) & 1, a.budget, a.st)) break;
                 mbar_arrive_expect_tx(qfull, QIMG_BYTES);
-                bulk_g2s(sQ, a.qimg + it.bq * (int64_t)QIMG_BYTES, QIMG_BYTES, qfull);
+                bulk_g2s(sQ, a.qimg + it.v * (int64_t)QIMG_BYTES, QIMG_BYTES, qfull);
                 issued_q = qi++;
             }
             // the last copy must land before the CTA exits
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
             for (int j = 0; j < 2; ++j) {
                 const int h = lane + 32 * j;
                 const float L = sLw[h] + sLw[TC_H + h] + sLw[2 * TC_H + h] + sLw[3 * TC_H + h];
-                const float zs = (a.sink && h < a.H) ? a.sink[h] : -INFINITY;
+                const float zs = (a.sink && h < it.H) ? a.sink[it.h0 + h] : -INFINITY;
                 float sc = 0.0f, ls = -INFINITY;
                 if (L > 0.0f) {
                     const float M = fmaxf(TC_SHIFT, zs);
@@ -755,13 +768,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = lane + 32 * j;
-                    if (h >= a.H) continue;
+                    if (h >= it.H) continue;
                     if (split) {
-                        float* p = a.part + ((it.bq * a.H + h) * a.n_split + it.split) * (int64_t)PART;
+                        float* p = a.part + ((it.prow + h) * a.n_split + it.split) * (int64_t)PART;
                         p[0] = L2[j] > 0.0f ? TC_SHIFT : -INFINITY;
                         p[1] = L2[j];
                     } else if (a.lse) {
-                        a.lse[it.bq * a.Hs + h] = lse2[j];
+                        a.lse[it.bq * a.Hs + it.h0 + h] = lse2[j];
                     }
                 }
             }
@@ -949,13 +962,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) attn_tc_kernel(const TcArgs a) 
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
         const ItemInfo it = item_info(a, blockIdx.x);
         const int ns = a.n_split;
-        const int hs = (a.H + ns - 1) / ns;
-        const int h0 = it.split * hs, h1 = min(a.H, h0 + hs);
+        const int hs = (it.H + ns - 1) / ns;
+        const int h0 = it.split * hs, h1 = min(it.H, h0 + hs);
         const float* cs = (a.flags & CSA2_ROPE) ? a.rope_cs + it.bq * 64 : nullptr;
         for (int h = h0 + warp; h < h1; h += TC_THREADS / 32)
-            tc_merge_row<TO>(a.part + (it.bq * a.H + h) * (int64_t)ns * PART, ns, a.sink ? a.sink[h] : -INFINITY, cs,
-                             reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + h) * (int64_t)TC_C,
-                             a.lse ? a.lse + it.bq * a.Hs + h : nullptr);
+            tc_merge_row<TO>(a.part + (it.prow + h) * (int64_t)ns * PART, ns, a.sink ? a.sink[it.h0 + h] : -INFINITY,
+                             cs, reinterpret_cast<TO*>(a.out) + (it.bq * a.Hs + it.h0 + h) * (int64_t)TC_C,
+                             a.lse ? a.lse + it.bq * a.Hs + it.h0 + h : nullptr);
     }
 }
 
@@ -983,16 +996,19 @@ struct WsLayout {
     bool table;
 };
 
-WsLayout ws_layout(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap) {
+WsLayout ws_layout(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap,
+                   int n_pass = 1) {
     WsLayout L;
     const int64_t n_bq = (int64_t)B * Q;
-    tc_splits(ctx, n_bq, k, window, L.n_split, L.tps);
+    // every pass of every query is an item group of its own
+    tc_splits(ctx, n_bq * n_pass, k, window, L.n_split, L.tps);
+    if (n_pass > 1) H = TC_H * n_pass;                   // partial rows of all passes
     const int64_t kv_rows = (k > 0) ? (int64_t)B * std::max<int64_t>(N, 0) : 0;
     const int64_t sw_rows = (window > 0) ? (int64_t)B * std::max<int64_t>(swa_cap, 0) : 0;
     L.table = want_row_table(n_bq, k, window, kv_rows + sw_rows);
     L.part = 0;
     L.qimg = L.n_split > 1 ? align_up((size_t)n_bq * H * L.n_split * PART * sizeof(float), 1024) : 0;
-    L.rope = L.qimg + (size_t)n_bq * QIMG_BYTES;
+    L.rope = L.qimg + (size_t)n_bq * n_pass * QIMG_BYTES;
     L.rinv_kv = align_up(L.rope + (size_t)n_bq * 64 * sizeof(float), 256);
     L.rinv_swa = align_up(L.rinv_kv + (L.table ? (size_t)kv_rows * sizeof(float) : 0), 256);
     L.total = L.rinv_swa + (L.table ? (size_t)sw_rows * sizeof(float) : 0);
@@ -1074,8 +1090,15 @@ size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int win
     return ws_layout(ctx, B, Q, std::min(H, TC_H), k, window, N, swa_cap).total;
 }
 
+size_t attn_tc_ws_bytes_all_passes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N,
+                                   int64_t swa_cap) {
+    if (!ctx || H < 1 || B <= 0 || Q <= 0) return 0;
+    const int n_pass = (H + TC_H - 1) / TC_H;
+    return ws_layout(ctx, B, Q, std::min(H, TC_H), k, window, N, swa_cap, n_pass).total;
+}
+
 const float* attn_tc_rope_table(const csa2_ctx* ctx, const AttnTcCall& c, void* ws) {
-    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap, c.n_pass);
     return reinterpret_cast<const float*>(reinterpret_cast<uint8_t*>(ws) + L.rope);
 }
 
@@ -1085,18 +1108,19 @@ csa2_status attn_tc_prepare_into(const AttnTcCall& c, uint8_t* qimg, float* rope
     const int64_t n_bq = (int64_t)c.B * c.Q;
     const csa2_status rq =
         c.q_dt == CSA2_BF16
-            ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg,
-                         rope_cs)
-            : launch_pdl(attn_qprep_kernel<float>, dim3(8, (unsigned)n_bq), dim3(256), 0, s,
-                         reinterpret_cast<const float*>(c.q), c.q_pos, c.H, c.Hs, c.rope, c.flags, qimg, rope_cs);
+            ? launch_pdl(attn_qprep_kernel<__nv_bfloat16>, dim3(8 * c.n_pass, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const __nv_bfloat16*>(c.q), c.q_pos, c.n_pass > 1 ? c.Hs : c.H, c.Hs, c.rope,
+                         c.flags, qimg, rope_cs)
+            : launch_pdl(attn_qprep_kernel<float>, dim3(8 * c.n_pass, (unsigned)n_bq), dim3(256), 0, s,
+                         reinterpret_cast<const float*>(c.q), c.q_pos, c.n_pass > 1 ? c.Hs : c.H, c.Hs, c.rope,
+                         c.flags, qimg, rope_cs);
     return rq != CSA2_OK ? rq : csa2_launch_status();
 }
 
 }  // namespace
 
 csa2_status attn_tc_prepare(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s) {
-    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap, c.n_pass);
     if (!ws || !aligned(ws, 16) || ws_bytes < L.rinv_kv) return CSA2_ERR_INVALID_ARG;
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     return attn_tc_prepare_into(c, base + L.qimg, reinterpret_cast<float*>(base + L.rope), s);
@@ -1105,7 +1129,7 @@ csa2_status attn_tc_prepare(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t
 csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_bytes, cudaStream_t s,
                         int* n_split) {
     const int64_t n_bq = (int64_t)c.B * c.Q;
-    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap);
+    const WsLayout L = ws_layout(ctx, c.B, c.Q, c.H, c.k, c.window, c.N, c.swa_cap, c.n_pass);
     if (!ws || !aligned(ws, 16) || ws_bytes < L.rinv_kv) return CSA2_ERR_INVALID_ARG;
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     uint8_t* qimg = base + L.qimg;
@@ -1158,7 +1182,9 @@ csa2_status attn_tc_run(csa2_ctx* ctx, const AttnTcCall& c, void* ws, size_t ws_
     a.part = reinterpret_cast<float*>(base + L.part);
     a.n_split = L.n_split;
     a.tps = L.tps;
-    a.items = n_bq * L.n_split;
+    a.n_pass = c.n_pass;
+    a.n_bq = n_bq;
+    a.items = n_bq * c.n_pass * L.n_split;
     a.st = ctx->status;
     a.budget = WAIT_BUDGET;
     a.stall = 0;

@@ -87,6 +87,8 @@ struct AttnTcCall {
     const int64_t* q_pos;
     const float* sink;
     int B, Q, H;           // H: heads of this pass (<= 64)
+    int n_pass = 1;        // > 1: every 64-head pass in one launch (H = 64, q, out, lse and
+                           // sink not offset; pass p takes heads 64p .. of Hs)
     int Hs;                // heads per query in q / out / lse (q, out, lse, sink point at this
                            // pass's first head)
     RopeTable rope;
@@ -101,10 +103,15 @@ bool attn_tc_applies(const AttnTcCall& c);
 
 // Workspace bytes the tensor-core path uses for these sizes: per-split partials
 // (when the keys are split), the query images, and, when the call gathers each
-// row many times over, the rows' RMS factors (B*N + B*swa_cap floats).  More than 64
-// heads run in passes of 64 that reuse the workspace, so H is capped at 64 here.
+// row many times over, the rows' RMS factors (B*N + B*swa_cap floats), for one pass of
+// at most 64 heads (H is capped at 64 here; passes run one after another in it).
 // The path runs with any workspace that holds the partials and the images.
 size_t attn_tc_ws_bytes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N, int64_t swa_cap);
+
+// Workspace bytes of one launch over every head pass of H heads (H > 64): the passes'
+// query images and partials side by side.
+size_t attn_tc_ws_bytes_all_passes(const csa2_ctx* ctx, int B, int Q, int H, int k, int window, int64_t N,
+                                   int64_t swa_cap);
 
 // Workspace bytes of the CUDA-core path (attn.cu) for these sizes: its key-split
 // partials, 0 when it runs unsplit.

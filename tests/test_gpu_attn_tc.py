@@ -110,8 +110,9 @@ def test_tensor_core_out_of_range_index_is_flagged():
 @pytest.mark.parametrize("kv_kind", ["bf16", "fp4"])
 def test_more_than_64_heads_in_passes(H, k, kv_kind):
     """More than 64 heads (V4-Pro: 128): the tensor-core path runs 64-head passes over
-    the same rows (the second one ragged for H = 100); against the oracle and against
-    the CUDA-core path of the same call."""
+    the same rows (the second one ragged for H = 100), all in one launch, or one after
+    another when the workspace holds one pass only; against the oracle, against each
+    other and against the CUDA-core path of the same call."""
     B, Q, N, window = 2, 2, 6000, 128
     pos = [[N, N + 300], [700, 5000]]
     q = W.normal_tensor((B, Q, H, 512), 341, 1, torch.bfloat16, DEV)
@@ -136,10 +137,20 @@ def test_more_than_64_heads_in_passes(H, k, kv_kind):
     tiny = torch.empty(16, dtype=torch.uint8, device=DEV)
     cc, cc_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
                                     want_lse=True, ws=tiny)
+    # a workspace below what all passes in one launch need: the passes run one after
+    # another (or, below one pass's need, on the CUDA cores)
+    full = C.csa2_sparse_attn_workspace_bytes(B, Q, H, k, window)
+    one = torch.empty(max(16, min(C.csa2_sparse_attn_workspace_bytes(B, Q, 64, k, window), full - 1)),
+                      dtype=torch.uint8, device=DEV)
+    pp, pp_lse = C.csa2_sparse_attn(q, kv, idx, swa, q_pos, sink, window=window, out_dtype=torch.float32,
+                                    want_lse=True, ws=one)
     C.csa2_ctx_check()
     assert_close(to_np(tc), to_np(cc), 2e-2, "tensor-core vs CUDA-core output")
     assert_close(to_np(tc_lse), to_np(cc_lse), 2e-3, "tensor-core vs CUDA-core lse")
+    assert_close(to_np(tc), to_np(pp), 2e-2, "all passes in one launch vs the smaller workspace")
+    assert_close(to_np(tc_lse), to_np(pp_lse), 2e-3, "all passes in one launch vs the smaller workspace (lse)")
     _check(q, kv_np, idx, swa, q_pos, sink, window, to_np(tc), to_np(tc_lse), [(0, 1), (1, 0)])
+    _check(q, kv_np, idx, swa, q_pos, sink, window, to_np(pp), to_np(pp_lse), [(0, 0), (1, 1)])
 
 
 @pytest.mark.parametrize("B", [8, 200])
