@@ -11,8 +11,10 @@
 //
 // Warp roles (320 threads):
 //   warp 0     producer: bulk / TMA copies of key tiles into a shared-memory ring
-//              (bf16 candidates: the 32 lanes each issue one of the tile's 32 tensor
-//              copies, 1 KB each, a third faster than one lane issuing all of them)
+//              (bf16 candidates: lanes 0-15 each copy one of the tile's 16 pooled
+//              blocks, 2 KB, with a single 3-D tensor copy that lands both 64-dim
+//              halves; one copy per half, 32 a tile, took 94 us for 64 x 16,384
+//              candidates against 80 us, and one lane issuing them all 148 us)
 //   warp 1     MMA issuer (one lane); owns the tensor-memory allocation
 //   warps 2-5  converters (MXFP4 keys only): each thread takes one entry row of the
 //              staged tile, turns its 128 E2M1 codes into f16 with the block scale
@@ -235,9 +237,9 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
     if (warp == 0) {
         // ============================ producer ============================
         if (CAND && KF == KF_BF16) {
-            // 16 pooled blocks per tile, two 64-dim halves each: lane l copies half l / 16
-            // of block l % 16 (one 1 KB tensor copy), with its own arrival on the stage
-            // barrier; an empty pool slot only arrives
+            // 16 pooled blocks per tile: lane j < 16 copies block j whole (one 2 KB tensor
+            // copy into [block j][half][8 rows x 128 B]), with its own arrival on the
+            // stage barrier; lanes 16-31 and empty pool slots only arrive
             int issued = 0;
             const int j = lane & 15, hf = lane >> 4;
             const int64_t gq = (int64_t)b * a.Q + q0;
@@ -250,10 +252,10 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                 const int64_t pi = (int64_t)tile * 16 + j;
                 int32_t pb = pi < a.n_pool ? a.pool[gq * a.n_pool + pi] : -1;
                 if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
-                if (pb >= 0) {
-                    mbar_arrive_expect_tx(&full[s], 1024);
-                    tma_load_2d(dst + hf * (BF_STAGE / 2) + j * 1024, &tmap_blk, 64 * hf,
-                                (int32_t)((int64_t)b * a.N + (int64_t)pb * 8), &full[s]);
+                if (pb >= 0 && hf == 0) {
+                    mbar_arrive_expect_tx(&full[s], 2048);
+                    tma_load_3d(dst + j * 2048, &tmap_blk, 0, (int32_t)((int64_t)b * a.N + (int64_t)pb * 8), 0,
+                                &full[s]);
                 } else {
                     mbar_arrive(&full[s]);
                 }
@@ -283,8 +285,9 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                         tma_load_2d(dst, &tmap_full, 0, y, &full[s]);
                         tma_load_2d(dst + BF_STAGE / 2, &tmap_full, 64, y, &full[s]);
                     }
-                } else {
-                    // 16 pooled blocks of 8 entries per tile
+                } else if (KF == KF_MX) {
+                    // 16 pooled blocks of 8 MXFP4 entries per tile (bf16 candidates take the
+                    // 32-lane path above)
                     const int32_t* pl = a.pool + gq * a.n_pool + (int64_t)tile * 16;
                     int32_t blk[16];
                     uint32_t bytes = 0;
@@ -293,19 +296,14 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                         int32_t pb = ((int64_t)tile * 16 + j < a.n_pool) ? pl[j] : -1;
                         if (pb < 0 || (int64_t)pb * 8 + 8 > a.N) pb = -1;
                         blk[j] = pb;
-                        if (pb >= 0) bytes += (KF == KF_MX) ? 8 * MX_ROW : 2 * 8 * 128;
+                        if (pb >= 0) bytes += 8 * MX_ROW;
                     }
                     mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (blk[j] < 0) continue;
                         const int64_t row0 = (int64_t)b * a.N + (int64_t)blk[j] * 8;
-                        if (KF == KF_MX) {
-                            bulk_g2s(dst + j * 8 * MX_ROW, a.kmx + row0 * MX_ROW, 8 * MX_ROW, &full[s]);
-                        } else {
-                            tma_load_2d(dst + j * 1024, &tmap_blk, 0, (int32_t)row0, &full[s]);
-                            tma_load_2d(dst + BF_STAGE / 2 + j * 1024, &tmap_blk, 64, (int32_t)row0, &full[s]);
-                        }
+                        bulk_g2s(dst + j * 8 * MX_ROW, a.kmx + row0 * MX_ROW, 8 * MX_ROW, &full[s]);
                     }
                 }
                 ++issued;
@@ -338,7 +336,10 @@ __global__ void __launch_bounds__(NTHREADS, Cfg<KF, QT>::MIN_BLOCKS) index_scan_
                         mma_ts(d_tmem, tmem + j * 64 + kk * 8, bdesc, IDESC, kk > 0);
                     } else {
                         const uint32_t a_base = smem_u32(sStage + s * C::STAGE_BYTES);
-                        const uint64_t adesc = sdesc_sw128(a_base + kc * (BF_STAGE / 2) + ko);
+                        // full tiles: K-chunk kc is 16 KB of 128 rows; pooled tiles: block j's
+                        // chunk kc is the 1 KB atom at 2 KB j + 1 KB kc
+                        const uint64_t adesc = CAND ? sdesc_sw128_sbo(a_base + kc * 1024 + ko, 2048)
+                                                    : sdesc_sw128(a_base + kc * (BF_STAGE / 2) + ko);
                         mma_ss(d_tmem, adesc, bdesc, IDESC, kk > 0);
                     }
                 }
@@ -523,7 +524,7 @@ csa2_status launch_tc(csa2_ctx* ctx, TcArgs& a, const void* kbf, cudaStream_t s)
     memset(&mfull, 0, sizeof(mfull));
     memset(&mblk, 0, sizeof(mblk));
     if (KF == KF_BF16) {
-        if (!make_map(&mfull, kbf, (int64_t)a.B * a.N, TILE) || !make_map(&mblk, kbf, (int64_t)a.B * a.N, 8))
+        if (!make_map(&mfull, kbf, (int64_t)a.B * a.N, TILE) || !csa2_make_bf16_block_map(&mblk, kbf, (int64_t)a.B * a.N, 8))
             return CSA2_ERR_CUDA;
     }
     const int groups = a.B * ((a.Q + QT - 1) / QT);

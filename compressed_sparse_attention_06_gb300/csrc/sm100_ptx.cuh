@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared (x = innermost coordinate, in elements).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -268,6 +278,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
     d |= (uint64_t)((addr >> 4) & 0x3FFF);
     d |= (uint64_t)1 << 16;                  // leading byte offset (unused for this layout)
     d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset: 8-row atoms
+    d |= (uint64_t)1 << 46;                  // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// The same K-major 128-byte-swizzle descriptor with another distance between 8-row
+// atoms (sbo bytes, a multiple of 16): the atoms of one K-chunk need not be adjacent.
+__device__ __forceinline__ uint64_t sdesc_sw128_sbo(uint32_t addr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;                  // leading byte offset (unused for this layout)
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;                  // descriptor version for tcgen05
     d |= (uint64_t)2 << 61;                  // 128-byte swizzle
     return d;
