@@ -108,6 +108,39 @@ def test_full_scan_several_queries_share_tiles(kind):
             assert_close(sc[b, q], ref, 1e-5, f"b{b} q{q}")
 
 
+@pytest.mark.parametrize("kind", ["mx", "bf16", "mxq"])
+def test_candidates_at_the_cache_edges(kind):
+    """Pooled blocks at both ends of the key buffer (the first block of the first
+    sequence, the last block of the last one: the copies reach the buffer's last row),
+    block ids past the cache (skipped: -inf) and -1 padding, on the grid so that the
+    scores are bit-exact."""
+    B, N, n_pool = 2, 8 * 1024, 64
+    kI, K_np = _keys(B, N, 141, kind, grid=True)
+    qI, w = _queries(B, 1, 142, grid=True)
+    qI, qn = _q_as(kind, qI)
+    nv = torch.tensor([[N - 1], [N]], dtype=torch.int64, device=DEV)
+    nb = N // 8
+    pool = torch.full((B, 1, n_pool), -1, dtype=torch.int32)
+    for b in range(B):
+        mid = W.distinct_sample(nb - 2, 40, 143, b) + 1
+        ids = torch.cat([torch.tensor([0, nb - 1]), mid, torch.tensor([nb, nb + 5])])   # nb, nb + 5: past the cache
+        pool[b, 0, :ids.numel()] = torch.sort(ids).values.to(torch.int32)
+    pool = pool.to(DEV)
+    sc, _ = C.csa2_index_score(qI, w, kI, nv, pool=pool)
+    sc = to_np(sc)
+    for b in range(B):
+        V = int(nv[b, 0])
+        full = O.index_score(qn[b, 0], w[b, 0].double().cpu().numpy(), K_np[b], V)
+        pl = to_np(pool[b, 0])
+        exp = np.full(n_pool * 8, -np.inf)
+        for c_ in range(n_pool * 8):
+            blk = int(pl[c_ // 8])
+            s_ = blk * 8 + c_ % 8
+            if 0 <= blk < nb and s_ < V:
+                exp[c_] = full[s_]
+        assert np.array_equal(sc[b, 0], exp), f"candidates at the edges {kind} b{b}"
+
+
 @pytest.mark.parametrize("kind", ["mx", "mxq"])
 def test_mx_extreme_block_scales(kind):
     B, N = 2, 1024
