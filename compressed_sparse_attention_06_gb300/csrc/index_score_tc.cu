@@ -523,8 +523,13 @@ csa2_status launch_tc(csa2_ctx* ctx, TcArgs& a, const void* kbf, cudaStream_t s)
     CUtensorMap mfull, mblk;
     memset(&mfull, 0, sizeof(mfull));
     memset(&mblk, 0, sizeof(mblk));
+    // full scans read 128-row tiles, pooled candidates 8-row blocks whole (a 3-D map
+    // whose halves' stride, 128 B, is below the rows' 256 B: the two dimensions never
+    // address the same element, and the encoder takes it; were it refused, the call
+    // would report CSA2_ERR_CUDA)
     if (KF == KF_BF16) {
-        if (!make_map(&mfull, kbf, (int64_t)a.B * a.N, TILE) || !csa2_make_bf16_block_map(&mblk, kbf, (int64_t)a.B * a.N, 8))
+        if (CAND ? !csa2_make_bf16_block_map(&mblk, kbf, (int64_t)a.B * a.N, 8)
+                 : !make_map(&mfull, kbf, (int64_t)a.B * a.N, TILE))
             return CSA2_ERR_CUDA;
     }
     const int groups = a.B * ((a.Q + QT - 1) / QT);
