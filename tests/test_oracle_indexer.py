@@ -166,3 +166,23 @@ def test_merge_topk_over_entry_shards():
         ids.append(g)
         scs.append(np.where(g >= 0, s[np.maximum(g, 0)], -np.inf))
     np.testing.assert_array_equal(O.merge_topk(ids, scs, k), full)
+
+
+def test_planted_keys_of_the_bf16_decode_workload_are_selected():
+    """The bf16 decode workload plants 16 keys per sequence along the direction of the
+    positively weighted indexer heads (about twelve times a random key's length): on
+    the oracle they score at least 8 standard deviations above the mean, sit in the
+    top-512 and their blocks in the 2,048-block pool (DSA-to-CSA/HCA eqs. (16)-(17);
+    CSA2 page «解码器里的分层索引»).  Two sequences at the workload's 64K entries."""
+    from compressed_sparse_attention_06_gb300 import workloads as W
+    wl = W.decode_full_bf16("cpu", B=2, N=65536, with_main_kv=False)
+    t = wl.tensors
+    V = wl.N - 1
+    for b in range(2):
+        sc = O.index_score(t["qI"][b, 0].double().numpy(), t["w"][b, 0].double().numpy(),
+                           t["KI"][b].double().numpy(), V)
+        planted = t["planted"][b].numpy()
+        vis = sc[:V]
+        assert np.all(sc[planted] >= vis.mean() + 8 * vis.std())
+        assert set(planted.tolist()) <= set(O.topk(sc, V, 512).tolist())
+        assert set((planted // 8).tolist()) <= set(O.block_pool(O.block_max(sc, V, 8), V, 8, 2048).tolist())
